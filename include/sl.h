@@ -1,0 +1,233 @@
+/*
+ * sl.h -- C ABI of libsl, the B300 (sm_103a) layer-streamed NF4 LoRA library.
+ *
+ * What it computes (sources by page title and section):
+ *  - LoRA fine-tuning on a frozen base held in NF4: "Exact Layer Streaming:
+ *    LoRA Fine-Tuning of an 8B Model on a 4 GB Laptop GPU" (abstract);
+ *    "Soup CLI Lets You Fine-Tune an 8B LLM on a 4 GB Laptop GPU" ("Key
+ *    Takeaways": Llama-3.1-8B-Instruct + NF4).
+ *  - Layer streaming: the frozen base stays in (pinned) host RAM and decoder
+ *    layers are brought to the GPU for the forward and again, in reverse, for
+ *    the backward ("Soup CLI ...", "How Layer Streaming Works"), through two
+ *    device buffers ("Soup: Fine-Tuning an 8B LLM on a 4 GB Laptop GPU with One
+ *    YAML File", "Layer Streaming: The Mechanism Behind the 4 GB Claim": a
+ *    pinned base store and two VRAM buffers).  The streamed run must be
+ *    bit-exact against a resident run of the same numerics ("Exact Layer
+ *    Streaming ...", abstract; "Soup CLI ...", "v0.73.0: Fixing Silent Wrong
+ *    Gradients").
+ *  - The base is never upcast: it is consumed in its storage dtype ("Soup:
+ *    Fine-Tuning ...", "The FP32 Bug and What It Means for Your VRAM"), and
+ *    adapter gradients are fp32 ("Known Limitations and Failure Modes").
+ *  - The cross-entropy over the LM head without the full logits ("Exact Layer
+ *    Streaming ...", abstract: the logits term's bytes per element).
+ *
+ * Conventions for every call:
+ *  - Device pointers unless stated; the CALLER owns every tensor passed in.
+ *    libsl owns only what sl_stack_create allocates (two device layer buffers,
+ *    a copy stream, events) and one int per device for error reporting.
+ *  - Work is enqueued on the caller's stream and the call returns without
+ *    waiting, except where a call says it synchronises.
+ *  - bf16 tensors are passed as void* (IEEE bfloat16 bit patterns, row-major,
+ *    densely packed); sizes are element counts.
+ *  - Every call returns sl_status; on failure nothing is enqueued (argument
+ *    errors) or the CUDA error is reported (SL_ERR_CUDA), and
+ *    sl_last_error() (thread-local) describes it.  No C++ exception crosses
+ *    the ABI.
+ *  - Kernels never trap.  A bounded wait that gives up (after about two
+ *    seconds) writes SL_ERR_TIMEOUT into the device error word and returns;
+ *    sl_check_device_errors() reports it.
+ */
+#ifndef SL_H_
+#define SL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SL_OK = 0,
+  SL_ERR_INVALID = 1,      /* bad argument: null pointer, shape, alignment, workspace too small */
+  SL_ERR_CUDA = 2,         /* a CUDA runtime/driver call failed */
+  SL_ERR_UNSUPPORTED = 3,  /* valid but not implemented (e.g. no sm_103a device) */
+  SL_ERR_TIMEOUT = 4,      /* a device-side bounded wait gave up */
+  SL_ERR_NONFINITE = 5,    /* non-finite input where the operation forbids it */
+  SL_ERR_OOM = 6           /* a libsl-owned allocation failed */
+} sl_status;
+
+typedef enum { SL_DTYPE_BF16 = 0, SL_DTYPE_F32 = 1 } sl_dtype;
+typedef enum { SL_WEIGHT_NF4 = 0, SL_WEIGHT_BF16 = 1 } sl_weight_kind;
+typedef enum { SL_MODE_STREAMED = 0, SL_MODE_RESIDENT = 1 } sl_stack_mode;
+
+/* A frozen base weight W [N, K] (N = out features, K = in features), the
+ * layout of a PyTorch Linear.weight.
+ *  kind = SL_WEIGHT_NF4:  codes  [N*K/2] bytes, row-major, element 2i in the
+ *                         HIGH nibble of byte i; absmax [N*K/64] fp32, one per
+ *                         64 consecutive elements of a row.  Needs K % 256 == 0.
+ *  kind = SL_WEIGHT_BF16: w [N, K] bf16.
+ * All pointers 16-byte aligned; N % 32 == 0. */
+typedef struct {
+  int32_t kind;
+  int64_t N;
+  int64_t K;
+  const uint8_t* codes;
+  const float* absmax;
+  const void* w;
+} sl_weight;
+
+/* ---------------------------------------------------------------- library */
+
+/* Thread-local description of the last failure in this thread ("" if none). */
+const char* sl_last_error(void);
+
+/* ABI version (major*10000 + minor*100 + patch). */
+int32_t sl_version(void);
+
+/* Host copy of the library's NF4 levels (16 fp32, ascending).  The levels are
+ * the published NormalFloat-4 construction (QLoRA); the pages name NF4 but do
+ * not print them.  Never fails. */
+void sl_nf4_code_table(float out[16]);
+
+/* Synchronises `stream`, then reads and clears this device's error word.
+ * Returns SL_OK, or the code a kernel recorded (SL_ERR_TIMEOUT, ...). */
+sl_status sl_check_device_errors(cudaStream_t stream);
+
+/* Launches one kernel that waits on a device flag nothing ever sets, with a
+ * wait limit of `limit_ns` nanoseconds (clamped to [1e3, 2e9]); the kernel
+ * gives up, records SL_ERR_TIMEOUT in the error word and exits normally.
+ * Exists so that tests can prove a bounded wait ends without faulting the
+ * GPU.  `mbarrier` != 0 makes the wait an mbarrier wait instead of a flag
+ * poll. */
+sl_status sl_debug_timeout_probe(int64_t limit_ns, int32_t mbarrier, cudaStream_t stream);
+
+/* ------------------------------------------------------------- NF4 (K0/K1) */
+
+/* NF4-quantise W [N, K] (dtype SL_DTYPE_BF16 or SL_DTYPE_F32) into codes
+ * [N*K/2] and absmax [N*K/64] (layouts of sl_weight).  Per 64-element block:
+ * absmax = max |w|; x = w / absmax (IEEE fp32 division); code = nearest NF4
+ * level to x, ties to the lower level; absmax == 0 gives code 7 (the zero
+ * level) everywhere.  Requires K % 64 == 0, pointers 16-byte aligned.
+ * SYNCHRONISES `stream` to read the non-finite flag: returns
+ * SL_ERR_NONFINITE if any input is NaN or infinite (outputs then undefined). */
+sl_status sl_nf4_quantize(const void* W, int32_t dtype, int64_t N, int64_t K,
+                          uint8_t* codes, float* absmax, cudaStream_t stream);
+
+/* w_hat = fp32(T[code] * absmax), written as bf16 (rounded to nearest even)
+ * or fp32 per `out_dtype`, out [N, K].  Requires K % 64 == 0. */
+sl_status sl_nf4_dequantize(const uint8_t* codes, const float* absmax, int64_t N, int64_t K,
+                            int32_t out_dtype, void* out, cudaStream_t stream);
+
+/* ------------------------------------------------------ LoRA linear (a3-a6) */
+
+/* Forward of the frozen-base LoRA linear
+ *     Y = X W^T + s (X A^T) B^T,    s = alpha / r,
+ * X [M, K] bf16, A [r, K] bf16, B [N, r] bf16, Y [M, N] bf16 (fp32
+ * accumulation, one rounding).  T_save [M, r] bf16 receives X A^T (kept for
+ * the backward); may be NULL only when r == 0.  r == 0 (or A == B == NULL)
+ * computes the base alone -- the adapters-off pass.  r <= 64, r % 8 == 0.
+ * `ws` is unused (pass NULL / 0); kept for ABI symmetry. */
+sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M,
+                             const void* A, const void* B, int32_t r, float alpha,
+                             void* Y, void* T_save, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* Backward of the linear above for upstream gradient dY [M, N] bf16:
+ *     U = dY B;  dX = dY W + s U A;  dA = s U^T X;  dB = s dY^T T_save.
+ * dX [M, K] bf16 (may be NULL to skip); dA [r, K] and dB [N, r] fp32,
+ * overwritten when accumulate == 0, added to otherwise.  Reductions over M
+ * run in a fixed order: results are bitwise reproducible.  `ws` must hold
+ * sl_lora_linear_workspace_size(M, N, K, r) bytes (256-byte aligned). */
+sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M,
+                             const void* A, const void* B, int32_t r, float alpha,
+                             const void* T_save, void* dX, float* dA, float* dB,
+                             int32_t accumulate, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r);
+
+/* ------------------------------------------------- streamed stack (a2-a7) */
+
+/* Byte layout of one layer blob (the unit that is streamed): the seven
+ * projections q, k, v, o, gate, up, down of a decoder layer with hidden D,
+ * kv width Dkv and MLP width F.  For NF4 each projection contributes its
+ * codes then its absmax; for BF16 its weight.  offsets[2p] / offsets[2p+1]
+ * receive the byte offsets of projection p's codes / absmax (NF4) or of its
+ * weight / 0 (BF16), every offset 256-byte aligned; *blob_bytes the total. */
+sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F,
+                               size_t offsets[14], size_t* blob_bytes);
+
+typedef struct {
+  int32_t L;                        /* number of layers */
+  int32_t kind;                     /* SL_WEIGHT_NF4 or SL_WEIGHT_BF16 */
+  int64_t D, Dkv, F;                /* hidden, kv width (multiple of 128), MLP width */
+  const void* const* host_blobs;    /* L pointers to PINNED host blobs (sl_stack_blob_layout) */
+  const void* const* device_blobs;  /* L device copies for SL_MODE_RESIDENT, or NULL */
+} sl_stack_desc;
+
+typedef struct sl_stack sl_stack;
+
+/* Creates a stack handle: checks that every host blob is page-locked
+ * (cudaPointerGetAttributes; pageable memory -> SL_ERR_INVALID), allocates
+ * the two device layer buffers, a copy stream and the buffer events on the
+ * current device.  The pre-flight report ("Soup: Fine-Tuning ...", "Layer
+ * Streaming: The Mechanism ...") comes back in *host_bytes (L * blob bytes)
+ * and *buffer_bytes (the two buffers together).  The descriptor's pointer
+ * arrays are copied; the blobs themselves stay owned by the caller and must
+ * outlive the handle. */
+sl_status sl_stack_create(const sl_stack_desc* desc, sl_stack** out,
+                          size_t* host_bytes, size_t* buffer_bytes);
+sl_status sl_stack_destroy(sl_stack* s);
+
+/* Workspace for sl_stream_stack_step at M tokens and rank r. */
+size_t sl_stack_workspace_size(const sl_stack* s, int64_t M, int32_t r);
+
+/* One training step of the stack:
+ *  forward layers 0..L-1 from h0 [M, D] fp32 to hL [M, D] fp32, then
+ *  backward L-1..0 from dh_top [M, D] fp32 to dh0 [M, D] fp32, writing for
+ *  every layer l and projection p (index 7*l + p, order q k v o gate up down)
+ *  dA[7l+p] [r, K_p] fp32 and dB[7l+p] [N_p, r] fp32 (overwritten).
+ *  A[7l+p] [r, K_p] bf16 and B[7l+p] [N_p, r] bf16 are the adapters.
+ * The layer is the pre-norm decoder layer with token-local mixing described
+ * in the library's design notes (RMS norm without weight, a = q*rep(k) +
+ * rep(v), SiLU-gated MLP, fp32 residual stream, bf16 GEMM inputs/outputs).
+ * SL_MODE_STREAMED: layer l is copied from its pinned host blob into device
+ * buffer l % 2 on the handle's copy stream; CUDA events order each copy
+ * after the last kernel that read the buffer and each layer's kernels after
+ * its copy.  The backward reuses the two layers already resident at the
+ * turn.  SL_MODE_RESIDENT: the same kernels, in the same order, read the
+ * descriptor's device_blobs; results are bitwise identical.  `ws` must hold
+ * sl_stack_workspace_size(s, M, r) bytes, 256-byte aligned. */
+sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64_t M,
+                               const float* dh_top, const void* const* A,
+                               const void* const* B, int32_t r, float alpha,
+                               float* hL, float* dh0, float* const* dA, float* const* dB,
+                               void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Host-side counters of the last step on this handle: bytes copied host to
+ * device and the number of libsl kernels launched. */
+sl_status sl_stack_last_step_stats(const sl_stack* s, uint64_t* h2d_bytes, uint64_t* kernels);
+
+/* ------------------------------------------------ LM-head cross-entropy (a8) */
+
+/* loss = (1/N_valid) sum over rows with labels[i] != ignore_index of
+ * (logsumexp_v z_iv - z_i,label), z = H W_head^T;
+ * dH = (softmax(z) - onehot(label)) W_head / N_valid on valid rows, 0 elsewhere.
+ * H [M, D] bf16, W_head [V, D] bf16, labels [M] int32 (in [0, V) or
+ * ignore_index), loss: ONE fp32 on the device, dH [M, D] bf16.  The vocab is
+ * processed in chunks of chunk_V (multiple of 256) rows of W_head; no [M, V]
+ * logits tensor ever exists, only an [M, chunk_V] bf16 gradient chunk in
+ * `ws`.  N_valid == 0 gives loss 0 and dH 0.  D % 256 == 0.  `ws` must hold
+ * sl_ce_workspace_size(M, D, V, chunk_V) bytes. */
+sl_status sl_ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W_head, int64_t V,
+                        const int32_t* labels, int32_t ignore_index, int64_t chunk_V,
+                        float* loss, void* dH, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+size_t sl_ce_workspace_size(int64_t M, int64_t D, int64_t V, int64_t chunk_V);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SL_H_ */

@@ -1,0 +1,247 @@
+"""Python binding of libsl (the layer-streamed NF4 LoRA library for B300).
+
+Argument marshalling only: every function below forwards torch tensors' device
+pointers (and the current CUDA stream) to the C ABI declared in
+``include/sl.h`` under the same name.  All arithmetic runs in libsl's CUDA
+kernels; there is no CPU or PyTorch fallback -- if ``libsl.so`` is missing or
+cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsl.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "sl.h")
+
+SL_OK, SL_ERR_INVALID, SL_ERR_CUDA, SL_ERR_UNSUPPORTED, SL_ERR_TIMEOUT, SL_ERR_NONFINITE, SL_ERR_OOM = range(7)
+SL_DTYPE_BF16, SL_DTYPE_F32 = 0, 1
+SL_WEIGHT_NF4, SL_WEIGHT_BF16 = 0, 1
+SL_MODE_STREAMED, SL_MODE_RESIDENT = 0, 1
+STATUS_NAMES = {0: "SL_OK", 1: "SL_ERR_INVALID", 2: "SL_ERR_CUDA", 3: "SL_ERR_UNSUPPORTED",
+                4: "SL_ERR_TIMEOUT", 5: "SL_ERR_NONFINITE", 6: "SL_ERR_OOM"}
+
+
+class SLError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class sl_weight(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("codes", ctypes.c_void_p), ("absmax", ctypes.c_void_p), ("w", ctypes.c_void_p)]
+
+
+class sl_stack_desc(ctypes.Structure):
+    _fields_ = [("L", ctypes.c_int32), ("kind", ctypes.c_int32), ("D", ctypes.c_int64),
+                ("Dkv", ctypes.c_int64), ("F", ctypes.c_int64),
+                ("host_blobs", ctypes.POINTER(ctypes.c_void_p)),
+                ("device_blobs", ctypes.POINTER(ctypes.c_void_p))]
+
+
+_lib = None
+_P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_SIGS = {
+    "sl_last_error": (ctypes.c_char_p, []),
+    "sl_version": (_I32, []),
+    "sl_nf4_code_table": (None, [_P]),
+    "sl_check_device_errors": (_I32, [_P]),
+    "sl_debug_timeout_probe": (_I32, [_I64, _I32, _P]),
+    "sl_nf4_quantize": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P]),
+    "sl_nf4_dequantize": (_I32, [_P, _P, _I64, _I64, _I32, _P, _P]),
+    "sl_lora_linear_fwd": (_I32, [ctypes.POINTER(sl_weight), _P, _I64, _P, _P, _I32, _F, _P, _P, _P, _SZ, _P]),
+    "sl_lora_linear_bwd": (_I32, [ctypes.POINTER(sl_weight), _P, _P, _I64, _P, _P, _I32, _F, _P, _P, _P, _P,
+                                  _I32, _P, _SZ, _P]),
+    "sl_lora_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
+    "sl_stack_blob_layout": (_I32, [_I32, _I64, _I64, _I64, _P, _P]),
+    "sl_stack_create": (_I32, [ctypes.POINTER(sl_stack_desc), _P, _P, _P]),
+    "sl_stack_destroy": (_I32, [_P]),
+    "sl_stack_workspace_size": (_SZ, [_P, _I64, _I32]),
+    "sl_stream_stack_step": (_I32, [_P, _I32, _P, _I64, _P, _P, _P, _I32, _F, _P, _P, _P, _P, _P, _SZ, _P]),
+    "sl_stack_last_step_stats": (_I32, [_P, _P, _P]),
+    "sl_ce_fwd_bwd": (_I32, [_P, _I64, _I64, _P, _I64, _P, _I32, _I64, _P, _P, _P, _SZ, _P]),
+    "sl_ce_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsl; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libsl.so not found at {LIB_PATH}: run __graft_entry__.build() "
+                               "(python -m layer_streamed_qlora_linear_b300.build)")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            if hasattr(l, name):
+                f = getattr(l, name)
+                f.restype = res
+                f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def header_functions() -> list:
+    """Names of every function declared in include/sl.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sl_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status: int):
+    if status != SL_OK:
+        raise SLError(status, lib().sl_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ library
+def sl_version() -> int:
+    return lib().sl_version()
+
+
+def sl_nf4_code_table():
+    buf = (ctypes.c_float * 16)()
+    lib().sl_nf4_code_table(buf)
+    return list(buf)
+
+
+def sl_check_device_errors(stream=None):
+    _check(lib().sl_check_device_errors(_stream(stream)))
+
+
+def sl_debug_timeout_probe(limit_ns: int, mbarrier: bool = False, stream=None):
+    _check(lib().sl_debug_timeout_probe(int(limit_ns), int(bool(mbarrier)), _stream(stream)))
+
+
+# ---------------------------------------------------------------------- NF4
+def sl_nf4_quantize(W, codes, absmax, stream=None):
+    """W [N, K] bf16/fp32 -> codes uint8 [N*K/2], absmax fp32 [N*K/64] (synchronises)."""
+    import torch
+    N, K = W.shape
+    dt = SL_DTYPE_F32 if W.dtype == torch.float32 else SL_DTYPE_BF16
+    _check(lib().sl_nf4_quantize(_ptr(W), dt, N, K, _ptr(codes), _ptr(absmax), _stream(stream)))
+
+
+def sl_nf4_dequantize(codes, absmax, N, K, out, stream=None):
+    import torch
+    dt = SL_DTYPE_F32 if out.dtype == torch.float32 else SL_DTYPE_BF16
+    _check(lib().sl_nf4_dequantize(_ptr(codes), _ptr(absmax), N, K, dt, _ptr(out), _stream(stream)))
+
+
+# ---------------------------------------------------------------- weights
+class Weight:
+    """An sl_weight descriptor that keeps its tensors alive."""
+
+    def __init__(self, kind, N, K, codes=None, absmax=None, w=None):
+        self.tensors = (codes, absmax, w)
+        self.desc = sl_weight(kind, N, K, codes.data_ptr() if codes is not None else None,
+                              absmax.data_ptr() if absmax is not None else None,
+                              w.data_ptr() if w is not None else None)
+
+    @staticmethod
+    def nf4(codes, absmax, N, K):
+        return Weight(SL_WEIGHT_NF4, N, K, codes=codes, absmax=absmax)
+
+    @staticmethod
+    def bf16(w):
+        return Weight(SL_WEIGHT_BF16, w.shape[0], w.shape[1], w=w)
+
+
+# ------------------------------------------------------------- LoRA linear
+def sl_lora_linear_fwd(weight: Weight, X, A, B, r, alpha, Y, T_save, stream=None):
+    M = X.shape[0]
+    _check(lib().sl_lora_linear_fwd(ctypes.byref(weight.desc), _ptr(X), M, _ptr(A), _ptr(B), int(r),
+                                    float(alpha), _ptr(Y), _ptr(T_save), None, 0, _stream(stream)))
+
+
+def sl_lora_linear_workspace_size(M, N, K, r) -> int:
+    return lib().sl_lora_linear_workspace_size(M, N, K, r)
+
+
+def sl_lora_linear_bwd(weight: Weight, X, dY, A, B, r, alpha, T_save, dX, dA, dB, accumulate=False,
+                       ws=None, stream=None):
+    M = dY.shape[0]
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(lib().sl_lora_linear_bwd(ctypes.byref(weight.desc), _ptr(X), _ptr(dY), M, _ptr(A), _ptr(B), int(r),
+                                    float(alpha), _ptr(T_save), _ptr(dX), _ptr(dA), _ptr(dB),
+                                    int(bool(accumulate)), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+# -------------------------------------------------------------------- stack
+def sl_stack_blob_layout(kind, D, Dkv, F):
+    offs = (ctypes.c_size_t * 14)()
+    total = ctypes.c_size_t(0)
+    _check(lib().sl_stack_blob_layout(kind, D, Dkv, F, offs, ctypes.byref(total)))
+    return list(offs), total.value
+
+
+class Stack:
+    """Owns an sl_stack handle (two device layer buffers, copy stream, events)."""
+
+    def __init__(self, kind, D, Dkv, F, host_blobs, device_blobs=None):
+        self.L = len(host_blobs)
+        self._host = host_blobs
+        self._dev = device_blobs
+        self._hp = (ctypes.c_void_p * self.L)(*[b.data_ptr() for b in host_blobs])
+        self._dp = (ctypes.c_void_p * self.L)(*[b.data_ptr() for b in device_blobs]) if device_blobs else None
+        self.desc = sl_stack_desc(self.L, kind, D, Dkv, F, self._hp, self._dp)
+        self.handle = ctypes.c_void_p()
+        hb, bb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+        _check(lib().sl_stack_create(ctypes.byref(self.desc), ctypes.byref(self.handle), ctypes.byref(hb),
+                                     ctypes.byref(bb)))
+        self.host_bytes, self.buffer_bytes = hb.value, bb.value
+
+    def workspace_size(self, M, r):
+        return lib().sl_stack_workspace_size(self.handle, M, r)
+
+    def step(self, mode, h0, dh_top, A, B, r, alpha, hL, dh0, dA, dB, ws, stream=None):
+        n = 7 * self.L
+        pa = (ctypes.c_void_p * n)(*[t.data_ptr() for t in A])
+        pb = (ctypes.c_void_p * n)(*[t.data_ptr() for t in B])
+        pga = (ctypes.c_void_p * n)(*[t.data_ptr() for t in dA])
+        pgb = (ctypes.c_void_p * n)(*[t.data_ptr() for t in dB])
+        M = h0.shape[0]
+        _check(lib().sl_stream_stack_step(self.handle, mode, _ptr(h0), M, _ptr(dh_top), pa, pb, int(r),
+                                          float(alpha), _ptr(hL), _ptr(dh0), pga, pgb, _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream(stream)))
+
+    def last_step_stats(self):
+        a, b = ctypes.c_uint64(0), ctypes.c_uint64(0)
+        _check(lib().sl_stack_last_step_stats(self.handle, ctypes.byref(a), ctypes.byref(b)))
+        return a.value, b.value
+
+    def close(self):
+        if self.handle:
+            _check(lib().sl_stack_destroy(self.handle))
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------ cross-entropy
+def sl_ce_workspace_size(M, D, V, chunk_V) -> int:
+    return lib().sl_ce_workspace_size(M, D, V, chunk_V)
+
+
+def sl_ce_fwd_bwd(H, W_head, labels, loss, dH, ws, chunk_V=8192, ignore_index=-100, stream=None):
+    M, D = H.shape
+    V = W_head.shape[0]
+    _check(lib().sl_ce_fwd_bwd(_ptr(H), M, D, _ptr(W_head), V, _ptr(labels), int(ignore_index), int(chunk_V),
+                               _ptr(loss), _ptr(dH), _ptr(ws), ws.numel() * ws.element_size(),
+                               _stream(stream)))

@@ -1,0 +1,111 @@
+// Host side of the tcgen05 GEMM: TMA tensor maps and launch dispatch.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace sl {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major matrix: inner extent `cols`, outer `rows`, row
+// pitch `pitch_bytes`; box (box_cols x box_rows).
+static sl_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                          uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(SL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (pitch_bytes & 15))
+    return set_error(SL_ERR_INVALID, "TMA operand: base and row pitch must be 16-byte aligned");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(SL_ERR_INVALID, "cuTensorMapEncodeTiled failed (code " + std::to_string((int)r) + ")");
+  return SL_OK;
+}
+
+template <int BSRC, int BMN, int EPI>
+static sl_status run(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms, const GemmArgs& a,
+                     cudaStream_t stream) {
+  using Cfg = GemmCfg<BSRC>;
+  auto kern = gemm_tc_kernel<BSRC, BMN, EPI>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  SL_CHECK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    SL_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem));
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  dim3 grid(static_cast<unsigned>(ceil_div(a.N, kBN)), static_cast<unsigned>(ceil_div(a.M, kBM)));
+  kern<<<grid, kGemmThreads, Cfg::kSmem, stream>>>(ma, mb, ms, a);
+  return check_launch("gemm_tc_kernel");
+}
+
+sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
+  const GemmArgs& a = g.args;
+  if (a.M <= 0 || a.N <= 0 || a.K <= 0) return set_error(SL_ERR_INVALID, "gemm: empty problem");
+  if (a.N % 32) return set_error(SL_ERR_INVALID, "gemm: output columns must be a multiple of 32");
+  if (a.r < 0 || a.r > 64 || (a.r % 8)) return set_error(SL_ERR_INVALID, "gemm: LoRA rank must be 0..64, multiple of 8");
+  CUtensorMap ma, mb, ms;
+  sl_status st = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, a.K, a.M, g.lda * 2, kBK, kBM,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  if (g.bsrc == kBSrcBF16) {
+    if (!g.bmn)
+      st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.w, a.K, a.N, g.ldw * 2, kBK, kBN,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.w, a.N, a.K, g.ldw * 2, 64, kBK,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != SL_OK) return st;
+    ms = mb;
+  } else {
+    // NF4: codes are bytes (two elements each), absmax one fp32 per 64 elements of a row.
+    const int64_t rows = g.bmn ? a.K : a.N;   // weight rows
+    const int64_t cols = g.ldw;               // weight row length in elements
+    if (cols % 256) return set_error(SL_ERR_INVALID, "gemm: NF4 weight rows must be a multiple of 256 elements");
+    if (!g.bmn) {
+      st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.codes, cols / 2, rows, cols / 2, kBK / 2, kBN,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st == SL_OK)
+        st = make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax, cols / 64, rows, cols / 64 * 4, 4, kBN,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.codes, cols / 2, rows, cols / 2, kBN / 2, kBK,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st == SL_OK)
+        st = make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax, cols / 64, rows, cols / 64 * 4, 4, kBK,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (st != SL_OK) return st;
+  }
+#define SL_GEMM_CASE(B, MN, E) \
+  if (g.bsrc == B && g.bmn == MN && g.epi == E) return run<B, MN, E>(ma, mb, ms, a, stream);
+  SL_GEMM_CASE(kBSrcNF4, 0, kEpiStoreBF16)
+  SL_GEMM_CASE(kBSrcNF4, 1, kEpiStoreBF16)
+  SL_GEMM_CASE(kBSrcBF16, 0, kEpiStoreBF16)
+  SL_GEMM_CASE(kBSrcBF16, 1, kEpiStoreBF16)
+  SL_GEMM_CASE(kBSrcBF16, 0, kEpiCELse)
+  SL_GEMM_CASE(kBSrcBF16, 0, kEpiCEGrad)
+  SL_GEMM_CASE(kBSrcBF16, 1, kEpiAddF32)
+#undef SL_GEMM_CASE
+  return set_error(SL_ERR_UNSUPPORTED, "gemm: unsupported (source, layout, epilogue) combination");
+}
+
+}  // namespace sl
