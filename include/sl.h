@@ -103,6 +103,20 @@ sl_status sl_check_device_errors(cudaStream_t stream);
  * poll. */
 sl_status sl_debug_timeout_probe(int64_t limit_ns, int32_t mbarrier, cudaStream_t stream);
 
+/* Kernel timing for measurement.  enable != 0 clears earlier records and
+ * starts recording a CUDA event pair, on the launching stream, around every
+ * tensor-core GEMM launch; enable == 0 stops recording.  Costs one event
+ * pair per GEMM launch.  Variants: 0 NF4 forward, 1 NF4 dX, 2 bf16
+ * forward, 3 bf16 dX, 4 CE logits (lse partials), 5 CE softmax chunk,
+ * 6 CE dH accumulation. */
+sl_status sl_kernel_timing(int32_t enable);
+
+/* Totals over the launches of one variant recorded since timing was
+ * enabled: launch count, summed device time in ms (waits for the recorded
+ * events) and algorithmic FLOPs (2 M N K, plus 2 M N r for the folded LoRA
+ * side product). */
+sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms, double* flops);
+
 /* ------------------------------------------------------------- NF4 (K0/K1) */
 
 /* NF4-quantise W [N, K] (dtype SL_DTYPE_BF16 or SL_DTYPE_F32) into codes
@@ -125,9 +139,11 @@ sl_status sl_nf4_dequantize(const uint8_t* codes, const float* absmax, int64_t N
 /* Forward of the frozen-base LoRA linear
  *     Y = X W^T + s (X A^T) B^T,    s = alpha / r,
  * X [M, K] bf16, A [r, K] bf16, B [N, r] bf16, Y [M, N] bf16 (fp32
- * accumulation, one rounding).  T_save [M, r] bf16 receives X A^T (kept for
- * the backward); may be NULL only when r == 0.  r == 0 (or A == B == NULL)
- * computes the base alone -- the adapters-off pass.  r <= 64, r % 8 == 0.
+ * accumulation, one rounding).  T_save [M, r] fp32 receives X A^T (kept for
+ * the backward; the side product s T B^T is folded into the same
+ * accumulator with fp32 accuracy); may be NULL only when r == 0.  r == 0 (or
+ * A == B == NULL) computes the base alone -- the adapters-off pass.
+ * r <= 32, r % 8 == 0.
  * `ws` is unused (pass NULL / 0); kept for ABI symmetry. */
 sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M,
                              const void* A, const void* B, int32_t r, float alpha,
@@ -135,7 +151,8 @@ sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M,
                              cudaStream_t stream);
 
 /* Backward of the linear above for upstream gradient dY [M, N] bf16:
- *     U = dY B;  dX = dY W + s U A;  dA = s U^T X;  dB = s dY^T T_save.
+ *     U = dY B (fp32);  dX = dY W + s U A;  dA = s U^T X;  dB = s dY^T T_save,
+ * T_save [M, r] fp32 from the forward.
  * dX [M, K] bf16 (may be NULL to skip); dA [r, K] and dB [N, r] fp32,
  * overwritten when accumulate == 0, added to otherwise.  Reductions over M
  * run in a fixed order: results are bitwise reproducible.  `ws` must hold
@@ -216,14 +233,18 @@ sl_status sl_stack_last_step_stats(const sl_stack* s, uint64_t* h2d_bytes, uint6
  * (logsumexp_v z_iv - z_i,label), z = H W_head^T;
  * dH = (softmax(z) - onehot(label)) W_head / N_valid on valid rows, 0 elsewhere.
  * H [M, D] bf16, W_head [V, D] bf16, labels [M] int32 (in [0, V) or
- * ignore_index), loss: ONE fp32 on the device, dH [M, D] bf16.  The vocab is
- * processed in chunks of chunk_V (multiple of 256) rows of W_head; no [M, V]
- * logits tensor ever exists, only an [M, chunk_V] bf16 gradient chunk in
- * `ws`.  N_valid == 0 gives loss 0 and dH 0.  D % 256 == 0.  `ws` must hold
- * sl_ce_workspace_size(M, D, V, chunk_V) bytes. */
+ * ignore_index), loss: ONE fp32 on the device, dH [M, D] fp32 (the residual
+ * stream's gradient dtype; it can feed sl_stream_stack_step's dh_top).  The
+ * vocab is processed in chunks of chunk_V (multiple of 256) rows of W_head;
+ * no [M, V] logits tensor ever exists, only an [M, chunk_V] bf16 softmax
+ * chunk and O(M * V / 256) per-tile partials in `ws`.  N_valid == 0 gives
+ * loss 0 and dH 0.  D % 256 == 0, V % 32 == 0.  A label outside [0, V) that
+ * is not ignore_index is treated as ignored and recorded as SL_ERR_INVALID
+ * in the device error word.  `ws` must hold sl_ce_workspace_size(M, D, V,
+ * chunk_V) bytes, 256-byte aligned. */
 sl_status sl_ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W_head, int64_t V,
                         const int32_t* labels, int32_t ignore_index, int64_t chunk_V,
-                        float* loss, void* dH, void* ws, size_t ws_bytes, cudaStream_t stream);
+                        float* loss, float* dH, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 size_t sl_ce_workspace_size(int64_t M, int64_t D, int64_t V, int64_t chunk_V);
 

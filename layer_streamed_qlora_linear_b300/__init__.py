@@ -50,6 +50,8 @@ _SIGS = {
     "sl_nf4_code_table": (None, [_P]),
     "sl_check_device_errors": (_I32, [_P]),
     "sl_debug_timeout_probe": (_I32, [_I64, _I32, _P]),
+    "sl_kernel_timing": (_I32, [_I32]),
+    "sl_kernel_timing_read": (_I32, [_I32, _P, _P, _P]),
     "sl_nf4_quantize": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P]),
     "sl_nf4_dequantize": (_I32, [_P, _P, _I64, _I64, _I32, _P, _P]),
     "sl_lora_linear_fwd": (_I32, [ctypes.POINTER(sl_weight), _P, _I64, _P, _P, _I32, _F, _P, _P, _P, _SZ, _P]),
@@ -125,6 +127,20 @@ def sl_debug_timeout_probe(limit_ns: int, mbarrier: bool = False, stream=None):
     _check(lib().sl_debug_timeout_probe(int(limit_ns), int(bool(mbarrier)), _stream(stream)))
 
 
+GEMM_VARIANTS = ("nf4_fwd", "nf4_dx", "bf16_fwd", "bf16_dx", "ce_lse", "ce_softmax", "ce_dh")
+
+
+def sl_kernel_timing(enable: bool):
+    _check(lib().sl_kernel_timing(int(bool(enable))))
+
+
+def sl_kernel_timing_read(variant: int):
+    """(launches, ms, flops) of one GEMM variant since timing was enabled."""
+    n, ms, fl = ctypes.c_uint64(0), ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().sl_kernel_timing_read(int(variant), ctypes.byref(n), ctypes.byref(ms), ctypes.byref(fl)))
+    return n.value, ms.value, fl.value
+
+
 # ---------------------------------------------------------------------- NF4
 def sl_nf4_quantize(W, codes, absmax, stream=None):
     """W [N, K] bf16/fp32 -> codes uint8 [N*K/2], absmax fp32 [N*K/64] (synchronises)."""
@@ -187,6 +203,34 @@ def sl_stack_blob_layout(kind, D, Dkv, F):
     return list(offs), total.value
 
 
+PROJ_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+def proj_shapes(D, Dkv, F):
+    """(N, K) of the seven projections of a layer, in blob order."""
+    return [(D, D), (Dkv, D), (Dkv, D), (D, D), (F, D), (F, D), (D, F)]
+
+
+def build_layer_blob(kind, D, Dkv, F, weights, stream=None):
+    """One layer blob on the device from its seven bf16 weights [N, K] (device tensors).
+
+    NF4 blobs are filled by sl_nf4_quantize directly at the layout offsets;
+    bf16 blobs hold the weights as they are (the storage dtype).
+    """
+    import torch
+    offs, total = sl_stack_blob_layout(kind, D, Dkv, F)
+    blob = torch.zeros(total, dtype=torch.uint8, device="cuda")
+    for p, ((N, K), W) in enumerate(zip(proj_shapes(D, Dkv, F), weights)):
+        assert tuple(W.shape) == (N, K)
+        if kind == SL_WEIGHT_NF4:
+            codes = blob[offs[2 * p]: offs[2 * p] + N * K // 2]
+            absmax = blob[offs[2 * p + 1]: offs[2 * p + 1] + N * K // 64 * 4].view(torch.float32)
+            sl_nf4_quantize(W, codes, absmax, stream)
+        else:
+            blob[offs[2 * p]: offs[2 * p] + N * K * 2].view(torch.bfloat16).copy_(W.reshape(-1))
+    return blob
+
+
 class Stack:
     """Owns an sl_stack handle (two device layer buffers, copy stream, events)."""
 
@@ -240,6 +284,7 @@ def sl_ce_workspace_size(M, D, V, chunk_V) -> int:
 
 
 def sl_ce_fwd_bwd(H, W_head, labels, loss, dH, ws, chunk_V=8192, ignore_index=-100, stream=None):
+    """loss: 1-element fp32 device tensor; dH: [M, D] fp32 device tensor."""
     M, D = H.shape
     V = W_head.shape[0]
     _check(lib().sl_ce_fwd_bwd(_ptr(H), M, D, _ptr(W_head), V, _ptr(labels), int(ignore_index), int(chunk_V),

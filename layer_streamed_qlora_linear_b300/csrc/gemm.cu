@@ -2,6 +2,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <vector>
 
 #include "gemm.cuh"
 
@@ -40,6 +41,37 @@ static sl_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ba
   return SL_OK;
 }
 
+// ------------------------------------------------------------ launch timing
+namespace {
+struct TimedLaunch {
+  cudaEvent_t start, stop;
+  int variant;
+  double flops;
+};
+std::mutex g_time_mu;
+bool g_time_on = false;
+std::vector<TimedLaunch> g_timed;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+int variant_of(const GemmLaunch& g) {
+  if (g.epi == kEpiCELse) return 4;
+  if (g.epi == kEpiCEGrad) return 5;
+  if (g.epi == kEpiAddF32) return 6;
+  return (g.bsrc == kBSrcNF4 ? 0 : 2) + (g.bmn ? 1 : 0);
+}
+}  // namespace
+
 template <int BSRC, int BMN, int EPI>
 static sl_status run(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms, const GemmArgs& a,
                      cudaStream_t stream) {
@@ -57,11 +89,14 @@ static sl_status run(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
   return check_launch("gemm_tc_kernel");
 }
 
+sl_status dispatch(const GemmLaunch& g, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms,
+                   cudaStream_t stream);
+
 sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   const GemmArgs& a = g.args;
   if (a.M <= 0 || a.N <= 0 || a.K <= 0) return set_error(SL_ERR_INVALID, "gemm: empty problem");
   if (a.N % 32) return set_error(SL_ERR_INVALID, "gemm: output columns must be a multiple of 32");
-  if (a.r < 0 || a.r > 64 || (a.r % 8)) return set_error(SL_ERR_INVALID, "gemm: LoRA rank must be 0..64, multiple of 8");
+  if (a.r < 0 || a.r > 32 || (a.r % 8)) return set_error(SL_ERR_INVALID, "gemm: LoRA rank must be 0..32, multiple of 8");
   CUtensorMap ma, mb, ms;
   sl_status st = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, a.K, a.M, g.lda * 2, kBK, kBM,
                           CU_TENSOR_MAP_SWIZZLE_128B);
@@ -95,6 +130,29 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     }
     if (st != SL_OK) return st;
   }
+  TimedLaunch tl{nullptr, nullptr, 0, 0.0};
+  {
+    std::lock_guard<std::mutex> lk(g_time_mu);
+    if (g_time_on) {
+      tl.start = pool_event();
+      tl.stop = pool_event();
+      tl.variant = variant_of(g);
+      tl.flops = 2.0 * a.M * static_cast<double>(a.N) * a.K + 2.0 * a.M * static_cast<double>(a.N) * a.r;
+      if (tl.start) cudaEventRecord(tl.start, stream);
+    }
+  }
+  st = dispatch(g, ma, mb, ms, stream);
+  if (tl.start && tl.stop) {
+    cudaEventRecord(tl.stop, stream);
+    std::lock_guard<std::mutex> lk(g_time_mu);
+    g_timed.push_back(tl);
+  }
+  return st;
+}
+
+sl_status dispatch(const GemmLaunch& g, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms,
+                   cudaStream_t stream) {
+  const GemmArgs& a = g.args;
 #define SL_GEMM_CASE(B, MN, E) \
   if (g.bsrc == B && g.bmn == MN && g.epi == E) return run<B, MN, E>(ma, mb, ms, a, stream);
   SL_GEMM_CASE(kBSrcNF4, 0, kEpiStoreBF16)
@@ -109,3 +167,37 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
 }
 
 }  // namespace sl
+
+using namespace sl;
+
+extern "C" sl_status sl_kernel_timing(int32_t enable) {
+  std::lock_guard<std::mutex> lk(g_time_mu);
+  for (auto& t : g_timed) {
+    cudaEventSynchronize(t.stop);
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  if (enable) g_timed.clear();
+  g_time_on = enable != 0;
+  return SL_OK;
+}
+
+extern "C" sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms, double* flops) {
+  SL_REQUIRE(variant >= 0 && variant <= 6, "sl_kernel_timing_read: variant must be 0..6");
+  std::lock_guard<std::mutex> lk(g_time_mu);
+  uint64_t n = 0;
+  double t = 0.0, f = 0.0;
+  for (auto& tl : g_timed) {
+    if (tl.variant != variant) continue;
+    SL_CHECK_CUDA(cudaEventSynchronize(tl.stop));
+    float e = 0.0f;
+    SL_CHECK_CUDA(cudaEventElapsedTime(&e, tl.start, tl.stop));
+    ++n;
+    t += e;
+    f += tl.flops;
+  }
+  if (launches) *launches = n;
+  if (ms) *ms = t;
+  if (flops) *flops = f;
+  return SL_OK;
+}

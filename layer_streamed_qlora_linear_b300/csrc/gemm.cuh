@@ -13,9 +13,10 @@
 //        the tensor core reads; both layouts share one dequant routine
 //        because a row of 64 elements with one absmax is the unit of both.
 // Xe/Be: the rank-r LoRA side product, folded into the same TMEM
-//        accumulator as ceil(r/16) extra K = 16 steps after the main loop
-//        (r <= 64, zero-padded to 16): forward Xe = T = X A^T, Be = s B;
-//        dX         Xe = U = dY B,  Be = s A (MN-major).
+//        accumulator after the main loop: s*Xe (fp32) is split into bf16
+//        hi + lo and multiplied by [Be | Be] over K = 2r (r <= 32, padded to
+//        16): forward Xe = T = X A^T, Be = B;  dX Xe = U = dY B, Be = A
+//        (MN-major).
 //
 // Tile: 128 (M) x 256 (N) x 64 (K), fp32 accumulator in 256 TMEM columns,
 // one tcgen05.mma.cta_group::1.kind::f16 128x256x16 per 16 of K.
@@ -40,7 +41,7 @@ enum GemmBSrc { kBSrcBF16 = 0, kBSrcNF4 = 1 };
 enum GemmEpi {
   kEpiStoreBF16 = 0,   // out[m, j] = bf16(acc)
   kEpiCELse = 1,       // per-row (max, sum exp) over the tile + label logit gather
-  kEpiCEGrad = 2,      // out[m, j] = bf16((exp(acc - lse[m]) - [j == label]) * scale[m])
+  kEpiCEGrad = 2,      // out[m, j] = bf16(exp(acc - lse[m]) * scale[m])  (softmax / N_valid)
   kEpiAddF32 = 3,      // outf[m, j] (+)= acc (fp32), "beta" = 0 on the first call
 };
 
@@ -70,7 +71,7 @@ struct GemmCfg {
 
 struct GemmArgs {
   int M, N, K;                 // rows, output columns, reduction length
-  const uint16_t* lora_x;      // [M, r] bf16 (T or U) or nullptr
+  const float* lora_x;         // [M, r] fp32 (T or U) or nullptr
   const uint16_t* lora_w;      // K-major: [N, r]; MN-major: [r, N] (ld N); bf16
   int r;
   float s;                     // LoRA scale alpha / r
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         } else {
           ptx::tc_fence_after();
           const int s = KB % S;
-          const int ksteps = (args.r + 15) / 16;
+          const int ksteps = (2 * args.r + 15) / 16;
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint64_t ad = ptx::smem_desc(a_base + s * kATileBytes + kk * 32, 16, 1024, 2);
             const uint64_t bd = BMN ? ptx::smem_desc(b_base + s * kBTileBytes + kk * 2048, 64 * 128, 1024, 2)
@@ -269,60 +270,91 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int dq = tid - 64;  // 0..127
     const float* tab = sTab + ((lane >> 4) << 4);
     bool ok = true;
-    // LoRA side operands, as 16-byte chunks (8 bf16).  Xe: this thread's row
-    // dq, chunks 0..nchunk-1.  Be: K-major -- rows dq + 128*(t/nchunk), chunk
-    // t % nchunk; MN-major -- task dq + 128*t = (row i = task/32, chunk task%32).
-    // Rank is zero-padded to a multiple of 16; Be carries the scale s.
+    // LoRA side operands.  s * Xe (fp32; Xe = T or U) is split into bf16
+    // hi + lo halves and folded over K = 2r columns [hi | lo] against
+    // [Be | Be], so the side product keeps fp32 accuracy; Be (B_lora for the
+    // forward, A_lora for dX) is used as stored.  The folded K is zero-padded
+    // to a multiple of 16.  Thread dq owns row dq of Xe; Be is handled in
+    // 2 * r/8 sixteen-byte tasks per thread (K-major: rows dq and dq + 128 x
+    // rank groups; MN-major: rank rows x 32 column chunks).
     const int r = args.r;
-    const int nchunk = has_lora ? ((r + 15) / 16) * 2 : 0;
-    const int nbe = nchunk * 2;  // K-major: 256 rows x nchunk; MN-major: (2*nchunk*8) rows x 32 / 128
-    auto scale8 = [&](uint4 v) {
-      uint32_t* p = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) p[e] = pack_bf16x2(bf16_lo(p[e]) * args.s, bf16_hi(p[e]) * args.s);
-      return v;
-    };
-    auto load_xe = [&](int c) -> uint4 {
+    const int nr = r / 8;
+    const int kpad = ((2 * r + 15) / 16) * 16;
+    const int nchunk = kpad / 8;
+    const int nbe = 2 * nr;
+    auto load_xe = [&](int g, float (&v)[8]) {
       const int gm = m0 + dq;
-      if (gm < args.M && c * 8 < r)
-        return *reinterpret_cast<const uint4*>(args.lora_x + static_cast<int64_t>(gm) * r + c * 8);
-      return make_uint4(0, 0, 0, 0);
+      if (gm < args.M) {
+        const float4* p = reinterpret_cast<const float4*>(args.lora_x + static_cast<int64_t>(gm) * r + g * 8);
+        const float4 a = p[0], b = p[1];
+        v[0] = a.x * args.s; v[1] = a.y * args.s; v[2] = a.z * args.s; v[3] = a.w * args.s;
+        v[4] = b.x * args.s; v[5] = b.y * args.s; v[6] = b.z * args.s; v[7] = b.w * args.s;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+      }
     };
-    auto store_xe = [&](uint8_t* at, int c, uint4 v) {
-      *reinterpret_cast<uint4*>(at + dq * 128 + ((c ^ (dq & 7)) << 4)) = v;
+    auto chunk_at = [&](uint8_t* base, int row, int c) {
+      return reinterpret_cast<uint4*>(base + row * 128 + ((c ^ (row & 7)) << 4));
+    };
+    auto store_xe = [&](uint8_t* at, int g, const float (&v)[8]) {
+      uint4 hi, lo;
+      uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
+      uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ph[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+        pl[e] = pack_bf16x2(v[2 * e] - bf16_lo(ph[e]), v[2 * e + 1] - bf16_hi(ph[e]));
+      }
+      *chunk_at(at, dq, g) = hi;
+      *chunk_at(at, dq, nr + g) = lo;
     };
     auto load_be = [&](int t) -> uint4 {
       if (!BMN) {
-        const int j = dq + 128 * (t / nchunk), c = t % nchunk;
+        const int j = dq + 128 * (t / nr), g = t % nr;
         const int gn = n0 + j;
-        if (gn < args.N && c * 8 < r)
-          return scale8(*reinterpret_cast<const uint4*>(args.lora_w + static_cast<int64_t>(gn) * r + c * 8));
+        if (gn < args.N) return *reinterpret_cast<const uint4*>(args.lora_w + static_cast<int64_t>(gn) * r + g * 8);
       } else {
         const int task = dq + 128 * t;
         const int i = task >> 5, gcol = n0 + (task & 31) * 8;
-        if (i < r && gcol < args.N)
-          return scale8(*reinterpret_cast<const uint4*>(args.lora_w + static_cast<int64_t>(i) * args.N + gcol));
+        if (gcol < args.N) return *reinterpret_cast<const uint4*>(args.lora_w + static_cast<int64_t>(i) * args.N + gcol);
       }
       return make_uint4(0, 0, 0, 0);
     };
+    auto mn_chunk = [&](uint8_t* bt, int i, int cc) {
+      return reinterpret_cast<uint4*>(bt + (cc >> 3) * (64 * 128) + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
+    };
     auto store_be = [&](uint8_t* bt, int t, uint4 v) {
       if (!BMN) {
-        const int j = dq + 128 * (t / nchunk), c = t % nchunk;
-        *reinterpret_cast<uint4*>(bt + j * 128 + ((c ^ (j & 7)) << 4)) = v;
+        const int j = dq + 128 * (t / nr), g = t % nr;
+        *chunk_at(bt, j, g) = v;
+        *chunk_at(bt, j, nr + g) = v;
       } else {
         const int task = dq + 128 * t;
         const int i = task >> 5, cc = task & 31;
-        *reinterpret_cast<uint4*>(bt + (cc >> 3) * (64 * 128) + i * 128 + (((cc & 7) ^ (i & 7)) << 4)) = v;
+        *mn_chunk(bt, i, cc) = v;
+        *mn_chunk(bt, r + i, cc) = v;
       }
+    };
+    auto store_pad = [&](uint8_t* at, uint8_t* bt) {  // zero the K columns 2r .. kpad-1
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int c = 2 * nr; c < nchunk; ++c) {
+        *chunk_at(at, dq, c) = z;
+        if (!BMN) {
+          *chunk_at(bt, dq, c) = z;
+          *chunk_at(bt, dq + 128, c) = z;
+        }
+      }
+      if (BMN)
+        for (int task = dq; task < (kpad - 2 * r) * 32; task += 128) *mn_chunk(bt, 2 * r + (task >> 5), task & 31) = z;
     };
     // Rank <= 16: fetch the operands now, while the main loop runs.
     const bool lora_pref = has_lora && r <= 16;
-    uint4 pre[6];
+    float pre_x[2][8];
+    uint4 pre_b[4];
     if (lora_pref) {
-#pragma unroll
-      for (int c = 0; c < 2; ++c) pre[c] = load_xe(c);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) pre[2 + t] = load_be(t);
+      for (int g = 0; g < nr; ++g) load_xe(g, pre_x[g]);
+      for (int t = 0; t < nbe; ++t) pre_b[t] = load_be(t);
     }
     if (BSRC == kBSrcNF4) {
       for (int kb = 0; kb < KB; ++kb) {
@@ -361,14 +393,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint8_t* at = sA + s * kATileBytes;
         uint8_t* bt = sB + s * kBTileBytes;
         if (lora_pref) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) store_xe(at, c, pre[c]);
-#pragma unroll
-          for (int t = 0; t < 4; ++t) store_be(bt, t, pre[2 + t]);
+          for (int g = 0; g < nr; ++g) store_xe(at, g, pre_x[g]);
+          for (int t = 0; t < nbe; ++t) store_be(bt, t, pre_b[t]);
         } else {
-          for (int c = 0; c < nchunk; ++c) store_xe(at, c, load_xe(c));
+          for (int g = 0; g < nr; ++g) {
+            float v[8];
+            load_xe(g, v);
+            store_xe(at, g, v);
+          }
           for (int t = 0; t < nbe; ++t) store_be(bt, t, load_be(t));
         }
+        store_pad(at, bt);
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(lora_full);
       }
@@ -463,24 +498,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint16_t* out = reinterpret_cast<uint16_t*>(args.out);
         const float lse = (gm < args.M) ? args.row_lse[gm] : 0.0f;
         const float sc = (gm < args.M) ? args.row_scale[gm] : 0.0f;
-        const int lab = (gm < args.M) ? args.labels[gm] : -1;
 #pragma unroll 1
         for (int c0 = 0; c0 < kBN; c0 += 32) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c0, v);
           ptx::tmem_wait_ld();
           if (gm < args.M && n0 + c0 < args.N) {
-            const int vid = args.vocab_base + n0 + c0;
             uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(gm) * args.ld_out + n0 + c0);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               float f[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int idx = 8 * g + e;
-                const float p = __expf(__uint_as_float(v[idx]) - lse);
-                f[e] = (p - ((vid + idx) == lab ? 1.0f : 0.0f)) * sc;
-              }
+              for (int e = 0; e < 8; ++e) f[e] = __expf(__uint_as_float(v[8 * g + e]) - lse) * sc;
               uint4 o;
               o.x = pack_bf16x2(f[0], f[1]);
               o.y = pack_bf16x2(f[2], f[3]);

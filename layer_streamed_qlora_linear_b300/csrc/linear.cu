@@ -14,12 +14,12 @@
 
 namespace sl {
 
-// out[m, i] = bf16( sum_k X[m, k] * W(i, k) ),  W(i, k) = Wp[i * w_si + k * w_sk]
+// out[m, i] = sum_k X[m, k] * W(i, k)  (fp32),  W(i, k) = Wp[i * w_si + k * w_sk]
 // 8 warps x 2 rows per block; W staged 256 columns at a time.
 template <int R>
 __global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t* __restrict__ X, int64_t M, int K,
                                                         const uint16_t* __restrict__ Wp, int64_t w_si,
-                                                        int64_t w_sk, int r, uint16_t* __restrict__ out) {
+                                                        int64_t w_sk, int r, float* __restrict__ out) {
   __shared__ __align__(16) uint16_t wsm[R][256 + 8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * 16 + warp * 2;
@@ -78,14 +78,14 @@ __global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t* __restri
       float v = acc[a][i];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0 && row < M && i < r) out[row * r + i] = f32_to_bf16(v);
+      if (lane == 0 && row < M && i < r) out[row * r + i] = v;
     }
   }
 }
 
 // part[split][i][k] = sum_{m in split} P[m, i] * Q[m, k]   (fixed m order)
 template <int R>
-__global__ void __launch_bounds__(256) lora_grad_partial_kernel(const uint16_t* __restrict__ P,
+__global__ void __launch_bounds__(256) lora_grad_partial_kernel(const float* __restrict__ P,
                                                                 const uint16_t* __restrict__ Q, int64_t M, int Kq,
                                                                 int r, int64_t m_per_split,
                                                                 float* __restrict__ part) {
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256) lora_grad_partial_kernel(const uint16_t* 
     __syncthreads();
     for (int idx = threadIdx.x; idx < 64 * R; idx += 256) {
       const int mm = idx / R, i = idx % R;
-      psm[mm][i] = (mc + mm < me && i < r) ? bf16_to_f32(P[(mc + mm) * r + i]) : 0.0f;
+      psm[mm][i] = (mc + mm < me && i < r) ? P[(mc + mm) * r + i] : 0.0f;
     }
     __syncthreads();
     const int nrow = static_cast<int>((me - mc) < 64 ? (me - mc) : 64);
@@ -146,18 +146,17 @@ int grad_splits(int64_t M) {
 }
 
 sl_status lora_down(const uint16_t* X, int64_t M, int K, const uint16_t* W, int64_t w_si, int64_t w_sk, int r,
-                    uint16_t* out, cudaStream_t stream) {
+                    float* out, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(ceil_div(M, 16));
 #define SL_DOWN(RR) lora_down_kernel<RR><<<grid, 256, 0, stream>>>(X, M, K, W, w_si, w_sk, r, out)
   if (r <= 8) SL_DOWN(8);
   else if (r <= 16) SL_DOWN(16);
-  else if (r <= 32) SL_DOWN(32);
-  else SL_DOWN(64);
+  else SL_DOWN(32);
 #undef SL_DOWN
   return check_launch("lora_down_kernel");
 }
 
-sl_status lora_grad(const uint16_t* P, const uint16_t* Q, int64_t M, int Kq, int r, float s, float* out,
+sl_status lora_grad(const float* P, const uint16_t* Q, int64_t M, int Kq, int r, float s, float* out,
                     int transpose, int accumulate, float* part, cudaStream_t stream) {
   const int splits = grad_splits(M);
   const int64_t mps = ceil_div(ceil_div(M, splits), 64) * 64;
@@ -165,8 +164,7 @@ sl_status lora_grad(const uint16_t* P, const uint16_t* Q, int64_t M, int Kq, int
 #define SL_GRAD(RR) lora_grad_partial_kernel<RR><<<grid, 256, 0, stream>>>(P, Q, M, Kq, r, mps, part)
   if (r <= 8) SL_GRAD(8);
   else if (r <= 16) SL_GRAD(16);
-  else if (r <= 32) SL_GRAD(32);
-  else SL_GRAD(64);
+  else SL_GRAD(32);
 #undef SL_GRAD
   sl_status st = check_launch("lora_grad_partial_kernel");
   if (st != SL_OK) return st;
@@ -180,7 +178,7 @@ sl_status lora_grad(const uint16_t* P, const uint16_t* Q, int64_t M, int Kq, int
 size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
   if (r <= 0) return 0;
   const int splits = grad_splits(M);
-  return align_up(static_cast<size_t>(M) * r * 2, 256) + align_up(static_cast<size_t>(splits) * r * K * 4, 256) +
+  return align_up(static_cast<size_t>(M) * r * 4, 256) + align_up(static_cast<size_t>(splits) * r * K * 4, 256) +
          align_up(static_cast<size_t>(splits) * r * N * 4, 256);
 }
 
@@ -206,13 +204,13 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
   if (st != SL_OK) return st;
   SL_REQUIRE(X && Y && M > 0, "sl_lora_linear_fwd: null X/Y or M <= 0");
   const bool lora = r > 0 && A && B;
-  SL_REQUIRE(!lora || (r % 8 == 0 && r <= 64 && T_save), "sl_lora_linear_fwd: need r % 8 == 0, r <= 64, T_save");
+  SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32 && T_save), "sl_lora_linear_fwd: need r % 8 == 0, r <= 32, T_save");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_fwd: M too large");
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   if (lora) {
     st = lora_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A),
-                   w->K, 1, r, static_cast<uint16_t*>(T_save), stream);
+                   w->K, 1, r, static_cast<float*>(T_save), stream);
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
@@ -228,7 +226,7 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
   g.args.M = static_cast<int>(M);
   g.args.N = static_cast<int>(w->N);
   g.args.K = static_cast<int>(w->K);
-  g.args.lora_x = lora ? static_cast<const uint16_t*>(T_save) : nullptr;
+  g.args.lora_x = lora ? static_cast<const float*>(T_save) : nullptr;
   g.args.lora_w = lora ? static_cast<const uint16_t*>(B) : nullptr;
   g.args.r = lora ? r : 0;
   g.args.s = lora ? alpha / static_cast<float>(r) : 0.0f;
@@ -245,7 +243,7 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   if (st != SL_OK) return st;
   SL_REQUIRE(dY && M > 0, "sl_lora_linear_bwd: null dY or M <= 0");
   const bool lora = r > 0 && A && B;
-  SL_REQUIRE(!lora || (r % 8 == 0 && r <= 64), "sl_lora_linear_bwd: need r % 8 == 0 and r <= 64");
+  SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32), "sl_lora_linear_bwd: need r % 8 == 0 and r <= 32");
   SL_REQUIRE(!lora || (X && T_save && dA && dB), "sl_lora_linear_bwd: LoRA backward needs X, T_save, dA, dB");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_bwd: M too large");
   const size_t need = lora ? linear_bwd_ws_bytes(M, w->N, w->K, r) : 0;
@@ -254,13 +252,13 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   uint8_t* p = static_cast<uint8_t*>(ws);
-  uint16_t* U = nullptr;
+  float* U = nullptr;
   float* partA = nullptr;
   float* partB = nullptr;
   if (lora) {
     const int splits = grad_splits(M);
-    U = reinterpret_cast<uint16_t*>(p);
-    p += align_up(static_cast<size_t>(M) * r * 2, 256);
+    U = reinterpret_cast<float*>(p);
+    p += align_up(static_cast<size_t>(M) * r * 4, 256);
     partA = reinterpret_cast<float*>(p);
     p += align_up(static_cast<size_t>(splits) * r * w->K * 4, 256);
     partB = reinterpret_cast<float*>(p);
@@ -299,7 +297,7 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
     st = lora_grad(U, static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), r, s, dA, 0, accumulate, partA,
                    stream);
     if (st != SL_OK) return st;
-    st = lora_grad(static_cast<const uint16_t*>(T_save), static_cast<const uint16_t*>(dY), M,
+    st = lora_grad(static_cast<const float*>(T_save), static_cast<const uint16_t*>(dY), M,
                    static_cast<int>(w->N), r, s, dB, 1, accumulate, partB, stream);
     if (st != SL_OK) return st;
   }

@@ -1,12 +1,466 @@
-// Temporary: the streamed stack is filled in by the stack scheduler.
+// The layer-streamed stack step (steps a2, a5, a7 plus the seven linears of
+// every layer).
+//
+// "Soup CLI Lets You Fine-Tune an 8B LLM on a 4 GB Laptop GPU", "How Layer
+// Streaming Works": the frozen base stays in system RAM and decoder layers
+// are brought to the GPU for the forward and backward passes.  "Soup:
+// Fine-Tuning an 8B LLM ... with One YAML File", "Layer Streaming: The
+// Mechanism Behind the 4 GB Claim": a pinned base store and two device
+// buffers.  "Exact Layer Streaming ..." (abstract): the streamed run is
+// bit-exact against a resident run of the same numerics.
+//
+// Design: one pinned host blob per layer (sl_stack_blob_layout); two device
+// buffers; layer l lives in buffer l % 2.  A non-blocking copy stream does
+// one cudaMemcpyAsync per layer; event ready[b] (recorded after the copy)
+// gates the compute stream, event free[b] (recorded after the last kernel
+// that read buffer b) gates the next copy into b.  The forward walks layers
+// 0..L-1 prefetching l+2, the backward walks L-1..0 prefetching l-2; the two
+// layers resident at the turn are not copied again, and neither are layers
+// 0 and 1 at the start of the next step when the buffers still hold them
+// (the base is frozen).  RESIDENT mode runs the same kernels in the same
+// order on device copies of the blobs, so both modes give identical bits.
+#include <cstring>
+#include <vector>
+
 #include "common.cuh"
+#include "glue.cuh"
+#include "linear.cuh"
+
 using namespace sl;
-struct sl_stack { int dummy; };
-extern "C" {
-sl_status sl_stack_blob_layout(int32_t, int64_t, int64_t, int64_t, size_t*, size_t*) { return set_error(SL_ERR_UNSUPPORTED, "not built yet"); }
-sl_status sl_stack_create(const sl_stack_desc*, sl_stack**, size_t*, size_t*) { return set_error(SL_ERR_UNSUPPORTED, "not built yet"); }
-sl_status sl_stack_destroy(sl_stack*) { return SL_OK; }
-size_t sl_stack_workspace_size(const sl_stack*, int64_t, int32_t) { return 0; }
-sl_status sl_stream_stack_step(sl_stack*, int32_t, const float*, int64_t, const float*, const void* const*, const void* const*, int32_t, float, float*, float*, float* const*, float* const*, void*, size_t, cudaStream_t) { return set_error(SL_ERR_UNSUPPORTED, "not built yet"); }
-sl_status sl_stack_last_step_stats(const sl_stack*, uint64_t*, uint64_t*) { return set_error(SL_ERR_UNSUPPORTED, "not built yet"); }
+
+struct sl_stack {
+  int L = 0;
+  int kind = 0;
+  int64_t D = 0, Dkv = 0, F = 0;
+  std::vector<const void*> host;
+  std::vector<const void*> dev;
+  size_t offs[14] = {0};
+  size_t blob_bytes = 0;
+  void* buf[2] = {nullptr, nullptr};
+  int buf_layer[2] = {-1, -1};
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ready[2] = {nullptr, nullptr};
+  cudaEvent_t freed[2] = {nullptr, nullptr};
+  int device = 0;
+  uint64_t last_h2d = 0;
+  uint64_t last_kernels = 0;
+};
+
+namespace {
+
+struct Proj {
+  int64_t N, K;
+};
+
+void proj_shapes(int64_t D, int64_t Dkv, int64_t F, Proj p[7]) {
+  p[0] = {D, D};    // q
+  p[1] = {Dkv, D};  // k
+  p[2] = {Dkv, D};  // v
+  p[3] = {D, D};    // o
+  p[4] = {F, D};    // gate
+  p[5] = {F, D};    // up
+  p[6] = {D, F};    // down
+}
+
+sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[14], size_t* total) {
+  Proj p[7];
+  proj_shapes(D, Dkv, F, p);
+  size_t off = 0;
+  for (int i = 0; i < 7; ++i) {
+    const size_t n = static_cast<size_t>(p[i].N) * static_cast<size_t>(p[i].K);
+    if (kind == SL_WEIGHT_NF4) {
+      offs[2 * i] = off;
+      off = align_up(off + n / 2, 256);
+      offs[2 * i + 1] = off;
+      off = align_up(off + n / 64 * 4, 256);
+    } else {
+      offs[2 * i] = off;
+      off = align_up(off + n * 2, 256);
+      offs[2 * i + 1] = 0;
+    }
+  }
+  *total = off;
+  return SL_OK;
+}
+
+// Workspace plan: per-layer saved activations plus shared scratch.
+struct Plan {
+  size_t total = 0;
+  // per layer
+  std::vector<size_t> hin, h1, rstd1, rstd2, x1, q, k, v, a, x2, g, u, m;
+  std::vector<size_t> T;  // [L * 7]
+  // shared
+  size_t o, d, dhA, dhB, dd, dm, dg, du, dx2a, dx2b, dh1, do_, da, dq, dk, dv, dx1q, dx1k, dx1v, lin_ws;
+  size_t lin_ws_bytes = 0;
+};
+
+Plan make_plan(const sl_stack* s, int64_t M, int r) {
+  Plan P;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t MD = static_cast<size_t>(M) * s->D, MK = static_cast<size_t>(M) * s->Dkv,
+               MF = static_cast<size_t>(M) * s->F;
+  const int L = s->L;
+  const int rr = r > 0 ? r : 0;
+  for (int l = 0; l < L; ++l) {
+    P.hin.push_back(l == 0 ? 0 : take(MD * 4));
+    P.h1.push_back(take(MD * 4));
+    P.rstd1.push_back(take(M * 4));
+    P.rstd2.push_back(take(M * 4));
+    P.x1.push_back(take(MD * 2));
+    P.q.push_back(take(MD * 2));
+    P.k.push_back(take(MK * 2));
+    P.v.push_back(take(MK * 2));
+    P.a.push_back(take(MD * 2));
+    P.x2.push_back(take(MD * 2));
+    P.g.push_back(take(MF * 2));
+    P.u.push_back(take(MF * 2));
+    P.m.push_back(take(MF * 2));
+    for (int p = 0; p < 7; ++p) P.T.push_back(take(static_cast<size_t>(M) * (rr ? rr : 1) * 4));
+  }
+  P.o = take(MD * 2);
+  P.d = take(MD * 2);
+  P.dhA = take(MD * 4);
+  P.dhB = take(MD * 4);
+  P.dd = take(MD * 2);
+  P.dm = take(MF * 2);
+  P.dg = take(MF * 2);
+  P.du = take(MF * 2);
+  P.dx2a = take(MD * 2);
+  P.dx2b = take(MD * 2);
+  P.dh1 = take(MD * 4);
+  P.do_ = take(MD * 2);
+  P.da = take(MD * 2);
+  P.dq = take(MD * 2);
+  P.dk = take(MK * 2);
+  P.dv = take(MK * 2);
+  P.dx1q = take(MD * 2);
+  P.dx1k = take(MD * 2);
+  P.dx1v = take(MD * 2);
+  Proj pr[7];
+  proj_shapes(s->D, s->Dkv, s->F, pr);
+  size_t lw = 0;
+  for (int p = 0; p < 7; ++p) {
+    const size_t b = linear_bwd_ws_bytes(M, pr[p].N, pr[p].K, rr);
+    if (b > lw) lw = b;
+  }
+  P.lin_ws_bytes = lw;
+  P.lin_ws = take(lw ? lw : 256);
+  P.total = off;
+  return P;
+}
+
+struct StepCtx {
+  sl_stack* s;
+  const Plan* P;
+  uint8_t* ws;
+  int64_t M;
+  int r;
+  float alpha;
+  const void* const* A;
+  const void* const* B;
+  float* const* dA;
+  float* const* dB;
+  cudaStream_t stream;
+  uint64_t kernels = 0;
+
+  template <typename T>
+  T* at(size_t off) const {
+    return reinterpret_cast<T*>(ws + off);
+  }
+};
+
+void weights_of(const sl_stack* s, const void* base, sl_weight w[7]) {
+  Proj p[7];
+  proj_shapes(s->D, s->Dkv, s->F, p);
+  const uint8_t* b = static_cast<const uint8_t*>(base);
+  for (int i = 0; i < 7; ++i) {
+    w[i].kind = s->kind;
+    w[i].N = p[i].N;
+    w[i].K = p[i].K;
+    if (s->kind == SL_WEIGHT_NF4) {
+      w[i].codes = b + s->offs[2 * i];
+      w[i].absmax = reinterpret_cast<const float*>(b + s->offs[2 * i + 1]);
+      w[i].w = nullptr;
+    } else {
+      w[i].codes = nullptr;
+      w[i].absmax = nullptr;
+      w[i].w = b + s->offs[2 * i];
+    }
+  }
+}
+
+#define SL_TRY(expr)                  \
+  do {                                \
+    sl_status _st = (expr);           \
+    if (_st != SL_OK) return _st;     \
+  } while (0)
+
+sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, float* h_out) {
+  const Plan& P = *c.P;
+  const sl_stack* s = c.s;
+  const int64_t M = c.M;
+  const int D = static_cast<int>(s->D), Dkv = static_cast<int>(s->Dkv);
+  const int r = c.r;
+  auto A = [&](int p) { return r > 0 ? c.A[7 * l + p] : nullptr; };
+  auto B = [&](int p) { return r > 0 ? c.B[7 * l + p] : nullptr; };
+  auto T = [&](int p) { return c.at<float>(P.T[7 * l + p]); };
+  uint16_t* x1 = c.at<uint16_t>(P.x1[l]);
+  uint16_t* q = c.at<uint16_t>(P.q[l]);
+  uint16_t* k = c.at<uint16_t>(P.k[l]);
+  uint16_t* v = c.at<uint16_t>(P.v[l]);
+  uint16_t* a = c.at<uint16_t>(P.a[l]);
+  uint16_t* x2 = c.at<uint16_t>(P.x2[l]);
+  uint16_t* g = c.at<uint16_t>(P.g[l]);
+  uint16_t* u = c.at<uint16_t>(P.u[l]);
+  uint16_t* m = c.at<uint16_t>(P.m[l]);
+  float* h1 = c.at<float>(P.h1[l]);
+  uint16_t* o = c.at<uint16_t>(P.o);
+  uint16_t* d = c.at<uint16_t>(P.d);
+  const uint64_t lin = r > 0 ? 2 : 1;
+  SL_TRY(glue_rms_fwd(h_in, nullptr, nullptr, x1, c.at<float>(P.rstd1[l]), M, D, c.stream));
+  SL_TRY(linear_fwd(&w[0], x1, M, A(0), B(0), r, c.alpha, q, T(0), c.stream));
+  SL_TRY(linear_fwd(&w[1], x1, M, A(1), B(1), r, c.alpha, k, T(1), c.stream));
+  SL_TRY(linear_fwd(&w[2], x1, M, A(2), B(2), r, c.alpha, v, T(2), c.stream));
+  SL_TRY(glue_mix_fwd(q, k, v, a, M, D, Dkv, c.stream));
+  SL_TRY(linear_fwd(&w[3], a, M, A(3), B(3), r, c.alpha, o, T(3), c.stream));
+  SL_TRY(glue_rms_fwd(h_in, o, h1, x2, c.at<float>(P.rstd2[l]), M, D, c.stream));
+  SL_TRY(linear_fwd(&w[4], x2, M, A(4), B(4), r, c.alpha, g, T(4), c.stream));
+  SL_TRY(linear_fwd(&w[5], x2, M, A(5), B(5), r, c.alpha, u, T(5), c.stream));
+  SL_TRY(glue_swiglu_fwd(g, u, m, M * s->F, c.stream));
+  SL_TRY(linear_fwd(&w[6], m, M, A(6), B(6), r, c.alpha, d, T(6), c.stream));
+  SL_TRY(glue_resid_add(h1, d, h_out, M * s->D, c.stream));
+  c.kernels += 5 + 7 * lin;
+  return SL_OK;
+}
+
+// dh2: gradient w.r.t. this layer's output (fp32) and its bf16 copy dd;
+// writes dh (w.r.t. the layer input) and, if dh_bf16, its bf16 copy.
+sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, const float* dh2,
+                    const uint16_t* dd, float* dh, uint16_t* dh_bf16) {
+  const Plan& P = *c.P;
+  const sl_stack* s = c.s;
+  const int64_t M = c.M;
+  const int D = static_cast<int>(s->D), Dkv = static_cast<int>(s->Dkv);
+  const int r = c.r;
+  auto A = [&](int p) { return r > 0 ? c.A[7 * l + p] : nullptr; };
+  auto B = [&](int p) { return r > 0 ? c.B[7 * l + p] : nullptr; };
+  auto T = [&](int p) { return c.at<float>(P.T[7 * l + p]); };
+  auto dA = [&](int p) { return r > 0 ? c.dA[7 * l + p] : nullptr; };
+  auto dB = [&](int p) { return r > 0 ? c.dB[7 * l + p] : nullptr; };
+  void* lws = c.at<uint8_t>(P.lin_ws);
+  const size_t lwb = P.lin_ws_bytes;
+  uint16_t* dm = c.at<uint16_t>(P.dm);
+  uint16_t* dg = c.at<uint16_t>(P.dg);
+  uint16_t* du = c.at<uint16_t>(P.du);
+  uint16_t* dx2a = c.at<uint16_t>(P.dx2a);
+  uint16_t* dx2b = c.at<uint16_t>(P.dx2b);
+  float* dh1 = c.at<float>(P.dh1);
+  uint16_t* do_ = c.at<uint16_t>(P.do_);
+  uint16_t* da = c.at<uint16_t>(P.da);
+  uint16_t* dq = c.at<uint16_t>(P.dq);
+  uint16_t* dk = c.at<uint16_t>(P.dk);
+  uint16_t* dv = c.at<uint16_t>(P.dv);
+  uint16_t* dx1q = c.at<uint16_t>(P.dx1q);
+  uint16_t* dx1k = c.at<uint16_t>(P.dx1k);
+  uint16_t* dx1v = c.at<uint16_t>(P.dx1v);
+  const uint64_t lin = r > 0 ? 6 : 1;
+  SL_TRY(linear_bwd(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, T(6), dm, dA(6), dB(6), 0, lws,
+                    lwb, c.stream));
+  SL_TRY(glue_swiglu_bwd(dm, c.at<uint16_t>(P.g[l]), c.at<uint16_t>(P.u[l]), dg, du, M * s->F, c.stream));
+  SL_TRY(linear_bwd(&w[4], c.at<uint16_t>(P.x2[l]), dg, M, A(4), B(4), r, c.alpha, T(4), dx2a, dA(4), dB(4), 0,
+                    lws, lwb, c.stream));
+  SL_TRY(linear_bwd(&w[5], c.at<uint16_t>(P.x2[l]), du, M, A(5), B(5), r, c.alpha, T(5), dx2b, dA(5), dB(5), 0,
+                    lws, lwb, c.stream));
+  SL_TRY(glue_rms_bwd(dh2, dx2a, dx2b, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]), dh1, do_, M, D,
+                      c.stream));
+  SL_TRY(linear_bwd(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, T(3), da, dA(3), dB(3), 0, lws,
+                    lwb, c.stream));
+  SL_TRY(glue_mix_bwd(da, c.at<uint16_t>(P.q[l]), c.at<uint16_t>(P.k[l]), dq, dk, dv, M, D, Dkv, c.stream));
+  const uint16_t* x1 = c.at<uint16_t>(P.x1[l]);
+  SL_TRY(linear_bwd(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, T(0), dx1q, dA(0), dB(0), 0, lws, lwb, c.stream));
+  SL_TRY(linear_bwd(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, T(1), dx1k, dA(1), dB(1), 0, lws, lwb, c.stream));
+  SL_TRY(linear_bwd(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, T(2), dx1v, dA(2), dB(2), 0, lws, lwb, c.stream));
+  SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, h_in, c.at<float>(P.rstd1[l]), dh, dh_bf16, M, D, c.stream));
+  c.kernels += 4 + 7 * lin;
+  return SL_OK;
+}
+
+// Make sure buffer l % 2 holds layer l (copy only if it does not already).
+sl_status ensure_layer(sl_stack* s, int l, uint64_t* h2d) {
+  const int b = l % 2;
+  if (s->buf_layer[b] == l) return SL_OK;
+  SL_CHECK_CUDA(cudaStreamWaitEvent(s->copy_stream, s->freed[b], 0));
+  SL_CHECK_CUDA(cudaMemcpyAsync(s->buf[b], s->host[l], s->blob_bytes, cudaMemcpyHostToDevice, s->copy_stream));
+  SL_CHECK_CUDA(cudaEventRecord(s->ready[b], s->copy_stream));
+  s->buf_layer[b] = l;
+  *h2d += s->blob_bytes;
+  return SL_OK;
+}
+
+}  // namespace
+
+extern "C" sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F, size_t offsets[14],
+                                          size_t* blob_bytes) {
+  SL_REQUIRE(offsets && blob_bytes, "sl_stack_blob_layout: null output");
+  SL_REQUIRE(kind == SL_WEIGHT_NF4 || kind == SL_WEIGHT_BF16, "sl_stack_blob_layout: unknown kind");
+  SL_REQUIRE(D > 0 && Dkv > 0 && F > 0 && D % 256 == 0 && F % 256 == 0 && Dkv % 128 == 0 && D % Dkv == 0,
+             "sl_stack_blob_layout: need D, F multiples of 256, Dkv a multiple of 128 dividing D");
+  return layout(kind, D, Dkv, F, offsets, blob_bytes);
+}
+
+extern "C" sl_status sl_stack_create(const sl_stack_desc* desc, sl_stack** out, size_t* host_bytes,
+                                     size_t* buffer_bytes) {
+  SL_REQUIRE(desc && out, "sl_stack_create: null argument");
+  SL_REQUIRE(desc->L > 0 && desc->host_blobs, "sl_stack_create: need L > 0 and host_blobs");
+  size_t offs[14], bytes = 0;
+  sl_status st = sl_stack_blob_layout(desc->kind, desc->D, desc->Dkv, desc->F, offs, &bytes);
+  if (st != SL_OK) return st;
+  for (int l = 0; l < desc->L; ++l) {
+    const void* p = desc->host_blobs[l];
+    SL_REQUIRE(p, "sl_stack_create: null host blob");
+    for (const void* q : {p, static_cast<const void*>(static_cast<const uint8_t*>(p) + bytes - 1)}) {
+      cudaPointerAttributes at{};
+      cudaError_t e = cudaPointerGetAttributes(&at, q);
+      if (e != cudaSuccess || at.type != cudaMemoryTypeHost) {
+        cudaGetLastError();
+        return set_error(SL_ERR_INVALID, "sl_stack_create: host blob " + std::to_string(l) +
+                                             " is not page-locked (pinned) host memory");
+      }
+    }
+    if (desc->device_blobs) {
+      cudaPointerAttributes at{};
+      cudaError_t e = cudaPointerGetAttributes(&at, desc->device_blobs[l]);
+      if (e != cudaSuccess || at.type != cudaMemoryTypeDevice) {
+        cudaGetLastError();
+        return set_error(SL_ERR_INVALID, "sl_stack_create: device blob " + std::to_string(l) +
+                                             " is not device memory");
+      }
+    }
+  }
+  sl_stack* s = new sl_stack();
+  s->L = desc->L;
+  s->kind = desc->kind;
+  s->D = desc->D;
+  s->Dkv = desc->Dkv;
+  s->F = desc->F;
+  s->host.assign(desc->host_blobs, desc->host_blobs + desc->L);
+  if (desc->device_blobs) s->dev.assign(desc->device_blobs, desc->device_blobs + desc->L);
+  std::memcpy(s->offs, offs, sizeof(offs));
+  s->blob_bytes = bytes;
+  cudaGetDevice(&s->device);
+  auto fail = [&](cudaError_t e, const char* what) {
+    sl_status r = cuda_error(e, what);
+    sl_stack_destroy(s);
+    return r;
+  };
+  cudaError_t e;
+  for (int b = 0; b < 2; ++b) {
+    if ((e = cudaMalloc(&s->buf[b], bytes)) != cudaSuccess) return fail(e, "sl_stack_create: cudaMalloc buffer");
+    if ((e = cudaEventCreateWithFlags(&s->ready[b], cudaEventDisableTiming)) != cudaSuccess)
+      return fail(e, "sl_stack_create: event");
+    if ((e = cudaEventCreateWithFlags(&s->freed[b], cudaEventDisableTiming)) != cudaSuccess)
+      return fail(e, "sl_stack_create: event");
+  }
+  if ((e = cudaStreamCreateWithFlags(&s->copy_stream, cudaStreamNonBlocking)) != cudaSuccess)
+    return fail(e, "sl_stack_create: copy stream");
+  if (host_bytes) *host_bytes = bytes * static_cast<size_t>(desc->L);
+  if (buffer_bytes) *buffer_bytes = 2 * bytes;
+  *out = s;
+  return SL_OK;
+}
+
+extern "C" sl_status sl_stack_destroy(sl_stack* s) {
+  if (!s) return SL_OK;
+  if (s->copy_stream) cudaStreamSynchronize(s->copy_stream);
+  for (int b = 0; b < 2; ++b) {
+    if (s->freed[b]) cudaEventSynchronize(s->freed[b]);
+    if (s->buf[b]) cudaFree(s->buf[b]);
+    if (s->ready[b]) cudaEventDestroy(s->ready[b]);
+    if (s->freed[b]) cudaEventDestroy(s->freed[b]);
+  }
+  if (s->copy_stream) cudaStreamDestroy(s->copy_stream);
+  delete s;
+  return SL_OK;
+}
+
+extern "C" size_t sl_stack_workspace_size(const sl_stack* s, int64_t M, int32_t r) {
+  if (!s || M <= 0) return 0;
+  return make_plan(s, M, r).total;
+}
+
+extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64_t M,
+                                          const float* dh_top, const void* const* A, const void* const* B,
+                                          int32_t r, float alpha, float* hL, float* dh0, float* const* dA,
+                                          float* const* dB, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  SL_REQUIRE(s, "sl_stream_stack_step: null stack");
+  SL_REQUIRE(mode == SL_MODE_STREAMED || mode == SL_MODE_RESIDENT, "sl_stream_stack_step: bad mode");
+  SL_REQUIRE(mode == SL_MODE_STREAMED || !s->dev.empty(), "sl_stream_stack_step: RESIDENT needs device_blobs");
+  SL_REQUIRE(h0 && dh_top && hL && dh0 && ws && M > 0, "sl_stream_stack_step: null argument");
+  SL_REQUIRE(r == 0 || (A && B && dA && dB), "sl_stream_stack_step: adapters and gradients required for r > 0");
+  SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_stream_stack_step: workspace must be 256-byte aligned");
+  int dev = 0;
+  SL_CHECK_CUDA(cudaGetDevice(&dev));
+  SL_REQUIRE(dev == s->device, "sl_stream_stack_step: current device differs from the handle's");
+  const Plan P = make_plan(s, M, r);
+  SL_REQUIRE(ws_bytes >= P.total, "sl_stream_stack_step: workspace too small (need " + std::to_string(P.total) +
+                                      " bytes)");
+  StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, stream};
+  const int L = s->L;
+  const bool streamed = mode == SL_MODE_STREAMED;
+  uint64_t h2d = 0;
+  sl_weight w[7];
+  auto base_of = [&](int l) -> const void* { return streamed ? s->buf[l % 2] : s->dev[l]; };
+  auto h_in = [&](int l) -> const float* { return l == 0 ? h0 : c.at<float>(P.hin[l]); };
+
+  // ---------------------------------------------------------------- forward
+  if (streamed) {
+    SL_TRY(ensure_layer(s, 0, &h2d));
+    if (L > 1) SL_TRY(ensure_layer(s, 1, &h2d));
+  }
+  for (int l = 0; l < L; ++l) {
+    if (streamed) SL_CHECK_CUDA(cudaStreamWaitEvent(stream, s->ready[l % 2], 0));
+    weights_of(s, base_of(l), w);
+    float* out = (l == L - 1) ? hL : c.at<float>(P.hin[l + 1]);
+    SL_TRY(layer_fwd(c, l, w, h_in(l), out));
+    if (streamed) {
+      SL_CHECK_CUDA(cudaEventRecord(s->freed[l % 2], stream));
+      if (l + 2 < L) SL_TRY(ensure_layer(s, l + 2, &h2d));
+    }
+  }
+  // --------------------------------------------------------------- backward
+  float* dhA = c.at<float>(P.dhA);
+  float* dhB = c.at<float>(P.dhB);
+  uint16_t* dd = c.at<uint16_t>(P.dd);
+  SL_TRY(glue_to_bf16(dh_top, dd, M * s->D, stream));
+  c.kernels += 1;
+  const float* dh_cur = dh_top;
+  for (int l = L - 1; l >= 0; --l) {
+    if (streamed) {
+      SL_TRY(ensure_layer(s, l, &h2d));
+      SL_CHECK_CUDA(cudaStreamWaitEvent(stream, s->ready[l % 2], 0));
+    }
+    weights_of(s, base_of(l), w);
+    float* dh_next = (l == 0) ? dh0 : ((dh_cur == dhA) ? dhB : dhA);
+    SL_TRY(layer_bwd(c, l, w, h_in(l), dh_cur, dd, dh_next, l == 0 ? nullptr : dd));
+    dh_cur = dh_next;
+    if (streamed) {
+      SL_CHECK_CUDA(cudaEventRecord(s->freed[l % 2], stream));
+      if (l - 2 >= 0) SL_TRY(ensure_layer(s, l - 2, &h2d));
+    }
+  }
+  s->last_h2d = h2d;
+  s->last_kernels = c.kernels;
+  return SL_OK;
+}
+
+extern "C" sl_status sl_stack_last_step_stats(const sl_stack* s, uint64_t* h2d_bytes, uint64_t* kernels) {
+  SL_REQUIRE(s, "sl_stack_last_step_stats: null stack");
+  if (h2d_bytes) *h2d_bytes = s->last_h2d;
+  if (kernels) *kernels = s->last_kernels;
+  return SL_OK;
 }

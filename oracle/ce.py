@@ -18,8 +18,11 @@ Float64 throughout, rows processed in chunks only to bound memory.
 import numpy as np
 
 
-def ce_rows(H, W, labels, n_valid, ignore_index=-100, want_soft=False):
-    """Per-row loss terms and dH rows for the given rows, with the global N_valid."""
+def ce_rows(H, W, labels, n_valid, ignore_index=-100, want_soft=False, want_grad=True):
+    """Per-row loss terms and dH rows for the given rows, with the global N_valid.
+
+    want_grad=False skips the dH rows (loss terms only); it changes no value.
+    """
     H = np.asarray(H, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64) if np.asarray(W).dtype != np.float64 else W
     labels = np.asarray(labels)
@@ -39,6 +42,8 @@ def ce_rows(H, W, labels, n_valid, ignore_index=-100, want_soft=False):
         idx = np.nonzero(valid)[0]
         terms[s + idx] = lse[idx] - Z[idx, lab[idx]]
         P[~valid] = 0.0
+        if not want_grad:
+            continue
         if want_soft:
             soft[s:s + 64] = (P @ W) / n_valid
         P[idx, lab[idx]] -= 1.0

@@ -1,0 +1,140 @@
+"""The layer-streamed stack step on the GPU: oracle parity and streamed == resident bitwise."""
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+from oracle import nf4, stack
+from gpu_util import BF16_TOL, dev_bf16, host, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+class Setup:
+    """Blobs (pinned host + device copies), adapters and grads for one synthetic stack."""
+
+    def __init__(self, sl, kind, L, M, D, Dkv, F, r, alpha, seed, with_oracle=True, torch_weights=False):
+        self.sl, self.kind, self.L, self.M, self.D, self.Dkv, self.F, self.r, self.alpha = \
+            sl, kind, L, M, D, Dkv, F, r, alpha
+        shapes = sl.proj_shapes(D, Dkv, F)
+        self.host_blobs, self.dev_blobs, self.A, self.B, self.ref_layers = [], [], [], [], []
+        if torch_weights:   # large stacks: weights drawn on the device from a seeded torch generator
+            gen = torch.Generator(device="cuda").manual_seed(seed)
+            rnd = lambda shape, std: (torch.randn(*shape, generator=gen, device="cuda") * std).to(torch.bfloat16)
+            for l in range(L):
+                Ws = [rnd((N, K), 0.02) for N, K in shapes]
+                blob = sl.build_layer_blob(kind, D, Dkv, F, Ws)
+                self._add_blob(blob)
+                for N, K in shapes:
+                    self.A.append(rnd((r, K), 0.02))
+                    self.B.append(rnd((N, r), 0.02))
+            self.h0 = torch.randn(M, D, generator=gen, device="cuda").to(torch.bfloat16).float()
+            self.dh = torch.randn(M, D, generator=gen, device="cuda").to(torch.bfloat16).float()
+        else:
+            c = si.stack_case(seed, L, M, D, Dkv, F, r)
+            for l in range(L):
+                lw = c["layers"][l]
+                Ws = [dev_bf16(lw[n]["W"]) for n in si.PROJ_NAMES]
+                blob = sl.build_layer_blob(kind, D, Dkv, F, Ws)
+                self._add_blob(blob)
+                ref = {}
+                for n in si.PROJ_NAMES:
+                    W = lw[n]["W"]
+                    if with_oracle:
+                        Wr = nf4.dequantize_bf16(*nf4.quantize(W), *W.shape) if kind == sl.SL_WEIGHT_NF4 \
+                            else W.astype(np.float64)
+                        ref[n] = dict(W=Wr, A=lw[n]["A"].astype(np.float64), B=lw[n]["B"].astype(np.float64))
+                    self.A.append(dev_bf16(lw[n]["A"]))
+                    self.B.append(dev_bf16(lw[n]["B"]))
+                self.ref_layers.append(ref)
+            self.h0_np, self.dh_np = c["h0"], c["dh_top"]
+            self.h0 = torch.from_numpy(c["h0"]).cuda()
+            self.dh = torch.from_numpy(c["dh_top"]).cuda()
+        self.stack = sl.Stack(kind, D, Dkv, F, self.host_blobs, self.dev_blobs)
+        self.ws = torch.empty(self.stack.workspace_size(M, r), dtype=torch.uint8, device="cuda")
+
+    def _add_blob(self, blob):
+        h = torch.empty(blob.numel(), dtype=torch.uint8, pin_memory=True)
+        h.copy_(blob)
+        self.host_blobs.append(h)
+        self.dev_blobs.append(blob)
+
+    def run(self, mode):
+        sl = self.sl
+        hL = torch.empty(self.M, self.D, device="cuda")
+        dh0 = torch.empty_like(hL)
+        dA = [torch.full_like(a, float("nan"), dtype=torch.float32) for a in self.A]
+        dB = [torch.full_like(b, float("nan"), dtype=torch.float32) for b in self.B]
+        self.stack.step(mode, self.h0, self.dh, self.A, self.B, self.r, self.alpha, hL, dh0, dA, dB, self.ws)
+        sl.sl_check_device_errors()
+        return hL, dh0, dA, dB
+
+
+def same_bits(a, b):
+    return torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("kind_name", ["nf4", "bf16"])
+def test_small_stack_matches_oracle_and_resident(gpu_lib, kind_name):
+    sl = gpu_lib
+    kind = sl.SL_WEIGHT_NF4 if kind_name == "nf4" else sl.SL_WEIGHT_BF16
+    S = Setup(sl, kind, L=3, M=96, D=256, Dkv=128, F=512, r=16, alpha=32.0, seed=21)
+    hL, dh0, dA, dB = S.run(sl.SL_MODE_STREAMED)
+    h2d, kernels = S.stack.last_step_stats()
+    assert h2d == (2 * S.L - 2) * S.stack.host_bytes // S.L and kernels > 0
+    ohL, odh0, ograds = stack.stack_step(S.h0_np, S.dh_np, S.ref_layers, 32.0, rnd=True)
+    assert rel_fro(host(hL), ohL) <= BF16_TOL
+    assert rel_fro(host(dh0), odh0) <= BF16_TOL
+    for l in range(S.L):
+        for p, n in enumerate(si.PROJ_NAMES):
+            assert rel_fro(host(dA[7 * l + p]), ograds[l][n][0]) <= BF16_TOL, (l, n)
+            assert rel_fro(host(dB[7 * l + p]), ograds[l][n][1]) <= BF16_TOL, (l, n)
+    # the streamed run equals the resident run bit for bit, and re-runs are identical
+    r_ = S.run(sl.SL_MODE_RESIDENT)
+    s2 = S.run(sl.SL_MODE_STREAMED)
+    h2d2, _ = S.stack.last_step_stats()
+    assert h2d2 == (2 * S.L - 4) * S.stack.host_bytes // S.L     # layers 0 and 1 still resident
+    for x, y, z in zip((hL, dh0, *dA, *dB), (r_[0], r_[1], *r_[2], *r_[3]), (s2[0], s2[1], *s2[2], *s2[3])):
+        assert same_bits(x, y) and same_bits(x, z)
+    S.stack.close()
+
+
+def test_two_full_width_layers_match_oracle(gpu_lib):
+    """Llama-3.1-8B layer widths (bf16 base so the oracle needs no 218M-element quantisation), M=64."""
+    sl = gpu_lib
+    S = Setup(sl, sl.SL_WEIGHT_BF16, L=2, M=64, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0, seed=5)
+    hL, dh0, dA, dB = S.run(sl.SL_MODE_STREAMED)
+    ohL, odh0, ograds = stack.stack_step(S.h0_np, S.dh_np, S.ref_layers, 32.0, rnd=True)
+    errs = {"hL": rel_fro(host(hL), ohL), "dh0": rel_fro(host(dh0), odh0)}
+    for l in range(2):
+        for p, n in enumerate(si.PROJ_NAMES):
+            errs[f"dA{l}{n}"] = rel_fro(host(dA[7 * l + p]), ograds[l][n][0])
+            errs[f"dB{l}{n}"] = rel_fro(host(dB[7 * l + p]), ograds[l][n][1])
+    print({k: round(float(v), 5) for k, v in errs.items()})
+    assert max(errs.values()) <= BF16_TOL, errs
+    S.stack.close()
+
+
+@pytest.mark.parametrize("kind_name,L", [("nf4", 6), ("bf16", 4)])
+def test_full_width_streamed_equals_resident_bitwise(gpu_lib, kind_name, L):
+    """8B-shaped layers (bf16 layers are 416 MiB, above the ~165 MiB size of the pages' NF4 bug)."""
+    sl = gpu_lib
+    kind = sl.SL_WEIGHT_NF4 if kind_name == "nf4" else sl.SL_WEIGHT_BF16
+    S = Setup(sl, kind, L=L, M=160, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0, seed=77,
+              with_oracle=False, torch_weights=True)
+    a = S.run(sl.SL_MODE_STREAMED)
+    b = S.run(sl.SL_MODE_RESIDENT)
+    for x, y in zip((a[0], a[1], *a[2], *a[3]), (b[0], b[1], *b[2], *b[3])):
+        assert same_bits(x, y)
+    for g in a[2] + a[3]:            # every adapter received a finite, non-zero gradient
+        assert torch.isfinite(g).all() and g.abs().sum() > 0
+    S.stack.close()
+
+
+def test_pageable_host_memory_rejected(gpu_lib):
+    sl = gpu_lib
+    offs, total = sl.sl_stack_blob_layout(sl.SL_WEIGHT_BF16, 256, 128, 512)
+    pageable = torch.zeros(total, dtype=torch.uint8)
+    with pytest.raises(sl.SLError) as e:
+        sl.Stack(sl.SL_WEIGHT_BF16, 256, 128, 512, [pageable])
+    assert e.value.status == sl.SL_ERR_INVALID
