@@ -143,8 +143,8 @@ sl_status sl_nf4_dequantize(const uint8_t* codes, const float* absmax, int64_t N
  * the backward; the side product s T B^T is folded into the same
  * accumulator with fp32 accuracy); may be NULL only when r == 0.  r == 0 (or
  * A == B == NULL) computes the base alone -- the adapters-off pass.
- * r <= 32, r % 8 == 0.
- * `ws` is unused (pass NULL / 0); kept for ABI symmetry. */
+ * r <= 32, r % 8 == 0.  `ws` must hold sl_lora_linear_workspace_size(M, N,
+ * K, r) bytes (256-byte aligned; may be NULL when r == 0). */
 sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M,
                              const void* A, const void* B, int32_t r, float alpha,
                              void* Y, void* T_save, void* ws, size_t ws_bytes,
@@ -163,6 +163,8 @@ sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const void* dY, 
                              int32_t accumulate, void* ws, size_t ws_bytes,
                              cudaStream_t stream);
 
+/* Scratch bytes of one linear call (the forward and the backward of the same
+ * shape can share one buffer); 0 when r == 0. */
 size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r);
 
 /* ------------------------------------------------- streamed stack (a2-a7) */

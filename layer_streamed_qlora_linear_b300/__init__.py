@@ -176,10 +176,11 @@ class Weight:
 
 
 # ------------------------------------------------------------- LoRA linear
-def sl_lora_linear_fwd(weight: Weight, X, A, B, r, alpha, Y, T_save, stream=None):
+def sl_lora_linear_fwd(weight: Weight, X, A, B, r, alpha, Y, T_save, ws=None, stream=None):
     M = X.shape[0]
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(lib().sl_lora_linear_fwd(ctypes.byref(weight.desc), _ptr(X), M, _ptr(A), _ptr(B), int(r),
-                                    float(alpha), _ptr(Y), _ptr(T_save), None, 0, _stream(stream)))
+                                    float(alpha), _ptr(Y), _ptr(T_save), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def sl_lora_linear_workspace_size(M, N, K, r) -> int:

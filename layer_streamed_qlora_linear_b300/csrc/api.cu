@@ -1,5 +1,6 @@
 // Library-wide entry points: error reporting, version, the NF4 table export,
 // the per-device error word and the bounded-wait probe.
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <cstring>
@@ -22,11 +23,16 @@ sl_status cuda_error(cudaError_t e, const char* what) {
   return e == cudaErrorMemoryAllocation ? SL_ERR_OOM : SL_ERR_CUDA;
 }
 
+static std::atomic<uint64_t> g_launches{0};
+
 sl_status check_launch(const char* what) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, what);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   return SL_OK;
 }
+
+uint64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 static std::mutex g_word_mu;
 static int* g_words[64] = {nullptr};

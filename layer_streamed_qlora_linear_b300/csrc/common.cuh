@@ -27,8 +27,9 @@ sl_status cuda_error(cudaError_t e, const char* what);
     if (!(cond)) return ::sl::set_error(SL_ERR_INVALID, std::string(msg));     \
   } while (0)
 
-// After a launch: map a launch error to SL_ERR_CUDA.
+// After a launch: map a launch error to SL_ERR_CUDA; counts successful launches.
 sl_status check_launch(const char* what);
+uint64_t launch_count();  // libsl kernel launches so far (all threads)
 
 // ------------------------------------------------------ device error word
 // One int per device, allocated on first use, read and cleared by

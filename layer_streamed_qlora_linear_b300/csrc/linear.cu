@@ -14,113 +14,200 @@
 
 namespace sl {
 
-// out[m, i] = sum_k X[m, k] * W(i, k)  (fp32),  W(i, k) = Wp[i * w_si + k * w_sk]
-// 8 warps x 2 rows per block; W staged 256 columns at a time.
-template <int R>
-__global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t* __restrict__ X, int64_t M, int K,
-                                                        const uint16_t* __restrict__ Wp, int64_t w_si,
-                                                        int64_t w_sk, int r, float* __restrict__ out) {
-  __shared__ __align__(16) uint16_t wsm[R][256 + 8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * 16 + warp * 2;
-  float acc[2][R];
+// ---------------------------------------------------------------- cp.async
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// -------------------------------------------------------------- K2 / K4
+// part[split][m][i] = sum_{k in split} X[m, k] * W(i, k), fp32.
+// W(i, k) = Wp[i * K + k] (kWT == 0: A [r, K]) or Wp[k * r + i] (kWT == 1: B [N, r]).
+// Block: 128 threads, 32 rows x 512 columns of X staged in shared memory by
+// cp.async (all loads in flight at once); thread = (row, quarter of the rank).
+constexpr int kDnRows = 32;
+constexpr int kDnCols = 512;
+constexpr int kDnPad = 8;
+
+template <int R, int kWT>
+__global__ void __launch_bounds__(128) lora_down_kernel(const uint16_t* __restrict__ X, int64_t M, int K,
+                                                        const uint16_t* __restrict__ Wp, int r,
+                                                        float* __restrict__ part) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(dsm);                            // [32][512 + 8]
+  uint16_t* ws = xs + kDnRows * (kDnCols + kDnPad);                           // [R][512 + 8] or [512][R]
+  const int tid = threadIdx.x;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kDnRows;
+  const int k0 = blockIdx.y * kDnCols;
+  const int kn = (K - k0 < kDnCols) ? (K - k0) : kDnCols;  // multiple of 8
+  // X tile: 32 rows x 64 chunks of 16 bytes
+  for (int c = tid; c < kDnRows * (kDnCols / 8); c += 128) {
+    const int row = c / (kDnCols / 8), ch = c % (kDnCols / 8);
+    const bool ok = (m0 + row < M) && (ch * 8 < kn);
+    const uint16_t* src = ok ? X + (m0 + row) * K + k0 + ch * 8 : X;
+    cp_async16(xs + row * (kDnCols + kDnPad) + ch * 8, src, ok);
+  }
+  if (kWT == 0) {
+    for (int c = tid; c < R * (kDnCols / 8); c += 128) {
+      const int i = c / (kDnCols / 8), ch = c % (kDnCols / 8);
+      const bool ok = (i < r) && (ch * 8 < kn);
+      const uint16_t* src = ok ? Wp + static_cast<int64_t>(i) * K + k0 + ch * 8 : Wp;
+      cp_async16(ws + i * (kDnCols + kDnPad) + ch * 8, src, ok);
+    }
+  } else {
+    // contiguous [kn, r] slice of B; smem layout [k][R]
+    for (int c = tid; c < kDnCols * R / 8; c += 128) {
+      const int kk = (c * 8) / R, i0 = (c * 8) % R;
+      const bool ok = (kk < kn) && (i0 < r);
+      const uint16_t* src = ok ? Wp + static_cast<int64_t>(k0 + kk) * r + i0 : Wp;
+      cp_async16(ws + kk * R + i0, src, ok);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+
+  constexpr int RQ = R / 4;
+  const int row = tid >> 2, g = tid & 3;
+  float acc[RQ];
 #pragma unroll
-  for (int a = 0; a < 2; ++a)
+  for (int j = 0; j < RQ; ++j) acc[j] = 0.0f;
+  const uint16_t* xr = xs + row * (kDnCols + kDnPad);
+  for (int k = 0; k < kn; k += 8) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(xr + k);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    float x[8];
 #pragma unroll
-    for (int i = 0; i < R; ++i) acc[a][i] = 0.0f;
-  for (int k0 = 0; k0 < K; k0 += 256) {
-    __syncthreads();
-    if (w_sk == 1) {
-      for (int idx = threadIdx.x; idx < R * 256; idx += 256) {
-        const int i = idx >> 8, kk = idx & 255;
-        wsm[i][kk] = (i < r && k0 + kk < K) ? Wp[i * w_si + (k0 + kk)] : 0;
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = bf16_lo(xw[e]);
+      x[2 * e + 1] = bf16_hi(xw[e]);
+    }
+    if (kWT == 0) {
+#pragma unroll
+      for (int j = 0; j < RQ; ++j) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(ws + (g * RQ + j) * (kDnCols + kDnPad) + k);
+        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          acc[j] = fmaf(x[2 * e + 1], bf16_hi(w[e]), fmaf(x[2 * e], bf16_lo(w[e]), acc[j]));
       }
     } else {
-      for (int idx = threadIdx.x; idx < R * 256; idx += 256) {
-        const int kk = idx / R, i = idx % R;
-        wsm[i][kk] = (i < r && k0 + kk < K) ? Wp[i * w_si + static_cast<int64_t>(k0 + kk) * w_sk] : 0;
-      }
-    }
-    __syncthreads();
-    const int kk = lane * 8;
-    if (k0 + kk < K) {
-      float xv[2][8];
 #pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int64_t row = row0 + a;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < M) v = *reinterpret_cast<const uint4*>(X + row * K + k0 + kk);
-        const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+      for (int e = 0; e < 8; ++e) {
+        const uint16_t* wk = ws + (k + e) * R + g * RQ;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          xv[a][2 * e] = bf16_lo(p[e]);
-          xv[a][2 * e + 1] = bf16_hi(p[e]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < R; ++i) {
-        const uint4 wv = *reinterpret_cast<const uint4*>(&wsm[i][kk]);
-        const uint32_t p[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float w0 = bf16_lo(p[e]), w1 = bf16_hi(p[e]);
-#pragma unroll
-          for (int a = 0; a < 2; ++a) acc[a][i] = fmaf(xv[a][2 * e + 1], w1, fmaf(xv[a][2 * e], w0, acc[a][i]));
+        for (int j = 0; j < RQ; j += 2) {
+          const uint32_t w2 = *reinterpret_cast<const uint32_t*>(wk + j);
+          acc[j] = fmaf(x[e], bf16_lo(w2), acc[j]);
+          acc[j + 1] = fmaf(x[e], bf16_hi(w2), acc[j + 1]);
         }
       }
     }
   }
+  const int64_t gm = m0 + row;
+  if (gm < M) {
+    float* dst = part + (static_cast<int64_t>(blockIdx.y) * M + gm) * r;
 #pragma unroll
-  for (int a = 0; a < 2; ++a) {
-    const int64_t row = row0 + a;
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      float v = acc[a][i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0 && row < M && i < r) out[row * r + i] = v;
+    for (int j = 0; j < RQ; ++j) {
+      const int i = g * RQ + j;
+      if (i < r) dst[i] = acc[j];
     }
   }
 }
 
-// part[split][i][k] = sum_{m in split} P[m, i] * Q[m, k]   (fixed m order)
+// out[m][i] = sum over splits (fixed order) of part[split][m][i]
+__global__ void sum_splits_kernel(const float* __restrict__ part, int splits, int64_t n, float* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n; idx += stride) {
+    float v = 0.0f;
+    for (int sp = 0; sp < splits; ++sp) v += part[static_cast<int64_t>(sp) * n + idx];
+    out[idx] = v;
+  }
+}
+
+// ------------------------------------------------------------------- K6
+// part[split][i][k] = sum_{m in split} P[m, i] * Q[m, k]  (fixed m order)
+// Block: 256 threads = 256 columns of Q; rows of the split in tiles of 64,
+// double-buffered through shared memory by cp.async; thread = one column,
+// all R rank entries.
+constexpr int kGrRows = 64;
+constexpr int kGrCols = 256;
+constexpr int kGrPad = 8;
+
 template <int R>
-__global__ void __launch_bounds__(256) lora_grad_partial_kernel(const float* __restrict__ P,
-                                                                const uint16_t* __restrict__ Q, int64_t M, int Kq,
-                                                                int r, int64_t m_per_split,
-                                                                float* __restrict__ part) {
-  constexpr int RG = R / 4;
-  __shared__ float psm[64][R + 1];
-  const int c = threadIdx.x & 63, g = threadIdx.x >> 6;
-  const int col = blockIdx.x * 64 + c;
-  const int split = blockIdx.y;
-  const int64_t mb = split * m_per_split;
-  const int64_t me = (mb + m_per_split < M) ? mb + m_per_split : M;
-  float acc[RG];
+__global__ void __launch_bounds__(256) lora_grad_kernel(const float* __restrict__ P, const uint16_t* __restrict__ Q,
+                                                        int64_t M, int Kq, int r, int64_t rows_per_split,
+                                                        float* __restrict__ part) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  constexpr int kQTile = kGrRows * (kGrCols + kGrPad);  // bf16 elements per stage
+  uint16_t* qs = reinterpret_cast<uint16_t*>(dsm);                        // [2][64][256 + 8]
+  float* ps = reinterpret_cast<float*>(dsm + 2 * kQTile * 2);             // [2][64][R]
+  const int tid = threadIdx.x;
+  const int c0 = blockIdx.x * kGrCols;
+  const int64_t mb = blockIdx.y * rows_per_split;
+  const int64_t me = (mb + rows_per_split < M) ? mb + rows_per_split : M;
+  const int ntiles = static_cast<int>((me - mb + kGrRows - 1) / kGrRows);
+
+  auto issue = [&](int t, int buf) {
+    const int64_t r0 = mb + static_cast<int64_t>(t) * kGrRows;
+    uint16_t* qd = qs + buf * kQTile;
+    for (int c = tid; c < kGrRows * (kGrCols / 8); c += 256) {
+      const int row = c / (kGrCols / 8), ch = c % (kGrCols / 8);
+      const bool ok = (r0 + row < me) && (c0 + ch * 8 < Kq);
+      const uint16_t* src = ok ? Q + (r0 + row) * Kq + c0 + ch * 8 : Q;
+      cp_async16(qd + row * (kGrCols + kGrPad) + ch * 8, src, ok);
+    }
+    float* pd = ps + buf * kGrRows * R;
+    for (int c = tid; c < kGrRows * R / 4; c += 256) {
+      const int row = (c * 4) / R, i0 = (c * 4) % R;
+      const bool ok = (r0 + row < me) && (i0 < r);
+      const float* src = ok ? P + (r0 + row) * r + i0 : P;
+      cp_async16(pd + row * R + i0, src, ok);
+    }
+    cp_async_commit();
+  };
+
+  float acc[R];
 #pragma unroll
-  for (int j = 0; j < RG; ++j) acc[j] = 0.0f;
-  for (int64_t mc = mb; mc < me; mc += 64) {
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < 64 * R; idx += 256) {
-      const int mm = idx / R, i = idx % R;
-      psm[mm][i] = (mc + mm < me && i < r) ? P[(mc + mm) * r + i] : 0.0f;
+  for (int i = 0; i < R; ++i) acc[i] = 0.0f;
+  if (ntiles > 0) issue(0, 0);
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1;
+    if (t + 1 < ntiles) {
+      issue(t + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-    const int nrow = static_cast<int>((me - mc) < 64 ? (me - mc) : 64);
-    if (col < Kq) {
-      for (int mm = 0; mm < nrow; ++mm) {
-        const float q = bf16_to_f32(Q[(mc + mm) * Kq + col]);
+    const uint16_t* qd = qs + buf * kQTile + tid;
+    const float* pd = ps + buf * kGrRows * R;
+    const int nrow = static_cast<int>((me - (mb + static_cast<int64_t>(t) * kGrRows)) < kGrRows
+                                          ? (me - (mb + static_cast<int64_t>(t) * kGrRows))
+                                          : kGrRows);
+    for (int row = 0; row < nrow; ++row) {
+      const float q = bf16_to_f32(qd[row * (kGrCols + kGrPad)]);
 #pragma unroll
-        for (int j = 0; j < RG; ++j) acc[j] = fmaf(psm[mm][g * RG + j], q, acc[j]);
+      for (int i = 0; i < R; i += 4) {
+        const float4 p = *reinterpret_cast<const float4*>(pd + row * R + i);
+        acc[i] = fmaf(p.x, q, acc[i]);
+        acc[i + 1] = fmaf(p.y, q, acc[i + 1]);
+        acc[i + 2] = fmaf(p.z, q, acc[i + 2]);
+        acc[i + 3] = fmaf(p.w, q, acc[i + 3]);
       }
     }
+    __syncthreads();
   }
+  const int col = c0 + tid;
   if (col < Kq) {
 #pragma unroll
-    for (int j = 0; j < RG; ++j) {
-      const int i = g * RG + j;
-      if (i < r) part[(static_cast<int64_t>(split) * r + i) * Kq + col] = acc[j];
-    }
+    for (int i = 0; i < R; ++i)
+      if (i < r) part[(static_cast<int64_t>(blockIdx.y) * r + i) * Kq + col] = acc[i];
   }
 }
 
@@ -140,33 +227,88 @@ __global__ void lora_grad_reduce_kernel(const float* __restrict__ part, int spli
   }
 }
 
-int grad_splits(int64_t M) {
-  int64_t s = ceil_div(M, 256);
-  return static_cast<int>(s < 1 ? 1 : (s > 16 ? 16 : s));
+static int rank_bucket(int r) { return r <= 8 ? 8 : (r <= 16 ? 16 : 32); }
+
+int down_splits(int64_t K) { return static_cast<int>(ceil_div(K, kDnCols)); }
+
+// Splits of the M reduction for dA/dB: enough blocks to cover the SMs twice.
+int grad_splits(int64_t M, int64_t Kq) {
+  const int64_t slabs = ceil_div(Kq, kGrCols);
+  int64_t s = ceil_div(2 * 148, slabs);
+  const int64_t cap = ceil_div(M, kGrRows);
+  if (s > cap) s = cap;
+  return static_cast<int>(s < 1 ? 1 : s);
 }
 
-sl_status lora_down(const uint16_t* X, int64_t M, int K, const uint16_t* W, int64_t w_si, int64_t w_sk, int r,
-                    float* out, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>(ceil_div(M, 16));
-#define SL_DOWN(RR) lora_down_kernel<RR><<<grid, 256, 0, stream>>>(X, M, K, W, w_si, w_sk, r, out)
-  if (r <= 8) SL_DOWN(8);
-  else if (r <= 16) SL_DOWN(16);
-  else SL_DOWN(32);
+static size_t down_smem(int R) {
+  return (static_cast<size_t>(kDnRows) * (kDnCols + kDnPad) + static_cast<size_t>(R) * (kDnCols + kDnPad)) * 2;
+}
+static size_t grad_smem(int R) {
+  return 2 * static_cast<size_t>(kGrRows) * (kGrCols + kGrPad) * 2 + 2 * static_cast<size_t>(kGrRows) * R * 4;
+}
+
+template <typename Kern>
+static sl_status set_smem(Kern k, size_t bytes) {
+  static bool done[64] = {false};
+  (void)done;
+  SL_CHECK_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)));
+  return SL_OK;
+}
+
+// out [M, r] fp32 = X [M, K] * W^T; W given as A [r, K] (wt = 0) or B [K, r] (wt = 1).
+// part: scratch of down_splits(K) * M * r floats (unused when one split).
+sl_status lora_down(const uint16_t* X, int64_t M, int K, const uint16_t* W, int wt, int r, float* out, float* part,
+                    cudaStream_t stream) {
+  const int splits = down_splits(K);
+  float* dst = splits == 1 ? out : part;
+  dim3 grid(static_cast<unsigned>(ceil_div(M, kDnRows)), static_cast<unsigned>(splits));
+  const int R = rank_bucket(r);
+  const size_t sm = down_smem(R);
+#define SL_DOWN(RR, WT)                                                                           \
+  do {                                                                                            \
+    static bool attr = false;                                                                     \
+    if (!attr) {                                                                                  \
+      sl_status st_ = set_smem(lora_down_kernel<RR, WT>, sm);                                     \
+      if (st_ != SL_OK) return st_;                                                               \
+      attr = true;                                                                                \
+    }                                                                                             \
+    lora_down_kernel<RR, WT><<<grid, 128, sm, stream>>>(X, M, K, W, r, dst);                      \
+  } while (0)
+  if (R == 8) { if (wt) SL_DOWN(8, 1); else SL_DOWN(8, 0); }
+  else if (R == 16) { if (wt) SL_DOWN(16, 1); else SL_DOWN(16, 0); }
+  else { if (wt) SL_DOWN(32, 1); else SL_DOWN(32, 0); }
 #undef SL_DOWN
-  return check_launch("lora_down_kernel");
+  sl_status st = check_launch("lora_down_kernel");
+  if (st != SL_OK || splits == 1) return st;
+  const int64_t n = M * r;
+  int g = static_cast<int>(ceil_div(n, 256));
+  if (g > num_sms() * 4) g = num_sms() * 4;
+  sum_splits_kernel<<<g, 256, 0, stream>>>(part, splits, n, out);
+  return check_launch("sum_splits_kernel");
 }
 
 sl_status lora_grad(const float* P, const uint16_t* Q, int64_t M, int Kq, int r, float s, float* out,
                     int transpose, int accumulate, float* part, cudaStream_t stream) {
-  const int splits = grad_splits(M);
-  const int64_t mps = ceil_div(ceil_div(M, splits), 64) * 64;
-  dim3 grid(static_cast<unsigned>(ceil_div(Kq, 64)), static_cast<unsigned>(splits));
-#define SL_GRAD(RR) lora_grad_partial_kernel<RR><<<grid, 256, 0, stream>>>(P, Q, M, Kq, r, mps, part)
-  if (r <= 8) SL_GRAD(8);
-  else if (r <= 16) SL_GRAD(16);
+  const int splits = grad_splits(M, Kq);
+  const int64_t rps = ceil_div(ceil_div(M, splits), kGrRows) * kGrRows;
+  dim3 grid(static_cast<unsigned>(ceil_div(Kq, kGrCols)), static_cast<unsigned>(splits));
+  const int R = rank_bucket(r);
+  const size_t sm = grad_smem(R);
+#define SL_GRAD(RR)                                                                    \
+  do {                                                                                 \
+    static bool attr = false;                                                          \
+    if (!attr) {                                                                       \
+      sl_status st_ = set_smem(lora_grad_kernel<RR>, sm);                              \
+      if (st_ != SL_OK) return st_;                                                    \
+      attr = true;                                                                     \
+    }                                                                                  \
+    lora_grad_kernel<RR><<<grid, 256, sm, stream>>>(P, Q, M, Kq, r, rps, part);        \
+  } while (0)
+  if (R == 8) SL_GRAD(8);
+  else if (R == 16) SL_GRAD(16);
   else SL_GRAD(32);
 #undef SL_GRAD
-  sl_status st = check_launch("lora_grad_partial_kernel");
+  sl_status st = check_launch("lora_grad_kernel");
   if (st != SL_OK) return st;
   const int64_t total = static_cast<int64_t>(r) * Kq;
   int grid2 = static_cast<int>(ceil_div(total, 256));
@@ -175,12 +317,31 @@ sl_status lora_grad(const float* P, const uint16_t* Q, int64_t M, int Kq, int r,
   return check_launch("lora_grad_reduce_kernel");
 }
 
-size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
-  if (r <= 0) return 0;
-  const int splits = grad_splits(M);
-  return align_up(static_cast<size_t>(M) * r * 4, 256) + align_up(static_cast<size_t>(splits) * r * K * 4, 256) +
-         align_up(static_cast<size_t>(splits) * r * N * 4, 256);
+// Workspace of one linear (forward and backward share it):
+//   U [M, r] fp32 | rank-r partials (down_splits x M x r) | dA partials | dB partials
+struct LinWs {
+  size_t U, dpart, partA, partB, total;
+};
+
+static LinWs lin_ws(int64_t M, int64_t N, int64_t K, int r) {
+  LinWs w{};
+  if (r <= 0) return w;
+  size_t off = 0;
+  auto take = [&](size_t b) {
+    const size_t o = off;
+    off = align_up(off + b, 256);
+    return o;
+  };
+  const int ds = down_splits(K) > down_splits(N) ? down_splits(K) : down_splits(N);
+  w.U = take(static_cast<size_t>(M) * r * 4);
+  w.dpart = take(static_cast<size_t>(ds) * M * r * 4);
+  w.partA = take(static_cast<size_t>(grad_splits(M, K)) * r * K * 4);
+  w.partB = take(static_cast<size_t>(grad_splits(M, N)) * r * N * 4);
+  w.total = off;
+  return w;
 }
+
+size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return lin_ws(M, N, K, r).total; }
 
 static sl_status check_weight(const sl_weight* w) {
   SL_REQUIRE(w, "null sl_weight");
@@ -199,18 +360,22 @@ static sl_status check_weight(const sl_weight* w) {
 }
 
 sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
-                     float alpha, void* Y, void* T_save, cudaStream_t stream) {
+                     float alpha, void* Y, void* T_save, void* ws, size_t ws_bytes, cudaStream_t stream) {
   sl_status st = check_weight(w);
   if (st != SL_OK) return st;
   SL_REQUIRE(X && Y && M > 0, "sl_lora_linear_fwd: null X/Y or M <= 0");
   const bool lora = r > 0 && A && B;
   SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32 && T_save), "sl_lora_linear_fwd: need r % 8 == 0, r <= 32, T_save");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_fwd: M too large");
+  const LinWs L = lin_ws(M, w->N, w->K, lora ? r : 0);
+  SL_REQUIRE(!lora || (ws && ws_bytes >= L.total), "sl_lora_linear_fwd: workspace too small");
+  SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_lora_linear_fwd: workspace must be 256-byte aligned");
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   if (lora) {
-    st = lora_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A),
-                   w->K, 1, r, static_cast<float*>(T_save), stream);
+    st = lora_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A), 0, r,
+                   static_cast<float*>(T_save), reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.dpart),
+                   stream);
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
@@ -246,7 +411,8 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32), "sl_lora_linear_bwd: need r % 8 == 0 and r <= 32");
   SL_REQUIRE(!lora || (X && T_save && dA && dB), "sl_lora_linear_bwd: LoRA backward needs X, T_save, dA, dB");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_bwd: M too large");
-  const size_t need = lora ? linear_bwd_ws_bytes(M, w->N, w->K, r) : 0;
+  const LinWs L = lin_ws(M, w->N, w->K, lora ? r : 0);
+  const size_t need = L.total;
   SL_REQUIRE(ws_bytes >= need && (need == 0 || ws), "sl_lora_linear_bwd: workspace too small");
   SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_lora_linear_bwd: workspace must be 256-byte aligned");
   int* err = device_error_word();
@@ -256,15 +422,12 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   float* partA = nullptr;
   float* partB = nullptr;
   if (lora) {
-    const int splits = grad_splits(M);
-    U = reinterpret_cast<float*>(p);
-    p += align_up(static_cast<size_t>(M) * r * 4, 256);
-    partA = reinterpret_cast<float*>(p);
-    p += align_up(static_cast<size_t>(splits) * r * w->K * 4, 256);
-    partB = reinterpret_cast<float*>(p);
+    U = reinterpret_cast<float*>(p + L.U);
+    partA = reinterpret_cast<float*>(p + L.partA);
+    partB = reinterpret_cast<float*>(p + L.partB);
     // U = dY B : W(i, n) = B[n * r + i]
     st = lora_down(static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), static_cast<const uint16_t*>(B), 1,
-                   r, r, U, stream);
+                   r, U, reinterpret_cast<float*>(p + L.dpart), stream);
     if (st != SL_OK) return st;
   }
   if (dX) {
@@ -311,9 +474,7 @@ using namespace sl;
 extern "C" sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B,
                                         int32_t r, float alpha, void* Y, void* T_save, void* ws, size_t ws_bytes,
                                         cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
-  return linear_fwd(w, X, M, A, B, r, alpha, Y, T_save, stream);
+  return linear_fwd(w, X, M, A, B, r, alpha, Y, T_save, ws, ws_bytes, stream);
 }
 
 extern "C" sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A,
@@ -324,5 +485,5 @@ extern "C" sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const
 }
 
 extern "C" size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r) {
-  return linear_bwd_ws_bytes(M, N, K, r);
+  return linear_ws_bytes(M, N, K, r);
 }

@@ -7,11 +7,10 @@
 namespace sl {
 
 sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
-                     float alpha, void* Y, void* T_save, cudaStream_t stream);
+                     float alpha, void* Y, void* T_save, void* ws, size_t ws_bytes, cudaStream_t stream);
 sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A, const void* B,
                      int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
                      void* ws, size_t ws_bytes, cudaStream_t stream);
-size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
-int grad_splits(int64_t M);
+size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
 
 }  // namespace sl

@@ -145,7 +145,7 @@ Plan make_plan(const sl_stack* s, int64_t M, int r) {
   proj_shapes(s->D, s->Dkv, s->F, pr);
   size_t lw = 0;
   for (int p = 0; p < 7; ++p) {
-    const size_t b = linear_bwd_ws_bytes(M, pr[p].N, pr[p].K, rr);
+    const size_t b = linear_ws_bytes(M, pr[p].N, pr[p].K, rr);
     if (b > lw) lw = b;
   }
   P.lin_ws_bytes = lw;
@@ -221,20 +221,18 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
   float* h1 = c.at<float>(P.h1[l]);
   uint16_t* o = c.at<uint16_t>(P.o);
   uint16_t* d = c.at<uint16_t>(P.d);
-  const uint64_t lin = r > 0 ? 2 : 1;
   SL_TRY(glue_rms_fwd(h_in, nullptr, nullptr, x1, c.at<float>(P.rstd1[l]), M, D, c.stream));
-  SL_TRY(linear_fwd(&w[0], x1, M, A(0), B(0), r, c.alpha, q, T(0), c.stream));
-  SL_TRY(linear_fwd(&w[1], x1, M, A(1), B(1), r, c.alpha, k, T(1), c.stream));
-  SL_TRY(linear_fwd(&w[2], x1, M, A(2), B(2), r, c.alpha, v, T(2), c.stream));
+  SL_TRY(linear_fwd(&w[0], x1, M, A(0), B(0), r, c.alpha, q, T(0), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
+  SL_TRY(linear_fwd(&w[1], x1, M, A(1), B(1), r, c.alpha, k, T(1), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
+  SL_TRY(linear_fwd(&w[2], x1, M, A(2), B(2), r, c.alpha, v, T(2), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
   SL_TRY(glue_mix_fwd(q, k, v, a, M, D, Dkv, c.stream));
-  SL_TRY(linear_fwd(&w[3], a, M, A(3), B(3), r, c.alpha, o, T(3), c.stream));
+  SL_TRY(linear_fwd(&w[3], a, M, A(3), B(3), r, c.alpha, o, T(3), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
   SL_TRY(glue_rms_fwd(h_in, o, h1, x2, c.at<float>(P.rstd2[l]), M, D, c.stream));
-  SL_TRY(linear_fwd(&w[4], x2, M, A(4), B(4), r, c.alpha, g, T(4), c.stream));
-  SL_TRY(linear_fwd(&w[5], x2, M, A(5), B(5), r, c.alpha, u, T(5), c.stream));
+  SL_TRY(linear_fwd(&w[4], x2, M, A(4), B(4), r, c.alpha, g, T(4), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
+  SL_TRY(linear_fwd(&w[5], x2, M, A(5), B(5), r, c.alpha, u, T(5), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
   SL_TRY(glue_swiglu_fwd(g, u, m, M * s->F, c.stream));
-  SL_TRY(linear_fwd(&w[6], m, M, A(6), B(6), r, c.alpha, d, T(6), c.stream));
+  SL_TRY(linear_fwd(&w[6], m, M, A(6), B(6), r, c.alpha, d, T(6), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
   SL_TRY(glue_resid_add(h1, d, h_out, M * s->D, c.stream));
-  c.kernels += 5 + 7 * lin;
   return SL_OK;
 }
 
@@ -268,7 +266,6 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
   uint16_t* dx1q = c.at<uint16_t>(P.dx1q);
   uint16_t* dx1k = c.at<uint16_t>(P.dx1k);
   uint16_t* dx1v = c.at<uint16_t>(P.dx1v);
-  const uint64_t lin = r > 0 ? 6 : 1;
   SL_TRY(linear_bwd(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, T(6), dm, dA(6), dB(6), 0, lws,
                     lwb, c.stream));
   SL_TRY(glue_swiglu_bwd(dm, c.at<uint16_t>(P.g[l]), c.at<uint16_t>(P.u[l]), dg, du, M * s->F, c.stream));
@@ -286,7 +283,6 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
   SL_TRY(linear_bwd(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, T(1), dx1k, dA(1), dB(1), 0, lws, lwb, c.stream));
   SL_TRY(linear_bwd(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, T(2), dx1v, dA(2), dB(2), 0, lws, lwb, c.stream));
   SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, h_in, c.at<float>(P.rstd1[l]), dh, dh_bf16, M, D, c.stream));
-  c.kernels += 4 + 7 * lin;
   return SL_OK;
 }
 
@@ -410,6 +406,7 @@ extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float
   SL_REQUIRE(ws_bytes >= P.total, "sl_stream_stack_step: workspace too small (need " + std::to_string(P.total) +
                                       " bytes)");
   StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, stream};
+  const uint64_t launches0 = launch_count();
   const int L = s->L;
   const bool streamed = mode == SL_MODE_STREAMED;
   uint64_t h2d = 0;
@@ -437,7 +434,6 @@ extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float
   float* dhB = c.at<float>(P.dhB);
   uint16_t* dd = c.at<uint16_t>(P.dd);
   SL_TRY(glue_to_bf16(dh_top, dd, M * s->D, stream));
-  c.kernels += 1;
   const float* dh_cur = dh_top;
   for (int l = L - 1; l >= 0; --l) {
     if (streamed) {
@@ -454,7 +450,7 @@ extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float
     }
   }
   s->last_h2d = h2d;
-  s->last_kernels = c.kernels;
+  s->last_kernels = launch_count() - launches0;
   return SL_OK;
 }
 

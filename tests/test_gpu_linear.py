@@ -27,11 +27,11 @@ def make(sl, seed, M, N, K, r, kind):
 def run(sl, w, t, M, N, K, r, alpha, accumulate=False, dA0=None, dB0=None):
     Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     T = torch.empty(M, max(r, 1), dtype=torch.float32, device="cuda")
-    sl.sl_lora_linear_fwd(w, t["X"], t["A"], t["B"], r, alpha, Y, T)
+    ws = torch.empty(max(sl.sl_lora_linear_workspace_size(M, N, K, r), 1), dtype=torch.uint8, device="cuda")
+    sl.sl_lora_linear_fwd(w, t["X"], t["A"], t["B"], r, alpha, Y, T, ws)
     dX = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
     dA = dA0.clone() if dA0 is not None else torch.empty(r, K, dtype=torch.float32, device="cuda")
     dB = dB0.clone() if dB0 is not None else torch.empty(N, r, dtype=torch.float32, device="cuda")
-    ws = torch.empty(max(sl.sl_lora_linear_workspace_size(M, N, K, r), 1), dtype=torch.uint8, device="cuda")
     sl.sl_lora_linear_bwd(w, t["X"], t["dY"], t["A"], t["B"], r, alpha, T, dX, dA, dB, accumulate, ws)
     sl.sl_check_device_errors()
     return Y, T, dX, dA, dB
@@ -68,7 +68,8 @@ def test_zero_B_equals_base_and_rank_zero(gpu_lib):
     Y1 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     Y0 = torch.empty_like(Y1)
     T = torch.empty(M, r, dtype=torch.float32, device="cuda")
-    gpu_lib.sl_lora_linear_fwd(w, t["X"], t["A"], t["B"], r, 32.0, Y1, T)
+    ws = torch.empty(gpu_lib.sl_lora_linear_workspace_size(M, N, K, r), dtype=torch.uint8, device="cuda")
+    gpu_lib.sl_lora_linear_fwd(w, t["X"], t["A"], t["B"], r, 32.0, Y1, T, ws)
     gpu_lib.sl_lora_linear_fwd(w, t["X"], None, None, 0, 32.0, Y0, None)
     assert torch.equal(Y1.float(), Y0.float())
     assert rel_fro(host(Y0), c["X"].astype(np.float64) @ W_ref.T) <= BF16_TOL
