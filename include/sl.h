@@ -163,6 +163,26 @@ sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const void* dY, 
                              int32_t accumulate, void* ws, size_t ws_bytes,
                              cudaStream_t stream);
 
+/* The forward above for callers that cannot allocate device memory -- code
+ * running under a memory manager that owns all device memory (a framework's
+ * caching allocator with a hard budget, or an embedding application that
+ * forbids cudaMalloc because it synchronises the device and fragments its
+ * pool) and therefore cannot pass a workspace.  No counterpart on the pages:
+ * it exists for those callers only.  Same arguments and results as
+ * sl_lora_linear_fwd without `ws`; the call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).  Its scratch, the K-split partial
+ * sums of X A^T, lives in one fixed 4 MiB device array inside libsl that
+ * every device loading the library holds until exit; a call needing more
+ * than 4 MiB (ceil(K/512) * M * r * 4 bytes) returns SL_ERR_INVALID and
+ * enqueues nothing.  The first call on a device looks up that array's
+ * device address (cudaGetSymbolAddress) and should come before any stream
+ * capture.  All calls share the array and it keeps the last call's
+ * contents (nothing in it needs to start at zero); calls that overlap on
+ * the GPU, e.g. on two streams, race on it and must be serialised. */
+sl_status sl_lora_linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t M,
+                                     const void* A, const void* B, int32_t r, float alpha,
+                                     void* Y, void* T_save, cudaStream_t stream);
+
 /* Scratch bytes of one linear call (the forward and the backward of the same
  * shape can share one buffer); 0 when r == 0. */
 size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r);

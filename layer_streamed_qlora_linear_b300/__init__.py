@@ -58,6 +58,7 @@ _SIGS = {
     "sl_lora_linear_bwd": (_I32, [ctypes.POINTER(sl_weight), _P, _P, _I64, _P, _P, _I32, _F, _P, _P, _P, _P,
                                   _I32, _P, _SZ, _P]),
     "sl_lora_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
+    "sl_lora_linear_fwd_noalloc": (_I32, [ctypes.POINTER(sl_weight), _P, _I64, _P, _P, _I32, _F, _P, _P, _P]),
     "sl_stack_blob_layout": (_I32, [_I32, _I64, _I64, _I64, _P, _P]),
     "sl_stack_create": (_I32, [ctypes.POINTER(sl_stack_desc), _P, _P, _P]),
     "sl_stack_destroy": (_I32, [_P]),
@@ -181,6 +182,15 @@ def sl_lora_linear_fwd(weight: Weight, X, A, B, r, alpha, Y, T_save, ws=None, st
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(lib().sl_lora_linear_fwd(ctypes.byref(weight.desc), _ptr(X), M, _ptr(A), _ptr(B), int(r),
                                     float(alpha), _ptr(Y), _ptr(T_save), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def sl_lora_linear_fwd_noalloc(weight: Weight, X, A, B, r, alpha, Y, T_save, stream=None):
+    """The forward without a workspace argument: its scratch is a fixed 4 MiB device array in libsl.
+
+    For callers that cannot allocate device memory; calls overlapping on the GPU race on the array."""
+    M = X.shape[0]
+    _check(lib().sl_lora_linear_fwd_noalloc(ctypes.byref(weight.desc), _ptr(X), M, _ptr(A), _ptr(B), int(r),
+                                            float(alpha), _ptr(Y), _ptr(T_save), _stream(stream)))
 
 
 def sl_lora_linear_workspace_size(M, N, K, r) -> int:

@@ -8,6 +8,9 @@
 // The skinny kernels are HBM-bound streams over X / dY; the rank-r operand
 // is staged in shared memory and every reduction runs in a fixed order so
 // that results are bitwise reproducible.
+#include <mutex>
+#include <string>
+
 #include "common.cuh"
 #include "gemm.cuh"
 #include "linear.cuh"
@@ -467,6 +470,93 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   return SL_OK;
 }
 
+// ------------------------------------------------ allocation-free forward
+// Some callers cannot hand libsl a workspace: they run under a memory
+// manager that owns all device memory (a framework caching allocator with a
+// hard budget, an embedding application that forbids cudaMalloc because it
+// synchronises the device and fragments its pool).  For them the forward
+// keeps its only scratch -- the K-split partial sums of T = X A^T -- in this
+// file-scope device array, so the call allocates nothing.  Every device that
+// loads libsl holds the array until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array, looked up once per device (with that device
+// current): in host code the symbol is only a host-side stand-in.
+static sl_status noalloc_scratch_ptr(void** out) {
+  static std::mutex mu;
+  static void* ptrs[64] = {nullptr};
+  int dev = 0;
+  SL_CHECK_CUDA(cudaGetDevice(&dev));
+  SL_REQUIRE(dev >= 0 && dev < 64, "sl_lora_linear_fwd_noalloc: device index out of range");
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_error(e, "sl_lora_linear_fwd_noalloc: cudaGetSymbolAddress");
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return SL_OK;
+}
+
+// Bytes of scratch the forward needs: one fp32 [M, r] partial per 512-column
+// split of K (none when K fits one split).
+static size_t noalloc_need(int64_t M, int64_t K, int r) {
+  const int splits = down_splits(K);
+  return splits > 1 ? static_cast<size_t>(splits) * M * r * 4 : 0;
+}
+
+sl_status linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
+                             float alpha, void* Y, void* T_save, cudaStream_t stream) {
+  sl_status st = check_weight(w);
+  if (st != SL_OK) return st;
+  SL_REQUIRE(X && Y && M > 0, "sl_lora_linear_fwd_noalloc: null X/Y or M <= 0");
+  const bool lora = r > 0 && A && B;
+  SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32 && T_save),
+             "sl_lora_linear_fwd_noalloc: need r % 8 == 0, r <= 32, T_save");
+  SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_fwd_noalloc: M too large");
+  const size_t need = lora ? noalloc_need(M, w->K, r) : 0;
+  if (need > kNoAllocScratchBytes)
+    return set_error(SL_ERR_INVALID, "sl_lora_linear_fwd_noalloc: needs " + std::to_string(need) +
+                                         " bytes of scratch (ceil(K/512) * M * r * 4), above the fixed " +
+                                         std::to_string(kNoAllocScratchBytes) +
+                                         "-byte maximum; use sl_lora_linear_fwd with a workspace");
+  void* scratch = nullptr;
+  st = noalloc_scratch_ptr(&scratch);
+  if (st != SL_OK) return st;
+  int* err = device_error_word();
+  if (!err) return SL_ERR_CUDA;
+  if (lora) {
+    // Every partial element that the split sum reads is written first by
+    // this call, so the array needs no clearing between calls.
+    st = lora_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A), 0, r,
+                   static_cast<float*>(T_save), static_cast<float*>(scratch), stream);
+    if (st != SL_OK) return st;
+  }
+  GemmLaunch g{};
+  g.bsrc = (w->kind == SL_WEIGHT_NF4) ? kBSrcNF4 : kBSrcBF16;
+  g.bmn = 0;
+  g.epi = kEpiStoreBF16;
+  g.A = X;
+  g.lda = w->K;
+  g.w = w->w;
+  g.codes = w->codes;
+  g.absmax = w->absmax;
+  g.ldw = w->K;
+  g.args.M = static_cast<int>(M);
+  g.args.N = static_cast<int>(w->N);
+  g.args.K = static_cast<int>(w->K);
+  g.args.lora_x = lora ? static_cast<const float*>(T_save) : nullptr;
+  g.args.lora_w = lora ? static_cast<const uint16_t*>(B) : nullptr;
+  g.args.r = lora ? r : 0;
+  g.args.s = lora ? alpha / static_cast<float>(r) : 0.0f;
+  g.args.out = Y;
+  g.args.ld_out = w->N;
+  g.args.err = err;
+  return launch_gemm(g, stream);
+}
+
 }  // namespace sl
 
 using namespace sl;
@@ -486,4 +576,10 @@ extern "C" sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const
 
 extern "C" size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r) {
   return linear_ws_bytes(M, N, K, r);
+}
+
+extern "C" sl_status sl_lora_linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t M, const void* A,
+                                                const void* B, int32_t r, float alpha, void* Y, void* T_save,
+                                                cudaStream_t stream) {
+  return linear_fwd_noalloc(w, X, M, A, B, r, alpha, Y, T_save, stream);
 }
