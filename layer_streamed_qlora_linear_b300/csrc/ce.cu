@@ -33,7 +33,7 @@ CEPlan ce_plan(int64_t M, int64_t D, int64_t V, int64_t chunk_V) {
     off = align_up(off + b, 256);
     return o;
   };
-  p.ntiles = static_cast<int>(ceil_div(V, kBN));
+  p.ntiles = static_cast<int>(ceil_div(V, kBN)) * 2;   // two column halves per 256-wide tile
   p.part_max = take(static_cast<size_t>(M) * p.ntiles * 4);
   p.part_sum = take(static_cast<size_t>(M) * p.ntiles * 4);
   p.label_logit = take(M * 4);
@@ -45,7 +45,7 @@ CEPlan ce_plan(int64_t M, int64_t D, int64_t V, int64_t chunk_V) {
   return p;
 }
 
-// One warp per row: lse from the per-tile (max, sum exp) partials; the row's
+// One warp per row: lse from the per-half-tile (max, sum exp) partials; the row's
 // loss term lse - z_label (0 for ignored rows).  Out-of-range labels are
 // reported through the error word and treated as ignored.
 __global__ void ce_row_kernel(const float* __restrict__ pmax, const float* __restrict__ psum, int ntiles,

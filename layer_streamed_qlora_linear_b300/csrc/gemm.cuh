@@ -20,11 +20,12 @@
 //
 // Tile: 128 (M) x 256 (N) x 64 (K), fp32 accumulator in 256 TMEM columns,
 // one tcgen05.mma.cta_group::1.kind::f16 128x256x16 per 16 of K.
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM allocator + MMA issuer (one lane)
-//   warps 2..5  NF4 dequant during the main loop, LoRA staging, epilogue
-//               (warp w reads TMEM lanes 32*(w%4) .. +31).
+//   warps 2..9  NF4 dequant during the main loop (one 64-element row per
+//               thread per k-block), LoRA staging, epilogue (warp w reads
+//               TMEM lanes 32*(w%4) .. +31, columns of its half).
 // Pipeline: S stages, mbarriers tma_full / b_full / empty, one acc_full.
 // Every wait is bounded (two seconds); a wait that gives up records
 // SL_ERR_TIMEOUT in the device error word and the CTA winds down cleanly.
@@ -52,7 +53,8 @@ constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBTileBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kCodesBytes = kBN * kBK / 2;  // 8 KB (both layouts)
 constexpr int kAbsmaxBytes = kBN * 16;      // 4 KB (K-major box 4 x 256; MN-major uses 1 KB)
-constexpr int kGemmThreads = 192;
+constexpr int kNumDq = 256;                 // dequant / staging / epilogue threads (warps 2..9)
+constexpr int kGemmThreads = 64 + kNumDq;
 
 template <int BSRC>
 struct GemmCfg {
@@ -92,25 +94,59 @@ struct GemmArgs {
   int* err;                    // device error word
 };
 
-// One row segment: 16 packed code bytes (32 elements) with one absmax ->
-// four 16-byte chunks (logical chunk index chunk0 + j) of a 128-byte
-// swizzled smem row.  tab: 16 fp32 levels (per-half-warp copy).
-__device__ __forceinline__ void dequant_half_row(const uint4 q, float amax, const float* tab, uint8_t* row,
-                                                 int chunk0, int rsw) {
-  const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+// One row segment of 64 NF4 elements (32 packed code bytes, one absmax) ->
+// 64 bf16 = bf16(T[code] * absmax), written as eight 16-byte chunks of a
+// 128-byte-swizzled smem row (logical chunk j at physical j ^ rsw).
+//
+// The 16 products bf16(T[i] * absmax) are formed once per segment (fp32
+// multiply, one rounding) and split into byte planes L (low bytes) and H
+// (high bytes), four registers each.  A code then costs a few byte
+// permutes: prmt selects from entries 0-7 and 8-15 by the code's low 3 bits,
+// and a lop3 picks between the two by the code's bit 3 (a byte mask made by
+// prmt's sign-replicate mode from the packed codes themselves).  No shared
+// memory table, no per-element multiply.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t select_bytes(uint32_t lo8, uint32_t hi8, uint32_t mask) {
+  uint32_t d;  // (lo8 & ~mask) | (hi8 & mask)
+  asm("lop3.b32 %0, %1, %2, %3, 0xD8;" : "=r"(d) : "r"(lo8), "r"(hi8), "r"(mask));
+  return d;
+}
+
+__device__ __forceinline__ void nf4_row_bf16(const uint8_t* codes, float amax, uint8_t* row, int rsw) {
+  uint32_t P[8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t w = words[j];
+  for (int i = 0; i < 8; ++i)
+    P[i] = pack_bf16x2(__fmul_rn(__uint_as_float(d_nf4_level_bits[2 * i]), amax),
+                       __fmul_rn(__uint_as_float(d_nf4_level_bits[2 * i + 1]), amax));
+  const uint32_t L0 = prmt(P[0], P[1], 0x6420), H0 = prmt(P[0], P[1], 0x7531);
+  const uint32_t L1 = prmt(P[2], P[3], 0x6420), H1 = prmt(P[2], P[3], 0x7531);
+  const uint32_t L2 = prmt(P[4], P[5], 0x6420), H2 = prmt(P[4], P[5], 0x7531);
+  const uint32_t L3 = prmt(P[6], P[7], 0x6420), H3 = prmt(P[6], P[7], 0x7531);
+  const uint4 q0 = *reinterpret_cast<const uint4*>(codes);
+  const uint4 q1 = *reinterpret_cast<const uint4*>(codes + 16);
+  const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t w = words[j];         // byte i = (e_{2i} << 4) | e_{2i+1}
+    const uint32_t w4 = w << 4;          // bit 7 of byte i = bit 3 of e_{2i+1}
+    const uint32_t s7 = w & 0x77777777u; // code bits 0-2
+    const uint32_t sA = s7, sB = s7 >> 16;
+    // nibbles of sA: (e1, e0, e3, e2); of sB: (e5, e4, e7, e6)
+    const uint32_t mA = prmt(w4, w, 0xD9C8), mB = prmt(w4, w, 0xFBEA);  // 0xFF where bit 3 set
+    const uint32_t loA = select_bytes(prmt(L0, L1, sA), prmt(L2, L3, sA), mA);
+    const uint32_t hiA = select_bytes(prmt(H0, H1, sA), prmt(H2, H3, sA), mA);
+    const uint32_t loB = select_bytes(prmt(L0, L1, sB), prmt(L2, L3, sB), mB);
+    const uint32_t hiB = select_bytes(prmt(H0, H1, sB), prmt(H2, H3, sB), mB);
     uint4 o;
-    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t byte = (w >> (8 * b)) & 0xFFu;
-      const float v0 = __fmul_rn(tab[byte >> 4], amax);
-      const float v1 = __fmul_rn(tab[byte & 15u], amax);
-      op[b] = pack_bf16x2(v0, v1);
-    }
-    *reinterpret_cast<uint4*>(row + (((chunk0 + j) ^ rsw) << 4)) = o;
+    o.x = prmt(loA, hiA, 0x4051);  // (e0, e1)
+    o.y = prmt(loA, hiA, 0x6273);  // (e2, e3)
+    o.z = prmt(loB, hiB, 0x4051);  // (e4, e5)
+    o.w = prmt(loB, hiB, 0x6273);  // (e6, e7)
+    *reinterpret_cast<uint4*>(row + ((j ^ rsw) << 4)) = o;
   }
 }
 
@@ -125,7 +161,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* sA = smem + Cfg::kOffA;
   uint8_t* sB = smem + Cfg::kOffB;
   uint8_t* sRaw = smem + Cfg::kOffRaw;
-  float* sTab = reinterpret_cast<float*>(smem + Cfg::kOffTab);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
   uint64_t* tma_full = bars;
   uint64_t* b_full = bars + S;
@@ -147,10 +182,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       ptx::mbar_init(&tma_full[i], 1);
-      ptx::mbar_init(&b_full[i], 128);
+      ptx::mbar_init(&b_full[i], kNumDq);
       ptx::mbar_init(&empty[i], 1);
     }
-    ptx::mbar_init(lora_full, 128);
+    ptx::mbar_init(lora_full, kNumDq);
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(main_done, 1);
     *abort_flag = 0;
@@ -163,7 +198,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::tmem_alloc(tmem_holder, 256);
     ptx::tmem_relinquish();
   }
-  if (tid >= 64 && tid < 96) sTab[tid - 64] = __uint_as_float(d_nf4_level_bits[(tid - 64) & 15]);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -267,21 +301,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------- dequant / LoRA staging / epilogue
-    const int dq = tid - 64;  // 0..127
-    const float* tab = sTab + ((lane >> 4) << 4);
+    const int dq = tid - 64;  // 0..255
     bool ok = true;
     // LoRA side operands.  s * Xe (fp32; Xe = T or U) is split into bf16
     // hi + lo halves and folded over K = 2r columns [hi | lo] against
     // [Be | Be], so the side product keeps fp32 accuracy; Be (B_lora for the
     // forward, A_lora for dX) is used as stored.  The folded K is zero-padded
-    // to a multiple of 16.  Thread dq owns row dq of Xe; Be is handled in
-    // 2 * r/8 sixteen-byte tasks per thread (K-major: rows dq and dq + 128 x
-    // rank groups; MN-major: rank rows x 32 column chunks).
+    // to a multiple of 16.  Threads dq < 128 own row dq of Xe; Be is handled
+    // in r/8 sixteen-byte tasks per thread (K-major: row dq x rank groups;
+    // MN-major: rank rows x 32 column chunks, task dq + 256 t).
     const int r = args.r;
     const int nr = r / 8;
     const int kpad = ((2 * r + 15) / 16) * 16;
     const int nchunk = kpad / 8;
-    const int nbe = 2 * nr;
+    const int nbe = nr;
+    const bool xe_row = dq < kBM;
     auto load_xe = [&](int g, float (&v)[8]) {
       const int gm = m0 + dq;
       if (gm < args.M) {
@@ -311,11 +345,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     };
     auto load_be = [&](int t) -> uint4 {
       if (!BMN) {
-        const int j = dq + 128 * (t / nr), g = t % nr;
+        const int j = dq, g = t;
         const int gn = n0 + j;
         if (gn < args.N) return *reinterpret_cast<const uint4*>(args.lora_w + static_cast<int64_t>(gn) * r + g * 8);
       } else {
-        const int task = dq + 128 * t;
+        const int task = dq + kNumDq * t;
         const int i = task >> 5, gcol = n0 + (task & 31) * 8;
         if (gcol < args.N) return *reinterpret_cast<const uint4*>(args.lora_w + static_cast<int64_t>(i) * args.N + gcol);
       }
@@ -326,11 +360,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     };
     auto store_be = [&](uint8_t* bt, int t, uint4 v) {
       if (!BMN) {
-        const int j = dq + 128 * (t / nr), g = t % nr;
+        const int j = dq, g = t;
         *chunk_at(bt, j, g) = v;
         *chunk_at(bt, j, nr + g) = v;
       } else {
-        const int task = dq + 128 * t;
+        const int task = dq + kNumDq * t;
         const int i = task >> 5, cc = task & 31;
         *mn_chunk(bt, i, cc) = v;
         *mn_chunk(bt, r + i, cc) = v;
@@ -339,22 +373,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto store_pad = [&](uint8_t* at, uint8_t* bt) {  // zero the K columns 2r .. kpad-1
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int c = 2 * nr; c < nchunk; ++c) {
-        *chunk_at(at, dq, c) = z;
-        if (!BMN) {
-          *chunk_at(bt, dq, c) = z;
-          *chunk_at(bt, dq + 128, c) = z;
-        }
+        if (xe_row) *chunk_at(at, dq, c) = z;
+        if (!BMN) *chunk_at(bt, dq, c) = z;
       }
       if (BMN)
-        for (int task = dq; task < (kpad - 2 * r) * 32; task += 128) *mn_chunk(bt, 2 * r + (task >> 5), task & 31) = z;
+        for (int task = dq; task < (kpad - 2 * r) * 32; task += kNumDq)
+          *mn_chunk(bt, 2 * r + (task >> 5), task & 31) = z;
     };
     // Rank <= 16: fetch the operands now, while the main loop runs.
     const bool lora_pref = has_lora && r <= 16;
     float pre_x[2][8];
-    uint4 pre_b[4];
+    uint4 pre_b[2];
     if (lora_pref) {
-      for (int g = 0; g < nr; ++g) load_xe(g, pre_x[g]);
-      for (int t = 0; t < nbe; ++t) pre_b[t] = load_be(t);
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (xe_row && g < nr) load_xe(g, pre_x[g]);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (t < nbe) pre_b[t] = load_be(t);
     }
     if (BSRC == kBSrcNF4) {
       for (int kb = 0; kb < KB; ++kb) {
@@ -367,18 +403,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint8_t* codes = sRaw + s * Cfg::kRawBytes;
         const float* amax = reinterpret_cast<const float*>(codes + kCodesBytes);
         uint8_t* bt = sB + s * kBTileBytes;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int h = i * 128 + dq;
-          if (!BMN) {
-            const int row = h >> 1, half = h & 1;
-            const uint4 q = *reinterpret_cast<const uint4*>(codes + row * 32 + half * 16);
-            dequant_half_row(q, amax[row * 4 + (kb & 3)], tab, bt + row * 128, half * 4, row & 7);
-          } else {
-            const int n = h >> 3, a = (h >> 1) & 3, half = h & 1;
-            const uint4 q = *reinterpret_cast<const uint4*>(codes + n * 128 + a * 32 + half * 16);
-            dequant_half_row(q, amax[n * 4 + a], tab, bt + a * (64 * 128) + n * 128, half * 4, n & 7);
-          }
+        if (!BMN) {  // row dq of the [256 x 64] tile
+          nf4_row_bf16(codes + dq * 32, amax[dq * 4 + (kb & 3)], bt + dq * 128, dq & 7);
+        } else {     // reduction row n, 64-column atom a of the [64 x 256] tile
+          const int n = dq >> 2, a = dq & 3;
+          nf4_row_bf16(codes + n * 128 + a * 32, amax[n * 4 + a], bt + a * (64 * 128) + n * 128, n & 7);
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(&b_full[s]);
@@ -393,10 +422,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint8_t* at = sA + s * kATileBytes;
         uint8_t* bt = sB + s * kBTileBytes;
         if (lora_pref) {
-          for (int g = 0; g < nr; ++g) store_xe(at, g, pre_x[g]);
-          for (int t = 0; t < nbe; ++t) store_be(bt, t, pre_b[t]);
+#pragma unroll
+          for (int g = 0; g < 2; ++g)
+            if (xe_row && g < nr) store_xe(at, g, pre_x[g]);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (t < nbe) store_be(bt, t, pre_b[t]);
         } else {
-          for (int g = 0; g < nr; ++g) {
+          for (int g = 0; g < nr && xe_row; ++g) {
             float v[8];
             load_xe(g, v);
             store_xe(at, g, v);
@@ -413,14 +446,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     acc_ready = __all_sync(0xffffffffu, acc_ready);  // tcgen05.ld below is warp-collective
     if (acc_ready) {
       ptx::tc_fence_after();
-      const int q = warp & 3;
+      const int q = warp & 3;                 // TMEM lane quadrant of this warp
+      const int ch = (warp - 2) >> 2;         // column half: warps 2-5 -> 0..127, 6-9 -> 128..255
+      const int cbeg = ch * (kBN / 2), cend = cbeg + kBN / 2;
       const int row = q * 32 + lane;
       const int gm = m0 + row;
       const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
       if (EPI == kEpiStoreBF16) {
         uint16_t* out = reinterpret_cast<uint16_t*>(args.out);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c0, v);
           ptx::tmem_wait_ld();
@@ -440,7 +475,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if (EPI == kEpiAddF32) {
         float* out = reinterpret_cast<float*>(args.out);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c0, v);
           ptx::tmem_wait_ld();
@@ -467,7 +502,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int lab = (gm < args.M) ? args.labels[gm] : args.ignore_index;
         float mx = -INFINITY, sm = 0.0f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c0, v);
           ptx::tmem_wait_ld();
@@ -490,7 +525,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (gm < args.M) {
-          const int64_t p = static_cast<int64_t>(gm) * args.part_ld + args.tile_base + blockIdx.x;
+          const int64_t p = static_cast<int64_t>(gm) * args.part_ld + 2 * (args.tile_base + blockIdx.x) + ch;
           args.part_max[p] = mx;
           args.part_sum[p] = sm;
         }
@@ -499,7 +534,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const float lse = (gm < args.M) ? args.row_lse[gm] : 0.0f;
         const float sc = (gm < args.M) ? args.row_scale[gm] : 0.0f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c0, v);
           ptx::tmem_wait_ld();
