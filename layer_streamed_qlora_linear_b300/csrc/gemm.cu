@@ -5,6 +5,7 @@
 #include <vector>
 
 #include "gemm.cuh"
+#include "gemm2.cuh"
 
 namespace sl {
 
@@ -72,6 +73,23 @@ int variant_of(const GemmLaunch& g) {
 }
 }  // namespace
 
+// NF4 GEMM on CTA pairs (M = 256 per pair); used when M > 128.
+template <int BMN>
+static sl_status run_pair(const CUtensorMap& ma, const CUtensorMap& mc, const CUtensorMap& ms, const GemmArgs& a,
+                          cudaStream_t stream) {
+  auto kern = gemm_nf4_pair_kernel<BMN>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  SL_CHECK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    SL_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gemm2Cfg::kSmem));
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  dim3 grid(static_cast<unsigned>(2 * ceil_div(a.M, 256)), static_cast<unsigned>(ceil_div(a.N, kBN)));
+  kern<<<grid, kGemm2Threads, Gemm2Cfg::kSmem, stream>>>(ma, mc, ms, a);
+  return check_launch("gemm_nf4_pair_kernel");
+}
+
 template <int BSRC, int BMN, int EPI>
 static sl_status run(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms, const GemmArgs& a,
                      cudaStream_t stream) {
@@ -98,6 +116,7 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (a.N % 32) return set_error(SL_ERR_INVALID, "gemm: output columns must be a multiple of 32");
   if (a.r < 0 || a.r > 32 || (a.r % 8)) return set_error(SL_ERR_INVALID, "gemm: LoRA rank must be 0..32, multiple of 8");
   CUtensorMap ma, mb, ms;
+  bool pair = false;
   sl_status st = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, a.K, a.M, g.lda * 2, kBK, kBM,
                           CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != SL_OK) return st;
@@ -115,7 +134,24 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     const int64_t rows = g.bmn ? a.K : a.N;   // weight rows
     const int64_t cols = g.ldw;               // weight row length in elements
     if (cols % 256) return set_error(SL_ERR_INVALID, "gemm: NF4 weight rows must be a multiple of 256 elements");
-    if (!g.bmn) {
+    if (g.epi == kEpiStoreBF16 && a.M > kBM) {
+      // CTA-pair kernel: each CTA maps its own half of the B tile.
+      if (!g.bmn) {
+        st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.codes, cols / 2, rows, cols / 2, kBK / 2, 128,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st == SL_OK)
+          st = make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax, cols / 64, rows, cols / 64 * 4, 4, 128,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+      } else {
+        st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.codes, cols / 2, rows, cols / 2, 64, kBK,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st == SL_OK)
+          st = make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax, cols / 64, rows, cols / 64 * 4, 4, kBK,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+      }
+      if (st != SL_OK) return st;
+      pair = true;
+    } else if (!g.bmn) {
       st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.codes, cols / 2, rows, cols / 2, kBK / 2, kBN,
                     CU_TENSOR_MAP_SWIZZLE_NONE);
       if (st == SL_OK)
@@ -141,7 +177,8 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
       if (tl.start) cudaEventRecord(tl.start, stream);
     }
   }
-  st = dispatch(g, ma, mb, ms, stream);
+  st = pair ? (g.bmn ? run_pair<1>(ma, mb, ms, a, stream) : run_pair<0>(ma, mb, ms, a, stream))
+            : dispatch(g, ma, mb, ms, stream);
   if (tl.start && tl.stop) {
     cudaEventRecord(tl.stop, stream);
     std::lock_guard<std::mutex> lk(g_time_mu);
