@@ -1,14 +1,20 @@
 #!/usr/bin/env python
-"""Benchmark of the layer-streamed NF4 LoRA training step on B300.
+"""Benchmark of the layer-streamed NF4 LoRA training path on B300.
 
-Workload (one "step"): forward over 32 Llama-3.1-8B-shaped decoder layers
-(q 4096x4096, k/v 1024x4096, o 4096x4096, gate/up 14336x4096, down 4096x14336,
-NF4 base, LoRA r=16 alpha=32 on all seven projections) then backward in
-reverse, M = 1024 tokens, the frozen base streamed layer by layer from pinned
-host RAM through two device buffers.  Synthetic seeded data; no trained
-weights.  Prints ONE JSON line (rank 0).
+Default workload (one "step"): forward over 32 Llama-3.1-8B-shaped decoder
+layers (q 4096x4096, k/v 1024x4096, o 4096x4096, gate/up 14336x4096, down
+4096x14336, NF4 base, LoRA r=16 alpha=32 on all seven projections) then
+backward in reverse, M = 1024 tokens, the frozen base streamed layer by layer
+from pinned host RAM through two device buffers.  Synthetic seeded data; no
+trained weights.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload stack8b|stack_qwen3b|layer8b|ce]
+
+Other workloads (not the headline line): the 36-layer Qwen2.5-3B-shaped
+stack with a bf16 base streamed at M=2048; one Llama-8B layer's seven NF4
+LoRA linears resident at M=2048 (fwd+bwd); the LM-head cross-entropy
+(M=2048, D=4096, V=128256).
 
 --impl reference times the plain CPU oracle (the reference of this build) on
 the host cores, on a bounded sample of the same workload.
@@ -26,8 +32,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "train tokens/s (8B-shape NF4 streamed fwd+bwd); % of PCIe/HBM/TC roofline"
 UNIT = "tokens/s"
-L, M, D, DKV, F, R, ALPHA = 32, 1024, 4096, 1024, 14336, 16, 32.0
-WORKLOAD = "llama-3.1-8b-shaped 32-layer NF4 LoRA stack streamed from pinned host RAM, fwd 0..31 + bwd 31..0"
+WORKLOADS = {
+    "stack8b": dict(kind="stack", base="nf4", L=32, M=1024, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
+                    name="llama-3.1-8b-shaped 32-layer NF4 LoRA stack streamed from pinned host RAM, "
+                         "fwd 0..31 + bwd 31..0"),
+    "stack_qwen3b": dict(kind="stack", base="bf16", L=36, M=2048, D=2048, Dkv=256, F=11008, r=16, alpha=32.0,
+                         name="qwen2.5-3b-shaped 36-layer bf16-base LoRA stack streamed from pinned host RAM"),
+    "layer8b": dict(kind="layer", base="nf4", M=2048, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
+                    name="one llama-3.1-8b-shaped layer: seven NF4 LoRA linears resident, fwd+bwd"),
+    "ce": dict(kind="ce", M=2048, D=4096, V=128256, chunk=8192,
+               name="LM-head cross-entropy fwd+bwd, vocab-chunked (llama-3.1-8b head)"),
+}
 
 
 def load_peaks():
@@ -41,6 +56,10 @@ def load_peaks():
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def proj_shapes(D, Dkv, F):
+    return [("q", D, D), ("k", Dkv, D), ("v", Dkv, D), ("o", D, D), ("gate", F, D), ("up", F, D), ("down", D, F)]
 
 
 # --------------------------------------------------------------------- clocks
@@ -95,107 +114,94 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_layer_sample(m_sample, seed=3):
-    """The oracle on a bounded sample of the workload: ONE full-width NF4 layer,
-    m_sample tokens.  Returns (seconds per step of the sample, threads used, closure)."""
-    import numpy as np
-    import seeded_inputs as si
-    from oracle import nf4, stack
-    c = si.stack_case(seed, 1, m_sample, D, DKV, F, R)
-    lw = c["layers"][0]
-    q = {n: nf4.quantize(lw[n]["W"]) for n in si.PROJ_NAMES}   # offline (not timed), like the GPU's blobs
-
-    def step():
-        layer = {n: dict(W=nf4.dequantize_bf16(*q[n], *lw[n]["W"].shape), A=lw[n]["A"].astype(np.float64),
-                         B=lw[n]["B"].astype(np.float64)) for n in si.PROJ_NAMES}
-        stack.stack_step(c["h0"], c["dh_top"], [layer], ALPHA, rnd=True)
-
+def _threads():
     try:
         from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [os.cpu_count() or 1])
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [os.cpu_count() or 1])
     except ImportError:   # numpy's BLAS runs one thread per host core by default
-        threads = os.cpu_count() or 1
-    return step, threads
+        return os.cpu_count() or 1
 
 
-def cpu_baseline(m_sample=64):
-    step, threads = oracle_layer_sample(m_sample)
-    step()  # warm
+def oracle_sample(w):
+    """The oracle on a bounded sample of workload w.
+
+    Returns (step, sample_tokens, scale, description): tokens/s of the full
+    workload = sample_tokens / (scale * seconds per sample step)."""
+    import numpy as np
+    import seeded_inputs as si
+    from oracle import ce, lora, nf4, stack
+    if w["kind"] in ("stack", "layer"):
+        ms = 64
+        c = si.stack_case(3, 1, ms, w["D"], w["Dkv"], w["F"], w["r"])
+        lw = c["layers"][0]
+        nf = w["base"] == "nf4"
+        q = {n: nf4.quantize(lw[n]["W"]) for n in si.PROJ_NAMES} if nf else None  # offline, not timed
+
+        def layer():
+            return {n: dict(W=(nf4.dequantize_bf16(*q[n], *lw[n]["W"].shape) if nf else lw[n]["W"].astype(np.float64)),
+                            A=lw[n]["A"].astype(np.float64), B=lw[n]["B"].astype(np.float64)) for n in si.PROJ_NAMES}
+
+        if w["kind"] == "stack":
+            def step():
+                stack.stack_step(c["h0"], c["dh_top"], [layer()], w["alpha"], rnd=True)
+            return step, ms, w["L"], (f"one full-width {w['base']} layer (of {w['L']}), {ms} tokens, fwd+bwd "
+                                      f"incl. dequantisation; tokens/s scaled by 1/{w['L']} layers")
+        shp = proj_shapes(w["D"], w["Dkv"], w["F"])
+        ys = {n: si.normal_bf16(77 + i, (ms, N), 1.0) for i, (n, N, K) in enumerate(shp)}
+        xs = {n: si.normal_bf16(55 + i, (ms, K), 1.0) for i, (n, N, K) in enumerate(shp)}
+
+        def step():
+            P = layer()
+            for n in si.PROJ_NAMES:
+                lora.lora_linear_fwd(xs[n], P[n]["W"], P[n]["A"], P[n]["B"], w["alpha"])
+                lora.lora_linear_bwd(xs[n], ys[n], P[n]["W"], P[n]["A"], P[n]["B"], w["alpha"])
+        return step, ms, 1, f"the seven linears of one layer at {ms} tokens, fwd+bwd incl. dequantisation"
+    # cross-entropy: 16 rows against the whole vocabulary (loss terms and dH rows)
+    rows = 16
+    cc = si.ce_case(5, rows, w["D"], w["V"])
+    W64 = cc["W"].astype(np.float64)
+    nv = int(np.sum(cc["labels"] != -100))
+
+    def step():
+        ce.ce_rows(cc["H"], W64, cc["labels"], max(nv, 1))
+    return step, rows, 1, f"{rows} rows of the {w['M']}-row batch against the full {w['V']}-entry vocabulary"
+
+
+def cpu_baseline(w):
+    step, ms, scale, desc = oracle_sample(w)
+    step()
     t0 = time.perf_counter()
     step()
     dt = time.perf_counter() - t0
-    tok_s = m_sample / (L * dt)       # the full stack is L such layers
-    return {"value": tok_s, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"one full-width NF4 layer (of {L}), {m_sample} tokens, fwd+bwd incl. dequantisation; "
-                      f"{dt:.2f} s; tokens/s scaled by 1/{L} layers"}
+    return {"value": ms / (scale * dt), "unit": UNIT, "cores": _threads(), "kind": "oracle",
+            "sample": f"{desc}; {dt:.2f} s per sample"}
 
 
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    m_sample = 64
-    step, threads = oracle_layer_sample(m_sample)
+    w = WORKLOADS[args.workload]
+    step, ms, scale, desc = oracle_sample(w)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     dt = (time.perf_counter() - t0) / args.steps
-    v = m_sample / (L * dt)
+    v = ms / (scale * dt)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 * L * M / m_sample,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": w["M"] / v * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "tokens": M, "layers": L, "rank": R,
-                                            "sample": f"1 layer x {m_sample} tokens per step"},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"each step: one full-width NF4 layer, {m_sample} tokens, fwd+bwd; "
-                                       f"tokens/s scaled by 1/{L} layers"},
+            "data": "synthetic", "config": {"workload": w["name"], "tokens": w["M"], "sample": desc},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _threads(), "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------------- ours
-def run_ours(args):
-    import torch
-    import layer_streamed_qlora_linear_b300 as sl
-    rank, local, world = dist_env()
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    peaks, peak_src = load_peaks()
-    dev = torch.device("cuda", local)
-    nl = args.layers
-    gen = torch.Generator(device=dev).manual_seed(1234 + rank)
-    rnd = lambda shape, std: (torch.randn(*shape, generator=gen, device=dev) * std).to(torch.bfloat16)
-    shapes = sl.proj_shapes(D, DKV, F)
-
-    # frozen NF4 base: quantised on the device by the library, kept in pinned host RAM
-    host_blobs, A, B = [], [], []
-    for l in range(nl):
-        blob = sl.build_layer_blob(sl.SL_WEIGHT_NF4, D, DKV, F, [rnd((N, K), 0.02) for N, K in shapes])
-        h = torch.empty(blob.numel(), dtype=torch.uint8, pin_memory=True)
-        h.copy_(blob)
-        host_blobs.append(h)
-        del blob
-        for N, K in shapes:
-            A.append(rnd((R, K), 0.02))
-            B.append(rnd((N, R), 0.02))
-    dA = [torch.empty(a.shape, dtype=torch.float32, device=dev) for a in A]
-    dB = [torch.empty(b.shape, dtype=torch.float32, device=dev) for b in B]
-    h0 = torch.randn(M, D, generator=gen, device=dev).to(torch.bfloat16).float()
-    dh = torch.randn(M, D, generator=gen, device=dev).to(torch.bfloat16).float()
-    hL = torch.empty(M, D, device=dev)
-    dh0 = torch.empty(M, D, device=dev)
-    stk = sl.Stack(sl.SL_WEIGHT_NF4, D, DKV, F, host_blobs)
-    ws = torch.empty(stk.workspace_size(M, R), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step():
-        stk.step(sl.SL_MODE_STREAMED, h0, dh, A, B, R, ALPHA, hL, dh0, dA, dB, ws)
-
-    # pinned H2D bandwidth of this box: 1 GiB, best of 10, CUDA events
+def pinned_h2d_peak(torch, dev):
+    """Pinned host -> device copy bandwidth of this machine: 1 GiB, best of 10, CUDA events."""
     hb = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
     db = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
     best = 1e9
@@ -206,8 +212,144 @@ def run_ours(args):
         e1.record()
         torch.cuda.synchronize()
         best = min(best, e0.elapsed_time(e1))
-    h2d_peak = (1 << 30) / (best * 1e-3) / 1e9
-    del hb, db
+    return (1 << 30) / (best * 1e-3) / 1e9
+
+
+def run_ours(args):
+    import torch
+    import layer_streamed_qlora_linear_b300 as sl
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda", local)
+    w = dict(WORKLOADS[args.workload])
+    if args.layers and w["kind"] == "stack":
+        w["L"] = args.layers
+    M = w["M"]
+    gen = torch.Generator(device=dev).manual_seed(1234 + rank)
+    rnd = lambda shape, std: (torch.randn(*shape, generator=gen, device=dev) * std).to(torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    extra = {}
+    dominant = ("nf4_fwd", "nf4_dx")
+    kname = "gemm_nf4_pair_kernel (fused NF4 dequant + LoRA fold, CTA pairs; fwd and dX)"
+    h2d_peak = None
+
+    if w["kind"] == "stack":
+        kind = sl.SL_WEIGHT_NF4 if w["base"] == "nf4" else sl.SL_WEIGHT_BF16
+        if kind == sl.SL_WEIGHT_BF16:
+            dominant = ("bf16_fwd", "bf16_dx")
+            kname = "gemm_tc_kernel<BF16> (bf16 base + LoRA fold; fwd and dX)"
+        D, Dkv, F, L, r, alpha = w["D"], w["Dkv"], w["F"], w["L"], w["r"], w["alpha"]
+        shapes = sl.proj_shapes(D, Dkv, F)
+        host_blobs, A, B = [], [], []
+        for l in range(L):
+            blob = sl.build_layer_blob(kind, D, Dkv, F, [rnd((N, K), 0.02) for N, K in shapes])
+            h = torch.empty(blob.numel(), dtype=torch.uint8, pin_memory=True)
+            h.copy_(blob)
+            host_blobs.append(h)
+            del blob
+            for N, K in shapes:
+                A.append(rnd((r, K), 0.02))
+                B.append(rnd((N, r), 0.02))
+        dA = [torch.empty(a.shape, dtype=torch.float32, device=dev) for a in A]
+        dB = [torch.empty(b.shape, dtype=torch.float32, device=dev) for b in B]
+        h0 = torch.randn(M, D, generator=gen, device=dev).to(torch.bfloat16).float()
+        dh = torch.randn(M, D, generator=gen, device=dev).to(torch.bfloat16).float()
+        hL = torch.empty(M, D, device=dev)
+        dh0 = torch.empty(M, D, device=dev)
+        stk = sl.Stack(kind, D, Dkv, F, host_blobs)
+        ws = torch.empty(stk.workspace_size(M, r), dtype=torch.uint8, device=dev)
+
+        def step():
+            stk.step(sl.SL_MODE_STREAMED, h0, dh, A, B, r, alpha, hL, dh0, dA, dB, ws)
+
+        h0_h, dh_h = h0.cpu().pin_memory(), dh.cpu().pin_memory()
+        out_h = torch.empty(M, D, dtype=torch.float32, pin_memory=True)
+        h0_d, dh_d = torch.empty_like(h0), torch.empty_like(dh)
+
+        def e2e_step():
+            h0_d.copy_(h0_h, non_blocking=True)
+            dh_d.copy_(dh_h, non_blocking=True)
+            stk.step(sl.SL_MODE_STREAMED, h0_d, dh_d, A, B, r, alpha, hL, dh0, dA, dB, ws)
+            out_h.copy_(hL, non_blocking=True)
+        e2e_bytes = (h0_h.numel() * 4 + dh_h.numel() * 4, out_h.numel() * 4)
+        h2d_peak = pinned_h2d_peak(torch, dev)
+        config = {"workload": w["name"], "tokens": M, "layers": L, "D": D, "Dkv": Dkv, "F": F, "rank": r,
+                  "alpha": alpha, "base": "NF4 blocksize 64 fp32 absmax" if kind == sl.SL_WEIGHT_NF4 else "bf16",
+                  "l2": f"inputs larger than L2 ({stk.host_bytes / 1e9:.1f} GB streamed base + activations)"}
+    elif w["kind"] == "layer":
+        D, Dkv, F, r, alpha = w["D"], w["Dkv"], w["F"], w["r"], w["alpha"]
+        lin = []
+        for name, N, K in proj_shapes(D, Dkv, F):
+            Wt = rnd((N, K), 0.02)
+            codes = torch.empty(N * K // 2, dtype=torch.uint8, device=dev)
+            absmax = torch.empty(N * K // 64, dtype=torch.float32, device=dev)
+            sl.sl_nf4_quantize(Wt, codes, absmax)
+            del Wt
+            lin.append(dict(w=sl.Weight.nf4(codes, absmax, N, K), X=rnd((M, K), 1.0), dY=rnd((M, N), 1.0),
+                            A=rnd((r, K), 0.02), B=rnd((N, r), 0.02),
+                            Y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+                            T=torch.empty(M, r, dtype=torch.float32, device=dev),
+                            dX=torch.empty(M, K, dtype=torch.bfloat16, device=dev),
+                            dA=torch.empty(r, K, device=dev), dB=torch.empty(N, r, device=dev),
+                            ws=torch.empty(sl.sl_lora_linear_workspace_size(M, N, K, r), dtype=torch.uint8,
+                                           device=dev), N=N, K=K))
+
+        def step():
+            for p in lin:
+                sl.sl_lora_linear_fwd(p["w"], p["X"], p["A"], p["B"], r, alpha, p["Y"], p["T"], p["ws"])
+                sl.sl_lora_linear_bwd(p["w"], p["X"], p["dY"], p["A"], p["B"], r, alpha, p["T"], p["dX"], p["dA"],
+                                      p["dB"], False, p["ws"])
+
+        hosts = [(p["X"].cpu().pin_memory(), p["dY"].cpu().pin_memory()) for p in lin]
+        res_h = torch.empty(7, 8, dtype=torch.float32, pin_memory=True)
+
+        def e2e_step():
+            for p, (xh, yh) in zip(lin, hosts):
+                p["X"].copy_(xh, non_blocking=True)
+                p["dY"].copy_(yh, non_blocking=True)
+            step()
+            for i, p in enumerate(lin):   # a slice of every adapter gradient read back
+                res_h[i].copy_(p["dA"][0, :8], non_blocking=True)
+        e2e_bytes = (sum(xh.numel() * 2 + yh.numel() * 2 for xh, yh in hosts), res_h.numel() * 4)
+        # algorithmic work: base fwd + dX (4 M N K) and the LoRA side products (T, U, fold x2, dA, dB)
+        flops = sum(4.0 * M * p["N"] * p["K"] + 6.0 * M * r * (p["N"] + p["K"]) for p in lin)
+        nbytes = sum(2 * (p["N"] * p["K"] * 0.5625) + 3 * (M * p["K"] * 2) + 3 * (M * p["N"] * 2) for p in lin)
+        extra["step_roofline_inputs"] = {"flops": flops, "bytes": nbytes}
+        config = {"workload": w["name"], "tokens": M, "D": D, "Dkv": Dkv, "F": F, "rank": r, "alpha": alpha,
+                  "base": "NF4 blocksize 64 fp32 absmax", "l2": "inputs larger than L2 (~0.8 GB touched per step)"}
+    else:  # cross-entropy
+        D, V, chunk = w["D"], w["V"], w["chunk"]
+        dominant = ("ce_lse", "ce_softmax", "ce_dh")
+        kname = "gemm_tc_kernel<BF16> CE epilogues (logits/lse, softmax chunk, dH)"
+        H = rnd((M, D), 1.0)
+        Wh = rnd((V, D), 0.02)
+        lab = torch.randint(0, V, (M,), generator=gen, device=dev, dtype=torch.int32)
+        lab[torch.randperm(M, generator=gen, device=dev)[: round(0.05 * M)]] = -100
+        loss = torch.empty(1, device=dev)
+        dH = torch.empty(M, D, device=dev)
+        ws = torch.empty(sl.sl_ce_workspace_size(M, D, V, chunk), dtype=torch.uint8, device=dev)
+
+        def step():
+            sl.sl_ce_fwd_bwd(H, Wh, lab, loss, dH, ws, chunk_V=chunk)
+
+        Hh, labh = H.cpu().pin_memory(), lab.cpu().pin_memory()
+        loss_h = torch.empty(1, dtype=torch.float32, pin_memory=True)
+
+        def e2e_step():
+            H.copy_(Hh, non_blocking=True)
+            lab.copy_(labh, non_blocking=True)
+            step()
+            loss_h.copy_(loss, non_blocking=True)
+        e2e_bytes = (Hh.numel() * 2 + labh.numel() * 4, 4)
+        # algorithmic work: the logits GEMM and the dH GEMM (2 x 2 M V D); head read twice
+        extra["step_roofline_inputs"] = {"flops": 2 * 2.0 * M * V * D, "bytes": V * D * 2.0 * 2 + M * D * 6.0}
+        extra["extra_bytes_per_logit"] = ws.numel() / (M * V)
+        config = {"workload": w["name"], "tokens": M, "D": D, "V": V, "chunk_V": chunk, "ignore_frac": 0.05,
+                  "l2": "inputs larger than L2 (1.05 GB head read per GEMM pass)"}
 
     for _ in range(args.warmup):
         step()
@@ -220,104 +362,110 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    def max_over_ranks(x):
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([x], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return x
+
+    # timed region: K steps, CUDA events on the compute stream
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
-    sl.sl_kernel_timing(True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     barrier()
-    sl.sl_kernel_timing(False)
     clk = clocks.stop()
-    ms_total = e0.elapsed_time(e1)
-    h2d_step, kernels_step = stk.last_step_stats()
-    timing = {name: sl.sl_kernel_timing_read(i) for i, name in enumerate(sl.GEMM_VARIANTS)}
-    sl.sl_check_device_errors()
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / args.steps
     value = world * M * args.steps / (ms_total * 1e-3)
+    h2d_step = kernels_step = None
+    if w["kind"] == "stack":
+        h2d_step, kernels_step = stk.last_step_stats()
+
+    # the same K steps again with a CUDA event pair around every tensor-core GEMM launch
+    sl.sl_kernel_timing(True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms_instr = e0.elapsed_time(e1)
+    sl.sl_kernel_timing(False)
+    timing = {name: sl.sl_kernel_timing_read(i) for i, name in enumerate(sl.GEMM_VARIANTS)}
+    sl.sl_check_device_errors()
 
     # end to end through the public API: host inputs in, host result out, every step
-    h0_h = h0.cpu().pin_memory()
-    dh_h = dh.cpu().pin_memory()
-    hL_h = torch.empty(M, D, dtype=torch.float32, pin_memory=True)
-    h0_d, dh_d = torch.empty_like(h0), torch.empty_like(dh)
     barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        h0_d.copy_(h0_h, non_blocking=True)
-        dh_d.copy_(dh_h, non_blocking=True)
-        stk.step(sl.SL_MODE_STREAMED, h0_d, dh_d, A, B, R, ALPHA, hL, dh0, dA, dB, ws)
-        hL_h.copy_(hL, non_blocking=True)
+        e2e_step()
     barrier()
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * M * args.steps / e2e_s, "unit": UNIT,
-           "h2d_bytes_per_step": int(h0_h.numel() * 4 + dh_h.numel() * 4),
-           "d2h_bytes_per_step": int(hL_h.numel() * 4)}
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    e2e = {"value": world * M * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(e2e_bytes[0]),
+           "d2h_bytes_per_step": int(e2e_bytes[1])}
 
-    # dominant kernel: the fused NF4 dequant + LoRA tcgen05 GEMM (forward and dX variants)
-    n_f, ms_f, fl_f = timing["nf4_fwd"]
-    n_x, ms_x, fl_x = timing["nf4_dx"]
-    gemm_ms = ms_f + ms_x
-    achieved = (fl_f + fl_x) / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else 0.0
+    n_d = sum(timing[k][0] for k in dominant)
+    ms_d = sum(timing[k][1] for k in dominant)
+    fl_d = sum(timing[k][2] for k in dominant)
+    achieved = fl_d / (ms_d * 1e-3) / 1e12 if ms_d > 0 else 0.0
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-    roofline = {"bound": "tensor", "kernel": "gemm_tc_kernel<NF4> (fused dequant + LoRA fold; fwd and dX)",
-                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
-                "traffic": None, "launches": n_f + n_x, "avg_launch_ms": gemm_ms / max(1, n_f + n_x),
-                "share_of_step": gemm_ms / ms_total}
-    stream_roof = {"bound": "pcie_h2d", "h2d_bytes_per_step": h2d_step,
-                   "achieved_gbs": h2d_step / (ms_step * 1e-3) / 1e9, "peak_gbs": h2d_peak,
-                   "frac": h2d_step / (ms_step * 1e-3) / 1e9 / h2d_peak,
-                   "peak_source": "measured in this run: pinned 1 GiB cudaMemcpyAsync, best of 10"}
+                "traffic": None, "launches": n_d, "avg_launch_ms": ms_d / max(1, n_d),
+                "share_of_step": ms_d / ms_instr,
+                "timing": "per-launch CUDA event pairs (libsl, on the launching stream) over a second timed "
+                          "region of the same K steps"}
     per_variant = {k: {"launches": v[0], "ms": v[1], "tflops": (v[2] / (v[1] * 1e-3) / 1e12) if v[1] else 0.0}
                    for k, v in timing.items() if v[0]}
-
-    # resident run of the same kernels (compute-only context number)
-    resident = None
-    if not args.no_resident:
-        dev_blobs = [hb.to(dev) for hb in host_blobs]
-        stk_r = sl.Stack(sl.SL_WEIGHT_NF4, D, DKV, F, host_blobs, dev_blobs)
-        stk_r.step(sl.SL_MODE_RESIDENT, h0, dh, A, B, R, ALPHA, hL, dh0, dA, dB, ws)
-        barrier()
-        e0.record(stream)
-        nres = max(2, min(args.steps, 5))
-        for _ in range(nres):
-            stk_r.step(sl.SL_MODE_RESIDENT, h0, dh, A, B, R, ALPHA, hL, dh0, dA, dB, ws)
-        e1.record(stream)
-        barrier()
-        resident = {"tokens_per_s": M * nres / (e0.elapsed_time(e1) * 1e-3),
-                    "ms_per_step": e0.elapsed_time(e1) / nres}
-        stk_r.close()
-        del dev_blobs
-
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded device RNG)",
+            "config": dict(config, parallelism=f"replicas x{world} (no collective on the data path)"),
+            "roofline": roofline, "kernels": per_variant, "e2e": e2e, "clocks": clk}
+    if w["kind"] == "stack":
+        line["stream"] = {"bound": "pcie_h2d", "h2d_bytes_per_step": h2d_step,
+                          "achieved_gbs": h2d_step / (ms_step * 1e-3) / 1e9, "peak_gbs": h2d_peak,
+                          "frac": h2d_step / (ms_step * 1e-3) / 1e9 / h2d_peak,
+                          "peak_source": "measured in this run: pinned 1 GiB cudaMemcpyAsync, best of 10"}
+        line["gpu_launches"] = int(kernels_step * args.steps)
+        line["preflight"] = {"host_bytes": stk.host_bytes, "buffer_bytes": stk.buffer_bytes}
+        if not args.no_resident:
+            dev_blobs = [hb.to(dev) for hb in host_blobs]
+            stk_r = sl.Stack(kind, D, Dkv, F, host_blobs, dev_blobs)
+            stk_r.step(sl.SL_MODE_RESIDENT, h0, dh, A, B, r, alpha, hL, dh0, dA, dB, ws)
+            barrier()
+            e0.record(stream)
+            nres = max(2, min(args.steps, 5))
+            for _ in range(nres):
+                stk_r.step(sl.SL_MODE_RESIDENT, h0, dh, A, B, r, alpha, hL, dh0, dA, dB, ws)
+            e1.record(stream)
+            barrier()
+            line["resident"] = {"tokens_per_s": M * nres / (e0.elapsed_time(e1) * 1e-3),
+                                "ms_per_step": e0.elapsed_time(e1) / nres}
+            stk_r.close()
+            del dev_blobs
+    else:
+        fl, nb = extra["step_roofline_inputs"]["flops"], extra["step_roofline_inputs"]["bytes"]
+        t_roof = max(fl / (peaks["bf16_tflops"] * 1e12), nb / (peaks["hbm_gbs"] * 1e9))
+        line["step_roofline"] = {"algorithmic_flops": fl, "algorithmic_bytes": nb,
+                                 "roofline_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3),
+                                 "peaks": f"{peak_src} bf16_tflops (burst) and hbm_gbs"}
+        if "extra_bytes_per_logit" in extra:
+            line["extra_device_bytes_per_logit"] = extra["extra_bytes_per_logit"]
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded device RNG weights, NF4 on device)",
-                "config": {"workload": WORKLOAD, "tokens": M, "layers": nl, "D": D, "Dkv": DKV, "F": F, "rank": R,
-                           "alpha": ALPHA, "base": "NF4 blocksize 64 fp32 absmax",
-                           "parallelism": f"replicas x{world} (no collective on the data path)",
-                           "l2": "inputs larger than L2 (3.9 GB streamed base + ~5 GB activations per step)"},
-                "roofline": roofline, "stream": stream_roof, "kernels": per_variant,
-                "e2e": e2e, "gpu_launches": int(kernels_step * args.steps), "clocks": clk,
-                "resident": resident, "preflight": {"host_bytes": stk.host_bytes, "buffer_bytes": stk.buffer_bytes}}
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
-    stk.close()
+    if w["kind"] == "stack":
+        stk.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -329,7 +477,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--layers", type=int, default=L, help="layers (default 32; fewer only for quick checks)")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack8b")
+    ap.add_argument("--layers", type=int, default=0, help="stack depth override (quick checks only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-resident", action="store_true")
     args = ap.parse_args()
