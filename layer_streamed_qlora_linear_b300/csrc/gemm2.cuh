@@ -116,7 +116,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
     for (int i = 0; i < S; ++i) {
       ptx::mbar_init(&full[i], 1);
       ptx::mbar_init(&raw_full[i], 1);
-      ptx::mbar_init(&b_local[i], kNumDq2 / 32);
+      ptx::mbar_init(&b_local[i], kNumDq2 / 64);  // the 4 warps of the group that owns this k-block
       ptx::mbar_init(&empty[i], 1);
       ptx::mbar_init(&b_peer[i], 1);
     }
@@ -327,7 +327,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
         if (t < nbe && be_valid(t)) pre_b[t] = load_be(t);
     }
 
-    for (int kb = 0; kb < KB; ++kb) {
+    // Two groups of four warps take alternate k-blocks; each thread expands
+    // one full 64-element row (one 16-entry table per row and k-block).
+    const int grp = (warp - 2) >> 2;  // 0: even k-blocks, 1: odd
+    const int t = dq & 127;
+    for (int kb = grp; kb < KB; kb += 2) {
       const int s = kb % S;
       if (!ptx::mbar_wait_cluster(&raw_full[s], (kb / S) & 1, abort_flag)) {
         give_up();
@@ -337,16 +341,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
       const uint8_t* codes = sRaw + s * Cfg::kRawBytes;
       const float* amax = reinterpret_cast<const float*>(codes + kHalfCodesBytes);
       uint8_t* bt = sB + s * kHalfBTileBytes;
-      if (!BMN) {  // half row (32 elements) of row dq/2 of the [128 x 64] half tile
-        const int row = dq >> 1, half = dq & 1;
-        const uint4 q = *reinterpret_cast<const uint4*>(codes + row * 32 + half * 16);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        nf4_words_bf16<4>(w, amax[row * 4 + (kb & 3)], bt + row * 128, half * 4, row & 7);
-      } else {     // reduction row n, atom a (of 2), half of its 64 columns
-        const int n = dq >> 2, a = (dq >> 1) & 1, half = dq & 1;
-        const uint4 q = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32 + half * 16);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        nf4_words_bf16<4>(w, amax[n * 4 + 2 * static_cast<int>(rank) + a], bt + a * (64 * 128) + n * 128, half * 4,
+      if (!BMN) {  // row t of the [128 x 64] half tile
+        const uint4 q0 = *reinterpret_cast<const uint4*>(codes + t * 32);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(codes + t * 32 + 16);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        nf4_words_bf16<8>(w, amax[t * 4 + (kb & 3)], bt + t * 128, 0, t & 7);
+      } else {     // reduction row n, 64-column atom a (of 2)
+        const int n = t >> 1, a = t & 1;
+        const uint4 q0 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32 + 16);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        nf4_words_bf16<8>(w, amax[n * 4 + 2 * static_cast<int>(rank) + a], bt + a * (64 * 128) + n * 128, 0,
                           n & 7);
       }
       ptx::fence_proxy_async_smem();
