@@ -227,8 +227,14 @@ size_t sl_stack_workspace_size(const sl_stack* s, int64_t M, int32_t r);
  *  forward layers 0..L-1 from h0 [M, D] fp32 to hL [M, D] fp32, then
  *  backward L-1..0 from dh_top [M, D] fp32 to dh0 [M, D] fp32, writing for
  *  every layer l and projection p (index 7*l + p, order q k v o gate up down)
- *  dA[7l+p] [r, K_p] fp32 and dB[7l+p] [N_p, r] fp32 (overwritten).
- *  A[7l+p] [r, K_p] bf16 and B[7l+p] [N_p, r] bf16 are the adapters.
+ *  dA[7l+p] [r, K_p] fp32 and dB[7l+p] [N_p, r] fp32 (overwritten when
+ *  accumulate == 0, added to otherwise: gradient accumulation over
+ *  micro-batches, each of which re-streams the base -- "Exact Layer
+ *  Streaming ..." (abstract): accumulation is per-token I/O-neutral).
+ *  A[7l+p] [r, K_p] bf16 and B[7l+p] [N_p, r] bf16 are the adapters; r == 0
+ *  (A, B, dA, dB may then be NULL) runs the frozen base alone, the
+ *  adapters-off reference pass ("Soup CLI ...", "Key Takeaways": preference
+ *  training with the streamed base and adapters off).
  * The layer is the pre-norm decoder layer with token-local mixing described
  * in the library's design notes (RMS norm without weight, a = q*rep(k) +
  * rep(v), SiLU-gated MLP, fp32 residual stream, bf16 GEMM inputs/outputs).
@@ -243,7 +249,7 @@ sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64
                                const float* dh_top, const void* const* A,
                                const void* const* B, int32_t r, float alpha,
                                float* hL, float* dh0, float* const* dA, float* const* dB,
-                               void* ws, size_t ws_bytes, cudaStream_t stream);
+                               int32_t accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Host-side counters of the last step on this handle: bytes copied host to
  * device and the number of libsl kernels launched. */

@@ -63,7 +63,8 @@ _SIGS = {
     "sl_stack_create": (_I32, [ctypes.POINTER(sl_stack_desc), _P, _P, _P]),
     "sl_stack_destroy": (_I32, [_P]),
     "sl_stack_workspace_size": (_SZ, [_P, _I64, _I32]),
-    "sl_stream_stack_step": (_I32, [_P, _I32, _P, _I64, _P, _P, _P, _I32, _F, _P, _P, _P, _P, _P, _SZ, _P]),
+    "sl_stream_stack_step": (_I32, [_P, _I32, _P, _I64, _P, _P, _P, _I32, _F, _P, _P, _P, _P, _I32, _P, _SZ,
+                                    _P]),
     "sl_stack_last_step_stats": (_I32, [_P, _P, _P]),
     "sl_ce_fwd_bwd": (_I32, [_P, _I64, _I64, _P, _I64, _P, _I32, _I64, _P, _P, _P, _SZ, _P]),
     "sl_ce_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
@@ -261,16 +262,15 @@ class Stack:
     def workspace_size(self, M, r):
         return lib().sl_stack_workspace_size(self.handle, M, r)
 
-    def step(self, mode, h0, dh_top, A, B, r, alpha, hL, dh0, dA, dB, ws, stream=None):
+    def step(self, mode, h0, dh_top, A, B, r, alpha, hL, dh0, dA, dB, ws, accumulate=False, stream=None):
+        """One fwd+bwd step; A, B, dA, dB are lists of 7*L tensors (or None when r == 0)."""
         n = 7 * self.L
-        pa = (ctypes.c_void_p * n)(*[t.data_ptr() for t in A])
-        pb = (ctypes.c_void_p * n)(*[t.data_ptr() for t in B])
-        pga = (ctypes.c_void_p * n)(*[t.data_ptr() for t in dA])
-        pgb = (ctypes.c_void_p * n)(*[t.data_ptr() for t in dB])
+        arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts]) if ts is not None else None
         M = h0.shape[0]
-        _check(lib().sl_stream_stack_step(self.handle, mode, _ptr(h0), M, _ptr(dh_top), pa, pb, int(r),
-                                          float(alpha), _ptr(hL), _ptr(dh0), pga, pgb, _ptr(ws),
-                                          ws.numel() * ws.element_size(), _stream(stream)))
+        _check(lib().sl_stream_stack_step(self.handle, mode, _ptr(h0), M, _ptr(dh_top), arr(A), arr(B), int(r),
+                                          float(alpha), _ptr(hL), _ptr(dh0), arr(dA), arr(dB),
+                                          int(bool(accumulate)), _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream(stream)))
 
     def last_step_stats(self):
         a, b = ctypes.c_uint64(0), ctypes.c_uint64(0)

@@ -166,6 +166,7 @@ struct StepCtx {
   float* const* dA;
   float* const* dB;
   cudaStream_t stream;
+  int accumulate = 0;
   uint64_t kernels = 0;
 
   template <typename T>
@@ -266,22 +267,22 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
   uint16_t* dx1q = c.at<uint16_t>(P.dx1q);
   uint16_t* dx1k = c.at<uint16_t>(P.dx1k);
   uint16_t* dx1v = c.at<uint16_t>(P.dx1v);
-  SL_TRY(linear_bwd(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, T(6), dm, dA(6), dB(6), 0, lws,
+  SL_TRY(linear_bwd(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, T(6), dm, dA(6), dB(6), c.accumulate, lws,
                     lwb, c.stream));
   SL_TRY(glue_swiglu_bwd(dm, c.at<uint16_t>(P.g[l]), c.at<uint16_t>(P.u[l]), dg, du, M * s->F, c.stream));
-  SL_TRY(linear_bwd(&w[4], c.at<uint16_t>(P.x2[l]), dg, M, A(4), B(4), r, c.alpha, T(4), dx2a, dA(4), dB(4), 0,
+  SL_TRY(linear_bwd(&w[4], c.at<uint16_t>(P.x2[l]), dg, M, A(4), B(4), r, c.alpha, T(4), dx2a, dA(4), dB(4), c.accumulate,
                     lws, lwb, c.stream));
-  SL_TRY(linear_bwd(&w[5], c.at<uint16_t>(P.x2[l]), du, M, A(5), B(5), r, c.alpha, T(5), dx2b, dA(5), dB(5), 0,
+  SL_TRY(linear_bwd(&w[5], c.at<uint16_t>(P.x2[l]), du, M, A(5), B(5), r, c.alpha, T(5), dx2b, dA(5), dB(5), c.accumulate,
                     lws, lwb, c.stream));
   SL_TRY(glue_rms_bwd(dh2, dx2a, dx2b, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]), dh1, do_, M, D,
                       c.stream));
-  SL_TRY(linear_bwd(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, T(3), da, dA(3), dB(3), 0, lws,
+  SL_TRY(linear_bwd(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, T(3), da, dA(3), dB(3), c.accumulate, lws,
                     lwb, c.stream));
   SL_TRY(glue_mix_bwd(da, c.at<uint16_t>(P.q[l]), c.at<uint16_t>(P.k[l]), dq, dk, dv, M, D, Dkv, c.stream));
   const uint16_t* x1 = c.at<uint16_t>(P.x1[l]);
-  SL_TRY(linear_bwd(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, T(0), dx1q, dA(0), dB(0), 0, lws, lwb, c.stream));
-  SL_TRY(linear_bwd(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, T(1), dx1k, dA(1), dB(1), 0, lws, lwb, c.stream));
-  SL_TRY(linear_bwd(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, T(2), dx1v, dA(2), dB(2), 0, lws, lwb, c.stream));
+  SL_TRY(linear_bwd(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, T(0), dx1q, dA(0), dB(0), c.accumulate, lws, lwb, c.stream));
+  SL_TRY(linear_bwd(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, T(1), dx1k, dA(1), dB(1), c.accumulate, lws, lwb, c.stream));
+  SL_TRY(linear_bwd(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, T(2), dx1v, dA(2), dB(2), c.accumulate, lws, lwb, c.stream));
   SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, h_in, c.at<float>(P.rstd1[l]), dh, dh_bf16, M, D, c.stream));
   return SL_OK;
 }
@@ -392,7 +393,8 @@ extern "C" size_t sl_stack_workspace_size(const sl_stack* s, int64_t M, int32_t 
 extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64_t M,
                                           const float* dh_top, const void* const* A, const void* const* B,
                                           int32_t r, float alpha, float* hL, float* dh0, float* const* dA,
-                                          float* const* dB, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                                          float* const* dB, int32_t accumulate, void* ws, size_t ws_bytes,
+                                          cudaStream_t stream) {
   SL_REQUIRE(s, "sl_stream_stack_step: null stack");
   SL_REQUIRE(mode == SL_MODE_STREAMED || mode == SL_MODE_RESIDENT, "sl_stream_stack_step: bad mode");
   SL_REQUIRE(mode == SL_MODE_STREAMED || !s->dev.empty(), "sl_stream_stack_step: RESIDENT needs device_blobs");
@@ -406,6 +408,7 @@ extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float
   SL_REQUIRE(ws_bytes >= P.total, "sl_stream_stack_step: workspace too small (need " + std::to_string(P.total) +
                                       " bytes)");
   StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, stream};
+  c.accumulate = accumulate ? 1 : 0;
   const uint64_t launches0 = launch_count();
   const int L = s->L;
   const bool streamed = mode == SL_MODE_STREAMED;

@@ -138,3 +138,44 @@ def test_pageable_host_memory_rejected(gpu_lib):
     with pytest.raises(sl.SLError) as e:
         sl.Stack(sl.SL_WEIGHT_BF16, 256, 128, 512, [pageable])
     assert e.value.status == sl.SL_ERR_INVALID
+
+
+def test_gradient_accumulation_over_micro_batches(gpu_lib):
+    """accumulate=1 adds each micro-batch's adapter gradients; bytes streamed per token stay the same."""
+    sl = gpu_lib
+    S = Setup(sl, sl.SL_WEIGHT_NF4, L=3, M=64, D=256, Dkv=128, F=512, r=16, alpha=32.0, seed=31, with_oracle=False)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    batches = [(torch.randn(64, 256, generator=g, device="cuda"), torch.randn(64, 256, generator=g, device="cuda"))
+               for _ in range(2)]
+    hL, dh0 = torch.empty(64, 256, device="cuda"), torch.empty(64, 256, device="cuda")
+    S.run(sl.SL_MODE_STREAMED)                   # warm: layers 0 and 1 stay resident from here on
+    single = []
+    for h0, dh in batches:
+        dA = [torch.empty(a.shape, device="cuda") for a in S.A]
+        dB = [torch.empty(b.shape, device="cuda") for b in S.B]
+        S.stack.step(sl.SL_MODE_STREAMED, h0, dh, S.A, S.B, 16, 32.0, hL, dh0, dA, dB, S.ws)
+        single.append((dA, dB, S.stack.last_step_stats()[0]))
+    accA = [torch.empty(a.shape, device="cuda") for a in S.A]
+    accB = [torch.empty(b.shape, device="cuda") for b in S.B]
+    for i, (h0, dh) in enumerate(batches):
+        S.stack.step(sl.SL_MODE_STREAMED, h0, dh, S.A, S.B, 16, 32.0, hL, dh0, accA, accB, S.ws, accumulate=i > 0)
+    sl.sl_check_device_errors()
+    for j in range(len(S.A)):
+        assert torch.equal(accA[j], single[0][0][j] + single[1][0][j])
+        assert torch.equal(accB[j], single[0][1][j] + single[1][1][j])
+    assert single[0][2] == single[1][2]          # same streamed bytes for every micro-batch of M tokens
+    S.stack.close()
+
+
+def test_adapters_off_pass_equals_zero_B(gpu_lib):
+    """r = 0 runs the frozen base alone: the same hL and dh0 as adapters whose B is zero."""
+    sl = gpu_lib
+    S = Setup(sl, sl.SL_WEIGHT_NF4, L=2, M=96, D=256, Dkv=128, F=512, r=16, alpha=32.0, seed=41, with_oracle=False)
+    hL0, dh00 = torch.empty(96, 256, device="cuda"), torch.empty(96, 256, device="cuda")
+    S.stack.step(sl.SL_MODE_STREAMED, S.h0, S.dh, None, None, 0, 32.0, hL0, dh00, None, None, S.ws)
+    S.B = [torch.zeros_like(b) for b in S.B]
+    hL1, dh01, dA, dB = S.run(sl.SL_MODE_STREAMED)
+    assert torch.equal(hL0, hL1) and torch.equal(dh00, dh01)
+    assert all(torch.count_nonzero(a) == 0 for a in dA)      # dA = s (dY B)^T X = 0 when B = 0
+    assert all(torch.count_nonzero(b) > 0 for b in dB)
+    S.stack.close()
