@@ -105,17 +105,18 @@ sl_status sl_debug_timeout_probe(int64_t limit_ns, int32_t mbarrier, cudaStream_
 
 /* Kernel timing for measurement.  enable != 0 clears earlier records and
  * starts recording a CUDA event pair, on the launching stream, around every
- * tensor-core GEMM launch; enable == 0 stops recording.  Costs one event
- * pair per GEMM launch.  Variants: 0 NF4 forward, 1 NF4 dX, 2 bf16
- * forward, 3 bf16 dX, 4 CE logits (lse partials), 5 CE softmax chunk,
- * 6 CE dH accumulation. */
+ * tensor-core launch; enable == 0 stops recording.  Costs one event pair
+ * per launch.  Variants: 0 NF4 forward, 1 NF4 dX, 2 bf16 forward, 3 bf16
+ * dX, 4 CE logits (lse partials), 5 CE softmax chunk, 6 CE dH
+ * accumulation, 7 rank-r T = X A^T, 8 rank-r U = dY B, 9 rank-r dA / dB. */
 sl_status sl_kernel_timing(int32_t enable);
 
 /* Totals over the launches of one variant recorded since timing was
  * enabled: launch count, summed device time in ms (waits for the recorded
- * events) and algorithmic FLOPs (2 M N K, plus 2 M N r for the folded LoRA
- * side product). */
-sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms, double* flops);
+ * events) and algorithmic work: FLOPs for the GEMM variants 0-6 (2 M N K,
+ * plus 2 M N r for the folded LoRA side product), bytes for the rank-r
+ * passes 7-9 (the large operand once, the rank-r operands and the output). */
+sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms, double* work);
 
 /* ------------------------------------------------------------- NF4 (K0/K1) */
 
@@ -141,10 +142,11 @@ sl_status sl_nf4_dequantize(const uint8_t* codes, const float* absmax, int64_t N
  * X [M, K] bf16, A [r, K] bf16, B [N, r] bf16, Y [M, N] bf16 (fp32
  * accumulation, one rounding).  T_save [M, r] fp32 receives X A^T (kept for
  * the backward; the side product s T B^T is folded into the same
- * accumulator with fp32 accuracy); may be NULL only when r == 0.  r == 0 (or
- * A == B == NULL) computes the base alone -- the adapters-off pass.
- * r <= 32, r % 8 == 0.  `ws` must hold sl_lora_linear_workspace_size(M, N,
- * K, r) bytes (256-byte aligned; may be NULL when r == 0). */
+ * accumulator with fp32 accuracy); may be NULL only when r == 0; 16-byte
+ * aligned (it is read by TMA).  r == 0 (or A == B == NULL) computes the base
+ * alone -- the adapters-off pass.  r <= 32, r % 8 == 0.  The forward needs
+ * no scratch: `ws` may be NULL (the argument stays so that one buffer of
+ * sl_lora_linear_workspace_size bytes serves both directions). */
 sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M,
                              const void* A, const void* B, int32_t r, float alpha,
                              void* Y, void* T_save, void* ws, size_t ws_bytes,
@@ -154,9 +156,10 @@ sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M,
  *     U = dY B (fp32);  dX = dY W + s U A;  dA = s U^T X;  dB = s dY^T T_save,
  * T_save [M, r] fp32 from the forward.
  * dX [M, K] bf16 (may be NULL to skip); dA [r, K] and dB [N, r] fp32,
- * overwritten when accumulate == 0, added to otherwise.  Reductions over M
- * run in a fixed order: results are bitwise reproducible.  `ws` must hold
- * sl_lora_linear_workspace_size(M, N, K, r) bytes (256-byte aligned). */
+ * overwritten when accumulate == 0, added to otherwise.  Every reduction
+ * runs in a fixed order: results are bitwise reproducible.  `ws` must hold
+ * sl_lora_linear_workspace_size(M, N, K, r) bytes (256-byte aligned): it
+ * carries U between the rank-r passes. */
 sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M,
                              const void* A, const void* B, int32_t r, float alpha,
                              const void* T_save, void* dX, float* dA, float* dB,
@@ -183,8 +186,8 @@ sl_status sl_lora_linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t 
                                      const void* A, const void* B, int32_t r, float alpha,
                                      void* Y, void* T_save, cudaStream_t stream);
 
-/* Scratch bytes of one linear call (the forward and the backward of the same
- * shape can share one buffer); 0 when r == 0. */
+/* Scratch bytes of one linear call: the backward's U [M, r] fp32, rounded up
+ * to 256 (the forward needs none); 0 when r == 0. */
 size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r);
 
 /* ------------------------------------------------- streamed stack (a2-a7) */

@@ -130,6 +130,7 @@ def sl_debug_timeout_probe(limit_ns: int, mbarrier: bool = False, stream=None):
 
 
 GEMM_VARIANTS = ("nf4_fwd", "nf4_dx", "bf16_fwd", "bf16_dx", "ce_lse", "ce_softmax", "ce_dh")
+RANK_R_VARIANTS = ("rank_t", "rank_u", "rank_grad")  # timing variants 7, 8, 9 (work in bytes)
 
 
 def sl_kernel_timing(enable: bool):
@@ -137,7 +138,8 @@ def sl_kernel_timing(enable: bool):
 
 
 def sl_kernel_timing_read(variant: int):
-    """(launches, ms, flops) of one GEMM variant since timing was enabled."""
+    """(launches, ms, work) of one timed variant since timing was enabled:
+    work is FLOPs for GEMM variants 0-6 and bytes for rank-r variants 7-9."""
     n, ms, fl = ctypes.c_uint64(0), ctypes.c_double(0), ctypes.c_double(0)
     _check(lib().sl_kernel_timing_read(int(variant), ctypes.byref(n), ctypes.byref(ms), ctypes.byref(fl)))
     return n.value, ms.value, fl.value

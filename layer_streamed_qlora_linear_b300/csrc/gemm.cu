@@ -1,11 +1,15 @@
 // Host side of the tcgen05 GEMM: TMA tensor maps and launch dispatch.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
 #include "gemm.cuh"
 #include "gemm2.cuh"
+#include "gemm3.cuh"
+#include "timing.cuh"
+#include "tmap.cuh"
 
 namespace sl {
 
@@ -23,9 +27,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over a row-major matrix: inner extent `cols`, outer `rows`, row
-// pitch `pitch_bytes`; box (box_cols x box_rows).
-static sl_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+sl_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
                           uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
   if (!fn) return set_error(SL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -73,6 +75,25 @@ int variant_of(const GemmLaunch& g) {
 }
 }  // namespace
 
+TimingToken timing_begin(int variant, double work, cudaStream_t stream) {
+  TimingToken t;
+  std::lock_guard<std::mutex> lk(g_time_mu);
+  if (!g_time_on) return t;
+  t.start = pool_event();
+  t.stop = pool_event();
+  t.variant = variant;
+  t.work = work;
+  if (t.start) cudaEventRecord(t.start, stream);
+  return t;
+}
+
+void timing_end(const TimingToken& t, cudaStream_t stream) {
+  if (!t.start || !t.stop) return;
+  cudaEventRecord(t.stop, stream);
+  std::lock_guard<std::mutex> lk(g_time_mu);
+  g_timed.push_back(TimedLaunch{t.start, t.stop, t.variant, t.work});
+}
+
 // NF4 GEMM on CTA pairs (M = 256 per pair); used when M > 128.
 template <int BMN>
 static sl_status run_pair(const CUtensorMap& ma, const CUtensorMap& mc, const CUtensorMap& ms, const GemmArgs& a,
@@ -88,6 +109,52 @@ static sl_status run_pair(const CUtensorMap& ma, const CUtensorMap& mc, const CU
   dim3 grid(static_cast<unsigned>(2 * ceil_div(a.M, 256)), static_cast<unsigned>(ceil_div(a.N, kBN)));
   kern<<<grid, kGemm2Threads, Gemm2Cfg::kSmem, stream>>>(ma, mc, ms, a);
   return check_launch("gemm_nf4_pair_kernel");
+}
+
+// CTA pairs of the persistent kernel that the device holds at once (driver
+// query, once per device); the grid never exceeds it, so all clusters run
+// together and none waits for a second wave.
+template <int BMN>
+static int pair_clusters_resident() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms() / 2;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == 0) {
+    cudaFuncSetAttribute(gemm_nf4_pair_persistent_kernel<BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Gemm3Cfg::kSmem);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kGemm3Threads, 1, 1);
+    cfg.dynamicSmemBytes = Gemm3Cfg::kSmem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_nf4_pair_persistent_kernel<BMN>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    cached[dev] = std::min(n, num_sms() / 2);
+  }
+  return cached[dev];
+}
+
+// Persistent NF4 GEMM on CTA pairs: one cluster per SM pair walks its share
+// of the pair tiles.
+template <int BMN>
+static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, const CUtensorMap& ms,
+                                const GemmArgs& a, cudaStream_t stream) {
+  auto kern = gemm_nf4_pair_persistent_kernel<BMN>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  SL_CHECK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    SL_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gemm3Cfg::kSmem));
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int ntiles = ceil_div(a.M, 256) * ceil_div(a.N, kBN);
+  const int nclusters = std::min(ntiles, pair_clusters_resident<BMN>());
+  kern<<<dim3(static_cast<unsigned>(2 * nclusters)), kGemm3Threads, Gemm3Cfg::kSmem, stream>>>(ma, mc, ms, a);
+  return check_launch("gemm_nf4_pair_persistent_kernel");
 }
 
 template <int BSRC, int BMN, int EPI>
@@ -166,24 +233,20 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     }
     if (st != SL_OK) return st;
   }
-  TimedLaunch tl{nullptr, nullptr, 0, 0.0};
-  {
-    std::lock_guard<std::mutex> lk(g_time_mu);
-    if (g_time_on) {
-      tl.start = pool_event();
-      tl.stop = pool_event();
-      tl.variant = variant_of(g);
-      tl.flops = 2.0 * a.M * static_cast<double>(a.N) * a.K + 2.0 * a.M * static_cast<double>(a.N) * a.r;
-      if (tl.start) cudaEventRecord(tl.start, stream);
-    }
-  }
-  st = pair ? (g.bmn ? run_pair<1>(ma, mb, ms, a, stream) : run_pair<0>(ma, mb, ms, a, stream))
-            : dispatch(g, ma, mb, ms, stream);
-  if (tl.start && tl.stop) {
-    cudaEventRecord(tl.stop, stream);
-    std::lock_guard<std::mutex> lk(g_time_mu);
-    g_timed.push_back(tl);
-  }
+  TimingToken tl = timing_begin(variant_of(g),
+                                2.0 * a.M * static_cast<double>(a.N) * a.K + 2.0 * a.M * static_cast<double>(a.N) * a.r,
+                                stream);
+  // More pair tiles than resident clusters: the persistent kernel (its
+  // epilogue overlaps the next tile); one wave or less: one cluster per tile
+  // with the epilogue spread over all eight dequant warps.
+  const bool persistent =
+      pair && ceil_div(a.M, 256) * ceil_div(a.N, kBN) > (g.bmn ? pair_clusters_resident<1>() : pair_clusters_resident<0>());
+  if (persistent)
+    st = g.bmn ? run_persistent<1>(ma, mb, ms, a, stream) : run_persistent<0>(ma, mb, ms, a, stream);
+  else
+    st = pair ? (g.bmn ? run_pair<1>(ma, mb, ms, a, stream) : run_pair<0>(ma, mb, ms, a, stream))
+              : dispatch(g, ma, mb, ms, stream);
+  timing_end(tl, stream);
   return st;
 }
 
@@ -220,7 +283,7 @@ extern "C" sl_status sl_kernel_timing(int32_t enable) {
 }
 
 extern "C" sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms, double* flops) {
-  SL_REQUIRE(variant >= 0 && variant <= 6, "sl_kernel_timing_read: variant must be 0..6");
+  SL_REQUIRE(variant >= 0 && variant < kNumTimedVariants, "sl_kernel_timing_read: variant must be 0..9");
   std::lock_guard<std::mutex> lk(g_time_mu);
   uint64_t n = 0;
   double t = 0.0, f = 0.0;

@@ -1,0 +1,415 @@
+// Persistent fused NF4 GEMM on CTA pairs (tcgen05.mma.cta_group::2).
+//
+// The computation and the per-k-block pipeline are those of
+// gemm_nf4_pair_kernel (gemm2.cuh); this kernel adds:
+//   * persistence: one cluster (two SMs) per SM pair walks its share of the
+//     256 x 256 pair tiles; the stage ring runs on across tiles;
+//   * two TMEM accumulators (2 x 256 columns): four epilogue warps drain one
+//     while the MMAs of the next tile fill the other (acc_full / acc_empty);
+//   * the LoRA side product is folded after the last k-block of a tile from
+//     a dedicated shared-memory region that the epilogue warps fill while
+//     the tile's main loop runs (lora_full / lora_empty): no pipeline drain,
+//     and the dequant warps carry no LoRA state;
+// Warps: 0 A/code TMA producer, 1 MMA issuer (leader) or peer forwarder,
+// 2..9 NF4 dequant (two groups on alternate k-blocks), 10..13 LoRA staging +
+// epilogue.  Every wait is bounded.
+#pragma once
+#include "gemm2.cuh"
+
+namespace sl {
+
+constexpr int kNumEpi3 = 128;
+constexpr int kGemm3Threads = 64 + kNumDq2 + kNumEpi3;
+
+struct Gemm3Cfg {
+  static constexpr int S = 5;
+  static constexpr int kRawBytes = kHalfCodesBytes + kPairAbsBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + S * kATileBytes;
+  static constexpr int kOffLA = kOffB + S * kHalfBTileBytes;     // LoRA Xe [128 x 128 B]
+  static constexpr int kOffLB = kOffLA + kATileBytes;            // LoRA Be (K-major 128 rows / MN 2 atoms)
+  static constexpr int kOffRaw = kOffLB + kHalfBTileBytes;
+  static constexpr int kOffBar = kOffRaw + S * kRawBytes;
+  static constexpr int kNumBars = 5 * S + 7;
+  static constexpr int kOffSink = (kOffBar + kNumBars * 8 + 15) / 16 * 16;
+  static constexpr int kOffMisc = kOffSink + 16;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kSmem = kBytes + 1024;
+};
+
+// Barrier of the four epilogue warps only (named barrier 1).
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kNumEpi3) : "memory"); }
+
+template <int BMN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
+    gemm_nf4_pair_persistent_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
+                                    const __grid_constant__ CUtensorMap map_s, const GemmArgs args) {
+  using Cfg = Gemm3Cfg;
+  constexpr int S = Cfg::S;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + Cfg::kOffA;
+  uint8_t* sB = smem + Cfg::kOffB;
+  uint8_t* sLA = smem + Cfg::kOffLA;
+  uint8_t* sLB = smem + Cfg::kOffLB;
+  uint8_t* sRaw = smem + Cfg::kOffRaw;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
+  uint64_t* full = bars;                 // [S] leader: A tiles of both CTAs landed
+  uint64_t* raw_full = bars + S;         // [S] each CTA: codes + absmax landed
+  uint64_t* b_local = bars + 2 * S;      // [S] each CTA: its B half dequantised (4 warps of one group)
+  uint64_t* empty = bars + 3 * S;        // [S] each CTA: stage consumed by the MMAs
+  uint64_t* b_peer = bars + 4 * S;       // [S] leader: the peer's B half dequantised
+  uint64_t* lora_full = bars + 5 * S;    // leader: both CTAs staged this tile's LoRA operands
+  uint64_t* lora_empty = lora_full + 1;  // each CTA: the fold MMAs of the previous tile are done with them
+  uint64_t* acc_full = lora_full + 2;    // [2] each CTA: accumulator a holds a finished segment
+  uint64_t* acc_empty = lora_full + 4;   // [2] leader: both CTAs' epilogues drained accumulator a
+  uint64_t* drain = lora_full + 6;       // leader, failure path only: issued MMAs completed
+  uint8_t* sink = smem + Cfg::kOffSink;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  volatile int* epi_stop = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int mpairs = (args.M + 255) / 256;
+  const int ntiles_n = (args.N + kBN - 1) / kBN;
+  const int ntiles = mpairs * ntiles_n;
+  const int KB = (args.K + kBK - 1) / kBK;
+  const bool has_lora = args.lora_x != nullptr && args.r > 0;
+  // pair tile t -> (m pair, n tile); concurrent clusters share the n tile (weight reuse in L2)
+  auto tile_m0 = [&](int t) { return (t % mpairs) * 256 + static_cast<int>(rank) * 128; };
+  auto tile_n0 = [&](int t) { return (t / mpairs) * kBN; };
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&raw_full[i], 1);
+      ptx::mbar_init(&b_local[i], kNumDq2 / 64);
+      ptx::mbar_init(&empty[i], 1);
+      ptx::mbar_init(&b_peer[i], 1);
+    }
+    ptx::mbar_init(lora_full, 2 * (kNumEpi3 / 32));
+    ptx::mbar_init(lora_empty, 1);
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&acc_full[a], 1);
+      ptx::mbar_init(&acc_empty[a], 2 * (kNumEpi3 / 32));
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *epi_stop = 0;
+    ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&map_a);
+    ptx::tma_prefetch_desc(&map_c);
+    ptx::tma_prefetch_desc(&map_s);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_holder, 512);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    report_device_error(args.err, SL_ERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint32_t rawtx = kHalfCodesBytes + (BMN ? kBK * 16 : 128 * 16);
+      int g = 0;  // k-blocks issued by this cluster
+      bool ok = true;
+      for (int t = cluster; ok && t < ntiles; t += nclusters) {
+        const int m0 = tile_m0(t), n0 = tile_n0(t), nh = n0 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % S;
+          if (!ptx::mbar_wait_cluster(&empty[s], ((g / S) & 1) ^ 1, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          if (leader) ptx::mbar_arrive_expect_tx(&full[s], 2 * kATileBytes);
+          ptx::tma_load_2d_pair(sA + s * kATileBytes, &map_a, ptx::map_to_rank(&full[s], 0), kb * kBK, m0);
+          uint8_t* raw = sRaw + s * Cfg::kRawBytes;
+          ptx::mbar_arrive_expect_tx(&raw_full[s], rawtx);
+          if (!BMN) {
+            ptx::tma_load_2d(raw, &map_c, &raw_full[s], kb * (kBK / 2), nh);
+            ptx::tma_load_2d(raw + kHalfCodesBytes, &map_s, &raw_full[s], kb & ~3, nh);
+          } else {
+            ptx::tma_load_2d(raw, &map_c, &raw_full[s], nh / 2, kb * kBK);
+            ptx::tma_load_2d(raw + kHalfCodesBytes, &map_s, &raw_full[s], n0 / 64, kb * kBK);
+          }
+        }
+      }
+      if (!ok) {
+        for (int k = (g > S ? g - S : 0); k < g; ++k) ptx::mbar_wait_cluster(&raw_full[k % S], (k / S) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = ptx::idesc_bf16(256, kBN, 0, BMN);
+      const uint32_t a_base = ptx::smem_addr(sA);
+      const uint32_t b_base = ptx::smem_addr(sB);
+      const uint32_t la = ptx::smem_addr(sLA);
+      const uint32_t lb = ptx::smem_addr(sLB);
+      const int ksteps = has_lora ? (2 * args.r + 15) / 16 : 0;
+      int g = 0, it = 0;
+      bool ok = true;
+      for (int t = cluster; ok && t < ntiles; t += nclusters, ++it) {
+        const int acc = it & 1;
+        const uint32_t d = tmem + static_cast<uint32_t>(acc * kBN);
+        if (!ptx::mbar_wait_cluster(&acc_empty[acc], ((it >> 1) & 1) ^ 1, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        uint32_t accum = 0;
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % S;
+          const uint32_t ph = (g / S) & 1;
+          if (!ptx::mbar_wait_cluster(&full[s], ph, abort_flag) || !ptx::mbar_wait(&b_local[s], ph, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&b_peer[s], 16);
+          if (!ptx::mbar_wait_cluster(&b_peer[s], ph, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = ptx::smem_desc(a_base + s * kATileBytes + kk * 32, 16, 1024, 2);
+            const uint64_t bd = BMN ? ptx::smem_desc(b_base + s * kHalfBTileBytes + kk * 2048, 64 * 128, 1024, 2)
+                                    : ptx::smem_desc(b_base + s * kHalfBTileBytes + kk * 32, 16, 1024, 2);
+            ptx::mma_bf16_pair(d, ad, bd, idesc, accum);
+            accum = 1;
+          }
+          ptx::mma_commit_pair(&empty[s], 0x3);
+        }
+        if (!ok) break;
+        if (has_lora) {  // fold the LoRA side product into this accumulator
+          if (!ptx::mbar_wait_cluster(lora_full, it & 1, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t ad = ptx::smem_desc(la + kk * 32, 16, 1024, 2);
+            const uint64_t bd = BMN ? ptx::smem_desc(lb + kk * 2048, 64 * 128, 1024, 2)
+                                    : ptx::smem_desc(lb + kk * 32, 16, 1024, 2);
+            ptx::mma_bf16_pair(d, ad, bd, idesc, 1u);
+          }
+          ptx::mma_commit_pair(lora_empty, 0x3);
+        }
+        ptx::mma_commit_pair(&acc_full[acc], 0x3);
+      }
+      if (!ok) {  // let the MMAs already issued finish before teardown
+        ptx::mma_commit_pair(drain, 0x1);
+        ptx::mbar_wait(drain, 0, nullptr);
+      }
+    } else if (lane == 0) {
+      // -------------------------------------------------- peer: B-ready forwarder
+      const uint32_t leader_b_peer = ptx::map_to_rank(&b_peer[0], 0);
+      const uint32_t leader_sink = ptx::map_to_rank(sink, 0);
+      int g = 0;
+      bool ok = true;
+      for (int t = cluster; ok && t < ntiles; t += nclusters) {
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % S;
+          if (!ptx::mbar_wait(&b_local[s], (g / S) & 1, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          ptx::bulk_signal_16(leader_sink, sink, leader_b_peer + s * 8);
+        }
+      }
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------- NF4 dequant (each CTA, 256 threads)
+    const int dq = tid - 64;
+    const int grp = (warp - 2) >> 2;
+    const int tr = dq & 127;
+    int g = 0;
+    bool ok = true;
+    for (int t = cluster; ok && t < ntiles; t += nclusters) {
+      // two groups of four warps take alternate k-blocks (cluster counter g)
+      for (int kb = 0; kb < KB; ++kb, ++g) {
+        if ((g & 1) != grp) continue;
+        const int s = g % S;
+        if (!ptx::mbar_wait_cluster(&raw_full[s], (g / S) & 1, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        const uint8_t* codes = sRaw + s * Cfg::kRawBytes;
+        const float* amax = reinterpret_cast<const float*>(codes + kHalfCodesBytes);
+        uint8_t* bt = sB + s * kHalfBTileBytes;
+        if (!BMN) {
+          const uint4 q0 = *reinterpret_cast<const uint4*>(codes + tr * 32);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(codes + tr * 32 + 16);
+          const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          nf4_words_bf16<8>(w, amax[tr * 4 + (kb & 3)], bt + tr * 128, 0, tr & 7);
+        } else {
+          const int n = tr >> 1, a = tr & 1;
+          const uint4 q0 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32 + 16);
+          const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          nf4_words_bf16<8>(w, amax[n * 4 + 2 * static_cast<int>(rank) + a], bt + a * (64 * 128) + n * 128, 0,
+                            n & 7);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&b_local[s]);
+      }
+    }
+  } else {
+    // ------------------------------------- LoRA staging + epilogue (each CTA, 128 threads)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    const int e = tid - (64 + kNumDq2);  // 0..127
+    const uint32_t acc_empty_leader = ptx::map_to_rank(&acc_empty[0], 0);
+    const uint32_t lora_full_leader = ptx::map_to_rank(lora_full, 0);
+    uint16_t* out = reinterpret_cast<uint16_t*>(args.out);
+    const int r = args.r;
+    const int nr = r / 8;  // r % 8 == 0, so 2r is a whole number of k16 steps: no padding
+    auto chunk_at = [&](uint8_t* base, int rw, int c) {
+      return reinterpret_cast<uint4*>(base + rw * 128 + ((c ^ (rw & 7)) << 4));
+    };
+    auto mn_chunk = [&](uint8_t* bt, int i, int cc) {  // cc: 0..15 over two 64-column atoms
+      return reinterpret_cast<uint4*>(bt + (cc >> 3) * (64 * 128) + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
+    };
+    // Xe = [s T_hi | s T_lo] (row e of this CTA's 128 rows), Be = [B | B] for
+    // this CTA's 128 output columns, in the operand layouts of the main loop.
+    auto stage_lora = [&](int t) {
+      const int gm = tile_m0(t) + e;
+      const int nh = tile_n0(t) + static_cast<int>(rank) * 128;
+      for (int gi = 0; gi < nr; ++gi) {
+        float v[8];
+        if (gm < args.M) {
+          const float4* p = reinterpret_cast<const float4*>(args.lora_x + static_cast<int64_t>(gm) * r + gi * 8);
+          const float4 a0 = p[0], a1 = p[1];
+          v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w; v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+        }
+        uint4 hi, lo;
+        uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
+        uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float x0 = v[2 * k] * args.s, x1 = v[2 * k + 1] * args.s;
+          ph[k] = pack_bf16x2(x0, x1);
+          pl[k] = pack_bf16x2(x0 - bf16_lo(ph[k]), x1 - bf16_hi(ph[k]));
+        }
+        *chunk_at(sLA, e, gi) = hi;
+        *chunk_at(sLA, e, nr + gi) = lo;
+      }
+      if (!BMN) {
+        const int gn = nh + e;
+        for (int gi = 0; gi < nr; ++gi) {
+          uint4 b = make_uint4(0, 0, 0, 0);
+          if (gn < args.N) b = *reinterpret_cast<const uint4*>(args.lora_w + static_cast<int64_t>(gn) * r + gi * 8);
+          *chunk_at(sLB, e, gi) = b;
+          *chunk_at(sLB, e, nr + gi) = b;
+        }
+      } else {
+        for (int task = e; task < r * 16; task += kNumEpi3) {
+          const int i = task >> 4, cc = task & 15, gcol = nh + cc * 8;
+          uint4 b = make_uint4(0, 0, 0, 0);
+          if (gcol < args.N) b = *reinterpret_cast<const uint4*>(args.lora_w + static_cast<int64_t>(i) * args.N + gcol);
+          *mn_chunk(sLB, i, cc) = b;
+          *mn_chunk(sLB, r + i, cc) = b;
+        }
+      }
+    };
+    // bf16 store of the finished columns c0 .. c0+31 of this thread's row
+    auto store32 = [&](int gm, int n0, int c0, const float (&v)[32]) {
+      if (gm < args.M && n0 + c0 < args.N) {
+        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(gm) * args.ld_out + n0 + c0);
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          uint4 o;
+          o.x = pack_bf16x2(v[8 * g4 + 0], v[8 * g4 + 1]);
+          o.y = pack_bf16x2(v[8 * g4 + 2], v[8 * g4 + 3]);
+          o.z = pack_bf16x2(v[8 * g4 + 4], v[8 * g4 + 5]);
+          o.w = pack_bf16x2(v[8 * g4 + 6], v[8 * g4 + 7]);
+          dst[g4] = o;
+        }
+      }
+    };
+    // The four epilogue warps leave the loop together (they share named
+    // barrier 1): a warp whose wait failed raises epi_stop before the first
+    // barrier; every warp reads it between the two.
+    auto agree = [&](bool ok_w) {
+      if (!ok_w && lane == 0) *epi_stop = 1;
+      epi_bar_sync();
+      const bool go = *epi_stop == 0;
+      epi_bar_sync();
+      return go;
+    };
+    int it = 0;
+    for (int t = cluster; t < ntiles; t += nclusters, ++it) {
+      const int acc = it & 1;
+      if (has_lora) {
+        // the region is free once the previous tile's fold MMAs completed
+        bool free_ = ptx::mbar_wait_cluster_backoff(lora_empty, (it & 1) ^ 1, abort_flag) && !*abort_flag;
+        free_ = __all_sync(0xffffffffu, free_);
+        if (!free_ && !*abort_flag) give_up();
+        if (!agree(free_)) break;
+        stage_lora(t);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(lora_full_leader);
+      }
+      bool ready = ptx::mbar_wait_cluster_backoff(&acc_full[acc], (it >> 1) & 1, abort_flag) && !*abort_flag;
+      ready = __all_sync(0xffffffffu, ready);
+      if (!ready && !*abort_flag) give_up();
+      if (!agree(ready)) break;
+      ptx::tc_fence_after();
+      const int gm = tile_m0(t) + row;
+      const int n0 = tile_n0(t);
+      const uint32_t t_row = tmem + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(t_row + c0, u);
+        ptx::tmem_wait_ld();
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+        store32(gm, n0, c0, v);
+      }
+      // accumulator drained: let the leader reuse it
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_leader + acc * 8);
+    }
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+}  // namespace sl

@@ -2,18 +2,21 @@
 //
 // "Exact Layer Streaming ..." (abstract): LoRA training with the base frozen
 // in NF4; only the adapters A [r, K] and B [N, r] learn.
-//   forward   T = X A^T (K2, here);  Y = X W^T + s T B^T (one fused tcgen05 GEMM)
-//   backward  U = dY B (K4, here);   dX = dY W + s U A (one fused GEMM)
-//             dA = s U^T X, dB = s dY^T T (K6, here; fp32, fixed-order sums)
-// The skinny kernels are HBM-bound streams over X / dY; the rank-r operand
-// is staged in shared memory and every reduction runs in a fixed order so
-// that results are bitwise reproducible.
+//   forward   T = X A^T;  Y = X W^T + s T B^T (one fused tcgen05 GEMM)
+//   backward  U = dY B;   dX = dY W + s U A (one fused GEMM)
+//             dA = s U^T X, dB = s dY^T T
+// The rank-r products run as single tcgen05 launches (skinny.cu) with
+// fixed-order cluster reductions, so results are bitwise reproducible.  The
+// CUDA-core rank-r kernels below serve only the allocation-free forward,
+// whose K-split partials live in a fixed device array.
+#include <algorithm>
 #include <mutex>
 #include <string>
 
 #include "common.cuh"
 #include "gemm.cuh"
 #include "linear.cuh"
+#include "skinny.cuh"
 
 namespace sl {
 
@@ -28,7 +31,7 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// -------------------------------------------------------------- K2 / K4
+// ------------------------------------------- CUDA-core T (allocation-free forward)
 // part[split][m][i] = sum_{k in split} X[m, k] * W(i, k), fp32.
 // W(i, k) = Wp[i * K + k] (kWT == 0: A [r, K]) or Wp[k * r + i] (kWT == 1: B [N, r]).
 // Block: 128 threads, 32 rows x 512 columns of X staged in shared memory by
@@ -133,123 +136,13 @@ __global__ void sum_splits_kernel(const float* __restrict__ part, int splits, in
   }
 }
 
-// ------------------------------------------------------------------- K6
-// part[split][i][k] = sum_{m in split} P[m, i] * Q[m, k]  (fixed m order)
-// Block: 256 threads = 256 columns of Q; rows of the split in tiles of 64,
-// double-buffered through shared memory by cp.async; thread = one column,
-// all R rank entries.
-constexpr int kGrRows = 64;
-constexpr int kGrCols = 256;
-constexpr int kGrPad = 8;
-
-template <int R>
-__global__ void __launch_bounds__(256) lora_grad_kernel(const float* __restrict__ P, const uint16_t* __restrict__ Q,
-                                                        int64_t M, int Kq, int r, int64_t rows_per_split,
-                                                        float* __restrict__ part) {
-  extern __shared__ __align__(16) uint8_t dsm[];
-  constexpr int kQTile = kGrRows * (kGrCols + kGrPad);  // bf16 elements per stage
-  uint16_t* qs = reinterpret_cast<uint16_t*>(dsm);                        // [2][64][256 + 8]
-  float* ps = reinterpret_cast<float*>(dsm + 2 * kQTile * 2);             // [2][64][R]
-  const int tid = threadIdx.x;
-  const int c0 = blockIdx.x * kGrCols;
-  const int64_t mb = blockIdx.y * rows_per_split;
-  const int64_t me = (mb + rows_per_split < M) ? mb + rows_per_split : M;
-  const int ntiles = static_cast<int>((me - mb + kGrRows - 1) / kGrRows);
-
-  auto issue = [&](int t, int buf) {
-    const int64_t r0 = mb + static_cast<int64_t>(t) * kGrRows;
-    uint16_t* qd = qs + buf * kQTile;
-    for (int c = tid; c < kGrRows * (kGrCols / 8); c += 256) {
-      const int row = c / (kGrCols / 8), ch = c % (kGrCols / 8);
-      const bool ok = (r0 + row < me) && (c0 + ch * 8 < Kq);
-      const uint16_t* src = ok ? Q + (r0 + row) * Kq + c0 + ch * 8 : Q;
-      cp_async16(qd + row * (kGrCols + kGrPad) + ch * 8, src, ok);
-    }
-    float* pd = ps + buf * kGrRows * R;
-    for (int c = tid; c < kGrRows * R / 4; c += 256) {
-      const int row = (c * 4) / R, i0 = (c * 4) % R;
-      const bool ok = (r0 + row < me) && (i0 < r);
-      const float* src = ok ? P + (r0 + row) * r + i0 : P;
-      cp_async16(pd + row * R + i0, src, ok);
-    }
-    cp_async_commit();
-  };
-
-  float acc[R];
-#pragma unroll
-  for (int i = 0; i < R; ++i) acc[i] = 0.0f;
-  if (ntiles > 0) issue(0, 0);
-  for (int t = 0; t < ntiles; ++t) {
-    const int buf = t & 1;
-    if (t + 1 < ntiles) {
-      issue(t + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint16_t* qd = qs + buf * kQTile + tid;
-    const float* pd = ps + buf * kGrRows * R;
-    const int nrow = static_cast<int>((me - (mb + static_cast<int64_t>(t) * kGrRows)) < kGrRows
-                                          ? (me - (mb + static_cast<int64_t>(t) * kGrRows))
-                                          : kGrRows);
-    for (int row = 0; row < nrow; ++row) {
-      const float q = bf16_to_f32(qd[row * (kGrCols + kGrPad)]);
-#pragma unroll
-      for (int i = 0; i < R; i += 4) {
-        const float4 p = *reinterpret_cast<const float4*>(pd + row * R + i);
-        acc[i] = fmaf(p.x, q, acc[i]);
-        acc[i + 1] = fmaf(p.y, q, acc[i + 1]);
-        acc[i + 2] = fmaf(p.z, q, acc[i + 2]);
-        acc[i + 3] = fmaf(p.w, q, acc[i + 3]);
-      }
-    }
-    __syncthreads();
-  }
-  const int col = c0 + tid;
-  if (col < Kq) {
-#pragma unroll
-    for (int i = 0; i < R; ++i)
-      if (i < r) part[(static_cast<int64_t>(blockIdx.y) * r + i) * Kq + col] = acc[i];
-  }
-}
-
-// out = (accumulate ? out : 0) + s * sum_split part[split]   (fixed split order)
-// transpose: out[k * r + i] (dB [N, r]) instead of out[i * Kq + k] (dA [r, K]).
-__global__ void lora_grad_reduce_kernel(const float* __restrict__ part, int splits, int r, int Kq, float s,
-                                        float* __restrict__ out, int transpose, int accumulate) {
-  const int64_t total = static_cast<int64_t>(r) * Kq;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-    const int64_t i = idx / Kq, k = idx % Kq;
-    float v = 0.0f;
-    for (int sp = 0; sp < splits; ++sp) v += part[(static_cast<int64_t>(sp) * r + i) * Kq + k];
-    v *= s;
-    const int64_t o = transpose ? k * r + i : idx;
-    out[o] = accumulate ? out[o] + v : v;
-  }
-}
-
 static int rank_bucket(int r) { return r <= 8 ? 8 : (r <= 16 ? 16 : 32); }
 
 int down_splits(int64_t K) { return static_cast<int>(ceil_div(K, kDnCols)); }
 
-// Splits of the M reduction for dA/dB: enough blocks to cover the SMs twice.
-int grad_splits(int64_t M, int64_t Kq) {
-  const int64_t slabs = ceil_div(Kq, kGrCols);
-  int64_t s = ceil_div(2 * 148, slabs);
-  const int64_t cap = ceil_div(M, kGrRows);
-  if (s > cap) s = cap;
-  return static_cast<int>(s < 1 ? 1 : s);
-}
-
 static size_t down_smem(int R) {
   return (static_cast<size_t>(kDnRows) * (kDnCols + kDnPad) + static_cast<size_t>(R) * (kDnCols + kDnPad)) * 2;
 }
-static size_t grad_smem(int R) {
-  return 2 * static_cast<size_t>(kGrRows) * (kGrCols + kGrPad) * 2 + 2 * static_cast<size_t>(kGrRows) * R * 4;
-}
-
 template <typename Kern>
 static sl_status set_smem(Kern k, size_t bytes) {
   static bool done[64] = {false};
@@ -290,57 +183,18 @@ sl_status lora_down(const uint16_t* X, int64_t M, int K, const uint16_t* W, int 
   return check_launch("sum_splits_kernel");
 }
 
-sl_status lora_grad(const float* P, const uint16_t* Q, int64_t M, int Kq, int r, float s, float* out,
-                    int transpose, int accumulate, float* part, cudaStream_t stream) {
-  const int splits = grad_splits(M, Kq);
-  const int64_t rps = ceil_div(ceil_div(M, splits), kGrRows) * kGrRows;
-  dim3 grid(static_cast<unsigned>(ceil_div(Kq, kGrCols)), static_cast<unsigned>(splits));
-  const int R = rank_bucket(r);
-  const size_t sm = grad_smem(R);
-#define SL_GRAD(RR)                                                                    \
-  do {                                                                                 \
-    static bool attr = false;                                                          \
-    if (!attr) {                                                                       \
-      sl_status st_ = set_smem(lora_grad_kernel<RR>, sm);                              \
-      if (st_ != SL_OK) return st_;                                                    \
-      attr = true;                                                                     \
-    }                                                                                  \
-    lora_grad_kernel<RR><<<grid, 256, sm, stream>>>(P, Q, M, Kq, r, rps, part);        \
-  } while (0)
-  if (R == 8) SL_GRAD(8);
-  else if (R == 16) SL_GRAD(16);
-  else SL_GRAD(32);
-#undef SL_GRAD
-  sl_status st = check_launch("lora_grad_kernel");
-  if (st != SL_OK) return st;
-  const int64_t total = static_cast<int64_t>(r) * Kq;
-  int grid2 = static_cast<int>(ceil_div(total, 256));
-  if (grid2 > num_sms() * 8) grid2 = num_sms() * 8;
-  lora_grad_reduce_kernel<<<grid2, 256, 0, stream>>>(part, splits, r, Kq, s, out, transpose, accumulate);
-  return check_launch("lora_grad_reduce_kernel");
-}
-
-// Workspace of one linear (forward and backward share it):
-//   U [M, r] fp32 | rank-r partials (down_splits x M x r) | dA partials | dB partials
+// Workspace of one linear: U [M, r] fp32 (backward only; the forward needs none).
 struct LinWs {
-  size_t U, dpart, partA, partB, total;
+  size_t U, total;
 };
 
 static LinWs lin_ws(int64_t M, int64_t N, int64_t K, int r) {
+  (void)N;
+  (void)K;
   LinWs w{};
   if (r <= 0) return w;
-  size_t off = 0;
-  auto take = [&](size_t b) {
-    const size_t o = off;
-    off = align_up(off + b, 256);
-    return o;
-  };
-  const int ds = down_splits(K) > down_splits(N) ? down_splits(K) : down_splits(N);
-  w.U = take(static_cast<size_t>(M) * r * 4);
-  w.dpart = take(static_cast<size_t>(ds) * M * r * 4);
-  w.partA = take(static_cast<size_t>(grad_splits(M, K)) * r * K * 4);
-  w.partB = take(static_cast<size_t>(grad_splits(M, N)) * r * N * 4);
-  w.total = off;
+  w.U = 0;
+  w.total = align_up(static_cast<size_t>(M) * r * 4, 256);
   return w;
 }
 
@@ -370,15 +224,13 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
   const bool lora = r > 0 && A && B;
   SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32 && T_save), "sl_lora_linear_fwd: need r % 8 == 0, r <= 32, T_save");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_fwd: M too large");
-  const LinWs L = lin_ws(M, w->N, w->K, lora ? r : 0);
-  SL_REQUIRE(!lora || (ws && ws_bytes >= L.total), "sl_lora_linear_fwd: workspace too small");
-  SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_lora_linear_fwd: workspace must be 256-byte aligned");
+  (void)ws;
+  (void)ws_bytes;
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   if (lora) {
-    st = lora_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A), 0, r,
-                   static_cast<float*>(T_save), reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.dpart),
-                   stream);
+    st = skinny_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A), 0, r,
+                     static_cast<float*>(T_save), stream);
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
@@ -415,22 +267,17 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   SL_REQUIRE(!lora || (X && T_save && dA && dB), "sl_lora_linear_bwd: LoRA backward needs X, T_save, dA, dB");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_bwd: M too large");
   const LinWs L = lin_ws(M, w->N, w->K, lora ? r : 0);
-  const size_t need = L.total;
-  SL_REQUIRE(ws_bytes >= need && (need == 0 || ws), "sl_lora_linear_bwd: workspace too small");
+  SL_REQUIRE(ws_bytes >= L.total && (L.total == 0 || ws), "sl_lora_linear_bwd: workspace too small");
   SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_lora_linear_bwd: workspace must be 256-byte aligned");
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   uint8_t* p = static_cast<uint8_t*>(ws);
   float* U = nullptr;
-  float* partA = nullptr;
-  float* partB = nullptr;
   if (lora) {
     U = reinterpret_cast<float*>(p + L.U);
-    partA = reinterpret_cast<float*>(p + L.partA);
-    partB = reinterpret_cast<float*>(p + L.partB);
-    // U = dY B : W(i, n) = B[n * r + i]
-    st = lora_down(static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), static_cast<const uint16_t*>(B), 1,
-                   r, U, reinterpret_cast<float*>(p + L.dpart), stream);
+    // U = dY B
+    st = skinny_down(static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), static_cast<const uint16_t*>(B), 1,
+                     r, U, stream);
     if (st != SL_OK) return st;
   }
   if (dX) {
@@ -460,11 +307,11 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   }
   if (lora) {
     const float s = alpha / static_cast<float>(r);
-    st = lora_grad(U, static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), r, s, dA, 0, accumulate, partA,
-                   stream);
+    // dA [r, K] = s U^T X;  dB [N, r] = s dY^T T
+    st = skinny_grad(U, static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), r, s, dA, 1, accumulate, stream);
     if (st != SL_OK) return st;
-    st = lora_grad(static_cast<const float*>(T_save), static_cast<const uint16_t*>(dY), M,
-                   static_cast<int>(w->N), r, s, dB, 1, accumulate, partB, stream);
+    st = skinny_grad(static_cast<const float*>(T_save), static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), r,
+                     s, dB, 0, accumulate, stream);
     if (st != SL_OK) return st;
   }
   return SL_OK;

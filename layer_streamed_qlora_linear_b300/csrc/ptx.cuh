@@ -176,6 +176,19 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
   }
 }
+// As mbar_wait_cluster, for waiters off the critical path (epilogue warps):
+// sleeps between polls so the spinning warps leave issue slots to the
+// dequantising warps of the same SM.
+__device__ __forceinline__ bool mbar_wait_cluster_backoff(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(200);
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
 // TMA load whose completion is counted on an mbarrier of either CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
                                                  int32_t x, int32_t y) {

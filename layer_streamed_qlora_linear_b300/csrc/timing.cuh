@@ -1,0 +1,21 @@
+// Optional CUDA-event timing of libsl's launches (sl_kernel_timing).
+#pragma once
+#include "common.cuh"
+
+namespace sl {
+
+// Variants: 0..6 tensor-core GEMMs (see sl_kernel_timing), 7 rank-r T = X A^T,
+// 8 rank-r U = dY B, 9 rank-r dA / dB.
+constexpr int kNumTimedVariants = 10;
+
+struct TimingToken {
+  cudaEvent_t start = nullptr, stop = nullptr;
+  int variant = 0;
+  double work = 0.0;  // algorithmic FLOPs (GEMMs) or bytes (rank-r passes)
+};
+
+// No-ops (null events) unless timing is enabled.
+TimingToken timing_begin(int variant, double work, cudaStream_t stream);
+void timing_end(const TimingToken& t, cudaStream_t stream);
+
+}  // namespace sl

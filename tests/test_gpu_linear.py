@@ -96,3 +96,28 @@ def test_bounded_wait_times_out_without_fault(gpu_lib):
         gpu_lib.sl_check_device_errors()          # cleared; the context is still usable
     x = torch.ones(4, device="cuda")
     assert float(x.sum()) == 4.0
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 2560), (300, 1248, 2048)])
+def test_pair_gemm_tile_walk_matches_oracle(gpu_lib, M, N, K):
+    """The CTA-pair NF4 GEMM at sizes where tiles outnumber the SM pairs
+    (80 pair tiles on 74: some clusters run two tiles, alternating their
+    TMEM accumulators and LoRA staging) and with a ragged M pair and a
+    partial N tile; bitwise repeatable, and the forward ignores `ws`."""
+    r, alpha = 16, 32.0
+    c, W_ref, w, t = make(gpu_lib, 11, M, N, K, r, "nf4")
+    a = run(gpu_lib, w, t, M, N, K, r, alpha)
+    b = run(gpu_lib, w, t, M, N, K, r, alpha)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    T = torch.empty(M, r, dtype=torch.float32, device="cuda")
+    gpu_lib.sl_lora_linear_fwd(w, t["X"], t["A"], t["B"], r, alpha, Y, T, None)
+    gpu_lib.sl_check_device_errors()
+    assert torch.equal(Y, a[0]) and torch.equal(T, a[1])
+    Yo = lora.lora_linear_fwd(c["X"], W_ref, c["A"], c["B"], alpha)
+    dXo, dAo, dBo = lora.lora_linear_bwd(c["X"], c["dY"], W_ref, c["A"], c["B"], alpha)
+    assert rel_fro(host(a[0]), Yo) <= BF16_TOL
+    assert rel_fro(host(a[2]), dXo) <= BF16_TOL
+    assert rel_fro(host(a[3]), dAo) <= BF16_TOL
+    assert rel_fro(host(a[4]), dBo) <= BF16_TOL
