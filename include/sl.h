@@ -190,6 +190,41 @@ sl_status sl_lora_linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t 
  * to 256 (the forward needs none); 0 when r == 0. */
 size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r);
 
+/* ------------------------------------------------------ projection groups */
+
+/* The forward of G (<= 4) LoRA linears that read the same input X -- in a
+ * decoder layer ("Soup CLI ...", "How Layer Streaming Works") the q, k, v
+ * projections or gate, up -- as one fused GEMM plus one rank-r pass:
+ *     Y_g = X W_g^T + s (X A_g^T) B_g^T,  s = alpha / r,  g = 0 .. G-1.
+ * The pages describe no such grouping; it is how this library runs a
+ * layer's projections that share an input, with the same arithmetic as G
+ * calls of sl_lora_linear_fwd up to fp32 summation order.  Layout: w_cat is
+ * one NF4 weight of N = sum N_g rows (the projections' weights back to back,
+ * N_g multiples of 256); A_cat [G r, K] and B_cat [sum N_g, r] bf16 are the
+ * adapters back to back; Y_cat [M, sum N_g] bf16 holds Y_g in columns
+ * [N_0 + .. + N_{g-1}, + N_g); T_cat [M, G r] fp32 (16-byte aligned) holds
+ * X A_g^T in columns [g r, g r + r).  Requires NF4, 128 < M, r % 8 == 0,
+ * r <= 32, G r <= 64 (SL_ERR_INVALID otherwise); allocates nothing. */
+sl_status sl_lora_group_fwd(const sl_weight* w_cat, int32_t G, const int64_t* N_g,
+                            const void* X, int64_t M, const void* A_cat, const void* B_cat,
+                            int32_t r, float alpha, void* Y_cat, void* T_cat, cudaStream_t stream);
+
+/* The backward of the group above for dY_cat [M, sum N_g] bf16 (dY_g in the
+ * columns of Y_g):  dX = sum_g (dY_g W_g + s U_g A_g) with U_g = dY_g B_g
+ * (one fused GEMM), dA_cat [G r, K] (rows of adapter g = s U_g^T X) and
+ * dB_cat [sum N_g, r] (rows of projection g = s dY_g^T T_g), fp32,
+ * overwritten when accumulate == 0, added to otherwise.  dX [M, K] bf16 may
+ * be NULL.  `ws` must hold sl_lora_group_workspace_size(M, G, r) bytes
+ * (256-byte aligned): U_cat [M, G r] fp32.  Reductions run in a fixed
+ * order: results are bitwise reproducible. */
+sl_status sl_lora_group_bwd(const sl_weight* w_cat, int32_t G, const int64_t* N_g,
+                            const void* X, const void* dY_cat, int64_t M,
+                            const void* A_cat, const void* B_cat, int32_t r, float alpha,
+                            const void* T_cat, void* dX, float* dA_cat, float* dB_cat,
+                            int32_t accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+size_t sl_lora_group_workspace_size(int64_t M, int32_t G, int32_t r);
+
 /* ------------------------------------------------- streamed stack (a2-a7) */
 
 /* Byte layout of one layer blob (the unit that is streamed): the seven

@@ -59,6 +59,10 @@ _SIGS = {
                                   _I32, _P, _SZ, _P]),
     "sl_lora_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
     "sl_lora_linear_fwd_noalloc": (_I32, [ctypes.POINTER(sl_weight), _P, _I64, _P, _P, _I32, _F, _P, _P, _P]),
+    "sl_lora_group_fwd": (_I32, [ctypes.POINTER(sl_weight), _I32, _P, _P, _I64, _P, _P, _I32, _F, _P, _P, _P]),
+    "sl_lora_group_bwd": (_I32, [ctypes.POINTER(sl_weight), _I32, _P, _P, _P, _I64, _P, _P, _I32, _F, _P, _P,
+                                 _P, _P, _I32, _P, _SZ, _P]),
+    "sl_lora_group_workspace_size": (_SZ, [_I64, _I32, _I32]),
     "sl_stack_blob_layout": (_I32, [_I32, _I64, _I64, _I64, _P, _P]),
     "sl_stack_create": (_I32, [ctypes.POINTER(sl_stack_desc), _P, _P, _P]),
     "sl_stack_destroy": (_I32, [_P]),
@@ -207,6 +211,33 @@ def sl_lora_linear_bwd(weight: Weight, X, dY, A, B, r, alpha, T_save, dX, dA, dB
     _check(lib().sl_lora_linear_bwd(ctypes.byref(weight.desc), _ptr(X), _ptr(dY), M, _ptr(A), _ptr(B), int(r),
                                     float(alpha), _ptr(T_save), _ptr(dX), _ptr(dA), _ptr(dB),
                                     int(bool(accumulate)), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+# ---------------------------------------------------------- projection groups
+def _n_array(N_g):
+    arr = (ctypes.c_int64 * len(N_g))(*[int(n) for n in N_g])
+    return arr
+
+
+def sl_lora_group_fwd(weight: Weight, N_g, X, A_cat, B_cat, r, alpha, Y_cat, T_cat, stream=None):
+    """G projections reading X, weights/adapters back to back (see include/sl.h)."""
+    n = _n_array(N_g)
+    _check(lib().sl_lora_group_fwd(ctypes.byref(weight.desc), len(N_g), n, _ptr(X), X.shape[0], _ptr(A_cat),
+                                   _ptr(B_cat), int(r), float(alpha), _ptr(Y_cat), _ptr(T_cat), _stream(stream)))
+
+
+def sl_lora_group_bwd(weight: Weight, N_g, X, dY_cat, A_cat, B_cat, r, alpha, T_cat, dX, dA_cat, dB_cat,
+                      accumulate=False, ws=None, stream=None):
+    n = _n_array(N_g)
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(lib().sl_lora_group_bwd(ctypes.byref(weight.desc), len(N_g), n, _ptr(X), _ptr(dY_cat), dY_cat.shape[0],
+                                   _ptr(A_cat), _ptr(B_cat), int(r), float(alpha), _ptr(T_cat), _ptr(dX),
+                                   _ptr(dA_cat), _ptr(dB_cat), int(bool(accumulate)), _ptr(ws), ws_bytes,
+                                   _stream(stream)))
+
+
+def sl_lora_group_workspace_size(M, G, r):
+    return int(lib().sl_lora_group_workspace_size(int(M), int(G), int(r)))
 
 
 # -------------------------------------------------------------------- stack

@@ -181,7 +181,10 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   const GemmArgs& a = g.args;
   if (a.M <= 0 || a.N <= 0 || a.K <= 0) return set_error(SL_ERR_INVALID, "gemm: empty problem");
   if (a.N % 32) return set_error(SL_ERR_INVALID, "gemm: output columns must be a multiple of 32");
-  if (a.r < 0 || a.r > 32 || (a.r % 8)) return set_error(SL_ERR_INVALID, "gemm: LoRA rank must be 0..32, multiple of 8");
+  if (a.r < 0 || a.r > (g.grouped ? kLoraMaxR : 32) || (a.r % 8))
+    return set_error(SL_ERR_INVALID, "gemm: LoRA rank must be 0..32 (a group's 0..64), multiple of 8");
+  if (g.grouped && (g.bsrc != kBSrcNF4 || g.epi != kEpiStoreBF16 || a.M <= kBM))
+    return set_error(SL_ERR_UNSUPPORTED, "gemm: projection groups need NF4 weights and M > 128");
   CUtensorMap ma, mb, ms;
   bool pair = false;
   sl_status st = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, a.K, a.M, g.lda * 2, kBK, kBM,
@@ -239,8 +242,8 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   // More pair tiles than resident clusters: the persistent kernel (its
   // epilogue overlaps the next tile); one wave or less: one cluster per tile
   // with the epilogue spread over all eight dequant warps.
-  const bool persistent =
-      pair && ceil_div(a.M, 256) * ceil_div(a.N, kBN) > (g.bmn ? pair_clusters_resident<1>() : pair_clusters_resident<0>());
+  const bool persistent = pair && (g.grouped || ceil_div(a.M, 256) * ceil_div(a.N, kBN) >
+                                                    (g.bmn ? pair_clusters_resident<1>() : pair_clusters_resident<0>()));
   if (persistent)
     st = g.bmn ? run_persistent<1>(ma, mb, ms, a, stream) : run_persistent<0>(ma, mb, ms, a, stream);
   else

@@ -75,7 +75,10 @@ struct GemmArgs {
   int M, N, K;                 // rows, output columns, reduction length
   const float* lora_x;         // [M, r] fp32 (T or U) or nullptr
   const uint16_t* lora_w;      // K-major: [N, r]; MN-major: [r, N] (ld N); bf16
-  int r;
+  int r;                       // rank of the folded side product (a group's G r in the grouped dX)
+  int lora_ld;                 // row stride of lora_x in floats (0: r)
+  int lora_G;                  // grouped forward: projections sharing the GEMM (0 or 1: none)
+  int lora_bounds[5];          // grouped forward: first output column of projection g (multiples of 256), [G] = N
   float s;                     // LoRA scale alpha / r
   void* out;                   // epilogue output
   int64_t ld_out;              // elements
@@ -581,6 +584,7 @@ struct GemmLaunch {
   const float* absmax;   // NF4 absmax
   int64_t ldw;           // weight row length in elements (K for K-major, N for MN-major)
   GemmArgs args;
+  int grouped;           // a projection group: persistent CTA-pair kernel (NF4, M > 128) required
 };
 
 sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream);

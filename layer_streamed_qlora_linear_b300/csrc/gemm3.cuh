@@ -10,6 +10,10 @@
 //     a dedicated shared-memory region that the epilogue warps fill while
 //     the tile's main loop runs (lora_full / lora_empty): no pipeline drain,
 //     and the dequant warps carry no LoRA state;
+//   * projection groups (q, k, v or gate, up stored back to back along N):
+//     in the forward each tile folds the side product of the projection it
+//     lies in (T_cat columns g r .., row stride G r); the grouped dX is the
+//     plain fold at rank G r (s U_cat A_cat), up to 64;
 // Warps: 0 A/code TMA producer, 1 MMA issuer (leader) or peer forwarder,
 // 2..9 NF4 dequant (two groups on alternate k-blocks), 10..13 LoRA staging +
 // epilogue.  Every wait is bounded.
@@ -21,14 +25,17 @@ namespace sl {
 constexpr int kNumEpi3 = 128;
 constexpr int kGemm3Threads = 64 + kNumDq2 + kNumEpi3;
 
+constexpr int kLoraMaxR = 64;               // folded rank: K of the fold up to 2 * 64
+constexpr int kLoraAtom = 128 * 128;         // one 128-row x 128-byte SW128 atom
+
 struct Gemm3Cfg {
-  static constexpr int S = 5;
+  static constexpr int S = 4;
   static constexpr int kRawBytes = kHalfCodesBytes + kPairAbsBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + S * kATileBytes;
-  static constexpr int kOffLA = kOffB + S * kHalfBTileBytes;     // LoRA Xe [128 x 128 B]
-  static constexpr int kOffLB = kOffLA + kATileBytes;            // LoRA Be (K-major 128 rows / MN 2 atoms)
-  static constexpr int kOffRaw = kOffLB + kHalfBTileBytes;
+  static constexpr int kOffLA = kOffB + S * kHalfBTileBytes;     // LoRA Xe: K-major [128 rows x 2R], two atoms
+  static constexpr int kOffLB = kOffLA + 2 * kLoraAtom;          // LoRA Be: K-major [128 x 2r] / MN-major 2 atoms of [2R x 64]
+  static constexpr int kOffRaw = kOffLB + 2 * kLoraAtom;
   static constexpr int kOffBar = kOffRaw + S * kRawBytes;
   static constexpr int kNumBars = 5 * S + 7;
   static constexpr int kOffSink = (kOffBar + kNumBars * 8 + 15) / 16 * 16;
@@ -209,8 +216,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           }
           ptx::tc_fence_after();
           for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t ad = ptx::smem_desc(la + kk * 32, 16, 1024, 2);
-            const uint64_t bd = BMN ? ptx::smem_desc(lb + kk * 2048, 64 * 128, 1024, 2)
+            const uint64_t ad = ptx::smem_desc(la + (kk >> 2) * kLoraAtom + (kk & 3) * 32, 16, 1024, 2);
+            const uint64_t bd = BMN ? ptx::smem_desc(lb + kk * 2048, kLoraAtom, 1024, 2)
                                     : ptx::smem_desc(lb + kk * 32, 16, 1024, 2);
             ptx::mma_bf16_pair(d, ad, bd, idesc, 1u);
           }
@@ -291,18 +298,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     auto chunk_at = [&](uint8_t* base, int rw, int c) {
       return reinterpret_cast<uint4*>(base + rw * 128 + ((c ^ (rw & 7)) << 4));
     };
-    auto mn_chunk = [&](uint8_t* bt, int i, int cc) {  // cc: 0..15 over two 64-column atoms
-      return reinterpret_cast<uint4*>(bt + (cc >> 3) * (64 * 128) + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
+    auto mn_chunk = [&](uint8_t* bt, int i, int cc) {  // cc: 0..15 over two 64-column atoms of 128 rows
+      return reinterpret_cast<uint4*>(bt + (cc >> 3) * kLoraAtom + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
     };
-    // Xe = [s T_hi | s T_lo] (row e of this CTA's 128 rows), Be = [B | B] for
-    // this CTA's 128 output columns, in the operand layouts of the main loop.
+    auto xe_chunk = [&](int rw, int c) {  // 16-byte chunk c (8 elements of K) of Xe row rw, two atoms
+      return reinterpret_cast<uint4*>(sLA + (c >> 3) * kLoraAtom + rw * 128 + (((c & 7) ^ (rw & 7)) << 4));
+    };
+    const int lora_ld = args.lora_ld > 0 ? args.lora_ld : r;
+    // Xe = [s T_hi | s T_lo] (row e of this CTA's 128 rows; in a grouped
+    // forward the columns of tile t's projection), Be = [B | B] for this
+    // CTA's 128 output columns, in the operand layouts of the main loop.
     auto stage_lora = [&](int t) {
       const int gm = tile_m0(t) + e;
       const int nh = tile_n0(t) + static_cast<int>(rank) * 128;
+      int xcol = 0;
+      if (!BMN && args.lora_G > 1) {
+        const int n0 = tile_n0(t);
+        int g = 0;
+        if (args.lora_G > 1 && n0 >= args.lora_bounds[1]) g = 1;
+        if (args.lora_G > 2 && n0 >= args.lora_bounds[2]) g = 2;
+        if (args.lora_G > 3 && n0 >= args.lora_bounds[3]) g = 3;
+        xcol = g * r;
+      }
       for (int gi = 0; gi < nr; ++gi) {
         float v[8];
         if (gm < args.M) {
-          const float4* p = reinterpret_cast<const float4*>(args.lora_x + static_cast<int64_t>(gm) * r + gi * 8);
+          const float4* p =
+              reinterpret_cast<const float4*>(args.lora_x + static_cast<int64_t>(gm) * lora_ld + xcol + gi * 8);
           const float4 a0 = p[0], a1 = p[1];
           v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w; v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
         } else {
@@ -318,8 +340,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           ph[k] = pack_bf16x2(x0, x1);
           pl[k] = pack_bf16x2(x0 - bf16_lo(ph[k]), x1 - bf16_hi(ph[k]));
         }
-        *chunk_at(sLA, e, gi) = hi;
-        *chunk_at(sLA, e, nr + gi) = lo;
+        *xe_chunk(e, gi) = hi;
+        *xe_chunk(e, nr + gi) = lo;
       }
       if (!BMN) {
         const int gn = nh + e;

@@ -230,7 +230,7 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
   if (!err) return SL_ERR_CUDA;
   if (lora) {
     st = skinny_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A), 0, r,
-                     static_cast<float*>(T_save), stream);
+                     1, nullptr, static_cast<float*>(T_save), stream);
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
@@ -277,7 +277,7 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
     U = reinterpret_cast<float*>(p + L.U);
     // U = dY B
     st = skinny_down(static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), static_cast<const uint16_t*>(B), 1,
-                     r, U, stream);
+                     r, 1, nullptr, U, stream);
     if (st != SL_OK) return st;
   }
   if (dX) {
@@ -308,13 +308,129 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   if (lora) {
     const float s = alpha / static_cast<float>(r);
     // dA [r, K] = s U^T X;  dB [N, r] = s dY^T T
-    st = skinny_grad(U, static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), r, s, dA, 1, accumulate, stream);
+    st = skinny_grad(U, static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), r, 1, nullptr, 0, s, dA, 1,
+                     accumulate, stream);
     if (st != SL_OK) return st;
     st = skinny_grad(static_cast<const float*>(T_save), static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), r,
-                     s, dB, 0, accumulate, stream);
+                     1, nullptr, 1, s, dB, 0, accumulate, stream);
     if (st != SL_OK) return st;
   }
   return SL_OK;
+}
+
+// ---------------------------------------------------------- projection groups
+// G projections that read the same input (q, k, v or gate, up), frozen
+// weights stored back to back along N (one sl_weight of N = sum N_g rows),
+// adapters back to back (A_cat [G r, K], B_cat [sum N_g, r]).  One fused GEMM
+// and one rank-r pass of each kind for the whole group.
+
+static sl_status check_group(const sl_weight* w, int G, const int64_t* N_g, int64_t M, int r, int bounds[5]) {
+  sl_status st = check_weight(w);
+  if (st != SL_OK) return st;
+  SL_REQUIRE(w->kind == SL_WEIGHT_NF4, "projection group: NF4 weights only");
+  SL_REQUIRE(M > 128 && M < (1LL << 31), "projection group: need 128 < M < 2^31");
+  SL_REQUIRE(G >= 1 && G <= kSkMaxGroups && N_g, "projection group: need 1 <= G <= 4 projections");
+  SL_REQUIRE(r >= 8 && r % 8 == 0 && r <= 32 && G * r <= 64, "projection group: need r % 8 == 0, r <= 32, G r <= 64");
+  int64_t off = 0;
+  bounds[0] = 0;
+  for (int g = 0; g < G; ++g) {
+    SL_REQUIRE(N_g[g] > 0 && N_g[g] % 256 == 0, "projection group: every N_g must be a positive multiple of 256");
+    off += N_g[g];
+    bounds[g + 1] = static_cast<int>(off);
+  }
+  SL_REQUIRE(off == w->N, "projection group: the N_g must add up to the weight's N");
+  for (int g = G + 1; g < 5; ++g) bounds[g] = bounds[G];
+  return SL_OK;
+}
+
+size_t group_ws_bytes(int64_t M, int G, int r) { return align_up(static_cast<size_t>(M) * G * r * 4, 256); }
+
+sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, int64_t M, const void* A_cat,
+                    const void* B_cat, int r, float alpha, void* Y_cat, void* T_cat, cudaStream_t stream) {
+  int bounds[5];
+  sl_status st = check_group(w, G, N_g, M, r, bounds);
+  if (st != SL_OK) return st;
+  SL_REQUIRE(X && Y_cat && A_cat && B_cat && T_cat, "sl_lora_group_fwd: null argument");
+  int* err = device_error_word();
+  if (!err) return SL_ERR_CUDA;
+  // T_cat [M, G r] = X A_cat^T
+  st = skinny_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A_cat), 0, r,
+                   G, nullptr, static_cast<float*>(T_cat), stream);
+  if (st != SL_OK) return st;
+  GemmLaunch g{};
+  g.bsrc = kBSrcNF4;
+  g.bmn = 0;
+  g.epi = kEpiStoreBF16;
+  g.grouped = 1;
+  g.A = X;
+  g.lda = w->K;
+  g.codes = w->codes;
+  g.absmax = w->absmax;
+  g.ldw = w->K;
+  g.args.M = static_cast<int>(M);
+  g.args.N = static_cast<int>(w->N);
+  g.args.K = static_cast<int>(w->K);
+  g.args.lora_x = static_cast<const float*>(T_cat);
+  g.args.lora_w = static_cast<const uint16_t*>(B_cat);
+  g.args.r = r;
+  g.args.lora_ld = G * r;
+  g.args.lora_G = G;
+  for (int i = 0; i < 5; ++i) g.args.lora_bounds[i] = bounds[i];
+  g.args.s = alpha / static_cast<float>(r);
+  g.args.out = Y_cat;
+  g.args.ld_out = w->N;
+  g.args.err = err;
+  return launch_gemm(g, stream);
+}
+
+sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
+                    const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX, float* dA_cat,
+                    float* dB_cat, int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int bounds[5];
+  sl_status st = check_group(w, G, N_g, M, r, bounds);
+  if (st != SL_OK) return st;
+  SL_REQUIRE(X && dY_cat && A_cat && B_cat && T_cat && dA_cat && dB_cat, "sl_lora_group_bwd: null argument");
+  SL_REQUIRE(ws && ws_bytes >= group_ws_bytes(M, G, r) && (reinterpret_cast<uintptr_t>(ws) & 255) == 0,
+             "sl_lora_group_bwd: workspace too small or not 256-byte aligned");
+  int* err = device_error_word();
+  if (!err) return SL_ERR_CUDA;
+  const int NN = static_cast<int>(w->N), K = static_cast<int>(w->K);
+  const float s = alpha / static_cast<float>(r);
+  float* U = static_cast<float*>(ws);
+  // U_cat [M, G r] = dY_cat blockdiag(B_g)
+  st = skinny_down(static_cast<const uint16_t*>(dY_cat), M, NN, static_cast<const uint16_t*>(B_cat), 1, r, G, bounds, U,
+                   stream);
+  if (st != SL_OK) return st;
+  if (dX) {
+    // dX = dY_cat W_cat + s U_cat A_cat: the plain dX GEMM at rank G r
+    GemmLaunch g{};
+    g.bsrc = kBSrcNF4;
+    g.bmn = 1;
+    g.epi = kEpiStoreBF16;
+    g.grouped = 1;
+    g.A = dY_cat;
+    g.lda = NN;
+    g.codes = w->codes;
+    g.absmax = w->absmax;
+    g.ldw = K;
+    g.args.M = static_cast<int>(M);
+    g.args.N = K;
+    g.args.K = NN;
+    g.args.lora_x = U;
+    g.args.lora_w = static_cast<const uint16_t*>(A_cat);
+    g.args.r = G * r;
+    g.args.s = s;
+    g.args.out = dX;
+    g.args.ld_out = K;
+    g.args.err = err;
+    st = launch_gemm(g, stream);
+    if (st != SL_OK) return st;
+  }
+  // dA_cat [G r, K] = s U_cat^T X;  dB_cat [sum N_g, r]: rows of projection g = s dY_g^T T_g
+  st = skinny_grad(U, static_cast<const uint16_t*>(X), M, K, r, G, nullptr, 0, s, dA_cat, 1, accumulate, stream);
+  if (st != SL_OK) return st;
+  return skinny_grad(static_cast<const float*>(T_cat), static_cast<const uint16_t*>(dY_cat), M, NN, r, G, bounds, 1, s,
+                     dB_cat, 0, accumulate, stream);
 }
 
 // ------------------------------------------------ allocation-free forward
@@ -424,6 +540,22 @@ extern "C" sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const
 extern "C" size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r) {
   return linear_ws_bytes(M, N, K, r);
 }
+
+extern "C" sl_status sl_lora_group_fwd(const sl_weight* w_cat, int32_t G, const int64_t* N_g, const void* X, int64_t M,
+                                       const void* A_cat, const void* B_cat, int32_t r, float alpha, void* Y_cat,
+                                       void* T_cat, cudaStream_t stream) {
+  return group_fwd(w_cat, G, N_g, X, M, A_cat, B_cat, r, alpha, Y_cat, T_cat, stream);
+}
+
+extern "C" sl_status sl_lora_group_bwd(const sl_weight* w_cat, int32_t G, const int64_t* N_g, const void* X,
+                                       const void* dY_cat, int64_t M, const void* A_cat, const void* B_cat, int32_t r,
+                                       float alpha, const void* T_cat, void* dX, float* dA_cat, float* dB_cat,
+                                       int32_t accumulate, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return group_bwd(w_cat, G, N_g, X, dY_cat, M, A_cat, B_cat, r, alpha, T_cat, dX, dA_cat, dB_cat, accumulate, ws,
+                   ws_bytes, stream);
+}
+
+extern "C" size_t sl_lora_group_workspace_size(int64_t M, int32_t G, int32_t r) { return group_ws_bytes(M, G, r); }
 
 extern "C" sl_status sl_lora_linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t M, const void* A,
                                                 const void* B, int32_t r, float alpha, void* Y, void* T_save,

@@ -12,5 +12,12 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
                      int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
                      void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
+// Projection groups (sl_lora_group_fwd / _bwd).
+sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, int64_t M, const void* A_cat,
+                    const void* B_cat, int r, float alpha, void* Y_cat, void* T_cat, cudaStream_t stream);
+sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
+                    const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX, float* dA_cat,
+                    float* dB_cat, int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t group_ws_bytes(int64_t M, int G, int r);
 
 }  // namespace sl

@@ -7,23 +7,30 @@
 //   backward  U  = dY B           [M, r]   reduce over N     (mode kSkKB)
 //             dA = s U^T X        [r, K]   reduce over M     (mode kSkM)
 //             dB = s dY^T T       [N, r]   reduce over M     (mode kSkM)
+// A group of G adapters whose projections read the same input (q, k, v or
+// gate, up of a decoder layer) is done in the same four passes, with the
+// adapters stored back to back (A_cat [G r, K], B_cat [sum N_g, r], output
+// columns concatenated): T_cat = X A_cat^T, U_cat = dY_cat blockdiag(B_g),
+// dA_cat = s U_cat^T X, and dB_cat, whose rows in projection g use the
+// columns g r .. g r + r - 1 of T_cat.
 // These are HBM-bound streams (2r FLOP per element of Q); on the CUDA cores
 // the FMAs alone would outlast the read, so each pass runs tcgen05 MMAs with
-// a narrow N (r .. 2r columns) over TMA-staged tiles of Q:
-//   * mode K: D[128 rows of Q, r16] += Q[128 x 64] * W[r16 x 64]^T per step;
-//     W = A is TMA-loaded directly (K-major), W = B^T is transposed from a
-//     raw TMA tile by four converter warps;
-//   * mode M: D[128 columns of Q, 2r] += Q^T[128 x 64] * P'[2r x 64]^T per
-//     step, Q^T read MN-major straight from the TMA tile and P' = [P_hi ;
-//     P_lo] the two-term bf16 split of the fp32 operand (U or T), written by
-//     the converter warps, so D = Q^T P to fp32 accuracy.
+// a narrow N over TMA-staged steps of Q:
+//   * mode K: D[128 rows of Q, n] += Q[128 x step] * W[n x step]^T; W = A_cat
+//     is TMA-loaded directly (K-major), W = blockdiag(B_g)^T is transposed
+//     from a raw TMA tile of B_cat by four converter warps;
+//   * mode M: D[128 columns of Q, n] += Q^T[128 x step] * P'[n x step]^T, Q^T
+//     read MN-major straight from the TMA tile and P' = [P_hi ; P_lo] the
+//     two-term bf16 split of the fp32 operand (U or T) written by the
+//     converter warps (hi in D columns 0.., lo from the next multiple of 32), so
+//     D = Q^T P to fp32 accuracy.
 // The long reduction is split over the CTAs of a thread-block cluster (up to
-// 16); their fp32 partials are summed through distributed shared memory in
-// rank order, so one launch writes the final result with no partial buffers
-// in global memory and bitwise reproducible sums.  Every wait is bounded.
+// 16, sized so that the grid is one wave); their fp32 partials are summed
+// through distributed shared memory in rank order, so one launch writes the
+// final result with no partial buffers in global memory and bitwise
+// reproducible sums.  Every wait is bounded.
 #include <algorithm>
 #include <mutex>
-#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -37,33 +44,46 @@ enum SkMode { kSkKA = 0, kSkKB = 1, kSkM = 2 };
 
 constexpr int kSkThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 converters + epilogue
 constexpr int kSkMaxStages = 8;
-constexpr int kSkStep = 128;      // reduced elements per pipeline step
-constexpr int kSkQBytes = 128 * kSkStep * 2;  // Q tile of a step: two 16 KB TMA boxes (64 x 128)
-constexpr int kSkTmemCols = 64;
+constexpr int kSkTmemCols = 128;
 constexpr int kSkBarBytes = 1024; // barriers + misc, ahead of the 1024-aligned data
 constexpr int kSkSmemBudget = 227 * 1024 - 1024 - kSkBarBytes;
+constexpr int kSkRedLd = 68;      // fp32 partial row stride (64 columns + pad)
 
 struct SkArgs {
-  int M;          // rows of Q
-  int C;          // columns of Q
-  int r;          // rank (multiple of 8, <= 32)
-  int nsteps;     // 128-wide steps of the reduced extent (C in mode K, M in mode M)
-  int stages;     // pipeline depth (<= kSkMaxStages), sized to the shared memory
-  float s;        // output scale (mode M)
-  int transpose;  // mode M: out[i * C + c] (dA) instead of out[c * r + i] (dB)
-  int accumulate; // mode M: out += result
+  int M;           // rows of Q
+  int C;           // columns of Q
+  int r;           // adapter rank (multiple of 8, <= 32)
+  int R;           // G r: mode K output columns; mode M row stride of P
+  int rout;        // mode M: result columns per column of Q (R for dA, r for dB)
+  int select;      // mode M: use P columns [g r, g r + r) of the column block's group g
+  int G;           // adapters in the group (<= kSkMaxGroups)
+  int bounds[kSkMaxGroups + 1];  // group g covers columns [bounds[g], bounds[g+1]) of Q (multiples of 128)
+  int step;        // reduced elements per pipeline step: 64 or 128
+  int nsteps;      // steps of the reduced extent (C in mode K, M in mode M)
+  int stages;      // pipeline depth (<= kSkMaxStages), sized to the shared memory
+  float s;         // output scale (mode M)
+  int transpose;   // mode M: out[i * C + c] (dA) instead of out[c * rout + i] (dB)
+  int accumulate;  // mode M: out += result
   float* out;
   int* err;
 };
 
-// Per-stage byte counts of the three regions (Q, skinny operand, raw tile).
-__host__ __device__ inline int sk_n_mma(int mode, int r) { return mode == kSkM ? 2 * r : (r + 15) / 16 * 16; }
-__host__ __device__ inline int sk_op_bytes(int mode, int r) { return 2 * sk_n_mma(mode, r) * 128; }
-__host__ __device__ inline int sk_raw_bytes(int mode, int r) {
-  return mode == kSkKA ? 0 : (mode == kSkKB ? kSkStep * r * 2 : kSkStep * r * 4);
+// Mode M: first D column of the lo half (32-aligned, so TMEM loads of
+// result columns c .. c+31 and lo_col + c .. stay aligned).
+__host__ __device__ inline int sk_lo_col(int rout) { return (rout + 31) / 32 * 32; }
+// MMA N and the per-stage bytes of the three shared-memory regions.
+__host__ __device__ inline int sk_n_mma(int mode, int R, int rout) {
+  return mode == kSkM ? sk_lo_col(rout) + (rout + 15) / 16 * 16 : (R + 15) / 16 * 16;
 }
-__host__ __device__ inline int sk_stage_bytes(int mode, int r) {
-  return kSkQBytes + sk_op_bytes(mode, r) + sk_raw_bytes(mode, r);
+__host__ __device__ inline int sk_q_bytes(int step) { return 128 * step * 2; }
+__host__ __device__ inline int sk_op_bytes(int mode, int R, int rout, int step) {
+  return sk_n_mma(mode, R, rout) * step * 2;
+}
+__host__ __device__ inline int sk_raw_bytes(int mode, int r, int rout, int step) {
+  return mode == kSkKA ? 0 : (mode == kSkKB ? step * r * 2 : step * rout * 4);
+}
+__host__ __device__ inline int sk_stage_bytes(int mode, int r, int R, int rout, int step) {
+  return sk_q_bytes(step) + sk_op_bytes(mode, R, rout, step) + sk_raw_bytes(mode, r, rout, step);
 }
 
 __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr) {
@@ -78,6 +98,15 @@ __device__ __forceinline__ uint4* sw128_chunk(uint8_t* tile, int row, int chunk)
   return reinterpret_cast<uint4*>(tile + row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Adapter of column `col` of Q (constant indices: the bounds stay in registers).
+__device__ __forceinline__ int group_of(const SkArgs& a, int col) {
+  int g = 0;
+  if (a.G > 1 && col >= a.bounds[1]) g = 1;
+  if (a.G > 2 && col >= a.bounds[2]) g = 2;
+  if (a.G > 3 && col >= a.bounds[3]) g = 3;
+  return g;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kSkThreads, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w,
@@ -86,10 +115,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int r = a.r;
   const int S = a.stages;
-  const int n_mma = sk_n_mma(MODE, r);
+  const int step = a.step;
+  const int nh = step / 64;  // 64-wide halves of a step
+  const int n_mma = sk_n_mma(MODE, a.R, a.rout);
   const int op_half = n_mma * 128;  // one 64-wide K chunk of the skinny operand
-  const int op_bytes = sk_op_bytes(MODE, r);
-  const int raw_bytes = sk_raw_bytes(MODE, r);
+  const int q_bytes = sk_q_bytes(step);
+  const int op_bytes = sk_op_bytes(MODE, a.R, a.rout, step);
+  const int raw_bytes = sk_raw_bytes(MODE, r, a.rout, step);
+  const int ncols = MODE == kSkM ? a.rout : a.R;  // result columns per row of the accumulator
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint64_t* full = bars;                      // TMA bytes of the stage landed
   uint64_t* conv = bars + kSkMaxStages;       // converter warps wrote the stage's skinny operand
@@ -98,10 +131,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 516);
   uint8_t* sQ = smem + kSkBarBytes;
-  uint8_t* sOp = sQ + S * kSkQBytes;
+  uint8_t* sOp = sQ + S * q_bytes;
   uint8_t* sRaw = sOp + S * op_bytes;
-  const int red_ld = 36;                      // fp32 partial [128][36] (r <= 32 columns) in the Q region
-  float* red = reinterpret_cast<float*>(sQ);
+  float* red = reinterpret_cast<float*>(sQ);  // fp32 partial [128][kSkRedLd] after the main loop
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -112,6 +144,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int s1 = static_cast<int>(static_cast<int64_t>(a.nsteps) * (rank + 1) / cs);
   const int nloc = s1 - s0;
   const int base = static_cast<int>(blockIdx.x) * 128;  // rows of Q (mode K) or columns of Q (mode M)
+  // mode M with select: this column block's adapter g reads P columns g r ..
+  const int p_col0 = (MODE == kSkM && a.select) ? group_of(a, base) * r : 0;
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
@@ -124,15 +158,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&map_q);
     ptx::tma_prefetch_desc(&map_w);
-  }
-  if (MODE == kSkKB && n_mma > r) {
-    // rows r .. n_mma-1 of the transposed B operand stay zero for the whole kernel
-    const int pad = n_mma - r;
-    for (int i = tid; i < S * 2 * pad * 8; i += kSkThreads) {
-      const int st = i / (2 * pad * 8), h = (i / (pad * 8)) & 1, row = r + (i / 8) % pad, c = i % 8;
-      *sw128_chunk(sOp + st * op_bytes + h * op_half, row, c) = make_uint4(0, 0, 0, 0);
-    }
-    ptx::fence_proxy_async_smem();
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, kSkTmemCols);
@@ -151,7 +176,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint32_t tx = kSkQBytes + (MODE == kSkKA ? 2 * n_mma * 128 : raw_bytes);
+      const uint32_t tx = q_bytes + (MODE == kSkKA ? nh * op_half : raw_bytes);
       int j = 0;
       for (; j < nloc; ++j) {
         const int st = j % S;
@@ -159,22 +184,20 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           give_up();
           break;
         }
-        const int k0 = (s0 + j) * kSkStep;
-        uint8_t* q = sQ + st * kSkQBytes;
+        const int k0 = (s0 + j) * step;
+        uint8_t* q = sQ + st * q_bytes;
         ptx::mbar_arrive_expect_tx(&full[st], tx);
-        if (MODE == kSkKA) {  // Q [128 rows x 128 reduced], A [n_mma x 128 reduced], 64-wide halves
-          ptx::tma_load_2d(q, &map_q, &full[st], k0, base);
-          ptx::tma_load_2d(q + kSkQBytes / 2, &map_q, &full[st], k0 + 64, base);
-          ptx::tma_load_2d(sOp + st * op_bytes, &map_w, &full[st], k0, 0);
-          ptx::tma_load_2d(sOp + st * op_bytes + op_half, &map_w, &full[st], k0 + 64, 0);
-        } else if (MODE == kSkKB) {  // Q as above; raw B rows k0 .. k0+127
-          ptx::tma_load_2d(q, &map_q, &full[st], k0, base);
-          ptx::tma_load_2d(q + kSkQBytes / 2, &map_q, &full[st], k0 + 64, base);
-          ptx::tma_load_2d(sRaw + st * raw_bytes, &map_w, &full[st], 0, k0);
-        } else {  // Q rows k0 .. k0+127, columns base .. base+127 (two 64-column atoms); raw P rows
+        if (MODE != kSkM) {  // Q [128 rows x step], 64-wide halves 16 KB apart
+          for (int h = 0; h < nh; ++h) ptx::tma_load_2d(q + h * 16384, &map_q, &full[st], k0 + 64 * h, base);
+          if (MODE == kSkKA)
+            for (int h = 0; h < nh; ++h)
+              ptx::tma_load_2d(sOp + st * op_bytes + h * op_half, &map_w, &full[st], k0 + 64 * h, 0);
+          else
+            ptx::tma_load_2d(sRaw + st * raw_bytes, &map_w, &full[st], 0, k0);
+        } else {  // Q rows k0 .. k0+step-1, columns base .. base+127 (two 64-column atoms); raw P rows
           ptx::tma_load_2d(q, &map_q, &full[st], base, k0);
-          ptx::tma_load_2d(q + kSkQBytes / 2, &map_q, &full[st], base + 64, k0);
-          ptx::tma_load_2d(sRaw + st * raw_bytes, &map_w, &full[st], 0, k0);
+          ptx::tma_load_2d(q + step * 128, &map_q, &full[st], base + 64, k0);
+          ptx::tma_load_2d(sRaw + st * raw_bytes, &map_w, &full[st], p_col0, k0);
         }
       }
       if (*abort_flag)
@@ -195,15 +218,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t qs = q_base + st * kSkQBytes;
+        const uint32_t qs = q_base + st * q_bytes;
         const uint32_t os = op_base + st * op_bytes;
-#pragma unroll
-        for (int kk = 0; kk < kSkStep / 16; ++kk) {
+        for (int kk = 0; kk < step / 16; ++kk) {
           const int h = kk >> 2, k4 = kk & 3;
           // mode K: A = Q K-major, half h at +16 KB; mode M: A = Q^T MN-major,
-          // 16 reduced rows (2 KB) per k16 step, the two 64-column atoms 16 KB apart
-          const uint64_t ad = MODE == kSkM ? ptx::smem_desc(qs + kk * 2048, kSkQBytes / 2, 1024, 2)
-                                           : ptx::smem_desc(qs + h * (kSkQBytes / 2) + k4 * 32, 16, 1024, 2);
+          // 16 reduced rows (2 KB) per k16 step, the two 64-column atoms step * 128 B apart
+          const uint64_t ad = MODE == kSkM ? ptx::smem_desc(qs + kk * 2048, step * 128, 1024, 2)
+                                           : ptx::smem_desc(qs + h * 16384 + k4 * 32, 16, 1024, 2);
           const uint64_t bd = ptx::smem_desc(os + h * op_half + k4 * 32, 16, 1024, 2);
           ptx::mma_bf16(tmem, ad, bd, idesc, (j | kk) ? 1u : 0u);
         }
@@ -223,32 +245,42 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
         uint8_t* op = sOp + st * op_bytes;
         const uint8_t* raw = sRaw + st * raw_bytes;
-        // task = (8-wide chunk ch of the 128 reduced elements, rank index i),
-        // i fastest so that a warp reads consecutive words of the raw rows
-        for (int task = e; task < r * 16; task += 128) {
-          const int i = task % r, ch = task / r;
-          uint8_t* oh = op + (ch >> 3) * op_half;
-          const int c8 = ch & 7;
-          if (MODE == kSkKB) {
-            // raw: B rows k0 .. k0+127, r bf16 each -> operand row i = B[k][i]
-            const uint16_t* rb = reinterpret_cast<const uint16_t*>(raw) + (ch * 8) * r + i;
-            uint32_t w[4];
+        const int nch = step / 8;  // 8-element chunks of the step
+        if (MODE == kSkKB) {
+          // raw: B_cat rows k0 .. k0+step-1 (r bf16 each), all of group g;
+          // operand rows g r + i = B[k][i], every other row zero
+          const int g0 = group_of(a, (s0 + j) * step) * r;
+          const uint16_t* rb = reinterpret_cast<const uint16_t*>(raw);
+          for (int task = e; task < n_mma * nch; task += 128) {
+            const int row = task % n_mma, ch = task / n_mma;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            const int i = row - g0;
+            if (i >= 0 && i < r) {
+              const uint16_t* p = rb + (ch * 8) * r + i;
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
-              w[p] = static_cast<uint32_t>(rb[(2 * p) * r]) | (static_cast<uint32_t>(rb[(2 * p + 1) * r]) << 16);
-            *sw128_chunk(oh, i, c8) = make_uint4(w[0], w[1], w[2], w[3]);
-          } else {
-            // raw: P rows k0 .. k0+127, r fp32 each -> rows i (hi) and r + i (lo)
-            const float* rf = reinterpret_cast<const float*>(raw) + (ch * 8) * r + i;
+              for (int q = 0; q < 4; ++q)
+                w[q] = static_cast<uint32_t>(p[(2 * q) * r]) | (static_cast<uint32_t>(p[(2 * q + 1) * r]) << 16);
+            }
+            *sw128_chunk(op + (ch >> 3) * op_half, row, ch & 7) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          // raw: P rows k0 .. k0+step-1, rout fp32 each -> rows i (hi) and lo_col + i (lo)
+          const int ro = a.rout;
+          const int lo_col = sk_lo_col(ro);
+          const float* rf = reinterpret_cast<const float*>(raw);
+          for (int task = e; task < ro * nch; task += 128) {
+            const int i = task % ro, ch = task / ro;  // i fastest: a warp reads consecutive words
+            const float* p = rf + (ch * 8) * ro + i;
             uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              const float v0 = rf[(2 * p) * r], v1 = rf[(2 * p + 1) * r];
-              hi[p] = pack_bf16x2(v0, v1);
-              lo[p] = pack_bf16x2(v0 - bf16_lo(hi[p]), v1 - bf16_hi(hi[p]));
+            for (int q = 0; q < 4; ++q) {
+              const float v0 = p[(2 * q) * ro], v1 = p[(2 * q + 1) * ro];
+              hi[q] = pack_bf16x2(v0, v1);
+              lo[q] = pack_bf16x2(v0 - bf16_lo(hi[q]), v1 - bf16_hi(hi[q]));
             }
-            *sw128_chunk(oh, i, c8) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *sw128_chunk(oh, r + i, c8) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            uint8_t* oh = op + (ch >> 3) * op_half;
+            *sw128_chunk(oh, i, ch & 7) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *sw128_chunk(oh, lo_col + i, ch & 7) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
         }
         ptx::fence_proxy_async_smem();
@@ -256,8 +288,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&conv[st]);
       }
     }
-    // epilogue: TMEM lane `row` of the accumulator holds this CTA's partial
-    // for row `row` of the block (mode M: hi and lo halves, added here)
+    // epilogue: TMEM lane `row` holds this CTA's partial for row `row` of
+    // the 128 block; result columns are read 32 at a time (mode M adds the
+    // lo half from column lo_col + c)
     bool ready = ptx::mbar_wait(acc_full, 0, abort_flag) && !*abort_flag;
     ready = __all_sync(0xffffffffu, ready);
     if (!ready && !*abort_flag) give_up();
@@ -265,60 +298,53 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const bool keep = ready && nloc > 0;
-    float v[32];  // the r (<= 32) result columns of this row
-    {
-      uint32_t u[32];
-      ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16), u);
-      ptx::tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 32; ++c) v[c] = keep ? __uint_as_float(u[c]) : 0.0f;
-      if (MODE == kSkM) {
-        // D columns: [0, r) from P_hi, [r, 2r) from P_lo (r in {8, 16, 24, 32});
-        // the lo term of result column c sits at column c + r
-        uint32_t w[32];
-        ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + 32, w);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    for (int c0 = 0; c0 < ncols; c0 += 32) {
+      float v[32];
+      {
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(lane_addr + c0, u);
         ptx::tmem_wait_ld();
-        auto add_lo = [&](auto rc) {
-          constexpr int R = decltype(rc)::value;
 #pragma unroll
-          for (int c = 0; c < R; ++c) v[c] += keep ? __uint_as_float(c + R < 32 ? u[(c + R) & 31] : w[(c + R) & 31]) : 0.0f;
-        };
-        switch (r) {
-          case 8: add_lo(std::integral_constant<int, 8>{}); break;
-          case 16: add_lo(std::integral_constant<int, 16>{}); break;
-          case 24: add_lo(std::integral_constant<int, 24>{}); break;
-          default: add_lo(std::integral_constant<int, 32>{}); break;
+        for (int c = 0; c < 32; ++c) v[c] = keep ? __uint_as_float(u[c]) : 0.0f;
+        if (MODE == kSkM) {
+          ptx::tmem_ld_32x32b_x32(lane_addr + sk_lo_col(a.rout) + c0, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] += keep ? __uint_as_float(u[c]) : 0.0f;
         }
       }
-    }
-    if (cs == 1) {
-      // the whole reduction ran here: write straight from registers
-      if (MODE != kSkM) {
-        const int gm = base + row;
-        if (gm < a.M)
+      const int nc = ncols - c0 < 32 ? ncols - c0 : 32;  // a multiple of 8
+      if (cs == 1) {
+        // the whole reduction ran here: write straight from registers
+        if (MODE != kSkM) {
+          const int gm = base + row;
+          if (gm < a.M)
 #pragma unroll
-          for (int i4 = 0; i4 < 8; ++i4)
-            if (i4 * 4 < r)
-              *reinterpret_cast<float4*>(a.out + static_cast<int64_t>(gm) * r + i4 * 4) =
-                  make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
-      } else {
-        const int gc = base + row;
-        if (gc < a.C) {
+            for (int i4 = 0; i4 < 8; ++i4)
+              if (i4 * 4 < nc)
+                *reinterpret_cast<float4*>(a.out + static_cast<int64_t>(gm) * a.R + c0 + i4 * 4) =
+                    make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+        } else {
+          const int gc = base + row;
+          if (gc < a.C) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (i >= r) break;
-            float* o = a.transpose ? a.out + static_cast<int64_t>(i) * a.C + gc : a.out + static_cast<int64_t>(gc) * r + i;
-            const float x = v[i] * a.s;
-            *o = a.accumulate ? *o + x : x;
+            for (int i = 0; i < 32; ++i) {
+              if (i >= nc) break;
+              float* o = a.transpose ? a.out + static_cast<int64_t>(c0 + i) * a.C + gc
+                                     : a.out + static_cast<int64_t>(gc) * a.rout + c0 + i;
+              const float x = v[i] * a.s;
+              *o = a.accumulate ? *o + x : x;
+            }
           }
         }
-      }
-    } else {
-      float* dst = red + row * red_ld;
+      } else {
+        float* dst = red + row * kSkRedLd + c0;
 #pragma unroll
-      for (int i4 = 0; i4 < 8; ++i4)
-        if (i4 * 4 < r)
-          *reinterpret_cast<float4*>(dst + i4 * 4) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+        for (int i4 = 0; i4 < 8; ++i4)
+          if (i4 * 4 < nc)
+            *reinterpret_cast<float4*>(dst + i4 * 4) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+      }
     }
   }
 
@@ -330,13 +356,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     // 128-row block: partials summed over the cluster in rank order, four
     // result columns per task, all ranks' loads in flight at once.
     const int r0 = rank * 128 / cs, nrows = (rank + 1) * 128 / cs - r0;
-    const int nq = r / 4;
+    const int nq = ncols / 4;
     const bool by_col = MODE == kSkM && a.transpose;  // dA: rows vary fastest for coalesced stores
     for (int task = tid; task < nrows * nq; task += kSkThreads) {
       const int rl = by_col ? task % nrows : task / nq;
       const int i4 = by_col ? task / nrows : task % nq;
       const int row = r0 + rl;
-      const uint32_t own = ptx::smem_addr(red + row * red_ld + i4 * 4);
+      const uint32_t own = ptx::smem_addr(red + row * kSkRedLd + i4 * 4);
       float4 h[16];
 #pragma unroll
       for (int p = 0; p < 16; ++p) {
@@ -355,13 +381,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       }
       if (MODE != kSkM) {
         const int gm = base + row;
-        if (gm < a.M) *reinterpret_cast<float4*>(a.out + static_cast<int64_t>(gm) * r + i4 * 4) = acc;
+        if (gm < a.M) *reinterpret_cast<float4*>(a.out + static_cast<int64_t>(gm) * a.R + i4 * 4) = acc;
       } else {
         const int gc = base + row;
         if (gc < a.C) {
           const float x[4] = {acc.x * a.s, acc.y * a.s, acc.z * a.s, acc.w * a.s};
           if (!a.transpose) {
-            float4* o = reinterpret_cast<float4*>(a.out + static_cast<int64_t>(gc) * r + i4 * 4);
+            float4* o = reinterpret_cast<float4*>(a.out + static_cast<int64_t>(gc) * a.rout + i4 * 4);
             float4 v4 = make_float4(x[0], x[1], x[2], x[3]);
             if (a.accumulate) {
               const float4 old = *o;
@@ -389,9 +415,17 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 // ------------------------------------------------------------------ host side
 namespace {
 
-int stages_for(int mode, int r) {
-  const int s = kSkSmemBudget / sk_stage_bytes(mode, r);
-  return s < kSkMaxStages ? s : kSkMaxStages;
+// Step width and pipeline depth: the pair with the most Q bytes in flight.
+void choose_pipeline(int mode, int r, int R, int rout, SkArgs& a) {
+  int best = -1;
+  for (int step : {128, 64}) {
+    const int s = std::min(kSkMaxStages, kSkSmemBudget / sk_stage_bytes(mode, r, R, rout, step));
+    if (s >= 2 && s * sk_q_bytes(step) > best) {
+      best = s * sk_q_bytes(step);
+      a.step = step;
+      a.stages = s;
+    }
+  }
 }
 
 template <int MODE>
@@ -407,12 +441,13 @@ sl_status set_attributes() {
 }
 
 template <int MODE>
-cudaLaunchConfig_t make_config(int64_t blocks, int cs, int stages, int r, cudaStream_t stream,
+cudaLaunchConfig_t make_config(int64_t blocks, int cs, const SkArgs& a, cudaStream_t stream,
                                cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(cs), 1);
   cfg.blockDim = dim3(kSkThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(1024 + kSkBarBytes + stages * sk_stage_bytes(MODE, r));
+  cfg.dynamicSmemBytes =
+      static_cast<size_t>(1024 + kSkBarBytes + a.stages * sk_stage_bytes(MODE, a.r, a.R, a.rout, a.step));
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -423,19 +458,20 @@ cudaLaunchConfig_t make_config(int64_t blocks, int cs, int stages, int r, cudaSt
   return cfg;
 }
 
-// Clusters of `cs` CTAs that the device can hold at once (driver query,
-// cached per device, mode, rank and cluster size).
+// Clusters of `cs` CTAs that the device can hold at once for this shared-
+// memory size (driver query, cached per device, size and cluster size).
 template <int MODE>
-int max_active_clusters(int cs, int stages, int r) {
+int max_active_clusters(int cs, const SkArgs& a) {
   static std::mutex mu;
-  static int cache[64][5][17];  // [device][r / 8][cs], 0 = not yet asked
+  static int cache[64][64][17];  // [device][smem / 4 KB][cs], 0 = not yet asked
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_config<MODE>(1, cs, a, nullptr, attr);
+  const int key = static_cast<int>(cfg.dynamicSmemBytes / 4096) & 63;
   std::lock_guard<std::mutex> lk(mu);
-  int& slot = cache[dev][r / 8][cs];
+  int& slot = cache[dev][key][cs];
   if (slot == 0) {
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = make_config<MODE>(1, cs, stages, r, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, skinny_kernel<MODE>, &cfg) != cudaSuccess) {
       cudaGetLastError();
@@ -446,14 +482,14 @@ int max_active_clusters(int cs, int stages, int r) {
   return slot;
 }
 
-// Cluster size: the largest split of the reduction (at least two 128-wide
-// steps per CTA) whose clusters all fit on the device at once, so that the
-// launch is one wave of at most one CTA per SM.
+// Cluster size: the largest split of the reduction (at least two steps per
+// CTA) whose clusters all fit on the device at once, so that the launch is
+// one wave of at most one CTA per SM.
 template <int MODE>
-int choose_split(int64_t blocks, int64_t nsteps, int stages, int r) {
+int choose_split(int64_t blocks, const SkArgs& a) {
   for (int cs = 16; cs > 1; --cs) {
-    if (blocks * cs > num_sms() || nsteps < 2 * cs) continue;
-    if (max_active_clusters<MODE>(cs, stages, r) >= blocks) return cs;
+    if (blocks * cs > num_sms() || a.nsteps < 2 * cs) continue;
+    if (max_active_clusters<MODE>(cs, a) >= blocks) return cs;
   }
   return 1;
 }
@@ -462,8 +498,8 @@ int choose_split(int64_t blocks, int64_t nsteps, int stages, int r) {
 // written (and read too when accumulating).
 double pass_bytes(int mode, const SkArgs& a) {
   const double q = 2.0 * a.M * static_cast<double>(a.C);
-  if (mode != kSkM) return q + 2.0 * a.r * a.C + 4.0 * a.M * a.r;
-  return q + 4.0 * a.M * a.r + 4.0 * a.C * a.r * (a.accumulate ? 2 : 1);
+  if (mode != kSkM) return q + (mode == kSkKA ? 2.0 * a.R * a.C : 2.0 * a.r * a.C) + 4.0 * a.M * a.R;
+  return q + 4.0 * a.M * a.rout + 4.0 * a.C * a.rout * (a.accumulate ? 2 : 1);
 }
 
 template <int MODE>
@@ -471,9 +507,9 @@ sl_status launch(const CUtensorMap& mq, const CUtensorMap& mw, const SkArgs& a, 
                  cudaStream_t stream) {
   sl_status st = set_attributes<MODE>();
   if (st != SL_OK) return st;
-  const int cs = choose_split<MODE>(blocks, a.nsteps, a.stages, a.r);
+  const int cs = choose_split<MODE>(blocks, a);
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_config<MODE>(blocks, cs, a.stages, a.r, stream, attr);
+  cudaLaunchConfig_t cfg = make_config<MODE>(blocks, cs, a, stream, attr);
   const TimingToken tt = timing_begin(MODE == kSkKA ? 7 : (MODE == kSkKB ? 8 : 9), pass_bytes(MODE, a), stream);
   cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_kernel<MODE>, mq, mw, a);
   timing_end(tt, stream);
@@ -481,62 +517,90 @@ sl_status launch(const CUtensorMap& mq, const CUtensorMap& mw, const SkArgs& a, 
   return check_launch("skinny_kernel");
 }
 
+// bounds == nullptr: the pass does not split Q's columns by adapter (T_cat,
+// dA_cat); otherwise G + 1 increasing offsets, multiples of 128, ending at C.
+sl_status check_groups(int G, const int* bounds, int C, int r, SkArgs& a) {
+  SL_REQUIRE(r >= 8 && r <= 32 && r % 8 == 0, "rank-r product: r must be 8, 16, 24 or 32");
+  SL_REQUIRE(G >= 1 && G <= kSkMaxGroups && G * r <= 64, "rank-r product: need 1 <= G <= 4 and G r <= 64");
+  a.G = G;
+  a.r = r;
+  a.R = G * r;
+  a.bounds[0] = 0;
+  for (int g = 0; g < G; ++g) {
+    if (!bounds) {
+      a.bounds[g + 1] = C;
+      continue;
+    }
+    const int b = bounds[g + 1];
+    SL_REQUIRE(b > a.bounds[g] && (g + 1 == G ? b == C : b % 128 == 0),
+               "rank-r product: group bounds must increase in multiples of 128 and end at C");
+    a.bounds[g + 1] = b;
+  }
+  return SL_OK;
+}
+
 }  // namespace
 
-sl_status skinny_down(const uint16_t* Q, int64_t M, int C, const uint16_t* W, int wt, int r, float* out,
-                      cudaStream_t stream) {
-  SL_REQUIRE(r >= 8 && r <= 32 && r % 8 == 0, "rank-r product: r must be 8, 16, 24 or 32");
+sl_status skinny_down(const uint16_t* Q, int64_t M, int C, const uint16_t* W, int wt, int r, int G, const int* bounds,
+                      float* out, cudaStream_t stream) {
   SL_REQUIRE(C % 8 == 0 && M > 0 && M < (1LL << 31), "rank-r product: need C % 8 == 0 and 0 < M < 2^31");
+  SkArgs a{};
+  sl_status st = check_groups(G, bounds, C, r, a);
+  if (st != SL_OK) return st;
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
-  CUtensorMap mq, mw;
-  sl_status st = make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, C, M, static_cast<uint64_t>(C) * 2, 64, 128,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != SL_OK) return st;
-  if (wt == 0)  // A [r, C]: operand rows straight from TMA (rows past r read as zero)
-    st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, C, r, static_cast<uint64_t>(C) * 2, 64,
-                  (r + 15) / 16 * 16, CU_TENSOR_MAP_SWIZZLE_128B);
-  else  // B [C, r]: raw 64 x r tiles, transposed by the converter warps
-    st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, r, C, static_cast<uint64_t>(r) * 2, r, kSkStep,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st != SL_OK) return st;
-  SkArgs a{};
+  const int mode = wt == 0 ? kSkKA : kSkKB;
+  SL_REQUIRE(mode == kSkKA || G == 1 || bounds, "rank-r product: a grouped U pass needs the group bounds");
   a.M = static_cast<int>(M);
   a.C = C;
-  a.r = r;
-  a.nsteps = static_cast<int>(ceil_div(C, kSkStep));
-  a.stages = stages_for(wt == 0 ? kSkKA : kSkKB, r);
+  a.rout = a.R;
+  choose_pipeline(mode, r, a.R, a.rout, a);
+  a.nsteps = static_cast<int>(ceil_div(C, a.step));
   a.s = 1.0f;
   a.out = out;
   a.err = err;
+  CUtensorMap mq, mw;
+  st = make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, C, M, static_cast<uint64_t>(C) * 2, 64, 128,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  if (wt == 0)  // A_cat [G r, C]: operand rows straight from TMA (rows past G r read as zero)
+    st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, C, a.R, static_cast<uint64_t>(C) * 2, 64,
+                  sk_n_mma(mode, a.R, a.rout), CU_TENSOR_MAP_SWIZZLE_128B);
+  else  // B_cat [C, r]: raw step x r tiles, transposed by the converter warps
+    st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, r, C, static_cast<uint64_t>(r) * 2, r, a.step,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != SL_OK) return st;
   const int64_t blocks = ceil_div(M, 128);
   return wt == 0 ? launch<kSkKA>(mq, mw, a, blocks, stream) : launch<kSkKB>(mq, mw, a, blocks, stream);
 }
 
-sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, float s, float* out, int transpose,
-                      int accumulate, cudaStream_t stream) {
-  SL_REQUIRE(r >= 8 && r <= 32 && r % 8 == 0, "rank-r product: r must be 8, 16, 24 or 32");
+sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, int G, const int* bounds, int select,
+                      float s, float* out, int transpose, int accumulate, cudaStream_t stream) {
   SL_REQUIRE(C % 8 == 0 && M > 0 && M < (1LL << 31), "rank-r product: need C % 8 == 0 and 0 < M < 2^31");
+  SkArgs a{};
+  sl_status st = check_groups(G, bounds, C, r, a);
+  if (st != SL_OK) return st;
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
-  CUtensorMap mq, mw;
-  sl_status st = make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, C, M, static_cast<uint64_t>(C) * 2, 64, 128,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != SL_OK) return st;
-  st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, P, r, M, static_cast<uint64_t>(r) * 4, r, kSkStep,
-                CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st != SL_OK) return st;
-  SkArgs a{};
+  SL_REQUIRE(!select || G == 1 || bounds, "rank-r product: a grouped dB pass needs the group bounds");
   a.M = static_cast<int>(M);
   a.C = C;
-  a.r = r;
-  a.nsteps = static_cast<int>(ceil_div(M, kSkStep));
-  a.stages = stages_for(kSkM, r);
+  a.select = select;
+  a.rout = select ? r : a.R;
+  choose_pipeline(kSkM, r, a.R, a.rout, a);
+  a.nsteps = static_cast<int>(ceil_div(M, a.step));
   a.s = s;
   a.transpose = transpose;
   a.accumulate = accumulate;
   a.out = out;
   a.err = err;
+  CUtensorMap mq, mw;
+  st = make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, C, M, static_cast<uint64_t>(C) * 2, 64, a.step,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, P, a.R, M, static_cast<uint64_t>(a.R) * 4, a.rout, a.step,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != SL_OK) return st;
   const int64_t blocks = ceil_div(C, 128);
   return launch<kSkM>(mq, mw, a, blocks, stream);
 }

@@ -4,12 +4,22 @@
 
 namespace sl {
 
-// out [M, r] fp32 = Q [M, C] * W^T, W = A [r, C] (wt = 0) or B [C, r] (wt = 1).
-sl_status skinny_down(const uint16_t* Q, int64_t M, int C, const uint16_t* W, int wt, int r, float* out,
-                      cudaStream_t stream);
-// out = (accumulate ? out : 0) + s * P^T Q, P [M, r] fp32, Q [M, C] bf16;
-// stored [r, C] (transpose = 1, dA) or [C, r] (transpose = 0, dB).
-sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, float s, float* out, int transpose,
-                      int accumulate, cudaStream_t stream);
+constexpr int kSkMaxGroups = 4;
+
+// out [M, G r] fp32 = Q [M, C] * W^T for a group of G adapters of rank r
+// (G = 1: a single adapter):
+//   wt = 0: W = A_cat [G r, C] (the adapters' A stacked);
+//   wt = 1: W = blockdiag(B_g)^T with B_cat [C, r] (the adapters' B stacked
+//           along C; columns [bounds[g], bounds[g+1]) of Q belong to adapter g).
+// bounds: G + 1 increasing column offsets, multiples of 128, bounds[G] = C;
+// nullptr when G == 1.
+sl_status skinny_down(const uint16_t* Q, int64_t M, int C, const uint16_t* W, int wt, int r, int G, const int* bounds,
+                      float* out, cudaStream_t stream);
+// out = (accumulate ? out : 0) + s * P'^T Q with P [M, G r] fp32 and Q [M, C] bf16:
+//   select = 0: P' = P, out [G r, C] (transpose = 1, dA_cat) or [C, G r];
+//   select = 1: columns of Q in adapter g use P' = P[:, g r .. g r + r),
+//               out [C, r] (transpose = 0, dB_cat).
+sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, int G, const int* bounds, int select,
+                      float s, float* out, int transpose, int accumulate, cudaStream_t stream);
 
 }  // namespace sl
