@@ -204,7 +204,8 @@ size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r)
  * adapters back to back; Y_cat [M, sum N_g] bf16 holds Y_g in columns
  * [N_0 + .. + N_{g-1}, + N_g); T_cat [M, G r] fp32 (16-byte aligned) holds
  * X A_g^T in columns [g r, g r + r).  Requires NF4, 128 < M, r % 8 == 0,
- * r <= 32, G r <= 64 (SL_ERR_INVALID otherwise); allocates nothing. */
+ * r <= 32, G r <= 64 (SL_ERR_INVALID otherwise); r == 0 runs the bases
+ * alone (adapters off; A_cat, B_cat, T_cat may be NULL).  Allocates nothing. */
 sl_status sl_lora_group_fwd(const sl_weight* w_cat, int32_t G, const int64_t* N_g,
                             const void* X, int64_t M, const void* A_cat, const void* B_cat,
                             int32_t r, float alpha, void* Y_cat, void* T_cat, cudaStream_t stream);
@@ -215,8 +216,8 @@ sl_status sl_lora_group_fwd(const sl_weight* w_cat, int32_t G, const int64_t* N_
  * dB_cat [sum N_g, r] (rows of projection g = s dY_g^T T_g), fp32,
  * overwritten when accumulate == 0, added to otherwise.  dX [M, K] bf16 may
  * be NULL.  `ws` must hold sl_lora_group_workspace_size(M, G, r) bytes
- * (256-byte aligned): U_cat [M, G r] fp32.  Reductions run in a fixed
- * order: results are bitwise reproducible. */
+ * (256-byte aligned): U_cat [M, G r] fp32.  r == 0: dX of the bases only.
+ * Reductions run in a fixed order: results are bitwise reproducible. */
 sl_status sl_lora_group_bwd(const sl_weight* w_cat, int32_t G, const int64_t* N_g,
                             const void* X, const void* dY_cat, int64_t M,
                             const void* A_cat, const void* B_cat, int32_t r, float alpha,
@@ -229,10 +230,14 @@ size_t sl_lora_group_workspace_size(int64_t M, int32_t G, int32_t r);
 
 /* Byte layout of one layer blob (the unit that is streamed): the seven
  * projections q, k, v, o, gate, up, down of a decoder layer with hidden D,
- * kv width Dkv and MLP width F.  For NF4 each projection contributes its
- * codes then its absmax; for BF16 its weight.  offsets[2p] / offsets[2p+1]
- * receive the byte offsets of projection p's codes / absmax (NF4) or of its
- * weight / 0 (BF16), every offset 256-byte aligned; *blob_bytes the total. */
+ * kv width Dkv and MLP width F.  NF4: the seven projections' codes in that
+ * order, then their absmax in that order; BF16: the seven weights in order.
+ * With the size rules below every region is a multiple of 256 bytes, so the
+ * q, k, v and the gate, up weights each lie back to back (one weight of
+ * N = D + 2 Dkv or 2 F rows, as the projection groups use them).
+ * offsets[2p] / offsets[2p+1] receive the byte offsets of projection p's
+ * codes / absmax (NF4) or of its weight / 0 (BF16), every offset 256-byte
+ * aligned; *blob_bytes the total. */
 sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F,
                                size_t offsets[14], size_t* blob_bytes);
 

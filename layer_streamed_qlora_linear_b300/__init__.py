@@ -276,6 +276,28 @@ def build_layer_blob(kind, D, Dkv, F, weights, stream=None):
     return blob
 
 
+def packed_views(shapes, dtype, device="cuda"):
+    """Tensors of the given 2-D shapes back to back in one allocation (views, in order).
+
+    Adapters of a layer allocated this way (A: [r, K_p], B: [N_p, r] in
+    projection order) let the stack run q/k/v and gate/up as projection groups.
+    """
+    import torch
+    total = sum(int(a) * int(b) for a, b in shapes)
+    buf = torch.empty(total, dtype=dtype, device=device)
+    views, off = [], 0
+    for a, b in shapes:
+        views.append(buf[off:off + a * b].view(a, b))
+        off += a * b
+    return views
+
+
+def adapter_shapes(D, Dkv, F, r):
+    """([r, K_p]) and ([N_p, r]) of the seven projections, in blob order."""
+    shp = proj_shapes(D, Dkv, F)
+    return [(r, K) for N, K in shp], [(N, r) for N, K in shp]
+
+
 class Stack:
     """Owns an sl_stack handle (two device layer buffers, copy stream, events)."""
 

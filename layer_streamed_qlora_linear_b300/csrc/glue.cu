@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kRowThreads) rms_fwd_kernel(const float* __res
 // a[m, j] = bf16(q[m, j] * k[m, kv(j)] + v[m, kv(j)]); kv(j): head j/128 reads kv head (j/128)/g.
 __global__ void mix_fwd_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                                const uint16_t* __restrict__ v, uint16_t* __restrict__ a, int64_t M, int D,
-                               int Dkv) {
+                               int Dkv, int64_t ldq, int64_t ldkv) {
   const int g = D / Dkv;
   const int64_t n8 = M * D / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -109,9 +109,9 @@ __global__ void mix_fwd_kernel(const uint16_t* __restrict__ q, const uint16_t* _
     const int j = static_cast<int>(e0 % D);
     const int c = (j / 128 / g) * 128 + (j % 128);
     float fq[8], fk[8], fv[8], fa[8];
-    load8_bf16(q + e0, fq);
-    load8_bf16(k + m * Dkv + c, fk);
-    load8_bf16(v + m * Dkv + c, fv);
+    load8_bf16(q + m * ldq + j, fq);
+    load8_bf16(k + m * ldkv + c, fk);
+    load8_bf16(v + m * ldkv + c, fv);
 #pragma unroll
     for (int e = 0; e < 8; ++e) fa[e] = fmaf(fq[e], fk[e], fv[e]);
     store8_bf16(a + e0, fa);
@@ -121,14 +121,16 @@ __global__ void mix_fwd_kernel(const uint16_t* __restrict__ q, const uint16_t* _
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // m = bf16(SiLU(g) * u)
+// g, u: rows of F elements at row stride ld; m dense [M, F].
 __global__ void swiglu_fwd_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
-                                  uint16_t* __restrict__ m, int64_t n) {
-  const int64_t n8 = n / 8;
+                                  uint16_t* __restrict__ m, int64_t M, int F, int64_t ld) {
+  const int64_t n8 = M * F / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
+    const int64_t row = t * 8 / F, off = row * ld + t * 8 % F;
     float fg[8], fu[8], fm[8];
-    load8_bf16(g + t * 8, fg);
-    load8_bf16(u + t * 8, fu);
+    load8_bf16(g + off, fg);
+    load8_bf16(u + off, fu);
 #pragma unroll
     for (int e = 0; e < 8; ++e) fm[e] = fg[e] * sigmoidf_(fg[e]) * fu[e];
     store8_bf16(m + t * 8, fm);
@@ -161,24 +163,26 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ x, uint16_t* __rest
 }
 
 // dg = bf16(dm * u * s * (1 + g (1 - s))), du = bf16(dm * g * s), s = sigmoid(g)
+// dm dense [M, F]; g, u, dg, du: rows of F elements at row stride ld.
 __global__ void swiglu_bwd_kernel(const uint16_t* __restrict__ dm, const uint16_t* __restrict__ g,
                                   const uint16_t* __restrict__ u, uint16_t* __restrict__ dg,
-                                  uint16_t* __restrict__ du, int64_t n) {
-  const int64_t n8 = n / 8;
+                                  uint16_t* __restrict__ du, int64_t M, int F, int64_t ld) {
+  const int64_t n8 = M * F / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
+    const int64_t row = t * 8 / F, off = row * ld + t * 8 % F;
     float fdm[8], fg[8], fu[8], odg[8], odu[8];
     load8_bf16(dm + t * 8, fdm);
-    load8_bf16(g + t * 8, fg);
-    load8_bf16(u + t * 8, fu);
+    load8_bf16(g + off, fg);
+    load8_bf16(u + off, fu);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float s = sigmoidf_(fg[e]);
       odg[e] = fdm[e] * fu[e] * s * (1.0f + fg[e] * (1.0f - s));
       odu[e] = fdm[e] * fg[e] * s;
     }
-    store8_bf16(dg + t * 8, odg);
-    store8_bf16(du + t * 8, odu);
+    store8_bf16(dg + off, odg);
+    store8_bf16(du + off, odu);
   }
 }
 
@@ -229,9 +233,11 @@ __global__ void __launch_bounds__(kRowThreads) rms_bwd_kernel(
 }
 
 // dq = bf16(da * rep(k)); dk = bf16(sum over the g heads of da * q); dv = bf16(sum of da)
+// da dense [M, D]; q, dq at row stride ldq; k, dk, dv at row stride ldkv.
 __global__ void mix_bwd_kernel(const uint16_t* __restrict__ da, const uint16_t* __restrict__ q,
                                const uint16_t* __restrict__ k, uint16_t* __restrict__ dq,
-                               uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int64_t M, int D, int Dkv) {
+                               uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int64_t M, int D, int Dkv,
+                               int64_t ldq, int64_t ldkv) {
   const int g = D / Dkv;
   const int64_t n8 = M * Dkv / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -241,24 +247,24 @@ __global__ void mix_bwd_kernel(const uint16_t* __restrict__ da, const uint16_t* 
     const int c = static_cast<int>(e0 % Dkv);
     const int kvh = c / 128, e = c % 128;
     float fk[8], sk[8], sv[8];
-    load8_bf16(k + e0, fk);
+    load8_bf16(k + m * ldkv + c, fk);
 #pragma unroll
     for (int i = 0; i < 8; ++i) sk[i] = sv[i] = 0.0f;
     for (int hh = 0; hh < g; ++hh) {
-      const int64_t j = m * D + (kvh * g + hh) * 128 + e;
+      const int col = (kvh * g + hh) * 128 + e;
       float fa[8], fq[8], fdq[8];
-      load8_bf16(da + j, fa);
-      load8_bf16(q + j, fq);
+      load8_bf16(da + m * D + col, fa);
+      load8_bf16(q + m * ldq + col, fq);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         sk[i] = fmaf(fa[i], fq[i], sk[i]);
         sv[i] += fa[i];
         fdq[i] = fa[i] * fk[i];
       }
-      store8_bf16(dq + j, fdq);
+      store8_bf16(dq + m * ldq + col, fdq);
     }
-    store8_bf16(dk + e0, sk);
-    store8_bf16(dv + e0, sv);
+    store8_bf16(dk + m * ldkv + c, sk);
+    store8_bf16(dv + m * ldkv + c, sv);
   }
 }
 
@@ -274,12 +280,13 @@ sl_status glue_rms_fwd(const float* h, const uint16_t* add, float* h_out, uint16
   return check_launch("rms_fwd_kernel");
 }
 sl_status glue_mix_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* a, int64_t M, int D,
-                       int Dkv, cudaStream_t s) {
-  mix_fwd_kernel<<<ew_grid(M * D / 8), 256, 0, s>>>(q, k, v, a, M, D, Dkv);
+                       int Dkv, int64_t ldq, int64_t ldkv, cudaStream_t s) {
+  mix_fwd_kernel<<<ew_grid(M * D / 8), 256, 0, s>>>(q, k, v, a, M, D, Dkv, ldq, ldkv);
   return check_launch("mix_fwd_kernel");
 }
-sl_status glue_swiglu_fwd(const uint16_t* g, const uint16_t* u, uint16_t* m, int64_t n, cudaStream_t s) {
-  swiglu_fwd_kernel<<<ew_grid(n / 8), 256, 0, s>>>(g, u, m, n);
+sl_status glue_swiglu_fwd(const uint16_t* g, const uint16_t* u, uint16_t* m, int64_t M, int F, int64_t ld,
+                          cudaStream_t s) {
+  swiglu_fwd_kernel<<<ew_grid(M * F / 8), 256, 0, s>>>(g, u, m, M, F, ld);
   return check_launch("swiglu_fwd_kernel");
 }
 sl_status glue_resid_add(const float* h, const uint16_t* add, float* out, int64_t n, cudaStream_t s) {
@@ -291,8 +298,8 @@ sl_status glue_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s) {
   return check_launch("f32_to_bf16_kernel");
 }
 sl_status glue_swiglu_bwd(const uint16_t* dm, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,
-                          int64_t n, cudaStream_t s) {
-  swiglu_bwd_kernel<<<ew_grid(n / 8), 256, 0, s>>>(dm, g, u, dg, du, n);
+                          int64_t M, int F, int64_t ld, cudaStream_t s) {
+  swiglu_bwd_kernel<<<ew_grid(M * F / 8), 256, 0, s>>>(dm, g, u, dg, du, M, F, ld);
   return check_launch("swiglu_bwd_kernel");
 }
 sl_status glue_rms_bwd(const float* dh_in, const uint16_t* dx0, const uint16_t* dx1, const uint16_t* dx2,
@@ -303,8 +310,8 @@ sl_status glue_rms_bwd(const float* dh_in, const uint16_t* dx0, const uint16_t* 
   return check_launch("rms_bwd_kernel");
 }
 sl_status glue_mix_bwd(const uint16_t* da, const uint16_t* q, const uint16_t* k, uint16_t* dq, uint16_t* dk,
-                       uint16_t* dv, int64_t M, int D, int Dkv, cudaStream_t s) {
-  mix_bwd_kernel<<<ew_grid(M * Dkv / 8), 256, 0, s>>>(da, q, k, dq, dk, dv, M, D, Dkv);
+                       uint16_t* dv, int64_t M, int D, int Dkv, int64_t ldq, int64_t ldkv, cudaStream_t s) {
+  mix_bwd_kernel<<<ew_grid(M * Dkv / 8), 256, 0, s>>>(da, q, k, dq, dk, dv, M, D, Dkv, ldq, ldkv);
   return check_launch("mix_bwd_kernel");
 }
 

@@ -330,7 +330,7 @@ static sl_status check_group(const sl_weight* w, int G, const int64_t* N_g, int6
   SL_REQUIRE(w->kind == SL_WEIGHT_NF4, "projection group: NF4 weights only");
   SL_REQUIRE(M > 128 && M < (1LL << 31), "projection group: need 128 < M < 2^31");
   SL_REQUIRE(G >= 1 && G <= kSkMaxGroups && N_g, "projection group: need 1 <= G <= 4 projections");
-  SL_REQUIRE(r >= 8 && r % 8 == 0 && r <= 32 && G * r <= 64, "projection group: need r % 8 == 0, r <= 32, G r <= 64");
+  SL_REQUIRE(r >= 0 && r % 8 == 0 && r <= 32 && G * r <= 64, "projection group: need r % 8 == 0, r <= 32, G r <= 64");
   int64_t off = 0;
   bounds[0] = 0;
   for (int g = 0; g < G; ++g) {
@@ -343,20 +343,25 @@ static sl_status check_group(const sl_weight* w, int G, const int64_t* N_g, int6
   return SL_OK;
 }
 
-size_t group_ws_bytes(int64_t M, int G, int r) { return align_up(static_cast<size_t>(M) * G * r * 4, 256); }
+size_t group_ws_bytes(int64_t M, int G, int r) {
+  return r > 0 ? align_up(static_cast<size_t>(M) * G * r * 4, 256) : 0;
+}
 
 sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, int64_t M, const void* A_cat,
                     const void* B_cat, int r, float alpha, void* Y_cat, void* T_cat, cudaStream_t stream) {
   int bounds[5];
   sl_status st = check_group(w, G, N_g, M, r, bounds);
   if (st != SL_OK) return st;
-  SL_REQUIRE(X && Y_cat && A_cat && B_cat && T_cat, "sl_lora_group_fwd: null argument");
+  const bool lora = r > 0;
+  SL_REQUIRE(X && Y_cat && (!lora || (A_cat && B_cat && T_cat)), "sl_lora_group_fwd: null argument");
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
-  // T_cat [M, G r] = X A_cat^T
-  st = skinny_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A_cat), 0, r,
-                   G, nullptr, static_cast<float*>(T_cat), stream);
-  if (st != SL_OK) return st;
+  if (lora) {
+    // T_cat [M, G r] = X A_cat^T
+    st = skinny_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A_cat), 0,
+                     r, G, nullptr, static_cast<float*>(T_cat), stream);
+    if (st != SL_OK) return st;
+  }
   GemmLaunch g{};
   g.bsrc = kBSrcNF4;
   g.bmn = 0;
@@ -370,13 +375,13 @@ sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
   g.args.M = static_cast<int>(M);
   g.args.N = static_cast<int>(w->N);
   g.args.K = static_cast<int>(w->K);
-  g.args.lora_x = static_cast<const float*>(T_cat);
-  g.args.lora_w = static_cast<const uint16_t*>(B_cat);
+  g.args.lora_x = lora ? static_cast<const float*>(T_cat) : nullptr;
+  g.args.lora_w = lora ? static_cast<const uint16_t*>(B_cat) : nullptr;
   g.args.r = r;
   g.args.lora_ld = G * r;
   g.args.lora_G = G;
   for (int i = 0; i < 5; ++i) g.args.lora_bounds[i] = bounds[i];
-  g.args.s = alpha / static_cast<float>(r);
+  g.args.s = lora ? alpha / static_cast<float>(r) : 0.0f;
   g.args.out = Y_cat;
   g.args.ld_out = w->N;
   g.args.err = err;
@@ -389,18 +394,22 @@ sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
   int bounds[5];
   sl_status st = check_group(w, G, N_g, M, r, bounds);
   if (st != SL_OK) return st;
-  SL_REQUIRE(X && dY_cat && A_cat && B_cat && T_cat && dA_cat && dB_cat, "sl_lora_group_bwd: null argument");
-  SL_REQUIRE(ws && ws_bytes >= group_ws_bytes(M, G, r) && (reinterpret_cast<uintptr_t>(ws) & 255) == 0,
+  const bool lora = r > 0;
+  SL_REQUIRE(dY_cat && (!lora || (X && A_cat && B_cat && T_cat && dA_cat && dB_cat)),
+             "sl_lora_group_bwd: null argument");
+  SL_REQUIRE(!lora || (ws && ws_bytes >= group_ws_bytes(M, G, r) && (reinterpret_cast<uintptr_t>(ws) & 255) == 0),
              "sl_lora_group_bwd: workspace too small or not 256-byte aligned");
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   const int NN = static_cast<int>(w->N), K = static_cast<int>(w->K);
-  const float s = alpha / static_cast<float>(r);
-  float* U = static_cast<float*>(ws);
-  // U_cat [M, G r] = dY_cat blockdiag(B_g)
-  st = skinny_down(static_cast<const uint16_t*>(dY_cat), M, NN, static_cast<const uint16_t*>(B_cat), 1, r, G, bounds, U,
-                   stream);
-  if (st != SL_OK) return st;
+  const float s = lora ? alpha / static_cast<float>(r) : 0.0f;
+  float* U = lora ? static_cast<float*>(ws) : nullptr;
+  if (lora) {
+    // U_cat [M, G r] = dY_cat blockdiag(B_g)
+    st = skinny_down(static_cast<const uint16_t*>(dY_cat), M, NN, static_cast<const uint16_t*>(B_cat), 1, r, G, bounds,
+                     U, stream);
+    if (st != SL_OK) return st;
+  }
   if (dX) {
     // dX = dY_cat W_cat + s U_cat A_cat: the plain dX GEMM at rank G r
     GemmLaunch g{};
@@ -417,7 +426,7 @@ sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
     g.args.N = K;
     g.args.K = NN;
     g.args.lora_x = U;
-    g.args.lora_w = static_cast<const uint16_t*>(A_cat);
+    g.args.lora_w = lora ? static_cast<const uint16_t*>(A_cat) : nullptr;
     g.args.r = G * r;
     g.args.s = s;
     g.args.out = dX;
@@ -426,6 +435,7 @@ sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
     st = launch_gemm(g, stream);
     if (st != SL_OK) return st;
   }
+  if (!lora) return SL_OK;
   // dA_cat [G r, K] = s U_cat^T X;  dB_cat [sum N_g, r]: rows of projection g = s dY_g^T T_g
   st = skinny_grad(U, static_cast<const uint16_t*>(X), M, K, r, G, nullptr, 0, s, dA_cat, 1, accumulate, stream);
   if (st != SL_OK) return st;

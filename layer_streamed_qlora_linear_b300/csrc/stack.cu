@@ -19,6 +19,7 @@
 // 0 and 1 at the start of the next step when the buffers still hold them
 // (the base is frozen).  RESIDENT mode runs the same kernels in the same
 // order on device copies of the blobs, so both modes give identical bits.
+#include <algorithm>
 #include <cstring>
 #include <vector>
 
@@ -65,32 +66,38 @@ void proj_shapes(int64_t D, int64_t Dkv, int64_t F, Proj p[7]) {
 sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[14], size_t* total) {
   Proj p[7];
   proj_shapes(D, Dkv, F, p);
+  // NF4: all codes, then all absmax, so that the q, k, v and the gate, up
+  // codes (and absmax) are contiguous: with D, F multiples of 256 and Dkv a
+  // multiple of 128 every region is a multiple of 256 bytes (no padding).
   size_t off = 0;
   for (int i = 0; i < 7; ++i) {
     const size_t n = static_cast<size_t>(p[i].N) * static_cast<size_t>(p[i].K);
-    if (kind == SL_WEIGHT_NF4) {
-      offs[2 * i] = off;
-      off = align_up(off + n / 2, 256);
+    offs[2 * i] = off;
+    off = align_up(off + (kind == SL_WEIGHT_NF4 ? n / 2 : n * 2), 256);
+    offs[2 * i + 1] = 0;
+  }
+  if (kind == SL_WEIGHT_NF4)
+    for (int i = 0; i < 7; ++i) {
+      const size_t n = static_cast<size_t>(p[i].N) * static_cast<size_t>(p[i].K);
       offs[2 * i + 1] = off;
       off = align_up(off + n / 64 * 4, 256);
-    } else {
-      offs[2 * i] = off;
-      off = align_up(off + n * 2, 256);
-      offs[2 * i + 1] = 0;
     }
-  }
   *total = off;
   return SL_OK;
 }
 
-// Workspace plan: per-layer saved activations plus shared scratch.
+// Workspace plan: per-layer saved activations plus shared scratch.  The
+// q/k/v outputs live in one region of M x (D + 2 Dkv) and the gate/up
+// outputs in one of M x 2 F: as column blocks (row stride D + 2 Dkv, 2 F)
+// when a projection group produced them, as dense arrays one after the
+// other otherwise; the same holds for their gradients and side products T.
 struct Plan {
   size_t total = 0;
   // per layer
-  std::vector<size_t> hin, h1, rstd1, rstd2, x1, q, k, v, a, x2, g, u, m;
-  std::vector<size_t> T;  // [L * 7]
+  std::vector<size_t> hin, h1, rstd1, rstd2, x1, qkv, a, x2, gu, m;
+  std::vector<size_t> Tqkv, To, Tgu, Td;
   // shared
-  size_t o, d, dhA, dhB, dd, dm, dg, du, dx2a, dx2b, dh1, do_, da, dq, dk, dv, dx1q, dx1k, dx1v, lin_ws;
+  size_t o, d, dhA, dhB, dd, dm, dgu, dx2a, dx2b, dh1, do_, da, dqkv, dx1q, dx1k, dx1v, lin_ws;
   size_t lin_ws_bytes = 0;
 };
 
@@ -102,25 +109,26 @@ Plan make_plan(const sl_stack* s, int64_t M, int r) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  const size_t MD = static_cast<size_t>(M) * s->D, MK = static_cast<size_t>(M) * s->Dkv,
-               MF = static_cast<size_t>(M) * s->F;
+  const size_t MD = static_cast<size_t>(M) * s->D, MF = static_cast<size_t>(M) * s->F;
+  const size_t MQKV = static_cast<size_t>(M) * (s->D + 2 * s->Dkv);
   const int L = s->L;
   const int rr = r > 0 ? r : 0;
+  const size_t Tr = static_cast<size_t>(M) * (rr ? rr : 1) * 4;
   for (int l = 0; l < L; ++l) {
     P.hin.push_back(l == 0 ? 0 : take(MD * 4));
     P.h1.push_back(take(MD * 4));
     P.rstd1.push_back(take(M * 4));
     P.rstd2.push_back(take(M * 4));
     P.x1.push_back(take(MD * 2));
-    P.q.push_back(take(MD * 2));
-    P.k.push_back(take(MK * 2));
-    P.v.push_back(take(MK * 2));
+    P.qkv.push_back(take(MQKV * 2));
     P.a.push_back(take(MD * 2));
     P.x2.push_back(take(MD * 2));
-    P.g.push_back(take(MF * 2));
-    P.u.push_back(take(MF * 2));
+    P.gu.push_back(take(2 * MF * 2));
     P.m.push_back(take(MF * 2));
-    for (int p = 0; p < 7; ++p) P.T.push_back(take(static_cast<size_t>(M) * (rr ? rr : 1) * 4));
+    P.Tqkv.push_back(take(3 * Tr));
+    P.To.push_back(take(Tr));
+    P.Tgu.push_back(take(2 * Tr));
+    P.Td.push_back(take(Tr));
   }
   P.o = take(MD * 2);
   P.d = take(MD * 2);
@@ -128,26 +136,21 @@ Plan make_plan(const sl_stack* s, int64_t M, int r) {
   P.dhB = take(MD * 4);
   P.dd = take(MD * 2);
   P.dm = take(MF * 2);
-  P.dg = take(MF * 2);
-  P.du = take(MF * 2);
+  P.dgu = take(2 * MF * 2);
   P.dx2a = take(MD * 2);
   P.dx2b = take(MD * 2);
   P.dh1 = take(MD * 4);
   P.do_ = take(MD * 2);
   P.da = take(MD * 2);
-  P.dq = take(MD * 2);
-  P.dk = take(MK * 2);
-  P.dv = take(MK * 2);
+  P.dqkv = take(MQKV * 2);
   P.dx1q = take(MD * 2);
   P.dx1k = take(MD * 2);
   P.dx1v = take(MD * 2);
   Proj pr[7];
   proj_shapes(s->D, s->Dkv, s->F, pr);
   size_t lw = 0;
-  for (int p = 0; p < 7; ++p) {
-    const size_t b = linear_ws_bytes(M, pr[p].N, pr[p].K, rr);
-    if (b > lw) lw = b;
-  }
+  for (int p = 0; p < 7; ++p) lw = std::max(lw, linear_ws_bytes(M, pr[p].N, pr[p].K, rr));
+  if (rr) lw = std::max(lw, group_ws_bytes(M, 3, rr));
   P.lin_ws_bytes = lw;
   P.lin_ws = take(lw ? lw : 256);
   P.total = off;
@@ -167,6 +170,8 @@ struct StepCtx {
   float* const* dB;
   cudaStream_t stream;
   int accumulate = 0;
+  bool group_qkv = false;  // q, k, v as one projection group
+  bool group_gu = false;   // gate, up as one projection group
   uint64_t kernels = 0;
 
   template <typename T>
@@ -201,38 +206,76 @@ void weights_of(const sl_stack* s, const void* base, sl_weight w[7]) {
     if (_st != SL_OK) return _st;     \
   } while (0)
 
+// The q/k/v (p0 = 0, G = 3) or gate/up (p0 = 4, G = 2) weights as one NF4
+// weight: the blob keeps them back to back.
+sl_weight group_weight(const sl_weight w[7], int p0, int G) {
+  sl_weight g = w[p0];
+  for (int i = 1; i < G; ++i) g.N += w[p0 + i].N;
+  return g;
+}
+
 sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, float* h_out) {
   const Plan& P = *c.P;
   const sl_stack* s = c.s;
   const int64_t M = c.M;
-  const int D = static_cast<int>(s->D), Dkv = static_cast<int>(s->Dkv);
+  const int D = static_cast<int>(s->D), Dkv = static_cast<int>(s->Dkv), F = static_cast<int>(s->F);
   const int r = c.r;
+  const int64_t rr = r > 0 ? r : 1;
   auto A = [&](int p) { return r > 0 ? c.A[7 * l + p] : nullptr; };
   auto B = [&](int p) { return r > 0 ? c.B[7 * l + p] : nullptr; };
-  auto T = [&](int p) { return c.at<float>(P.T[7 * l + p]); };
+  void* lws = c.at<uint8_t>(P.lin_ws);
+  const size_t lwb = P.lin_ws_bytes;
   uint16_t* x1 = c.at<uint16_t>(P.x1[l]);
-  uint16_t* q = c.at<uint16_t>(P.q[l]);
-  uint16_t* k = c.at<uint16_t>(P.k[l]);
-  uint16_t* v = c.at<uint16_t>(P.v[l]);
+  uint16_t* qkv = c.at<uint16_t>(P.qkv[l]);
   uint16_t* a = c.at<uint16_t>(P.a[l]);
   uint16_t* x2 = c.at<uint16_t>(P.x2[l]);
-  uint16_t* g = c.at<uint16_t>(P.g[l]);
-  uint16_t* u = c.at<uint16_t>(P.u[l]);
+  uint16_t* gu = c.at<uint16_t>(P.gu[l]);
   uint16_t* m = c.at<uint16_t>(P.m[l]);
+  float* Tqkv = c.at<float>(P.Tqkv[l]);
+  float* Tgu = c.at<float>(P.Tgu[l]);
   float* h1 = c.at<float>(P.h1[l]);
   uint16_t* o = c.at<uint16_t>(P.o);
   uint16_t* d = c.at<uint16_t>(P.d);
   SL_TRY(glue_rms_fwd(h_in, nullptr, nullptr, x1, c.at<float>(P.rstd1[l]), M, D, c.stream));
-  SL_TRY(linear_fwd(&w[0], x1, M, A(0), B(0), r, c.alpha, q, T(0), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
-  SL_TRY(linear_fwd(&w[1], x1, M, A(1), B(1), r, c.alpha, k, T(1), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
-  SL_TRY(linear_fwd(&w[2], x1, M, A(2), B(2), r, c.alpha, v, T(2), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
-  SL_TRY(glue_mix_fwd(q, k, v, a, M, D, Dkv, c.stream));
-  SL_TRY(linear_fwd(&w[3], a, M, A(3), B(3), r, c.alpha, o, T(3), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
+  // q, k, v
+  const uint16_t *q, *k, *v;
+  int64_t ldq, ldkv;
+  if (c.group_qkv) {
+    const sl_weight wg = group_weight(w, 0, 3);
+    const int64_t Ng[3] = {D, Dkv, Dkv};
+    SL_TRY(group_fwd(&wg, 3, Ng, x1, M, A(0), B(0), r, c.alpha, qkv, Tqkv, c.stream));
+    q = qkv;
+    k = qkv + D;
+    v = qkv + D + Dkv;
+    ldq = ldkv = D + 2 * Dkv;
+  } else {
+    uint16_t* yq = qkv;
+    uint16_t* yk = qkv + M * D;
+    uint16_t* yv = yk + M * Dkv;
+    SL_TRY(linear_fwd(&w[0], x1, M, A(0), B(0), r, c.alpha, yq, Tqkv, lws, lwb, c.stream));
+    SL_TRY(linear_fwd(&w[1], x1, M, A(1), B(1), r, c.alpha, yk, Tqkv + M * rr, lws, lwb, c.stream));
+    SL_TRY(linear_fwd(&w[2], x1, M, A(2), B(2), r, c.alpha, yv, Tqkv + 2 * M * rr, lws, lwb, c.stream));
+    q = yq;
+    k = yk;
+    v = yv;
+    ldq = D;
+    ldkv = Dkv;
+  }
+  SL_TRY(glue_mix_fwd(q, k, v, a, M, D, Dkv, ldq, ldkv, c.stream));
+  SL_TRY(linear_fwd(&w[3], a, M, A(3), B(3), r, c.alpha, o, c.at<float>(P.To[l]), lws, lwb, c.stream));
   SL_TRY(glue_rms_fwd(h_in, o, h1, x2, c.at<float>(P.rstd2[l]), M, D, c.stream));
-  SL_TRY(linear_fwd(&w[4], x2, M, A(4), B(4), r, c.alpha, g, T(4), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
-  SL_TRY(linear_fwd(&w[5], x2, M, A(5), B(5), r, c.alpha, u, T(5), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
-  SL_TRY(glue_swiglu_fwd(g, u, m, M * s->F, c.stream));
-  SL_TRY(linear_fwd(&w[6], m, M, A(6), B(6), r, c.alpha, d, T(6), c.at<uint8_t>(P.lin_ws), P.lin_ws_bytes, c.stream));
+  // gate, up
+  if (c.group_gu) {
+    const sl_weight wg = group_weight(w, 4, 2);
+    const int64_t Ng[2] = {F, F};
+    SL_TRY(group_fwd(&wg, 2, Ng, x2, M, A(4), B(4), r, c.alpha, gu, Tgu, c.stream));
+    SL_TRY(glue_swiglu_fwd(gu, gu + F, m, M, F, 2 * F, c.stream));
+  } else {
+    SL_TRY(linear_fwd(&w[4], x2, M, A(4), B(4), r, c.alpha, gu, Tgu, lws, lwb, c.stream));
+    SL_TRY(linear_fwd(&w[5], x2, M, A(5), B(5), r, c.alpha, gu + M * F, Tgu + M * rr, lws, lwb, c.stream));
+    SL_TRY(glue_swiglu_fwd(gu, gu + M * F, m, M, F, F, c.stream));
+  }
+  SL_TRY(linear_fwd(&w[6], m, M, A(6), B(6), r, c.alpha, d, c.at<float>(P.Td[l]), lws, lwb, c.stream));
   SL_TRY(glue_resid_add(h1, d, h_out, M * s->D, c.stream));
   return SL_OK;
 }
@@ -244,47 +287,102 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
   const Plan& P = *c.P;
   const sl_stack* s = c.s;
   const int64_t M = c.M;
-  const int D = static_cast<int>(s->D), Dkv = static_cast<int>(s->Dkv);
+  const int D = static_cast<int>(s->D), Dkv = static_cast<int>(s->Dkv), F = static_cast<int>(s->F);
   const int r = c.r;
+  const int64_t rr = r > 0 ? r : 1;
   auto A = [&](int p) { return r > 0 ? c.A[7 * l + p] : nullptr; };
   auto B = [&](int p) { return r > 0 ? c.B[7 * l + p] : nullptr; };
-  auto T = [&](int p) { return c.at<float>(P.T[7 * l + p]); };
   auto dA = [&](int p) { return r > 0 ? c.dA[7 * l + p] : nullptr; };
   auto dB = [&](int p) { return r > 0 ? c.dB[7 * l + p] : nullptr; };
   void* lws = c.at<uint8_t>(P.lin_ws);
   const size_t lwb = P.lin_ws_bytes;
   uint16_t* dm = c.at<uint16_t>(P.dm);
-  uint16_t* dg = c.at<uint16_t>(P.dg);
-  uint16_t* du = c.at<uint16_t>(P.du);
+  uint16_t* dgu = c.at<uint16_t>(P.dgu);
   uint16_t* dx2a = c.at<uint16_t>(P.dx2a);
   uint16_t* dx2b = c.at<uint16_t>(P.dx2b);
   float* dh1 = c.at<float>(P.dh1);
   uint16_t* do_ = c.at<uint16_t>(P.do_);
   uint16_t* da = c.at<uint16_t>(P.da);
-  uint16_t* dq = c.at<uint16_t>(P.dq);
-  uint16_t* dk = c.at<uint16_t>(P.dk);
-  uint16_t* dv = c.at<uint16_t>(P.dv);
+  uint16_t* dqkv = c.at<uint16_t>(P.dqkv);
   uint16_t* dx1q = c.at<uint16_t>(P.dx1q);
   uint16_t* dx1k = c.at<uint16_t>(P.dx1k);
   uint16_t* dx1v = c.at<uint16_t>(P.dx1v);
-  SL_TRY(linear_bwd(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, T(6), dm, dA(6), dB(6), c.accumulate, lws,
-                    lwb, c.stream));
-  SL_TRY(glue_swiglu_bwd(dm, c.at<uint16_t>(P.g[l]), c.at<uint16_t>(P.u[l]), dg, du, M * s->F, c.stream));
-  SL_TRY(linear_bwd(&w[4], c.at<uint16_t>(P.x2[l]), dg, M, A(4), B(4), r, c.alpha, T(4), dx2a, dA(4), dB(4), c.accumulate,
-                    lws, lwb, c.stream));
-  SL_TRY(linear_bwd(&w[5], c.at<uint16_t>(P.x2[l]), du, M, A(5), B(5), r, c.alpha, T(5), dx2b, dA(5), dB(5), c.accumulate,
-                    lws, lwb, c.stream));
-  SL_TRY(glue_rms_bwd(dh2, dx2a, dx2b, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]), dh1, do_, M, D,
-                      c.stream));
-  SL_TRY(linear_bwd(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, T(3), da, dA(3), dB(3), c.accumulate, lws,
-                    lwb, c.stream));
-  SL_TRY(glue_mix_bwd(da, c.at<uint16_t>(P.q[l]), c.at<uint16_t>(P.k[l]), dq, dk, dv, M, D, Dkv, c.stream));
   const uint16_t* x1 = c.at<uint16_t>(P.x1[l]);
-  SL_TRY(linear_bwd(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, T(0), dx1q, dA(0), dB(0), c.accumulate, lws, lwb, c.stream));
-  SL_TRY(linear_bwd(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, T(1), dx1k, dA(1), dB(1), c.accumulate, lws, lwb, c.stream));
-  SL_TRY(linear_bwd(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, T(2), dx1v, dA(2), dB(2), c.accumulate, lws, lwb, c.stream));
-  SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, h_in, c.at<float>(P.rstd1[l]), dh, dh_bf16, M, D, c.stream));
+  const uint16_t* x2 = c.at<uint16_t>(P.x2[l]);
+  const uint16_t* qkv = c.at<uint16_t>(P.qkv[l]);
+  const uint16_t* gu = c.at<uint16_t>(P.gu[l]);
+  const float* Tqkv = c.at<float>(P.Tqkv[l]);
+  const float* Tgu = c.at<float>(P.Tgu[l]);
+  SL_TRY(linear_bwd(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, c.at<float>(P.Td[l]), dm, dA(6),
+                    dB(6), c.accumulate, lws, lwb, c.stream));
+  // gate, up
+  if (c.group_gu) {
+    SL_TRY(glue_swiglu_bwd(dm, gu, gu + F, dgu, dgu + F, M, F, 2 * F, c.stream));
+    const sl_weight wg = group_weight(w, 4, 2);
+    const int64_t Ng[2] = {F, F};
+    SL_TRY(group_bwd(&wg, 2, Ng, x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate, lws, lwb,
+                     c.stream));
+    SL_TRY(glue_rms_bwd(dh2, dx2a, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]), dh1, do_, M, D,
+                        c.stream));
+  } else {
+    SL_TRY(glue_swiglu_bwd(dm, gu, gu + M * F, dgu, dgu + M * F, M, F, F, c.stream));
+    SL_TRY(linear_bwd(&w[4], x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate, lws, lwb,
+                      c.stream));
+    SL_TRY(linear_bwd(&w[5], x2, dgu + M * F, M, A(5), B(5), r, c.alpha, Tgu + M * rr, dx2b, dA(5), dB(5),
+                      c.accumulate, lws, lwb, c.stream));
+    SL_TRY(glue_rms_bwd(dh2, dx2a, dx2b, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]), dh1, do_, M, D,
+                        c.stream));
+  }
+  SL_TRY(linear_bwd(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, c.at<float>(P.To[l]), da, dA(3),
+                    dB(3), c.accumulate, lws, lwb, c.stream));
+  // q, k, v
+  if (c.group_qkv) {
+    const int64_t ld = D + 2 * Dkv;
+    SL_TRY(glue_mix_bwd(da, qkv, qkv + D, dqkv, dqkv + D, dqkv + D + Dkv, M, D, Dkv, ld, ld, c.stream));
+    const sl_weight wg = group_weight(w, 0, 3);
+    const int64_t Ng[3] = {D, Dkv, Dkv};
+    SL_TRY(group_bwd(&wg, 3, Ng, x1, dqkv, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate, lws, lwb,
+                     c.stream));
+    SL_TRY(glue_rms_bwd(dh1, dx1q, nullptr, nullptr, h_in, c.at<float>(P.rstd1[l]), dh, dh_bf16, M, D, c.stream));
+  } else {
+    uint16_t* dq = dqkv;
+    uint16_t* dk = dqkv + M * D;
+    uint16_t* dv = dk + M * Dkv;
+    SL_TRY(glue_mix_bwd(da, qkv, qkv + M * D, dq, dk, dv, M, D, Dkv, D, Dkv, c.stream));
+    SL_TRY(linear_bwd(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate, lws, lwb,
+                      c.stream));
+    SL_TRY(linear_bwd(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, Tqkv + M * rr, dx1k, dA(1), dB(1), c.accumulate, lws,
+                      lwb, c.stream));
+    SL_TRY(linear_bwd(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, Tqkv + 2 * M * rr, dx1v, dA(2), dB(2), c.accumulate,
+                      lws, lwb, c.stream));
+    SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, h_in, c.at<float>(P.rstd1[l]), dh, dh_bf16, M, D, c.stream));
+  }
   return SL_OK;
+}
+
+// Projections p0 .. p0+G-1 run as one group when the weights are NF4, M
+// allows the CTA-pair GEMM, every projection is a whole number of 256-column
+// tiles, the folded rank fits, and every layer stores the group's adapters
+// and their gradients back to back.
+bool can_group(const sl_stack* s, int64_t M, int r, int p0, int G, const void* const* A, const void* const* B,
+               float* const* dA, float* const* dB) {
+  if (s->kind != SL_WEIGHT_NF4 || M <= 128 || M >= (1LL << 31)) return false;
+  if (r > 0 && G * r > 64) return false;
+  Proj p[7];
+  proj_shapes(s->D, s->Dkv, s->F, p);
+  for (int i = 0; i < G; ++i)
+    if (p[p0 + i].N % 256) return false;  // a GEMM tile must not straddle two projections
+  if (r == 0) return true;
+  for (int l = 0; l < s->L; ++l)
+    for (int i = 1; i < G; ++i) {
+      const int cur = 7 * l + p0 + i, prev = cur - 1;
+      const size_t a_prev = static_cast<size_t>(r) * p[p0 + i - 1].K, b_prev = static_cast<size_t>(p[p0 + i - 1].N) * r;
+      if (static_cast<const uint8_t*>(A[cur]) != static_cast<const uint8_t*>(A[prev]) + a_prev * 2) return false;
+      if (static_cast<const uint8_t*>(B[cur]) != static_cast<const uint8_t*>(B[prev]) + b_prev * 2) return false;
+      if (dA[cur] != dA[prev] + a_prev) return false;
+      if (dB[cur] != dB[prev] + b_prev) return false;
+    }
+  return true;
 }
 
 // Make sure buffer l % 2 holds layer l (copy only if it does not already).
@@ -409,6 +507,8 @@ extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float
                                       " bytes)");
   StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, stream};
   c.accumulate = accumulate ? 1 : 0;
+  c.group_qkv = can_group(s, M, r, 0, 3, A, B, dA, dB);
+  c.group_gu = can_group(s, M, r, 4, 2, A, B, dA, dB);
   const uint64_t launches0 = launch_count();
   const int L = s->L;
   const bool streamed = mode == SL_MODE_STREAMED;

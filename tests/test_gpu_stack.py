@@ -13,9 +13,13 @@ pytestmark = pytest.mark.gpu
 class Setup:
     """Blobs (pinned host + device copies), adapters and grads for one synthetic stack."""
 
-    def __init__(self, sl, kind, L, M, D, Dkv, F, r, alpha, seed, with_oracle=True, torch_weights=False):
+    def __init__(self, sl, kind, L, M, D, Dkv, F, r, alpha, seed, with_oracle=True, torch_weights=False,
+                 packed=False):
+        """packed: each layer's adapters (and gradients) back to back, so that
+        NF4 stacks with M > 128 run q/k/v and gate/up as projection groups."""
         self.sl, self.kind, self.L, self.M, self.D, self.Dkv, self.F, self.r, self.alpha = \
             sl, kind, L, M, D, Dkv, F, r, alpha
+        self.packed = packed
         shapes = sl.proj_shapes(D, Dkv, F)
         self.host_blobs, self.dev_blobs, self.A, self.B, self.ref_layers = [], [], [], [], []
         if torch_weights:   # large stacks: weights drawn on the device from a seeded torch generator
@@ -50,8 +54,29 @@ class Setup:
             self.h0_np, self.dh_np = c["h0"], c["dh_top"]
             self.h0 = torch.from_numpy(c["h0"]).cuda()
             self.dh = torch.from_numpy(c["dh_top"]).cuda()
+        if packed:
+            sa, sb = sl.adapter_shapes(D, Dkv, F, r)
+            for l in range(L):
+                for views, src in ((sl.packed_views(sa, torch.bfloat16), self.A), (sl.packed_views(sb, torch.bfloat16), self.B)):
+                    for p in range(7):
+                        views[p].copy_(src[7 * l + p])
+                        src[7 * l + p] = views[p]
         self.stack = sl.Stack(kind, D, Dkv, F, self.host_blobs, self.dev_blobs)
         self.ws = torch.empty(self.stack.workspace_size(M, r), dtype=torch.uint8, device="cuda")
+
+    def grads(self):
+        """NaN-filled gradient buffers shaped like the adapters (packed like them)."""
+        if not self.packed:
+            return ([torch.full_like(a, float("nan"), dtype=torch.float32) for a in self.A],
+                    [torch.full_like(b, float("nan"), dtype=torch.float32) for b in self.B])
+        sa, sb = self.sl.adapter_shapes(self.D, self.Dkv, self.F, self.r)
+        dA, dB = [], []
+        for _ in range(self.L):
+            dA += self.sl.packed_views(sa, torch.float32)
+            dB += self.sl.packed_views(sb, torch.float32)
+        for t in dA + dB:
+            t.fill_(float("nan"))
+        return dA, dB
 
     def _add_blob(self, blob):
         h = torch.empty(blob.numel(), dtype=torch.uint8, pin_memory=True)
@@ -63,8 +88,7 @@ class Setup:
         sl = self.sl
         hL = torch.empty(self.M, self.D, device="cuda")
         dh0 = torch.empty_like(hL)
-        dA = [torch.full_like(a, float("nan"), dtype=torch.float32) for a in self.A]
-        dB = [torch.full_like(b, float("nan"), dtype=torch.float32) for b in self.B]
+        dA, dB = self.grads()
         self.stack.step(mode, self.h0, self.dh, self.A, self.B, self.r, self.alpha, hL, dh0, dA, dB, self.ws)
         sl.sl_check_device_errors()
         return hL, dh0, dA, dB
@@ -99,6 +123,35 @@ def test_small_stack_matches_oracle_and_resident(gpu_lib, kind_name):
     S.stack.close()
 
 
+def test_grouped_stack_matches_oracle_and_resident(gpu_lib):
+    """NF4, M > 128, adapters back to back: q/k/v and gate/up run as projection
+    groups; same oracle tolerance, streamed == resident bit for bit, and close
+    to the per-projection run of the same stack."""
+    sl = gpu_lib
+    S = Setup(sl, sl.SL_WEIGHT_NF4, L=3, M=160, D=512, Dkv=256, F=768, r=16, alpha=32.0, seed=23, packed=True)
+    hL, dh0, dA, dB = S.run(sl.SL_MODE_STREAMED)
+    ohL, odh0, ograds = stack.stack_step(S.h0_np, S.dh_np, S.ref_layers, 32.0, rnd=True)
+    assert rel_fro(host(hL), ohL) <= BF16_TOL
+    assert rel_fro(host(dh0), odh0) <= BF16_TOL
+    for l in range(S.L):
+        for p, n in enumerate(si.PROJ_NAMES):
+            assert rel_fro(host(dA[7 * l + p]), ograds[l][n][0]) <= BF16_TOL, (l, n)
+            assert rel_fro(host(dB[7 * l + p]), ograds[l][n][1]) <= BF16_TOL, (l, n)
+    r_ = S.run(sl.SL_MODE_RESIDENT)
+    for x, y in zip((hL, dh0, *dA, *dB), (r_[0], r_[1], *r_[2], *r_[3])):
+        assert same_bits(x, y)
+    # the same stack with separately allocated adapters runs projection by projection
+    hL_u, dh0_u = torch.empty_like(hL), torch.empty_like(dh0)
+    dA_u = [torch.empty(a.shape, device="cuda") for a in S.A]
+    dB_u = [torch.empty(b.shape, device="cuda") for b in S.B]
+    A_u = [a.clone() for a in S.A]
+    B_u = [b.clone() for b in S.B]
+    S.stack.step(sl.SL_MODE_STREAMED, S.h0, S.dh, A_u, B_u, 16, 32.0, hL_u, dh0_u, dA_u, dB_u, S.ws)
+    sl.sl_check_device_errors()
+    assert rel_fro(host(hL_u), host(hL)) <= 2e-3 and rel_fro(host(dh0_u), host(dh0)) <= 5e-3
+    S.stack.close()
+
+
 def test_two_full_width_layers_match_oracle(gpu_lib):
     """Llama-3.1-8B layer widths (bf16 base so the oracle needs no 218M-element quantisation), M=64."""
     sl = gpu_lib
@@ -115,13 +168,14 @@ def test_two_full_width_layers_match_oracle(gpu_lib):
     S.stack.close()
 
 
-@pytest.mark.parametrize("kind_name,L", [("nf4", 6), ("bf16", 4)])
-def test_full_width_streamed_equals_resident_bitwise(gpu_lib, kind_name, L):
-    """8B-shaped layers (bf16 layers are 416 MiB, above the ~165 MiB size of the pages' NF4 bug)."""
+@pytest.mark.parametrize("kind_name,L,packed", [("nf4", 6, False), ("nf4", 4, True), ("bf16", 4, False)])
+def test_full_width_streamed_equals_resident_bitwise(gpu_lib, kind_name, L, packed):
+    """8B-shaped layers (bf16 layers are 416 MiB, above the ~165 MiB size of the pages' NF4 bug);
+    packed adapters run the NF4 layers' q/k/v and gate/up as projection groups."""
     sl = gpu_lib
     kind = sl.SL_WEIGHT_NF4 if kind_name == "nf4" else sl.SL_WEIGHT_BF16
     S = Setup(sl, kind, L=L, M=160, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0, seed=77,
-              with_oracle=False, torch_weights=True)
+              with_oracle=False, torch_weights=True, packed=packed)
     a = S.run(sl.SL_MODE_STREAMED)
     b = S.run(sl.SL_MODE_RESIDENT)
     for x, y in zip((a[0], a[1], *a[2], *a[3]), (b[0], b[1], *b[2], *b[3])):
