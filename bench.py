@@ -234,7 +234,8 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     extra = {}
     dominant = ("nf4_fwd", "nf4_dx")
-    kname = "gemm_nf4_pair_kernel (fused NF4 dequant + LoRA fold, CTA pairs; fwd and dX)"
+    kname = ("gemm_nf4_pair_persistent_kernel / gemm_nf4_pair_kernel (fused NF4 dequant + LoRA fold, "
+             "CTA pairs; fwd and dX)")
     h2d_peak = None
 
     if w["kind"] == "stack":
@@ -244,18 +245,22 @@ def run_ours(args):
             kname = "gemm_tc_kernel<BF16> (bf16 base + LoRA fold; fwd and dX)"
         D, Dkv, F, L, r, alpha = w["D"], w["Dkv"], w["F"], w["L"], w["r"], w["alpha"]
         shapes = sl.proj_shapes(D, Dkv, F)
-        host_blobs, A, B = [], [], []
+        sa, sb = sl.adapter_shapes(D, Dkv, F, r)
+        host_blobs, A, B, dA, dB = [], [], [], [], []
         for l in range(L):
             blob = sl.build_layer_blob(kind, D, Dkv, F, [rnd((N, K), 0.02) for N, K in shapes])
             h = torch.empty(blob.numel(), dtype=torch.uint8, pin_memory=True)
             h.copy_(blob)
             host_blobs.append(h)
             del blob
-            for N, K in shapes:
-                A.append(rnd((r, K), 0.02))
-                B.append(rnd((N, r), 0.02))
-        dA = [torch.empty(a.shape, dtype=torch.float32, device=dev) for a in A]
-        dB = [torch.empty(b.shape, dtype=torch.float32, device=dev) for b in B]
+            # each layer's adapters back to back: q/k/v and gate/up run as projection groups
+            la, lb = sl.packed_views(sa, torch.bfloat16, dev), sl.packed_views(sb, torch.bfloat16, dev)
+            for t, (n0, n1) in zip(la + lb, sa + sb):
+                t.copy_(rnd((n0, n1), 0.02))
+            A += la
+            B += lb
+            dA += sl.packed_views(sa, torch.float32, dev)
+            dB += sl.packed_views(sb, torch.float32, dev)
         h0 = torch.randn(M, D, generator=gen, device=dev).to(torch.bfloat16).float()
         dh = torch.randn(M, D, generator=gen, device=dev).to(torch.bfloat16).float()
         hL = torch.empty(M, D, device=dev)
@@ -281,46 +286,66 @@ def run_ours(args):
                   "alpha": alpha, "base": "NF4 blocksize 64 fp32 absmax" if kind == sl.SL_WEIGHT_NF4 else "bf16",
                   "l2": f"inputs larger than L2 ({stk.host_bytes / 1e9:.1f} GB streamed base + activations)"}
     elif w["kind"] == "layer":
+        # One decoder layer's seven projections as a framework runs them: q/k/v
+        # read the same input and run as one projection group, gate/up likewise;
+        # o and down alone.  NF4 weights of a group back to back, adapters too.
         D, Dkv, F, r, alpha = w["D"], w["Dkv"], w["F"], w["r"], w["alpha"]
-        lin = []
-        for name, N, K in proj_shapes(D, Dkv, F):
-            Wt = rnd((N, K), 0.02)
-            codes = torch.empty(N * K // 2, dtype=torch.uint8, device=dev)
-            absmax = torch.empty(N * K // 64, dtype=torch.float32, device=dev)
-            sl.sl_nf4_quantize(Wt, codes, absmax)
-            del Wt
-            lin.append(dict(w=sl.Weight.nf4(codes, absmax, N, K), X=rnd((M, K), 1.0), dY=rnd((M, N), 1.0),
-                            A=rnd((r, K), 0.02), B=rnd((N, r), 0.02),
-                            Y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
-                            T=torch.empty(M, r, dtype=torch.float32, device=dev),
-                            dX=torch.empty(M, K, dtype=torch.bfloat16, device=dev),
-                            dA=torch.empty(r, K, device=dev), dB=torch.empty(N, r, device=dev),
-                            ws=torch.empty(sl.sl_lora_linear_workspace_size(M, N, K, r), dtype=torch.uint8,
-                                           device=dev), N=N, K=K))
+        shp = dict(zip(("q", "k", "v", "o", "gate", "up", "down"), [(N, K) for _, N, K in proj_shapes(D, Dkv, F)]))
+        units = []
+        for names in (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)):
+            N_g = [shp[n][0] for n in names]
+            K = shp[names[0]][1]
+            NN = sum(N_g)
+            codes = torch.empty(NN * K // 2, dtype=torch.uint8, device=dev)
+            absmax = torch.empty(NN * K // 64, dtype=torch.float32, device=dev)
+            row = 0
+            for N in N_g:   # quantise each projection into its rows of the group weight
+                Wt = rnd((N, K), 0.02)
+                sl.sl_nf4_quantize(Wt, codes[row * K // 2:(row + N) * K // 2], absmax[row * K // 64:(row + N) * K // 64])
+                row += N
+                del Wt
+            G = len(N_g)
+            units.append(dict(w=sl.Weight.nf4(codes, absmax, NN, K), N_g=N_g, G=G, N=NN, K=K, X=rnd((M, K), 1.0),
+                              dY=rnd((M, NN), 1.0), A=rnd((G * r, K), 0.02), B=rnd((NN, r), 0.02),
+                              Y=torch.empty(M, NN, dtype=torch.bfloat16, device=dev),
+                              T=torch.empty(M, G * r, dtype=torch.float32, device=dev),
+                              dX=torch.empty(M, K, dtype=torch.bfloat16, device=dev),
+                              dA=torch.empty(G * r, K, device=dev), dB=torch.empty(NN, r, device=dev),
+                              ws=torch.empty(max(sl.sl_lora_group_workspace_size(M, G, r),
+                                                 sl.sl_lora_linear_workspace_size(M, NN, K, r)),
+                                             dtype=torch.uint8, device=dev)))
 
         def step():
-            for p in lin:
-                sl.sl_lora_linear_fwd(p["w"], p["X"], p["A"], p["B"], r, alpha, p["Y"], p["T"], p["ws"])
-                sl.sl_lora_linear_bwd(p["w"], p["X"], p["dY"], p["A"], p["B"], r, alpha, p["T"], p["dX"], p["dA"],
-                                      p["dB"], False, p["ws"])
+            for u in units:
+                if u["G"] > 1:
+                    sl.sl_lora_group_fwd(u["w"], u["N_g"], u["X"], u["A"], u["B"], r, alpha, u["Y"], u["T"])
+                    sl.sl_lora_group_bwd(u["w"], u["N_g"], u["X"], u["dY"], u["A"], u["B"], r, alpha, u["T"], u["dX"],
+                                         u["dA"], u["dB"], False, u["ws"])
+                else:
+                    sl.sl_lora_linear_fwd(u["w"], u["X"], u["A"], u["B"], r, alpha, u["Y"], u["T"], u["ws"])
+                    sl.sl_lora_linear_bwd(u["w"], u["X"], u["dY"], u["A"], u["B"], r, alpha, u["T"], u["dX"], u["dA"],
+                                          u["dB"], False, u["ws"])
 
-        hosts = [(p["X"].cpu().pin_memory(), p["dY"].cpu().pin_memory()) for p in lin]
-        res_h = torch.empty(7, 8, dtype=torch.float32, pin_memory=True)
+        hosts = [(u["X"].cpu().pin_memory(), u["dY"].cpu().pin_memory()) for u in units]
+        res_h = torch.empty(len(units), 8, dtype=torch.float32, pin_memory=True)
 
         def e2e_step():
-            for p, (xh, yh) in zip(lin, hosts):
-                p["X"].copy_(xh, non_blocking=True)
-                p["dY"].copy_(yh, non_blocking=True)
+            for u, (xh, yh) in zip(units, hosts):
+                u["X"].copy_(xh, non_blocking=True)
+                u["dY"].copy_(yh, non_blocking=True)
             step()
-            for i, p in enumerate(lin):   # a slice of every adapter gradient read back
-                res_h[i].copy_(p["dA"][0, :8], non_blocking=True)
+            for i, u in enumerate(units):   # a slice of every adapter gradient read back
+                res_h[i].copy_(u["dA"][0, :8], non_blocking=True)
         e2e_bytes = (sum(xh.numel() * 2 + yh.numel() * 2 for xh, yh in hosts), res_h.numel() * 4)
-        # algorithmic work: base fwd + dX (4 M N K) and the LoRA side products (T, U, fold x2, dA, dB)
-        flops = sum(4.0 * M * p["N"] * p["K"] + 6.0 * M * r * (p["N"] + p["K"]) for p in lin)
-        nbytes = sum(2 * (p["N"] * p["K"] * 0.5625) + 3 * (M * p["K"] * 2) + 3 * (M * p["N"] * 2) for p in lin)
+        # algorithmic work per projection: base fwd + dX (4 M N K) and the LoRA side
+        # products (T, U, fold x2, dA, dB); bytes: weights twice, activations
+        pj = [shp[n] for n in ("q", "k", "v", "o", "gate", "up", "down")]
+        flops = sum(4.0 * M * N * K + 6.0 * M * r * (N + K) for N, K in pj)
+        nbytes = sum(2 * (N * K * 0.5625) + 3 * (M * K * 2) + 3 * (M * N * 2) for N, K in pj)
         extra["step_roofline_inputs"] = {"flops": flops, "bytes": nbytes}
         config = {"workload": w["name"], "tokens": M, "D": D, "Dkv": Dkv, "F": F, "rank": r, "alpha": alpha,
-                  "base": "NF4 blocksize 64 fp32 absmax", "l2": "inputs larger than L2 (~0.8 GB touched per step)"}
+                  "base": "NF4 blocksize 64 fp32 absmax", "grouping": "q/k/v and gate/up as projection groups",
+                  "l2": "inputs larger than L2 (~0.8 GB touched per step)"}
     else:  # cross-entropy
         D, V, chunk = w["D"], w["V"], w["chunk"]
         dominant = ("ce_lse", "ce_softmax", "ce_dh")
@@ -455,9 +480,15 @@ def run_ours(args):
     else:
         fl, nb = extra["step_roofline_inputs"]["flops"], extra["step_roofline_inputs"]["bytes"]
         t_roof = max(fl / (peaks["bf16_tflops"] * 1e12), nb / (peaks["hbm_gbs"] * 1e9))
+        sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        t_roof_s = max(fl / (sus * 1e12), nb / (peaks["hbm_gbs"] * 1e9))
         line["step_roofline"] = {"algorithmic_flops": fl, "algorithmic_bytes": nb,
                                  "roofline_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3),
-                                 "peaks": f"{peak_src} bf16_tflops (burst) and hbm_gbs"}
+                                 "peaks": f"{peak_src} bf16_tflops (burst) and hbm_gbs",
+                                 "roofline_ms_sustained": t_roof_s * 1e3,
+                                 "frac_sustained": t_roof_s / (ms_step * 1e-3),
+                                 "peaks_sustained": f"{peak_src} bf16_tflops_sustained (multi-ms step under the "
+                                                    "power cap) and hbm_gbs"}
         if "extra_bytes_per_logit" in extra:
             line["extra_device_bytes_per_logit"] = extra["extra_bytes_per_logit"]
     if rank == 0:
