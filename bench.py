@@ -79,10 +79,15 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # the sampler's first line, so that the timed region is covered from its start
+        t0 = time.time()
+        while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -399,6 +404,7 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
+    launches0 = sl.sl_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -406,6 +412,7 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     clk = clocks.stop()
+    launches_timed = sl.sl_launch_count() - launches0
     ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / args.steps
     value = world * M * args.steps / (ms_total * 1e-3)
@@ -454,13 +461,13 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded device RNG)",
             "config": dict(config, parallelism=f"replicas x{world} (no collective on the data path)"),
-            "roofline": roofline, "kernels": per_variant, "e2e": e2e, "clocks": clk}
+            "roofline": roofline, "kernels": per_variant, "e2e": e2e, "clocks": clk,
+            "gpu_launches": int(launches_timed)}
     if w["kind"] == "stack":
         line["stream"] = {"bound": "pcie_h2d", "h2d_bytes_per_step": h2d_step,
                           "achieved_gbs": h2d_step / (ms_step * 1e-3) / 1e9, "peak_gbs": h2d_peak,
                           "frac": h2d_step / (ms_step * 1e-3) / 1e9 / h2d_peak,
                           "peak_source": "measured in this run: pinned 1 GiB cudaMemcpyAsync, best of 10"}
-        line["gpu_launches"] = int(kernels_step * args.steps)
         line["preflight"] = {"host_bytes": stk.host_bytes, "buffer_bytes": stk.buffer_bytes}
         if not args.no_resident:
             dev_blobs = [hb.to(dev) for hb in host_blobs]
@@ -505,7 +512,8 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: 10 for the stacks, 200 for layer8b, 50 for ce -- ~0.3-1.5 s)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack8b")
@@ -513,6 +521,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-resident", action="store_true")
     args = ap.parse_args()
+    if args.steps <= 0:
+        args.steps = {"layer8b": 200, "ce": 50}.get(args.workload, 10)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

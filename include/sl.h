@@ -86,6 +86,10 @@ const char* sl_last_error(void);
 /* ABI version (major*10000 + minor*100 + patch). */
 int32_t sl_version(void);
 
+/* Kernels libsl has launched in this process so far (all devices and
+ * threads); the difference over a region counts the region's launches. */
+uint64_t sl_launch_count(void);
+
 /* Host copy of the library's NF4 levels (16 fp32, ascending).  The levels are
  * the published NormalFloat-4 construction (QLoRA); the pages name NF4 but do
  * not print them.  Never fails. */

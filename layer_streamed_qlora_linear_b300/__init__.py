@@ -47,6 +47,7 @@ _P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctype
 _SIGS = {
     "sl_last_error": (ctypes.c_char_p, []),
     "sl_version": (_I32, []),
+    "sl_launch_count": (ctypes.c_uint64, []),
     "sl_nf4_code_table": (None, [_P]),
     "sl_check_device_errors": (_I32, [_P]),
     "sl_debug_timeout_probe": (_I32, [_I64, _I32, _P]),
@@ -131,6 +132,11 @@ def sl_check_device_errors(stream=None):
 
 def sl_debug_timeout_probe(limit_ns: int, mbarrier: bool = False, stream=None):
     _check(lib().sl_debug_timeout_probe(int(limit_ns), int(bool(mbarrier)), _stream(stream)))
+
+
+def sl_launch_count() -> int:
+    """libsl kernel launches so far in this process."""
+    return int(lib().sl_launch_count())
 
 
 GEMM_VARIANTS = ("nf4_fwd", "nf4_dx", "bf16_fwd", "bf16_dx", "ce_lse", "ce_softmax", "ce_dh")

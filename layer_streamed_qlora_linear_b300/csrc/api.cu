@@ -109,6 +109,8 @@ const char* sl_last_error(void) { return g_last_error.c_str(); }
 
 int32_t sl_version(void) { return 1 * 10000 + 0 * 100 + 0; }
 
+uint64_t sl_launch_count(void) { return sl::launch_count(); }
+
 void sl_nf4_code_table(float out[16]) {
   if (!out) return;
   for (int i = 0; i < 16; ++i) {
