@@ -111,15 +111,15 @@ sl_status sl_debug_timeout_probe(int64_t limit_ns, int32_t mbarrier, cudaStream_
  * starts recording a CUDA event pair, on the launching stream, around every
  * tensor-core launch; enable == 0 stops recording.  Costs one event pair
  * per launch.  Variants: 0 NF4 forward, 1 NF4 dX, 2 bf16 forward, 3 bf16
- * dX, 4 CE logits (lse partials), 5 CE softmax chunk, 6 CE dH
- * accumulation, 7 rank-r T = X A^T, 8 rank-r U = dY B, 9 rank-r dA / dB. */
+ * dX, 4 CE logits chunk (exp epilogue), 5 CE dH accumulation, 6 rank-r
+ * T = X A^T, 7 rank-r U = dY B, 8 rank-r dA / dB. */
 sl_status sl_kernel_timing(int32_t enable);
 
 /* Totals over the launches of one variant recorded since timing was
  * enabled: launch count, summed device time in ms (waits for the recorded
- * events) and algorithmic work: FLOPs for the GEMM variants 0-6 (2 M N K,
+ * events) and algorithmic work: FLOPs for the GEMM variants 0-5 (2 M N K,
  * plus 2 M N r for the folded LoRA side product), bytes for the rank-r
- * passes 7-9 (the large operand once, the rank-r operands and the output). */
+ * passes 6-8 (the large operand once, the rank-r operands and the output). */
 sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms, double* work);
 
 /* ------------------------------------------------------------- NF4 (K0/K1) */

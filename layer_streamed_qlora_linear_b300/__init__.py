@@ -139,8 +139,8 @@ def sl_launch_count() -> int:
     return int(lib().sl_launch_count())
 
 
-GEMM_VARIANTS = ("nf4_fwd", "nf4_dx", "bf16_fwd", "bf16_dx", "ce_lse", "ce_softmax", "ce_dh")
-RANK_R_VARIANTS = ("rank_t", "rank_u", "rank_grad")  # timing variants 7, 8, 9 (work in bytes)
+GEMM_VARIANTS = ("nf4_fwd", "nf4_dx", "bf16_fwd", "bf16_dx", "ce_logits", "ce_dh")
+RANK_R_VARIANTS = ("rank_t", "rank_u", "rank_grad")  # timing variants 6, 7, 8 (work in bytes)
 
 
 def sl_kernel_timing(enable: bool):
@@ -149,7 +149,7 @@ def sl_kernel_timing(enable: bool):
 
 def sl_kernel_timing_read(variant: int):
     """(launches, ms, work) of one timed variant since timing was enabled:
-    work is FLOPs for GEMM variants 0-6 and bytes for rank-r variants 7-9."""
+    work is FLOPs for GEMM variants 0-5 and bytes for rank-r variants 6-8."""
     n, ms, fl = ctypes.c_uint64(0), ctypes.c_double(0), ctypes.c_double(0)
     _check(lib().sl_kernel_timing_read(int(variant), ctypes.byref(n), ctypes.byref(ms), ctypes.byref(fl)))
     return n.value, ms.value, fl.value

@@ -1,17 +1,22 @@
 // Step a8: cross-entropy over the LM head, loss and dH, without the logits.
 //
 // "Exact Layer Streaming ..." (abstract) measures the cross-entropy logits
-// term at 14 bytes per logit element; here no [M, V] tensor exists at all:
-//   pass 1  one tcgen05 GEMM Z = H W^T whose epilogue keeps, per row and per
-//           256-wide vocab tile, only (max, sum exp) and the label's logit;
-//   rows    lse_i = log sum exp(z_i) from the tile partials (fixed order),
-//           loss = mean over valid rows of lse_i - z_i,label (fixed order);
-//   pass 2  per vocab chunk of chunk_V rows of W: recompute Z_c, write
-//           G_c = softmax(Z_c) / N_valid (bf16, [M, chunk_V] scratch), then
-//           dH += G_c W_c (fp32, tcgen05 with an MN-major W operand);
-//   last    dH_i -= W[label_i] / N_valid (fp32 gather; the one-hot part is
-//           kept out of the bf16 chunk so that it is exact).
-// Extra device bytes: the chunk scratch plus O(M * V / 256) partials.
+// term at 14 bytes per logit element; here no [M, V] tensor exists, and the
+// logits are computed once (online softmax over vocab chunks):
+//   per chunk c of chunk_V rows of W
+//     logits  one tcgen05 GEMM Z_c = H W_c^T whose epilogue writes, per row
+//             and 128-column half tile h, its max m_h, P = bf16(exp(z - m_h))
+//             into a [M, chunk_V] scratch and s_h = sum exp(z - m_h), and
+//             gathers the label's logit;
+//     rows    per row: the chunk's max and sum from its half tiles (fixed
+//             order), the running max m and sum S updated, P rescaled in
+//             place to exp(z - m_new), and alpha = exp(m_old - m_new);
+//     dH      acc = alpha * acc + P W_c (fp32, tcgen05 with an MN-major W);
+//   last      lse = m + log S, loss = mean over valid rows of lse - z_label
+//             (fixed order), dH = acc / (S N_valid) - W[label] / N_valid
+//             (the one-hot part exact in fp32, ignored rows 0).
+// Two passes over the head instead of three; extra device bytes: the chunk
+// scratch plus O(M * chunk_V / 128) partials.
 #include "common.cuh"
 #include "gemm.cuh"
 
@@ -20,12 +25,13 @@ namespace sl {
 namespace {
 
 struct CEPlan {
-  size_t part_max, part_sum, label_logit, lse, term, scale, G, total;
-  int ntiles;
+  size_t part_max, part_sum, label_logit, run_max, run_sum, alpha, lse, term, scale, P, total;
+  int halves;  // 128-column half tiles of a chunk
 };
 
 CEPlan ce_plan(int64_t M, int64_t D, int64_t V, int64_t chunk_V) {
   (void)D;
+  (void)V;
   CEPlan p{};
   size_t off = 0;
   auto take = [&](size_t b) {
@@ -33,52 +39,77 @@ CEPlan ce_plan(int64_t M, int64_t D, int64_t V, int64_t chunk_V) {
     off = align_up(off + b, 256);
     return o;
   };
-  p.ntiles = static_cast<int>(ceil_div(V, kBN)) * 2;   // two column halves per 256-wide tile
-  p.part_max = take(static_cast<size_t>(M) * p.ntiles * 4);
-  p.part_sum = take(static_cast<size_t>(M) * p.ntiles * 4);
+  p.halves = static_cast<int>(ceil_div(chunk_V, kBN)) * 2;
+  p.part_max = take(static_cast<size_t>(M) * p.halves * 4);
+  p.part_sum = take(static_cast<size_t>(M) * p.halves * 4);
   p.label_logit = take(M * 4);
+  p.run_max = take(M * 4);
+  p.run_sum = take(M * 4);
+  p.alpha = take(M * 4);
   p.lse = take(M * 4);
   p.term = take(M * 4);
   p.scale = take(M * 4);
-  p.G = take(static_cast<size_t>(M) * chunk_V * 2);
+  p.P = take(static_cast<size_t>(M) * chunk_V * 2);
   p.total = off;
   return p;
 }
 
-// One warp per row: lse from the per-half-tile (max, sum exp) partials; the row's
-// loss term lse - z_label (0 for ignored rows).  Out-of-range labels are
-// reported through the error word and treated as ignored.
-__global__ void ce_row_kernel(const float* __restrict__ pmax, const float* __restrict__ psum, int ntiles,
-                              const float* __restrict__ zlab, const int32_t* __restrict__ labels, int ignore, int V,
-                              int64_t M, float* __restrict__ lse, float* __restrict__ term, int* err) {
+// One warp per row, after a chunk's logits GEMM: the chunk's max and sum from
+// its half-tile partials (fixed order), the running (max, sum) updated, the
+// row's P rescaled in place from exp(z - m_h) to exp(z - m_new), and
+// alpha = exp(m_old - m_new) for the dH accumulator.  first: no earlier chunk.
+// halves: this chunk's half tiles; part_ld: the partials' row stride.
+__global__ void ce_chunk_kernel(const float* __restrict__ pmax, const float* __restrict__ psum, int halves,
+                                int part_ld, int ncols, int64_t M, uint16_t* __restrict__ P, int ldp,
+                                float* __restrict__ run_max, float* __restrict__ run_sum, float* __restrict__ alpha,
+                                int first) {
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
-  float mx = -INFINITY, sm = 0.0f;
-  for (int t = lane; t < ntiles; t += 32) {
-    const float m2 = pmax[row * ntiles + t], s2 = psum[row * ntiles + t];
-    const float nm = fmaxf(mx, m2);
-    if (nm == -INFINITY) continue;
-    sm = sm * __expf(mx - nm) + s2 * __expf(m2 - nm);
-    mx = nm;
-  }
+  const float* pm = pmax + row * part_ld;
+  const float* ps = psum + row * part_ld;
+  // chunk max, then chunk sum in half-tile order (lane 0 sums: fixed order)
+  float cm = -INFINITY;
+  for (int h = lane; h < halves; h += 32) cm = fmaxf(cm, pm[h]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, mx, o), s2 = __shfl_xor_sync(0xffffffffu, sm, o);
-    const float nm = fmaxf(mx, m2);
-    if (nm != -INFINITY) {
-      sm = sm * __expf(mx - nm) + s2 * __expf(m2 - nm);
-      mx = nm;
-    }
-  }
+  for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+  const float m_old = first ? -INFINITY : run_max[row];
+  const float m_new = fmaxf(m_old, cm);
   if (lane == 0) {
-    const float l = mx + logf(sm);
-    lse[row] = l;
-    const int lab = labels[row];
-    const bool valid = lab != ignore && lab >= 0 && lab < V;
-    if (lab != ignore && !valid) report_device_error(err, SL_ERR_INVALID);
-    term[row] = valid ? (l - zlab[row]) : 0.0f;
+    float cs = 0.0f;
+    for (int h = 0; h < halves; ++h)
+      if (pm[h] != -INFINITY) cs += ps[h] * __expf(pm[h] - m_new);
+    const float a = (m_old == -INFINITY) ? 0.0f : __expf(m_old - m_new);
+    run_sum[row] = (first ? 0.0f : run_sum[row] * a) + cs;
+    run_max[row] = m_new;
+    alpha[row] = a;
   }
+  // P[row, h * 128 .. +128) *= exp(m_h - m_new): lanes take 8-element chunks
+  uint16_t* pr = P + row * static_cast<int64_t>(ldp);
+  for (int c = lane * 8; c < ncols; c += 32 * 8) {
+    const float f = (pm[c / 128] == -INFINITY) ? 0.0f : __expf(pm[c / 128] - m_new);
+    uint4 v = *reinterpret_cast<const uint4*>(pr + c);
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = pack_bf16x2(bf16_lo(w[k]) * f, bf16_hi(w[k]) * f);
+    *reinterpret_cast<uint4*>(pr + c) = v;
+  }
+}
+
+// One warp per row: lse = m + log S and the row's loss term lse - z_label
+// (0 for ignored rows).  Out-of-range labels are reported through the error
+// word and treated as ignored.
+__global__ void ce_row_kernel(const float* __restrict__ run_max, const float* __restrict__ run_sum,
+                              const float* __restrict__ zlab, const int32_t* __restrict__ labels, int ignore, int V,
+                              int64_t M, float* __restrict__ lse, float* __restrict__ term, int* err) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (row >= M) return;
+  const float l = run_max[row] + logf(run_sum[row]);
+  lse[row] = l;
+  const int lab = labels[row];
+  const bool valid = lab != ignore && lab >= 0 && lab < V;
+  if (lab != ignore && !valid) report_device_error(err, SL_ERR_INVALID);
+  term[row] = valid ? (l - zlab[row]) : 0.0f;
 }
 
 // Single block: N_valid, loss = sum(term) / N_valid (fixed order), per-row scale.
@@ -124,27 +155,32 @@ __global__ void __launch_bounds__(1024) ce_finalize_kernel(const int32_t* __rest
   }
 }
 
-// dH[i, :] -= W[label_i, :] * scale_i   (valid rows)
-__global__ void ce_label_kernel(float* __restrict__ dH, const uint16_t* __restrict__ W,
-                                const int32_t* __restrict__ labels, const float* __restrict__ scale, int ignore,
-                                int V, int D) {
+// dH[i, :] = acc[i, :] * scale_i / S_i - W[label_i, :] * scale_i (valid rows; 0 otherwise)
+__global__ void ce_final_kernel(float* __restrict__ dH, const uint16_t* __restrict__ W,
+                                const int32_t* __restrict__ labels, const float* __restrict__ scale,
+                                const float* __restrict__ run_sum, int ignore, int V, int D) {
   const int64_t row = blockIdx.x;
   const int lab = labels[row];
-  if (lab == ignore || lab < 0 || lab >= V) return;
-  const float sc = scale[row];
+  const bool valid = lab != ignore && lab >= 0 && lab < V;
+  const float sc = valid ? scale[row] : 0.0f;
+  const float f = valid ? sc / run_sum[row] : 0.0f;
   for (int j = threadIdx.x * 8; j < D; j += blockDim.x * 8) {
-    const uint4 w = *reinterpret_cast<const uint4*>(W + static_cast<int64_t>(lab) * D + j);
-    const uint32_t p[4] = {w.x, w.y, w.z, w.w};
     float4* o = reinterpret_cast<float4*>(dH + row * D + j);
     float4 a = o[0], b = o[1];
-    a.x -= bf16_lo(p[0]) * sc;
-    a.y -= bf16_hi(p[0]) * sc;
-    a.z -= bf16_lo(p[1]) * sc;
-    a.w -= bf16_hi(p[1]) * sc;
-    b.x -= bf16_lo(p[2]) * sc;
-    b.y -= bf16_hi(p[2]) * sc;
-    b.z -= bf16_lo(p[3]) * sc;
-    b.w -= bf16_hi(p[3]) * sc;
+    a.x *= f; a.y *= f; a.z *= f; a.w *= f;
+    b.x *= f; b.y *= f; b.z *= f; b.w *= f;
+    if (valid) {
+      const uint4 w = *reinterpret_cast<const uint4*>(W + static_cast<int64_t>(lab) * D + j);
+      const uint32_t p[4] = {w.x, w.y, w.z, w.w};
+      a.x -= bf16_lo(p[0]) * sc;
+      a.y -= bf16_hi(p[0]) * sc;
+      a.z -= bf16_lo(p[1]) * sc;
+      a.w -= bf16_hi(p[1]) * sc;
+      b.x -= bf16_lo(p[2]) * sc;
+      b.y -= bf16_hi(p[2]) * sc;
+      b.z -= bf16_lo(p[3]) * sc;
+      b.w -= bf16_hi(p[3]) * sc;
+    }
     o[0] = a;
     o[1] = b;
   }
@@ -169,52 +205,22 @@ sl_status ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W, int64_t
   float* pmax = reinterpret_cast<float*>(base + P.part_max);
   float* psum = reinterpret_cast<float*>(base + P.part_sum);
   float* zlab = reinterpret_cast<float*>(base + P.label_logit);
+  float* run_max = reinterpret_cast<float*>(base + P.run_max);
+  float* run_sum = reinterpret_cast<float*>(base + P.run_sum);
+  float* alpha = reinterpret_cast<float*>(base + P.alpha);
   float* lse = reinterpret_cast<float*>(base + P.lse);
   float* term = reinterpret_cast<float*>(base + P.term);
   float* scale = reinterpret_cast<float*>(base + P.scale);
-  uint16_t* G = reinterpret_cast<uint16_t*>(base + P.G);
+  uint16_t* Pc = reinterpret_cast<uint16_t*>(base + P.P);
   const uint16_t* Wh = static_cast<const uint16_t*>(W);
-
-  // pass 1: row (max, sum exp) partials and label logits over the whole vocab
-  {
-    GemmLaunch g{};
-    g.bsrc = kBSrcBF16;
-    g.bmn = 0;
-    g.epi = kEpiCELse;
-    g.A = H;
-    g.lda = D;
-    g.w = W;
-    g.ldw = D;
-    g.args.M = static_cast<int>(M);
-    g.args.N = static_cast<int>(V);
-    g.args.K = static_cast<int>(D);
-    g.args.labels = labels;
-    g.args.ignore_index = ignore;
-    g.args.vocab_base = 0;
-    g.args.part_max = pmax;
-    g.args.part_sum = psum;
-    g.args.label_logit = zlab;
-    g.args.part_ld = P.ntiles;
-    g.args.tile_base = 0;
-    g.args.err = err;
-    sl_status st = launch_gemm(g, stream);
-    if (st != SL_OK) return st;
-  }
-  ce_row_kernel<<<static_cast<unsigned>(ceil_div(M * 32, 256)), 256, 0, stream>>>(
-      pmax, psum, P.ntiles, zlab, labels, ignore, static_cast<int>(V), M, lse, term, err);
-  sl_status st = check_launch("ce_row_kernel");
-  if (st != SL_OK) return st;
-  ce_finalize_kernel<<<1, 1024, 0, stream>>>(labels, ignore, static_cast<int>(V), term, M, loss, scale);
-  st = check_launch("ce_finalize_kernel");
-  if (st != SL_OK) return st;
-
-  // pass 2: chunked softmax gradient and dH accumulation
+  sl_status st = SL_OK;
   for (int64_t v0 = 0; v0 < V; v0 += chunk_V) {
     const int64_t vc = (V - v0 < chunk_V) ? (V - v0) : chunk_V;
+    // logits of the chunk: exp against the half-tile max, partials, label logit
     GemmLaunch g{};
     g.bsrc = kBSrcBF16;
     g.bmn = 0;
-    g.epi = kEpiCEGrad;
+    g.epi = kEpiCEExp;
     g.A = H;
     g.lda = D;
     g.w = Wh + v0 * D;
@@ -222,22 +228,31 @@ sl_status ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W, int64_t
     g.args.M = static_cast<int>(M);
     g.args.N = static_cast<int>(vc);
     g.args.K = static_cast<int>(D);
-    g.args.out = G;
+    g.args.out = Pc;
     g.args.ld_out = chunk_V;
     g.args.labels = labels;
     g.args.ignore_index = ignore;
     g.args.vocab_base = static_cast<int>(v0);
-    g.args.row_lse = lse;
-    g.args.row_scale = scale;
+    g.args.part_max = pmax;
+    g.args.part_sum = psum;
+    g.args.label_logit = zlab;
+    g.args.part_ld = P.halves;
     g.args.err = err;
     st = launch_gemm(g, stream);
     if (st != SL_OK) return st;
-
+    // running (max, sum); P rescaled to the running max; alpha for dH
+    const int halves_c = static_cast<int>(ceil_div(vc, kBN)) * 2;
+    ce_chunk_kernel<<<static_cast<unsigned>(ceil_div(M * 32, 256)), 256, 0, stream>>>(
+        pmax, psum, halves_c, P.halves, static_cast<int>(vc), M, Pc, static_cast<int>(chunk_V), run_max, run_sum,
+        alpha, v0 == 0 ? 1 : 0);
+    st = check_launch("ce_chunk_kernel");
+    if (st != SL_OK) return st;
+    // dH accumulator = alpha * dH accumulator + P W_c
     GemmLaunch h{};
     h.bsrc = kBSrcBF16;
     h.bmn = 1;
     h.epi = kEpiAddF32;
-    h.A = G;
+    h.A = Pc;
     h.lda = chunk_V;
     h.w = Wh + v0 * D;
     h.ldw = D;
@@ -247,13 +262,21 @@ sl_status ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W, int64_t
     h.args.out = dH;
     h.args.ld_out = D;
     h.args.accumulate = v0 > 0 ? 1 : 0;
+    h.args.row_alpha = alpha;
     h.args.err = err;
     st = launch_gemm(h, stream);
     if (st != SL_OK) return st;
   }
-  ce_label_kernel<<<static_cast<unsigned>(M), 256, 0, stream>>>(dH, Wh, labels, scale, ignore, static_cast<int>(V),
-                                                               static_cast<int>(D));
-  return check_launch("ce_label_kernel");
+  ce_row_kernel<<<static_cast<unsigned>(ceil_div(M, 256)), 256, 0, stream>>>(run_max, run_sum, zlab, labels, ignore,
+                                                                            static_cast<int>(V), M, lse, term, err);
+  st = check_launch("ce_row_kernel");
+  if (st != SL_OK) return st;
+  ce_finalize_kernel<<<1, 1024, 0, stream>>>(labels, ignore, static_cast<int>(V), term, M, loss, scale);
+  st = check_launch("ce_finalize_kernel");
+  if (st != SL_OK) return st;
+  ce_final_kernel<<<static_cast<unsigned>(M), 256, 0, stream>>>(dH, Wh, labels, scale, run_sum, ignore,
+                                                               static_cast<int>(V), static_cast<int>(D));
+  return check_launch("ce_final_kernel");
 }
 
 }  // namespace sl

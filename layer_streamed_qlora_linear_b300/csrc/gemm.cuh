@@ -41,9 +41,8 @@ namespace sl {
 enum GemmBSrc { kBSrcBF16 = 0, kBSrcNF4 = 1 };
 enum GemmEpi {
   kEpiStoreBF16 = 0,   // out[m, j] = bf16(acc)
-  kEpiCELse = 1,       // per-row (max, sum exp) over the tile + label logit gather
-  kEpiCEGrad = 2,      // out[m, j] = bf16(exp(acc - lse[m]) * scale[m])  (softmax / N_valid)
-  kEpiAddF32 = 3,      // outf[m, j] (+)= acc (fp32), "beta" = 0 on the first call
+  kEpiCEExp = 1,       // per row and 128-column half tile: m = max, out = bf16(exp(acc - m)), sum, label logit
+  kEpiAddF32 = 3,      // outf[m, j] = (accumulate ? outf[m, j] * alpha[m] : 0) + acc (fp32; alpha 1 if absent)
 };
 
 constexpr int kBM = 128;
@@ -86,13 +85,11 @@ struct GemmArgs {
   const int32_t* labels;       // [M]
   int32_t ignore_index;
   int vocab_base;              // first vocab id of this chunk
-  float* part_max;             // [M, ntiles] (kEpiCELse)
-  float* part_sum;             // [M, ntiles]
+  float* part_max;             // [M, part_ld] per 128-column half tile of the chunk (kEpiCEExp)
+  float* part_sum;             // [M, part_ld]
   float* label_logit;          // [M] written by the tile that holds the label
-  int part_ld;                 // ntiles of the whole vocab
-  int tile_base;               // tile index of this launch's first column tile
-  const float* row_lse;        // [M] (kEpiCEGrad)
-  const float* row_scale;      // [M] 1/N_valid or 0 (kEpiCEGrad)
+  int part_ld;                 // half tiles of a chunk
+  const float* row_alpha;      // [M] kEpiAddF32: factor on the accumulated output, or nullptr
   int accumulate;              // kEpiAddF32: add into out (1) or overwrite (0)
   int* err;                    // device error word
 };
@@ -477,6 +474,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       } else if (EPI == kEpiAddF32) {
         float* out = reinterpret_cast<float*>(args.out);
+        const float alpha = (args.row_alpha && gm < args.M) ? args.row_alpha[gm] : 1.0f;
 #pragma unroll 1
         for (int c0 = cbeg; c0 < cend; c0 += 32) {
           uint32_t v[32];
@@ -490,35 +488,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                      __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
               if (args.accumulate) {
                 const float4 p = dst[g];
-                o.x += p.x;
-                o.y += p.y;
-                o.z += p.z;
-                o.w += p.w;
+                o.x = fmaf(p.x, alpha, o.x);
+                o.y = fmaf(p.y, alpha, o.y);
+                o.z = fmaf(p.z, alpha, o.z);
+                o.w = fmaf(p.w, alpha, o.w);
               }
               dst[g] = o;
             }
           }
         }
-      } else if (EPI == kEpiCELse) {
-        // Online (max, sum exp) over this tile's 256 vocab columns, in a
+      } else if (EPI == kEpiCEExp) {
+        // This thread's row over its 128-column half tile: the max m (one
+        // read of the accumulator), then P = bf16(exp(z - m)) to the chunk
+        // scratch and the fp32 sum of exp(z - m) (a second read), both in a
         // fixed left-to-right order; the label's logit is gathered here too.
+        uint16_t* out = reinterpret_cast<uint16_t*>(args.out);
         const int lab = (gm < args.M) ? args.labels[gm] : args.ignore_index;
-        float mx = -INFINITY, sm = 0.0f;
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c0, v);
+          ptx::tmem_wait_ld();
+          if (n0 + c0 < args.N)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+        }
+        float sm = 0.0f;
 #pragma unroll 1
         for (int c0 = cbeg; c0 < cend; c0 += 32) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c0, v);
           ptx::tmem_wait_ld();
           if (n0 + c0 < args.N) {
-            float cm = -INFINITY;
+            float f[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) cm = fmaxf(cm, __uint_as_float(v[e]));
-            const float nm = fmaxf(mx, cm);
-            float acc = 0.0f;
+            for (int e = 0; e < 32; ++e) {
+              f[e] = __expf(__uint_as_float(v[e]) - mx);
+              sm += f[e];
+            }
+            if (gm < args.M) {
+              uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(gm) * args.ld_out + n0 + c0);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) acc += __expf(__uint_as_float(v[e]) - nm);
-            sm = sm * __expf(mx - nm) + acc;
-            mx = nm;
+              for (int g = 0; g < 4; ++g) {
+                uint4 o;
+                o.x = pack_bf16x2(f[8 * g + 0], f[8 * g + 1]);
+                o.y = pack_bf16x2(f[8 * g + 2], f[8 * g + 3]);
+                o.z = pack_bf16x2(f[8 * g + 4], f[8 * g + 5]);
+                o.w = pack_bf16x2(f[8 * g + 6], f[8 * g + 7]);
+                dst[g] = o;
+              }
+            }
             const int vid = args.vocab_base + n0 + c0;
             if (lab >= vid && lab < vid + 32 && gm < args.M) {
 #pragma unroll
@@ -528,34 +548,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (gm < args.M) {
-          const int64_t p = static_cast<int64_t>(gm) * args.part_ld + 2 * (args.tile_base + blockIdx.x) + ch;
+          const int64_t p = static_cast<int64_t>(gm) * args.part_ld + 2 * blockIdx.x + ch;
           args.part_max[p] = mx;
           args.part_sum[p] = sm;
-        }
-      } else if (EPI == kEpiCEGrad) {
-        uint16_t* out = reinterpret_cast<uint16_t*>(args.out);
-        const float lse = (gm < args.M) ? args.row_lse[gm] : 0.0f;
-        const float sc = (gm < args.M) ? args.row_scale[gm] : 0.0f;
-#pragma unroll 1
-        for (int c0 = cbeg; c0 < cend; c0 += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c0, v);
-          ptx::tmem_wait_ld();
-          if (gm < args.M && n0 + c0 < args.N) {
-            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(gm) * args.ld_out + n0 + c0);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              float f[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = __expf(__uint_as_float(v[8 * g + e]) - lse) * sc;
-              uint4 o;
-              o.x = pack_bf16x2(f[0], f[1]);
-              o.y = pack_bf16x2(f[2], f[3]);
-              o.z = pack_bf16x2(f[4], f[5]);
-              o.w = pack_bf16x2(f[6], f[7]);
-              dst[g] = o;
-            }
-          }
         }
       }
     } else if (!*abort_flag) {

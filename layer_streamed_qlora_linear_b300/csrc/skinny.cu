@@ -510,7 +510,7 @@ sl_status launch(const CUtensorMap& mq, const CUtensorMap& mw, const SkArgs& a, 
   const int cs = choose_split<MODE>(blocks, a);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_config<MODE>(blocks, cs, a, stream, attr);
-  const TimingToken tt = timing_begin(MODE == kSkKA ? 7 : (MODE == kSkKB ? 8 : 9), pass_bytes(MODE, a), stream);
+  const TimingToken tt = timing_begin(MODE == kSkKA ? 6 : (MODE == kSkKB ? 7 : 8), pass_bytes(MODE, a), stream);
   cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_kernel<MODE>, mq, mw, a);
   timing_end(tt, stream);
   if (e != cudaSuccess) return cuda_error(e, "skinny_kernel launch");

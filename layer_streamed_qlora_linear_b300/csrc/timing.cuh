@@ -4,9 +4,9 @@
 
 namespace sl {
 
-// Variants: 0..6 tensor-core GEMMs (see sl_kernel_timing), 7 rank-r T = X A^T,
-// 8 rank-r U = dY B, 9 rank-r dA / dB.
-constexpr int kNumTimedVariants = 10;
+// Variants: 0..5 tensor-core GEMMs (see sl_kernel_timing), 6 rank-r T = X A^T,
+// 7 rank-r U = dY B, 8 rank-r dA / dB.
+constexpr int kNumTimedVariants = 9;
 
 struct TimingToken {
   cudaEvent_t start = nullptr, stop = nullptr;

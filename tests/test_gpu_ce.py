@@ -21,9 +21,14 @@ def run(sl, H, W, lab, chunk):
     return float(loss.item()), dH
 
 
-@pytest.mark.parametrize("M,D,V,chunk", [(200, 256, 1056, 512), (130, 512, 4096, 1024), (64, 256, 256, 8192)])
-def test_ce_matches_oracle(gpu_lib, M, D, V, chunk):
-    c = si.ce_case(3 + M, M, D, V, h_std=1.0, w_std=0.05)
+@pytest.mark.parametrize("M,D,V,chunk,w_std", [
+    (200, 256, 1056, 512, 0.05),     # ragged last chunk (32 columns, one empty half tile)
+    (130, 512, 4096, 1024, 0.05),
+    (64, 256, 256, 8192, 0.05),      # one chunk larger than the vocabulary
+    (192, 256, 2048, 256, 0.5),      # logits spread ~ +-25: the running max moves across 8 chunks
+])
+def test_ce_matches_oracle(gpu_lib, M, D, V, chunk, w_std):
+    c = si.ce_case(3 + M, M, D, V, h_std=1.0, w_std=w_std)
     loss, dH = run(gpu_lib, dev_bf16(c["H"]), dev_bf16(c["W"]), torch.from_numpy(c["labels"]).cuda(), chunk)
     ol, odH, osoft = ce.ce_fwd_bwd(c["H"], c["W"], c["labels"], want_soft=True)
     assert abs(loss - ol) <= LOSS_TOL * abs(ol)
