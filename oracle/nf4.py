@@ -102,3 +102,82 @@ def dequantize(codes, absmax, N: int, K: int) -> np.ndarray:
 def dequantize_bf16(codes, absmax, N: int, K: int) -> np.ndarray:
     """bf16(w_hat) as float64: the weight the NF4 linear multiplies by."""
     return round_bf16(dequantize(codes, absmax, N, K))
+
+
+# ------------------------------------------------------ double quantisation
+# The pages' base store (3.60 GB pinned, two 113 MB layer buffers for
+# Llama-3.1-8B: "Soup: Fine-Tuning ...", "Layer Streaming: The Mechanism
+# Behind the 4 GB Claim") fits 4-bit codes plus an 8-bit absmax per block --
+# QLoRA's double quantisation.  The pages do not define its format; the
+# reading taken here (a plain, fully specified one):
+#
+# * the fp32 absmax a[n, j] (row n, 64-block j) is stored transposed as
+#   q[j, n] (int8), so that the blocks of consecutive rows are contiguous;
+# * per 256 consecutive columns of a transposed row (block b of row j):
+#     c = float32(sum of the 256 a values in float64, ascending n) / 256),
+#     d_n = float32(a_n - c),  s = float32(max |d_n| / 127),
+#     q_n = 0 if s == 0 else clip(rint(float32(d_n / s)), -127, 127)
+#   (IEEE float32 subtraction and division, rint rounding ties to even);
+# * the absmax used is a'_n = fma(s, q_n, c), rounded once to float32.
+DQ_BLOCK = 256
+
+
+def fma32(s, q, c) -> np.ndarray:
+    """float32(s * q + c) rounded once: s, c float32, q small integers.
+
+    s * q is exact in float64; TwoSum gives the float64 sum and its exact
+    error; rounding the sum to float32 is already correct unless the sum sits
+    exactly on a float32 midpoint, where the error's sign decides.
+    """
+    s = np.asarray(s, np.float32).astype(np.float64)
+    c = np.asarray(c, np.float32).astype(np.float64)
+    p = s * np.asarray(q, np.float64)
+    t = p + c
+    bb = t - p
+    err = (p - (t - bb)) + (c - bb)
+    r = t.astype(np.float32)
+    # float32 neighbours of r and the midpoint toward t
+    up = np.nextafter(r, np.float32(np.inf))
+    dn = np.nextafter(r, np.float32(-np.inf))
+    nb = np.where(t > r.astype(np.float64), up, dn)
+    mid = (r.astype(np.float64) + nb.astype(np.float64)) / 2
+    on_mid = (t == mid) & (err != 0)
+    toward = ((err > 0) & (nb > r)) | ((err < 0) & (nb < r))
+    return np.where(on_mid & toward, nb, r).astype(np.float32)
+
+
+def double_quantize(absmax, N: int, K: int) -> tuple:
+    """fp32 absmax (row-major [N, K/64]) -> (q int8 [K/64, N], a2 float32 [K/64, N/256, 2] = (c, s))."""
+    if N % DQ_BLOCK or K % BLOCK:
+        raise ValueError("double quantisation needs N % 256 == 0 and K % 64 == 0")
+    a = np.asarray(absmax, np.float32).reshape(N, K // BLOCK).T          # [K/64, N]
+    blocks = a.reshape(K // BLOCK, N // DQ_BLOCK, DQ_BLOCK)
+    total = np.zeros(blocks.shape[:2], np.float64)
+    for i in range(DQ_BLOCK):                                            # ascending n, float64
+        total = total + blocks[:, :, i].astype(np.float64)
+    c = (total / DQ_BLOCK).astype(np.float32)
+    d = np.subtract(blocks, c[:, :, None], dtype=np.float32)
+    m = np.max(np.abs(d), axis=2)
+    s = np.divide(m, np.float32(127), dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.divide(d, s[:, :, None], dtype=np.float32)
+    q = np.where(s[:, :, None] > 0, np.clip(np.rint(r), -127, 127), 0).astype(np.int8)
+    a2 = np.stack([c, s], axis=2).astype(np.float32)
+    return q.reshape(K // BLOCK, N), a2
+
+
+def dq_absmax(q, a2, N: int, K: int) -> np.ndarray:
+    """The absmax a' = fma(s, q, c) as float32 [N*K/64] (row-major [N, K/64], like `quantize`)."""
+    q = np.asarray(q, np.int8).reshape(K // BLOCK, N // DQ_BLOCK, DQ_BLOCK)
+    a2 = np.asarray(a2, np.float32).reshape(K // BLOCK, N // DQ_BLOCK, 2)
+    ap = fma32(a2[:, :, 1:2], q, a2[:, :, 0:1])
+    return ap.reshape(K // BLOCK, N).T.reshape(-1)
+
+
+def dequantize_dq(codes, q, a2, N: int, K: int) -> np.ndarray:
+    """w_hat = float32(T[code] * a') with the double-quantised absmax, [N, K] float32."""
+    return dequantize(codes, dq_absmax(q, a2, N, K), N, K)
+
+
+def dequantize_dq_bf16(codes, q, a2, N: int, K: int) -> np.ndarray:
+    return round_bf16(dequantize_dq(codes, q, a2, N, K))

@@ -5,6 +5,7 @@ import os
 import numpy as np
 import pytest
 
+import seeded_inputs as si
 from oracle import nf4
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "nf4_levels_qlora.txt")
@@ -144,3 +145,82 @@ def test_zero_block_and_nonfinite():
         nf4.quantize(W)
     with pytest.raises(ValueError):
         nf4.quantize(np.zeros((1, 96), np.float32))
+
+
+# ------------------------------------------------------ double quantisation
+def test_fma32_is_one_rounding_of_the_exact_value():
+    from fractions import Fraction
+    rng = np.random.default_rng(7)
+    n = 3000
+    s = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    c = (rng.standard_normal(n) * np.exp(rng.uniform(-25, 25, n))).astype(np.float32)   # c >> s q too
+    q = rng.integers(-127, 128, n)
+    r = nf4.fma32(s, q, c)
+    for i in range(n):
+        ex = Fraction(float(s[i])) * int(q[i]) + Fraction(float(c[i]))
+        f = np.float32(float(ex))
+        cands = [f, np.nextafter(f, np.float32(np.inf)), np.nextafter(f, np.float32(-np.inf))]
+        best = min(cands, key=lambda v: (abs(Fraction(float(v)) - ex), int(np.float32(v).view(np.uint32)) & 1))
+        assert r[i] == best, i
+
+
+def test_dq_block_mean_scale_and_extremes():
+    # values on a 2^-12 grid: float64 sums are exact, the mean is a plain average
+    rng = np.random.default_rng(3)
+    N, K = 512, 128                                   # 2 transposed rows x 2 blocks of 256
+    a = (rng.integers(100, 400, size=N * K // 64) * 2.0 ** -12).astype(np.float32)
+    q, a2 = nf4.double_quantize(a, N, K)
+    at = a.reshape(N, K // 64).T.reshape(K // 64, N // 256, 256)
+    for j in range(K // 64):
+        for b in range(N // 256):
+            v = at[j, b].astype(np.float64)
+            c = np.float32(v.sum() / 256)
+            assert a2[j, b, 0] == c
+            d = (at[j, b] - c).astype(np.float32)
+            s = np.float32(np.max(np.abs(d)) / np.float32(127))
+            assert a2[j, b, 1] == s
+            qq = q[j, b * 256:(b + 1) * 256].astype(np.int32)
+            k = int(np.argmax(np.abs(d)))
+            assert abs(qq[k]) == 127 and np.sign(qq[k]) == np.sign(d[k])
+            assert np.all(np.abs(qq) <= 127)
+
+
+def test_dq_nearest_level_brute_force_and_error_bound():
+    rng = np.random.default_rng(11)
+    N, K = 256, 64 * 6
+    W = si.normal_bf16(5, (N, K), 0.02)
+    _, a = nf4.quantize(W)
+    q, a2 = nf4.double_quantize(a, N, K)
+    ap = nf4.dq_absmax(q, a2, N, K)
+    at = a.reshape(N, K // 64).T
+    apt = ap.reshape(N, K // 64).T
+    for j in range(K // 64):
+        c, s = a2[j, 0]
+        d = (at[j] - c).astype(np.float32)
+        r = (d / s).astype(np.float32)                         # the float32 quotient the rule rounds
+        cand = np.arange(-127, 128, dtype=np.float64)
+        dist = np.abs(r.astype(np.float64)[:, None] - cand[None, :])
+        best = dist.min(axis=1)
+        for n in range(N):                                     # nearest integer, ties to even
+            ks = cand[dist[n] == best[n]]
+            want = ks[0] if len(ks) == 1 else ks[np.argmin(np.abs(ks) % 2)]
+            assert q[j, n] == want
+        # |a' - a| <= s / 2 (plus the final float32 rounding)
+        assert np.all(np.abs(apt[j].astype(np.float64) - at[j]) <= s / 2 * (1 + 1e-6) + np.spacing(at[j]))
+
+
+def test_dq_constant_block_is_exact():
+    N, K = 256, 64
+    a = np.full(N, 0.03125, np.float32)
+    q, a2 = nf4.double_quantize(a, N, K)
+    assert np.all(q == 0) and a2[0, 0, 1] == 0
+    assert np.array_equal(nf4.dq_absmax(q, a2, N, K), a)
+
+
+def test_dq_layer_bytes_match_the_pages_buffer():
+    # 8B layer: 218.1M params; 4-bit codes + 8-bit absmax per 64 + (c, s) per 256 blocks
+    params = sum(n * k for n, k in ((4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096),
+                                    (14336, 4096), (14336, 4096), (4096, 14336)))
+    dq = params // 2 + params // 64 + params // (64 * 256) * 8
+    assert abs(dq / 1e6 - 113) / 113 < 0.01            # the pages' two 113 MB layer buffers
+    assert abs(32 * dq / 1e9 - 3.60) / 3.60 < 0.01     # and the 3.60 GB pinned base store
