@@ -59,7 +59,7 @@ typedef enum {
 } sl_status;
 
 typedef enum { SL_DTYPE_BF16 = 0, SL_DTYPE_F32 = 1 } sl_dtype;
-typedef enum { SL_WEIGHT_NF4 = 0, SL_WEIGHT_BF16 = 1 } sl_weight_kind;
+typedef enum { SL_WEIGHT_NF4 = 0, SL_WEIGHT_BF16 = 1, SL_WEIGHT_NF4_DQ = 2 } sl_weight_kind;
 typedef enum { SL_MODE_STREAMED = 0, SL_MODE_RESIDENT = 1 } sl_stack_mode;
 
 /* A frozen base weight W [N, K] (N = out features, K = in features), the
@@ -68,7 +68,18 @@ typedef enum { SL_MODE_STREAMED = 0, SL_MODE_RESIDENT = 1 } sl_stack_mode;
  *                         HIGH nibble of byte i; absmax [N*K/64] fp32, one per
  *                         64 consecutive elements of a row.  Needs K % 256 == 0.
  *  kind = SL_WEIGHT_BF16: w [N, K] bf16.
- * All pointers 16-byte aligned; N % 32 == 0. */
+ *  kind = SL_WEIGHT_NF4_DQ: codes as for NF4; the absmax double-quantised
+ *                         (sl_nf4_double_quantize): qabsmax int8 transposed,
+ *                         element [j, dq_col0 + n] for row n and 64-block j,
+ *                         rows of qabsmax_ld bytes; absmax2 fp32 (offset,
+ *                         scale) pairs, pair [j, (dq_col0 + n) / 256] at
+ *                         absmax2 + j * absmax2_ld + 2 * ((dq_col0 + n) / 256).
+ *                         dq_col0 lets a weight be a column range of arrays
+ *                         that several projections share.  Needs K % 256 == 0,
+ *                         N and dq_col0 multiples of 256, and M > 128 in the
+ *                         linear and group calls (the CTA-pair GEMM).
+ * All pointers 16-byte aligned; N % 32 == 0; qabsmax_ld a multiple of 16,
+ * absmax2_ld of 4. */
 typedef struct {
   int32_t kind;
   int64_t N;
@@ -76,6 +87,11 @@ typedef struct {
   const uint8_t* codes;
   const float* absmax;
   const void* w;
+  const int8_t* qabsmax;  /* SL_WEIGHT_NF4_DQ only (NULL otherwise) */
+  int64_t qabsmax_ld;
+  const float* absmax2;
+  int64_t absmax2_ld;
+  int64_t dq_col0;
 } sl_weight;
 
 /* ---------------------------------------------------------------- library */
@@ -134,10 +150,29 @@ sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms,
 sl_status sl_nf4_quantize(const void* W, int32_t dtype, int64_t N, int64_t K,
                           uint8_t* codes, float* absmax, cudaStream_t stream);
 
+/* Double quantisation of the absmax (QLoRA's 8-bit absmax: the pages' 3.60 GB
+ * store and 113 MB layer buffers for Llama-3.1-8B, "Soup: Fine-Tuning ...",
+ * "Layer Streaming: The Mechanism Behind the 4 GB Claim"; the format is this
+ * library's reading): absmax [N, K/64] fp32 as written by sl_nf4_quantize ->
+ * qabsmax[j * qabsmax_ld + n] int8 and, per 256 consecutive n of block j,
+ * (c, s) at absmax2[j * absmax2_ld + 2 * (n / 256)]:
+ *   c = fp32(float64 sum of the 256 values, ascending n) / 256),
+ *   d = fp32(a - c), s = fp32(max |d| / 127),
+ *   q = s == 0 ? 0 : clamp(rint(fp32(d / s)), -127, 127)  (ties to even);
+ * the absmax a GEMM then uses is fma(s, q, c) rounded once.  N % 256 == 0,
+ * K % 64 == 0; the output pointers may be column offsets into wider arrays
+ * (see sl_weight); 16-byte aligned input. */
+sl_status sl_nf4_double_quantize(const float* absmax, int64_t N, int64_t K, int8_t* qabsmax, int64_t qabsmax_ld,
+                                 float* absmax2, int64_t absmax2_ld, cudaStream_t stream);
+
 /* w_hat = fp32(T[code] * absmax), written as bf16 (rounded to nearest even)
  * or fp32 per `out_dtype`, out [N, K].  Requires K % 64 == 0. */
 sl_status sl_nf4_dequantize(const uint8_t* codes, const float* absmax, int64_t N, int64_t K,
                             int32_t out_dtype, void* out, cudaStream_t stream);
+
+/* The same for any sl_weight of kind NF4 or NF4_DQ (w_hat with the absmax the
+ * GEMMs use: fma(s, q, c) for NF4_DQ). */
+sl_status sl_weight_dequantize(const sl_weight* w, int32_t out_dtype, void* out, cudaStream_t stream);
 
 /* ------------------------------------------------------ LoRA linear (a3-a6) */
 

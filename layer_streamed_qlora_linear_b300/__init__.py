@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "sl.h")
 
 SL_OK, SL_ERR_INVALID, SL_ERR_CUDA, SL_ERR_UNSUPPORTED, SL_ERR_TIMEOUT, SL_ERR_NONFINITE, SL_ERR_OOM = range(7)
 SL_DTYPE_BF16, SL_DTYPE_F32 = 0, 1
-SL_WEIGHT_NF4, SL_WEIGHT_BF16 = 0, 1
+SL_WEIGHT_NF4, SL_WEIGHT_BF16, SL_WEIGHT_NF4_DQ = 0, 1, 2
 SL_MODE_STREAMED, SL_MODE_RESIDENT = 0, 1
 STATUS_NAMES = {0: "SL_OK", 1: "SL_ERR_INVALID", 2: "SL_ERR_CUDA", 3: "SL_ERR_UNSUPPORTED",
                 4: "SL_ERR_TIMEOUT", 5: "SL_ERR_NONFINITE", 6: "SL_ERR_OOM"}
@@ -32,7 +32,9 @@ class SLError(RuntimeError):
 
 class sl_weight(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("codes", ctypes.c_void_p), ("absmax", ctypes.c_void_p), ("w", ctypes.c_void_p)]
+                ("codes", ctypes.c_void_p), ("absmax", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("qabsmax", ctypes.c_void_p), ("qabsmax_ld", ctypes.c_int64),
+                ("absmax2", ctypes.c_void_p), ("absmax2_ld", ctypes.c_int64), ("dq_col0", ctypes.c_int64)]
 
 
 class sl_stack_desc(ctypes.Structure):
@@ -55,6 +57,8 @@ _SIGS = {
     "sl_kernel_timing_read": (_I32, [_I32, _P, _P, _P]),
     "sl_nf4_quantize": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P]),
     "sl_nf4_dequantize": (_I32, [_P, _P, _I64, _I64, _I32, _P, _P]),
+    "sl_nf4_double_quantize": (_I32, [_P, _I64, _I64, _P, _I64, _P, _I64, _P]),
+    "sl_weight_dequantize": (_I32, [ctypes.POINTER(sl_weight), _I32, _P, _P]),
     "sl_lora_linear_fwd": (_I32, [ctypes.POINTER(sl_weight), _P, _I64, _P, _P, _I32, _F, _P, _P, _P, _SZ, _P]),
     "sl_lora_linear_bwd": (_I32, [ctypes.POINTER(sl_weight), _P, _P, _I64, _P, _P, _I32, _F, _P, _P, _P, _P,
                                   _I32, _P, _SZ, _P]),
@@ -170,19 +174,42 @@ def sl_nf4_dequantize(codes, absmax, N, K, out, stream=None):
     _check(lib().sl_nf4_dequantize(_ptr(codes), _ptr(absmax), N, K, dt, _ptr(out), _stream(stream)))
 
 
+def sl_nf4_double_quantize(absmax, N, K, qabsmax, absmax2, qabsmax_ld=None, absmax2_ld=None, stream=None):
+    """absmax [N*K/64] fp32 -> qabsmax int8 [K/64, >= N] and absmax2 fp32 [K/64, >= 2 N/256] (see include/sl.h)."""
+    q_ld = qabsmax.shape[-1] if qabsmax_ld is None else qabsmax_ld
+    a2_ld = absmax2.shape[-1] if absmax2_ld is None else absmax2_ld
+    _check(lib().sl_nf4_double_quantize(_ptr(absmax), N, K, _ptr(qabsmax), q_ld, _ptr(absmax2), a2_ld,
+                                        _stream(stream)))
+
+
+def sl_weight_dequantize(weight, out, stream=None):
+    import torch
+    dt = SL_DTYPE_F32 if out.dtype == torch.float32 else SL_DTYPE_BF16
+    _check(lib().sl_weight_dequantize(ctypes.byref(weight.desc), dt, _ptr(out), _stream(stream)))
+
+
 # ---------------------------------------------------------------- weights
 class Weight:
     """An sl_weight descriptor that keeps its tensors alive."""
 
-    def __init__(self, kind, N, K, codes=None, absmax=None, w=None):
-        self.tensors = (codes, absmax, w)
+    def __init__(self, kind, N, K, codes=None, absmax=None, w=None, qabsmax=None, absmax2=None, col0=0):
+        self.tensors = (codes, absmax, w, qabsmax, absmax2)
         self.desc = sl_weight(kind, N, K, codes.data_ptr() if codes is not None else None,
                               absmax.data_ptr() if absmax is not None else None,
-                              w.data_ptr() if w is not None else None)
+                              w.data_ptr() if w is not None else None,
+                              qabsmax.data_ptr() if qabsmax is not None else None,
+                              qabsmax.shape[-1] if qabsmax is not None else 0,
+                              absmax2.data_ptr() if absmax2 is not None else None,
+                              absmax2.shape[-1] if absmax2 is not None else 0, int(col0))
 
     @staticmethod
     def nf4(codes, absmax, N, K):
         return Weight(SL_WEIGHT_NF4, N, K, codes=codes, absmax=absmax)
+
+    @staticmethod
+    def nf4_dq(codes, qabsmax, absmax2, N, K, col0=0):
+        """Double-quantised NF4: qabsmax int8 [K/64, ld], absmax2 fp32 [K/64, ld2]; columns col0 .. col0+N."""
+        return Weight(SL_WEIGHT_NF4_DQ, N, K, codes=codes, qabsmax=qabsmax, absmax2=absmax2, col0=col0)
 
     @staticmethod
     def bf16(w):

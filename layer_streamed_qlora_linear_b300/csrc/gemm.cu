@@ -141,7 +141,7 @@ static int pair_clusters_resident() {
 // of the pair tiles.
 template <int BMN>
 static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, const CUtensorMap& ms,
-                                const GemmArgs& a, cudaStream_t stream) {
+                                const CUtensorMap& ms2, const GemmArgs& a, cudaStream_t stream) {
   auto kern = gemm_nf4_pair_persistent_kernel<BMN>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -152,7 +152,7 @@ static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, co
   }
   const int ntiles = ceil_div(a.M, 256) * ceil_div(a.N, kBN);
   const int nclusters = std::min(ntiles, pair_clusters_resident<BMN>());
-  kern<<<dim3(static_cast<unsigned>(2 * nclusters)), kGemm3Threads, Gemm3Cfg::kSmem, stream>>>(ma, mc, ms, a);
+  kern<<<dim3(static_cast<unsigned>(2 * nclusters)), kGemm3Threads, Gemm3Cfg::kSmem, stream>>>(ma, mc, ms, ms2, a);
   return check_launch("gemm_nf4_pair_persistent_kernel");
 }
 
@@ -184,7 +184,9 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     return set_error(SL_ERR_INVALID, "gemm: LoRA rank must be 0..32 (a group's 0..64), multiple of 8");
   if (g.grouped && (g.bsrc != kBSrcNF4 || g.epi != kEpiStoreBF16 || a.M <= kBM))
     return set_error(SL_ERR_UNSUPPORTED, "gemm: projection groups need NF4 weights and M > 128");
-  CUtensorMap ma, mb, ms;
+  if (a.dq && (g.bsrc != kBSrcNF4 || g.epi != kEpiStoreBF16 || a.M <= kBM))
+    return set_error(SL_ERR_UNSUPPORTED, "gemm: the double-quantised absmax needs M > 128 (persistent pair GEMM)");
+  CUtensorMap ma, mb, ms, ms2;
   bool pair = false;
   sl_status st = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, a.K, a.M, g.lda * 2, kBK, kBM,
                           CU_TENSOR_MAP_SWIZZLE_128B);
@@ -218,6 +220,20 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
           st = make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax, cols / 64, rows, cols / 64 * 4, 4, kBK,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
       }
+      if (st == SL_OK && a.dq) {
+        // int8 absmax, transposed: [cols / 64][dq_col0 + rows]; (c, s) pairs fp32
+        // [cols / 64][2 per 256 of dq_col0 + rows], read as aligned 16-byte boxes
+        const int64_t qcols = a.dq_col0 + rows, pcols = 2 * (qcols / 256);
+        if (a.dq_col0 < 0 || a.dq_col0 % 256 || rows % 256 || g.q_ld < qcols || g.a2_ld < pcols)
+          return set_error(SL_ERR_INVALID, "gemm: double-quantised absmax layout (column offset, row lengths)");
+        st = make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.qabsmax, qcols, cols / 64, g.q_ld, g.bmn ? 64 : 128,
+                      g.bmn ? 2 : 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st == SL_OK)
+          st = make_map(&ms2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax2, pcols, cols / 64, g.a2_ld * 4, 4,
+                        g.bmn ? 2 : 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+      } else {
+        ms2 = ms;
+      }
       if (st != SL_OK) return st;
       pair = true;
     } else if (!g.bmn) {
@@ -241,10 +257,10 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   // More pair tiles than resident clusters: the persistent kernel (its
   // epilogue overlaps the next tile); one wave or less: one cluster per tile
   // with the epilogue spread over all eight dequant warps.
-  const bool persistent = pair && (g.grouped || ceil_div(a.M, 256) * ceil_div(a.N, kBN) >
+  const bool persistent = pair && (g.grouped || a.dq || ceil_div(a.M, 256) * ceil_div(a.N, kBN) >
                                                     (g.bmn ? pair_clusters_resident<1>() : pair_clusters_resident<0>()));
   if (persistent)
-    st = g.bmn ? run_persistent<1>(ma, mb, ms, a, stream) : run_persistent<0>(ma, mb, ms, a, stream);
+    st = g.bmn ? run_persistent<1>(ma, mb, ms, ms2, a, stream) : run_persistent<0>(ma, mb, ms, ms2, a, stream);
   else
     st = pair ? (g.bmn ? run_pair<1>(ma, mb, ms, a, stream) : run_pair<0>(ma, mb, ms, a, stream))
               : dispatch(g, ma, mb, ms, stream);

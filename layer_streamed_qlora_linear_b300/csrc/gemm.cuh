@@ -79,6 +79,8 @@ struct GemmArgs {
   int lora_G;                  // grouped forward: projections sharing the GEMM (0 or 1: none)
   int lora_bounds[5];          // grouped forward: first output column of projection g (multiples of 256), [G] = N
   float s;                     // LoRA scale alpha / r
+  int dq;                      // NF4 with the double-quantised absmax (persistent pair GEMM)
+  int dq_col0;                 // the weight's first column in the qabsmax / absmax2 arrays
   void* out;                   // epilogue output
   int64_t ld_out;              // elements
   // cross-entropy epilogues
@@ -580,6 +582,11 @@ struct GemmLaunch {
   int64_t ldw;           // weight row length in elements (K for K-major, N for MN-major)
   GemmArgs args;
   int grouped;           // a projection group: persistent CTA-pair kernel (NF4, M > 128) required
+  // double-quantised absmax (args.dq): int8 [weight K / 64][q_ld], (c, s) pairs [weight K / 64][a2_ld]
+  const int8_t* qabsmax;
+  int64_t q_ld;
+  const float* absmax2;
+  int64_t a2_ld;
 };
 
 sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream);

@@ -50,7 +50,8 @@ __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" 
 template <int BMN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     gemm_nf4_pair_persistent_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
-                                    const __grid_constant__ CUtensorMap map_s, const GemmArgs args) {
+                                    const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_s2,
+                                    const GemmArgs args) {
   using Cfg = Gemm3Cfg;
   constexpr int S = Cfg::S;
   extern __shared__ uint8_t smem_raw[];
@@ -113,6 +114,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     ptx::tma_prefetch_desc(&map_a);
     ptx::tma_prefetch_desc(&map_c);
     ptx::tma_prefetch_desc(&map_s);
+    if (args.dq) ptx::tma_prefetch_desc(&map_s2);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(tmem_holder, 512);
@@ -132,7 +134,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint32_t rawtx = kHalfCodesBytes + (BMN ? kBK * 16 : 128 * 16);
+      // absmax per stage: fp32 (K-major 4 x 128, MN-major 4 x 64) or, double
+      // quantised, 128 int8 + 16 B (K-major) / 32 B (MN-major) of (c, s) pairs
+      const uint32_t rawtx =
+          kHalfCodesBytes + (args.dq ? (128 + (BMN ? 32 : 16)) : (BMN ? kBK * 16 : 128 * 16));
       int g = 0;  // k-blocks issued by this cluster
       bool ok = true;
       for (int t = cluster; ok && t < ntiles; t += nclusters) {
@@ -150,10 +155,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           ptx::mbar_arrive_expect_tx(&raw_full[s], rawtx);
           if (!BMN) {
             ptx::tma_load_2d(raw, &map_c, &raw_full[s], kb * (kBK / 2), nh);
-            ptx::tma_load_2d(raw + kHalfCodesBytes, &map_s, &raw_full[s], kb & ~3, nh);
+            if (!args.dq) {
+              ptx::tma_load_2d(raw + kHalfCodesBytes, &map_s, &raw_full[s], kb & ~3, nh);
+            } else {  // int8 absmax of rows nh .. nh+127 at block kb; their (c, s) pair
+              const int col = args.dq_col0 + nh;
+              ptx::tma_load_2d(raw + kHalfCodesBytes, &map_s, &raw_full[s], col, kb);
+              // the 16-byte box at x = 4 (col / 512) (TMA: x * 4 B on a 16-byte
+              // boundary) holds the pairs of 256-blocks 2 (col / 512) and + 1
+              ptx::tma_load_2d(raw + kHalfCodesBytes + 128, &map_s2, &raw_full[s], 4 * (col / 512), kb);
+            }
           } else {
             ptx::tma_load_2d(raw, &map_c, &raw_full[s], nh / 2, kb * kBK);
-            ptx::tma_load_2d(raw + kHalfCodesBytes, &map_s, &raw_full[s], n0 / 64, kb * kBK);
+            if (!args.dq) {
+              ptx::tma_load_2d(raw + kHalfCodesBytes, &map_s, &raw_full[s], n0 / 64, kb * kBK);
+            } else {  // int8 absmax of weight rows kb*64 .. +63 at blocks nh/64, +1; their (c, s) pairs
+              const int col = args.dq_col0 + kb * kBK;
+              ptx::tma_load_2d(raw + kHalfCodesBytes, &map_s, &raw_full[s], col, nh / 64);
+              ptx::tma_load_2d(raw + kHalfCodesBytes + 128, &map_s2, &raw_full[s], 4 * (col / 512), nh / 64);
+            }
           }
         }
       }
@@ -266,19 +285,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
         }
         const uint8_t* codes = sRaw + s * Cfg::kRawBytes;
         const float* amax = reinterpret_cast<const float*>(codes + kHalfCodesBytes);
+        const int8_t* qam = reinterpret_cast<const int8_t*>(codes + kHalfCodesBytes);
+        const float* cs = reinterpret_cast<const float*>(codes + kHalfCodesBytes + 128);
         uint8_t* bt = sB + s * kHalfBTileBytes;
         if (!BMN) {
           const uint4 q0 = *reinterpret_cast<const uint4*>(codes + tr * 32);
           const uint4 q1 = *reinterpret_cast<const uint4*>(codes + tr * 32 + 16);
           const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          nf4_words_bf16<8>(w, amax[tr * 4 + (kb & 3)], bt + tr * 128, 0, tr & 7);
+          const int p = ((args.dq_col0 + tile_n0(t) + static_cast<int>(rank) * 128) >> 8) & 1;
+          const float am =
+              args.dq ? fmaf(cs[2 * p + 1], static_cast<float>(qam[tr]), cs[2 * p]) : amax[tr * 4 + (kb & 3)];
+          nf4_words_bf16<8>(w, am, bt + tr * 128, 0, tr & 7);
         } else {
           const int n = tr >> 1, a = tr & 1;
           const uint4 q0 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32);
           const uint4 q1 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32 + 16);
           const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          nf4_words_bf16<8>(w, amax[n * 4 + 2 * static_cast<int>(rank) + a], bt + a * (64 * 128) + n * 128, 0,
-                            n & 7);
+          const int p = ((args.dq_col0 + kb * kBK) >> 8) & 1;
+          const float am = args.dq ? fmaf(cs[a * 4 + 2 * p + 1], static_cast<float>(qam[a * 64 + n]), cs[a * 4 + 2 * p])
+                                   : amax[n * 4 + 2 * static_cast<int>(rank) + a];
+          nf4_words_bf16<8>(w, am, bt + a * (64 * 128) + n * 128, 0, n & 7);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();

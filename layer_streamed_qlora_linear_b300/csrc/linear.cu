@@ -207,12 +207,44 @@ static sl_status check_weight(const sl_weight* w) {
   if (w->kind == SL_WEIGHT_NF4) {
     SL_REQUIRE(w->codes && w->absmax, "sl_weight: NF4 needs codes and absmax");
     SL_REQUIRE(w->K % 256 == 0, "sl_weight: NF4 needs K % 256 == 0");
+  } else if (w->kind == SL_WEIGHT_NF4_DQ) {
+    SL_REQUIRE(w->codes && w->qabsmax && w->absmax2, "sl_weight: NF4_DQ needs codes, qabsmax and absmax2");
+    SL_REQUIRE(w->K % 256 == 0 && w->N % 256 == 0, "sl_weight: NF4_DQ needs N % 256 == 0 and K % 256 == 0");
+    SL_REQUIRE(w->dq_col0 >= 0 && w->dq_col0 % 256 == 0, "sl_weight: NF4_DQ needs dq_col0 a multiple of 256");
+    SL_REQUIRE(w->qabsmax_ld % 16 == 0 && w->qabsmax_ld >= w->dq_col0 + w->N,
+               "sl_weight: NF4_DQ needs qabsmax_ld % 16 == 0 and >= dq_col0 + N");
+    SL_REQUIRE(w->absmax2_ld % 4 == 0 && w->absmax2_ld >= 2 * ((w->dq_col0 + w->N) / 256),
+               "sl_weight: NF4_DQ needs absmax2_ld % 4 == 0 and >= 2 (dq_col0 + N) / 256");
   } else if (w->kind == SL_WEIGHT_BF16) {
     SL_REQUIRE(w->w, "sl_weight: BF16 needs w");
     SL_REQUIRE(w->K % 64 == 0, "sl_weight: BF16 needs K % 64 == 0");
   } else {
     return set_error(SL_ERR_INVALID, "sl_weight: unknown kind");
   }
+  return SL_OK;
+}
+
+// The frozen weight as the GEMM's B operand.
+static void bind_weight(GemmLaunch& g, const sl_weight* w) {
+  g.bsrc = (w->kind == SL_WEIGHT_BF16) ? kBSrcBF16 : kBSrcNF4;
+  g.w = w->w;
+  g.codes = w->codes;
+  g.absmax = w->absmax;
+  g.ldw = w->K;
+  if (w->kind == SL_WEIGHT_NF4_DQ) {
+    g.args.dq = 1;
+    g.args.dq_col0 = static_cast<int>(w->dq_col0);
+    g.qabsmax = w->qabsmax;
+    g.q_ld = w->qabsmax_ld;
+    g.absmax2 = w->absmax2;
+    g.a2_ld = w->absmax2_ld;
+  }
+}
+
+// The double-quantised absmax is read by the persistent CTA-pair GEMM only.
+static sl_status check_rows(const sl_weight* w, int64_t M, const char* who) {
+  if (w->kind == SL_WEIGHT_NF4_DQ && M <= 128)
+    return set_error(SL_ERR_UNSUPPORTED, std::string(who) + ": NF4_DQ weights need M > 128");
   return SL_OK;
 }
 
@@ -224,6 +256,8 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
   const bool lora = r > 0 && A && B;
   SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32 && T_save), "sl_lora_linear_fwd: need r % 8 == 0, r <= 32, T_save");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_fwd: M too large");
+  st = check_rows(w, M, "sl_lora_linear_fwd");
+  if (st != SL_OK) return st;
   (void)ws;
   (void)ws_bytes;
   int* err = device_error_word();
@@ -234,15 +268,11 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
-  g.bsrc = (w->kind == SL_WEIGHT_NF4) ? kBSrcNF4 : kBSrcBF16;
+  bind_weight(g, w);
   g.bmn = 0;
   g.epi = kEpiStoreBF16;
   g.A = X;
   g.lda = w->K;
-  g.w = w->w;
-  g.codes = w->codes;
-  g.absmax = w->absmax;
-  g.ldw = w->K;
   g.args.M = static_cast<int>(M);
   g.args.N = static_cast<int>(w->N);
   g.args.K = static_cast<int>(w->K);
@@ -266,6 +296,10 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32), "sl_lora_linear_bwd: need r % 8 == 0 and r <= 32");
   SL_REQUIRE(!lora || (X && T_save && dA && dB), "sl_lora_linear_bwd: LoRA backward needs X, T_save, dA, dB");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_bwd: M too large");
+  if (dX) {
+    st = check_rows(w, M, "sl_lora_linear_bwd");
+    if (st != SL_OK) return st;
+  }
   const LinWs L = lin_ws(M, w->N, w->K, lora ? r : 0);
   SL_REQUIRE(ws_bytes >= L.total && (L.total == 0 || ws), "sl_lora_linear_bwd: workspace too small");
   SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_lora_linear_bwd: workspace must be 256-byte aligned");
@@ -282,15 +316,11 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   }
   if (dX) {
     GemmLaunch g{};
-    g.bsrc = (w->kind == SL_WEIGHT_NF4) ? kBSrcNF4 : kBSrcBF16;
+    bind_weight(g, w);
     g.bmn = 1;
     g.epi = kEpiStoreBF16;
     g.A = dY;
     g.lda = w->N;
-    g.w = w->w;
-    g.codes = w->codes;
-    g.absmax = w->absmax;
-    g.ldw = w->K;
     g.args.M = static_cast<int>(M);
     g.args.N = static_cast<int>(w->K);
     g.args.K = static_cast<int>(w->N);
@@ -327,7 +357,7 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
 static sl_status check_group(const sl_weight* w, int G, const int64_t* N_g, int64_t M, int r, int bounds[5]) {
   sl_status st = check_weight(w);
   if (st != SL_OK) return st;
-  SL_REQUIRE(w->kind == SL_WEIGHT_NF4, "projection group: NF4 weights only");
+  SL_REQUIRE(w->kind != SL_WEIGHT_BF16, "projection group: NF4 weights only");
   SL_REQUIRE(M > 128 && M < (1LL << 31), "projection group: need 128 < M < 2^31");
   SL_REQUIRE(G >= 1 && G <= kSkMaxGroups && N_g, "projection group: need 1 <= G <= 4 projections");
   SL_REQUIRE(r >= 0 && r % 8 == 0 && r <= 32 && G * r <= 64, "projection group: need r % 8 == 0, r <= 32, G r <= 64");
@@ -363,15 +393,12 @@ sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
-  g.bsrc = kBSrcNF4;
+  bind_weight(g, w);
   g.bmn = 0;
   g.epi = kEpiStoreBF16;
   g.grouped = 1;
   g.A = X;
   g.lda = w->K;
-  g.codes = w->codes;
-  g.absmax = w->absmax;
-  g.ldw = w->K;
   g.args.M = static_cast<int>(M);
   g.args.N = static_cast<int>(w->N);
   g.args.K = static_cast<int>(w->K);
@@ -413,15 +440,12 @@ sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
   if (dX) {
     // dX = dY_cat W_cat + s U_cat A_cat: the plain dX GEMM at rank G r
     GemmLaunch g{};
-    g.bsrc = kBSrcNF4;
+    bind_weight(g, w);
     g.bmn = 1;
     g.epi = kEpiStoreBF16;
     g.grouped = 1;
     g.A = dY_cat;
     g.lda = NN;
-    g.codes = w->codes;
-    g.absmax = w->absmax;
-    g.ldw = K;
     g.args.M = static_cast<int>(M);
     g.args.N = K;
     g.args.K = NN;
@@ -489,6 +513,8 @@ sl_status linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t M, const
   SL_REQUIRE(!lora || (r % 8 == 0 && r <= 32 && T_save),
              "sl_lora_linear_fwd_noalloc: need r % 8 == 0, r <= 32, T_save");
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_fwd_noalloc: M too large");
+  st = check_rows(w, M, "sl_lora_linear_fwd_noalloc");
+  if (st != SL_OK) return st;
   const size_t need = lora ? noalloc_need(M, w->K, r) : 0;
   if (need > kNoAllocScratchBytes)
     return set_error(SL_ERR_INVALID, "sl_lora_linear_fwd_noalloc: needs " + std::to_string(need) +
@@ -508,15 +534,11 @@ sl_status linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t M, const
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
-  g.bsrc = (w->kind == SL_WEIGHT_NF4) ? kBSrcNF4 : kBSrcBF16;
+  bind_weight(g, w);
   g.bmn = 0;
   g.epi = kEpiStoreBF16;
   g.A = X;
   g.lda = w->K;
-  g.w = w->w;
-  g.codes = w->codes;
-  g.absmax = w->absmax;
-  g.ldw = w->K;
   g.args.M = static_cast<int>(M);
   g.args.N = static_cast<int>(w->N);
   g.args.K = static_cast<int>(w->K);
