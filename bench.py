@@ -9,9 +9,11 @@ from pinned host RAM through two device buffers.  Synthetic seeded data; no
 trained weights.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload stack8b|stack_qwen3b|layer8b|ce]
+                  [--workload stack8b|stack8b_dq|stack_qwen3b|layer8b|ce]
 
-Other workloads (not the headline line): the 36-layer Qwen2.5-3B-shaped
+Other workloads (not the headline line): the same 32-layer stack with the
+absmax double-quantised to 8 bits (the ~3.6 GB pinned store, 113 MB per
+layer, that the pages quote); the 36-layer Qwen2.5-3B-shaped
 stack with a bf16 base streamed at M=2048; one Llama-8B layer's seven NF4
 LoRA linears resident at M=2048 (fwd+bwd); the LM-head cross-entropy
 (M=2048, D=4096, V=128256).
@@ -36,6 +38,9 @@ WORKLOADS = {
     "stack8b": dict(kind="stack", base="nf4", L=32, M=1024, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
                     name="llama-3.1-8b-shaped 32-layer NF4 LoRA stack streamed from pinned host RAM, "
                          "fwd 0..31 + bwd 31..0"),
+    "stack8b_dq": dict(kind="stack", base="nf4dq", L=32, M=1024, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
+                       name="llama-3.1-8b-shaped 32-layer NF4 LoRA stack, 8-bit double-quantised absmax, streamed "
+                            "from pinned host RAM, fwd 0..31 + bwd 31..0"),
     "stack_qwen3b": dict(kind="stack", base="bf16", L=36, M=2048, D=2048, Dkv=256, F=11008, r=16, alpha=32.0,
                          name="qwen2.5-3b-shaped 36-layer bf16-base LoRA stack streamed from pinned host RAM"),
     "layer8b": dict(kind="layer", base="nf4", M=2048, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
@@ -139,12 +144,29 @@ def oracle_sample(w):
         ms = 64
         c = si.stack_case(3, 1, ms, w["D"], w["Dkv"], w["F"], w["r"])
         lw = c["layers"][0]
-        nf = w["base"] == "nf4"
+        nf = w["base"] in ("nf4", "nf4dq")
         q = {n: nf4.quantize(lw[n]["W"]) for n in si.PROJ_NAMES} if nf else None  # offline, not timed
+        dq = []
+        if w["base"] == "nf4dq":   # each absmax group double-quantised as one array (offline, not timed)
+            for names in (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)):
+                K, Ns = lw[names[0]]["W"].shape[1], [lw[n]["W"].shape[0] for n in names]
+                dq.append((names, Ns, K, *nf4.double_quantize(np.concatenate([q[n][1] for n in names]), sum(Ns), K)))
+
+        def base(n):
+            return nf4.dequantize_bf16(*q[n], *lw[n]["W"].shape) if nf else lw[n]["W"].astype(np.float64)
 
         def layer():
-            return {n: dict(W=(nf4.dequantize_bf16(*q[n], *lw[n]["W"].shape) if nf else lw[n]["W"].astype(np.float64)),
-                            A=lw[n]["A"].astype(np.float64), B=lw[n]["B"].astype(np.float64)) for n in si.PROJ_NAMES}
+            Ws = {}
+            if dq:
+                for names, Ns, K, qa, a2 in dq:
+                    ap, off = nf4.dq_absmax(qa, a2, sum(Ns), K), 0
+                    for n, N in zip(names, Ns):
+                        Ws[n] = nf4.dequantize_bf16(q[n][0], ap[off * K // 64:(off + N) * K // 64], N, K)
+                        off += N
+            else:
+                Ws = {n: base(n) for n in si.PROJ_NAMES}
+            return {n: dict(W=Ws[n], A=lw[n]["A"].astype(np.float64), B=lw[n]["B"].astype(np.float64))
+                    for n in si.PROJ_NAMES}
 
         if w["kind"] == "stack":
             def step():
@@ -244,7 +266,7 @@ def run_ours(args):
     h2d_peak = None
 
     if w["kind"] == "stack":
-        kind = sl.SL_WEIGHT_NF4 if w["base"] == "nf4" else sl.SL_WEIGHT_BF16
+        kind = {"nf4": sl.SL_WEIGHT_NF4, "nf4dq": sl.SL_WEIGHT_NF4_DQ, "bf16": sl.SL_WEIGHT_BF16}[w["base"]]
         if kind == sl.SL_WEIGHT_BF16:
             dominant = ("bf16_fwd", "bf16_dx")
             kname = "gemm_tc_kernel<BF16> (bf16 base + LoRA fold; fwd and dX)"
@@ -288,7 +310,10 @@ def run_ours(args):
         e2e_bytes = (h0_h.numel() * 4 + dh_h.numel() * 4, out_h.numel() * 4)
         h2d_peak = pinned_h2d_peak(torch, dev)
         config = {"workload": w["name"], "tokens": M, "layers": L, "D": D, "Dkv": Dkv, "F": F, "rank": r,
-                  "alpha": alpha, "base": "NF4 blocksize 64 fp32 absmax" if kind == sl.SL_WEIGHT_NF4 else "bf16",
+                  "alpha": alpha, "base": {sl.SL_WEIGHT_NF4: "NF4 blocksize 64 fp32 absmax",
+                                           sl.SL_WEIGHT_NF4_DQ: "NF4 blocksize 64, 8-bit absmax (fp32 offset and "
+                                                                "scale per 256 blocks)",
+                                           sl.SL_WEIGHT_BF16: "bf16"}[kind],
                   "l2": f"inputs larger than L2 ({stk.host_bytes / 1e9:.1f} GB streamed base + activations)"}
     elif w["kind"] == "layer":
         # One decoder layer's seven projections as a framework runs them: q/k/v

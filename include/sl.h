@@ -276,13 +276,29 @@ size_t sl_lora_group_workspace_size(int64_t M, int32_t G, int32_t r);
  * N = D + 2 Dkv or 2 F rows, as the projection groups use them).
  * offsets[2p] / offsets[2p+1] receive the byte offsets of projection p's
  * codes / absmax (NF4) or of its weight / 0 (BF16), every offset 256-byte
- * aligned; *blob_bytes the total. */
+ * aligned; *blob_bytes the total.
+ * NF4_DQ (the 8-bit absmax that makes the pages' 113 MB layer buffer and
+ * 3.60 GB base store for Llama-3.1-8B: "Soup: Fine-Tuning ...", "Layer
+ * Streaming: The Mechanism ..."): the codes as for NF4, then for each of the
+ * four absmax groups q/k/v, o, gate/up, down (projections that read one
+ * input) its qabsmax int8 [K/64, N_group] and its absmax2 fp32
+ * [K/64, round_up(2 N_group / 256, 4)] (sl_nf4_double_quantize of the
+ * group's fp32 absmax, rows of its projections in order); offsets[2p+1] is
+ * the qabsmax array of projection p's group.  Needs Dkv % 256 == 0. */
 sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F,
                                size_t offsets[14], size_t* blob_bytes);
 
+/* The double-quantised absmax of an NF4_DQ layer blob, per projection p:
+ * its group's qabsmax at byte q_off[p] (rows of q_ld[p] bytes), absmax2 at
+ * byte a2_off[p] (rows of a2_ld[p] floats), and the projection's first
+ * column col0[p] in both (its sl_weight's dq_col0).  Same size rules as
+ * sl_stack_blob_layout for NF4_DQ. */
+sl_status sl_stack_dq_layout(int64_t D, int64_t Dkv, int64_t F, size_t q_off[7], int64_t q_ld[7],
+                             size_t a2_off[7], int64_t a2_ld[7], int64_t col0[7]);
+
 typedef struct {
   int32_t L;                        /* number of layers */
-  int32_t kind;                     /* SL_WEIGHT_NF4 or SL_WEIGHT_BF16 */
+  int32_t kind;                     /* SL_WEIGHT_NF4, SL_WEIGHT_NF4_DQ (M > 128 only) or SL_WEIGHT_BF16 */
   int64_t D, Dkv, F;                /* hidden, kv width (multiple of 128), MLP width */
   const void* const* host_blobs;    /* L pointers to PINNED host blobs (sl_stack_blob_layout) */
   const void* const* device_blobs;  /* L device copies for SL_MODE_RESIDENT, or NULL */

@@ -69,6 +69,7 @@ _SIGS = {
                                  _P, _P, _I32, _P, _SZ, _P]),
     "sl_lora_group_workspace_size": (_SZ, [_I64, _I32, _I32]),
     "sl_stack_blob_layout": (_I32, [_I32, _I64, _I64, _I64, _P, _P]),
+    "sl_stack_dq_layout": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "sl_stack_create": (_I32, [ctypes.POINTER(sl_stack_desc), _P, _P, _P]),
     "sl_stack_destroy": (_I32, [_P]),
     "sl_stack_workspace_size": (_SZ, [_P, _I64, _I32]),
@@ -281,7 +282,18 @@ def sl_stack_blob_layout(kind, D, Dkv, F):
     return list(offs), total.value
 
 
+def sl_stack_dq_layout(D, Dkv, F):
+    """Per projection of an NF4_DQ blob: dict(q_off, q_ld, a2_off, a2_ld, col0) (see include/sl.h)."""
+    arrs = [(ctypes.c_size_t * 7)(), (ctypes.c_int64 * 7)(), (ctypes.c_size_t * 7)(), (ctypes.c_int64 * 7)(),
+            (ctypes.c_int64 * 7)()]
+    _check(lib().sl_stack_dq_layout(D, Dkv, F, *arrs))
+    keys = ("q_off", "q_ld", "a2_off", "a2_ld", "col0")
+    return [{k: int(a[p]) for k, a in zip(keys, arrs)} for p in range(7)]
+
+
 PROJ_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+# projections whose absmax a double-quantised blob keeps in one 8-bit array
+DQ_GROUPS = ((0, 1, 2), (3,), (4, 5), (6,))
 
 
 def proj_shapes(D, Dkv, F):
@@ -293,12 +305,34 @@ def build_layer_blob(kind, D, Dkv, F, weights, stream=None):
     """One layer blob on the device from its seven bf16 weights [N, K] (device tensors).
 
     NF4 blobs are filled by sl_nf4_quantize directly at the layout offsets;
-    bf16 blobs hold the weights as they are (the storage dtype).
+    NF4_DQ blobs take the codes the same way and the absmax of each group
+    (DQ_GROUPS) through sl_nf4_double_quantize; bf16 blobs hold the weights
+    as they are (the storage dtype).
     """
     import torch
     offs, total = sl_stack_blob_layout(kind, D, Dkv, F)
     blob = torch.zeros(total, dtype=torch.uint8, device="cuda")
-    for p, ((N, K), W) in enumerate(zip(proj_shapes(D, Dkv, F), weights)):
+    shapes = proj_shapes(D, Dkv, F)
+    if kind == SL_WEIGHT_NF4_DQ:
+        dq = sl_stack_dq_layout(D, Dkv, F)
+        for group in DQ_GROUPS:
+            K = shapes[group[0]][1]
+            Ng = sum(shapes[p][0] for p in group)
+            am = torch.empty(Ng * K // 64, dtype=torch.float32, device="cuda")
+            for p in group:
+                N = shapes[p][0]
+                assert tuple(weights[p].shape) == (N, K)
+                c0 = dq[p]["col0"] * K // 64
+                sl_nf4_quantize(weights[p], blob[offs[2 * p]: offs[2 * p] + N * K // 2], am[c0: c0 + N * K // 64],
+                                stream)
+            d = dq[group[0]]
+            rows = K // 64
+            q = blob[d["q_off"]: d["q_off"] + rows * d["q_ld"]].view(torch.int8).view(rows, d["q_ld"])
+            a2 = blob[d["a2_off"]: d["a2_off"] + rows * d["a2_ld"] * 4].view(torch.float32).view(rows, d["a2_ld"])
+            sl_nf4_double_quantize(am, Ng, K, q, a2, stream=stream)
+        torch.cuda.synchronize()   # the fp32 absmax `am` is freed on return
+        return blob
+    for p, ((N, K), W) in enumerate(zip(shapes, weights)):
         assert tuple(W.shape) == (N, K)
         if kind == SL_WEIGHT_NF4:
             codes = blob[offs[2 * p]: offs[2 * p] + N * K // 2]

@@ -36,6 +36,10 @@ struct sl_stack {
   std::vector<const void*> host;
   std::vector<const void*> dev;
   size_t offs[14] = {0};
+  // NF4_DQ: per projection its group's qabsmax / absmax2 arrays, their row
+  // lengths and the projection's first column in them
+  size_t dq_q[7] = {0}, dq_a2[7] = {0};
+  int64_t dq_qld[7] = {0}, dq_a2ld[7] = {0}, dq_col0[7] = {0};
   size_t blob_bytes = 0;
   void* buf[2] = {nullptr, nullptr};
   int buf_layer[2] = {-1, -1};
@@ -63,7 +67,18 @@ void proj_shapes(int64_t D, int64_t Dkv, int64_t F, Proj p[7]) {
   p[6] = {D, F};    // down
 }
 
-sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[14], size_t* total) {
+struct DqLayout {
+  size_t q[7], a2[7];
+  int64_t q_ld[7], a2_ld[7], col0[7];
+};
+
+// Absmax groups of a double-quantised blob: q/k/v, o, gate/up, down (the
+// projections of one group read one input, so their absmax share one
+// transposed 8-bit array and the projection group reads it as one weight).
+constexpr int kDqFirst[4] = {0, 3, 4, 6};
+constexpr int kDqCount[4] = {3, 1, 2, 1};
+
+sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[14], size_t* total, DqLayout* dq) {
   Proj p[7];
   proj_shapes(D, Dkv, F, p);
   // NF4: all codes, then all absmax, so that the q, k, v and the gate, up
@@ -73,7 +88,7 @@ sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[14], s
   for (int i = 0; i < 7; ++i) {
     const size_t n = static_cast<size_t>(p[i].N) * static_cast<size_t>(p[i].K);
     offs[2 * i] = off;
-    off = align_up(off + (kind == SL_WEIGHT_NF4 ? n / 2 : n * 2), 256);
+    off = align_up(off + (kind == SL_WEIGHT_BF16 ? n * 2 : n / 2), 256);
     offs[2 * i + 1] = 0;
   }
   if (kind == SL_WEIGHT_NF4)
@@ -81,6 +96,30 @@ sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[14], s
       const size_t n = static_cast<size_t>(p[i].N) * static_cast<size_t>(p[i].K);
       offs[2 * i + 1] = off;
       off = align_up(off + n / 64 * 4, 256);
+    }
+  if (kind == SL_WEIGHT_NF4_DQ)
+    for (int g = 0; g < 4; ++g) {
+      const int p0 = kDqFirst[g];
+      int64_t N = 0;
+      for (int i = 0; i < kDqCount[g]; ++i) N += p[p0 + i].N;
+      const int64_t rows = p[p0].K / 64, q_ld = N, a2_ld = (2 * (N / 256) + 3) / 4 * 4;
+      const size_t q_off = off;
+      off = align_up(off + static_cast<size_t>(rows * q_ld), 256);
+      const size_t a2_off = off;
+      off = align_up(off + static_cast<size_t>(rows * a2_ld) * 4, 256);
+      int64_t col = 0;
+      for (int i = 0; i < kDqCount[g]; ++i) {
+        const int pi = p0 + i;
+        offs[2 * pi + 1] = q_off;
+        if (dq) {
+          dq->q[pi] = q_off;
+          dq->a2[pi] = a2_off;
+          dq->q_ld[pi] = q_ld;
+          dq->a2_ld[pi] = a2_ld;
+          dq->col0[pi] = col;
+        }
+        col += p[pi].N;
+      }
     }
   *total = off;
   return SL_OK;
@@ -188,10 +227,24 @@ void weights_of(const sl_stack* s, const void* base, sl_weight w[7]) {
     w[i].kind = s->kind;
     w[i].N = p[i].N;
     w[i].K = p[i].K;
+    w[i].qabsmax = nullptr;
+    w[i].qabsmax_ld = 0;
+    w[i].absmax2 = nullptr;
+    w[i].absmax2_ld = 0;
+    w[i].dq_col0 = 0;
     if (s->kind == SL_WEIGHT_NF4) {
       w[i].codes = b + s->offs[2 * i];
       w[i].absmax = reinterpret_cast<const float*>(b + s->offs[2 * i + 1]);
       w[i].w = nullptr;
+    } else if (s->kind == SL_WEIGHT_NF4_DQ) {
+      w[i].codes = b + s->offs[2 * i];
+      w[i].absmax = nullptr;
+      w[i].w = nullptr;
+      w[i].qabsmax = reinterpret_cast<const int8_t*>(b + s->dq_q[i]);
+      w[i].qabsmax_ld = s->dq_qld[i];
+      w[i].absmax2 = reinterpret_cast<const float*>(b + s->dq_a2[i]);
+      w[i].absmax2_ld = s->dq_a2ld[i];
+      w[i].dq_col0 = s->dq_col0[i];
     } else {
       w[i].codes = nullptr;
       w[i].absmax = nullptr;
@@ -207,7 +260,8 @@ void weights_of(const sl_stack* s, const void* base, sl_weight w[7]) {
   } while (0)
 
 // The q/k/v (p0 = 0, G = 3) or gate/up (p0 = 4, G = 2) weights as one NF4
-// weight: the blob keeps them back to back.
+// weight: the blob keeps them back to back (and a double-quantised blob
+// their absmax in one array, from the first projection's column on).
 sl_weight group_weight(const sl_weight w[7], int p0, int G) {
   sl_weight g = w[p0];
   for (int i = 1; i < G; ++i) g.N += w[p0 + i].N;
@@ -366,7 +420,7 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
 // and their gradients back to back.
 bool can_group(const sl_stack* s, int64_t M, int r, int p0, int G, const void* const* A, const void* const* B,
                float* const* dA, float* const* dB) {
-  if (s->kind != SL_WEIGHT_NF4 || M <= 128 || M >= (1LL << 31)) return false;
+  if (s->kind == SL_WEIGHT_BF16 || M <= 128 || M >= (1LL << 31)) return false;
   if (r > 0 && G * r > 64) return false;
   Proj p[7];
   proj_shapes(s->D, s->Dkv, s->F, p);
@@ -402,10 +456,31 @@ sl_status ensure_layer(sl_stack* s, int l, uint64_t* h2d) {
 extern "C" sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F, size_t offsets[14],
                                           size_t* blob_bytes) {
   SL_REQUIRE(offsets && blob_bytes, "sl_stack_blob_layout: null output");
-  SL_REQUIRE(kind == SL_WEIGHT_NF4 || kind == SL_WEIGHT_BF16, "sl_stack_blob_layout: unknown kind");
+  SL_REQUIRE(kind == SL_WEIGHT_NF4 || kind == SL_WEIGHT_BF16 || kind == SL_WEIGHT_NF4_DQ,
+             "sl_stack_blob_layout: unknown kind");
   SL_REQUIRE(D > 0 && Dkv > 0 && F > 0 && D % 256 == 0 && F % 256 == 0 && Dkv % 128 == 0 && D % Dkv == 0,
              "sl_stack_blob_layout: need D, F multiples of 256, Dkv a multiple of 128 dividing D");
-  return layout(kind, D, Dkv, F, offsets, blob_bytes);
+  SL_REQUIRE(kind != SL_WEIGHT_NF4_DQ || Dkv % 256 == 0,
+             "sl_stack_blob_layout: the double-quantised absmax needs Dkv a multiple of 256");
+  return layout(kind, D, Dkv, F, offsets, blob_bytes, nullptr);
+}
+
+extern "C" sl_status sl_stack_dq_layout(int64_t D, int64_t Dkv, int64_t F, size_t q_off[7], int64_t q_ld[7],
+                                        size_t a2_off[7], int64_t a2_ld[7], int64_t col0[7]) {
+  SL_REQUIRE(q_off && q_ld && a2_off && a2_ld && col0, "sl_stack_dq_layout: null output");
+  size_t offs[14], bytes = 0;
+  sl_status st = sl_stack_blob_layout(SL_WEIGHT_NF4_DQ, D, Dkv, F, offs, &bytes);
+  if (st != SL_OK) return st;
+  DqLayout dq{};
+  layout(SL_WEIGHT_NF4_DQ, D, Dkv, F, offs, &bytes, &dq);
+  for (int i = 0; i < 7; ++i) {
+    q_off[i] = dq.q[i];
+    q_ld[i] = dq.q_ld[i];
+    a2_off[i] = dq.a2[i];
+    a2_ld[i] = dq.a2_ld[i];
+    col0[i] = dq.col0[i];
+  }
+  return SL_OK;
 }
 
 extern "C" sl_status sl_stack_create(const sl_stack_desc* desc, sl_stack** out, size_t* host_bytes,
@@ -446,6 +521,17 @@ extern "C" sl_status sl_stack_create(const sl_stack_desc* desc, sl_stack** out, 
   s->host.assign(desc->host_blobs, desc->host_blobs + desc->L);
   if (desc->device_blobs) s->dev.assign(desc->device_blobs, desc->device_blobs + desc->L);
   std::memcpy(s->offs, offs, sizeof(offs));
+  if (s->kind == SL_WEIGHT_NF4_DQ) {
+    DqLayout dq{};
+    layout(s->kind, s->D, s->Dkv, s->F, offs, &bytes, &dq);
+    for (int i = 0; i < 7; ++i) {
+      s->dq_q[i] = dq.q[i];
+      s->dq_a2[i] = dq.a2[i];
+      s->dq_qld[i] = dq.q_ld[i];
+      s->dq_a2ld[i] = dq.a2_ld[i];
+      s->dq_col0[i] = dq.col0[i];
+    }
+  }
   s->blob_bytes = bytes;
   cudaGetDevice(&s->device);
   auto fail = [&](cudaError_t e, const char* what) {
@@ -499,6 +585,8 @@ extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float
   SL_REQUIRE(h0 && dh_top && hL && dh0 && ws && M > 0, "sl_stream_stack_step: null argument");
   SL_REQUIRE(r == 0 || (A && B && dA && dB), "sl_stream_stack_step: adapters and gradients required for r > 0");
   SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_stream_stack_step: workspace must be 256-byte aligned");
+  if (s->kind == SL_WEIGHT_NF4_DQ && M <= 128)
+    return set_error(SL_ERR_UNSUPPORTED, "sl_stream_stack_step: double-quantised stacks need M > 128");
   int dev = 0;
   SL_CHECK_CUDA(cudaGetDevice(&dev));
   SL_REQUIRE(dev == s->device, "sl_stream_stack_step: current device differs from the handle's");

@@ -42,11 +42,16 @@ class Setup:
                 blob = sl.build_layer_blob(kind, D, Dkv, F, Ws)
                 self._add_blob(blob)
                 ref = {}
+                Wdq = dq_ref_weights(sl, lw) if with_oracle and kind == sl.SL_WEIGHT_NF4_DQ else None
                 for n in si.PROJ_NAMES:
                     W = lw[n]["W"]
                     if with_oracle:
-                        Wr = nf4.dequantize_bf16(*nf4.quantize(W), *W.shape) if kind == sl.SL_WEIGHT_NF4 \
-                            else W.astype(np.float64)
+                        if kind == sl.SL_WEIGHT_NF4:
+                            Wr = nf4.dequantize_bf16(*nf4.quantize(W), *W.shape)
+                        elif kind == sl.SL_WEIGHT_NF4_DQ:
+                            Wr = Wdq[n]
+                        else:
+                            Wr = W.astype(np.float64)
                         ref[n] = dict(W=Wr, A=lw[n]["A"].astype(np.float64), B=lw[n]["B"].astype(np.float64))
                     self.A.append(dev_bf16(lw[n]["A"]))
                     self.B.append(dev_bf16(lw[n]["B"]))
@@ -92,6 +97,24 @@ class Setup:
         self.stack.step(mode, self.h0, self.dh, self.A, self.B, self.r, self.alpha, hL, dh0, dA, dB, self.ws)
         sl.sl_check_device_errors()
         return hL, dh0, dA, dB
+
+
+def dq_ref_weights(sl, lw):
+    """The oracle's bf16 weights of a double-quantised layer: each absmax group
+    (q/k/v, o, gate/up, down) double-quantised as one [K/64, N_group] array."""
+    out = {}
+    for group in sl.DQ_GROUPS:
+        names = [si.PROJ_NAMES[p] for p in group]
+        qs = [nf4.quantize(lw[n]["W"]) for n in names]
+        K = lw[names[0]]["W"].shape[1]
+        Ns = [lw[n]["W"].shape[0] for n in names]
+        q, a2 = nf4.double_quantize(np.concatenate([a for _, a in qs]), sum(Ns), K)
+        ap = nf4.dq_absmax(q, a2, sum(Ns), K)
+        off = 0
+        for n, (codes, _), N in zip(names, qs, Ns):
+            out[n] = nf4.dequantize_bf16(codes, ap[off * K // 64:(off + N) * K // 64], N, K)
+            off += N
+    return out
 
 
 def same_bits(a, b):
@@ -232,4 +255,37 @@ def test_adapters_off_pass_equals_zero_B(gpu_lib):
     assert torch.equal(hL0, hL1) and torch.equal(dh00, dh01)
     assert all(torch.count_nonzero(a) == 0 for a in dA)      # dA = s (dY B)^T X = 0 when B = 0
     assert all(torch.count_nonzero(b) > 0 for b in dB)
+    S.stack.close()
+
+
+@pytest.mark.parametrize("packed", [True, False])
+def test_dq_stack_matches_oracle_and_resident(gpu_lib, packed):
+    """Double-quantised absmax (8-bit, per absmax group): oracle parity on the
+    grouped (packed adapters) and per-projection paths, streamed == resident
+    bit for bit, and the blob is the smaller one that streams."""
+    sl = gpu_lib
+    S = Setup(sl, sl.SL_WEIGHT_NF4_DQ, L=3, M=160, D=512, Dkv=256, F=768, r=16, alpha=32.0, seed=29, packed=packed)
+    hL, dh0, dA, dB = S.run(sl.SL_MODE_STREAMED)
+    ohL, odh0, ograds = stack.stack_step(S.h0_np, S.dh_np, S.ref_layers, 32.0, rnd=True)
+    assert rel_fro(host(hL), ohL) <= BF16_TOL
+    assert rel_fro(host(dh0), odh0) <= BF16_TOL
+    for l in range(S.L):
+        for p, n in enumerate(si.PROJ_NAMES):
+            assert rel_fro(host(dA[7 * l + p]), ograds[l][n][0]) <= BF16_TOL, (l, n)
+            assert rel_fro(host(dB[7 * l + p]), ograds[l][n][1]) <= BF16_TOL, (l, n)
+    r_ = S.run(sl.SL_MODE_RESIDENT)
+    for x, y in zip((hL, dh0, *dA, *dB), (r_[0], r_[1], *r_[2], *r_[3])):
+        assert same_bits(x, y)
+    _, nf4_bytes = sl.sl_stack_blob_layout(sl.SL_WEIGHT_NF4, 512, 256, 768)
+    assert S.stack.host_bytes // S.L < nf4_bytes
+    S.stack.close()
+
+
+def test_dq_stack_rejects_small_m(gpu_lib):
+    sl = gpu_lib
+    S = Setup(sl, sl.SL_WEIGHT_NF4_DQ, L=2, M=128, D=256, Dkv=256, F=512, r=8, alpha=16.0, seed=31,
+              with_oracle=False)
+    with pytest.raises(sl.SLError) as e:
+        S.run(sl.SL_MODE_STREAMED)
+    assert e.value.status == sl.SL_ERR_UNSUPPORTED
     S.stack.close()
