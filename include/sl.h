@@ -353,6 +353,51 @@ sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64
  * device and the number of libsl kernels launched. */
 sl_status sl_stack_last_step_stats(const sl_stack* s, uint64_t* h2d_bytes, uint64_t* kernels);
 
+/* ------------------------------------- attention of the full decoder layer */
+/* Causal grouped-query attention with rotary positions, the token mixing of
+ * a Llama-shaped decoder layer (the pages name Llama-3.1-8B and Qwen2.5-3B
+ * but do not describe the layer: "Soup CLI Lets You Fine-Tune an 8B LLM
+ * ...", "How Layer Streaming Works").  Layout: M rows = M / S sequences of S
+ * tokens (S % 128 == 0), positions 0..S-1 in every sequence; q [M, H*128],
+ * k and v [M, Hkv*128] bf16 with row strides (elements, multiples of 8,
+ * 16-byte aligned bases); query head h reads kv head h / (H / Hkv); scores
+ * q . k / sqrt(128), causal inside each sequence. */
+
+/* Rotary table for positions 0..S-1: table[p*128 + i] = cos(p theta^(-i/64)),
+ * table[p*128 + 64 + i] = sin(p theta^(-i/64)), i < 64; fp32 [S, 128],
+ * computed in fp64. */
+sl_status sl_rope_table(int64_t S, double theta, float* table, cudaStream_t stream);
+
+/* In place on x [M, nheads*128] bf16 (row stride ld): the pairs (i, i + 64)
+ * of every head rotated by the angle of the row's position (row % S), or by
+ * its negative (inverse != 0), in fp32, rounded once to bf16. */
+sl_status sl_rope_apply(void* x, int64_t ld, int64_t M, int32_t nheads, int64_t S, const float* table,
+                        int32_t inverse, cudaStream_t stream);
+
+/* o [M, H*128] bf16 (row stride ldo) = softmax(q k^T / sqrt(128) + causal
+ * mask) v per head, and lse [H, M] fp32 (head-major) = the natural log of
+ * each row's softmax normaliser.  One kernel (tcgen05: S and P V on the
+ * tensor cores, the online softmax in registers). */
+sl_status sl_attention_fwd(const void* q, int64_t ldq, const void* k, int64_t ldk, const void* v, int64_t ldv,
+                           int64_t M, int64_t S, int32_t H, int32_t Hkv, void* o, int64_t ldo, float* lse,
+                           cudaStream_t stream);
+
+/* Bytes of the backward's workspace: Di [H, M] fp32. */
+size_t sl_attention_workspace_size(int64_t M, int32_t H);
+
+/* The backward given o, lse of the forward and dO = dL/do (bf16, row
+ * stride lddo): dq [M, H*128], dk and dv [M, Hkv*128] bf16, each written
+ * once (dk, dv summed over the query heads of their kv head inside one CTA:
+ * bitwise reproducible).  rope_table (nullable, sl_rope_table): dq and dk
+ * leave rotated by the inverse angle, i.e. they are the gradients of q and
+ * k before sl_rope_apply.  ws: sl_attention_workspace_size bytes, 16-byte
+ * aligned. */
+sl_status sl_attention_bwd(const void* q, int64_t ldq, const void* k, int64_t ldk, const void* v, int64_t ldv,
+                           const void* o, int64_t ldo, const void* dO, int64_t lddo, const float* lse, int64_t M,
+                           int64_t S, int32_t H, int32_t Hkv, void* dq, int64_t lddq, void* dk, int64_t lddk,
+                           void* dv, int64_t lddv, const float* rope_table, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
 /* ------------------------------------------------ LM-head cross-entropy (a8) */
 
 /* loss = (1/N_valid) sum over rows with labels[i] != ignore_index of

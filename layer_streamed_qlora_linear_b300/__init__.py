@@ -70,6 +70,12 @@ _SIGS = {
     "sl_lora_group_workspace_size": (_SZ, [_I64, _I32, _I32]),
     "sl_stack_blob_layout": (_I32, [_I32, _I64, _I64, _I64, _P, _P]),
     "sl_stack_dq_layout": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "sl_rope_table": (_I32, [_I64, ctypes.c_double, _P, _P]),
+    "sl_rope_apply": (_I32, [_P, _I64, _I64, _I32, _I64, _P, _I32, _P]),
+    "sl_attention_fwd": (_I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I32, _I32, _P, _I64, _P, _P]),
+    "sl_attention_workspace_size": (_SZ, [_I64, _I32]),
+    "sl_attention_bwd": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I32, _I32,
+                                _P, _I64, _P, _I64, _P, _I64, _P, _P, _SZ, _P]),
     "sl_stack_create": (_I32, [ctypes.POINTER(sl_stack_desc), _P, _P, _P]),
     "sl_stack_destroy": (_I32, [_P]),
     "sl_stack_workspace_size": (_SZ, [_P, _I64, _I32]),
@@ -272,6 +278,45 @@ def sl_lora_group_bwd(weight: Weight, N_g, X, dY_cat, A_cat, B_cat, r, alpha, T_
 
 def sl_lora_group_workspace_size(M, G, r):
     return int(lib().sl_lora_group_workspace_size(int(M), int(G), int(r)))
+
+
+# ---------------------------------------------------------------- attention
+def _ld(t):
+    """Row stride (elements) of a 2-D row-major view."""
+    return int(t.stride(0))
+
+
+def sl_rope_table(S, theta, table, stream=None):
+    """table fp32 [S, 128]: cos / sin of p * theta^(-i/64)."""
+    _check(lib().sl_rope_table(int(S), float(theta), _ptr(table), _stream(stream)))
+
+
+def sl_rope_apply(x, S, table, inverse=False, stream=None):
+    """In place on the bf16 2-D view x [M, nheads*128] (any row stride)."""
+    _check(lib().sl_rope_apply(_ptr(x), _ld(x), x.shape[0], x.shape[1] // 128, int(S), _ptr(table), int(inverse),
+                               _stream(stream)))
+
+
+def sl_attention_fwd(q, k, v, S, o, lse, stream=None):
+    """Causal GQA attention on 2-D bf16 views q [M, H*128], k, v [M, Hkv*128]; o [M, H*128], lse fp32 [H, M]."""
+    M, H, Hkv = q.shape[0], q.shape[1] // 128, k.shape[1] // 128
+    _check(lib().sl_attention_fwd(_ptr(q), _ld(q), _ptr(k), _ld(k), _ptr(v), _ld(v), M, int(S), H, Hkv, _ptr(o),
+                                  _ld(o), _ptr(lse), _stream(stream)))
+
+
+def sl_attention_workspace_size(M, H):
+    return int(lib().sl_attention_workspace_size(int(M), int(H)))
+
+
+def sl_attention_bwd(q, k, v, o, dO, lse, S, dq, dk, dv, rope_table=None, ws=None, stream=None):
+    import torch
+    M, H, Hkv = q.shape[0], q.shape[1] // 128, k.shape[1] // 128
+    if ws is None:
+        ws = torch.empty(sl_attention_workspace_size(M, H), dtype=torch.uint8, device=q.device)
+    _check(lib().sl_attention_bwd(_ptr(q), _ld(q), _ptr(k), _ld(k), _ptr(v), _ld(v), _ptr(o), _ld(o), _ptr(dO),
+                                  _ld(dO), _ptr(lse), M, int(S), H, Hkv, _ptr(dq), _ld(dq), _ptr(dk), _ld(dk),
+                                  _ptr(dv), _ld(dv), _ptr(rope_table), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)))
 
 
 # -------------------------------------------------------------------- stack

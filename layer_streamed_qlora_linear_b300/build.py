@@ -13,7 +13,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libsl.so")
-SOURCES = ["api.cu", "nf4.cu", "gemm.cu", "linear.cu", "glue.cu", "stack.cu", "ce.cu", "skinny.cu"]
+SOURCES = ["api.cu", "nf4.cu", "gemm.cu", "linear.cu", "glue.cu", "stack.cu", "ce.cu", "skinny.cu", "attn.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
          "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC,-O2", "-I", os.path.join(ROOT, "include")]

@@ -1,0 +1,1105 @@
+// Causal grouped-query attention with rotary positions on tcgen05.
+//
+// Forward (one CTA per 128-query tile, head and sequence): Q stays in shared
+// memory, K and V tiles of 128 keys stream through a two-stage TMA ring.
+// The MMA warp computes S = Q K^T into one of two TMEM buffers one tile
+// ahead; four softmax warps (one query row per thread) take the running
+// row max over the tile, write P = exp2(S c - m) as bf16 into a 128-byte-
+// swizzled tile, and the MMA warp computes O_part = P V (V as an MN-major
+// operand) into one of two more TMEM buffers.  The softmax warps keep O in
+// registers: O = O alpha + O_part with alpha = exp2(m_old - m_new).
+//
+// Backward (no atomics: every output element is summed by one CTA in a
+// fixed order, so results are bitwise reproducible):
+//   dq kernel  (per 128-query tile and head): over the key blocks of 64,
+//              S = Q K^T and dP = dO V^T, dS = P (dP - Di) into shared
+//              memory, dQ += dS K;
+//   dkdv kernel (per 128-key tile and kv head): over the query heads of the
+//              kv head and their query blocks of 64, S^T = K Q^T and
+//              dP^T = V dO^T, P^T and dS^T into shared memory,
+//              dV += P^T dO, dK += dS^T Q.
+// Di = rowsum(dO * O) comes from a small pre-pass.  The epilogues scale dQ
+// and dK by 1/sqrt(128) and rotate them back by the inverse rotary angle.
+// Every wait is bounded; a timeout raises SL_ERR_TIMEOUT through the
+// library's device error word.
+#include <cmath>
+#include <utility>
+
+#include "attn.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace sl {
+namespace {
+
+constexpr int kAtAtom128 = 128 * 128;   // 128 rows x 128 B (one SW128 atom of 128 rows)
+constexpr int kAtAtom64 = 64 * 128;     // 64 rows x 128 B
+constexpr int kAtTile = 2 * kAtAtom128; // [128 rows][128] bf16
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+  return lo | (hi << 16);
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 16-byte chunk c (0..7) of row `row` of a 128-byte-swizzled atom.
+__device__ __forceinline__ uint4* swz(uint8_t* atom, int row, int c) {
+  return reinterpret_cast<uint4*>(atom + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+// K-major SW128 operand whose K extent spans atoms of `atom` bytes: k16 step kk.
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, int atom) {
+  return ptx::smem_desc(base + (kk >> 2) * atom + (kk & 3) * 32, 16, 1024, 2);
+}
+// MN-major SW128 operand (N = 128: two atoms of `atom` bytes along N): k16 step kk.
+__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk, int atom) {
+  return ptx::smem_desc(base + kk * 2048, atom, 1024, 2);
+}
+
+// ------------------------------------------------------------------- rope
+__global__ void rope_table_kernel(int64_t S, double theta, float* __restrict__ table) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= S * 64) return;
+  const int64_t p = t / 64;
+  const int i = static_cast<int>(t % 64);
+  const double ang = static_cast<double>(p) * pow(theta, -static_cast<double>(i) / 64.0);
+  table[p * 128 + i] = static_cast<float>(cos(ang));
+  table[p * 128 + 64 + i] = static_cast<float>(sin(ang));
+}
+
+// One thread per (row, head, 8 pairs).
+__global__ void rope_apply_kernel(uint16_t* __restrict__ x, int64_t ld, int64_t M, int nheads, int64_t S,
+                                  const float* __restrict__ table, float sgn) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= M * nheads * 8) return;
+  const int64_t row = t / (nheads * 8);
+  const int hc = static_cast<int>(t % (nheads * 8));
+  const int h = hc / 8, c = hc % 8;
+  uint16_t* p = x + row * ld + h * 128 + c * 8;
+  const float* cs = table + (row % S) * 128 + c * 8;
+  uint4 a = *reinterpret_cast<const uint4*>(p);
+  uint4 b = *reinterpret_cast<const uint4*>(p + 64);
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  uint32_t ao[4], bo[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float x1[2] = {bf_lo(aw[e]), bf_hi(aw[e])}, x2[2] = {bf_lo(bw[e]), bf_hi(bw[e])}, y1[2], y2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float cv = cs[2 * e + u], sv = sgn * cs[64 + 2 * e + u];
+      y1[u] = x1[u] * cv - x2[u] * sv;
+      y2[u] = x2[u] * cv + x1[u] * sv;
+    }
+    ao[e] = pack2(y1[0], y1[1]);
+    bo[e] = pack2(y2[0], y2[1]);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(ao[0], ao[1], ao[2], ao[3]);
+  *reinterpret_cast<uint4*>(p + 64) = make_uint4(bo[0], bo[1], bo[2], bo[3]);
+}
+
+// ------------------------------------------------------------ shared args
+struct AttnArgs {
+  int S, H, Hkv, nseq;
+  float c;        // log2(e) / sqrt(128)
+  uint16_t* out0; // fwd: o;  dq kernel: dq;  dkdv kernel: dk
+  int64_t ld0;
+  uint16_t* out1; // dkdv kernel: dv
+  int64_t ld1;
+  float* lse;     // fwd output [H][M] (natural log); bwd input
+  const float* Di;  // bwd: [H][M]
+  const float* rope;  // bwd: table [S][128] or nullptr
+  int* err;
+};
+
+// Roles of the 192-thread CTAs: warp 0 TMA producer, warp 1 MMA issuer (and
+// TMEM owner), warps 2..5 row workers (TMEM lane quarter = warp % 4).
+constexpr int kAtThreads = 192;
+
+struct FwdCfg {
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kAtTile;        // 2 stages
+  static constexpr int kOffV = kOffK + 2 * kAtTile;    // 2 stages
+  static constexpr int kOffP = kOffV + 2 * kAtTile;
+  static constexpr int kOffBar = kOffP + kAtTile;
+  static constexpr int kNumBars = 14;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffMisc + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(kAtThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + FwdCfg::kOffQ;
+  uint8_t* sK = smem + FwdCfg::kOffK;
+  uint8_t* sV = smem + FwdCfg::kOffV;
+  uint8_t* sP = smem + FwdCfg::kOffP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FwdCfg::kOffBar);
+  uint64_t* q_full = bars;        // Q landed
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2] PV of the stage done
+  uint64_t* s_full = bars + 5;    // [2] S tile in TMEM buffer b
+  uint64_t* p_full = bars + 7;    // P written (4 warp arrivals); S buffer read
+  uint64_t* o_full = bars + 8;    // [2] O_part in TMEM buffer b
+  uint64_t* o_empty = bars + 10;  // [2] O_part read (4 warp arrivals)
+  uint64_t* drain = bars + 12;    // failure path: every issued MMA completed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + FwdCfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + FwdCfg::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntq = a.S / 128;
+  const int per = a.H * a.nseq;
+  const int qt = ntq - 1 - static_cast<int>(blockIdx.x) / per;  // heaviest tiles first
+  const int hb = static_cast<int>(blockIdx.x) % per;
+  const int h = hb % a.H, b = hb / a.H;
+  const int g = h / (a.H / a.Hkv);
+  const int row0 = b * a.S + qt * 128;
+  const int kv0 = b * a.S;
+  const int n = qt + 1;  // key tiles 0..qt
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&kv_full[i], 1);
+      ptx::mbar_init(&kv_empty[i], 1);
+      ptx::mbar_init(&s_full[i], 1);
+      ptx::mbar_init(&o_full[i], 1);
+      ptx::mbar_init(&o_empty[i], 4);
+    }
+    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&map_q);
+    ptx::tma_prefetch_desc(&map_k);
+    ptx::tma_prefetch_desc(&map_v);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    report_device_error(a.err, SL_ERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      ptx::mbar_arrive_expect_tx(q_full, kAtTile);
+      ptx::tma_load_2d(sQ, &map_q, q_full, h * 128, row0);
+      ptx::tma_load_2d(sQ + kAtAtom128, &map_q, q_full, h * 128 + 64, row0);
+      for (int j = 0; j < n; ++j) {
+        const int s = j & 1;
+        if (!ptx::mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&kv_full[s], 2 * kAtTile);
+        uint8_t* k_dst = sK + s * kAtTile;
+        uint8_t* v_dst = sV + s * kAtTile;
+        ptx::tma_load_2d(k_dst, &map_k, &kv_full[s], g * 128, kv0 + j * 128);
+        ptx::tma_load_2d(k_dst + kAtAtom128, &map_k, &kv_full[s], g * 128 + 64, kv0 + j * 128);
+        ptx::tma_load_2d(v_dst, &map_v, &kv_full[s], g * 128, kv0 + j * 128);
+        ptx::tma_load_2d(v_dst + kAtAtom128, &map_v, &kv_full[s], g * 128 + 64, kv0 + j * 128);
+        ++issued;
+      }
+      // before the CTA exits every issued copy must have landed
+      ptx::mbar_wait(q_full, 0, nullptr);
+      if (!ok)
+        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+          ptx::mbar_wait(&kv_full[j & 1], (j >> 1) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t id_o = ptx::idesc_bf16(128, 128, 0, 1);
+      const uint32_t q_base = ptx::smem_addr(sQ), k_base = ptx::smem_addr(sK), v_base = ptx::smem_addr(sV),
+                     p_base = ptx::smem_addr(sP);
+      bool ok = ptx::mbar_wait(q_full, 0, abort_flag);
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        if (!ptx::mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag)) return false;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(s * 128);
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(d, kdesc(q_base, kk, kAtAtom128), kdesc(k_base + s * kAtTile, kk, kAtAtom128), id_s,
+                        kk ? 1u : 0u);
+        ptx::mma_commit(&s_full[s]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      int issued_pv = 0;
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        const int s = j & 1;
+        if (!ptx::mbar_wait(p_full, j & 1, abort_flag) ||
+            !ptx::mbar_wait(&o_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + 256u + static_cast<uint32_t>(s * 128);
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(d, kdesc(p_base, kk, kAtAtom128), mndesc(v_base + s * kAtTile, kk, kAtAtom128), id_o,
+                        kk ? 1u : 0u);
+        ptx::mma_commit(&o_full[s]);
+        ptx::mma_commit(&kv_empty[s]);
+        ++issued_pv;
+      }
+      if (!ok) {
+        give_up();
+        // let every issued MMA finish before TMEM is released
+        ptx::mma_commit(drain);
+        ptx::mbar_wait(drain, 0, nullptr);
+      }
+      (void)issued_pv;
+    }
+  } else {
+    // ------------------------------------------------------------ softmax rows
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row in the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float O[128];
+#pragma unroll
+    for (int e = 0; e < 128; ++e) O[e] = 0.0f;
+    float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, uint32_t par) {
+      bool w = ptx::mbar_wait(bar, par, abort_flag);
+      w = __all_sync(0xffffffffu, w);
+      if (!w && lane == 0 && !*abort_flag) give_up();
+      return w;
+    };
+    auto accumulate = [&](int j) {  // O = O alpha_j + O_part_j
+      const int s = j & 1;
+      if (!wait_all(&o_full[s], (j >> 1) & 1)) return false;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + c * 32), u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) O[c * 32 + e] = fmaf(O[c * 32 + e], alpha_prev, __uint_as_float(u[e]));
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&o_empty[s]);
+      return true;
+    };
+    for (int j = 0; j < n; ++j) {
+      const int s = j & 1;
+      if (!wait_all(&s_full[s], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const bool diag = (j == qt);
+      const uint32_t s_addr = lane_base + static_cast<uint32_t>(s * 128);
+      // pass 1: row max of the scaled scores
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const bool vis = !diag || (c * 32 + e <= r);
+          if (vis) mt = fmaxf(mt, __uint_as_float(u[e]) * a.c);
+        }
+      }
+      const float m_new = fmaxf(m, mt);
+      const float alpha = exp2f(m - m_new);
+      // O_part of the previous tile joins O with the previous alpha; this also
+      // frees the P tile (its MMA has completed)
+      if (j > 0 && !accumulate(j - 1)) {
+        ok = false;
+        break;
+      }
+      alpha_prev = alpha;
+      // pass 2: P = exp2(S c - m_new) as bf16 into the swizzled P tile
+      float lsum = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, u);
+        ptx::tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = exp2f(__uint_as_float(u[e]) * a.c - m_new);
+          float p1 = exp2f(__uint_as_float(u[e + 1]) * a.c - m_new);
+          if (diag && c * 32 + e > r) p0 = 0.0f;
+          if (diag && c * 32 + e + 1 > r) p1 = 0.0f;
+          lsum += p0 + p1;
+          w[e / 2] = pack2(p0, p1);
+        }
+        uint8_t* atom = sP + (c >> 1) * kAtAtom128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *swz(atom, r, (c & 1) * 4 + q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+      }
+      l = l * alpha + lsum;
+      m = m_new;
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(p_full);
+    }
+    if (ok && accumulate(n - 1)) {
+      const float inv = 1.0f / l;
+      uint16_t* dst = a.out0 + static_cast<int64_t>(row0 + r) * a.ld0 + h * 128;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        reinterpret_cast<uint4*>(dst)[c] =
+            make_uint4(pack2(O[8 * c] * inv, O[8 * c + 1] * inv), pack2(O[8 * c + 2] * inv, O[8 * c + 3] * inv),
+                       pack2(O[8 * c + 4] * inv, O[8 * c + 5] * inv), pack2(O[8 * c + 6] * inv, O[8 * c + 7] * inv));
+      const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
+      a.lse[static_cast<int64_t>(h) * M + row0 + r] = (m + log2f(l)) * 0.69314718055994531f;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------ Di pre-pass
+// Di[h][row] = sum_d dO[row, h*128 + d] * O[row, h*128 + d]; one warp per (row, head).
+__global__ void attn_di_kernel(const uint16_t* __restrict__ o, int64_t ldo, const uint16_t* __restrict__ dout,
+                               int64_t lddo, int64_t M, int H, float* __restrict__ Di) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= M * H) return;
+  const int64_t row = w / H;
+  const int h = static_cast<int>(w % H);
+  const uint2 ov = *reinterpret_cast<const uint2*>(o + row * ldo + h * 128 + lane * 4);
+  const uint2 dv = *reinterpret_cast<const uint2*>(dout + row * lddo + h * 128 + lane * 4);
+  float s = bf_lo(ov.x) * bf_lo(dv.x) + bf_hi(ov.x) * bf_hi(dv.x) + bf_lo(ov.y) * bf_lo(dv.y) +
+            bf_hi(ov.y) * bf_hi(dv.y);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) Di[static_cast<int64_t>(h) * M + row] = s;
+}
+
+// Scale by 1/sqrt(128), rotate back by the inverse angle of position `pos`
+// (table may be null), round to bf16 and store one 128-wide row.
+__device__ __forceinline__ void store_grad_row(const float* v, float scale, const float* table, int pos,
+                                               uint16_t* dst) {
+  float y[128];
+#pragma unroll
+  for (int e = 0; e < 128; ++e) y[e] = v[e] * scale;
+  if (table) {
+    const float* cs = table + static_cast<int64_t>(pos) * 128;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float cv = cs[i], sv = cs[64 + i];
+      const float x1 = y[i], x2 = y[64 + i];
+      y[i] = x1 * cv + x2 * sv;
+      y[64 + i] = x2 * cv - x1 * sv;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    reinterpret_cast<uint4*>(dst)[c] = make_uint4(pack2(y[8 * c], y[8 * c + 1]), pack2(y[8 * c + 2], y[8 * c + 3]),
+                                                  pack2(y[8 * c + 4], y[8 * c + 5]), pack2(y[8 * c + 6], y[8 * c + 7]));
+}
+
+// ------------------------------------------------------------ dQ
+struct DqCfg {
+  static constexpr int kOffQ = 0;                      // [128][128]
+  static constexpr int kOffDO = kOffQ + kAtTile;       // [128][128]
+  static constexpr int kOffK = kOffDO + kAtTile;       // 2 stages of [64][128]
+  static constexpr int kOffV = kOffK + 2 * 2 * kAtAtom64;
+  static constexpr int kOffDS = kOffV + 2 * 2 * kAtAtom64;  // [128][64]
+  static constexpr int kOffBar = kOffDS + kAtAtom128;
+  static constexpr int kNumBars = 14;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffMisc + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(kAtThreads, 1)
+    attn_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                   const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + DqCfg::kOffQ;
+  uint8_t* sDO = smem + DqCfg::kOffDO;
+  uint8_t* sK = smem + DqCfg::kOffK;
+  uint8_t* sV = smem + DqCfg::kOffV;
+  uint8_t* sDS = smem + DqCfg::kOffDS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DqCfg::kOffBar);
+  uint64_t* q_full = bars;         // Q and dO landed
+  uint64_t* kv_full = bars + 1;    // [2]
+  uint64_t* kv_empty = bars + 3;   // [2]
+  uint64_t* sp_full = bars + 5;    // [2] S and dP in TMEM buffer b
+  uint64_t* ds_full = bars + 7;    // dS written (4 arrivals); S/dP buffer read
+  uint64_t* ds_empty = bars + 8;   // dQ MMA of dS done
+  uint64_t* acc_full = bars + 9;   // dQ complete
+  uint64_t* drain = bars + 10;     // failure path: every issued MMA completed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DqCfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DqCfg::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntq = a.S / 128;
+  const int per = a.H * a.nseq;
+  const int qt = ntq - 1 - static_cast<int>(blockIdx.x) / per;
+  const int hb = static_cast<int>(blockIdx.x) % per;
+  const int h = hb % a.H, b = hb / a.H;
+  const int g = h / (a.H / a.Hkv);
+  const int row0 = b * a.S + qt * 128;
+  const int kv0 = b * a.S;
+  const int n = 2 * (qt + 1);  // key blocks of 64
+  const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&kv_full[i], 1);
+      ptx::mbar_init(&kv_empty[i], 1);
+      ptx::mbar_init(&sp_full[i], 1);
+    }
+    ptx::mbar_init(ds_full, 4);
+    ptx::mbar_init(ds_empty, 1);
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // TMEM: S buffers at 0 / 64, dP at 128 / 192, dQ at 256
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    report_device_error(a.err, SL_ERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      ptx::mbar_arrive_expect_tx(q_full, 2 * kAtTile);
+      ptx::tma_load_2d(sQ, &map_q, q_full, h * 128, row0);
+      ptx::tma_load_2d(sQ + kAtAtom128, &map_q, q_full, h * 128 + 64, row0);
+      ptx::tma_load_2d(sDO, &map_do, q_full, h * 128, row0);
+      ptx::tma_load_2d(sDO + kAtAtom128, &map_do, q_full, h * 128 + 64, row0);
+      for (int j = 0; j < n; ++j) {
+        const int s = j & 1;
+        if (!ptx::mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&kv_full[s], 4 * kAtAtom64);
+        uint8_t* k_dst = sK + s * 2 * kAtAtom64;
+        uint8_t* v_dst = sV + s * 2 * kAtAtom64;
+        ptx::tma_load_2d(k_dst, &map_k, &kv_full[s], g * 128, kv0 + j * 64);
+        ptx::tma_load_2d(k_dst + kAtAtom64, &map_k, &kv_full[s], g * 128 + 64, kv0 + j * 64);
+        ptx::tma_load_2d(v_dst, &map_v, &kv_full[s], g * 128, kv0 + j * 64);
+        ptx::tma_load_2d(v_dst + kAtAtom64, &map_v, &kv_full[s], g * 128 + 64, kv0 + j * 64);
+        ++issued;
+      }
+      ptx::mbar_wait(q_full, 0, nullptr);
+      if (!ok)
+        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+          ptx::mbar_wait(&kv_full[j & 1], (j >> 1) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = ptx::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t id_q = ptx::idesc_bf16(128, 128, 0, 1);
+      const uint32_t q_base = ptx::smem_addr(sQ), do_base = ptx::smem_addr(sDO), k_base = ptx::smem_addr(sK),
+                     v_base = ptx::smem_addr(sV), ds_base = ptx::smem_addr(sDS);
+      bool ok = ptx::mbar_wait(q_full, 0, abort_flag);
+      auto issue_sp = [&](int j) {
+        const int s = j & 1;
+        if (!ptx::mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag)) return false;
+        ptx::tc_fence_after();
+        const uint32_t kb = k_base + s * 2 * kAtAtom64, vb = v_base + s * 2 * kAtAtom64;
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tmem + static_cast<uint32_t>(s * 64), kdesc(q_base, kk, kAtAtom128), kdesc(kb, kk, kAtAtom64),
+                        id_s, kk ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(s * 64), kdesc(do_base, kk, kAtAtom128),
+                        kdesc(vb, kk, kAtAtom64), id_s, kk ? 1u : 0u);
+        ptx::mma_commit(&sp_full[s]);
+        return true;
+      };
+      if (ok) ok = issue_sp(0);
+      int done = 0;
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n && !issue_sp(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!ptx::mbar_wait(ds_full, j & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t kb = k_base + (j & 1) * 2 * kAtAtom64;
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_bf16(tmem + 256u, kdesc(ds_base, kk, kAtAtom128), mndesc(kb, kk, kAtAtom64), id_q,
+                        (j | kk) ? 1u : 0u);
+        ptx::mma_commit(ds_empty);
+        ptx::mma_commit(&kv_empty[j & 1]);
+        ++done;
+      }
+      if (ok) {
+        ptx::mma_commit(acc_full);
+      } else {
+        give_up();
+        ptx::mma_commit(drain);
+        ptx::mbar_wait(drain, 0, nullptr);
+      }
+      (void)done;
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qrow = qt * 128 + r;  // position in the sequence
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float lse2 = a.lse[static_cast<int64_t>(h) * M + row0 + r] * kLog2e;
+    const float di = a.Di[static_cast<int64_t>(h) * M + row0 + r];
+    auto wait_all = [&](uint64_t* bar, uint32_t par) {
+      bool w = ptx::mbar_wait(bar, par, abort_flag);
+      w = __all_sync(0xffffffffu, w);
+      if (!w && lane == 0 && !*abort_flag) give_up();
+      return w;
+    };
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int s = j & 1;
+      if (!wait_all(&sp_full[s], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t w[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t us[32], up[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + c * 32), us);
+        ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + c * 32), up);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float ds2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int key = j * 64 + c * 32 + e + u;
+            const float p = key <= qrow ? exp2f(__uint_as_float(us[e + u]) * a.c - lse2) : 0.0f;
+            ds2[u] = p * (__uint_as_float(up[e + u]) - di);
+          }
+          w[c * 16 + e / 2] = pack2(ds2[0], ds2[1]);
+        }
+      }
+      // the previous dS must have been consumed by its MMA
+      if (j > 0 && !wait_all(ds_empty, (j - 1) & 1)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8)
+        *swz(sDS, r, q8) = make_uint4(w[4 * q8], w[4 * q8 + 1], w[4 * q8 + 2], w[4 * q8 + 3]);
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ds_full);
+    }
+    if (ok && wait_all(acc_full, 0)) {
+      ptx::tc_fence_after();
+      float v[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(c * 32), u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[c * 32 + e] = __uint_as_float(u[e]);
+      }
+      store_grad_row(v, 0.08838834764831845f, a.rope, qrow, a.out0 + static_cast<int64_t>(row0 + r) * a.ld0 + h * 128);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------ dK, dV
+struct DkvCfg {
+  static constexpr int kOffK = 0;                    // [128][128]
+  static constexpr int kOffV = kOffK + kAtTile;      // [128][128]
+  static constexpr int kStageBytes = 4 * kAtAtom64 + 512;  // Q [64][128], dO [64][128], lse and Di of 64 rows
+  static constexpr int kStage = 4 * kAtAtom64 + 1024;      // stage stride (1024-aligned for the swizzled tiles)
+  static constexpr int kOffStage = kOffV + kAtTile;  // 2 stages
+  static constexpr int kOffPT = kOffStage + 2 * kStage;  // [128][64]
+  static constexpr int kOffDST = kOffPT + kAtAtom128;    // [128][64]
+  static constexpr int kOffBar = kOffDST + kAtAtom128;
+  static constexpr int kNumBars = 14;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffMisc + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(kAtThreads, 1)
+    attn_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                     const __grid_constant__ CUtensorMap map_lse, const __grid_constant__ CUtensorMap map_di,
+                     const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + DkvCfg::kOffK;
+  uint8_t* sV = smem + DkvCfg::kOffV;
+  uint8_t* sStage = smem + DkvCfg::kOffStage;
+  uint8_t* sPT = smem + DkvCfg::kOffPT;
+  uint8_t* sDST = smem + DkvCfg::kOffDST;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DkvCfg::kOffBar);
+  uint64_t* kv_full = bars;        // K and V landed
+  uint64_t* st_full = bars + 1;    // [2]
+  uint64_t* st_empty = bars + 3;   // [2]
+  uint64_t* sp_full = bars + 5;    // [2] S^T and dP^T in TMEM buffer b
+  uint64_t* ds_full = bars + 7;    // P^T and dS^T written (4 arrivals)
+  uint64_t* ds_empty = bars + 8;   // their MMAs done
+  uint64_t* acc_full = bars + 9;   // dK, dV complete
+  uint64_t* drain = bars + 10;     // failure path: every issued MMA completed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DkvCfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DkvCfg::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = a.Hkv * a.nseq;
+  const int kt = static_cast<int>(blockIdx.x) / per;  // key tile; heaviest (kt = 0) first
+  const int gb = static_cast<int>(blockIdx.x) % per;
+  const int g = gb % a.Hkv, b = gb / a.Hkv;
+  const int rep = a.H / a.Hkv;
+  const int key0 = b * a.S + kt * 128;
+  const int nqb = a.S / 64 - 2 * kt;  // query blocks of 64 that see this key tile
+  const int n = rep * nqb;            // iterations: (query head, query block)
+  auto it_head = [&](int t) { return g * rep + t / nqb; };
+  auto it_qb = [&](int t) { return 2 * kt + t % nqb; };
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&st_full[i], 1);
+      ptx::mbar_init(&st_empty[i], 1);
+      ptx::mbar_init(&sp_full[i], 1);
+    }
+    ptx::mbar_init(ds_full, 4);
+    ptx::mbar_init(ds_empty, 1);
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // TMEM: S^T buffers at 0 / 64, dP^T at 128 / 192, dV at 256, dK at 384
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    report_device_error(a.err, SL_ERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      ptx::mbar_arrive_expect_tx(kv_full, 2 * kAtTile);
+      ptx::tma_load_2d(sK, &map_k, kv_full, g * 128, key0);
+      ptx::tma_load_2d(sK + kAtAtom128, &map_k, kv_full, g * 128 + 64, key0);
+      ptx::tma_load_2d(sV, &map_v, kv_full, g * 128, key0);
+      ptx::tma_load_2d(sV + kAtAtom128, &map_v, kv_full, g * 128 + 64, key0);
+      for (int t = 0; t < n; ++t) {
+        const int s = t & 1;
+        if (!ptx::mbar_wait(&st_empty[s], ((t >> 1) & 1) ^ 1, abort_flag)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        const int h = it_head(t), qrow = b * a.S + it_qb(t) * 64;
+        uint8_t* st = sStage + s * DkvCfg::kStage;
+        ptx::mbar_arrive_expect_tx(&st_full[s], DkvCfg::kStageBytes);
+        ptx::tma_load_2d(st, &map_q, &st_full[s], h * 128, qrow);
+        ptx::tma_load_2d(st + kAtAtom64, &map_q, &st_full[s], h * 128 + 64, qrow);
+        ptx::tma_load_2d(st + 2 * kAtAtom64, &map_do, &st_full[s], h * 128, qrow);
+        ptx::tma_load_2d(st + 3 * kAtAtom64, &map_do, &st_full[s], h * 128 + 64, qrow);
+        ptx::tma_load_2d(st + 4 * kAtAtom64, &map_lse, &st_full[s], qrow, h);
+        ptx::tma_load_2d(st + 4 * kAtAtom64 + 256, &map_di, &st_full[s], qrow, h);
+        ++issued;
+      }
+      ptx::mbar_wait(kv_full, 0, nullptr);
+      if (!ok)
+        for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t)
+          ptx::mbar_wait(&st_full[t & 1], (t >> 1) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = ptx::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t id_g = ptx::idesc_bf16(128, 128, 0, 1);
+      const uint32_t k_base = ptx::smem_addr(sK), v_base = ptx::smem_addr(sV), st_base = ptx::smem_addr(sStage),
+                     pt_base = ptx::smem_addr(sPT), dst_base = ptx::smem_addr(sDST);
+      bool ok = ptx::mbar_wait(kv_full, 0, abort_flag);
+      auto issue_sp = [&](int t) {
+        const int s = t & 1;
+        if (!ptx::mbar_wait(&st_full[s], (t >> 1) & 1, abort_flag)) return false;
+        ptx::tc_fence_after();
+        const uint32_t qb = st_base + s * DkvCfg::kStage, dob = qb + 2 * kAtAtom64;
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tmem + static_cast<uint32_t>(s * 64), kdesc(k_base, kk, kAtAtom128), kdesc(qb, kk, kAtAtom64),
+                        id_s, kk ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(s * 64), kdesc(v_base, kk, kAtAtom128),
+                        kdesc(dob, kk, kAtAtom64), id_s, kk ? 1u : 0u);
+        ptx::mma_commit(&sp_full[s]);
+        return true;
+      };
+      if (ok && n > 0) ok = issue_sp(0);
+      int done = 0;
+      for (int t = 0; ok && t < n; ++t) {
+        if (t + 1 < n && !issue_sp(t + 1)) {
+          ok = false;
+          break;
+        }
+        if (!ptx::mbar_wait(ds_full, t & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t qb = st_base + (t & 1) * DkvCfg::kStage, dob = qb + 2 * kAtAtom64;
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_bf16(tmem + 256u, kdesc(pt_base, kk, kAtAtom128), mndesc(dob, kk, kAtAtom64), id_g,
+                        (t | kk) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_bf16(tmem + 384u, kdesc(dst_base, kk, kAtAtom128), mndesc(qb, kk, kAtAtom64), id_g,
+                        (t | kk) ? 1u : 0u);
+        ptx::mma_commit(ds_empty);
+        ptx::mma_commit(&st_empty[t & 1]);
+        ++done;
+      }
+      if (ok) {
+        ptx::mma_commit(acc_full);
+      } else {
+        give_up();
+        ptx::mma_commit(drain);
+        ptx::mbar_wait(drain, 0, nullptr);
+      }
+      (void)done;
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // key row in the tile
+    const int kpos = kt * 128 + r;      // key position in the sequence
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    auto wait_all = [&](uint64_t* bar, uint32_t par) {
+      bool w = ptx::mbar_wait(bar, par, abort_flag);
+      w = __all_sync(0xffffffffu, w);
+      if (!w && lane == 0 && !*abort_flag) give_up();
+      return w;
+    };
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const int s = t & 1;
+      if (!wait_all(&sp_full[s], (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const float* lse_s = reinterpret_cast<const float*>(sStage + s * DkvCfg::kStage + 4 * kAtAtom64);
+      const float* di_s = lse_s + 64;
+      const int q0 = it_qb(t) * 64;
+      uint32_t wp[32], wd[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t us[32], up[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + c * 32), us);
+        ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + c * 32), up);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p2[2], d2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qi = c * 32 + e + u;
+            const float p =
+                (q0 + qi >= kpos) ? exp2f(__uint_as_float(us[e + u]) * a.c - lse_s[qi] * kLog2e) : 0.0f;
+            p2[u] = p;
+            d2[u] = p * (__uint_as_float(up[e + u]) - di_s[qi]);
+          }
+          wp[c * 16 + e / 2] = pack2(p2[0], p2[1]);
+          wd[c * 16 + e / 2] = pack2(d2[0], d2[1]);
+        }
+      }
+      if (t > 0 && !wait_all(ds_empty, (t - 1) & 1)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        *swz(sPT, r, q8) = make_uint4(wp[4 * q8], wp[4 * q8 + 1], wp[4 * q8 + 2], wp[4 * q8 + 3]);
+        *swz(sDST, r, q8) = make_uint4(wd[4 * q8], wd[4 * q8 + 1], wd[4 * q8 + 2], wd[4 * q8 + 3]);
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ds_full);
+    }
+    if (ok && n > 0 && wait_all(acc_full, 0)) {
+      ptx::tc_fence_after();
+      float v[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(c * 32), u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[c * 32 + e] = __uint_as_float(u[e]);
+      }
+      store_grad_row(v, 1.0f, nullptr, 0, a.out1 + static_cast<int64_t>(key0 + r) * a.ld1 + g * 128);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(c * 32), u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[c * 32 + e] = __uint_as_float(u[e]);
+      }
+      store_grad_row(v, 0.08838834764831845f, a.rope, kpos, a.out0 + static_cast<int64_t>(key0 + r) * a.ld0 + g * 128);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------ host side
+sl_status check_shape(const AttnShape& sh) {
+  SL_REQUIRE(sh.M > 0 && sh.S > 0 && sh.S % 128 == 0 && sh.M % sh.S == 0,
+             "attention: need S a positive multiple of 128 and M a multiple of S");
+  SL_REQUIRE(sh.H > 0 && sh.Hkv > 0 && sh.H % sh.Hkv == 0, "attention: need H a multiple of Hkv");
+  SL_REQUIRE(sh.M < (1LL << 31) && static_cast<int64_t>(sh.H) * sh.M < (1LL << 31), "attention: M too large");
+  return SL_OK;
+}
+
+sl_status map_rows(CUtensorMap* m, const uint16_t* base, int64_t cols, int64_t rows, int64_t ld, int box_rows) {
+  SL_REQUIRE(base, "attention: null operand");
+  SL_REQUIRE(ld >= cols && (ld * 2) % 16 == 0, "attention: row stride must cover the row and be a multiple of 8");
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                  static_cast<uint64_t>(ld) * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <typename K>
+sl_status set_smem(K kern, int bytes) {
+  static bool done[64] = {false};
+  int dev = 0;
+  SL_CHECK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64 || !done[dev]) {
+    SL_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    if (dev >= 0 && dev < 64) done[dev] = true;
+  }
+  return SL_OK;
+}
+
+}  // namespace
+
+sl_status rope_table(int64_t S, double theta, float* table, cudaStream_t stream) {
+  SL_REQUIRE(S > 0 && table && theta > 1.0, "rope table: need S > 0, theta > 1 and a table");
+  const int64_t n = S * 64;
+  rope_table_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(S, theta, table);
+  return check_launch("rope_table_kernel");
+}
+
+sl_status rope_apply(uint16_t* x, int64_t ld, int64_t M, int nheads, int64_t S, const float* table, int inverse,
+                     cudaStream_t stream) {
+  SL_REQUIRE(x && table && M > 0 && nheads > 0 && S > 0 && ld >= nheads * 128 && ld % 8 == 0,
+             "rope: bad arguments");
+  SL_REQUIRE((reinterpret_cast<uintptr_t>(x) & 15) == 0, "rope: x must be 16-byte aligned");
+  const int64_t n = M * nheads * 8;
+  rope_apply_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(x, ld, M, nheads, S, table,
+                                                                                inverse ? -1.0f : 1.0f);
+  return check_launch("rope_apply_kernel");
+}
+
+sl_status attention_fwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, const uint16_t* k, int64_t ldk,
+                        const uint16_t* v, int64_t ldv, uint16_t* o, int64_t ldo, float* lse, cudaStream_t stream) {
+  sl_status st = check_shape(sh);
+  if (st != SL_OK) return st;
+  SL_REQUIRE(o && lse && ldo >= sh.H * 128 && ldo % 8 == 0 && (reinterpret_cast<uintptr_t>(o) & 15) == 0,
+             "attention_fwd: bad output");
+  CUtensorMap mq, mk, mv;
+  if ((st = map_rows(&mq, q, sh.H * 128, sh.M, ldq, 128)) != SL_OK) return st;
+  if ((st = map_rows(&mk, k, sh.Hkv * 128, sh.M, ldk, 128)) != SL_OK) return st;
+  if ((st = map_rows(&mv, v, sh.Hkv * 128, sh.M, ldv, 128)) != SL_OK) return st;
+  int* err = device_error_word();
+  if (!err) return SL_ERR_CUDA;
+  AttnArgs a{};
+  a.S = static_cast<int>(sh.S);
+  a.H = sh.H;
+  a.Hkv = sh.Hkv;
+  a.nseq = static_cast<int>(sh.M / sh.S);
+  a.c = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  a.out0 = o;
+  a.ld0 = ldo;
+  a.lse = lse;
+  a.err = err;
+  if ((st = set_smem(attn_fwd_kernel, FwdCfg::kSmem)) != SL_OK) return st;
+  const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.H * a.nseq);
+  attn_fwd_kernel<<<grid, kAtThreads, FwdCfg::kSmem, stream>>>(mq, mk, mv, a);
+  return check_launch("attn_fwd_kernel");
+}
+
+size_t attention_ws_bytes(int64_t M, int H) { return static_cast<size_t>(M) * H * 4; }
+
+sl_status attention_bwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, const uint16_t* k, int64_t ldk,
+                        const uint16_t* v, int64_t ldv, const uint16_t* o, int64_t ldo, const uint16_t* dout,
+                        int64_t lddo, const float* lse, uint16_t* dq, int64_t lddq, uint16_t* dk, int64_t lddk,
+                        uint16_t* dv, int64_t lddv, const float* rope, void* ws, cudaStream_t stream) {
+  sl_status st = check_shape(sh);
+  if (st != SL_OK) return st;
+  SL_REQUIRE(o && dout && lse && ws && dq && dk && dv, "attention_bwd: null argument");
+  SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 15) == 0 && (reinterpret_cast<uintptr_t>(lse) & 15) == 0,
+             "attention_bwd: lse and workspace must be 16-byte aligned");
+  SL_REQUIRE(ldo % 4 == 0 && lddo % 4 == 0 && (reinterpret_cast<uintptr_t>(o) & 7) == 0 &&
+                 (reinterpret_cast<uintptr_t>(dout) & 7) == 0,
+             "attention_bwd: o and do rows must be 8-byte aligned");
+  for (auto pr : {std::make_pair(static_cast<const void*>(dq), lddq), std::make_pair(static_cast<const void*>(dk), lddk),
+                  std::make_pair(static_cast<const void*>(dv), lddv)})
+    SL_REQUIRE((reinterpret_cast<uintptr_t>(pr.first) & 15) == 0 && pr.second % 8 == 0,
+               "attention_bwd: gradient outputs must be 16-byte aligned with row strides a multiple of 8");
+  SL_REQUIRE(lddq >= sh.H * 128 && lddk >= sh.Hkv * 128 && lddv >= sh.Hkv * 128, "attention_bwd: row strides");
+  int* err = device_error_word();
+  if (!err) return SL_ERR_CUDA;
+  float* Di = static_cast<float*>(ws);
+  {
+    const int64_t warps = sh.M * sh.H;
+    attn_di_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, stream>>>(o, ldo, dout, lddo, sh.M,
+                                                                                        sh.H, Di);
+    if ((st = check_launch("attn_di_kernel")) != SL_OK) return st;
+  }
+  AttnArgs a{};
+  a.S = static_cast<int>(sh.S);
+  a.H = sh.H;
+  a.Hkv = sh.Hkv;
+  a.nseq = static_cast<int>(sh.M / sh.S);
+  a.c = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  a.lse = const_cast<float*>(lse);
+  a.Di = Di;
+  a.rope = rope;
+  a.err = err;
+  // dQ
+  {
+    CUtensorMap mq, mdo, mk, mv;
+    if ((st = map_rows(&mq, q, sh.H * 128, sh.M, ldq, 128)) != SL_OK) return st;
+    if ((st = map_rows(&mdo, dout, sh.H * 128, sh.M, lddo, 128)) != SL_OK) return st;
+    if ((st = map_rows(&mk, k, sh.Hkv * 128, sh.M, ldk, 64)) != SL_OK) return st;
+    if ((st = map_rows(&mv, v, sh.Hkv * 128, sh.M, ldv, 64)) != SL_OK) return st;
+    AttnArgs ad = a;
+    ad.out0 = dq;
+    ad.ld0 = lddq;
+    if ((st = set_smem(attn_dq_kernel, DqCfg::kSmem)) != SL_OK) return st;
+    const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.H * a.nseq);
+    attn_dq_kernel<<<grid, kAtThreads, DqCfg::kSmem, stream>>>(mq, mdo, mk, mv, ad);
+    if ((st = check_launch("attn_dq_kernel")) != SL_OK) return st;
+  }
+  // dK, dV
+  {
+    CUtensorMap mq, mdo, mk, mv, ml, md;
+    if ((st = map_rows(&mq, q, sh.H * 128, sh.M, ldq, 64)) != SL_OK) return st;
+    if ((st = map_rows(&mdo, dout, sh.H * 128, sh.M, lddo, 64)) != SL_OK) return st;
+    if ((st = map_rows(&mk, k, sh.Hkv * 128, sh.M, ldk, 128)) != SL_OK) return st;
+    if ((st = map_rows(&mv, v, sh.Hkv * 128, sh.M, ldv, 128)) != SL_OK) return st;
+    if ((st = make_map(&ml, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, lse, static_cast<uint64_t>(sh.M),
+                       static_cast<uint64_t>(sh.H), static_cast<uint64_t>(sh.M) * 4, 64, 1,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != SL_OK)
+      return st;
+    if ((st = make_map(&md, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Di, static_cast<uint64_t>(sh.M),
+                       static_cast<uint64_t>(sh.H), static_cast<uint64_t>(sh.M) * 4, 64, 1,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != SL_OK)
+      return st;
+    AttnArgs ak = a;
+    ak.out0 = dk;
+    ak.ld0 = lddk;
+    ak.out1 = dv;
+    ak.ld1 = lddv;
+    if ((st = set_smem(attn_dkdv_kernel, DkvCfg::kSmem)) != SL_OK) return st;
+    const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.Hkv * a.nseq);
+    attn_dkdv_kernel<<<grid, kAtThreads, DkvCfg::kSmem, stream>>>(mq, mdo, mk, mv, ml, md, ak);
+    if ((st = check_launch("attn_dkdv_kernel")) != SL_OK) return st;
+  }
+  return SL_OK;
+}
+
+}  // namespace sl
+
+// ------------------------------------------------------------------ C ABI
+using namespace sl;
+
+extern "C" sl_status sl_rope_table(int64_t S, double theta, float* table, cudaStream_t stream) {
+  return rope_table(S, theta, table, stream);
+}
+
+extern "C" sl_status sl_rope_apply(void* x, int64_t ld, int64_t M, int32_t nheads, int64_t S, const float* table,
+                                   int32_t inverse, cudaStream_t stream) {
+  return rope_apply(static_cast<uint16_t*>(x), ld, M, nheads, S, table, inverse, stream);
+}
+
+extern "C" sl_status sl_attention_fwd(const void* q, int64_t ldq, const void* k, int64_t ldk, const void* v,
+                                      int64_t ldv, int64_t M, int64_t S, int32_t H, int32_t Hkv, void* o,
+                                      int64_t ldo, float* lse, cudaStream_t stream) {
+  const AttnShape sh{M, S, H, Hkv};
+  return attention_fwd(sh, static_cast<const uint16_t*>(q), ldq, static_cast<const uint16_t*>(k), ldk,
+                       static_cast<const uint16_t*>(v), ldv, static_cast<uint16_t*>(o), ldo, lse, stream);
+}
+
+extern "C" size_t sl_attention_workspace_size(int64_t M, int32_t H) {
+  return M > 0 && H > 0 ? attention_ws_bytes(M, H) : 0;
+}
+
+extern "C" sl_status sl_attention_bwd(const void* q, int64_t ldq, const void* k, int64_t ldk, const void* v,
+                                      int64_t ldv, const void* o, int64_t ldo, const void* dO, int64_t lddo,
+                                      const float* lse, int64_t M, int64_t S, int32_t H, int32_t Hkv, void* dq,
+                                      int64_t lddq, void* dk, int64_t lddk, void* dv, int64_t lddv,
+                                      const float* rope_table_or_null, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream) {
+  const AttnShape sh{M, S, H, Hkv};
+  SL_REQUIRE(M > 0 && H > 0 && ws_bytes >= attention_ws_bytes(M, H), "sl_attention_bwd: workspace too small");
+  return attention_bwd(sh, static_cast<const uint16_t*>(q), ldq, static_cast<const uint16_t*>(k), ldk,
+                       static_cast<const uint16_t*>(v), ldv, static_cast<const uint16_t*>(o), ldo,
+                       static_cast<const uint16_t*>(dO), lddo, lse, static_cast<uint16_t*>(dq), lddq,
+                       static_cast<uint16_t*>(dk), lddk, static_cast<uint16_t*>(dv), lddv, rope_table_or_null, ws,
+                       stream);
+}
