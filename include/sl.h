@@ -284,9 +284,12 @@ size_t sl_lora_group_workspace_size(int64_t M, int32_t G, int32_t r);
  * input) its qabsmax int8 [K/64, N_group] and its absmax2 fp32
  * [K/64, round_up(2 N_group / 256, 4)] (sl_nf4_double_quantize of the
  * group's fp32 absmax, rows of its projections in order); offsets[2p+1] is
- * the qabsmax array of projection p's group.  Needs Dkv % 256 == 0. */
+ * the qabsmax array of projection p's group.  Needs Dkv % 256 == 0.
+ * Every kind ends with the layer's two RMS-norm weights, fp32 [D] each:
+ * offsets[14] (before the attention / mixing step) and offsets[15] (before
+ * the MLP); all ones reproduce the unweighted norm exactly. */
 sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F,
-                               size_t offsets[14], size_t* blob_bytes);
+                               size_t offsets[16], size_t* blob_bytes);
 
 /* The double-quantised absmax of an NF4_DQ layer blob, per projection p:
  * its group's qabsmax at byte q_off[p] (rows of q_ld[p] bytes), absmax2 at
@@ -296,12 +299,17 @@ sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F,
 sl_status sl_stack_dq_layout(int64_t D, int64_t Dkv, int64_t F, size_t q_off[7], int64_t q_ld[7],
                              size_t a2_off[7], int64_t a2_ld[7], int64_t col0[7]);
 
+typedef enum { SL_MIX_TOKEN_LOCAL = 0, SL_MIX_ATTENTION = 1 } sl_mixer;
+
 typedef struct {
   int32_t L;                        /* number of layers */
   int32_t kind;                     /* SL_WEIGHT_NF4, SL_WEIGHT_NF4_DQ (M > 128 only) or SL_WEIGHT_BF16 */
   int64_t D, Dkv, F;                /* hidden, kv width (multiple of 128), MLP width */
   const void* const* host_blobs;    /* L pointers to PINNED host blobs (sl_stack_blob_layout) */
   const void* const* device_blobs;  /* L device copies for SL_MODE_RESIDENT, or NULL */
+  int32_t mixer;                    /* SL_MIX_TOKEN_LOCAL (0) or SL_MIX_ATTENTION */
+  int64_t seq_len;                  /* attention: tokens per sequence (multiple of 128; M % seq_len == 0) */
+  double rope_theta;                /* attention: rotary base (500000 for Llama-3.1) */
 } sl_stack_desc;
 
 typedef struct sl_stack sl_stack;
@@ -333,9 +341,12 @@ size_t sl_stack_workspace_size(const sl_stack* s, int64_t M, int32_t r);
  *  (A, B, dA, dB may then be NULL) runs the frozen base alone, the
  *  adapters-off reference pass ("Soup CLI ...", "Key Takeaways": preference
  *  training with the streamed base and adapters off).
- * The layer is the pre-norm decoder layer with token-local mixing described
- * in the library's design notes (RMS norm without weight, a = q*rep(k) +
- * rep(v), SiLU-gated MLP, fp32 residual stream, bf16 GEMM inputs/outputs).
+ * The layer is a pre-norm decoder layer: weighted RMS norm (weights in the
+ * blob), q/k/v, the mixing step, o, weighted RMS norm, SiLU-gated MLP, fp32
+ * residual stream, bf16 GEMM inputs/outputs.  Mixing: SL_MIX_ATTENTION is
+ * causal grouped-query attention with rotary positions (sl_attention_fwd:
+ * q and k rotated in place, the saved q/k are the rotated ones);
+ * SL_MIX_TOKEN_LOCAL is a = q*rep(k) + rep(v).
  * SL_MODE_STREAMED: layer l is copied from its pinned host blob into device
  * buffer l % 2 on the handle's copy stream; CUDA events order each copy
  * after the last kernel that read the buffer and each layer's kernels after
@@ -348,6 +359,24 @@ sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64
                                const void* const* B, int32_t r, float alpha,
                                float* hL, float* dh0, float* const* dA, float* const* dB,
                                int32_t accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* One complete supervised fine-tuning step on top of the stack:
+ * h0 = embed[tokens] (embed [V, D] bf16, tokens [M] int32; a token outside
+ * [0, V) gives a zero row and SL_ERR_INVALID in the device error word), the
+ * stack forward, x = bf16(RMS(hL) * norm_final) (norm_final fp32 [D] or
+ * NULL), the mean cross-entropy of x against W_head [V, D] bf16 with
+ * labels [M] int32 (-100 ignored; sl_ce_fwd_bwd, vocab chunks of chunk_V)
+ * into *loss (one fp32 on the device), its gradient back through the final
+ * norm, and the stack backward into dA, dB as sl_stream_stack_step.  The
+ * embedding and the head stay on the device; the layers stream as in
+ * sl_stream_stack_step.  `ws`: sl_sft_workspace_size bytes, 256-byte
+ * aligned. */
+sl_status sl_sft_step(sl_stack* s, int32_t mode, const int32_t* tokens, const int32_t* labels, int64_t M,
+                      const void* embed, int64_t V, const float* norm_final, const void* W_head, int64_t chunk_V,
+                      const void* const* A, const void* const* B, int32_t r, float alpha, float* loss,
+                      float* const* dA, float* const* dB, int32_t accumulate, void* ws, size_t ws_bytes,
+                      cudaStream_t stream);
+size_t sl_sft_workspace_size(const sl_stack* s, int64_t M, int32_t r, int64_t V, int64_t chunk_V);
 
 /* Host-side counters of the last step on this handle: bytes copied host to
  * device and the number of libsl kernels launched. */

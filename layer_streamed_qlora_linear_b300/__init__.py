@@ -20,6 +20,7 @@ SL_OK, SL_ERR_INVALID, SL_ERR_CUDA, SL_ERR_UNSUPPORTED, SL_ERR_TIMEOUT, SL_ERR_N
 SL_DTYPE_BF16, SL_DTYPE_F32 = 0, 1
 SL_WEIGHT_NF4, SL_WEIGHT_BF16, SL_WEIGHT_NF4_DQ = 0, 1, 2
 SL_MODE_STREAMED, SL_MODE_RESIDENT = 0, 1
+SL_MIX_TOKEN_LOCAL, SL_MIX_ATTENTION = 0, 1
 STATUS_NAMES = {0: "SL_OK", 1: "SL_ERR_INVALID", 2: "SL_ERR_CUDA", 3: "SL_ERR_UNSUPPORTED",
                 4: "SL_ERR_TIMEOUT", 5: "SL_ERR_NONFINITE", 6: "SL_ERR_OOM"}
 
@@ -41,7 +42,8 @@ class sl_stack_desc(ctypes.Structure):
     _fields_ = [("L", ctypes.c_int32), ("kind", ctypes.c_int32), ("D", ctypes.c_int64),
                 ("Dkv", ctypes.c_int64), ("F", ctypes.c_int64),
                 ("host_blobs", ctypes.POINTER(ctypes.c_void_p)),
-                ("device_blobs", ctypes.POINTER(ctypes.c_void_p))]
+                ("device_blobs", ctypes.POINTER(ctypes.c_void_p)),
+                ("mixer", ctypes.c_int32), ("seq_len", ctypes.c_int64), ("rope_theta", ctypes.c_double)]
 
 
 _lib = None
@@ -70,6 +72,9 @@ _SIGS = {
     "sl_lora_group_workspace_size": (_SZ, [_I64, _I32, _I32]),
     "sl_stack_blob_layout": (_I32, [_I32, _I64, _I64, _I64, _P, _P]),
     "sl_stack_dq_layout": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "sl_sft_step": (_I32, [_P, _I32, _P, _P, _I64, _P, _I64, _P, _P, _I64, _P, _P, _I32, _F, _P, _P, _P, _I32,
+                           _P, _SZ, _P]),
+    "sl_sft_workspace_size": (_SZ, [_P, _I64, _I32, _I64, _I64]),
     "sl_rope_table": (_I32, [_I64, ctypes.c_double, _P, _P]),
     "sl_rope_apply": (_I32, [_P, _I64, _I64, _I32, _I64, _P, _I32, _P]),
     "sl_attention_fwd": (_I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I32, _I32, _P, _I64, _P, _P]),
@@ -321,7 +326,7 @@ def sl_attention_bwd(q, k, v, o, dO, lse, S, dq, dk, dv, rope_table=None, ws=Non
 
 # -------------------------------------------------------------------- stack
 def sl_stack_blob_layout(kind, D, Dkv, F):
-    offs = (ctypes.c_size_t * 14)()
+    offs = (ctypes.c_size_t * 16)()
     total = ctypes.c_size_t(0)
     _check(lib().sl_stack_blob_layout(kind, D, Dkv, F, offs, ctypes.byref(total)))
     return list(offs), total.value
@@ -346,8 +351,9 @@ def proj_shapes(D, Dkv, F):
     return [(D, D), (Dkv, D), (Dkv, D), (D, D), (F, D), (F, D), (D, F)]
 
 
-def build_layer_blob(kind, D, Dkv, F, weights, stream=None):
-    """One layer blob on the device from its seven bf16 weights [N, K] (device tensors).
+def build_layer_blob(kind, D, Dkv, F, weights, stream=None, norms=None):
+    """One layer blob on the device from its seven bf16 weights [N, K] (device tensors)
+    and its two RMS-norm weights (fp32 [D] each; None: ones).
 
     NF4 blobs are filled by sl_nf4_quantize directly at the layout offsets;
     NF4_DQ blobs take the codes the same way and the absmax of each group
@@ -358,6 +364,9 @@ def build_layer_blob(kind, D, Dkv, F, weights, stream=None):
     offs, total = sl_stack_blob_layout(kind, D, Dkv, F)
     blob = torch.zeros(total, dtype=torch.uint8, device="cuda")
     shapes = proj_shapes(D, Dkv, F)
+    for i in range(2):
+        dst = blob[offs[14 + i]: offs[14 + i] + D * 4].view(torch.float32)
+        dst.copy_(norms[i].reshape(-1).to(dst.device, torch.float32) if norms is not None else torch.ones(D))
     if kind == SL_WEIGHT_NF4_DQ:
         dq = sl_stack_dq_layout(D, Dkv, F)
         for group in DQ_GROUPS:
@@ -413,13 +422,16 @@ def adapter_shapes(D, Dkv, F, r):
 class Stack:
     """Owns an sl_stack handle (two device layer buffers, copy stream, events)."""
 
-    def __init__(self, kind, D, Dkv, F, host_blobs, device_blobs=None):
+    def __init__(self, kind, D, Dkv, F, host_blobs, device_blobs=None, mixer=SL_MIX_TOKEN_LOCAL, seq_len=0,
+                 rope_theta=0.0):
+        """mixer=SL_MIX_ATTENTION: causal GQA attention over sequences of seq_len tokens."""
         self.L = len(host_blobs)
         self._host = host_blobs
         self._dev = device_blobs
         self._hp = (ctypes.c_void_p * self.L)(*[b.data_ptr() for b in host_blobs])
         self._dp = (ctypes.c_void_p * self.L)(*[b.data_ptr() for b in device_blobs]) if device_blobs else None
-        self.desc = sl_stack_desc(self.L, kind, D, Dkv, F, self._hp, self._dp)
+        self.desc = sl_stack_desc(self.L, kind, D, Dkv, F, self._hp, self._dp, int(mixer), int(seq_len),
+                                  float(rope_theta))
         self.handle = ctypes.c_void_p()
         hb, bb = ctypes.c_size_t(0), ctypes.c_size_t(0)
         _check(lib().sl_stack_create(ctypes.byref(self.desc), ctypes.byref(self.handle), ctypes.byref(hb),
@@ -438,6 +450,19 @@ class Stack:
                                           float(alpha), _ptr(hL), _ptr(dh0), arr(dA), arr(dB),
                                           int(bool(accumulate)), _ptr(ws), ws.numel() * ws.element_size(),
                                           _stream(stream)))
+
+    def sft_workspace_size(self, M, r, V, chunk_V):
+        return int(lib().sl_sft_workspace_size(self.handle, int(M), int(r), int(V), int(chunk_V)))
+
+    def sft_step(self, mode, tokens, labels, embed, norm_final, W_head, chunk_V, A, B, r, alpha, loss, dA, dB, ws,
+                 accumulate=False, stream=None):
+        """One complete SFT step (embedding, stack, final norm, head CE, backward); loss: fp32 [1] on the device."""
+        n = 7 * self.L
+        arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts]) if ts is not None else None
+        _check(lib().sl_sft_step(self.handle, mode, _ptr(tokens), _ptr(labels), tokens.shape[0], _ptr(embed),
+                                 embed.shape[0], _ptr(norm_final), _ptr(W_head), int(chunk_V), arr(A), arr(B),
+                                 int(r), float(alpha), _ptr(loss), arr(dA), arr(dB), int(bool(accumulate)), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream)))
 
     def last_step_stats(self):
         a, b = ctypes.c_uint64(0), ctypes.c_uint64(0)

@@ -60,12 +60,14 @@ __device__ __forceinline__ void store8_f32(float* p, const float (&f)[8]) {
   reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
-// hs = h (+ add);  x = bf16(hs * rstd);  rstd = 1 / sqrt(mean(hs^2) + eps)
-// h_out receives hs when `add` is given (the residual update h1 = h + o).
+// hs = h (+ add);  x = bf16(hs * rstd (* w));  rstd = 1 / sqrt(mean(hs^2) + eps)
+// h_out receives hs when `add` is given (the residual update h1 = h + o);
+// w (nullable) is the norm's fp32 weight [D].
 __global__ void __launch_bounds__(kRowThreads) rms_fwd_kernel(const float* __restrict__ h,
                                                               const uint16_t* __restrict__ add,
                                                               float* __restrict__ h_out, uint16_t* __restrict__ x,
-                                                              float* __restrict__ rstd, int D) {
+                                                              float* __restrict__ rstd, const float* __restrict__ w,
+                                                              int D) {
   __shared__ float red[kRowThreads / 32];
   const int64_t row = blockIdx.x;
   const float* hr = h + row * D;
@@ -92,6 +94,12 @@ __global__ void __launch_bounds__(kRowThreads) rms_fwd_kernel(const float* __res
     load8_f32(src + i, f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] *= r;
+    if (w) {
+      float fw[8];
+      load8_f32(w + i, fw);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] *= fw[e];
+    }
     store8_bf16(x + row * D + i, f);
   }
 }
@@ -186,18 +194,24 @@ __global__ void swiglu_bwd_kernel(const uint16_t* __restrict__ dm, const uint16_
   }
 }
 
-// Backward of hs -> RMS(hs) with a residual pass-through:
-//   dx = sum of the nx bf16 GEMM outputs;  y = h * rstd;
-//   dh_out = dh_in + rstd * (dx - y * sum(dx * y) / D);  optional bf16 copy.
+// Backward of hs -> RMS(hs) * w with a residual pass-through:
+//   dx = w * (the fp32 dxf, or the sum of up to three bf16 GEMM outputs);
+//   y = h * rstd;  dh_out = dh_in + rstd * (dx - y * sum(dx * y) / D);
+//   dh_in and w nullable (no residual, no weight); optional bf16 copy.
 __global__ void __launch_bounds__(kRowThreads) rms_bwd_kernel(
     const float* __restrict__ dh_in, const uint16_t* __restrict__ dx0, const uint16_t* __restrict__ dx1,
-    const uint16_t* __restrict__ dx2, const float* __restrict__ h, const float* __restrict__ rstd,
-    float* __restrict__ dh_out, uint16_t* __restrict__ dh_bf16, int D) {
+    const uint16_t* __restrict__ dx2, const float* __restrict__ dxf, const float* __restrict__ h,
+    const float* __restrict__ rstd, const float* __restrict__ w, float* __restrict__ dh_out,
+    uint16_t* __restrict__ dh_bf16, int D) {
   __shared__ float red[kRowThreads / 32];
   const int64_t row = blockIdx.x;
   const float r = rstd[row];
   auto dx_at = [&](int i, float (&f)[8]) {
-    load8_bf16(dx0 + row * D + i, f);
+    if (dxf) {
+      load8_f32(dxf + row * D + i, f);
+    } else {
+      load8_bf16(dx0 + row * D + i, f);
+    }
     if (dx1) {
       float t[8];
       load8_bf16(dx1 + row * D + i, t);
@@ -209,6 +223,12 @@ __global__ void __launch_bounds__(kRowThreads) rms_bwd_kernel(
       load8_bf16(dx2 + row * D + i, t);
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] += t[e];
+    }
+    if (w) {
+      float fw[8];
+      load8_f32(w + i, fw);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] *= fw[e];
     }
   };
   float dot = 0.0f;
@@ -224,7 +244,12 @@ __global__ void __launch_bounds__(kRowThreads) rms_bwd_kernel(
     float fx[8], fh[8], fd[8];
     dx_at(i, fx);
     load8_f32(h + row * D + i, fh);
-    load8_f32(dh_in + row * D + i, fd);
+    if (dh_in) {
+      load8_f32(dh_in + row * D + i, fd);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) fd[e] = 0.0f;
+    }
 #pragma unroll
     for (int e = 0; e < 8; ++e) fd[e] += r * (fx[e] - fh[e] * r * c);
     store8_f32(dh_out + row * D + i, fd);
@@ -268,15 +293,37 @@ __global__ void mix_bwd_kernel(const uint16_t* __restrict__ da, const uint16_t* 
   }
 }
 
+// h0[m] = fp32(embed[tokens[m]]) (8 elements per thread); a token outside
+// [0, V) gives a zero row and SL_ERR_INVALID in the device error word.
+__global__ void embed_kernel(const int32_t* __restrict__ tokens, const uint16_t* __restrict__ embed, int64_t V,
+                             float* __restrict__ h0, int64_t M, int D, int* err) {
+  const int64_t n8 = M * D / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
+    const int64_t m = t * 8 / D;
+    const int j = static_cast<int>(t * 8 % D);
+    const int64_t tok = tokens[m];
+    float f[8];
+    if (tok >= 0 && tok < V) {
+      load8_bf16(embed + tok * D + j, f);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.0f;
+      if (j == 0) report_device_error(err, SL_ERR_INVALID);
+    }
+    store8_f32(h0 + m * D + j, f);
+  }
+}
+
 static int ew_grid(int64_t n8) {
   int64_t g = ceil_div(n8, 256);
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   return static_cast<int>(g < 1 ? 1 : (g > cap ? cap : g));
 }
 
-sl_status glue_rms_fwd(const float* h, const uint16_t* add, float* h_out, uint16_t* x, float* rstd, int64_t M,
-                       int D, cudaStream_t s) {
-  rms_fwd_kernel<<<static_cast<unsigned>(M), kRowThreads, 0, s>>>(h, add, h_out, x, rstd, D);
+sl_status glue_rms_fwd(const float* h, const uint16_t* add, float* h_out, uint16_t* x, float* rstd,
+                       const float* w, int64_t M, int D, cudaStream_t s) {
+  rms_fwd_kernel<<<static_cast<unsigned>(M), kRowThreads, 0, s>>>(h, add, h_out, x, rstd, w, D);
   return check_launch("rms_fwd_kernel");
 }
 sl_status glue_mix_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* a, int64_t M, int D,
@@ -303,10 +350,10 @@ sl_status glue_swiglu_bwd(const uint16_t* dm, const uint16_t* g, const uint16_t*
   return check_launch("swiglu_bwd_kernel");
 }
 sl_status glue_rms_bwd(const float* dh_in, const uint16_t* dx0, const uint16_t* dx1, const uint16_t* dx2,
-                       const float* h, const float* rstd, float* dh_out, uint16_t* dh_bf16, int64_t M, int D,
-                       cudaStream_t s) {
-  rms_bwd_kernel<<<static_cast<unsigned>(M), kRowThreads, 0, s>>>(dh_in, dx0, dx1, dx2, h, rstd, dh_out,
-                                                                  dh_bf16, D);
+                       const float* dxf, const float* h, const float* rstd, const float* w, float* dh_out,
+                       uint16_t* dh_bf16, int64_t M, int D, cudaStream_t s) {
+  rms_bwd_kernel<<<static_cast<unsigned>(M), kRowThreads, 0, s>>>(dh_in, dx0, dx1, dx2, dxf, h, rstd, w, dh_out,
+                                                                   dh_bf16, D);
   return check_launch("rms_bwd_kernel");
 }
 sl_status glue_mix_bwd(const uint16_t* da, const uint16_t* q, const uint16_t* k, uint16_t* dq, uint16_t* dk,
@@ -315,4 +362,12 @@ sl_status glue_mix_bwd(const uint16_t* da, const uint16_t* q, const uint16_t* k,
   return check_launch("mix_bwd_kernel");
 }
 
+}  // namespace sl
+
+namespace sl {
+sl_status glue_embed(const int32_t* tokens, const uint16_t* embed, int64_t V, float* h0, int64_t M, int D, int* err,
+                     cudaStream_t s) {
+  embed_kernel<<<ew_grid(M * D / 8), 256, 0, s>>>(tokens, embed, V, h0, M, D, err);
+  return check_launch("embed_kernel");
+}
 }  // namespace sl

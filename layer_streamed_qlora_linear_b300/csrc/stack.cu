@@ -23,6 +23,7 @@
 #include <cstring>
 #include <vector>
 
+#include "attn.cuh"
 #include "common.cuh"
 #include "glue.cuh"
 #include "linear.cuh"
@@ -33,9 +34,12 @@ struct sl_stack {
   int L = 0;
   int kind = 0;
   int64_t D = 0, Dkv = 0, F = 0;
+  int mixer = SL_MIX_TOKEN_LOCAL;
+  int64_t seq_len = 0;
+  double rope_theta = 0.0;
   std::vector<const void*> host;
   std::vector<const void*> dev;
-  size_t offs[14] = {0};
+  size_t offs[16] = {0};
   // NF4_DQ: per projection its group's qabsmax / absmax2 arrays, their row
   // lengths and the projection's first column in them
   size_t dq_q[7] = {0}, dq_a2[7] = {0};
@@ -78,7 +82,7 @@ struct DqLayout {
 constexpr int kDqFirst[4] = {0, 3, 4, 6};
 constexpr int kDqCount[4] = {3, 1, 2, 1};
 
-sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[14], size_t* total, DqLayout* dq) {
+sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[16], size_t* total, DqLayout* dq) {
   Proj p[7];
   proj_shapes(D, Dkv, F, p);
   // NF4: all codes, then all absmax, so that the q, k, v and the gate, up
@@ -121,6 +125,11 @@ sl_status layout(int kind, int64_t D, int64_t Dkv, int64_t F, size_t offs[14], s
         col += p[pi].N;
       }
     }
+  // the two RMS-norm weights (fp32 [D]: before attention, before the MLP)
+  for (int i = 0; i < 2; ++i) {
+    offs[14 + i] = off;
+    off = align_up(off + static_cast<size_t>(D) * 4, 256);
+  }
   *total = off;
   return SL_OK;
 }
@@ -134,9 +143,10 @@ struct Plan {
   size_t total = 0;
   // per layer
   std::vector<size_t> hin, h1, rstd1, rstd2, x1, qkv, a, x2, gu, m;
-  std::vector<size_t> Tqkv, To, Tgu, Td;
+  std::vector<size_t> Tqkv, To, Tgu, Td, lse;
   // shared
   size_t o, d, dhA, dhB, dd, dm, dgu, dx2a, dx2b, dh1, do_, da, dqkv, dx1q, dx1k, dx1v, lin_ws;
+  size_t att_ws = 0, rope = 0;  // attention: Di [H, M] and the rotary table [S, 128]
   size_t lin_ws_bytes = 0;
 };
 
@@ -168,6 +178,7 @@ Plan make_plan(const sl_stack* s, int64_t M, int r) {
     P.To.push_back(take(Tr));
     P.Tgu.push_back(take(2 * Tr));
     P.Td.push_back(take(Tr));
+    P.lse.push_back(s->mixer == SL_MIX_ATTENTION ? take(attention_ws_bytes(M, static_cast<int>(s->D / 128))) : 0);
   }
   P.o = take(MD * 2);
   P.d = take(MD * 2);
@@ -192,6 +203,10 @@ Plan make_plan(const sl_stack* s, int64_t M, int r) {
   if (rr) lw = std::max(lw, group_ws_bytes(M, 3, rr));
   P.lin_ws_bytes = lw;
   P.lin_ws = take(lw ? lw : 256);
+  if (s->mixer == SL_MIX_ATTENTION) {
+    P.att_ws = take(attention_ws_bytes(M, static_cast<int>(s->D / 128)));
+    P.rope = take(static_cast<size_t>(s->seq_len) * 128 * 4);
+  }
   P.total = off;
   return P;
 }
@@ -219,10 +234,12 @@ struct StepCtx {
   }
 };
 
-void weights_of(const sl_stack* s, const void* base, sl_weight w[7]) {
+void weights_of(const sl_stack* s, const void* base, sl_weight w[7], const float* norms[2]) {
   Proj p[7];
   proj_shapes(s->D, s->Dkv, s->F, p);
   const uint8_t* b = static_cast<const uint8_t*>(base);
+  norms[0] = reinterpret_cast<const float*>(b + s->offs[14]);
+  norms[1] = reinterpret_cast<const float*>(b + s->offs[15]);
   for (int i = 0; i < 7; ++i) {
     w[i].kind = s->kind;
     w[i].N = p[i].N;
@@ -268,7 +285,8 @@ sl_weight group_weight(const sl_weight w[7], int p0, int G) {
   return g;
 }
 
-sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, float* h_out) {
+sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* const norms[2], const float* h_in,
+                    float* h_out) {
   const Plan& P = *c.P;
   const sl_stack* s = c.s;
   const int64_t M = c.M;
@@ -290,9 +308,9 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
   float* h1 = c.at<float>(P.h1[l]);
   uint16_t* o = c.at<uint16_t>(P.o);
   uint16_t* d = c.at<uint16_t>(P.d);
-  SL_TRY(glue_rms_fwd(h_in, nullptr, nullptr, x1, c.at<float>(P.rstd1[l]), M, D, c.stream));
+  SL_TRY(glue_rms_fwd(h_in, nullptr, nullptr, x1, c.at<float>(P.rstd1[l]), norms[0], M, D, c.stream));
   // q, k, v
-  const uint16_t *q, *k, *v;
+  uint16_t *q, *k, *v;
   int64_t ldq, ldkv;
   if (c.group_qkv) {
     const sl_weight wg = group_weight(w, 0, 3);
@@ -315,9 +333,22 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
     ldq = D;
     ldkv = Dkv;
   }
-  SL_TRY(glue_mix_fwd(q, k, v, a, M, D, Dkv, ldq, ldkv, c.stream));
+  if (s->mixer == SL_MIX_ATTENTION) {
+    // rotate q and k in place (the saved q/k are the rotated ones), then attention
+    const float* rope = c.at<float>(P.rope);
+    if (c.group_qkv) {
+      SL_TRY(rope_apply(q, ldq, M, (D + Dkv) / 128, s->seq_len, rope, 0, c.stream));  // q | k columns
+    } else {
+      SL_TRY(rope_apply(q, ldq, M, D / 128, s->seq_len, rope, 0, c.stream));
+      SL_TRY(rope_apply(k, ldkv, M, Dkv / 128, s->seq_len, rope, 0, c.stream));
+    }
+    const AttnShape sh{M, s->seq_len, D / 128, Dkv / 128};
+    SL_TRY(attention_fwd(sh, q, ldq, k, ldkv, v, ldkv, a, D, c.at<float>(P.lse[l]), c.stream));
+  } else {
+    SL_TRY(glue_mix_fwd(q, k, v, a, M, D, Dkv, ldq, ldkv, c.stream));
+  }
   SL_TRY(linear_fwd(&w[3], a, M, A(3), B(3), r, c.alpha, o, c.at<float>(P.To[l]), lws, lwb, c.stream));
-  SL_TRY(glue_rms_fwd(h_in, o, h1, x2, c.at<float>(P.rstd2[l]), M, D, c.stream));
+  SL_TRY(glue_rms_fwd(h_in, o, h1, x2, c.at<float>(P.rstd2[l]), norms[1], M, D, c.stream));
   // gate, up
   if (c.group_gu) {
     const sl_weight wg = group_weight(w, 4, 2);
@@ -336,8 +367,8 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
 
 // dh2: gradient w.r.t. this layer's output (fp32) and its bf16 copy dd;
 // writes dh (w.r.t. the layer input) and, if dh_bf16, its bf16 copy.
-sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, const float* dh2,
-                    const uint16_t* dd, float* dh, uint16_t* dh_bf16) {
+sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const norms[2], const float* h_in,
+                    const float* dh2, const uint16_t* dd, float* dh, uint16_t* dh_bf16) {
   const Plan& P = *c.P;
   const sl_stack* s = c.s;
   const int64_t M = c.M;
@@ -376,40 +407,49 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* h_in, 
     const int64_t Ng[2] = {F, F};
     SL_TRY(group_bwd(&wg, 2, Ng, x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate, lws, lwb,
                      c.stream));
-    SL_TRY(glue_rms_bwd(dh2, dx2a, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]), dh1, do_, M, D,
-                        c.stream));
+    SL_TRY(glue_rms_bwd(dh2, dx2a, nullptr, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]),
+                        norms[1], dh1, do_, M, D, c.stream));
   } else {
     SL_TRY(glue_swiglu_bwd(dm, gu, gu + M * F, dgu, dgu + M * F, M, F, F, c.stream));
     SL_TRY(linear_bwd(&w[4], x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate, lws, lwb,
                       c.stream));
     SL_TRY(linear_bwd(&w[5], x2, dgu + M * F, M, A(5), B(5), r, c.alpha, Tgu + M * rr, dx2b, dA(5), dB(5),
                       c.accumulate, lws, lwb, c.stream));
-    SL_TRY(glue_rms_bwd(dh2, dx2a, dx2b, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]), dh1, do_, M, D,
-                        c.stream));
+    SL_TRY(glue_rms_bwd(dh2, dx2a, dx2b, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]),
+                        norms[1], dh1, do_, M, D, c.stream));
   }
   SL_TRY(linear_bwd(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, c.at<float>(P.To[l]), da, dA(3),
                     dB(3), c.accumulate, lws, lwb, c.stream));
-  // q, k, v
+  // q, k, v: the mixing step's backward into the dq/dk/dv region
+  auto mix_bwd = [&](const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t ldq, int64_t ldkv,
+                     uint16_t* dq, uint16_t* dk, uint16_t* dv) -> sl_status {
+    if (s->mixer != SL_MIX_ATTENTION) return glue_mix_bwd(da, q, k, dq, dk, dv, M, D, Dkv, ldq, ldkv, c.stream);
+    const AttnShape sh{M, s->seq_len, D / 128, Dkv / 128};
+    return attention_bwd(sh, q, ldq, k, ldkv, v, ldkv, c.at<uint16_t>(P.a[l]), D, da, D, c.at<float>(P.lse[l]), dq,
+                         ldq, dk, ldkv, dv, ldkv, c.at<float>(P.rope), c.at<uint8_t>(P.att_ws), c.stream);
+  };
   if (c.group_qkv) {
     const int64_t ld = D + 2 * Dkv;
-    SL_TRY(glue_mix_bwd(da, qkv, qkv + D, dqkv, dqkv + D, dqkv + D + Dkv, M, D, Dkv, ld, ld, c.stream));
+    SL_TRY(mix_bwd(qkv, qkv + D, qkv + D + Dkv, ld, ld, dqkv, dqkv + D, dqkv + D + Dkv));
     const sl_weight wg = group_weight(w, 0, 3);
     const int64_t Ng[3] = {D, Dkv, Dkv};
     SL_TRY(group_bwd(&wg, 3, Ng, x1, dqkv, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate, lws, lwb,
                      c.stream));
-    SL_TRY(glue_rms_bwd(dh1, dx1q, nullptr, nullptr, h_in, c.at<float>(P.rstd1[l]), dh, dh_bf16, M, D, c.stream));
+    SL_TRY(glue_rms_bwd(dh1, dx1q, nullptr, nullptr, nullptr, h_in, c.at<float>(P.rstd1[l]), norms[0], dh, dh_bf16, M,
+                        D, c.stream));
   } else {
     uint16_t* dq = dqkv;
     uint16_t* dk = dqkv + M * D;
     uint16_t* dv = dk + M * Dkv;
-    SL_TRY(glue_mix_bwd(da, qkv, qkv + M * D, dq, dk, dv, M, D, Dkv, D, Dkv, c.stream));
+    SL_TRY(mix_bwd(qkv, qkv + M * D, qkv + M * D + M * Dkv, D, Dkv, dq, dk, dv));
     SL_TRY(linear_bwd(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate, lws, lwb,
                       c.stream));
     SL_TRY(linear_bwd(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, Tqkv + M * rr, dx1k, dA(1), dB(1), c.accumulate, lws,
                       lwb, c.stream));
     SL_TRY(linear_bwd(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, Tqkv + 2 * M * rr, dx1v, dA(2), dB(2), c.accumulate,
                       lws, lwb, c.stream));
-    SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, h_in, c.at<float>(P.rstd1[l]), dh, dh_bf16, M, D, c.stream));
+    SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, nullptr, h_in, c.at<float>(P.rstd1[l]), norms[0], dh, dh_bf16, M, D,
+                        c.stream));
   }
   return SL_OK;
 }
@@ -453,7 +493,7 @@ sl_status ensure_layer(sl_stack* s, int l, uint64_t* h2d) {
 
 }  // namespace
 
-extern "C" sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F, size_t offsets[14],
+extern "C" sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, int64_t F, size_t offsets[16],
                                           size_t* blob_bytes) {
   SL_REQUIRE(offsets && blob_bytes, "sl_stack_blob_layout: null output");
   SL_REQUIRE(kind == SL_WEIGHT_NF4 || kind == SL_WEIGHT_BF16 || kind == SL_WEIGHT_NF4_DQ,
@@ -468,7 +508,7 @@ extern "C" sl_status sl_stack_blob_layout(int32_t kind, int64_t D, int64_t Dkv, 
 extern "C" sl_status sl_stack_dq_layout(int64_t D, int64_t Dkv, int64_t F, size_t q_off[7], int64_t q_ld[7],
                                         size_t a2_off[7], int64_t a2_ld[7], int64_t col0[7]) {
   SL_REQUIRE(q_off && q_ld && a2_off && a2_ld && col0, "sl_stack_dq_layout: null output");
-  size_t offs[14], bytes = 0;
+  size_t offs[16], bytes = 0;
   sl_status st = sl_stack_blob_layout(SL_WEIGHT_NF4_DQ, D, Dkv, F, offs, &bytes);
   if (st != SL_OK) return st;
   DqLayout dq{};
@@ -487,9 +527,13 @@ extern "C" sl_status sl_stack_create(const sl_stack_desc* desc, sl_stack** out, 
                                      size_t* buffer_bytes) {
   SL_REQUIRE(desc && out, "sl_stack_create: null argument");
   SL_REQUIRE(desc->L > 0 && desc->host_blobs, "sl_stack_create: need L > 0 and host_blobs");
-  size_t offs[14], bytes = 0;
+  size_t offs[16], bytes = 0;
   sl_status st = sl_stack_blob_layout(desc->kind, desc->D, desc->Dkv, desc->F, offs, &bytes);
   if (st != SL_OK) return st;
+  SL_REQUIRE(desc->mixer == SL_MIX_TOKEN_LOCAL || desc->mixer == SL_MIX_ATTENTION, "sl_stack_create: unknown mixer");
+  SL_REQUIRE(desc->mixer != SL_MIX_ATTENTION ||
+                 (desc->seq_len > 0 && desc->seq_len % 128 == 0 && desc->rope_theta > 1.0),
+             "sl_stack_create: attention needs seq_len a positive multiple of 128 and rope_theta > 1");
   for (int l = 0; l < desc->L; ++l) {
     const void* p = desc->host_blobs[l];
     SL_REQUIRE(p, "sl_stack_create: null host blob");
@@ -518,6 +562,9 @@ extern "C" sl_status sl_stack_create(const sl_stack_desc* desc, sl_stack** out, 
   s->D = desc->D;
   s->Dkv = desc->Dkv;
   s->F = desc->F;
+  s->mixer = desc->mixer;
+  s->seq_len = desc->seq_len;
+  s->rope_theta = desc->rope_theta;
   s->host.assign(desc->host_blobs, desc->host_blobs + desc->L);
   if (desc->device_blobs) s->dev.assign(desc->device_blobs, desc->device_blobs + desc->L);
   std::memcpy(s->offs, offs, sizeof(offs));
@@ -574,22 +621,127 @@ extern "C" size_t sl_stack_workspace_size(const sl_stack* s, int64_t M, int32_t 
   return make_plan(s, M, r).total;
 }
 
+namespace {
+
+// Checks shared by the stack step and the SFT step.
+sl_status check_step(const sl_stack* s, int32_t mode, int64_t M, int32_t r, const void* const* A,
+                     const void* const* B, float* const* dA, float* const* dB, const void* ws) {
+  SL_REQUIRE(s, "stack step: null stack");
+  SL_REQUIRE(mode == SL_MODE_STREAMED || mode == SL_MODE_RESIDENT, "stack step: bad mode");
+  SL_REQUIRE(mode == SL_MODE_STREAMED || !s->dev.empty(), "stack step: RESIDENT needs device_blobs");
+  SL_REQUIRE(ws && M > 0, "stack step: null workspace or M <= 0");
+  SL_REQUIRE(r == 0 || (A && B && dA && dB), "stack step: adapters and gradients required for r > 0");
+  SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "stack step: workspace must be 256-byte aligned");
+  if (s->kind == SL_WEIGHT_NF4_DQ && M <= 128)
+    return set_error(SL_ERR_UNSUPPORTED, "stack step: double-quantised stacks need M > 128");
+  SL_REQUIRE(s->mixer != SL_MIX_ATTENTION || M % s->seq_len == 0,
+             "stack step: attention needs M a multiple of the sequence length");
+  int dev = 0;
+  SL_CHECK_CUDA(cudaGetDevice(&dev));
+  SL_REQUIRE(dev == s->device, "stack step: current device differs from the handle's");
+  return SL_OK;
+}
+
+// The forward over layers 0..L-1 and the backward over L-1..0 of one step;
+// the two layers resident at the turn are not copied again.
+struct Runner {
+  sl_stack* s;
+  StepCtx& c;
+  const Plan& P;
+  bool streamed;
+  uint64_t h2d = 0;
+
+  const void* base_of(int l) const { return streamed ? s->buf[l % 2] : s->dev[l]; }
+  const float* h_in(int l, const float* h0) const { return l == 0 ? h0 : c.at<float>(P.hin[l]); }
+
+  sl_status forward(const float* h0, float* hL) {
+    const int L = s->L;
+    if (s->mixer == SL_MIX_ATTENTION)
+      SL_TRY(rope_table(s->seq_len, s->rope_theta, c.at<float>(P.rope), c.stream));
+    if (streamed) {
+      SL_TRY(ensure_layer(s, 0, &h2d));
+      if (L > 1) SL_TRY(ensure_layer(s, 1, &h2d));
+    }
+    sl_weight w[7];
+    const float* norms[2];
+    for (int l = 0; l < L; ++l) {
+      if (streamed) SL_CHECK_CUDA(cudaStreamWaitEvent(c.stream, s->ready[l % 2], 0));
+      weights_of(s, base_of(l), w, norms);
+      float* out = (l == L - 1) ? hL : c.at<float>(P.hin[l + 1]);
+      SL_TRY(layer_fwd(c, l, w, norms, h_in(l, h0), out));
+      if (streamed) {
+        SL_CHECK_CUDA(cudaEventRecord(s->freed[l % 2], c.stream));
+        if (l + 2 < L) SL_TRY(ensure_layer(s, l + 2, &h2d));
+      }
+    }
+    return SL_OK;
+  }
+
+  sl_status backward(const float* h0, const float* dh_top, float* dh0) {
+    const int L = s->L;
+    float* dhA = c.at<float>(P.dhA);
+    float* dhB = c.at<float>(P.dhB);
+    uint16_t* dd = c.at<uint16_t>(P.dd);
+    SL_TRY(glue_to_bf16(dh_top, dd, c.M * s->D, c.stream));
+    const float* dh_cur = dh_top;
+    sl_weight w[7];
+    const float* norms[2];
+    for (int l = L - 1; l >= 0; --l) {
+      if (streamed) {
+        SL_TRY(ensure_layer(s, l, &h2d));
+        SL_CHECK_CUDA(cudaStreamWaitEvent(c.stream, s->ready[l % 2], 0));
+      }
+      weights_of(s, base_of(l), w, norms);
+      float* dh_next = (l == 0) ? dh0 : ((dh_cur == dhA) ? dhB : dhA);
+      SL_TRY(layer_bwd(c, l, w, norms, h_in(l, h0), dh_cur, dd, dh_next, l == 0 ? nullptr : dd));
+      dh_cur = dh_next;
+      if (streamed) {
+        SL_CHECK_CUDA(cudaEventRecord(s->freed[l % 2], c.stream));
+        if (l - 2 >= 0) SL_TRY(ensure_layer(s, l - 2, &h2d));
+      }
+    }
+    return SL_OK;
+  }
+};
+
+// Regions of the SFT step's workspace after the stack plan.
+struct SftPlan {
+  size_t h0, hL, xf, rstd, dX, dh_top, dh0, ce_ws, total;
+  size_t ce_bytes;
+};
+
+SftPlan make_sft_plan(const Plan& P, int64_t M, int64_t D, int64_t V, int64_t chunk_V) {
+  SftPlan S{};
+  size_t off = P.total;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t MD = static_cast<size_t>(M) * D;
+  S.h0 = take(MD * 4);
+  S.hL = take(MD * 4);
+  S.xf = take(MD * 2);
+  S.rstd = take(M * 4);
+  S.dX = take(MD * 4);
+  S.dh_top = take(MD * 4);
+  S.dh0 = take(MD * 4);
+  S.ce_bytes = sl_ce_workspace_size(M, D, V, chunk_V);
+  S.ce_ws = take(S.ce_bytes ? S.ce_bytes : 256);
+  S.total = off;
+  return S;
+}
+
+}  // namespace
+
 extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64_t M,
                                           const float* dh_top, const void* const* A, const void* const* B,
                                           int32_t r, float alpha, float* hL, float* dh0, float* const* dA,
                                           float* const* dB, int32_t accumulate, void* ws, size_t ws_bytes,
                                           cudaStream_t stream) {
-  SL_REQUIRE(s, "sl_stream_stack_step: null stack");
-  SL_REQUIRE(mode == SL_MODE_STREAMED || mode == SL_MODE_RESIDENT, "sl_stream_stack_step: bad mode");
-  SL_REQUIRE(mode == SL_MODE_STREAMED || !s->dev.empty(), "sl_stream_stack_step: RESIDENT needs device_blobs");
-  SL_REQUIRE(h0 && dh_top && hL && dh0 && ws && M > 0, "sl_stream_stack_step: null argument");
-  SL_REQUIRE(r == 0 || (A && B && dA && dB), "sl_stream_stack_step: adapters and gradients required for r > 0");
-  SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_stream_stack_step: workspace must be 256-byte aligned");
-  if (s->kind == SL_WEIGHT_NF4_DQ && M <= 128)
-    return set_error(SL_ERR_UNSUPPORTED, "sl_stream_stack_step: double-quantised stacks need M > 128");
-  int dev = 0;
-  SL_CHECK_CUDA(cudaGetDevice(&dev));
-  SL_REQUIRE(dev == s->device, "sl_stream_stack_step: current device differs from the handle's");
+  sl_status st = check_step(s, mode, M, r, A, B, dA, dB, ws);
+  if (st != SL_OK) return st;
+  SL_REQUIRE(h0 && dh_top && hL && dh0, "sl_stream_stack_step: null argument");
   const Plan P = make_plan(s, M, r);
   SL_REQUIRE(ws_bytes >= P.total, "sl_stream_stack_step: workspace too small (need " + std::to_string(P.total) +
                                       " bytes)");
@@ -598,49 +750,53 @@ extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float
   c.group_qkv = can_group(s, M, r, 0, 3, A, B, dA, dB);
   c.group_gu = can_group(s, M, r, 4, 2, A, B, dA, dB);
   const uint64_t launches0 = launch_count();
-  const int L = s->L;
-  const bool streamed = mode == SL_MODE_STREAMED;
-  uint64_t h2d = 0;
-  sl_weight w[7];
-  auto base_of = [&](int l) -> const void* { return streamed ? s->buf[l % 2] : s->dev[l]; };
-  auto h_in = [&](int l) -> const float* { return l == 0 ? h0 : c.at<float>(P.hin[l]); };
+  Runner run{s, c, P, mode == SL_MODE_STREAMED};
+  SL_TRY(run.forward(h0, hL));
+  SL_TRY(run.backward(h0, dh_top, dh0));
+  s->last_h2d = run.h2d;
+  s->last_kernels = launch_count() - launches0;
+  return SL_OK;
+}
 
-  // ---------------------------------------------------------------- forward
-  if (streamed) {
-    SL_TRY(ensure_layer(s, 0, &h2d));
-    if (L > 1) SL_TRY(ensure_layer(s, 1, &h2d));
-  }
-  for (int l = 0; l < L; ++l) {
-    if (streamed) SL_CHECK_CUDA(cudaStreamWaitEvent(stream, s->ready[l % 2], 0));
-    weights_of(s, base_of(l), w);
-    float* out = (l == L - 1) ? hL : c.at<float>(P.hin[l + 1]);
-    SL_TRY(layer_fwd(c, l, w, h_in(l), out));
-    if (streamed) {
-      SL_CHECK_CUDA(cudaEventRecord(s->freed[l % 2], stream));
-      if (l + 2 < L) SL_TRY(ensure_layer(s, l + 2, &h2d));
-    }
-  }
-  // --------------------------------------------------------------- backward
-  float* dhA = c.at<float>(P.dhA);
-  float* dhB = c.at<float>(P.dhB);
-  uint16_t* dd = c.at<uint16_t>(P.dd);
-  SL_TRY(glue_to_bf16(dh_top, dd, M * s->D, stream));
-  const float* dh_cur = dh_top;
-  for (int l = L - 1; l >= 0; --l) {
-    if (streamed) {
-      SL_TRY(ensure_layer(s, l, &h2d));
-      SL_CHECK_CUDA(cudaStreamWaitEvent(stream, s->ready[l % 2], 0));
-    }
-    weights_of(s, base_of(l), w);
-    float* dh_next = (l == 0) ? dh0 : ((dh_cur == dhA) ? dhB : dhA);
-    SL_TRY(layer_bwd(c, l, w, h_in(l), dh_cur, dd, dh_next, l == 0 ? nullptr : dd));
-    dh_cur = dh_next;
-    if (streamed) {
-      SL_CHECK_CUDA(cudaEventRecord(s->freed[l % 2], stream));
-      if (l - 2 >= 0) SL_TRY(ensure_layer(s, l - 2, &h2d));
-    }
-  }
-  s->last_h2d = h2d;
+extern "C" size_t sl_sft_workspace_size(const sl_stack* s, int64_t M, int32_t r, int64_t V, int64_t chunk_V) {
+  if (!s || M <= 0 || V <= 0 || chunk_V <= 0) return 0;
+  return make_sft_plan(make_plan(s, M, r), M, s->D, V, chunk_V).total;
+}
+
+extern "C" sl_status sl_sft_step(sl_stack* s, int32_t mode, const int32_t* tokens, const int32_t* labels, int64_t M,
+                                 const void* embed, int64_t V, const float* norm_final, const void* W_head,
+                                 int64_t chunk_V, const void* const* A, const void* const* B, int32_t r, float alpha,
+                                 float* loss, float* const* dA, float* const* dB, int32_t accumulate, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  sl_status st = check_step(s, mode, M, r, A, B, dA, dB, ws);
+  if (st != SL_OK) return st;
+  SL_REQUIRE(tokens && labels && embed && W_head && loss && V > 0, "sl_sft_step: null argument");
+  const Plan P = make_plan(s, M, r);
+  const SftPlan S = make_sft_plan(P, M, s->D, V, chunk_V);
+  SL_REQUIRE(ws_bytes >= S.total, "sl_sft_step: workspace too small (need " + std::to_string(S.total) + " bytes)");
+  int* err = device_error_word();
+  if (!err) return SL_ERR_CUDA;
+  StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, stream};
+  c.accumulate = accumulate ? 1 : 0;
+  c.group_qkv = can_group(s, M, r, 0, 3, A, B, dA, dB);
+  c.group_gu = can_group(s, M, r, 4, 2, A, B, dA, dB);
+  const uint64_t launches0 = launch_count();
+  Runner run{s, c, P, mode == SL_MODE_STREAMED};
+  const int D = static_cast<int>(s->D);
+  float* h0 = c.at<float>(S.h0);
+  float* hL = c.at<float>(S.hL);
+  uint16_t* xf = c.at<uint16_t>(S.xf);
+  float* rstd = c.at<float>(S.rstd);
+  float* dX = c.at<float>(S.dX);
+  float* dh_top = c.at<float>(S.dh_top);
+  SL_TRY(glue_embed(tokens, static_cast<const uint16_t*>(embed), V, h0, M, D, err, stream));
+  SL_TRY(run.forward(h0, hL));
+  SL_TRY(glue_rms_fwd(hL, nullptr, nullptr, xf, rstd, norm_final, M, D, stream));
+  SL_TRY(sl_ce_fwd_bwd(xf, M, D, W_head, V, labels, -100, chunk_V, loss, dX, c.at<uint8_t>(S.ce_ws), S.ce_bytes,
+                       stream));
+  SL_TRY(glue_rms_bwd(nullptr, nullptr, nullptr, nullptr, dX, hL, rstd, norm_final, dh_top, nullptr, M, D, stream));
+  SL_TRY(run.backward(h0, dh_top, c.at<float>(S.dh0)));
+  s->last_h2d = run.h2d;
   s->last_kernels = launch_count() - launches0;
   return SL_OK;
 }

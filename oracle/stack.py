@@ -178,7 +178,7 @@ def sft_step(tokens, labels, embed, layers, norm_final, W_head, alpha, rnd=True,
     h0 = embed[tokens] (the frozen embedding rows); the stack forward; x =
     R(RMS(hL) * norm_final); the mean cross-entropy of x against the frozen
     head W_head [V, D] (oracle/ce.py: labels aligned with rows, -100
-    ignored); its gradient dx = R(dH) back through the final norm into
+    ignored); its gradient dx (fp32 on the GPU, unrounded here) back through the final norm into
     dh_top; the stack backward.  Returns (loss, dh0, grads)."""
     R = round_bf16 if rnd else _ident
     h = np.asarray(embed, dtype=np.float64)[np.asarray(tokens)]
@@ -189,7 +189,7 @@ def sft_step(tokens, labels, embed, layers, norm_final, W_head, alpha, rnd=True,
     yf, rf = rms_fwd(h)
     x = R(_weighted(yf, norm_final))
     loss, dx = ce_fwd_bwd(x, W_head, labels)[:2]
-    dh = rms_bwd(yf, rf, R(dx), norm_final)
+    dh = rms_bwd(yf, rf, dx, norm_final)
     grads = [None] * len(layers)
     for l in range(len(layers) - 1, -1, -1):
         dh, grads[l] = layer_backward(caches[l], dh, layers[l], alpha, rnd, attn)

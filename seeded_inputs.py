@@ -13,7 +13,10 @@ Recipe (stated once, used everywhere):
   bf16 (round-to-nearest-even), the checkpoint dtype of every weight and
   activation on the pages (Llama-3.1-8B / Qwen2.5-3B are bf16 checkpoints);
 * labels: ``integers(0, V)`` then exactly ``round(0.05 * M)`` rows, picked by a
-  seeded permutation, set to ``ignore_index`` (-100).
+  seeded permutation, set to ``ignore_index`` (-100);
+* RMS-norm weights: ``1 + 0.1 * standard_normal(dtype=float32)`` kept in fp32
+  (a trained checkpoint's norm weights sit near 1);
+* tokens: ``integers(0, V)`` as int32.
 
 bf16 tensors are carried as float32 arrays whose values are bf16-exact; the
 GPU side reinterprets the top 16 bits (``bf16_bits``).
@@ -127,3 +130,20 @@ def ce_case(seed: int, M: int, D: int, V: int, ignore_frac: float = 0.05,
         W=normal_bf16(seed * 1000 + 1, (V, D), w_std),
         labels=labels(seed * 1000 + 2, M, V, ignore_frac),
     )
+
+
+def norm_weight(seed: int, D: int) -> np.ndarray:
+    """fp32 [D] RMS-norm weight near 1."""
+    g = rng(seed)
+    return (np.float32(1.0) + np.float32(0.1) * g.standard_normal(size=D, dtype=np.float32)).astype(np.float32)
+
+
+def tokens(seed: int, M: int, V: int) -> np.ndarray:
+    return rng(seed).integers(0, V, size=M, dtype=np.int64).astype(np.int32)
+
+
+def sft_case(seed: int, M: int, D: int, V: int):
+    """Token ids, labels, a bf16 embedding [V, D] ~ N(0, 1), a bf16 head [V, D] ~ N(0, 0.02), a final norm."""
+    return dict(tokens=tokens(seed * 1000 + 0, M, V), labels=labels(seed * 1000 + 1, M, V),
+                embed=normal_bf16(seed * 1000 + 2, (V, D), 1.0), head=normal_bf16(seed * 1000 + 3, (V, D), 0.02),
+                norm_final=norm_weight(seed * 1000 + 4, D))

@@ -5,7 +5,7 @@ import torch
 
 import seeded_inputs as si
 from oracle import nf4, stack
-from gpu_util import BF16_TOL, dev_bf16, host, rel_fro
+from gpu_util import BF16_TOL, LOSS_TOL, dev_bf16, host, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -14,9 +14,12 @@ class Setup:
     """Blobs (pinned host + device copies), adapters and grads for one synthetic stack."""
 
     def __init__(self, sl, kind, L, M, D, Dkv, F, r, alpha, seed, with_oracle=True, torch_weights=False,
-                 packed=False):
+                 packed=False, attn=None, norms=False):
         """packed: each layer's adapters (and gradients) back to back, so that
-        NF4 stacks with M > 128 run q/k/v and gate/up as projection groups."""
+        NF4 stacks with M > 128 run q/k/v and gate/up as projection groups;
+        attn = (S, theta): causal GQA attention over sequences of S tokens;
+        norms: random RMS-norm weights (ones otherwise)."""
+        self.attn = None if attn is None else dict(S=attn[0], theta=attn[1])
         self.sl, self.kind, self.L, self.M, self.D, self.Dkv, self.F, self.r, self.alpha = \
             sl, kind, L, M, D, Dkv, F, r, alpha
         self.packed = packed
@@ -39,9 +42,13 @@ class Setup:
             for l in range(L):
                 lw = c["layers"][l]
                 Ws = [dev_bf16(lw[n]["W"]) for n in si.PROJ_NAMES]
-                blob = sl.build_layer_blob(kind, D, Dkv, F, Ws)
+                nw = [si.norm_weight(seed * 1000 + 500 + 2 * l + i, D) for i in range(2)] if norms else None
+                blob = sl.build_layer_blob(kind, D, Dkv, F, Ws,
+                                           norms=[torch.from_numpy(w) for w in nw] if norms else None)
                 self._add_blob(blob)
                 ref = {}
+                if norms:
+                    ref["norm_attn"], ref["norm_mlp"] = nw[0].astype(np.float64), nw[1].astype(np.float64)
                 Wdq = dq_ref_weights(sl, lw) if with_oracle and kind == sl.SL_WEIGHT_NF4_DQ else None
                 for n in si.PROJ_NAMES:
                     W = lw[n]["W"]
@@ -66,7 +73,8 @@ class Setup:
                     for p in range(7):
                         views[p].copy_(src[7 * l + p])
                         src[7 * l + p] = views[p]
-        self.stack = sl.Stack(kind, D, Dkv, F, self.host_blobs, self.dev_blobs)
+        mix = dict(mixer=sl.SL_MIX_ATTENTION, seq_len=attn[0], rope_theta=attn[1]) if attn else {}
+        self.stack = sl.Stack(kind, D, Dkv, F, self.host_blobs, self.dev_blobs, **mix)
         self.ws = torch.empty(self.stack.workspace_size(M, r), dtype=torch.uint8, device="cuda")
 
     def grads(self):
@@ -288,4 +296,64 @@ def test_dq_stack_rejects_small_m(gpu_lib):
     with pytest.raises(sl.SLError) as e:
         S.run(sl.SL_MODE_STREAMED)
     assert e.value.status == sl.SL_ERR_UNSUPPORTED
+    S.stack.close()
+
+
+@pytest.mark.parametrize("kind_name,packed", [("nf4", True), ("nf4", False), ("bf16", False)])
+def test_attention_stack_matches_oracle_and_resident(gpu_lib, kind_name, packed):
+    """The full decoder layer: weighted RMS norms, causal GQA attention with
+    rotary positions over two sequences, SiLU-gated MLP; grouped (packed) and
+    per-projection paths; streamed == resident bit for bit."""
+    sl = gpu_lib
+    kind = sl.SL_WEIGHT_NF4 if kind_name == "nf4" else sl.SL_WEIGHT_BF16
+    S = Setup(sl, kind, L=2, M=256, D=512, Dkv=256, F=768, r=16, alpha=32.0, seed=37, packed=packed,
+              attn=(128, 500000.0), norms=True)
+    hL, dh0, dA, dB = S.run(sl.SL_MODE_STREAMED)
+    ohL, odh0, ograds = stack.stack_step(S.h0_np, S.dh_np, S.ref_layers, 32.0, rnd=True, attn=S.attn)
+    assert rel_fro(host(hL), ohL) <= BF16_TOL
+    assert rel_fro(host(dh0), odh0) <= BF16_TOL
+    for l in range(S.L):
+        for p, n in enumerate(si.PROJ_NAMES):
+            assert rel_fro(host(dA[7 * l + p]), ograds[l][n][0]) <= BF16_TOL, (l, n)
+            assert rel_fro(host(dB[7 * l + p]), ograds[l][n][1]) <= BF16_TOL, (l, n)
+    r_ = S.run(sl.SL_MODE_RESIDENT)
+    for x, y in zip((hL, dh0, *dA, *dB), (r_[0], r_[1], *r_[2], *r_[3])):
+        assert same_bits(x, y)
+    S.stack.close()
+
+
+def test_sft_step_matches_oracle_and_resident(gpu_lib):
+    """One complete step: embedding rows, the streamed attention stack, the
+    final weighted norm, the vocab-chunked head cross-entropy and the backward
+    into every adapter."""
+    sl = gpu_lib
+    M, D, Dkv, F, V, r, alpha = 256, 512, 256, 768, 1536, 16, 32.0
+    S = Setup(sl, sl.SL_WEIGHT_NF4, L=2, M=M, D=D, Dkv=Dkv, F=F, r=r, alpha=alpha, seed=43, packed=True,
+              attn=(128, 500000.0), norms=True)
+    c = si.sft_case(7, M, D, V)
+    tok, lab = torch.from_numpy(c["tokens"]).cuda(), torch.from_numpy(c["labels"]).cuda()
+    emb, head = dev_bf16(c["embed"]), dev_bf16(c["head"])
+    nf = torch.from_numpy(c["norm_final"]).cuda()
+    ws = torch.empty(S.stack.sft_workspace_size(M, r, V, 512), dtype=torch.uint8, device="cuda")
+
+    def run(mode):
+        loss = torch.empty(1, device="cuda")
+        dA, dB = S.grads()
+        S.stack.sft_step(mode, tok, lab, emb, nf, head, 512, S.A, S.B, r, alpha, loss, dA, dB, ws)
+        sl.sl_check_device_errors()
+        return loss, dA, dB
+
+    loss, dA, dB = run(sl.SL_MODE_STREAMED)
+    oloss, _, ograds = stack.sft_step(c["tokens"], c["labels"], c["embed"].astype(np.float64), S.ref_layers,
+                                      c["norm_final"].astype(np.float64), c["head"].astype(np.float64), alpha,
+                                      rnd=True, attn=S.attn)
+    assert abs(loss.item() - oloss) <= LOSS_TOL * abs(oloss)
+    for l in range(S.L):
+        for p, n in enumerate(si.PROJ_NAMES):
+            assert rel_fro(host(dA[7 * l + p]), ograds[l][n][0]) <= BF16_TOL, (l, n)
+            assert rel_fro(host(dB[7 * l + p]), ograds[l][n][1]) <= BF16_TOL, (l, n)
+    loss_r, dA_r, dB_r = run(sl.SL_MODE_RESIDENT)
+    assert same_bits(loss, loss_r)
+    for x, y in zip(dA + dB, dA_r + dB_r):
+        assert same_bits(x, y)
     S.stack.close()
