@@ -9,11 +9,15 @@ from pinned host RAM through two device buffers.  Synthetic seeded data; no
 trained weights.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload stack8b|stack8b_dq|stack_qwen3b|layer8b|ce]
+                  [--workload stack8b|stack8b_dq|stack8b_attn|sft8b|stack_qwen3b|layer8b|ce]
 
 Other workloads (not the headline line): the same 32-layer stack with the
 absmax double-quantised to 8 bits (the ~3.6 GB pinned store, 113 MB per
-layer, that the pages quote); the 36-layer Qwen2.5-3B-shaped
+layer, that the pages quote); the same stack as full decoder layers (causal
+GQA attention with rotary positions over one 1024-token sequence, weighted
+RMS norms); one complete SFT step on those layers (embedding rows, the
+streamed stack, final norm, the 128256-entry head's chunked cross-entropy,
+backward); the 36-layer Qwen2.5-3B-shaped
 stack with a bf16 base streamed at M=2048; one Llama-8B layer's seven NF4
 LoRA linears resident at M=2048 (fwd+bwd); the LM-head cross-entropy
 (M=2048, D=4096, V=128256).
@@ -41,6 +45,14 @@ WORKLOADS = {
     "stack8b_dq": dict(kind="stack", base="nf4dq", L=32, M=1024, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
                        name="llama-3.1-8b-shaped 32-layer NF4 LoRA stack, 8-bit double-quantised absmax, streamed "
                             "from pinned host RAM, fwd 0..31 + bwd 31..0"),
+    "stack8b_attn": dict(kind="stack", base="nf4", L=32, M=1024, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
+                         attn=(1024, 500000.0),
+                         name="llama-3.1-8b-shaped 32 full decoder layers (causal GQA attention, rotary positions, "
+                              "one 1024-token sequence), NF4 LoRA, streamed from pinned host RAM, fwd + bwd"),
+    "sft8b": dict(kind="stack", base="nf4", L=32, M=1024, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
+                  attn=(1024, 500000.0), sft=dict(V=128256, chunk=8192),
+                  name="llama-3.1-8b-shaped complete SFT step: embedding, 32 full decoder layers streamed, final "
+                       "norm, 128256-entry head cross-entropy (vocab chunks of 8192), backward"),
     "stack_qwen3b": dict(kind="stack", base="bf16", L=36, M=2048, D=2048, Dkv=256, F=11008, r=16, alpha=32.0,
                          name="qwen2.5-3b-shaped 36-layer bf16-base LoRA stack streamed from pinned host RAM"),
     "layer8b": dict(kind="layer", base="nf4", M=2048, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
@@ -169,10 +181,23 @@ def oracle_sample(w):
                     for n in si.PROJ_NAMES}
 
         if w["kind"] == "stack":
+            attn = dict(S=ms, theta=w["attn"][1]) if "attn" in w else None
+            what = "full decoder layer (attention over one 64-token sequence)" if attn else "layer"
+            sft = w.get("sft")
+            if sft:   # and 1/L of the head's vocabulary against the same rows
+                Vs = sft["V"] // w["L"]
+                cc = si.ce_case(5, ms, w["D"], Vs)
+                W64 = cc["W"].astype(np.float64)
+                nv = int(np.sum(cc["labels"] != -100))
+
             def step():
-                stack.stack_step(c["h0"], c["dh_top"], [layer()], w["alpha"], rnd=True)
-            return step, ms, w["L"], (f"one full-width {w['base']} layer (of {w['L']}), {ms} tokens, fwd+bwd "
-                                      f"incl. dequantisation; tokens/s scaled by 1/{w['L']} layers")
+                stack.stack_step(c["h0"], c["dh_top"], [layer()], w["alpha"], rnd=True, attn=attn)
+                if sft:
+                    ce.ce_rows(cc["H"], W64, cc["labels"], max(nv, 1))
+            extra = f" and the cross-entropy of the {ms} rows over {Vs} head rows (1/{w['L']} of the vocabulary)" \
+                if sft else ""
+            return step, ms, w["L"], (f"one full-width {w['base']} {what} (of {w['L']}), {ms} tokens, fwd+bwd "
+                                      f"incl. dequantisation{extra}; tokens/s scaled by 1/{w['L']}")
         shp = proj_shapes(w["D"], w["Dkv"], w["F"])
         ys = {n: si.normal_bf16(77 + i, (ms, N), 1.0) for i, (n, N, K) in enumerate(shp)}
         xs = {n: si.normal_bf16(55 + i, (ms, K), 1.0) for i, (n, N, K) in enumerate(shp)}
@@ -292,11 +317,26 @@ def run_ours(args):
         dh = torch.randn(M, D, generator=gen, device=dev).to(torch.bfloat16).float()
         hL = torch.empty(M, D, device=dev)
         dh0 = torch.empty(M, D, device=dev)
-        stk = sl.Stack(kind, D, Dkv, F, host_blobs)
-        ws = torch.empty(stk.workspace_size(M, r), dtype=torch.uint8, device=dev)
+        mix = dict(mixer=sl.SL_MIX_ATTENTION, seq_len=w["attn"][0], rope_theta=w["attn"][1]) if "attn" in w else {}
+        stk = sl.Stack(kind, D, Dkv, F, host_blobs, **mix)
+        sft = w.get("sft")
+        if sft:
+            V, chunk = sft["V"], sft["chunk"]
+            emb, head = rnd((V, D), 1.0), rnd((V, D), 0.02)
+            nfin = torch.ones(D, device=dev)
+            tok = torch.randint(0, V, (M,), generator=gen, device=dev, dtype=torch.int32)
+            lab = torch.randint(0, V, (M,), generator=gen, device=dev, dtype=torch.int32)
+            lab[torch.randperm(M, generator=gen, device=dev)[: round(0.05 * M)]] = -100
+            loss = torch.empty(1, device=dev)
+            ws = torch.empty(stk.sft_workspace_size(M, r, V, chunk), dtype=torch.uint8, device=dev)
 
-        def step():
-            stk.step(sl.SL_MODE_STREAMED, h0, dh, A, B, r, alpha, hL, dh0, dA, dB, ws)
+            def step():
+                stk.sft_step(sl.SL_MODE_STREAMED, tok, lab, emb, nfin, head, chunk, A, B, r, alpha, loss, dA, dB, ws)
+        else:
+            ws = torch.empty(stk.workspace_size(M, r), dtype=torch.uint8, device=dev)
+
+            def step():
+                stk.step(sl.SL_MODE_STREAMED, h0, dh, A, B, r, alpha, hL, dh0, dA, dB, ws)
 
         h0_h, dh_h = h0.cpu().pin_memory(), dh.cpu().pin_memory()
         out_h = torch.empty(M, D, dtype=torch.float32, pin_memory=True)
@@ -308,8 +348,24 @@ def run_ours(args):
             stk.step(sl.SL_MODE_STREAMED, h0_d, dh_d, A, B, r, alpha, hL, dh0, dA, dB, ws)
             out_h.copy_(hL, non_blocking=True)
         e2e_bytes = (h0_h.numel() * 4 + dh_h.numel() * 4, out_h.numel() * 4)
+        if sft:   # token ids and labels in, the loss out
+            tok_h, lab_h = tok.cpu().pin_memory(), lab.cpu().pin_memory()
+            loss_h = torch.empty(1, dtype=torch.float32, pin_memory=True)
+
+            def e2e_step():
+                tok.copy_(tok_h, non_blocking=True)
+                lab.copy_(lab_h, non_blocking=True)
+                step()
+                loss_h.copy_(loss, non_blocking=True)
+            e2e_bytes = (tok_h.numel() * 4 + lab_h.numel() * 4, 4)
         h2d_peak = pinned_h2d_peak(torch, dev)
-        config = {"workload": w["name"], "tokens": M, "layers": L, "D": D, "Dkv": Dkv, "F": F, "rank": r,
+        wl_extra = {}
+        if "attn" in w:
+            wl_extra["attention"] = {"seq_len": w["attn"][0], "rope_theta": w["attn"][1], "heads": D // 128,
+                                     "kv_heads": Dkv // 128}
+        if sft:
+            wl_extra["sft"] = {"V": V, "chunk_V": chunk, "ignore_frac": 0.05}
+        config = {**wl_extra, "workload": w["name"], "tokens": M, "layers": L, "D": D, "Dkv": Dkv, "F": F, "rank": r,
                   "alpha": alpha, "base": {sl.SL_WEIGHT_NF4: "NF4 blocksize 64 fp32 absmax",
                                            sl.SL_WEIGHT_NF4_DQ: "NF4 blocksize 64, 8-bit absmax (fp32 offset and "
                                                                 "scale per 256 blocks)",
@@ -455,7 +511,7 @@ def run_ours(args):
     barrier()
     ms_instr = e0.elapsed_time(e1)
     sl.sl_kernel_timing(False)
-    timing = {name: sl.sl_kernel_timing_read(i) for i, name in enumerate(sl.GEMM_VARIANTS)}
+    timing = {name: sl.sl_kernel_timing_read(i) for i, name in enumerate(sl.TIMED_VARIANTS)}
     sl.sl_check_device_errors()
 
     # end to end through the public API: host inputs in, host result out, every step
@@ -480,8 +536,13 @@ def run_ours(args):
                 "share_of_step": ms_d / ms_instr,
                 "timing": "per-launch CUDA event pairs (libsl, on the launching stream) over a second timed "
                           "region of the same K steps"}
-    per_variant = {k: {"launches": v[0], "ms": v[1], "tflops": (v[2] / (v[1] * 1e-3) / 1e12) if v[1] else 0.0}
-                   for k, v in timing.items() if v[0]}
+    per_variant = {}
+    for k, v in timing.items():
+        if not v[0]:
+            continue
+        rate = v[2] / (v[1] * 1e-3) if v[1] else 0.0
+        per_variant[k] = ({"launches": v[0], "ms": v[1], "gbs": rate / 1e9} if k in sl.RANK_R_VARIANTS
+                          else {"launches": v[0], "ms": v[1], "tflops": rate / 1e12})
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded device RNG)",
@@ -496,7 +557,7 @@ def run_ours(args):
         line["preflight"] = {"host_bytes": stk.host_bytes, "buffer_bytes": stk.buffer_bytes}
         if not args.no_resident:
             dev_blobs = [hb.to(dev) for hb in host_blobs]
-            stk_r = sl.Stack(kind, D, Dkv, F, host_blobs, dev_blobs)
+            stk_r = sl.Stack(kind, D, Dkv, F, host_blobs, dev_blobs, **mix)
             stk_r.step(sl.SL_MODE_RESIDENT, h0, dh, A, B, r, alpha, hL, dh0, dA, dB, ws)
             barrier()
             e0.record(stream)

@@ -128,14 +128,17 @@ sl_status sl_debug_timeout_probe(int64_t limit_ns, int32_t mbarrier, cudaStream_
  * tensor-core launch; enable == 0 stops recording.  Costs one event pair
  * per launch.  Variants: 0 NF4 forward, 1 NF4 dX, 2 bf16 forward, 3 bf16
  * dX, 4 CE logits chunk (exp epilogue), 5 CE dH accumulation, 6 rank-r
- * T = X A^T, 7 rank-r U = dY B, 8 rank-r dA / dB. */
+ * T = X A^T, 7 rank-r U = dY B, 8 rank-r dA / dB, 9 attention forward,
+ * 10 attention backward (its three kernels together). */
 sl_status sl_kernel_timing(int32_t enable);
 
 /* Totals over the launches of one variant recorded since timing was
  * enabled: launch count, summed device time in ms (waits for the recorded
  * events) and algorithmic work: FLOPs for the GEMM variants 0-5 (2 M N K,
  * plus 2 M N r for the folded LoRA side product), bytes for the rank-r
- * passes 6-8 (the large operand once, the rank-r operands and the output). */
+ * passes 6-8 (the large operand once, the rank-r operands and the output),
+ * FLOPs for attention (2 x 128 per product per visible causal (query, key)
+ * pair: 2 products forward; 5 backward, S recomputed once). */
 sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms, double* work);
 
 /* ------------------------------------------------------------- NF4 (K0/K1) */
@@ -411,13 +414,14 @@ sl_status sl_attention_fwd(const void* q, int64_t ldq, const void* k, int64_t ld
                            int64_t M, int64_t S, int32_t H, int32_t Hkv, void* o, int64_t ldo, float* lse,
                            cudaStream_t stream);
 
-/* Bytes of the backward's workspace: Di [H, M] fp32. */
+/* Bytes of the backward's workspace: Di [H, M] fp32 and the per-query-head
+ * fp32 partials of dK and dV [H, M, 128] each. */
 size_t sl_attention_workspace_size(int64_t M, int32_t H);
 
 /* The backward given o, lse of the forward and dO = dL/do (bf16, row
  * stride lddo): dq [M, H*128], dk and dv [M, Hkv*128] bf16, each written
- * once (dk, dv summed over the query heads of their kv head inside one CTA:
- * bitwise reproducible).  rope_table (nullable, sl_rope_table): dq and dk
+ * once (dk, dv: per-query-head partials summed over the query heads of
+ * their kv head in head order: bitwise reproducible).  rope_table (nullable, sl_rope_table): dq and dk
  * leave rotated by the inverse angle, i.e. they are the gradients of q and
  * k before sl_rope_apply.  ws: sl_attention_workspace_size bytes, 16-byte
  * aligned. */

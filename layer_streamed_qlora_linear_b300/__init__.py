@@ -157,6 +157,8 @@ def sl_launch_count() -> int:
 
 GEMM_VARIANTS = ("nf4_fwd", "nf4_dx", "bf16_fwd", "bf16_dx", "ce_logits", "ce_dh")
 RANK_R_VARIANTS = ("rank_t", "rank_u", "rank_grad")  # timing variants 6, 7, 8 (work in bytes)
+ATTN_VARIANTS = ("attn_fwd", "attn_bwd")              # timing variants 9, 10 (work in FLOPs)
+TIMED_VARIANTS = GEMM_VARIANTS + RANK_R_VARIANTS + ATTN_VARIANTS
 
 
 def sl_kernel_timing(enable: bool):

@@ -27,6 +27,7 @@
 
 #include "attn.cuh"
 #include "ptx.cuh"
+#include "timing.cuh"
 #include "tmap.cuh"
 
 namespace sl {
@@ -41,6 +42,12 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
   const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
   return lo | (hi << 16);
+}
+// 2^x by the hardware approximation (ex2.approx, relative error ~2^-22; -inf -> +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -124,7 +131,7 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + 2 * kAtTile;    // 2 stages
   static constexpr int kOffP = kOffV + 2 * kAtTile;
   static constexpr int kOffBar = kOffP + kAtTile;
-  static constexpr int kNumBars = 14;
+  static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
@@ -140,13 +147,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sP = smem + FwdCfg::kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FwdCfg::kOffBar);
   uint64_t* q_full = bars;        // Q landed
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2] PV of the stage done
-  uint64_t* s_full = bars + 5;    // [2] S tile in TMEM buffer b
-  uint64_t* p_full = bars + 7;    // P written (4 warp arrivals); S buffer read
-  uint64_t* o_full = bars + 8;    // [2] O_part in TMEM buffer b
-  uint64_t* o_empty = bars + 10;  // [2] O_part read (4 warp arrivals)
-  uint64_t* drain = bars + 12;    // failure path: every issued MMA completed
+  uint64_t* k_full = bars + 1;    // [2] K tile of the stage landed
+  uint64_t* k_empty = bars + 3;   // [2] its S MMA done
+  uint64_t* v_full = bars + 5;    // [2] V tile landed
+  uint64_t* v_empty = bars + 7;   // [2] its PV MMA done
+  uint64_t* s_full = bars + 9;    // [2] S tile in TMEM buffer b
+  uint64_t* p_full = bars + 11;   // P written (4 warp arrivals); S buffer read
+  uint64_t* o_full = bars + 12;   // [2] O_part in TMEM buffer b
+  uint64_t* o_empty = bars + 14;  // [2] O_part read (4 warp arrivals)
+  uint64_t* drain = bars + 16;    // failure path: every issued MMA completed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + FwdCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + FwdCfg::kOffMisc + 4);
 
@@ -164,8 +173,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&kv_full[i], 1);
-      ptx::mbar_init(&kv_empty[i], 1);
+      ptx::mbar_init(&k_full[i], 1);
+      ptx::mbar_init(&k_empty[i], 1);
+      ptx::mbar_init(&v_full[i], 1);
+      ptx::mbar_init(&v_empty[i], 1);
       ptx::mbar_init(&s_full[i], 1);
       ptx::mbar_init(&o_full[i], 1);
       ptx::mbar_init(&o_empty[i], 4);
@@ -193,32 +204,42 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
+      // K of tile j + 2 loads once S of tile j is done, V once P V of tile j is
+      int issued_k = 0, issued_v = 0;
       bool ok = true;
       ptx::mbar_arrive_expect_tx(q_full, kAtTile);
       ptx::tma_load_2d(sQ, &map_q, q_full, h * 128, row0);
       ptx::tma_load_2d(sQ + kAtAtom128, &map_q, q_full, h * 128 + 64, row0);
-      for (int j = 0; j < n; ++j) {
+      for (int j = 0; j < n && ok; ++j) {
         const int s = j & 1;
-        if (!ptx::mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) {
-          give_up();
+        const uint32_t par = ((j >> 1) & 1) ^ 1;
+        const int y = kv0 + j * 128;
+        if (!ptx::mbar_wait(&k_empty[s], par, abort_flag)) {
           ok = false;
           break;
         }
-        ptx::mbar_arrive_expect_tx(&kv_full[s], 2 * kAtTile);
-        uint8_t* k_dst = sK + s * kAtTile;
-        uint8_t* v_dst = sV + s * kAtTile;
-        ptx::tma_load_2d(k_dst, &map_k, &kv_full[s], g * 128, kv0 + j * 128);
-        ptx::tma_load_2d(k_dst + kAtAtom128, &map_k, &kv_full[s], g * 128 + 64, kv0 + j * 128);
-        ptx::tma_load_2d(v_dst, &map_v, &kv_full[s], g * 128, kv0 + j * 128);
-        ptx::tma_load_2d(v_dst + kAtAtom128, &map_v, &kv_full[s], g * 128 + 64, kv0 + j * 128);
-        ++issued;
+        ptx::mbar_arrive_expect_tx(&k_full[s], kAtTile);
+        ptx::tma_load_2d(sK + s * kAtTile, &map_k, &k_full[s], g * 128, y);
+        ptx::tma_load_2d(sK + s * kAtTile + kAtAtom128, &map_k, &k_full[s], g * 128 + 64, y);
+        ++issued_k;
+        if (!ptx::mbar_wait(&v_empty[s], par, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&v_full[s], kAtTile);
+        ptx::tma_load_2d(sV + s * kAtTile, &map_v, &v_full[s], g * 128, y);
+        ptx::tma_load_2d(sV + s * kAtTile + kAtAtom128, &map_v, &v_full[s], g * 128 + 64, y);
+        ++issued_v;
       }
       // before the CTA exits every issued copy must have landed
       ptx::mbar_wait(q_full, 0, nullptr);
-      if (!ok)
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-          ptx::mbar_wait(&kv_full[j & 1], (j >> 1) & 1, nullptr);
+      if (!ok) {
+        give_up();
+        for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
+          ptx::mbar_wait(&k_full[j & 1], (j >> 1) & 1, nullptr);
+        for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
+          ptx::mbar_wait(&v_full[j & 1], (j >> 1) & 1, nullptr);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -229,24 +250,24 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       bool ok = ptx::mbar_wait(q_full, 0, abort_flag);
       auto issue_s = [&](int j) {
         const int s = j & 1;
-        if (!ptx::mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag)) return false;
+        if (!ptx::mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(s * 128);
         for (int kk = 0; kk < 8; ++kk)
           ptx::mma_bf16(d, kdesc(q_base, kk, kAtAtom128), kdesc(k_base + s * kAtTile, kk, kAtAtom128), id_s,
                         kk ? 1u : 0u);
         ptx::mma_commit(&s_full[s]);
+        ptx::mma_commit(&k_empty[s]);
         return true;
       };
       if (ok) ok = issue_s(0);
-      int issued_pv = 0;
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n && !issue_s(j + 1)) {
           ok = false;
           break;
         }
         const int s = j & 1;
-        if (!ptx::mbar_wait(p_full, j & 1, abort_flag) ||
+        if (!ptx::mbar_wait(p_full, j & 1, abort_flag) || !ptx::mbar_wait(&v_full[s], (j >> 1) & 1, abort_flag) ||
             !ptx::mbar_wait(&o_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -257,8 +278,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ptx::mma_bf16(d, kdesc(p_base, kk, kAtAtom128), mndesc(v_base + s * kAtTile, kk, kAtAtom128), id_o,
                         kk ? 1u : 0u);
         ptx::mma_commit(&o_full[s]);
-        ptx::mma_commit(&kv_empty[s]);
-        ++issued_pv;
+        ptx::mma_commit(&v_empty[s]);
       }
       if (!ok) {
         give_up();
@@ -266,7 +286,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::mma_commit(drain);
         ptx::mbar_wait(drain, 0, nullptr);
       }
-      (void)issued_pv;
     }
   } else {
     // ------------------------------------------------------------ softmax rows
@@ -289,12 +308,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       if (!wait_all(&o_full[s], (j >> 1) & 1)) return false;
       ptx::tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + c * 32), u);
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t u0[32], u1[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + c * 32), u0);
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + c * 32 + 32), u1);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) O[c * 32 + e] = fmaf(O[c * 32 + e], alpha_prev, __uint_as_float(u[e]));
+        for (int e = 0; e < 32; ++e) {
+          O[c * 32 + e] = fmaf(O[c * 32 + e], alpha_prev, __uint_as_float(u0[e]));
+          O[c * 32 + 32 + e] = fmaf(O[c * 32 + 32 + e], alpha_prev, __uint_as_float(u1[e]));
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -313,18 +336,19 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       // pass 1: row max of the scaled scores
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, u);
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t u0[32], u1[32];
+        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, u0);
+        ptx::tmem_ld_32x32b_x32(s_addr + c * 32 + 32, u1);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const bool vis = !diag || (c * 32 + e <= r);
-          if (vis) mt = fmaxf(mt, __uint_as_float(u[e]) * a.c);
+          if (!diag || c * 32 + e <= r) mt = fmaxf(mt, __uint_as_float(u0[e]));
+          if (!diag || c * 32 + 32 + e <= r) mt = fmaxf(mt, __uint_as_float(u1[e]));
         }
       }
-      const float m_new = fmaxf(m, mt);
-      const float alpha = exp2f(m - m_new);
+      const float m_new = fmaxf(m, mt * a.c);
+      const float alpha = ex2(m - m_new);
       // O_part of the previous tile joins O with the previous alpha; this also
       // frees the P tile (its MMA has completed)
       if (j > 0 && !accumulate(j - 1)) {
@@ -335,24 +359,29 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       // pass 2: P = exp2(S c - m_new) as bf16 into the swizzled P tile
       float lsum = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, u);
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t u[2][32];
+        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, u[0]);
+        ptx::tmem_ld_32x32b_x32(s_addr + c * 32 + 32, u[1]);
         ptx::tmem_wait_ld();
-        uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = exp2f(__uint_as_float(u[e]) * a.c - m_new);
-          float p1 = exp2f(__uint_as_float(u[e + 1]) * a.c - m_new);
-          if (diag && c * 32 + e > r) p0 = 0.0f;
-          if (diag && c * 32 + e + 1 > r) p1 = 0.0f;
-          lsum += p0 + p1;
-          w[e / 2] = pack2(p0, p1);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int cc = c + hh;
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float p0 = ex2(fmaf(__uint_as_float(u[hh][e]), a.c, -m_new));
+            float p1 = ex2(fmaf(__uint_as_float(u[hh][e + 1]), a.c, -m_new));
+            if (diag && cc * 32 + e > r) p0 = 0.0f;
+            if (diag && cc * 32 + e + 1 > r) p1 = 0.0f;
+            lsum += p0 + p1;
+            w[e / 2] = pack2(p0, p1);
+          }
+          uint8_t* atom = sP + (cc >> 1) * kAtAtom128;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *swz(atom, r, (cc & 1) * 4 + q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
         }
-        uint8_t* atom = sP + (c >> 1) * kAtAtom128;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *swz(atom, r, (c & 1) * 4 + q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       }
       l = l * alpha + lsum;
       m = m_new;
@@ -423,14 +452,16 @@ __device__ __forceinline__ void store_grad_row(const float* v, float scale, cons
 }
 
 // ------------------------------------------------------------ dQ
+constexpr int kAtStages = 3;  // key/value (dQ) and query/dO (dK dV) rings of the backward
+
 struct DqCfg {
   static constexpr int kOffQ = 0;                      // [128][128]
   static constexpr int kOffDO = kOffQ + kAtTile;       // [128][128]
-  static constexpr int kOffK = kOffDO + kAtTile;       // 2 stages of [64][128]
-  static constexpr int kOffV = kOffK + 2 * 2 * kAtAtom64;
-  static constexpr int kOffDS = kOffV + 2 * 2 * kAtAtom64;  // [128][64]
+  static constexpr int kOffK = kOffDO + kAtTile;       // kAtStages stages of [64][128]
+  static constexpr int kOffV = kOffK + kAtStages * 2 * kAtAtom64;
+  static constexpr int kOffDS = kOffV + kAtStages * 2 * kAtAtom64;  // [128][64]
   static constexpr int kOffBar = kOffDS + kAtAtom128;
-  static constexpr int kNumBars = 14;
+  static constexpr int kNumBars = 16;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
@@ -448,13 +479,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sDS = smem + DqCfg::kOffDS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DqCfg::kOffBar);
   uint64_t* q_full = bars;         // Q and dO landed
-  uint64_t* kv_full = bars + 1;    // [2]
-  uint64_t* kv_empty = bars + 3;   // [2]
-  uint64_t* sp_full = bars + 5;    // [2] S and dP in TMEM buffer b
-  uint64_t* ds_full = bars + 7;    // dS written (4 arrivals); S/dP buffer read
-  uint64_t* ds_empty = bars + 8;   // dQ MMA of dS done
-  uint64_t* acc_full = bars + 9;   // dQ complete
-  uint64_t* drain = bars + 10;     // failure path: every issued MMA completed
+  uint64_t* kv_full = bars + 1;    // [kAtStages]
+  uint64_t* kv_empty = bars + 4;   // [kAtStages]
+  uint64_t* sp_full = bars + 7;    // [2] S and dP in TMEM buffer b
+  uint64_t* ds_full = bars + 9;    // dS written (4 arrivals); S/dP buffer read
+  uint64_t* ds_empty = bars + 10;  // dQ MMA of dS done
+  uint64_t* acc_full = bars + 11;  // dQ complete
+  uint64_t* drain = bars + 12;     // failure path: every issued MMA completed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DqCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DqCfg::kOffMisc + 4);
 
@@ -472,11 +503,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAtStages; ++i) {
       ptx::mbar_init(&kv_full[i], 1);
       ptx::mbar_init(&kv_empty[i], 1);
-      ptx::mbar_init(&sp_full[i], 1);
     }
+    for (int i = 0; i < 2; ++i) ptx::mbar_init(&sp_full[i], 1);
     ptx::mbar_init(ds_full, 4);
     ptx::mbar_init(ds_empty, 1);
     ptx::mbar_init(acc_full, 1);
@@ -508,8 +539,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       ptx::tma_load_2d(sDO, &map_do, q_full, h * 128, row0);
       ptx::tma_load_2d(sDO + kAtAtom128, &map_do, q_full, h * 128 + 64, row0);
       for (int j = 0; j < n; ++j) {
-        const int s = j & 1;
-        if (!ptx::mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) {
+        const int s = j % kAtStages;
+        if (!ptx::mbar_wait(&kv_empty[s], ((j / kAtStages) & 1) ^ 1, abort_flag)) {
           give_up();
           ok = false;
           break;
@@ -525,8 +556,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       }
       ptx::mbar_wait(q_full, 0, nullptr);
       if (!ok)
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-          ptx::mbar_wait(&kv_full[j & 1], (j >> 1) & 1, nullptr);
+        for (int j = (issued > kAtStages ? issued - kAtStages : 0); j < issued; ++j)
+          ptx::mbar_wait(&kv_full[j % kAtStages], (j / kAtStages) & 1, nullptr);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -536,17 +567,17 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                      v_base = ptx::smem_addr(sV), ds_base = ptx::smem_addr(sDS);
       bool ok = ptx::mbar_wait(q_full, 0, abort_flag);
       auto issue_sp = [&](int j) {
-        const int s = j & 1;
-        if (!ptx::mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag)) return false;
+        const int s = j % kAtStages, b2 = j & 1;
+        if (!ptx::mbar_wait(&kv_full[s], (j / kAtStages) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint32_t kb = k_base + s * 2 * kAtAtom64, vb = v_base + s * 2 * kAtAtom64;
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + static_cast<uint32_t>(s * 64), kdesc(q_base, kk, kAtAtom128), kdesc(kb, kk, kAtAtom64),
+          ptx::mma_bf16(tmem + static_cast<uint32_t>(b2 * 64), kdesc(q_base, kk, kAtAtom128), kdesc(kb, kk, kAtAtom64),
                         id_s, kk ? 1u : 0u);
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(s * 64), kdesc(do_base, kk, kAtAtom128),
+          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(b2 * 64), kdesc(do_base, kk, kAtAtom128),
                         kdesc(vb, kk, kAtAtom64), id_s, kk ? 1u : 0u);
-        ptx::mma_commit(&sp_full[s]);
+        ptx::mma_commit(&sp_full[b2]);
         return true;
       };
       if (ok) ok = issue_sp(0);
@@ -561,12 +592,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t kb = k_base + (j & 1) * 2 * kAtAtom64;
+        const uint32_t kb = k_base + (j % kAtStages) * 2 * kAtAtom64;
         for (int kk = 0; kk < 4; ++kk)
           ptx::mma_bf16(tmem + 256u, kdesc(ds_base, kk, kAtAtom128), mndesc(kb, kk, kAtAtom64), id_q,
                         (j | kk) ? 1u : 0u);
         ptx::mma_commit(ds_empty);
-        ptx::mma_commit(&kv_empty[j & 1]);
+        ptx::mma_commit(&kv_empty[j % kAtStages]);
         ++done;
       }
       if (ok) {
@@ -600,23 +631,27 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       }
       ptx::tc_fence_after();
       uint32_t w[32];
+      {
+        uint32_t us[2][32], up[2][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t us[32], up[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + c * 32), us);
-        ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + c * 32), up);
+        for (int c = 0; c < 2; ++c) {
+          ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + c * 32), us[c]);
+          ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + c * 32), up[c]);
+        }
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float ds2[2];
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int key = j * 64 + c * 32 + e + u;
-            const float p = key <= qrow ? exp2f(__uint_as_float(us[e + u]) * a.c - lse2) : 0.0f;
-            ds2[u] = p * (__uint_as_float(up[e + u]) - di);
+          for (int e = 0; e < 32; e += 2) {
+            float ds2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int key = j * 64 + c * 32 + e + u;
+              const float p = key <= qrow ? ex2(fmaf(__uint_as_float(us[c][e + u]), a.c, -lse2)) : 0.0f;
+              ds2[u] = p * (__uint_as_float(up[c][e + u]) - di);
+            }
+            w[c * 16 + e / 2] = pack2(ds2[0], ds2[1]);
           }
-          w[c * 16 + e / 2] = pack2(ds2[0], ds2[1]);
-        }
       }
       // the previous dS must have been consumed by its MMA
       if (j > 0 && !wait_all(ds_empty, (j - 1) & 1)) {
@@ -654,16 +689,20 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 }
 
 // ------------------------------------------------------------ dK, dV
+// One CTA per (128-key tile, query head, sequence): dK_h and dV_h of the
+// key tile accumulate in TMEM over the query blocks that see it and leave as
+// fp32 partials [H][M][128]; attn_kv_reduce_kernel sums the query heads of
+// each kv head in head order.
 struct DkvCfg {
   static constexpr int kOffK = 0;                    // [128][128]
   static constexpr int kOffV = kOffK + kAtTile;      // [128][128]
   static constexpr int kStageBytes = 4 * kAtAtom64 + 512;  // Q [64][128], dO [64][128], lse and Di of 64 rows
   static constexpr int kStage = 4 * kAtAtom64 + 1024;      // stage stride (1024-aligned for the swizzled tiles)
-  static constexpr int kOffStage = kOffV + kAtTile;  // 2 stages
-  static constexpr int kOffPT = kOffStage + 2 * kStage;  // [128][64]
-  static constexpr int kOffDST = kOffPT + kAtAtom128;    // [128][64]
+  static constexpr int kOffStage = kOffV + kAtTile;        // kAtStages stages
+  static constexpr int kOffPT = kOffStage + kAtStages * kStage;  // [128][64]
+  static constexpr int kOffDST = kOffPT + kAtAtom128;            // [128][64]
   static constexpr int kOffBar = kOffDST + kAtAtom128;
-  static constexpr int kNumBars = 14;
+  static constexpr int kNumBars = 16;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
@@ -672,7 +711,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                      const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                      const __grid_constant__ CUtensorMap map_lse, const __grid_constant__ CUtensorMap map_di,
-                     const AttnArgs a) {
+                     const AttnArgs a, float* __restrict__ part_dk, float* __restrict__ part_dv) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem + DkvCfg::kOffK;
@@ -682,35 +721,33 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sDST = smem + DkvCfg::kOffDST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DkvCfg::kOffBar);
   uint64_t* kv_full = bars;        // K and V landed
-  uint64_t* st_full = bars + 1;    // [2]
-  uint64_t* st_empty = bars + 3;   // [2]
-  uint64_t* sp_full = bars + 5;    // [2] S^T and dP^T in TMEM buffer b
-  uint64_t* ds_full = bars + 7;    // P^T and dS^T written (4 arrivals)
-  uint64_t* ds_empty = bars + 8;   // their MMAs done
-  uint64_t* acc_full = bars + 9;   // dK, dV complete
-  uint64_t* drain = bars + 10;     // failure path: every issued MMA completed
+  uint64_t* st_full = bars + 1;    // [kAtStages]
+  uint64_t* st_empty = bars + 4;   // [kAtStages]
+  uint64_t* sp_full = bars + 7;    // [2] S^T and dP^T in TMEM buffer b
+  uint64_t* ds_full = bars + 9;    // P^T and dS^T written (4 arrivals)
+  uint64_t* ds_empty = bars + 10;  // their MMAs done
+  uint64_t* acc_full = bars + 11;  // dK, dV complete
+  uint64_t* drain = bars + 12;     // failure path: every issued MMA completed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DkvCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DkvCfg::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per = a.Hkv * a.nseq;
+  const int per = a.H * a.nseq;
   const int kt = static_cast<int>(blockIdx.x) / per;  // key tile; heaviest (kt = 0) first
-  const int gb = static_cast<int>(blockIdx.x) % per;
-  const int g = gb % a.Hkv, b = gb / a.Hkv;
-  const int rep = a.H / a.Hkv;
+  const int hb = static_cast<int>(blockIdx.x) % per;
+  const int h = hb % a.H, b = hb / a.H;
+  const int g = h / (a.H / a.Hkv);
   const int key0 = b * a.S + kt * 128;
-  const int nqb = a.S / 64 - 2 * kt;  // query blocks of 64 that see this key tile
-  const int n = rep * nqb;            // iterations: (query head, query block)
-  auto it_head = [&](int t) { return g * rep + t / nqb; };
-  auto it_qb = [&](int t) { return 2 * kt + t % nqb; };
+  const int n = a.S / 64 - 2 * kt;  // query blocks of 64 that see this key tile
+  const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAtStages; ++i) {
       ptx::mbar_init(&st_full[i], 1);
       ptx::mbar_init(&st_empty[i], 1);
-      ptx::mbar_init(&sp_full[i], 1);
     }
+    for (int i = 0; i < 2; ++i) ptx::mbar_init(&sp_full[i], 1);
     ptx::mbar_init(ds_full, 4);
     ptx::mbar_init(ds_empty, 1);
     ptx::mbar_init(acc_full, 1);
@@ -742,13 +779,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       ptx::tma_load_2d(sV, &map_v, kv_full, g * 128, key0);
       ptx::tma_load_2d(sV + kAtAtom128, &map_v, kv_full, g * 128 + 64, key0);
       for (int t = 0; t < n; ++t) {
-        const int s = t & 1;
-        if (!ptx::mbar_wait(&st_empty[s], ((t >> 1) & 1) ^ 1, abort_flag)) {
+        const int s = t % kAtStages;
+        if (!ptx::mbar_wait(&st_empty[s], ((t / kAtStages) & 1) ^ 1, abort_flag)) {
           give_up();
           ok = false;
           break;
         }
-        const int h = it_head(t), qrow = b * a.S + it_qb(t) * 64;
+        const int qrow = b * a.S + (2 * kt + t) * 64;
         uint8_t* st = sStage + s * DkvCfg::kStage;
         ptx::mbar_arrive_expect_tx(&st_full[s], DkvCfg::kStageBytes);
         ptx::tma_load_2d(st, &map_q, &st_full[s], h * 128, qrow);
@@ -761,8 +798,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       }
       ptx::mbar_wait(kv_full, 0, nullptr);
       if (!ok)
-        for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t)
-          ptx::mbar_wait(&st_full[t & 1], (t >> 1) & 1, nullptr);
+        for (int t = (issued > kAtStages ? issued - kAtStages : 0); t < issued; ++t)
+          ptx::mbar_wait(&st_full[t % kAtStages], (t / kAtStages) & 1, nullptr);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -772,21 +809,20 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                      pt_base = ptx::smem_addr(sPT), dst_base = ptx::smem_addr(sDST);
       bool ok = ptx::mbar_wait(kv_full, 0, abort_flag);
       auto issue_sp = [&](int t) {
-        const int s = t & 1;
-        if (!ptx::mbar_wait(&st_full[s], (t >> 1) & 1, abort_flag)) return false;
+        const int s = t % kAtStages, b2 = t & 1;
+        if (!ptx::mbar_wait(&st_full[s], (t / kAtStages) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint32_t qb = st_base + s * DkvCfg::kStage, dob = qb + 2 * kAtAtom64;
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + static_cast<uint32_t>(s * 64), kdesc(k_base, kk, kAtAtom128), kdesc(qb, kk, kAtAtom64),
+          ptx::mma_bf16(tmem + static_cast<uint32_t>(b2 * 64), kdesc(k_base, kk, kAtAtom128), kdesc(qb, kk, kAtAtom64),
                         id_s, kk ? 1u : 0u);
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(s * 64), kdesc(v_base, kk, kAtAtom128),
+          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(b2 * 64), kdesc(v_base, kk, kAtAtom128),
                         kdesc(dob, kk, kAtAtom64), id_s, kk ? 1u : 0u);
-        ptx::mma_commit(&sp_full[s]);
+        ptx::mma_commit(&sp_full[b2]);
         return true;
       };
       if (ok && n > 0) ok = issue_sp(0);
-      int done = 0;
       for (int t = 0; ok && t < n; ++t) {
         if (t + 1 < n && !issue_sp(t + 1)) {
           ok = false;
@@ -797,7 +833,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t qb = st_base + (t & 1) * DkvCfg::kStage, dob = qb + 2 * kAtAtom64;
+        const uint32_t qb = st_base + (t % kAtStages) * DkvCfg::kStage, dob = qb + 2 * kAtAtom64;
         for (int kk = 0; kk < 4; ++kk)
           ptx::mma_bf16(tmem + 256u, kdesc(pt_base, kk, kAtAtom128), mndesc(dob, kk, kAtAtom64), id_g,
                         (t | kk) ? 1u : 0u);
@@ -805,8 +841,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ptx::mma_bf16(tmem + 384u, kdesc(dst_base, kk, kAtAtom128), mndesc(qb, kk, kAtAtom64), id_g,
                         (t | kk) ? 1u : 0u);
         ptx::mma_commit(ds_empty);
-        ptx::mma_commit(&st_empty[t & 1]);
-        ++done;
+        ptx::mma_commit(&st_empty[t % kAtStages]);
       }
       if (ok) {
         ptx::mma_commit(acc_full);
@@ -815,7 +850,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::mma_commit(drain);
         ptx::mbar_wait(drain, 0, nullptr);
       }
-      (void)done;
     }
   } else {
     const int quarter = warp & 3;
@@ -830,36 +864,40 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     };
     bool ok = true;
     for (int t = 0; t < n; ++t) {
-      const int s = t & 1;
-      if (!wait_all(&sp_full[s], (t >> 1) & 1)) {
+      const int b2 = t & 1;
+      if (!wait_all(&sp_full[b2], (t >> 1) & 1)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      const float* lse_s = reinterpret_cast<const float*>(sStage + s * DkvCfg::kStage + 4 * kAtAtom64);
+      const float* lse_s = reinterpret_cast<const float*>(sStage + (t % kAtStages) * DkvCfg::kStage + 4 * kAtAtom64);
       const float* di_s = lse_s + 64;
-      const int q0 = it_qb(t) * 64;
+      const int q0 = (2 * kt + t) * 64;
       uint32_t wp[32], wd[32];
+      {
+        uint32_t us[2][32], up[2][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t us[32], up[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + c * 32), us);
-        ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + c * 32), up);
+        for (int c = 0; c < 2; ++c) {
+          ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(b2 * 64 + c * 32), us[c]);
+          ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(b2 * 64 + c * 32), up[c]);
+        }
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p2[2], d2[2];
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qi = c * 32 + e + u;
-            const float p =
-                (q0 + qi >= kpos) ? exp2f(__uint_as_float(us[e + u]) * a.c - lse_s[qi] * kLog2e) : 0.0f;
-            p2[u] = p;
-            d2[u] = p * (__uint_as_float(up[e + u]) - di_s[qi]);
+          for (int e = 0; e < 32; e += 2) {
+            float p2[2], d2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int qi = c * 32 + e + u;
+              const float p =
+                  (q0 + qi >= kpos) ? ex2(fmaf(__uint_as_float(us[c][e + u]), a.c, -lse_s[qi] * kLog2e)) : 0.0f;
+              p2[u] = p;
+              d2[u] = p * (__uint_as_float(up[c][e + u]) - di_s[qi]);
+            }
+            wp[c * 16 + e / 2] = pack2(p2[0], p2[1]);
+            wd[c * 16 + e / 2] = pack2(d2[0], d2[1]);
           }
-          wp[c * 16 + e / 2] = pack2(p2[0], p2[1]);
-          wd[c * 16 + e / 2] = pack2(d2[0], d2[1]);
-        }
       }
       if (t > 0 && !wait_all(ds_empty, (t - 1) & 1)) {
         ok = false;
@@ -877,25 +915,23 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
     if (ok && n > 0 && wait_all(acc_full, 0)) {
       ptx::tc_fence_after();
-      float v[128];
+      // fp32 partials of this query head: rows key0 + r, columns 0..127
+      const int64_t row = static_cast<int64_t>(h) * M + key0 + r;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(c * 32), u);
-        ptx::tmem_wait_ld();
+      for (int part = 0; part < 2; ++part) {
+        float* dst = (part ? part_dk : part_dv) + row * 128;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[c * 32 + e] = __uint_as_float(u[e]);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          ptx::tmem_ld_32x32b_x32(lane_base + (part ? 384u : 256u) + static_cast<uint32_t>(c * 32), u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            reinterpret_cast<float4*>(dst + c * 32)[e / 4] =
+                make_float4(__uint_as_float(u[e]), __uint_as_float(u[e + 1]), __uint_as_float(u[e + 2]),
+                            __uint_as_float(u[e + 3]));
+        }
       }
-      store_grad_row(v, 1.0f, nullptr, 0, a.out1 + static_cast<int64_t>(key0 + r) * a.ld1 + g * 128);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(c * 32), u);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[c * 32 + e] = __uint_as_float(u[e]);
-      }
-      store_grad_row(v, 0.08838834764831845f, a.rope, kpos, a.out0 + static_cast<int64_t>(key0 + r) * a.ld0 + g * 128);
     }
   }
   ptx::tc_fence_before();
@@ -906,7 +942,76 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   }
 }
 
+// dk[row, g*128 + i] = rot^-1(scale * sum_{h of g} part_dk[h][row]) and
+// dv = sum_{h of g} part_dv[h][row] in head order, bf16.  One thread per
+// (row, kv head, 8 rotation pairs): columns i .. i+7 and 64 + i .. 64 + i + 7.
+__global__ void attn_kv_reduce_kernel(const float* __restrict__ part_dk, const float* __restrict__ part_dv, int64_t M,
+                                      int S, int H, int Hkv, const float* __restrict__ rope, float scale,
+                                      uint16_t* __restrict__ dk, int64_t lddk, uint16_t* __restrict__ dv,
+                                      int64_t lddv) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= M * Hkv * 8) return;
+  const int64_t row = t / (Hkv * 8);
+  const int gc = static_cast<int>(t % (Hkv * 8));
+  const int g = gc / 8, c = gc % 8;
+  const int rep = H / Hkv;
+  float k1[8] = {}, k2[8] = {}, v1[8] = {}, v2[8] = {};
+  for (int i = 0; i < rep; ++i) {
+    const int64_t base = (static_cast<int64_t>(g * rep + i) * M + row) * 128 + c * 8;
+    const float4* pk = reinterpret_cast<const float4*>(part_dk + base);
+    const float4* pv = reinterpret_cast<const float4*>(part_dv + base);
+    const float4 a0 = pk[0], a1 = pk[1], b0 = pk[16], b1 = pk[17];
+    const float4 c0 = pv[0], c1 = pv[1], d0 = pv[16], d1 = pv[17];
+    const float ka[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float kb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const float va[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float vb[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      k1[e] += ka[e];
+      k2[e] += kb[e];
+      v1[e] += va[e];
+      v2[e] += vb[e];
+    }
+  }
+  uint32_t o1[4], o2[4], w1[4], w2[4];
+  const float* cs = rope ? rope + (row % S) * 128 + c * 8 : nullptr;
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    float y1[2], y2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float x1 = k1[e + u] * scale, x2 = k2[e + u] * scale;
+      if (cs) {
+        const float cv = cs[e + u], sv = cs[64 + e + u];
+        y1[u] = x1 * cv + x2 * sv;
+        y2[u] = x2 * cv - x1 * sv;
+      } else {
+        y1[u] = x1;
+        y2[u] = x2;
+      }
+    }
+    o1[e / 2] = pack2(y1[0], y1[1]);
+    o2[e / 2] = pack2(y2[0], y2[1]);
+    w1[e / 2] = pack2(v1[e], v1[e + 1]);
+    w2[e / 2] = pack2(v2[e], v2[e + 1]);
+  }
+  uint16_t* pk = dk + row * lddk + g * 128 + c * 8;
+  uint16_t* pv = dv + row * lddv + g * 128 + c * 8;
+  *reinterpret_cast<uint4*>(pk) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+  *reinterpret_cast<uint4*>(pk + 64) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  *reinterpret_cast<uint4*>(pv) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+  *reinterpret_cast<uint4*>(pv + 64) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+}
+
 // ------------------------------------------------------------ host side
+// Algorithmic FLOPs: 2 d per product per visible (query, key) pair; the
+// forward has 2 products (Q K^T, P V), the backward 5 (S recomputed once, dP,
+// dV, dQ, dK).
+double causal_pairs(const AttnShape& sh) {
+  return static_cast<double>(sh.M / sh.S) * sh.H * static_cast<double>(sh.S) * (sh.S + 1) / 2.0;
+}
+
 sl_status check_shape(const AttnShape& sh) {
   SL_REQUIRE(sh.M > 0 && sh.S > 0 && sh.S % 128 == 0 && sh.M % sh.S == 0,
              "attention: need S a positive multiple of 128 and M a multiple of S");
@@ -978,11 +1083,22 @@ sl_status attention_fwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, con
   a.err = err;
   if ((st = set_smem(attn_fwd_kernel, FwdCfg::kSmem)) != SL_OK) return st;
   const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.H * a.nseq);
+  const TimingToken tt = timing_begin(9, 2.0 * 2.0 * kAtD * causal_pairs(sh), stream);
   attn_fwd_kernel<<<grid, kAtThreads, FwdCfg::kSmem, stream>>>(mq, mk, mv, a);
-  return check_launch("attn_fwd_kernel");
+  st = check_launch("attn_fwd_kernel");
+  timing_end(tt, stream);
+  return st;
 }
 
-size_t attention_ws_bytes(int64_t M, int H) { return static_cast<size_t>(M) * H * 4; }
+// Backward workspace: Di [H, M], then the fp32 partials of dK and dV [H, M, 128] each.
+static size_t di_bytes(int64_t M, int H) { return (static_cast<size_t>(M) * H * 4 + 255) / 256 * 256; }
+size_t attention_ws_bytes(int64_t M, int H) { return di_bytes(M, H) + 2 * static_cast<size_t>(M) * H * 128 * 4; }
+
+static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, int64_t ldq, const uint16_t* k,
+                                      int64_t ldk, const uint16_t* v, int64_t ldv, const uint16_t* o, int64_t ldo,
+                                      const uint16_t* dout, int64_t lddo, const float* lse, uint16_t* dq,
+                                      int64_t lddq, uint16_t* dk, int64_t lddk, uint16_t* dv, int64_t lddv,
+                                      const float* rope, float* Di, int* err, cudaStream_t stream);
 
 sl_status attention_bwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, const uint16_t* k, int64_t ldk,
                         const uint16_t* v, int64_t ldv, const uint16_t* o, int64_t ldo, const uint16_t* dout,
@@ -1004,6 +1120,19 @@ sl_status attention_bwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, con
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   float* Di = static_cast<float*>(ws);
+  const TimingToken tt = timing_begin(10, 5.0 * 2.0 * kAtD * causal_pairs(sh), stream);
+  st = attention_bwd_launch(sh, q, ldq, k, ldk, v, ldv, o, ldo, dout, lddo, lse, dq, lddq, dk, lddk, dv, lddv, rope,
+                            Di, err, stream);
+  timing_end(tt, stream);
+  return st;
+}
+
+static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, int64_t ldq, const uint16_t* k,
+                                      int64_t ldk, const uint16_t* v, int64_t ldv, const uint16_t* o, int64_t ldo,
+                                      const uint16_t* dout, int64_t lddo, const float* lse, uint16_t* dq,
+                                      int64_t lddq, uint16_t* dk, int64_t lddk, uint16_t* dv, int64_t lddv,
+                                      const float* rope, float* Di, int* err, cudaStream_t stream) {
+  sl_status st;
   {
     const int64_t warps = sh.M * sh.H;
     attn_di_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, stream>>>(o, ldo, dout, lddo, sh.M,
@@ -1050,15 +1179,17 @@ sl_status attention_bwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, con
                        static_cast<uint64_t>(sh.H), static_cast<uint64_t>(sh.M) * 4, 64, 1,
                        CU_TENSOR_MAP_SWIZZLE_NONE)) != SL_OK)
       return st;
-    AttnArgs ak = a;
-    ak.out0 = dk;
-    ak.ld0 = lddk;
-    ak.out1 = dv;
-    ak.ld1 = lddv;
+    float* part_dk = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(Di) + di_bytes(sh.M, sh.H));
+    float* part_dv = part_dk + static_cast<size_t>(sh.M) * sh.H * 128;
     if ((st = set_smem(attn_dkdv_kernel, DkvCfg::kSmem)) != SL_OK) return st;
-    const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.Hkv * a.nseq);
-    attn_dkdv_kernel<<<grid, kAtThreads, DkvCfg::kSmem, stream>>>(mq, mdo, mk, mv, ml, md, ak);
+    const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.H * a.nseq);
+    attn_dkdv_kernel<<<grid, kAtThreads, DkvCfg::kSmem, stream>>>(mq, mdo, mk, mv, ml, md, a, part_dk, part_dv);
     if ((st = check_launch("attn_dkdv_kernel")) != SL_OK) return st;
+    const int64_t nt = sh.M * sh.Hkv * 8;
+    attn_kv_reduce_kernel<<<static_cast<unsigned>((nt + 255) / 256), 256, 0, stream>>>(
+        part_dk, part_dv, sh.M, static_cast<int>(sh.S), sh.H, sh.Hkv, rope, 0.08838834764831845f, dk, lddk, dv,
+        lddv);
+    if ((st = check_launch("attn_kv_reduce_kernel")) != SL_OK) return st;
   }
   return SL_OK;
 }

@@ -30,8 +30,9 @@ sl_status attention_fwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, con
 
 // dq [M, H*128], dk, dv [M, Hkv*128] bf16 from o, do and lse of the forward.
 // rope (nullable): a table of rope_table; dq and dk then leave rotated back
-// by the inverse angle (the gradients of the unrotated q and k).  ws: Di
-// [H, M] fp32 (attention_ws_bytes), 16-byte aligned.
+// by the inverse angle (the gradients of the unrotated q and k).  ws
+// (attention_ws_bytes, 16-byte aligned): Di [H, M] and the fp32 per-head
+// partials of dK and dV [H, M, 128] each.
 size_t attention_ws_bytes(int64_t M, int H);
 sl_status attention_bwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, const uint16_t* k, int64_t ldk,
                         const uint16_t* v, int64_t ldv, const uint16_t* o, int64_t ldo, const uint16_t* dout,

@@ -178,7 +178,7 @@ Plan make_plan(const sl_stack* s, int64_t M, int r) {
     P.To.push_back(take(Tr));
     P.Tgu.push_back(take(2 * Tr));
     P.Td.push_back(take(Tr));
-    P.lse.push_back(s->mixer == SL_MIX_ATTENTION ? take(attention_ws_bytes(M, static_cast<int>(s->D / 128))) : 0);
+    P.lse.push_back(s->mixer == SL_MIX_ATTENTION ? take(static_cast<size_t>(M) * (s->D / 128) * 4) : 0);
   }
   P.o = take(MD * 2);
   P.d = take(MD * 2);

@@ -5,8 +5,9 @@
 namespace sl {
 
 // Variants: 0..5 tensor-core GEMMs (see sl_kernel_timing), 6 rank-r T = X A^T,
-// 7 rank-r U = dY B, 8 rank-r dA / dB.
-constexpr int kNumTimedVariants = 9;
+// 7 rank-r U = dY B, 8 rank-r dA / dB, 9 attention forward, 10 attention
+// backward (all of its kernels).
+constexpr int kNumTimedVariants = 11;
 
 struct TimingToken {
   cudaEvent_t start = nullptr, stop = nullptr;
