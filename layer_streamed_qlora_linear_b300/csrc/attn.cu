@@ -57,14 +57,19 @@ __device__ __forceinline__ uint4* swz(uint8_t* atom, int row, int c) {
   return reinterpret_cast<uint4*>(atom + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
-// K-major SW128 operand whose K extent spans atoms of `atom` bytes: k16 step kk.
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, int atom) {
-  return ptx::smem_desc(base + (kk >> 2) * atom + (kk & 3) * 32, 16, 1024, 2);
+// Shared-memory descriptors of SW128 operands, built once per buffer and
+// advanced by constant adds: the address field counts 16-byte units and no
+// offset inside the CTA's shared memory (< 228 KB) carries out of it.
+__device__ __forceinline__ uint64_t kdesc0(uint32_t base) { return ptx::smem_desc(base, 16, 1024, 2); }
+// MN-major, N = 128 as two atoms of `atom` bytes along N
+__device__ __forceinline__ uint64_t mndesc0(uint32_t base, int atom) { return ptx::smem_desc(base, atom, 1024, 2); }
+__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+// k16 step kk of a K-major operand whose K extent spans atoms of `atom` bytes
+__device__ __forceinline__ uint64_t kstep(uint64_t d0, int kk, int atom) {
+  return dadd(d0, static_cast<uint32_t>((kk >> 2) * atom + (kk & 3) * 32));
 }
-// MN-major SW128 operand (N = 128: two atoms of `atom` bytes along N): k16 step kk.
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk, int atom) {
-  return ptx::smem_desc(base + kk * 2048, atom, 1024, 2);
-}
+// k16 step kk of an MN-major operand (16 rows of 128 bytes)
+__device__ __forceinline__ uint64_t mnstep(uint64_t d0, int kk) { return dadd(d0, static_cast<uint32_t>(kk * 2048)); }
 
 // ------------------------------------------------------------------- rope
 __global__ void rope_table_kernel(int64_t S, double theta, float* __restrict__ table) {
@@ -121,16 +126,22 @@ struct AttnArgs {
   int* err;
 };
 
-// Roles of the 192-thread CTAs: warp 0 TMA producer, warp 1 MMA issuer (and
-// TMEM owner), warps 2..5 row workers (TMEM lane quarter = warp % 4).
-constexpr int kAtThreads = 192;
+// Roles of the 320-thread CTAs: warp 0 TMA producer, warp 1 MMA issuer (and
+// TMEM owner), warps 2..9 row workers: worker w = warp - 2 reads TMEM lane
+// quarter warp % 4 (rows 32 (warp % 4) ..) and column half w / 4.
+constexpr int kAtThreads = 320;
+constexpr int kAtWorkers = 8;
+
+// Barrier of the eight worker warps only (named barrier 1).
+__device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kAtTile;        // 2 stages
   static constexpr int kOffV = kOffK + 2 * kAtTile;    // 2 stages
   static constexpr int kOffP = kOffV + 2 * kAtTile;
-  static constexpr int kOffBar = kOffP + kAtTile;
+  static constexpr int kOffRed = kOffP + kAtTile;       // row maxima [2][2][128], row sums [2][128], stop flags
+  static constexpr int kOffBar = kOffRed + 6 * 128 * 4 + 16;
   static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
@@ -179,11 +190,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       ptx::mbar_init(&v_empty[i], 1);
       ptx::mbar_init(&s_full[i], 1);
       ptx::mbar_init(&o_full[i], 1);
-      ptx::mbar_init(&o_empty[i], 4);
+      ptx::mbar_init(&o_empty[i], kAtWorkers);
     }
-    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(p_full, kAtWorkers);
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
+    reinterpret_cast<volatile int*>(sP + kAtTile + 6 * 128 * 4)[0] = 0;
+    reinterpret_cast<volatile int*>(sP + kAtTile + 6 * 128 * 4)[1] = 0;
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&map_q);
     ptx::tma_prefetch_desc(&map_k);
@@ -245,17 +258,18 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t id_o = ptx::idesc_bf16(128, 128, 0, 1);
-      const uint32_t q_base = ptx::smem_addr(sQ), k_base = ptx::smem_addr(sK), v_base = ptx::smem_addr(sV),
-                     p_base = ptx::smem_addr(sP);
+      const uint64_t dq0 = kdesc0(ptx::smem_addr(sQ)), dk0 = kdesc0(ptx::smem_addr(sK)),
+                     dp0 = kdesc0(ptx::smem_addr(sP)), dv0 = mndesc0(ptx::smem_addr(sV), kAtAtom128);
       bool ok = ptx::mbar_wait(q_full, 0, abort_flag);
       auto issue_s = [&](int j) {
         const int s = j & 1;
         if (!ptx::mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(s * 128);
+        const uint64_t dk = dadd(dk0, s * kAtTile);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(d, kdesc(q_base, kk, kAtAtom128), kdesc(k_base + s * kAtTile, kk, kAtAtom128), id_s,
-                        kk ? 1u : 0u);
+          ptx::mma_bf16(d, kstep(dq0, kk, kAtAtom128), kstep(dk, kk, kAtAtom128), id_s, kk ? 1u : 0u);
         ptx::mma_commit(&s_full[s]);
         ptx::mma_commit(&k_empty[s]);
         return true;
@@ -274,9 +288,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d = tmem + 256u + static_cast<uint32_t>(s * 128);
+        const uint64_t dv = dadd(dv0, s * kAtTile);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(d, kdesc(p_base, kk, kAtAtom128), mndesc(v_base + s * kAtTile, kk, kAtAtom128), id_o,
-                        kk ? 1u : 0u);
+          ptx::mma_bf16(d, kstep(dp0, kk, kAtAtom128), mnstep(dv, kk), id_o, kk ? 1u : 0u);
         ptx::mma_commit(&o_full[s]);
         ptx::mma_commit(&v_empty[s]);
       }
@@ -289,14 +304,22 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax rows
+    // Worker (quarter, half): row r, S / P / O columns 64 half .. 64 half + 63.
+    // The two halves of a row exchange their maxima through red_max (double-
+    // buffered by tile parity) at one worker barrier per tile; the barrier
+    // also carries stop flags (per parity, only ever set) so that a timed-out
+    // wait ends every worker at the same barrier.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // query row in the tile
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float O[128];
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 64);
+    float* red = reinterpret_cast<float*>(sP + kAtTile);  // maxima [2 parity][2 half][128], sums [2 half][128]
+    volatile int* stop = reinterpret_cast<volatile int*>(red + 6 * 128);  // [2 parity]
+    float O[64];
 #pragma unroll
-    for (int e = 0; e < 128; ++e) O[e] = 0.0f;
+    for (int e = 0; e < 64; ++e) O[e] = 0.0f;
     float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
-    bool ok = true;
+    bool bad = false, stopped = false;
     auto wait_all = [&](uint64_t* bar, uint32_t par) {
       bool w = ptx::mbar_wait(bar, par, abort_flag);
       w = __all_sync(0xffffffffu, w);
@@ -307,17 +330,14 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       const int s = j & 1;
       if (!wait_all(&o_full[s], (j >> 1) & 1)) return false;
       ptx::tc_fence_after();
+      uint32_t u0[32], u1[32];
+      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128), u0);
+      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + 32), u1);
+      ptx::tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        uint32_t u0[32], u1[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + c * 32), u0);
-        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + c * 32 + 32), u1);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          O[c * 32 + e] = fmaf(O[c * 32 + e], alpha_prev, __uint_as_float(u0[e]));
-          O[c * 32 + 32 + e] = fmaf(O[c * 32 + 32 + e], alpha_prev, __uint_as_float(u1[e]));
-        }
+      for (int e = 0; e < 32; ++e) {
+        O[e] = fmaf(O[e], alpha_prev, __uint_as_float(u0[e]));
+        O[32 + e] = fmaf(O[32 + e], alpha_prev, __uint_as_float(u1[e]));
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -326,80 +346,91 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     };
     for (int j = 0; j < n; ++j) {
       const int s = j & 1;
-      if (!wait_all(&s_full[s], (j >> 1) & 1)) {
-        ok = false;
+      const bool diag = (j == qt);
+      uint32_t u[2][32];
+      float mt = -INFINITY;
+      if (!bad) bad = !wait_all(&s_full[s], (j >> 1) & 1);
+      if (!bad) {
+        ptx::tc_fence_after();
+        const uint32_t s_addr = lane_base + static_cast<uint32_t>(s * 128);
+        ptx::tmem_ld_32x32b_x32(s_addr, u[0]);
+        ptx::tmem_ld_32x32b_x32(s_addr + 32, u[1]);
+        ptx::tmem_wait_ld();
+        if (diag) {  // keys above the diagonal do not exist
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (half * 64 + c * 32 + e > r) u[c][e] = __float_as_uint(-INFINITY);
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(u[c][e]));
+        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      }
+      red[(s * 2 + half) * 128 + r] = mt;
+      if (bad && lane == 0) stop[s] = 1;
+      workers_sync();
+      if (stop[s]) {
+        stopped = true;
         break;
       }
-      ptx::tc_fence_after();
-      const bool diag = (j == qt);
-      const uint32_t s_addr = lane_base + static_cast<uint32_t>(s * 128);
-      // pass 1: row max of the scaled scores
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        uint32_t u0[32], u1[32];
-        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, u0);
-        ptx::tmem_ld_32x32b_x32(s_addr + c * 32 + 32, u1);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (!diag || c * 32 + e <= r) mt = fmaxf(mt, __uint_as_float(u0[e]));
-          if (!diag || c * 32 + 32 + e <= r) mt = fmaxf(mt, __uint_as_float(u1[e]));
-        }
-      }
-      const float m_new = fmaxf(m, mt * a.c);
+      const float m_new = fmaxf(m, fmaxf(mt, red[(s * 2 + (half ^ 1)) * 128 + r]) * a.c);
       const float alpha = ex2(m - m_new);
       // O_part of the previous tile joins O with the previous alpha; this also
       // frees the P tile (its MMA has completed)
       if (j > 0 && !accumulate(j - 1)) {
-        ok = false;
-        break;
+        bad = true;
+        continue;  // raise the stop flag at the next barrier
       }
       alpha_prev = alpha;
-      // pass 2: P = exp2(S c - m_new) as bf16 into the swizzled P tile
-      float lsum = 0.0f;
+      // P = exp2(S c - m_new) as bf16 into this half's atom of the P tile
+      float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      uint8_t* atom = sP + half * kAtAtom128;
 #pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        uint32_t u[2][32];
-        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, u[0]);
-        ptx::tmem_ld_32x32b_x32(s_addr + c * 32 + 32, u[1]);
-        ptx::tmem_wait_ld();
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[16];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int cc = c + hh;
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float p0 = ex2(fmaf(__uint_as_float(u[hh][e]), a.c, -m_new));
-            float p1 = ex2(fmaf(__uint_as_float(u[hh][e + 1]), a.c, -m_new));
-            if (diag && cc * 32 + e > r) p0 = 0.0f;
-            if (diag && cc * 32 + e + 1 > r) p1 = 0.0f;
-            lsum += p0 + p1;
-            w[e / 2] = pack2(p0, p1);
-          }
-          uint8_t* atom = sP + (cc >> 1) * kAtAtom128;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *swz(atom, r, (cc & 1) * 4 + q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(u[c][e]), a.c, -m_new));
+          const float p1 = ex2(fmaf(__uint_as_float(u[c][e + 1]), a.c, -m_new));
+          ls[e & 3] += p0;
+          ls[(e + 1) & 3] += p1;
+          w[e / 2] = pack2(p0, p1);
         }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *swz(atom, r, c * 4 + q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       }
-      l = l * alpha + lsum;
+      l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       m = m_new;
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(p_full);
     }
-    if (ok && accumulate(n - 1)) {
-      const float inv = 1.0f / l;
-      uint16_t* dst = a.out0 + static_cast<int64_t>(row0 + r) * a.ld0 + h * 128;
+    if (!stopped) {
+      // the last O_part, then the two halves' row sums
+      if (!bad) bad = !accumulate(n - 1);
+      red[(2 * 2 + half) * 128 + r] = l;  // third slot pair: row sums
+      if (bad && lane == 0) stop[n & 1] = 1;
+      workers_sync();
+      if (!stop[n & 1]) {
+        const float lrow = red[(4 + 0) * 128 + r] + red[(4 + 1) * 128 + r];
+        const float inv = 1.0f / lrow;
+        uint16_t* dst = a.out0 + static_cast<int64_t>(row0 + r) * a.ld0 + h * 128 + half * 64;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        reinterpret_cast<uint4*>(dst)[c] =
-            make_uint4(pack2(O[8 * c] * inv, O[8 * c + 1] * inv), pack2(O[8 * c + 2] * inv, O[8 * c + 3] * inv),
-                       pack2(O[8 * c + 4] * inv, O[8 * c + 5] * inv), pack2(O[8 * c + 6] * inv, O[8 * c + 7] * inv));
-      const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
-      a.lse[static_cast<int64_t>(h) * M + row0 + r] = (m + log2f(l)) * 0.69314718055994531f;
+        for (int c = 0; c < 8; ++c)
+          reinterpret_cast<uint4*>(dst)[c] =
+              make_uint4(pack2(O[8 * c] * inv, O[8 * c + 1] * inv), pack2(O[8 * c + 2] * inv, O[8 * c + 3] * inv),
+                         pack2(O[8 * c + 4] * inv, O[8 * c + 5] * inv), pack2(O[8 * c + 6] * inv, O[8 * c + 7] * inv));
+        if (half == 0) {
+          const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
+          a.lse[static_cast<int64_t>(h) * M + row0 + r] = (m + log2f(lrow)) * 0.69314718055994531f;
+        }
+      }
     }
   }
   ptx::tc_fence_before();
@@ -428,40 +459,53 @@ __global__ void attn_di_kernel(const uint16_t* __restrict__ o, int64_t ldo, cons
   if (lane == 0) Di[static_cast<int64_t>(h) * M + row] = s;
 }
 
-// Scale by 1/sqrt(128), rotate back by the inverse angle of position `pos`
-// (table may be null), round to bf16 and store one 128-wide row.
-__device__ __forceinline__ void store_grad_row(const float* v, float scale, const float* table, int pos,
-                                               uint16_t* dst) {
-  float y[128];
+// Rotation pairs 32 half .. 32 half + 31 of one 128-wide gradient row: lo
+// holds columns 32 half .., hi columns 64 + 32 half ..; scale by 1/sqrt(128),
+// rotate back by the inverse angle of position `pos` (table may be null),
+// round to bf16 and store both 64-byte pieces of the row.
+__device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
+                                                 const float* table, int pos, int half, uint16_t* row) {
+  uint32_t o1[16], o2[16];
+  const float* cs = table ? table + static_cast<int64_t>(pos) * 128 + half * 32 : nullptr;
 #pragma unroll
-  for (int e = 0; e < 128; ++e) y[e] = v[e] * scale;
-  if (table) {
-    const float* cs = table + static_cast<int64_t>(pos) * 128;
+  for (int e = 0; e < 32; e += 2) {
+    float y1[2], y2[2];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float cv = cs[i], sv = cs[64 + i];
-      const float x1 = y[i], x2 = y[64 + i];
-      y[i] = x1 * cv + x2 * sv;
-      y[64 + i] = x2 * cv - x1 * sv;
+    for (int u = 0; u < 2; ++u) {
+      const float x1 = __uint_as_float(lo[e + u]) * scale, x2 = __uint_as_float(hi[e + u]) * scale;
+      if (cs) {
+        const float cv = cs[e + u], sv = cs[64 + e + u];
+        y1[u] = x1 * cv + x2 * sv;
+        y2[u] = x2 * cv - x1 * sv;
+      } else {
+        y1[u] = x1;
+        y2[u] = x2;
+      }
     }
+    o1[e / 2] = pack2(y1[0], y1[1]);
+    o2[e / 2] = pack2(y2[0], y2[1]);
   }
+  uint4* d1 = reinterpret_cast<uint4*>(row + half * 32);
+  uint4* d2 = reinterpret_cast<uint4*>(row + 64 + half * 32);
 #pragma unroll
-  for (int c = 0; c < 16; ++c)
-    reinterpret_cast<uint4*>(dst)[c] = make_uint4(pack2(y[8 * c], y[8 * c + 1]), pack2(y[8 * c + 2], y[8 * c + 3]),
-                                                  pack2(y[8 * c + 4], y[8 * c + 5]), pack2(y[8 * c + 6], y[8 * c + 7]));
+  for (int c = 0; c < 4; ++c) {
+    d1[c] = make_uint4(o1[4 * c], o1[4 * c + 1], o1[4 * c + 2], o1[4 * c + 3]);
+    d2[c] = make_uint4(o2[4 * c], o2[4 * c + 1], o2[4 * c + 2], o2[4 * c + 3]);
+  }
 }
 
 // ------------------------------------------------------------ dQ
-constexpr int kAtStages = 3;  // key/value (dQ) and query/dO (dK dV) rings of the backward
+constexpr int kAtStages = 3;  // key/value ring of the dQ kernel
+constexpr int kKvStages = 2;  // query/dO ring of the dK dV kernel
 
 struct DqCfg {
   static constexpr int kOffQ = 0;                      // [128][128]
   static constexpr int kOffDO = kOffQ + kAtTile;       // [128][128]
   static constexpr int kOffK = kOffDO + kAtTile;       // kAtStages stages of [64][128]
   static constexpr int kOffV = kOffK + kAtStages * 2 * kAtAtom64;
-  static constexpr int kOffDS = kOffV + kAtStages * 2 * kAtAtom64;  // [128][64]
-  static constexpr int kOffBar = kOffDS + kAtAtom128;
-  static constexpr int kNumBars = 16;
+  static constexpr int kOffDS = kOffV + kAtStages * 2 * kAtAtom64;  // 2 buffers of [128][64]
+  static constexpr int kOffBar = kOffDS + 2 * kAtAtom128;
+  static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
@@ -482,10 +526,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint64_t* kv_full = bars + 1;    // [kAtStages]
   uint64_t* kv_empty = bars + 4;   // [kAtStages]
   uint64_t* sp_full = bars + 7;    // [2] S and dP in TMEM buffer b
-  uint64_t* ds_full = bars + 9;    // dS written (4 arrivals); S/dP buffer read
-  uint64_t* ds_empty = bars + 10;  // dQ MMA of dS done
-  uint64_t* acc_full = bars + 11;  // dQ complete
-  uint64_t* drain = bars + 12;     // failure path: every issued MMA completed
+  uint64_t* ds_full = bars + 9;    // [2] dS buffer b written (8 warp arrivals); S/dP buffer b read
+  uint64_t* ds_empty = bars + 11;  // [2] the dQ MMA of dS buffer b done
+  uint64_t* acc_full = bars + 13;  // dQ complete
+  uint64_t* drain = bars + 14;     // failure path: every issued MMA completed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DqCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DqCfg::kOffMisc + 4);
 
@@ -508,8 +552,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       ptx::mbar_init(&kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) ptx::mbar_init(&sp_full[i], 1);
-    ptx::mbar_init(ds_full, 4);
-    ptx::mbar_init(ds_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&ds_full[i], kAtWorkers);
+      ptx::mbar_init(&ds_empty[i], 1);
+    }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -563,20 +609,23 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = ptx::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_q = ptx::idesc_bf16(128, 128, 0, 1);
-      const uint32_t q_base = ptx::smem_addr(sQ), do_base = ptx::smem_addr(sDO), k_base = ptx::smem_addr(sK),
-                     v_base = ptx::smem_addr(sV), ds_base = ptx::smem_addr(sDS);
+      const uint64_t dq0 = kdesc0(ptx::smem_addr(sQ)), ddo0 = kdesc0(ptx::smem_addr(sDO)),
+                     dk0 = kdesc0(ptx::smem_addr(sK)), dv0 = kdesc0(ptx::smem_addr(sV)),
+                     dkmn0 = mndesc0(ptx::smem_addr(sK), kAtAtom64), dds0 = kdesc0(ptx::smem_addr(sDS));
       bool ok = ptx::mbar_wait(q_full, 0, abort_flag);
       auto issue_sp = [&](int j) {
         const int s = j % kAtStages, b2 = j & 1;
         if (!ptx::mbar_wait(&kv_full[s], (j / kAtStages) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
-        const uint32_t kb = k_base + s * 2 * kAtAtom64, vb = v_base + s * 2 * kAtAtom64;
+        const uint64_t dk = dadd(dk0, s * 2 * kAtAtom64), dv = dadd(dv0, s * 2 * kAtAtom64);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + static_cast<uint32_t>(b2 * 64), kdesc(q_base, kk, kAtAtom128), kdesc(kb, kk, kAtAtom64),
+          ptx::mma_bf16(tmem + static_cast<uint32_t>(b2 * 64), kstep(dq0, kk, kAtAtom128), kstep(dk, kk, kAtAtom64),
                         id_s, kk ? 1u : 0u);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(b2 * 64), kdesc(do_base, kk, kAtAtom128),
-                        kdesc(vb, kk, kAtAtom64), id_s, kk ? 1u : 0u);
+          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(b2 * 64), kstep(ddo0, kk, kAtAtom128),
+                        kstep(dv, kk, kAtAtom64), id_s, kk ? 1u : 0u);
         ptx::mma_commit(&sp_full[b2]);
         return true;
       };
@@ -587,16 +636,17 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ok = false;
           break;
         }
-        if (!ptx::mbar_wait(ds_full, j & 1, abort_flag)) {
+        if (!ptx::mbar_wait(&ds_full[j & 1], (j >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t kb = k_base + (j % kAtStages) * 2 * kAtAtom64;
+        const uint64_t dkmn = dadd(dkmn0, (j % kAtStages) * 2 * kAtAtom64);
+        const uint64_t dds = dadd(dds0, (j & 1) * kAtAtom128);
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_bf16(tmem + 256u, kdesc(ds_base, kk, kAtAtom128), mndesc(kb, kk, kAtAtom64), id_q,
-                        (j | kk) ? 1u : 0u);
-        ptx::mma_commit(ds_empty);
+          ptx::mma_bf16(tmem + 256u, kstep(dds, kk, kAtAtom128), mnstep(dkmn, kk), id_q, (j | kk) ? 1u : 0u);
+        ptx::mma_commit(&ds_empty[j & 1]);
         ptx::mma_commit(&kv_empty[j % kAtStages]);
         ++done;
       }
@@ -610,7 +660,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       (void)done;
     }
   } else {
+    // Worker (quarter, half): query row r, key columns 32 half .. 32 half + 31
+    // of each 64-key block; in the epilogue the rotation pairs 32 half ..
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int qrow = qt * 128 + r;  // position in the sequence
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -630,54 +683,46 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      uint32_t w[32];
+      uint32_t w[16];
       {
-        uint32_t us[2][32], up[2][32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + c * 32), us[c]);
-          ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + c * 32), up[c]);
-        }
+        uint32_t us[32], up[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + half * 32), us);
+        ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + half * 32), up);
         ptx::tmem_wait_ld();
+        const int key0 = j * 64 + half * 32;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int e = 0; e < 32; e += 2) {
+          float ds2[2];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float ds2[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int key = j * 64 + c * 32 + e + u;
-              const float p = key <= qrow ? ex2(fmaf(__uint_as_float(us[c][e + u]), a.c, -lse2)) : 0.0f;
-              ds2[u] = p * (__uint_as_float(up[c][e + u]) - di);
-            }
-            w[c * 16 + e / 2] = pack2(ds2[0], ds2[1]);
+          for (int u = 0; u < 2; ++u) {
+            const float p = key0 + e + u <= qrow ? ex2(fmaf(__uint_as_float(us[e + u]), a.c, -lse2)) : 0.0f;
+            ds2[u] = p * (__uint_as_float(up[e + u]) - di);
           }
+          w[e / 2] = pack2(ds2[0], ds2[1]);
+        }
       }
-      // the previous dS must have been consumed by its MMA
-      if (j > 0 && !wait_all(ds_empty, (j - 1) & 1)) {
+      // dS buffer j & 1 must have been consumed by the MMA of iteration j - 2
+      if (!wait_all(&ds_empty[j & 1], ((j >> 1) & 1) ^ 1)) {
         ok = false;
         break;
       }
+      uint8_t* ds_buf = sDS + (j & 1) * kAtAtom128;
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8)
-        *swz(sDS, r, q8) = make_uint4(w[4 * q8], w[4 * q8 + 1], w[4 * q8 + 2], w[4 * q8 + 3]);
+      for (int q4 = 0; q4 < 4; ++q4)
+        *swz(ds_buf, r, half * 4 + q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ds_full);
+      if (lane == 0) ptx::mbar_arrive(&ds_full[j & 1]);
     }
     if (ok && wait_all(acc_full, 0)) {
       ptx::tc_fence_after();
-      float v[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(c * 32), u);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[c * 32 + e] = __uint_as_float(u[e]);
-      }
-      store_grad_row(v, 0.08838834764831845f, a.rope, qrow, a.out0 + static_cast<int64_t>(row0 + r) * a.ld0 + h * 128);
+      uint32_t lo[32], hi[32];
+      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(half * 32), lo);
+      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(64 + half * 32), hi);
+      ptx::tmem_wait_ld();
+      store_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, qrow, half,
+                       a.out0 + static_cast<int64_t>(row0 + r) * a.ld0 + h * 128);
     }
   }
   ptx::tc_fence_before();
@@ -698,11 +743,11 @@ struct DkvCfg {
   static constexpr int kOffV = kOffK + kAtTile;      // [128][128]
   static constexpr int kStageBytes = 4 * kAtAtom64 + 512;  // Q [64][128], dO [64][128], lse and Di of 64 rows
   static constexpr int kStage = 4 * kAtAtom64 + 1024;      // stage stride (1024-aligned for the swizzled tiles)
-  static constexpr int kOffStage = kOffV + kAtTile;        // kAtStages stages
-  static constexpr int kOffPT = kOffStage + kAtStages * kStage;  // [128][64]
-  static constexpr int kOffDST = kOffPT + kAtAtom128;            // [128][64]
-  static constexpr int kOffBar = kOffDST + kAtAtom128;
-  static constexpr int kNumBars = 16;
+  static constexpr int kOffStage = kOffV + kAtTile;        // kKvStages stages
+  static constexpr int kOffPT = kOffStage + kKvStages * kStage;  // 2 buffers of [128][64]
+  static constexpr int kOffDST = kOffPT + 2 * kAtAtom128;        // 2 buffers of [128][64]
+  static constexpr int kOffBar = kOffDST + 2 * kAtAtom128;
+  static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
@@ -721,11 +766,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sDST = smem + DkvCfg::kOffDST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DkvCfg::kOffBar);
   uint64_t* kv_full = bars;        // K and V landed
-  uint64_t* st_full = bars + 1;    // [kAtStages]
-  uint64_t* st_empty = bars + 4;   // [kAtStages]
-  uint64_t* sp_full = bars + 7;    // [2] S^T and dP^T in TMEM buffer b
-  uint64_t* ds_full = bars + 9;    // P^T and dS^T written (4 arrivals)
-  uint64_t* ds_empty = bars + 10;  // their MMAs done
+  uint64_t* st_full = bars + 1;    // [kKvStages]
+  uint64_t* st_empty = bars + 3;   // [kKvStages]
+  uint64_t* sp_full = bars + 5;    // [2] S^T and dP^T in TMEM buffer b
+  uint64_t* ds_full = bars + 7;    // [2] P^T and dS^T buffer b written (8 warp arrivals)
+  uint64_t* ds_empty = bars + 9;   // [2] their MMAs done
   uint64_t* acc_full = bars + 11;  // dK, dV complete
   uint64_t* drain = bars + 12;     // failure path: every issued MMA completed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DkvCfg::kOffMisc);
@@ -743,13 +788,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(kv_full, 1);
-    for (int i = 0; i < kAtStages; ++i) {
+    for (int i = 0; i < kKvStages; ++i) {
       ptx::mbar_init(&st_full[i], 1);
       ptx::mbar_init(&st_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) ptx::mbar_init(&sp_full[i], 1);
-    ptx::mbar_init(ds_full, 4);
-    ptx::mbar_init(ds_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&sp_full[i], 1);
+      ptx::mbar_init(&ds_full[i], kAtWorkers);
+      ptx::mbar_init(&ds_empty[i], 1);
+    }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -779,8 +826,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       ptx::tma_load_2d(sV, &map_v, kv_full, g * 128, key0);
       ptx::tma_load_2d(sV + kAtAtom128, &map_v, kv_full, g * 128 + 64, key0);
       for (int t = 0; t < n; ++t) {
-        const int s = t % kAtStages;
-        if (!ptx::mbar_wait(&st_empty[s], ((t / kAtStages) & 1) ^ 1, abort_flag)) {
+        const int s = t % kKvStages;
+        if (!ptx::mbar_wait(&st_empty[s], ((t / kKvStages) & 1) ^ 1, abort_flag)) {
           give_up();
           ok = false;
           break;
@@ -798,27 +845,30 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       }
       ptx::mbar_wait(kv_full, 0, nullptr);
       if (!ok)
-        for (int t = (issued > kAtStages ? issued - kAtStages : 0); t < issued; ++t)
-          ptx::mbar_wait(&st_full[t % kAtStages], (t / kAtStages) & 1, nullptr);
+        for (int t = (issued > kKvStages ? issued - kKvStages : 0); t < issued; ++t)
+          ptx::mbar_wait(&st_full[t % kKvStages], (t / kKvStages) & 1, nullptr);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t id_s = ptx::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_g = ptx::idesc_bf16(128, 128, 0, 1);
-      const uint32_t k_base = ptx::smem_addr(sK), v_base = ptx::smem_addr(sV), st_base = ptx::smem_addr(sStage),
-                     pt_base = ptx::smem_addr(sPT), dst_base = ptx::smem_addr(sDST);
+      const uint64_t dk0 = kdesc0(ptx::smem_addr(sK)), dv0 = kdesc0(ptx::smem_addr(sV)),
+                     dst0 = kdesc0(ptx::smem_addr(sStage)), dstmn0 = mndesc0(ptx::smem_addr(sStage), kAtAtom64),
+                     dpt0 = kdesc0(ptx::smem_addr(sPT)), ddst0 = kdesc0(ptx::smem_addr(sDST));
       bool ok = ptx::mbar_wait(kv_full, 0, abort_flag);
       auto issue_sp = [&](int t) {
-        const int s = t % kAtStages, b2 = t & 1;
-        if (!ptx::mbar_wait(&st_full[s], (t / kAtStages) & 1, abort_flag)) return false;
+        const int s = t % kKvStages, b2 = t & 1;
+        if (!ptx::mbar_wait(&st_full[s], (t / kKvStages) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
-        const uint32_t qb = st_base + s * DkvCfg::kStage, dob = qb + 2 * kAtAtom64;
+        const uint64_t dq = dadd(dst0, s * DkvCfg::kStage), ddo = dadd(dq, 2 * kAtAtom64);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + static_cast<uint32_t>(b2 * 64), kdesc(k_base, kk, kAtAtom128), kdesc(qb, kk, kAtAtom64),
+          ptx::mma_bf16(tmem + static_cast<uint32_t>(b2 * 64), kstep(dk0, kk, kAtAtom128), kstep(dq, kk, kAtAtom64),
                         id_s, kk ? 1u : 0u);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(b2 * 64), kdesc(v_base, kk, kAtAtom128),
-                        kdesc(dob, kk, kAtAtom64), id_s, kk ? 1u : 0u);
+          ptx::mma_bf16(tmem + 128u + static_cast<uint32_t>(b2 * 64), kstep(dv0, kk, kAtAtom128),
+                        kstep(ddo, kk, kAtAtom64), id_s, kk ? 1u : 0u);
         ptx::mma_commit(&sp_full[b2]);
         return true;
       };
@@ -828,20 +878,21 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ok = false;
           break;
         }
-        if (!ptx::mbar_wait(ds_full, t & 1, abort_flag)) {
+        if (!ptx::mbar_wait(&ds_full[t & 1], (t >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t qb = st_base + (t % kAtStages) * DkvCfg::kStage, dob = qb + 2 * kAtAtom64;
+        const uint64_t qmn = dadd(dstmn0, (t % kKvStages) * DkvCfg::kStage), domn = dadd(qmn, 2 * kAtAtom64);
+        const uint64_t dpt = dadd(dpt0, (t & 1) * kAtAtom128), ddst = dadd(ddst0, (t & 1) * kAtAtom128);
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_bf16(tmem + 256u, kdesc(pt_base, kk, kAtAtom128), mndesc(dob, kk, kAtAtom64), id_g,
-                        (t | kk) ? 1u : 0u);
+          ptx::mma_bf16(tmem + 256u, kstep(dpt, kk, kAtAtom128), mnstep(domn, kk), id_g, (t | kk) ? 1u : 0u);
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_bf16(tmem + 384u, kdesc(dst_base, kk, kAtAtom128), mndesc(qb, kk, kAtAtom64), id_g,
-                        (t | kk) ? 1u : 0u);
-        ptx::mma_commit(ds_empty);
-        ptx::mma_commit(&st_empty[t % kAtStages]);
+          ptx::mma_bf16(tmem + 384u, kstep(ddst, kk, kAtAtom128), mnstep(qmn, kk), id_g, (t | kk) ? 1u : 0u);
+        ptx::mma_commit(&ds_empty[t & 1]);
+        ptx::mma_commit(&st_empty[t % kKvStages]);
       }
       if (ok) {
         ptx::mma_commit(acc_full);
@@ -852,7 +903,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       }
     }
   } else {
+    // Worker (quarter, half): key row r, query columns 32 half .. 32 half + 31
+    // of each 64-query block; in the epilogue dV / dK columns 64 half ..
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // key row in the tile
     const int kpos = kt * 128 + r;      // key position in the sequence
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -870,66 +924,67 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      const float* lse_s = reinterpret_cast<const float*>(sStage + (t % kAtStages) * DkvCfg::kStage + 4 * kAtAtom64);
+      const float* lse_s =
+          reinterpret_cast<const float*>(sStage + (t % kKvStages) * DkvCfg::kStage + 4 * kAtAtom64) + half * 32;
       const float* di_s = lse_s + 64;
-      const int q0 = (2 * kt + t) * 64;
-      uint32_t wp[32], wd[32];
+      const int q0 = (2 * kt + t) * 64 + half * 32;
+      uint32_t wp[16], wd[16];
       {
-        uint32_t us[2][32], up[2][32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(b2 * 64 + c * 32), us[c]);
-          ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(b2 * 64 + c * 32), up[c]);
-        }
+        uint32_t us[32], up[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(b2 * 64 + half * 32), us);
+        ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(b2 * 64 + half * 32), up);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int e = 0; e < 32; e += 2) {
+          float p2[2], d2[2];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float p2[2], d2[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int qi = c * 32 + e + u;
-              const float p =
-                  (q0 + qi >= kpos) ? ex2(fmaf(__uint_as_float(us[c][e + u]), a.c, -lse_s[qi] * kLog2e)) : 0.0f;
-              p2[u] = p;
-              d2[u] = p * (__uint_as_float(up[c][e + u]) - di_s[qi]);
-            }
-            wp[c * 16 + e / 2] = pack2(p2[0], p2[1]);
-            wd[c * 16 + e / 2] = pack2(d2[0], d2[1]);
+          for (int u = 0; u < 2; ++u) {
+            const int qi = e + u;
+            const float p =
+                (q0 + qi >= kpos) ? ex2(fmaf(__uint_as_float(us[qi]), a.c, -lse_s[qi] * kLog2e)) : 0.0f;
+            p2[u] = p;
+            d2[u] = p * (__uint_as_float(up[qi]) - di_s[qi]);
           }
+          wp[e / 2] = pack2(p2[0], p2[1]);
+          wd[e / 2] = pack2(d2[0], d2[1]);
+        }
       }
-      if (t > 0 && !wait_all(ds_empty, (t - 1) & 1)) {
+      // buffer t & 1 must have been consumed by the MMAs of iteration t - 2
+      if (!wait_all(&ds_empty[t & 1], ((t >> 1) & 1) ^ 1)) {
         ok = false;
         break;
       }
+      uint8_t* pt_buf = sPT + (t & 1) * kAtAtom128;
+      uint8_t* dst_buf = sDST + (t & 1) * kAtAtom128;
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        *swz(sPT, r, q8) = make_uint4(wp[4 * q8], wp[4 * q8 + 1], wp[4 * q8 + 2], wp[4 * q8 + 3]);
-        *swz(sDST, r, q8) = make_uint4(wd[4 * q8], wd[4 * q8 + 1], wd[4 * q8 + 2], wd[4 * q8 + 3]);
+      for (int q4 = 0; q4 < 4; ++q4) {
+        *swz(pt_buf, r, half * 4 + q4) = make_uint4(wp[4 * q4], wp[4 * q4 + 1], wp[4 * q4 + 2], wp[4 * q4 + 3]);
+        *swz(dst_buf, r, half * 4 + q4) = make_uint4(wd[4 * q4], wd[4 * q4 + 1], wd[4 * q4 + 2], wd[4 * q4 + 3]);
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ds_full);
+      if (lane == 0) ptx::mbar_arrive(&ds_full[t & 1]);
     }
     if (ok && n > 0 && wait_all(acc_full, 0)) {
       ptx::tc_fence_after();
-      // fp32 partials of this query head: rows key0 + r, columns 0..127
+      // fp32 partials of this query head: row key0 + r, columns 64 half .. 64 half + 63
       const int64_t row = static_cast<int64_t>(h) * M + key0 + r;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        float* dst = (part ? part_dk : part_dv) + row * 128;
+        float* dst = (part ? part_dk : part_dv) + row * 128 + half * 64;
+        uint32_t u0[32], u1[32];
+        const uint32_t base = lane_base + (part ? 384u : 256u) + static_cast<uint32_t>(half * 64);
+        ptx::tmem_ld_32x32b_x32(base, u0);
+        ptx::tmem_ld_32x32b_x32(base + 32, u1);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          ptx::tmem_ld_32x32b_x32(lane_base + (part ? 384u : 256u) + static_cast<uint32_t>(c * 32), u);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            reinterpret_cast<float4*>(dst + c * 32)[e / 4] =
-                make_float4(__uint_as_float(u[e]), __uint_as_float(u[e + 1]), __uint_as_float(u[e + 2]),
-                            __uint_as_float(u[e + 3]));
+        for (int e = 0; e < 32; e += 4) {
+          reinterpret_cast<float4*>(dst)[e / 4] = make_float4(__uint_as_float(u0[e]), __uint_as_float(u0[e + 1]),
+                                                              __uint_as_float(u0[e + 2]), __uint_as_float(u0[e + 3]));
+          reinterpret_cast<float4*>(dst + 32)[e / 4] =
+              make_float4(__uint_as_float(u1[e]), __uint_as_float(u1[e + 1]), __uint_as_float(u1[e + 2]),
+                          __uint_as_float(u1[e + 3]));
         }
       }
     }
