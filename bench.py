@@ -9,7 +9,7 @@ from pinned host RAM through two device buffers.  Synthetic seeded data; no
 trained weights.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload stack8b|stack8b_dq|stack8b_attn|sft8b|stack_qwen3b|layer8b|ce]
+                  [--workload stack8b|stack8b_dq|stack8b_attn|sft8b|stack_qwen3b|layer8b|attn8b|ce]
 
 Other workloads (not the headline line): the same 32-layer stack with the
 absmax double-quantised to 8 bits (the ~3.6 GB pinned store, 113 MB per
@@ -17,7 +17,8 @@ layer, that the pages quote); the same stack as full decoder layers (causal
 GQA attention with rotary positions over one 1024-token sequence, weighted
 RMS norms); one complete SFT step on those layers (embedding rows, the
 streamed stack, final norm, the 128256-entry head's chunked cross-entropy,
-backward); the 36-layer Qwen2.5-3B-shaped
+backward); one 8B layer's causal GQA attention alone (forward and
+backward, 8 sequences of 1024 tokens); the 36-layer Qwen2.5-3B-shaped
 stack with a bf16 base streamed at M=2048; one Llama-8B layer's seven NF4
 LoRA linears resident at M=2048 (fwd+bwd); the LM-head cross-entropy
 (M=2048, D=4096, V=128256).
@@ -57,6 +58,9 @@ WORKLOADS = {
                          name="qwen2.5-3b-shaped 36-layer bf16-base LoRA stack streamed from pinned host RAM"),
     "layer8b": dict(kind="layer", base="nf4", M=2048, D=4096, Dkv=1024, F=14336, r=16, alpha=32.0,
                     name="one llama-3.1-8b-shaped layer: seven NF4 LoRA linears resident, fwd+bwd"),
+    "attn8b": dict(kind="attn", M=8192, S=1024, H=32, Hkv=8, theta=500000.0,
+                   name="causal GQA attention of one llama-3.1-8b-shaped layer (32 query heads, 8 kv heads, rotary "
+                        "positions), forward + backward, 8 sequences of 1024 tokens"),
     "ce": dict(kind="ce", M=2048, D=4096, V=128256, chunk=8192,
                name="LM-head cross-entropy fwd+bwd, vocab-chunked (llama-3.1-8b head)"),
 }
@@ -208,6 +212,20 @@ def oracle_sample(w):
                 lora.lora_linear_fwd(xs[n], P[n]["W"], P[n]["A"], P[n]["B"], w["alpha"])
                 lora.lora_linear_bwd(xs[n], ys[n], P[n]["W"], P[n]["A"], P[n]["B"], w["alpha"])
         return step, ms, 1, f"the seven linears of one layer at {ms} tokens, fwd+bwd incl. dequantisation"
+    if w["kind"] == "attn":   # one sequence, 4 query heads over 1 kv head: 1/64 of the workload
+        from oracle import attention
+        S, hs = w["S"], 4
+        q = si.normal_bf16(61, (S, hs * 128), 1.0)
+        k = si.normal_bf16(62, (S, 128), 1.0)
+        v = si.normal_bf16(63, (S, 128), 1.0)
+        dO = si.normal_bf16(64, (S, hs * 128), 1.0)
+        scale = (w["M"] // S) * (w["H"] // hs)
+
+        def step():
+            o, _ = attention.attention_fwd(q, k, v, S)
+            attention.attention_bwd(q, k, v, o, dO, S)
+        return step, w["M"], scale, (f"one {S}-token sequence, {hs} query heads over 1 kv head, fwd+bwd "
+                                     f"(1/{scale} of the workload); tokens/s scaled by 1/{scale}")
     # cross-entropy: 16 rows against the whole vocabulary (loss terms and dH rows)
     rows = 16
     cc = si.ce_case(5, rows, w["D"], w["V"])
@@ -432,6 +450,39 @@ def run_ours(args):
         config = {"workload": w["name"], "tokens": M, "D": D, "Dkv": Dkv, "F": F, "rank": r, "alpha": alpha,
                   "base": "NF4 blocksize 64 fp32 absmax", "grouping": "q/k/v and gate/up as projection groups",
                   "l2": "inputs larger than L2 (~0.8 GB touched per step)"}
+    elif w["kind"] == "attn":
+        S, H, Hkv = w["S"], w["H"], w["Hkv"]
+        dominant = ("attn_fwd", "attn_bwd")
+        kname = "attn_fwd_kernel + attn_dq_kernel / attn_dkdv_kernel (tcgen05, causal GQA, rotary gradients)"
+        q, k, v = rnd((M, H * 128), 1.0), rnd((M, Hkv * 128), 1.0), rnd((M, Hkv * 128), 1.0)
+        dO = rnd((M, H * 128), 1.0)
+        o = torch.empty(M, H * 128, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(H, M, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        tab = torch.empty(S, 128, device=dev)
+        sl.sl_rope_table(S, w["theta"], tab)
+        aws = torch.empty(sl.sl_attention_workspace_size(M, H), dtype=torch.uint8, device=dev)
+
+        def step():
+            sl.sl_attention_fwd(q, k, v, S, o, lse)
+            sl.sl_attention_bwd(q, k, v, o, dO, lse, S, dq, dk, dv, rope_table=tab, ws=aws)
+
+        hosts = [t.cpu().pin_memory() for t in (q, k, v, dO)]
+        dq_h = torch.empty(8, H * 128, dtype=torch.bfloat16, pin_memory=True)
+
+        def e2e_step():
+            for t, th in zip((q, k, v, dO), hosts):
+                t.copy_(th, non_blocking=True)
+            step()
+            dq_h.copy_(dq[:8], non_blocking=True)
+        e2e_bytes = (sum(th.numel() * 2 for th in hosts), dq_h.numel() * 2)
+        pairs = (M // S) * H * S * (S + 1) / 2
+        # algorithmic work: 2 products forward, 5 backward (S recomputed once), 2 x 128 FLOPs each per
+        # visible pair; bytes: q, k, v, dO read, o written and read, dq, dk, dv written
+        extra["step_roofline_inputs"] = {"flops": 7 * 2.0 * 128 * pairs,
+                                         "bytes": 2.0 * (3 * M * H * 128 + 3 * M * Hkv * 128 + M * H * 128)}
+        config = {"workload": w["name"], "tokens": M, "seq_len": S, "heads": H, "kv_heads": Hkv,
+                  "rope_theta": w["theta"], "l2": "inputs larger than L2 (q, o, dO, dq 64 MB each)"}
     else:  # cross-entropy
         D, V, chunk = w["D"], w["V"], w["chunk"]
         dominant = ("ce_logits", "ce_dh")
@@ -599,7 +650,7 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0,
-                    help="timed steps (default: 10 for the stacks, 200 for layer8b, 50 for ce -- ~0.3-1.5 s)")
+                    help="timed steps (default: 10 for the stacks, 200 for layer8b, 100 for attn8b, 50 for ce)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="stack8b")
@@ -608,7 +659,7 @@ def main():
     ap.add_argument("--no-resident", action="store_true")
     args = ap.parse_args()
     if args.steps <= 0:
-        args.steps = {"layer8b": 200, "ce": 50}.get(args.workload, 10)
+        args.steps = {"layer8b": 200, "ce": 50, "attn8b": 100}.get(args.workload, 10)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

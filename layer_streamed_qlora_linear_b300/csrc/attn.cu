@@ -123,6 +123,7 @@ struct AttnArgs {
   float* lse;     // fwd output [H][M] (natural log); bwd input
   const float* Di;  // bwd: [H][M]
   const float* rope;  // bwd: table [S][128] or nullptr
+  int heads_per_cta;  // dK dV kernel: query heads summed inside one CTA (1, or H / Hkv: direct bf16 output)
   int* err;
 };
 
@@ -734,10 +735,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 }
 
 // ------------------------------------------------------------ dK, dV
-// One CTA per (128-key tile, query head, sequence): dK_h and dV_h of the
-// key tile accumulate in TMEM over the query blocks that see it and leave as
-// fp32 partials [H][M][128]; attn_kv_reduce_kernel sums the query heads of
-// each kv head in head order.
+// One CTA per (128-key tile, group of heads_per_cta query heads, sequence):
+// dK and dV of the key tile accumulate in TMEM over those heads' query blocks
+// that see it.  heads_per_cta = H / Hkv (enough CTAs to fill the GPU): the CTA
+// covers its kv head's query heads in head order and writes bf16 dk (scaled,
+// rotated back) and dv itself; heads_per_cta = 1: fp32 per-head partials
+// [H][M][128] that attn_kv_reduce_kernel sums in head order.
 struct DkvCfg {
   static constexpr int kOffK = 0;                    // [128][128]
   static constexpr int kOffV = kOffK + kAtTile;      // [128][128]
@@ -777,13 +780,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DkvCfg::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per = a.H * a.nseq;
+  const int hpc = a.heads_per_cta;
+  const int ngrp = a.H / hpc;
+  const int per = ngrp * a.nseq;
   const int kt = static_cast<int>(blockIdx.x) / per;  // key tile; heaviest (kt = 0) first
   const int hb = static_cast<int>(blockIdx.x) % per;
-  const int h = hb % a.H, b = hb / a.H;
-  const int g = h / (a.H / a.Hkv);
+  const int h0 = (hb % ngrp) * hpc, b = hb / ngrp;
+  const int g = h0 / (a.H / a.Hkv);
   const int key0 = b * a.S + kt * 128;
-  const int n = a.S / 64 - 2 * kt;  // query blocks of 64 that see this key tile
+  const int nqb = a.S / 64 - 2 * kt;  // query blocks of 64 that see this key tile
+  const int n = hpc * nqb;            // iterations: (query head, query block)
   const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
 
   if (threadIdx.x == 0) {
@@ -832,7 +838,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ok = false;
           break;
         }
-        const int qrow = b * a.S + (2 * kt + t) * 64;
+        const int h = h0 + t / nqb, qrow = b * a.S + (2 * kt + t % nqb) * 64;
         uint8_t* st = sStage + s * DkvCfg::kStage;
         ptx::mbar_arrive_expect_tx(&st_full[s], DkvCfg::kStageBytes);
         ptx::tma_load_2d(st, &map_q, &st_full[s], h * 128, qrow);
@@ -927,7 +933,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       const float* lse_s =
           reinterpret_cast<const float*>(sStage + (t % kKvStages) * DkvCfg::kStage + 4 * kAtAtom64) + half * 32;
       const float* di_s = lse_s + 64;
-      const int q0 = (2 * kt + t) * 64 + half * 32;
+      const int q0 = (2 * kt + t % nqb) * 64 + half * 32;
       uint32_t wp[16], wd[16];
       {
         uint32_t us[32], up[32];
@@ -966,10 +972,24 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ds_full[t & 1]);
     }
-    if (ok && n > 0 && wait_all(acc_full, 0)) {
+    const bool fin = ok && n > 0 && wait_all(acc_full, 0);
+    if (fin && hpc == a.H / a.Hkv) {
+      // every query head of the kv head is in: dV and dK of rotation pairs 32 half ..
       ptx::tc_fence_after();
-      // fp32 partials of this query head: row key0 + r, columns 64 half .. 64 half + 63
-      const int64_t row = static_cast<int64_t>(h) * M + key0 + r;
+      uint32_t lo[32], hi[32];
+      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(half * 32), lo);
+      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(64 + half * 32), hi);
+      ptx::tmem_wait_ld();
+      store_grad_pairs(lo, hi, 1.0f, nullptr, 0, half, a.out1 + static_cast<int64_t>(key0 + r) * a.ld1 + g * 128);
+      ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(half * 32), lo);
+      ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(64 + half * 32), hi);
+      ptx::tmem_wait_ld();
+      store_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, kpos, half,
+                       a.out0 + static_cast<int64_t>(key0 + r) * a.ld0 + g * 128);
+    } else if (fin) {
+      // fp32 partials of this query head, row key0 + r, columns 64 half ..
+      ptx::tc_fence_after();
+      const int64_t row = static_cast<int64_t>(h0) * M + key0 + r;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float* dst = (part ? part_dk : part_dv) + row * 128 + half * 64;
@@ -1237,9 +1257,19 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
     float* part_dk = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(Di) + di_bytes(sh.M, sh.H));
     float* part_dv = part_dk + static_cast<size_t>(sh.M) * sh.H * 128;
     if ((st = set_smem(attn_dkdv_kernel, DkvCfg::kSmem)) != SL_OK) return st;
-    const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.H * a.nseq);
-    attn_dkdv_kernel<<<grid, kAtThreads, DkvCfg::kSmem, stream>>>(mq, mdo, mk, mv, ml, md, a, part_dk, part_dv);
+    // a CTA per kv head when that alone fills the GPU or a kv head has one query
+    // head (no partials), else per query head
+    const bool direct = sh.H == sh.Hkv || (sh.S / 128) * sh.Hkv * a.nseq >= num_sms();
+    AttnArgs ak = a;
+    ak.heads_per_cta = direct ? sh.H / sh.Hkv : 1;
+    ak.out0 = dk;
+    ak.ld0 = lddk;
+    ak.out1 = dv;
+    ak.ld1 = lddv;
+    const unsigned grid = static_cast<unsigned>((sh.S / 128) * (sh.H / ak.heads_per_cta) * a.nseq);
+    attn_dkdv_kernel<<<grid, kAtThreads, DkvCfg::kSmem, stream>>>(mq, mdo, mk, mv, ml, md, ak, part_dk, part_dv);
     if ((st = check_launch("attn_dkdv_kernel")) != SL_OK) return st;
+    if (direct) return SL_OK;
     const int64_t nt = sh.M * sh.Hkv * 8;
     attn_kv_reduce_kernel<<<static_cast<unsigned>((nt + 255) / 256), 256, 0, stream>>>(
         part_dk, part_dv, sh.M, static_cast<int>(sh.S), sh.H, sh.Hkv, rope, 0.08838834764831845f, dk, lddk, dv,

@@ -51,6 +51,8 @@ CASES = [
     (768, 384, 4, 1),
     (512, 256, 2, 2),
     (512, 512, 32, 8),
+    # 16 sequences: (S/128) Hkv nseq = 256 CTAs fill the GPU, so dK/dV sum their kv head's query heads in-CTA
+    (4096, 256, 16, 8),
 ]
 
 
@@ -105,9 +107,11 @@ def test_attention_first_rows_and_determinism(gpu_lib):
             np.testing.assert_array_equal(o[t, h * 128:(h + 1) * 128], v[t, g * 128:(g + 1) * 128])
 
 
-def test_attention_bwd_rotates_gradients_back(gpu_lib):
-    """With the rotary table, dq and dk leave as the gradients of the unrotated q and k."""
-    M, S, H, Hkv, theta = 512, 256, 4, 2, 500000.0
+@pytest.mark.parametrize("M,S,H,Hkv", [(512, 256, 4, 2), (4096, 256, 16, 8)])
+def test_attention_bwd_rotates_gradients_back(gpu_lib, M, S, H, Hkv):
+    """With the rotary table, dq and dk leave as the gradients of the unrotated q and k
+    (per-query-head partials and the in-CTA head sum)."""
+    theta = 500000.0
     (q, k, v, dO), (o, lse, dq, dk, dv) = run_attention(gpu_lib, M, S, H, Hkv, seed=13, rope=table(gpu_lib, S, theta))
     o_ref, _ = at.attention_fwd(q, k, v, S)
     dq_ref, dk_ref, dv_ref = at.attention_bwd(q, k, v, o_ref, dO, S)
