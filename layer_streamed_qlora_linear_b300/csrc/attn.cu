@@ -52,9 +52,17 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// 16-byte chunk c (0..7) of row `row` of a 128-byte-swizzled atom.
-__device__ __forceinline__ uint4* swz(uint8_t* atom, int row, int c) {
-  return reinterpret_cast<uint4*>(atom + row * 128 + ((c ^ (row & 7)) << 4));
+// Store 16 bytes at chunk c (0..7) of row `row` of a 128-byte-swizzled atom
+// at shared address `atom` (st.shared: the address space is explicit).
+__device__ __forceinline__ void sts_swz(uint32_t atom, int row, int c, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(atom + row * 128 + ((c ^ (row & 7)) << 4)), "r"(x),
+               "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
 }
 
 // Shared-memory descriptors of SW128 operands, built once per buffer and
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       alpha_prev = alpha;
       // P = exp2(S c - m_new) as bf16 into this half's atom of the P tile
       float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      uint8_t* atom = sP + half * kAtAtom128;
+      const uint32_t atom = ptx::smem_addr(sP) + half * kAtAtom128;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
@@ -403,7 +411,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-          *swz(atom, r, c * 4 + q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+          sts_swz(atom, r, c * 4 + q4, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       }
       l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       m = m_new;
@@ -443,21 +451,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 }
 
 // ------------------------------------------------------------ Di pre-pass
-// Di[h][row] = sum_d dO[row, h*128 + d] * O[row, h*128 + d]; one warp per (row, head).
+// Di[h][row] = sum_d dO[row, h*128 + d] * O[row, h*128 + d]: half a warp per
+// (row, head), 16-byte loads (8 elements per lane), a 16-lane shuffle sum.
 __global__ void attn_di_kernel(const uint16_t* __restrict__ o, int64_t ldo, const uint16_t* __restrict__ dout,
                                int64_t lddo, int64_t M, int H, float* __restrict__ Di) {
-  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= M * H) return;
-  const int64_t row = w / H;
-  const int h = static_cast<int>(w % H);
-  const uint2 ov = *reinterpret_cast<const uint2*>(o + row * ldo + h * 128 + lane * 4);
-  const uint2 dv = *reinterpret_cast<const uint2*>(dout + row * lddo + h * 128 + lane * 4);
-  float s = bf_lo(ov.x) * bf_lo(dv.x) + bf_hi(ov.x) * bf_hi(dv.x) + bf_lo(ov.y) * bf_lo(dv.y) +
-            bf_hi(ov.y) * bf_hi(dv.y);
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int lane = threadIdx.x & 15;
+  const bool valid = w < M * H;
+  const int64_t row = valid ? w / H : 0;
+  const int h = valid ? static_cast<int>(w % H) : 0;
+  float s = 0.0f;
+  if (valid) {
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + row * ldo + h * 128 + lane * 8);
+    const uint4 dv = *reinterpret_cast<const uint4*>(dout + row * lddo + h * 128 + lane * 8);
+    const uint32_t a[4] = {ov.x, ov.y, ov.z, ov.w}, b[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-  for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) Di[static_cast<int64_t>(h) * M + row] = s;
+    for (int e = 0; e < 4; ++e) s += bf_lo(a[e]) * bf_lo(b[e]) + bf_hi(a[e]) * bf_hi(b[e]);
+  }
+#pragma unroll
+  for (int off = 8; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (valid && lane == 0) Di[static_cast<int64_t>(h) * M + row] = s;
 }
 
 // Rotation pairs 32 half .. 32 half + 31 of one 128-wide gradient row: lo
@@ -707,10 +720,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ok = false;
         break;
       }
-      uint8_t* ds_buf = sDS + (j & 1) * kAtAtom128;
+      const uint32_t ds_buf = ptx::smem_addr(sDS) + (j & 1) * kAtAtom128;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
-        *swz(ds_buf, r, half * 4 + q4) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        sts_swz(ds_buf, r, half * 4 + q4, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
@@ -930,9 +943,21 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      const float* lse_s =
-          reinterpret_cast<const float*>(sStage + (t % kKvStages) * DkvCfg::kStage + 4 * kAtAtom64) + half * 32;
-      const float* di_s = lse_s + 64;
+      // this half's 32 query rows: lse (scaled to log2) and Di, from the stage's shared copy
+      const uint32_t ls_addr = ptx::smem_addr(sStage) + (t % kKvStages) * DkvCfg::kStage + 4 * kAtAtom64 + half * 128;
+      float lse2[32], dis[32];
+#pragma unroll
+      for (int v4 = 0; v4 < 8; ++v4) {
+        const float4 lv = lds128(ls_addr + v4 * 16), dv4 = lds128(ls_addr + 256 + v4 * 16);
+        lse2[4 * v4] = lv.x * kLog2e;
+        lse2[4 * v4 + 1] = lv.y * kLog2e;
+        lse2[4 * v4 + 2] = lv.z * kLog2e;
+        lse2[4 * v4 + 3] = lv.w * kLog2e;
+        dis[4 * v4] = dv4.x;
+        dis[4 * v4 + 1] = dv4.y;
+        dis[4 * v4 + 2] = dv4.z;
+        dis[4 * v4 + 3] = dv4.w;
+      }
       const int q0 = (2 * kt + t % nqb) * 64 + half * 32;
       uint32_t wp[16], wd[16];
       {
@@ -947,9 +972,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           for (int u = 0; u < 2; ++u) {
             const int qi = e + u;
             const float p =
-                (q0 + qi >= kpos) ? ex2(fmaf(__uint_as_float(us[qi]), a.c, -lse_s[qi] * kLog2e)) : 0.0f;
+                (q0 + qi >= kpos) ? ex2(fmaf(__uint_as_float(us[qi]), a.c, -lse2[qi])) : 0.0f;
             p2[u] = p;
-            d2[u] = p * (__uint_as_float(up[qi]) - di_s[qi]);
+            d2[u] = p * (__uint_as_float(up[qi]) - dis[qi]);
           }
           wp[e / 2] = pack2(p2[0], p2[1]);
           wd[e / 2] = pack2(d2[0], d2[1]);
@@ -960,12 +985,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ok = false;
         break;
       }
-      uint8_t* pt_buf = sPT + (t & 1) * kAtAtom128;
-      uint8_t* dst_buf = sDST + (t & 1) * kAtAtom128;
+      const uint32_t pt_buf = ptx::smem_addr(sPT) + (t & 1) * kAtAtom128;
+      const uint32_t dst_buf = ptx::smem_addr(sDST) + (t & 1) * kAtAtom128;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        *swz(pt_buf, r, half * 4 + q4) = make_uint4(wp[4 * q4], wp[4 * q4 + 1], wp[4 * q4 + 2], wp[4 * q4 + 3]);
-        *swz(dst_buf, r, half * 4 + q4) = make_uint4(wd[4 * q4], wd[4 * q4 + 1], wd[4 * q4 + 2], wd[4 * q4 + 3]);
+        sts_swz(pt_buf, r, half * 4 + q4, wp[4 * q4], wp[4 * q4 + 1], wp[4 * q4 + 2], wp[4 * q4 + 3]);
+        sts_swz(dst_buf, r, half * 4 + q4, wd[4 * q4], wd[4 * q4 + 1], wd[4 * q4 + 2], wd[4 * q4 + 3]);
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -1184,9 +1209,9 @@ sl_status attention_bwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, con
   SL_REQUIRE(o && dout && lse && ws && dq && dk && dv, "attention_bwd: null argument");
   SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 15) == 0 && (reinterpret_cast<uintptr_t>(lse) & 15) == 0,
              "attention_bwd: lse and workspace must be 16-byte aligned");
-  SL_REQUIRE(ldo % 4 == 0 && lddo % 4 == 0 && (reinterpret_cast<uintptr_t>(o) & 7) == 0 &&
-                 (reinterpret_cast<uintptr_t>(dout) & 7) == 0,
-             "attention_bwd: o and do rows must be 8-byte aligned");
+  SL_REQUIRE(ldo % 8 == 0 && lddo % 8 == 0 && (reinterpret_cast<uintptr_t>(o) & 15) == 0 &&
+                 (reinterpret_cast<uintptr_t>(dout) & 15) == 0,
+             "attention_bwd: o and do rows must be 16-byte aligned");
   for (auto pr : {std::make_pair(static_cast<const void*>(dq), lddq), std::make_pair(static_cast<const void*>(dk), lddk),
                   std::make_pair(static_cast<const void*>(dv), lddv)})
     SL_REQUIRE((reinterpret_cast<uintptr_t>(pr.first) & 15) == 0 && pr.second % 8 == 0,
@@ -1209,9 +1234,9 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
                                       const float* rope, float* Di, int* err, cudaStream_t stream) {
   sl_status st;
   {
-    const int64_t warps = sh.M * sh.H;
-    attn_di_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, stream>>>(o, ldo, dout, lddo, sh.M,
-                                                                                        sh.H, Di);
+    const int64_t threads = sh.M * sh.H * 16;
+    attn_di_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(o, ldo, dout, lddo, sh.M, sh.H,
+                                                                                     Di);
     if ((st = check_launch("attn_di_kernel")) != SL_OK) return st;
   }
   AttnArgs a{};
