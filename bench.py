@@ -74,6 +74,29 @@ def load_peaks():
         return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+def rank_barrier(world):
+    """All replicas meet (no-op for one process)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks_of(x, world, device):
+    """The largest x over all replicas (the timing rule: the slowest rank's time counts)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds_max):
+    """Units all replicas processed per second of the slowest replica (weak scaling)."""
+    return world * units_per_rank / seconds_max
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
@@ -519,18 +542,11 @@ def run_ours(args):
 
     def barrier():
         torch.cuda.synchronize()
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        rank_barrier(world)
         torch.cuda.synchronize()
 
     def max_over_ranks(x):
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([x], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return x
+        return max_over_ranks_of(x, world, dev)
 
     # timed region: K steps, CUDA events on the compute stream
     clocks = ClockSampler(local)
@@ -547,7 +563,7 @@ def run_ours(args):
     launches_timed = sl.sl_launch_count() - launches0
     ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / args.steps
-    value = world * M * args.steps / (ms_total * 1e-3)
+    value = whole_job_rate(M * args.steps, world, ms_total * 1e-3)
     h2d_step = kernels_step = None
     if w["kind"] == "stack":
         h2d_step, kernels_step = stk.last_step_stats()
@@ -572,7 +588,7 @@ def run_ours(args):
         e2e_step()
     barrier()
     e2e_s = max_over_ranks(time.perf_counter() - t0)
-    e2e = {"value": world * M * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(e2e_bytes[0]),
+    e2e = {"value": whole_job_rate(M * args.steps, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": int(e2e_bytes[0]),
            "d2h_bytes_per_step": int(e2e_bytes[1])}
 
     n_d = sum(timing[k][0] for k in dominant)
