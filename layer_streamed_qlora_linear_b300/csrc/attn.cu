@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = ptx::align1024(smem_raw);
   uint8_t* sQ = smem + FwdCfg::kOffQ;
   uint8_t* sK = smem + FwdCfg::kOffK;
   uint8_t* sV = smem + FwdCfg::kOffV;
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                    const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = ptx::align1024(smem_raw);
   uint8_t* sQ = smem + DqCfg::kOffQ;
   uint8_t* sDO = smem + DqCfg::kOffDO;
   uint8_t* sK = smem + DqCfg::kOffK;
@@ -774,7 +774,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                      const __grid_constant__ CUtensorMap map_lse, const __grid_constant__ CUtensorMap map_di,
                      const AttnArgs a, float* __restrict__ part_dk, float* __restrict__ part_dv) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = ptx::align1024(smem_raw);
   uint8_t* sK = smem + DkvCfg::kOffK;
   uint8_t* sV = smem + DkvCfg::kOffV;
   uint8_t* sStage = smem + DkvCfg::kOffStage;

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   using Cfg = GemmCfg<BSRC>;
   constexpr int S = Cfg::S;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = ptx::align1024(smem_raw);
   uint8_t* sA = smem + Cfg::kOffA;
   uint8_t* sB = smem + Cfg::kOffB;
   uint8_t* sRaw = smem + Cfg::kOffRaw;

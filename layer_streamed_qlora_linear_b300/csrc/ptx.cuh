@@ -14,6 +14,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte-aligned byte of a dynamic shared-memory array, as an
+// offset from the array itself: the pointer stays visibly shared, so the
+// accesses through it compile to shared-memory loads and stores rather than
+// generic ones.
+__device__ __forceinline__ uint8_t* align1024(uint8_t* smem_raw) {
+  return smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");

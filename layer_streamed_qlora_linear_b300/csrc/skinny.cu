@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w,
                   const SkArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = ptx::align1024(smem_raw);
   const int r = a.r;
   const int S = a.stages;
   const int step = a.step;
