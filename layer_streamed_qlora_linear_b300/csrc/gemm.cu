@@ -113,7 +113,7 @@ static sl_status run_pair(const CUtensorMap& ma, const CUtensorMap& mc, const CU
 // CTA pairs of the persistent kernel that the device holds at once (driver
 // query, once per device); the grid never exceeds it, so all clusters run
 // together and none waits for a second wave.
-template <int BMN>
+template <int BMN, int SMALL>
 static int pair_clusters_resident() {
   static std::mutex mu;
   static int cached[64] = {0};
@@ -121,14 +121,15 @@ static int pair_clusters_resident() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms() / 2;
   std::lock_guard<std::mutex> lk(mu);
   if (cached[dev] == 0) {
-    cudaFuncSetAttribute(gemm_nf4_pair_persistent_kernel<BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Gemm3Cfg::kSmem);
+    cudaFuncSetAttribute(gemm_nf4_pair_persistent_kernel<BMN, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Gemm3Cfg<SMALL>::kSmem);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kGemm3Threads, 1, 1);
-    cfg.dynamicSmemBytes = Gemm3Cfg::kSmem;
+    cfg.dynamicSmemBytes = Gemm3Cfg<SMALL>::kSmem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_nf4_pair_persistent_kernel<BMN>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_nf4_pair_persistent_kernel<BMN, SMALL>, &cfg) != cudaSuccess ||
+        n <= 0) {
       cudaGetLastError();
       n = num_sms() / 2;
     }
@@ -139,20 +140,21 @@ static int pair_clusters_resident() {
 
 // Persistent NF4 GEMM on CTA pairs: one cluster per SM pair walks its share
 // of the pair tiles.
-template <int BMN>
+template <int BMN, int SMALL>
 static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, const CUtensorMap& ms,
                                 const CUtensorMap& ms2, const GemmArgs& a, cudaStream_t stream) {
-  auto kern = gemm_nf4_pair_persistent_kernel<BMN>;
+  auto kern = gemm_nf4_pair_persistent_kernel<BMN, SMALL>;
   static bool attr_set[64] = {false};
   int dev = 0;
   SL_CHECK_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    SL_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gemm3Cfg::kSmem));
+    SL_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gemm3Cfg<SMALL>::kSmem));
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int ntiles = ceil_div(a.M, 256) * ceil_div(a.N, kBN);
-  const int nclusters = std::min(ntiles, pair_clusters_resident<BMN>());
-  kern<<<dim3(static_cast<unsigned>(2 * nclusters)), kGemm3Threads, Gemm3Cfg::kSmem, stream>>>(ma, mc, ms, ms2, a);
+  const int nclusters = std::min(ntiles, pair_clusters_resident<BMN, SMALL>());
+  kern<<<dim3(static_cast<unsigned>(2 * nclusters)), kGemm3Threads, Gemm3Cfg<SMALL>::kSmem, stream>>>(ma, mc, ms,
+                                                                                                      ms2, a);
   return check_launch("gemm_nf4_pair_persistent_kernel");
 }
 
@@ -258,9 +260,12 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   // epilogue overlaps the next tile); one wave or less: one cluster per tile
   // with the epilogue spread over all eight dequant warps.
   const bool persistent = pair && (g.grouped || a.dq || ceil_div(a.M, 256) * ceil_div(a.N, kBN) >
-                                                    (g.bmn ? pair_clusters_resident<1>() : pair_clusters_resident<0>()));
-  if (persistent)
-    st = g.bmn ? run_persistent<1>(ma, mb, ms, ms2, a, stream) : run_persistent<0>(ma, mb, ms, ms2, a, stream);
+                                                    (g.bmn ? pair_clusters_resident<1, 1>() : pair_clusters_resident<0, 1>()));
+  // folded rank <= 32: the five-stage variant; above (a group's dX): four stages
+  if (persistent && a.r <= 32)
+    st = g.bmn ? run_persistent<1, 1>(ma, mb, ms, ms2, a, stream) : run_persistent<0, 1>(ma, mb, ms, ms2, a, stream);
+  else if (persistent)
+    st = g.bmn ? run_persistent<1, 0>(ma, mb, ms, ms2, a, stream) : run_persistent<0, 0>(ma, mb, ms, ms2, a, stream);
   else
     st = pair ? (g.bmn ? run_pair<1>(ma, mb, ms, a, stream) : run_pair<0>(ma, mb, ms, a, stream))
               : dispatch(g, ma, mb, ms, stream);

@@ -28,14 +28,21 @@ constexpr int kGemm3Threads = 64 + kNumDq2 + kNumEpi3;
 constexpr int kLoraMaxR = 64;               // folded rank: K of the fold up to 2 * 64
 constexpr int kLoraAtom = 128 * 128;         // one 128-row x 128-byte SW128 atom
 
+// SMALL = 1: folded rank at most 32 (2R <= 64 K columns): the LoRA operands
+// take one atom each (32 KB), which leaves room for a fifth pipeline stage;
+// SMALL = 0: folded rank up to 64 (a projection group's dX), four stages.
+template <int SMALL>
 struct Gemm3Cfg {
-  static constexpr int S = 4;
+  static constexpr int S = SMALL ? 5 : 4;
+  static constexpr int kLA = SMALL ? 1 : 2;                       // Xe atoms (64 K columns each)
+  static constexpr int kLBAtomMN = SMALL ? 64 * 128 : kLoraAtom;  // MN-major Be atom: 2R rows of 128 bytes
+  static constexpr int kLBBytes = SMALL ? kLoraAtom : 2 * kLoraAtom;
   static constexpr int kRawBytes = kHalfCodesBytes + kPairAbsBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + S * kATileBytes;
-  static constexpr int kOffLA = kOffB + S * kHalfBTileBytes;     // LoRA Xe: K-major [128 rows x 2R], two atoms
-  static constexpr int kOffLB = kOffLA + 2 * kLoraAtom;          // LoRA Be: K-major [128 x 2r] / MN-major 2 atoms of [2R x 64]
-  static constexpr int kOffRaw = kOffLB + 2 * kLoraAtom;
+  static constexpr int kOffLA = kOffB + S * kHalfBTileBytes;     // LoRA Xe: K-major [128 rows x 2R], kLA atoms
+  static constexpr int kOffLB = kOffLA + kLA * kLoraAtom;        // LoRA Be: K-major [128 x 2r] / MN-major 2 atoms of [2R x 64]
+  static constexpr int kOffRaw = kOffLB + kLBBytes;
   static constexpr int kOffBar = kOffRaw + S * kRawBytes;
   static constexpr int kNumBars = 5 * S + 7;
   static constexpr int kOffSink = (kOffBar + kNumBars * 8 + 15) / 16 * 16;
@@ -43,16 +50,17 @@ struct Gemm3Cfg {
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmem = kBytes + 1024;
 };
+static_assert(Gemm3Cfg<0>::kSmem <= 232448 && Gemm3Cfg<1>::kSmem <= 232448, "persistent GEMM shared memory");
 
 // Barrier of the four epilogue warps only (named barrier 1).
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kNumEpi3) : "memory"); }
 
-template <int BMN>
+template <int BMN, int SMALL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     gemm_nf4_pair_persistent_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
                                     const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_s2,
                                     const GemmArgs args) {
-  using Cfg = Gemm3Cfg;
+  using Cfg = Gemm3Cfg<SMALL>;
   constexpr int S = Cfg::S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = ptx::align1024(smem_raw);
@@ -236,7 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           ptx::tc_fence_after();
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint64_t ad = ptx::smem_desc(la + (kk >> 2) * kLoraAtom + (kk & 3) * 32, 16, 1024, 2);
-            const uint64_t bd = BMN ? ptx::smem_desc(lb + kk * 2048, kLoraAtom, 1024, 2)
+            const uint64_t bd = BMN ? ptx::smem_desc(lb + kk * 2048, Cfg::kLBAtomMN, 1024, 2)
                                     : ptx::smem_desc(lb + kk * 32, 16, 1024, 2);
             ptx::mma_bf16_pair(d, ad, bd, idesc, 1u);
           }
@@ -325,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       return reinterpret_cast<uint4*>(base + rw * 128 + ((c ^ (rw & 7)) << 4));
     };
     auto mn_chunk = [&](uint8_t* bt, int i, int cc) {  // cc: 0..15 over two 64-column atoms of 128 rows
-      return reinterpret_cast<uint4*>(bt + (cc >> 3) * kLoraAtom + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
+      return reinterpret_cast<uint4*>(bt + (cc >> 3) * Cfg::kLBAtomMN + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
     };
     auto xe_chunk = [&](int rw, int c) {  // 16-byte chunk c (8 elements of K) of Xe row rw, two atoms
       return reinterpret_cast<uint4*>(sLA + (c >> 3) * kLoraAtom + rw * 128 + (((c & 7) ^ (rw & 7)) << 4));
