@@ -595,11 +595,20 @@ def run_ours(args):
     ms_d = sum(timing[k][1] for k in dominant)
     fl_d = sum(timing[k][2] for k in dominant)
     achieved = fl_d / (ms_d * 1e-3) / 1e12 if ms_d > 0 else 0.0
+    # DRAM bytes per launch of the dominant kernel from an ncu capture of the same kernels (one full
+    # step of a 4-layer stack: the per-layer launch mix of the 32-layer workload); null elsewhere
+    traffic, traffic_note = None, None
+    if w["kind"] == "stack" and w["base"] == "nf4" and w["D"] == 4096 and w["M"] == 1024:
+        traffic = 51.7e6
+        traffic_note = {"unit": "bytes per launch", "algorithmic_read_bytes_per_launch": 48.5e6,
+                        "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the 32 NF4 GEMM launches "
+                                  "of one step of the 4-layer stack (profiles/ncu_nf4_gemm_dram_traffic_stack4_m1024.md)"}
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
     roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
-                "traffic": None, "launches": n_d, "avg_launch_ms": ms_d / max(1, n_d),
+                "traffic": traffic, "traffic_note": traffic_note, "launches": n_d,
+                "avg_launch_ms": ms_d / max(1, n_d),
                 "share_of_step": ms_d / ms_instr,
                 "timing": "per-launch CUDA event pairs (libsl, on the launching stream) over a second timed "
                           "region of the same K steps"}
