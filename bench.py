@@ -163,6 +163,17 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def _threads():
     try:
         from threadpoolctl import threadpool_info
@@ -266,7 +277,7 @@ def cpu_baseline(w):
     t0 = time.perf_counter()
     step()
     dt = time.perf_counter() - t0
-    return {"value": ms / (scale * dt), "unit": UNIT, "cores": _threads(), "kind": "oracle",
+    return {"value": ms / (scale * dt), "unit": UNIT, "cores": _threads(), "cpu_model": _cpu_model(), "kind": "oracle",
             "sample": f"{desc}; {dt:.2f} s per sample"}
 
 
@@ -287,7 +298,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": w["M"] / v * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w["name"], "tokens": w["M"], "sample": desc},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _threads(), "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _threads(), "cpu_model": _cpu_model(), "kind": "oracle",
+                             "sample": desc},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
