@@ -53,6 +53,8 @@ CASES = [
     (512, 512, 32, 8),
     # 16 sequences: (S/128) Hkv nseq = 256 CTAs fill the GPU, so dK/dV sum their kv head's query heads in-CTA
     (4096, 256, 16, 8),
+    # one 2048-token sequence: 16 query tiles, the longest causal loops
+    (2048, 2048, 4, 1),
 ]
 
 

@@ -357,3 +357,37 @@ def test_sft_step_matches_oracle_and_resident(gpu_lib):
     for x, y in zip(dA + dB, dA_r + dB_r):
         assert same_bits(x, y)
     S.stack.close()
+
+
+def test_sft_step_on_double_quantised_per_projection_stack(gpu_lib):
+    """The SFT step on an 8-bit-absmax stack with separately allocated adapters
+    (every projection its own GEMM): oracle parity and streamed == resident."""
+    sl = gpu_lib
+    M, D, Dkv, F, V, r, alpha = 256, 512, 256, 768, 1024, 8, 16.0
+    S = Setup(sl, sl.SL_WEIGHT_NF4_DQ, L=2, M=M, D=D, Dkv=Dkv, F=F, r=r, alpha=alpha, seed=47, packed=False,
+              attn=(256, 10000.0), norms=True)
+    c = si.sft_case(9, M, D, V)
+    tok, lab = torch.from_numpy(c["tokens"]).cuda(), torch.from_numpy(c["labels"]).cuda()
+    emb, head = dev_bf16(c["embed"]), dev_bf16(c["head"])
+    nf = torch.from_numpy(c["norm_final"]).cuda()
+    ws = torch.empty(S.stack.sft_workspace_size(M, r, V, 256), dtype=torch.uint8, device="cuda")
+    outs = []
+    for mode in (sl.SL_MODE_STREAMED, sl.SL_MODE_RESIDENT):
+        loss = torch.empty(1, device="cuda")
+        dA, dB = S.grads()
+        S.stack.sft_step(mode, tok, lab, emb, nf, head, 256, S.A, S.B, r, alpha, loss, dA, dB, ws)
+        sl.sl_check_device_errors()
+        outs.append((loss, dA, dB))
+    oloss, _, ograds = stack.sft_step(c["tokens"], c["labels"], c["embed"].astype(np.float64), S.ref_layers,
+                                      c["norm_final"].astype(np.float64), c["head"].astype(np.float64), alpha,
+                                      rnd=True, attn=S.attn)
+    loss, dA, dB = outs[0]
+    assert abs(loss.item() - oloss) <= LOSS_TOL * abs(oloss)
+    for l in range(S.L):
+        for p, n in enumerate(si.PROJ_NAMES):
+            assert rel_fro(host(dA[7 * l + p]), ograds[l][n][0]) <= BF16_TOL, (l, n)
+            assert rel_fro(host(dB[7 * l + p]), ograds[l][n][1]) <= BF16_TOL, (l, n)
+    assert same_bits(outs[0][0], outs[1][0])
+    for x, y in zip(outs[0][1] + outs[0][2], outs[1][1] + outs[1][2]):
+        assert same_bits(x, y)
+    S.stack.close()
