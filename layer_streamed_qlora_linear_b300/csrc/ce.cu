@@ -63,6 +63,8 @@ __global__ void ce_chunk_kernel(const float* __restrict__ pmax, const float* __r
                                 int part_ld, int ncols, int64_t M, uint16_t* __restrict__ P, int ldp,
                                 float* __restrict__ run_max, float* __restrict__ run_sum, float* __restrict__ alpha,
                                 int first) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -102,6 +104,8 @@ __global__ void ce_chunk_kernel(const float* __restrict__ pmax, const float* __r
 __global__ void ce_row_kernel(const float* __restrict__ run_max, const float* __restrict__ run_sum,
                               const float* __restrict__ zlab, const int32_t* __restrict__ labels, int ignore, int V,
                               int64_t M, float* __restrict__ lse, float* __restrict__ term, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (row >= M) return;
   const float l = run_max[row] + logf(run_sum[row]);
@@ -116,6 +120,8 @@ __global__ void ce_row_kernel(const float* __restrict__ run_max, const float* __
 __global__ void __launch_bounds__(1024) ce_finalize_kernel(const int32_t* __restrict__ labels, int ignore, int V,
                                                            const float* __restrict__ term, int64_t M,
                                                            float* __restrict__ loss, float* __restrict__ scale) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s_sum[32];
   __shared__ int s_cnt[32];
   float acc = 0.0f;
@@ -159,6 +165,8 @@ __global__ void __launch_bounds__(1024) ce_finalize_kernel(const int32_t* __rest
 __global__ void ce_final_kernel(float* __restrict__ dH, const uint16_t* __restrict__ W,
                                 const int32_t* __restrict__ labels, const float* __restrict__ scale,
                                 const float* __restrict__ run_sum, int ignore, int V, int D) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   const int lab = labels[row];
   const bool valid = lab != ignore && lab >= 0 && lab < V;
@@ -242,10 +250,9 @@ sl_status ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W, int64_t
     if (st != SL_OK) return st;
     // running (max, sum); P rescaled to the running max; alpha for dH
     const int halves_c = static_cast<int>(ceil_div(vc, kBN)) * 2;
-    ce_chunk_kernel<<<static_cast<unsigned>(ceil_div(M * 32, 256)), 256, 0, stream>>>(
-        pmax, psum, halves_c, P.halves, static_cast<int>(vc), M, Pc, static_cast<int>(chunk_V), run_max, run_sum,
-        alpha, v0 == 0 ? 1 : 0);
-    st = check_launch("ce_chunk_kernel");
+    st = launch_pdl("ce_chunk_kernel", ce_chunk_kernel, dim3(static_cast<unsigned>(ceil_div(M * 32, 256))), dim3(256),
+                    0, stream, pmax, psum, halves_c, P.halves, static_cast<int>(vc), M, Pc, static_cast<int>(chunk_V),
+                    run_max, run_sum, alpha, v0 == 0 ? 1 : 0);
     if (st != SL_OK) return st;
     // dH accumulator = alpha * dH accumulator + P W_c
     GemmLaunch h{};
@@ -267,16 +274,14 @@ sl_status ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W, int64_t
     st = launch_gemm(h, stream);
     if (st != SL_OK) return st;
   }
-  ce_row_kernel<<<static_cast<unsigned>(ceil_div(M, 256)), 256, 0, stream>>>(run_max, run_sum, zlab, labels, ignore,
-                                                                            static_cast<int>(V), M, lse, term, err);
-  st = check_launch("ce_row_kernel");
+  st = launch_pdl("ce_row_kernel", ce_row_kernel, dim3(static_cast<unsigned>(ceil_div(M, 256))), dim3(256), 0, stream,
+                  run_max, run_sum, zlab, labels, ignore, static_cast<int>(V), M, lse, term, err);
   if (st != SL_OK) return st;
-  ce_finalize_kernel<<<1, 1024, 0, stream>>>(labels, ignore, static_cast<int>(V), term, M, loss, scale);
-  st = check_launch("ce_finalize_kernel");
+  st = launch_pdl("ce_finalize_kernel", ce_finalize_kernel, dim3(1), dim3(1024), 0, stream, labels, ignore,
+                  static_cast<int>(V), term, M, loss, scale);
   if (st != SL_OK) return st;
-  ce_final_kernel<<<static_cast<unsigned>(M), 256, 0, stream>>>(dH, Wh, labels, scale, run_sum, ignore,
-                                                               static_cast<int>(V), static_cast<int>(D));
-  return check_launch("ce_final_kernel");
+  return launch_pdl("ce_final_kernel", ce_final_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, stream, dH, Wh,
+                    labels, scale, run_sum, ignore, static_cast<int>(V), static_cast<int>(D));
 }
 
 }  // namespace sl

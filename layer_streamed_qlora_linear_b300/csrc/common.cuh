@@ -31,6 +31,35 @@ sl_status cuda_error(cudaError_t e, const char* what);
 sl_status check_launch(const char* what);
 uint64_t launch_count();  // libsl kernel launches so far (all threads)
 
+// Programmatic dependent launch.  The training step's kernels are launched
+// with programmatic stream serialisation: the next kernel in the stream may
+// start while this one runs.  Every such kernel calls pdl_trigger() (its
+// dependents may launch once every CTA of it has started, so waiting CTAs
+// never hold resources its own CTAs need) and then pdl_wait() before its
+// first global-memory access (returns once the previous kernel has completed
+// and its writes are visible).  Both are no-ops under a normal launch.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialisation (see above), then check_launch.
+template <typename... KArgs, typename... Args>
+sl_status launch_pdl(const char* what, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) return cuda_error(e, what);
+  return check_launch(what);
+}
+
 // ------------------------------------------------------ device error word
 // One int per device, allocated on first use, read and cleared by
 // sl_check_device_errors().  Kernels whose bounded waits give up write a

@@ -106,8 +106,7 @@ static sl_status run_pair(const CUtensorMap& ma, const CUtensorMap& mc, const CU
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   dim3 grid(static_cast<unsigned>(2 * ceil_div(a.M, 256)), static_cast<unsigned>(ceil_div(a.N, kBN)));
-  kern<<<grid, kGemm2Threads, Gemm2Cfg::kSmem, stream>>>(ma, mc, ms, a);
-  return check_launch("gemm_nf4_pair_kernel");
+  return launch_pdl("gemm_nf4_pair_kernel", kern, grid, dim3(kGemm2Threads), Gemm2Cfg::kSmem, stream, ma, mc, ms, a);
 }
 
 // CTA pairs of the persistent kernel that the device holds at once (driver
@@ -153,9 +152,8 @@ static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, co
   }
   const int ntiles = ceil_div(a.M, 256) * ceil_div(a.N, kBN);
   const int nclusters = std::min(ntiles, pair_clusters_resident<BMN, SMALL>());
-  kern<<<dim3(static_cast<unsigned>(2 * nclusters)), kGemm3Threads, Gemm3Cfg<SMALL>::kSmem, stream>>>(ma, mc, ms,
-                                                                                                      ms2, a);
-  return check_launch("gemm_nf4_pair_persistent_kernel");
+  return launch_pdl("gemm_nf4_pair_persistent_kernel", kern, dim3(static_cast<unsigned>(2 * nclusters)),
+                    dim3(kGemm3Threads), Gemm3Cfg<SMALL>::kSmem, stream, ma, mc, ms, ms2, a);
 }
 
 template <int BSRC, int BMN, int EPI>
@@ -171,8 +169,7 @@ static sl_status run(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   dim3 grid(static_cast<unsigned>(ceil_div(a.N, kBN)), static_cast<unsigned>(ceil_div(a.M, kBM)));
-  kern<<<grid, kGemmThreads, Cfg::kSmem, stream>>>(ma, mb, ms, a);
-  return check_launch("gemm_tc_kernel");
+  return launch_pdl("gemm_tc_kernel", kern, grid, dim3(kGemmThreads), Cfg::kSmem, stream, ma, mb, ms, a);
 }
 
 sl_status dispatch(const GemmLaunch& g, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms,

@@ -204,6 +204,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  pdl_trigger();  // the next kernel may start its prologue
+  pdl_wait();     // the previous kernel's writes are visible from here on
 
   auto give_up = [&]() {
     *abort_flag = 1;

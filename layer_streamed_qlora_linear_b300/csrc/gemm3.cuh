@@ -133,6 +133,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  pdl_trigger();  // the next kernel may start its prologue
+  pdl_wait();     // the previous kernel's writes are visible from here on
 
   auto give_up = [&]() {
     *abort_flag = 1;

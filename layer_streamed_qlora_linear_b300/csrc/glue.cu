@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kRowThreads) rms_fwd_kernel(const float* __res
                                                               float* __restrict__ h_out, uint16_t* __restrict__ x,
                                                               float* __restrict__ rstd, const float* __restrict__ w,
                                                               int D) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[kRowThreads / 32];
   const int64_t row = blockIdx.x;
   const float* hr = h + row * D;
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(kRowThreads) rms_fwd_kernel(const float* __res
 __global__ void mix_fwd_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                                const uint16_t* __restrict__ v, uint16_t* __restrict__ a, int64_t M, int D,
                                int Dkv, int64_t ldq, int64_t ldkv) {
+  pdl_trigger();
+  pdl_wait();
   const int g = D / Dkv;
   const int64_t n8 = M * D / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -132,6 +136,8 @@ __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf
 // g, u: rows of F elements at row stride ld; m dense [M, F].
 __global__ void swiglu_fwd_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
                                   uint16_t* __restrict__ m, int64_t M, int F, int64_t ld) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t n8 = M * F / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
@@ -148,6 +154,8 @@ __global__ void swiglu_fwd_kernel(const uint16_t* __restrict__ g, const uint16_t
 // out = h + add (fp32 residual update), optional bf16 copy of nothing.
 __global__ void resid_add_kernel(const float* __restrict__ h, const uint16_t* __restrict__ add,
                                  float* __restrict__ out, int64_t n) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t n8 = n / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
@@ -161,6 +169,8 @@ __global__ void resid_add_kernel(const float* __restrict__ h, const uint16_t* __
 }
 
 __global__ void f32_to_bf16_kernel(const float* __restrict__ x, uint16_t* __restrict__ y, int64_t n) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t n8 = n / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
@@ -175,6 +185,8 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ x, uint16_t* __rest
 __global__ void swiglu_bwd_kernel(const uint16_t* __restrict__ dm, const uint16_t* __restrict__ g,
                                   const uint16_t* __restrict__ u, uint16_t* __restrict__ dg,
                                   uint16_t* __restrict__ du, int64_t M, int F, int64_t ld) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t n8 = M * F / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
@@ -203,6 +215,8 @@ __global__ void __launch_bounds__(kRowThreads) rms_bwd_kernel(
     const uint16_t* __restrict__ dx2, const float* __restrict__ dxf, const float* __restrict__ h,
     const float* __restrict__ rstd, const float* __restrict__ w, float* __restrict__ dh_out,
     uint16_t* __restrict__ dh_bf16, int D) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[kRowThreads / 32];
   const int64_t row = blockIdx.x;
   const float r = rstd[row];
@@ -263,6 +277,8 @@ __global__ void mix_bwd_kernel(const uint16_t* __restrict__ da, const uint16_t* 
                                const uint16_t* __restrict__ k, uint16_t* __restrict__ dq,
                                uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int64_t M, int D, int Dkv,
                                int64_t ldq, int64_t ldkv) {
+  pdl_trigger();
+  pdl_wait();
   const int g = D / Dkv;
   const int64_t n8 = M * Dkv / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -297,6 +313,8 @@ __global__ void mix_bwd_kernel(const uint16_t* __restrict__ da, const uint16_t* 
 // [0, V) gives a zero row and SL_ERR_INVALID in the device error word.
 __global__ void embed_kernel(const int32_t* __restrict__ tokens, const uint16_t* __restrict__ embed, int64_t V,
                              float* __restrict__ h0, int64_t M, int D, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t n8 = M * D / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
@@ -323,43 +341,40 @@ static int ew_grid(int64_t n8) {
 
 sl_status glue_rms_fwd(const float* h, const uint16_t* add, float* h_out, uint16_t* x, float* rstd,
                        const float* w, int64_t M, int D, cudaStream_t s) {
-  rms_fwd_kernel<<<static_cast<unsigned>(M), kRowThreads, 0, s>>>(h, add, h_out, x, rstd, w, D);
-  return check_launch("rms_fwd_kernel");
+  return launch_pdl("rms_fwd_kernel", rms_fwd_kernel, dim3(static_cast<unsigned>(M)), dim3(kRowThreads), 0, s, h,
+                    add, h_out, x, rstd, w, D);
 }
 sl_status glue_mix_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* a, int64_t M, int D,
                        int Dkv, int64_t ldq, int64_t ldkv, cudaStream_t s) {
-  mix_fwd_kernel<<<ew_grid(M * D / 8), 256, 0, s>>>(q, k, v, a, M, D, Dkv, ldq, ldkv);
-  return check_launch("mix_fwd_kernel");
+  return launch_pdl("mix_fwd_kernel", mix_fwd_kernel, dim3(ew_grid(M * D / 8)), dim3(256), 0, s, q, k, v, a, M, D,
+                    Dkv, ldq, ldkv);
 }
 sl_status glue_swiglu_fwd(const uint16_t* g, const uint16_t* u, uint16_t* m, int64_t M, int F, int64_t ld,
                           cudaStream_t s) {
-  swiglu_fwd_kernel<<<ew_grid(M * F / 8), 256, 0, s>>>(g, u, m, M, F, ld);
-  return check_launch("swiglu_fwd_kernel");
+  return launch_pdl("swiglu_fwd_kernel", swiglu_fwd_kernel, dim3(ew_grid(M * F / 8)), dim3(256), 0, s, g, u, m, M, F,
+                    ld);
 }
 sl_status glue_resid_add(const float* h, const uint16_t* add, float* out, int64_t n, cudaStream_t s) {
-  resid_add_kernel<<<ew_grid(n / 8), 256, 0, s>>>(h, add, out, n);
-  return check_launch("resid_add_kernel");
+  return launch_pdl("resid_add_kernel", resid_add_kernel, dim3(ew_grid(n / 8)), dim3(256), 0, s, h, add, out, n);
 }
 sl_status glue_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t s) {
-  f32_to_bf16_kernel<<<ew_grid(n / 8), 256, 0, s>>>(x, y, n);
-  return check_launch("f32_to_bf16_kernel");
+  return launch_pdl("f32_to_bf16_kernel", f32_to_bf16_kernel, dim3(ew_grid(n / 8)), dim3(256), 0, s, x, y, n);
 }
 sl_status glue_swiglu_bwd(const uint16_t* dm, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,
                           int64_t M, int F, int64_t ld, cudaStream_t s) {
-  swiglu_bwd_kernel<<<ew_grid(M * F / 8), 256, 0, s>>>(dm, g, u, dg, du, M, F, ld);
-  return check_launch("swiglu_bwd_kernel");
+  return launch_pdl("swiglu_bwd_kernel", swiglu_bwd_kernel, dim3(ew_grid(M * F / 8)), dim3(256), 0, s, dm, g, u, dg,
+                    du, M, F, ld);
 }
 sl_status glue_rms_bwd(const float* dh_in, const uint16_t* dx0, const uint16_t* dx1, const uint16_t* dx2,
                        const float* dxf, const float* h, const float* rstd, const float* w, float* dh_out,
                        uint16_t* dh_bf16, int64_t M, int D, cudaStream_t s) {
-  rms_bwd_kernel<<<static_cast<unsigned>(M), kRowThreads, 0, s>>>(dh_in, dx0, dx1, dx2, dxf, h, rstd, w, dh_out,
-                                                                   dh_bf16, D);
-  return check_launch("rms_bwd_kernel");
+  return launch_pdl("rms_bwd_kernel", rms_bwd_kernel, dim3(static_cast<unsigned>(M)), dim3(kRowThreads), 0, s, dh_in,
+                    dx0, dx1, dx2, dxf, h, rstd, w, dh_out, dh_bf16, D);
 }
 sl_status glue_mix_bwd(const uint16_t* da, const uint16_t* q, const uint16_t* k, uint16_t* dq, uint16_t* dk,
                        uint16_t* dv, int64_t M, int D, int Dkv, int64_t ldq, int64_t ldkv, cudaStream_t s) {
-  mix_bwd_kernel<<<ew_grid(M * Dkv / 8), 256, 0, s>>>(da, q, k, dq, dk, dv, M, D, Dkv, ldq, ldkv);
-  return check_launch("mix_bwd_kernel");
+  return launch_pdl("mix_bwd_kernel", mix_bwd_kernel, dim3(ew_grid(M * Dkv / 8)), dim3(256), 0, s, da, q, k, dq, dk,
+                    dv, M, D, Dkv, ldq, ldkv);
 }
 
 }  // namespace sl
@@ -367,7 +382,7 @@ sl_status glue_mix_bwd(const uint16_t* da, const uint16_t* q, const uint16_t* k,
 namespace sl {
 sl_status glue_embed(const int32_t* tokens, const uint16_t* embed, int64_t V, float* h0, int64_t M, int D, int* err,
                      cudaStream_t s) {
-  embed_kernel<<<ew_grid(M * D / 8), 256, 0, s>>>(tokens, embed, V, h0, M, D, err);
-  return check_launch("embed_kernel");
+  return launch_pdl("embed_kernel", embed_kernel, dim3(ew_grid(M * D / 8)), dim3(256), 0, s, tokens, embed, V, h0, M,
+                    D, err);
 }
 }  // namespace sl

@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  pdl_trigger();  // the next kernel may start its prologue
+  pdl_wait();     // the previous kernel's writes are visible from here on
 
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -508,8 +510,11 @@ sl_status launch(const CUtensorMap& mq, const CUtensorMap& mw, const SkArgs& a, 
   sl_status st = set_attributes<MODE>();
   if (st != SL_OK) return st;
   const int cs = choose_split<MODE>(blocks, a);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_config<MODE>(blocks, cs, a, stream, attr);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_trigger / pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   const TimingToken tt = timing_begin(MODE == kSkKA ? 6 : (MODE == kSkKB ? 7 : 8), pass_bytes(MODE, a), stream);
   cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_kernel<MODE>, mq, mw, a);
   timing_end(tt, stream);
