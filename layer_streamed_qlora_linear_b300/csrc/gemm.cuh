@@ -204,8 +204,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  pdl_trigger();  // the next kernel may start its prologue
-  pdl_wait();     // the previous kernel's writes are visible from here on
+  // No early pdl_trigger: this grid is one CTA per tile, often several waves;
+  // dependents launch as its CTAs exit (an early trigger let small follow-up
+  // kernels wait beside the last wave and slowed it).
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   auto give_up = [&]() {
     *abort_flag = 1;
