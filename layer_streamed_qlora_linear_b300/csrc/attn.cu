@@ -1,23 +1,27 @@
 // Causal grouped-query attention with rotary positions on tcgen05.
 //
 // Forward (one CTA per 128-query tile, head and sequence): Q stays in shared
-// memory, K and V tiles of 128 keys stream through a two-stage TMA ring.
-// The MMA warp computes S = Q K^T into one of two TMEM buffers one tile
-// ahead; four softmax warps (one query row per thread) take the running
-// row max over the tile, write P = exp2(S c - m) as bf16 into a 128-byte-
-// swizzled tile, and the MMA warp computes O_part = P V (V as an MN-major
-// operand) into one of two more TMEM buffers.  The softmax warps keep O in
-// registers: O = O alpha + O_part with alpha = exp2(m_old - m_new).
+// memory; K and V tiles of 128 keys stream through a two-stage TMA ring
+// (K released once S is computed, V once P V is).  The MMA warp computes
+// S = Q K^T into one of two TMEM buffers one tile ahead.  Eight row workers
+// (TMEM lane quarter x column half; 64 scores per thread) exchange their
+// row maxima through shared memory, write P = exp2(S c - m) as bf16 into a
+// 128-byte-swizzled tile, and the MMA warp computes O_part = P V (V as an
+// MN-major operand) into one of two more TMEM buffers.  The workers keep O
+// in registers: O = O alpha + O_part with alpha = exp2(m_old - m_new).
 //
-// Backward (no atomics: every output element is summed by one CTA in a
+// Backward (no atomics: every output element is summed in one CTA in a
 // fixed order, so results are bitwise reproducible):
 //   dq kernel  (per 128-query tile and head): over the key blocks of 64,
-//              S = Q K^T and dP = dO V^T, dS = P (dP - Di) into shared
-//              memory, dQ += dS K;
-//   dkdv kernel (per 128-key tile and kv head): over the query heads of the
-//              kv head and their query blocks of 64, S^T = K Q^T and
-//              dP^T = V dO^T, P^T and dS^T into shared memory,
-//              dV += P^T dO, dK += dS^T Q.
+//              S = Q K^T and dP = dO V^T, dS = P (dP - Di) into a
+//              double-buffered shared tile, dQ += dS K;
+//   dkdv kernel (per 128-key tile and kv head, or per query head when the
+//              kv heads alone leave SMs idle): over the query blocks of 64
+//              that see the key tile, S^T = K Q^T and dP^T = V dO^T, P^T and
+//              dS^T into double-buffered shared tiles, dV += P^T dO,
+//              dK += dS^T Q; per-query-head results leave as fp32 partials
+//              that attn_kv_reduce_kernel sums over the heads of each kv
+//              head in head order.
 // Di = rowsum(dO * O) comes from a small pre-pass.  The epilogues scale dQ
 // and dK by 1/sqrt(128) and rotate them back by the inverse rotary angle.
 // Every wait is bounded; a timeout raises SL_ERR_TIMEOUT through the
@@ -128,9 +132,9 @@ __global__ void rope_apply_kernel(uint16_t* __restrict__ x, int64_t ld, int64_t 
 struct AttnArgs {
   int S, H, Hkv, nseq;
   float c;        // log2(e) / sqrt(128)
-  uint16_t* out0; // fwd: o;  dq kernel: dq;  dkdv kernel: dk
+  uint16_t* out0; // fwd: o;  dq kernel: dq;  dkdv kernel: dk (in-CTA head sum only)
   int64_t ld0;
-  uint16_t* out1; // dkdv kernel: dv
+  uint16_t* out1; // dkdv kernel: dv (in-CTA head sum only)
   int64_t ld1;
   float* lse;     // fwd output [H][M] (natural log); bwd input
   const float* Di;  // bwd: [H][M]
@@ -660,7 +664,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         return true;
       };
       if (ok) ok = issue_sp(0);
-      int done = 0;
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n && !issue_sp(j + 1)) {
           ok = false;
@@ -678,7 +681,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ptx::mma_bf16(tmem + 256u, kstep(dds, kk, kAtAtom128), mnstep(dkmn, kk), id_q, (j | kk) ? 1u : 0u);
         ptx::mma_commit(&ds_empty[j & 1]);
         ptx::mma_commit(&kv_empty[j % kAtStages]);
-        ++done;
       }
       if (ok) {
         ptx::mma_commit(acc_full);
@@ -687,7 +689,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::mma_commit(drain);
         ptx::mbar_wait(drain, 0, nullptr);
       }
-      (void)done;
     }
   } else {
     // Worker (quarter, half): query row r, key columns 32 half .. 32 half + 31
