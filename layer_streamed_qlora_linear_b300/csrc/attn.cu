@@ -26,6 +26,7 @@
 // and dK by 1/sqrt(128) and rotate them back by the inverse rotary angle.
 // Every wait is bounded; a timeout raises SL_ERR_TIMEOUT through the
 // library's device error word.
+#include <algorithm>
 #include <cmath>
 #include <utility>
 
@@ -159,11 +160,17 @@ struct FwdCfg {
   static constexpr int kOffP = kOffV + 2 * kAtTile;
   static constexpr int kOffRed = kOffP + kAtTile;       // row maxima [2][2][128], row sums [2][128], stop flags
   static constexpr int kOffBar = kOffRed + 6 * 128 * 4 + 16;
-  static constexpr int kNumBars = 18;
+  static constexpr int kNumBars = 20;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
 
+// Persistent: one CTA per SM walks the (query tile, head, sequence) items
+// item = blockIdx.x, + gridDim.x, ... in heaviest-first order (the last query
+// tiles see the most keys).  Barriers, TMEM and the K/V ring run on across
+// items (tile parities count tiles over all of the CTA's items); Q of the
+// next item loads as soon as the current item's last S = Q K^T has
+// completed, while the row workers finish the item.
 __global__ void __launch_bounds__(kAtThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const AttnArgs a) {
@@ -174,32 +181,43 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sV = smem + FwdCfg::kOffV;
   uint8_t* sP = smem + FwdCfg::kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FwdCfg::kOffBar);
-  uint64_t* q_full = bars;        // Q landed
+  uint64_t* q_full = bars;        // Q of the item landed
   uint64_t* k_full = bars + 1;    // [2] K tile of the stage landed
   uint64_t* k_empty = bars + 3;   // [2] its S MMA done
   uint64_t* v_full = bars + 5;    // [2] V tile landed
   uint64_t* v_empty = bars + 7;   // [2] its PV MMA done
   uint64_t* s_full = bars + 9;    // [2] S tile in TMEM buffer b
-  uint64_t* p_full = bars + 11;   // P written (4 warp arrivals); S buffer read
+  uint64_t* p_full = bars + 11;   // P written (8 warp arrivals); S buffer read
   uint64_t* o_full = bars + 12;   // [2] O_part in TMEM buffer b
-  uint64_t* o_empty = bars + 14;  // [2] O_part read (4 warp arrivals)
+  uint64_t* o_empty = bars + 14;  // [2] O_part read (8 warp arrivals)
   uint64_t* drain = bars + 16;    // failure path: every issued MMA completed
+  uint64_t* q_empty = bars + 17;  // the item's last S MMA done: Q may be replaced
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + FwdCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + FwdCfg::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntq = a.S / 128;
   const int per = a.H * a.nseq;
-  const int qt = ntq - 1 - static_cast<int>(blockIdx.x) / per;  // heaviest tiles first
-  const int hb = static_cast<int>(blockIdx.x) % per;
-  const int h = hb % a.H, b = hb / a.H;
-  const int g = h / (a.H / a.Hkv);
-  const int row0 = b * a.S + qt * 128;
-  const int kv0 = b * a.S;
-  const int n = qt + 1;  // key tiles 0..qt
+  const int nitems = ntq * per;
+  struct Item {
+    int qt, h, g, row0, kv0, n;
+  };
+  auto item_of = [&](int item) {
+    Item t;
+    t.qt = ntq - 1 - item / per;  // heaviest tiles first
+    const int hb = item % per;
+    t.h = hb % a.H;
+    const int b = hb / a.H;
+    t.g = t.h / (a.H / a.Hkv);
+    t.row0 = b * a.S + t.qt * 128;
+    t.kv0 = b * a.S;
+    t.n = t.qt + 1;  // key tiles 0..qt
+    return t;
+  };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&k_full[i], 1);
       ptx::mbar_init(&k_empty[i], 1);
@@ -227,10 +245,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // No early pdl_trigger: these grids run in several waves and issue-bound;
-  // dependents that launched early would wait beside the last wave and take
-  // its issue slots (measured: 0.834 -> 0.900 ms per attention step).  They
-  // launch as this grid's CTAs exit.
+  // No early pdl_trigger: the grid keeps every SM busy until its end; the
+  // next kernel launches as its CTAs exit.
   pdl_wait();  // the previous kernel's writes are visible from here on
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -239,37 +255,44 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // K of tile j + 2 loads once S of tile j is done, V once P V of tile j is
-      int issued_k = 0, issued_v = 0;
+      // K of tile t + 2 loads once S of tile t is done, V once P V of tile t is
+      int issued_k = 0, issued_v = 0, issued_q = 0, it = 0, gt = 0;
       bool ok = true;
-      ptx::mbar_arrive_expect_tx(q_full, kAtTile);
-      ptx::tma_load_2d(sQ, &map_q, q_full, h * 128, row0);
-      ptx::tma_load_2d(sQ + kAtAtom128, &map_q, q_full, h * 128 + 64, row0);
-      for (int j = 0; j < n && ok; ++j) {
-        const int s = j & 1;
-        const uint32_t par = ((j >> 1) & 1) ^ 1;
-        const int y = kv0 + j * 128;
-        if (!ptx::mbar_wait(&k_empty[s], par, abort_flag)) {
+      for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x, ++it) {
+        const Item t = item_of(item);
+        if (!ptx::mbar_wait(q_empty, (it & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        ptx::mbar_arrive_expect_tx(&k_full[s], kAtTile);
-        ptx::tma_load_2d(sK + s * kAtTile, &map_k, &k_full[s], g * 128, y);
-        ptx::tma_load_2d(sK + s * kAtTile + kAtAtom128, &map_k, &k_full[s], g * 128 + 64, y);
-        ++issued_k;
-        if (!ptx::mbar_wait(&v_empty[s], par, abort_flag)) {
-          ok = false;
-          break;
+        ptx::mbar_arrive_expect_tx(q_full, kAtTile);
+        ptx::tma_load_2d(sQ, &map_q, q_full, t.h * 128, t.row0);
+        ptx::tma_load_2d(sQ + kAtAtom128, &map_q, q_full, t.h * 128 + 64, t.row0);
+        ++issued_q;
+        for (int j = 0; j < t.n; ++j, ++gt) {
+          const int s = gt & 1;
+          const uint32_t par = ((gt >> 1) & 1) ^ 1;
+          const int y = t.kv0 + j * 128;
+          if (!ptx::mbar_wait(&k_empty[s], par, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&k_full[s], kAtTile);
+          ptx::tma_load_2d(sK + s * kAtTile, &map_k, &k_full[s], t.g * 128, y);
+          ptx::tma_load_2d(sK + s * kAtTile + kAtAtom128, &map_k, &k_full[s], t.g * 128 + 64, y);
+          ++issued_k;
+          if (!ptx::mbar_wait(&v_empty[s], par, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&v_full[s], kAtTile);
+          ptx::tma_load_2d(sV + s * kAtTile, &map_v, &v_full[s], t.g * 128, y);
+          ptx::tma_load_2d(sV + s * kAtTile + kAtAtom128, &map_v, &v_full[s], t.g * 128 + 64, y);
+          ++issued_v;
         }
-        ptx::mbar_arrive_expect_tx(&v_full[s], kAtTile);
-        ptx::tma_load_2d(sV + s * kAtTile, &map_v, &v_full[s], g * 128, y);
-        ptx::tma_load_2d(sV + s * kAtTile + kAtAtom128, &map_v, &v_full[s], g * 128 + 64, y);
-        ++issued_v;
       }
-      // before the CTA exits every issued copy must have landed
-      ptx::mbar_wait(q_full, 0, nullptr);
-      if (!ok) {
+      if (!ok) {  // before the CTA exits every issued copy must have landed
         give_up();
+        if (issued_q > 0) ptx::mbar_wait(q_full, (issued_q - 1) & 1, nullptr);
         for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
           ptx::mbar_wait(&k_full[j & 1], (j >> 1) & 1, nullptr);
         for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
@@ -282,10 +305,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       constexpr uint32_t id_o = ptx::idesc_bf16(128, 128, 0, 1);
       const uint64_t dq0 = kdesc0(ptx::smem_addr(sQ)), dk0 = kdesc0(ptx::smem_addr(sK)),
                      dp0 = kdesc0(ptx::smem_addr(sP)), dv0 = mndesc0(ptx::smem_addr(sV), kAtAtom128);
-      bool ok = ptx::mbar_wait(q_full, 0, abort_flag);
-      auto issue_s = [&](int j) {
-        const int s = j & 1;
-        if (!ptx::mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag)) return false;
+      auto issue_s = [&](int gt) {  // S of the CTA's tile gt into TMEM buffer gt & 1
+        const int s = gt & 1;
+        if (!ptx::mbar_wait(&k_full[s], (gt >> 1) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(s * 128);
         const uint64_t dk = dadd(dk0, s * kAtTile);
@@ -296,26 +318,41 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::mma_commit(&k_empty[s]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n && !issue_s(j + 1)) {
+      bool ok = true;
+      int it = 0, gt = 0;
+      for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x, ++it) {
+        const int n = item_of(item).n;
+        if (!ptx::mbar_wait(q_full, it & 1, abort_flag) || !issue_s(gt)) {
           ok = false;
           break;
         }
-        const int s = j & 1;
-        if (!ptx::mbar_wait(p_full, j & 1, abort_flag) || !ptx::mbar_wait(&v_full[s], (j >> 1) & 1, abort_flag) ||
-            !ptx::mbar_wait(&o_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t d = tmem + 256u + static_cast<uint32_t>(s * 128);
-        const uint64_t dv = dadd(dv0, s * kAtTile);
+        if (n == 1) ptx::mma_commit(q_empty);
+        for (int j = 0; j < n; ++j) {
+          const int cur = gt + j;
+          if (j + 1 < n) {
+            if (!issue_s(cur + 1)) {
+              ok = false;
+              break;
+            }
+            if (j + 2 == n) ptx::mma_commit(q_empty);  // the item's last S has been issued
+          }
+          const int s = cur & 1;
+          if (!ptx::mbar_wait(p_full, cur & 1, abort_flag) ||
+              !ptx::mbar_wait(&v_full[s], (cur >> 1) & 1, abort_flag) ||
+              !ptx::mbar_wait(&o_empty[s], ((cur >> 1) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d = tmem + 256u + static_cast<uint32_t>(s * 128);
+          const uint64_t dv = dadd(dv0, s * kAtTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(d, kstep(dp0, kk, kAtAtom128), mnstep(dv, kk), id_o, kk ? 1u : 0u);
-        ptx::mma_commit(&o_full[s]);
-        ptx::mma_commit(&v_empty[s]);
+          for (int kk = 0; kk < 8; ++kk)
+            ptx::mma_bf16(d, kstep(dp0, kk, kAtAtom128), mnstep(dv, kk), id_o, kk ? 1u : 0u);
+          ptx::mma_commit(&o_full[s]);
+          ptx::mma_commit(&v_empty[s]);
+        }
+        gt += n;
       }
       if (!ok) {
         give_up();
@@ -337,122 +374,132 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 64);
     float* red = reinterpret_cast<float*>(sP + kAtTile);  // maxima [2 parity][2 half][128], sums [2 half][128]
     volatile int* stop = reinterpret_cast<volatile int*>(red + 6 * 128);  // [2 parity]
-    float O[64];
-#pragma unroll
-    for (int e = 0; e < 64; ++e) O[e] = 0.0f;
-    float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
-    bool bad = false, stopped = false;
+    const uint32_t atom = ptx::smem_addr(sP) + half * kAtAtom128;
     auto wait_all = [&](uint64_t* bar, uint32_t par) {
       bool w = ptx::mbar_wait(bar, par, abort_flag);
       w = __all_sync(0xffffffffu, w);
       if (!w && lane == 0 && !*abort_flag) give_up();
       return w;
     };
-    auto accumulate = [&](int j) {  // O = O alpha_j + O_part_j
-      const int s = j & 1;
-      if (!wait_all(&o_full[s], (j >> 1) & 1)) return false;
-      ptx::tc_fence_after();
-      uint32_t u0[32], u1[32];
-      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128), u0);
-      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + 32), u1);
-      ptx::tmem_wait_ld();
+    bool bad = false, stopped = false;
+    int gt = 0;
+    for (int item = blockIdx.x; !stopped && item < nitems; item += gridDim.x) {
+      const int n = ntq - item / per;  // key tiles of the item (its query tile + 1)
+      float O[64];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        O[e] = fmaf(O[e], alpha_prev, __uint_as_float(u0[e]));
-        O[32 + e] = fmaf(O[32 + e], alpha_prev, __uint_as_float(u1[e]));
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&o_empty[s]);
-      return true;
-    };
-    for (int j = 0; j < n; ++j) {
-      const int s = j & 1;
-      const bool diag = (j == qt);
-      uint32_t u[2][32];
-      float mt = -INFINITY;
-      if (!bad) bad = !wait_all(&s_full[s], (j >> 1) & 1);
-      if (!bad) {
+      for (int e = 0; e < 64; ++e) O[e] = 0.0f;
+      float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
+      auto accumulate = [&](int cur) {  // O = O alpha + O_part of the CTA's tile cur
+        const int s = cur & 1;
+        if (!wait_all(&o_full[s], (cur >> 1) & 1)) return false;
         ptx::tc_fence_after();
-        const uint32_t s_addr = lane_base + static_cast<uint32_t>(s * 128);
-        ptx::tmem_ld_32x32b_x32(s_addr, u[0]);
-        ptx::tmem_ld_32x32b_x32(s_addr + 32, u[1]);
+        uint32_t u0[32], u1[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128), u0);
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + 32), u1);
         ptx::tmem_wait_ld();
-        if (diag) {  // keys above the diagonal do not exist
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          O[e] = fmaf(O[e], alpha_prev, __uint_as_float(u0[e]));
+          O[32 + e] = fmaf(O[32 + e], alpha_prev, __uint_as_float(u1[e]));
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&o_empty[s]);
+        return true;
+      };
+      for (int j = 0; j < n; ++j) {
+        const int cur = gt + j;
+        const int s = cur & 1;
+        const bool diag = (j == n - 1);
+        uint32_t u[2][32];
+        float mt = -INFINITY;
+        if (!bad) bad = !wait_all(&s_full[s], (cur >> 1) & 1);
+        if (!bad) {
+          ptx::tc_fence_after();
+          const uint32_t s_addr = lane_base + static_cast<uint32_t>(s * 128);
+          ptx::tmem_ld_32x32b_x32(s_addr, u[0]);
+          ptx::tmem_ld_32x32b_x32(s_addr + 32, u[1]);
+          ptx::tmem_wait_ld();
+          if (diag) {  // keys above the diagonal do not exist
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (half * 64 + c * 32 + e > r) u[c][e] = __float_as_uint(-INFINITY);
+          }
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (half * 64 + c * 32 + e > r) u[c][e] = __float_as_uint(-INFINITY);
+            for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(u[c][e]));
+          mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         }
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        red[(s * 2 + half) * 128 + r] = mt;
+        if (bad && lane == 0) stop[s] = 1;
+        workers_sync();
+        if (stop[s]) {
+          stopped = true;
+          break;
+        }
+        const float m_new = fmaxf(m, fmaxf(mt, red[(s * 2 + (half ^ 1)) * 128 + r]) * a.c);
+        const float alpha = ex2(m - m_new);
+        // O_part of the previous tile joins O with the previous alpha; this also
+        // frees the P tile (its MMA has completed)
+        if (j > 0 && !accumulate(cur - 1)) {
+          bad = true;
+          continue;  // raise the stop flag at the next barrier
+        }
+        alpha_prev = alpha;
+        // P = exp2(S c - m_new) as bf16 into this half's atom of the P tile
+        float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 2; ++c) {
+          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(u[c][e]));
-        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(u[c][e]), a.c, -m_new));
+            const float p1 = ex2(fmaf(__uint_as_float(u[c][e + 1]), a.c, -m_new));
+            ls[e & 3] += p0;
+            ls[(e + 1) & 3] += p1;
+            w[e / 2] = pack2(p0, p1);
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            sts_swz(atom, r, c * 4 + q4, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        }
+        l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        m = m_new;
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(p_full);
       }
-      red[(s * 2 + half) * 128 + r] = mt;
-      if (bad && lane == 0) stop[s] = 1;
+      if (stopped) break;
+      // the last O_part, then the two halves' row sums (the barrier of the
+      // CTA's next tile parity)
+      const int nxt = gt + n;
+      if (!bad) bad = !accumulate(nxt - 1);
+      red[(2 * 2 + half) * 128 + r] = l;
+      if (bad && lane == 0) stop[nxt & 1] = 1;
       workers_sync();
-      if (stop[s]) {
+      if (stop[nxt & 1]) {
         stopped = true;
         break;
       }
-      const float m_new = fmaxf(m, fmaxf(mt, red[(s * 2 + (half ^ 1)) * 128 + r]) * a.c);
-      const float alpha = ex2(m - m_new);
-      // O_part of the previous tile joins O with the previous alpha; this also
-      // frees the P tile (its MMA has completed)
-      if (j > 0 && !accumulate(j - 1)) {
-        bad = true;
-        continue;  // raise the stop flag at the next barrier
+      const Item t = item_of(item);
+      const float lrow = red[(4 + 0) * 128 + r] + red[(4 + 1) * 128 + r];
+      const float inv = 1.0f / lrow;
+      uint16_t* dst = a.out0 + static_cast<int64_t>(t.row0 + r) * a.ld0 + t.h * 128 + half * 64;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        reinterpret_cast<uint4*>(dst)[c] =
+            make_uint4(pack2(O[8 * c] * inv, O[8 * c + 1] * inv), pack2(O[8 * c + 2] * inv, O[8 * c + 3] * inv),
+                       pack2(O[8 * c + 4] * inv, O[8 * c + 5] * inv), pack2(O[8 * c + 6] * inv, O[8 * c + 7] * inv));
+      if (half == 0) {
+        const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
+        a.lse[static_cast<int64_t>(t.h) * M + t.row0 + r] = (m + log2f(lrow)) * 0.69314718055994531f;
       }
-      alpha_prev = alpha;
-      // P = exp2(S c - m_new) as bf16 into this half's atom of the P tile
-      float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      const uint32_t atom = ptx::smem_addr(sP) + half * kAtAtom128;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(u[c][e]), a.c, -m_new));
-          const float p1 = ex2(fmaf(__uint_as_float(u[c][e + 1]), a.c, -m_new));
-          ls[e & 3] += p0;
-          ls[(e + 1) & 3] += p1;
-          w[e / 2] = pack2(p0, p1);
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          sts_swz(atom, r, c * 4 + q4, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-      }
-      l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      m = m_new;
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(p_full);
-    }
-    if (!stopped) {
-      // the last O_part, then the two halves' row sums
-      if (!bad) bad = !accumulate(n - 1);
-      red[(2 * 2 + half) * 128 + r] = l;  // third slot pair: row sums
-      if (bad && lane == 0) stop[n & 1] = 1;
-      workers_sync();
-      if (!stop[n & 1]) {
-        const float lrow = red[(4 + 0) * 128 + r] + red[(4 + 1) * 128 + r];
-        const float inv = 1.0f / lrow;
-        uint16_t* dst = a.out0 + static_cast<int64_t>(row0 + r) * a.ld0 + h * 128 + half * 64;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          reinterpret_cast<uint4*>(dst)[c] =
-              make_uint4(pack2(O[8 * c] * inv, O[8 * c + 1] * inv), pack2(O[8 * c + 2] * inv, O[8 * c + 3] * inv),
-                         pack2(O[8 * c + 4] * inv, O[8 * c + 5] * inv), pack2(O[8 * c + 6] * inv, O[8 * c + 7] * inv));
-        if (half == 0) {
-          const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
-          a.lse[static_cast<int64_t>(h) * M + row0 + r] = (m + log2f(lrow)) * 0.69314718055994531f;
-        }
-      }
+      gt = nxt;
     }
   }
   ptx::tc_fence_before();
@@ -1205,7 +1252,8 @@ sl_status attention_fwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, con
   a.lse = lse;
   a.err = err;
   if ((st = set_smem(attn_fwd_kernel, FwdCfg::kSmem)) != SL_OK) return st;
-  const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.H * a.nseq);
+  const int64_t items = (sh.S / 128) * sh.H * a.nseq;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, num_sms()));
   const TimingToken tt = timing_begin(9, 2.0 * 2.0 * kAtD * causal_pairs(sh), stream);
   st = launch_pdl("attn_fwd_kernel", attn_fwd_kernel, dim3(grid), dim3(kAtThreads), FwdCfg::kSmem, stream, mq, mk, mv,
                   a);
