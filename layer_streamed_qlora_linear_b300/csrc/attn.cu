@@ -542,24 +542,33 @@ __global__ void attn_di_kernel(const uint16_t* __restrict__ o, int64_t ldo, cons
 __device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
                                                  const float* table, int pos, int half, uint16_t* row) {
   uint32_t o1[16], o2[16];
-  const float* cs = table ? table + static_cast<int64_t>(pos) * 128 + half * 32 : nullptr;
+  // the table row holds cos at 0..63 and sin at 64..127; 16-byte loads
+  const float4* cs = table ? reinterpret_cast<const float4*>(table + static_cast<int64_t>(pos) * 128 + half * 32)
+                           : nullptr;
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    float y1[2], y2[2];
+  for (int e4 = 0; e4 < 32; e4 += 4) {
+    float cv[4] = {1.0f, 1.0f, 1.0f, 1.0f}, sv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (cs) {
+      const float4 c = __ldg(cs + e4 / 4), sn = __ldg(cs + 16 + e4 / 4);
+      cv[0] = c.x, cv[1] = c.y, cv[2] = c.z, cv[3] = c.w;
+      sv[0] = sn.x, sv[1] = sn.y, sv[2] = sn.z, sv[3] = sn.w;
+    }
+    float y1[4], y2[4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const float x1 = __uint_as_float(lo[e + u]) * scale, x2 = __uint_as_float(hi[e + u]) * scale;
+    for (int u = 0; u < 4; ++u) {
+      const float x1 = __uint_as_float(lo[e4 + u]) * scale, x2 = __uint_as_float(hi[e4 + u]) * scale;
       if (cs) {
-        const float cv = cs[e + u], sv = cs[64 + e + u];
-        y1[u] = x1 * cv + x2 * sv;
-        y2[u] = x2 * cv - x1 * sv;
+        y1[u] = x1 * cv[u] + x2 * sv[u];
+        y2[u] = x2 * cv[u] - x1 * sv[u];
       } else {
         y1[u] = x1;
         y2[u] = x2;
       }
     }
-    o1[e / 2] = pack2(y1[0], y1[1]);
-    o2[e / 2] = pack2(y2[0], y2[1]);
+    o1[e4 / 2] = pack2(y1[0], y1[1]);
+    o1[e4 / 2 + 1] = pack2(y1[2], y1[3]);
+    o2[e4 / 2] = pack2(y2[0], y2[1]);
+    o2[e4 / 2 + 1] = pack2(y2[2], y2[3]);
   }
   uint4* d1 = reinterpret_cast<uint4*>(row + half * 32);
   uint4* d2 = reinterpret_cast<uint4*>(row + 64 + half * 32);
@@ -572,7 +581,7 @@ __device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const
 
 // ------------------------------------------------------------ dQ
 constexpr int kAtStages = 3;  // key/value ring of the dQ kernel
-constexpr int kKvStages = 2;  // query/dO ring of the dK dV kernel
+constexpr int kKvStages = 3;  // query/dO ring of the dK dV kernel
 
 struct DqCfg {
   static constexpr int kOffQ = 0;                      // [128][128]
@@ -821,16 +830,19 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 struct DkvCfg {
   static constexpr int kOffK = 0;                    // [128][128]
   static constexpr int kOffV = kOffK + kAtTile;      // [128][128]
-  static constexpr int kStageBytes = 4 * kAtAtom64 + 512;  // Q [64][128], dO [64][128], lse and Di of 64 rows
-  static constexpr int kStage = 4 * kAtAtom64 + 1024;      // stage stride (1024-aligned for the swizzled tiles)
-  static constexpr int kOffStage = kOffV + kAtTile;        // kKvStages stages
+  static constexpr int kStage = 4 * kAtAtom64;              // Q [64][128], dO [64][128] (1024-aligned tiles)
+  static constexpr int kStageBytes = kStage + 512;           // + lse and Di of the 64 rows
+  static constexpr int kOffStage = kOffV + kAtTile;          // kKvStages stages
   static constexpr int kOffPT = kOffStage + kKvStages * kStage;  // 2 buffers of [128][64]
   static constexpr int kOffDST = kOffPT + 2 * kAtAtom128;        // 2 buffers of [128][64]
-  static constexpr int kOffBar = kOffDST + 2 * kAtAtom128;
+  static constexpr int kOffLD = kOffDST + 2 * kAtAtom128;        // kKvStages x (lse [64], Di [64]) fp32
+  static constexpr int kOffBar = kOffLD + kKvStages * 512;
   static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
+static_assert(DkvCfg::kSmem <= 232448, "dK/dV shared memory exceeds the per-CTA limit");
+static_assert(1 + 2 * kKvStages + 8 <= DkvCfg::kNumBars, "dK/dV barrier count");
 
 __global__ void __launch_bounds__(kAtThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
@@ -846,13 +858,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sDST = smem + DkvCfg::kOffDST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DkvCfg::kOffBar);
   uint64_t* kv_full = bars;        // K and V landed
-  uint64_t* st_full = bars + 1;    // [kKvStages]
-  uint64_t* st_empty = bars + 3;   // [kKvStages]
-  uint64_t* sp_full = bars + 5;    // [2] S^T and dP^T in TMEM buffer b
-  uint64_t* ds_full = bars + 7;    // [2] P^T and dS^T buffer b written (8 warp arrivals)
-  uint64_t* ds_empty = bars + 9;   // [2] their MMAs done
-  uint64_t* acc_full = bars + 11;  // dK, dV complete
-  uint64_t* drain = bars + 12;     // failure path: every issued MMA completed
+  uint64_t* st_full = bars + 1;                  // [kKvStages]
+  uint64_t* st_empty = bars + 1 + kKvStages;     // [kKvStages]
+  uint64_t* sp_full = bars + 1 + 2 * kKvStages;  // [2] S^T and dP^T in TMEM buffer b
+  uint64_t* ds_full = sp_full + 2;               // [2] P^T and dS^T buffer b written (8 warp arrivals)
+  uint64_t* ds_empty = sp_full + 4;              // [2] their MMAs done
+  uint64_t* acc_full = sp_full + 6;              // dK, dV complete
+  uint64_t* drain = sp_full + 7;                 // failure path: every issued MMA completed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DkvCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DkvCfg::kOffMisc + 4);
 
@@ -927,8 +939,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::tma_load_2d(st + kAtAtom64, &map_q, &st_full[s], h * 128 + 64, qrow);
         ptx::tma_load_2d(st + 2 * kAtAtom64, &map_do, &st_full[s], h * 128, qrow);
         ptx::tma_load_2d(st + 3 * kAtAtom64, &map_do, &st_full[s], h * 128 + 64, qrow);
-        ptx::tma_load_2d(st + 4 * kAtAtom64, &map_lse, &st_full[s], qrow, h);
-        ptx::tma_load_2d(st + 4 * kAtAtom64 + 256, &map_di, &st_full[s], qrow, h);
+        uint8_t* ld = smem + DkvCfg::kOffLD + s * 512;
+        ptx::tma_load_2d(ld, &map_lse, &st_full[s], qrow, h);
+        ptx::tma_load_2d(ld + 256, &map_di, &st_full[s], qrow, h);
         ++issued;
       }
       ptx::mbar_wait(kv_full, 0, nullptr);
@@ -1013,7 +1026,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       }
       ptx::tc_fence_after();
       // this half's 32 query rows: lse (scaled to log2) and Di, from the stage's shared copy
-      const uint32_t ls_addr = ptx::smem_addr(sStage) + (t % kKvStages) * DkvCfg::kStage + 4 * kAtAtom64 + half * 128;
+      const uint32_t ls_addr = ptx::smem_addr(smem + DkvCfg::kOffLD) + (t % kKvStages) * 512 + half * 128;
       float lse2[32], dis[32];
 #pragma unroll
       for (int v4 = 0; v4 < 8; ++v4) {
