@@ -1,6 +1,12 @@
 // Causal grouped-query attention with rotary positions on tcgen05.
 //
-// Forward (one CTA per 128-query tile, head and sequence): Q stays in shared
+// All three tensor-core kernels are persistent: one CTA per SM walks work
+// items (numbered heaviest first) in a serpentine order; barriers, TMEM and
+// the operand rings run on across items, and the per-item operand (Q, or K
+// and V) of the next item loads as soon as the current item's last MMA that
+// reads it has completed.
+//
+// Forward (items: 128-query tile, head, sequence): Q stays in shared
 // memory; K and V tiles of 128 keys stream through a two-stage TMA ring
 // (K released once S is computed, V once P V is).  The MMA warp computes
 // S = Q K^T into one of two TMEM buffers one tile ahead.  Eight row workers
@@ -12,16 +18,16 @@
 //
 // Backward (no atomics: every output element is summed in one CTA in a
 // fixed order, so results are bitwise reproducible):
-//   dq kernel  (per 128-query tile and head): over the key blocks of 64,
+//   dq kernel  (items: 128-query tile and head): over the key blocks of 64,
 //              S = Q K^T and dP = dO V^T, dS = P (dP - Di) into a
 //              double-buffered shared tile, dQ += dS K;
-//   dkdv kernel (per 128-key tile and kv head, or per query head when the
+//   dkdv kernel (items: 128-key tile and kv head, or query head when the
 //              kv heads alone leave SMs idle): over the query blocks of 64
-//              that see the key tile, S^T = K Q^T and dP^T = V dO^T, P^T and
-//              dS^T into double-buffered shared tiles, dV += P^T dO,
-//              dK += dS^T Q; per-query-head results leave as fp32 partials
-//              that attn_kv_reduce_kernel sums over the heads of each kv
-//              head in head order.
+//              that see the key tile (a three-stage ring), S^T = K Q^T and
+//              dP^T = V dO^T, P^T and dS^T into double-buffered shared
+//              tiles, dV += P^T dO, dK += dS^T Q; per-query-head results
+//              leave as fp32 partials that attn_kv_reduce_kernel sums over
+//              the heads of each kv head in head order.
 // Di = rowsum(dO * O) comes from a small pre-pass.  The epilogues scale dQ
 // and dK by 1/sqrt(128) and rotate them back by the inverse rotary angle.
 // Every wait is bounded; a timeout raises SL_ERR_TIMEOUT through the
@@ -68,6 +74,15 @@ __device__ __forceinline__ float4 lds128(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
+}
+
+// The k-th work item of this CTA in a persistent grid: rounds of gridDim.x
+// consecutive items (ordered heaviest first), walked forwards and backwards in
+// turn so that every CTA gets a similar mix of heavy and light items.  The
+// sequence increases with k, so the first index past the end ends the walk.
+__device__ __forceinline__ int nth_item(int k) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return k * G + ((k & 1) ? G - 1 - c : c);
 }
 
 // Shared-memory descriptors of SW128 operands, built once per buffer and
@@ -165,9 +180,9 @@ struct FwdCfg {
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
 
-// Persistent: one CTA per SM walks the (query tile, head, sequence) items
-// item = blockIdx.x, + gridDim.x, ... in heaviest-first order (the last query
-// tiles see the most keys).  Barriers, TMEM and the K/V ring run on across
+// Persistent: one CTA per SM walks the (query tile, head, sequence) items,
+// numbered heaviest first (the last query tiles see the most keys), in the
+// order nth_item gives.  Barriers, TMEM and the K/V ring run on across
 // items (tile parities count tiles over all of the CTA's items); Q of the
 // next item loads as soon as the current item's last S = Q K^T has
 // completed, while the row workers finish the item.
@@ -258,7 +273,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       // K of tile t + 2 loads once S of tile t is done, V once P V of tile t is
       int issued_k = 0, issued_v = 0, issued_q = 0, it = 0, gt = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x, ++it) {
+      for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
         const Item t = item_of(item);
         if (!ptx::mbar_wait(q_empty, (it & 1) ^ 1, abort_flag)) {
           ok = false;
@@ -320,7 +335,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       };
       bool ok = true;
       int it = 0, gt = 0;
-      for (int item = blockIdx.x; ok && item < nitems; item += gridDim.x, ++it) {
+      for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
         const int n = item_of(item).n;
         if (!ptx::mbar_wait(q_full, it & 1, abort_flag) || !issue_s(gt)) {
           ok = false;
@@ -383,7 +398,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     };
     bool bad = false, stopped = false;
     int gt = 0;
-    for (int item = blockIdx.x; !stopped && item < nitems; item += gridDim.x) {
+    for (int k = 0, item = nth_item(0); !stopped && item < nitems; item = nth_item(++k)) {
       const int n = ntq - item / per;  // key tiles of the item (its query tile + 1)
       float O[64];
 #pragma unroll
@@ -595,6 +610,11 @@ struct DqCfg {
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
 
+// Persistent: one CTA per SM walks the (query tile, head, sequence) items,
+// numbered heaviest first, in the order nth_item gives.  The key/value ring and
+// the S / dP / dS buffers run on across items (block parities count the
+// CTA's 64-key blocks over all of its items); Q and dO of the next item load
+// as soon as the current item's last S / dP MMAs have completed.
 __global__ void __launch_bounds__(kAtThreads, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -607,31 +627,42 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sV = smem + DqCfg::kOffV;
   uint8_t* sDS = smem + DqCfg::kOffDS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DqCfg::kOffBar);
-  uint64_t* q_full = bars;         // Q and dO landed
+  uint64_t* q_full = bars;         // Q and dO of the item landed
   uint64_t* kv_full = bars + 1;    // [kAtStages]
   uint64_t* kv_empty = bars + 4;   // [kAtStages]
   uint64_t* sp_full = bars + 7;    // [2] S and dP in TMEM buffer b
   uint64_t* ds_full = bars + 9;    // [2] dS buffer b written (8 warp arrivals); S/dP buffer b read
   uint64_t* ds_empty = bars + 11;  // [2] the dQ MMA of dS buffer b done
-  uint64_t* acc_full = bars + 13;  // dQ complete
+  uint64_t* acc_full = bars + 13;  // dQ of the item complete
   uint64_t* drain = bars + 14;     // failure path: every issued MMA completed
+  uint64_t* q_empty = bars + 15;   // the item's last S / dP MMAs done: Q and dO may be replaced
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DqCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DqCfg::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntq = a.S / 128;
   const int per = a.H * a.nseq;
-  const int qt = ntq - 1 - static_cast<int>(blockIdx.x) / per;
-  const int hb = static_cast<int>(blockIdx.x) % per;
-  const int h = hb % a.H, b = hb / a.H;
-  const int g = h / (a.H / a.Hkv);
-  const int row0 = b * a.S + qt * 128;
-  const int kv0 = b * a.S;
-  const int n = 2 * (qt + 1);  // key blocks of 64
+  const int nitems = ntq * per;
   const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
+  struct Item {
+    int qt, h, g, row0, kv0, n;
+  };
+  auto item_of = [&](int item) {
+    Item t;
+    t.qt = ntq - 1 - item / per;  // heaviest tiles first
+    const int hb = item % per;
+    t.h = hb % a.H;
+    const int b = hb / a.H;
+    t.g = t.h / (a.H / a.Hkv);
+    t.row0 = b * a.S + t.qt * 128;
+    t.kv0 = b * a.S;
+    t.n = 2 * (t.qt + 1);  // key blocks of 64
+    return t;
+  };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
     for (int i = 0; i < kAtStages; ++i) {
       ptx::mbar_init(&kv_full[i], 1);
       ptx::mbar_init(&kv_empty[i], 1);
@@ -645,6 +676,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&map_q);
+    ptx::tma_prefetch_desc(&map_do);
+    ptx::tma_prefetch_desc(&map_k);
+    ptx::tma_prefetch_desc(&map_v);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, 512);
@@ -654,10 +689,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // No early pdl_trigger: these grids run in several waves and issue-bound;
-  // dependents that launched early would wait beside the last wave and take
-  // its issue slots (measured: 0.834 -> 0.900 ms per attention step).  They
-  // launch as this grid's CTAs exit.
+  // No early pdl_trigger: the grid keeps every SM busy until its end; the
+  // next kernel launches as its CTAs exit.
   pdl_wait();  // the previous kernel's writes are visible from here on
   // TMEM: S buffers at 0 / 64, dP at 128 / 192, dQ at 256
   auto give_up = [&]() {
@@ -667,33 +700,43 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
+      int issued = 0, issued_q = 0, it = 0, gb = 0;
       bool ok = true;
-      ptx::mbar_arrive_expect_tx(q_full, 2 * kAtTile);
-      ptx::tma_load_2d(sQ, &map_q, q_full, h * 128, row0);
-      ptx::tma_load_2d(sQ + kAtAtom128, &map_q, q_full, h * 128 + 64, row0);
-      ptx::tma_load_2d(sDO, &map_do, q_full, h * 128, row0);
-      ptx::tma_load_2d(sDO + kAtAtom128, &map_do, q_full, h * 128 + 64, row0);
-      for (int j = 0; j < n; ++j) {
-        const int s = j % kAtStages;
-        if (!ptx::mbar_wait(&kv_empty[s], ((j / kAtStages) & 1) ^ 1, abort_flag)) {
-          give_up();
+      for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
+        const Item t = item_of(item);
+        if (!ptx::mbar_wait(q_empty, (it & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        ptx::mbar_arrive_expect_tx(&kv_full[s], 4 * kAtAtom64);
-        uint8_t* k_dst = sK + s * 2 * kAtAtom64;
-        uint8_t* v_dst = sV + s * 2 * kAtAtom64;
-        ptx::tma_load_2d(k_dst, &map_k, &kv_full[s], g * 128, kv0 + j * 64);
-        ptx::tma_load_2d(k_dst + kAtAtom64, &map_k, &kv_full[s], g * 128 + 64, kv0 + j * 64);
-        ptx::tma_load_2d(v_dst, &map_v, &kv_full[s], g * 128, kv0 + j * 64);
-        ptx::tma_load_2d(v_dst + kAtAtom64, &map_v, &kv_full[s], g * 128 + 64, kv0 + j * 64);
-        ++issued;
+        ptx::mbar_arrive_expect_tx(q_full, 2 * kAtTile);
+        ptx::tma_load_2d(sQ, &map_q, q_full, t.h * 128, t.row0);
+        ptx::tma_load_2d(sQ + kAtAtom128, &map_q, q_full, t.h * 128 + 64, t.row0);
+        ptx::tma_load_2d(sDO, &map_do, q_full, t.h * 128, t.row0);
+        ptx::tma_load_2d(sDO + kAtAtom128, &map_do, q_full, t.h * 128 + 64, t.row0);
+        ++issued_q;
+        for (int j = 0; j < t.n; ++j, ++gb) {
+          const int s = gb % kAtStages;
+          if (!ptx::mbar_wait(&kv_empty[s], ((gb / kAtStages) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&kv_full[s], 4 * kAtAtom64);
+          uint8_t* k_dst = sK + s * 2 * kAtAtom64;
+          uint8_t* v_dst = sV + s * 2 * kAtAtom64;
+          const int y = t.kv0 + j * 64;
+          ptx::tma_load_2d(k_dst, &map_k, &kv_full[s], t.g * 128, y);
+          ptx::tma_load_2d(k_dst + kAtAtom64, &map_k, &kv_full[s], t.g * 128 + 64, y);
+          ptx::tma_load_2d(v_dst, &map_v, &kv_full[s], t.g * 128, y);
+          ptx::tma_load_2d(v_dst + kAtAtom64, &map_v, &kv_full[s], t.g * 128 + 64, y);
+          ++issued;
+        }
       }
-      ptx::mbar_wait(q_full, 0, nullptr);
-      if (!ok)
+      if (!ok) {  // before the CTA exits every issued copy must have landed
+        give_up();
+        if (issued_q > 0) ptx::mbar_wait(q_full, (issued_q - 1) & 1, nullptr);
         for (int j = (issued > kAtStages ? issued - kAtStages : 0); j < issued; ++j)
           ptx::mbar_wait(&kv_full[j % kAtStages], (j / kAtStages) & 1, nullptr);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -702,10 +745,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       const uint64_t dq0 = kdesc0(ptx::smem_addr(sQ)), ddo0 = kdesc0(ptx::smem_addr(sDO)),
                      dk0 = kdesc0(ptx::smem_addr(sK)), dv0 = kdesc0(ptx::smem_addr(sV)),
                      dkmn0 = mndesc0(ptx::smem_addr(sK), kAtAtom64), dds0 = kdesc0(ptx::smem_addr(sDS));
-      bool ok = ptx::mbar_wait(q_full, 0, abort_flag);
-      auto issue_sp = [&](int j) {
-        const int s = j % kAtStages, b2 = j & 1;
-        if (!ptx::mbar_wait(&kv_full[s], (j / kAtStages) & 1, abort_flag)) return false;
+      auto issue_sp = [&](int gb) {  // S and dP of the CTA's block gb into TMEM buffer gb & 1
+        const int s = gb % kAtStages, b2 = gb & 1;
+        if (!ptx::mbar_wait(&kv_full[s], (gb / kAtStages) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint64_t dk = dadd(dk0, s * 2 * kAtAtom64), dv = dadd(dv0, s * 2 * kAtAtom64);
 #pragma unroll
@@ -719,28 +761,41 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::mma_commit(&sp_full[b2]);
         return true;
       };
-      if (ok) ok = issue_sp(0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n && !issue_sp(j + 1)) {
+      bool ok = true;
+      int it = 0, gb = 0;
+      for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
+        const int n = item_of(item).n;  // >= 2
+        if (!ptx::mbar_wait(q_full, it & 1, abort_flag) || !issue_sp(gb)) {
           ok = false;
           break;
         }
-        if (!ptx::mbar_wait(&ds_full[j & 1], (j >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint64_t dkmn = dadd(dkmn0, (j % kAtStages) * 2 * kAtAtom64);
-        const uint64_t dds = dadd(dds0, (j & 1) * kAtAtom128);
+        for (int j = 0; j < n; ++j) {
+          const int cur = gb + j;
+          if (j + 1 < n) {
+            if (!issue_sp(cur + 1)) {
+              ok = false;
+              break;
+            }
+            if (j + 2 == n) ptx::mma_commit(q_empty);  // the item's last S / dP have been issued
+          }
+          if (!ptx::mbar_wait(&ds_full[cur & 1], (cur >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t dkmn = dadd(dkmn0, (cur % kAtStages) * 2 * kAtAtom64);
+          const uint64_t dds = dadd(dds0, (cur & 1) * kAtAtom128);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_bf16(tmem + 256u, kstep(dds, kk, kAtAtom128), mnstep(dkmn, kk), id_q, (j | kk) ? 1u : 0u);
-        ptx::mma_commit(&ds_empty[j & 1]);
-        ptx::mma_commit(&kv_empty[j % kAtStages]);
-      }
-      if (ok) {
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_bf16(tmem + 256u, kstep(dds, kk, kAtAtom128), mnstep(dkmn, kk), id_q, (j | kk) ? 1u : 0u);
+          ptx::mma_commit(&ds_empty[cur & 1]);
+          ptx::mma_commit(&kv_empty[cur % kAtStages]);
+        }
+        if (!ok) break;
         ptx::mma_commit(acc_full);
-      } else {
+        gb += n;
+      }
+      if (!ok) {
         give_up();
         ptx::mma_commit(drain);
         ptx::mbar_wait(drain, 0, nullptr);
@@ -752,10 +807,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    const int qrow = qt * 128 + r;  // position in the sequence
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float lse2 = a.lse[static_cast<int64_t>(h) * M + row0 + r] * kLog2e;
-    const float di = a.Di[static_cast<int64_t>(h) * M + row0 + r];
     auto wait_all = [&](uint64_t* bar, uint32_t par) {
       bool w = ptx::mbar_wait(bar, par, abort_flag);
       w = __all_sync(0xffffffffu, w);
@@ -763,53 +815,67 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       return w;
     };
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int s = j & 1;
-      if (!wait_all(&sp_full[s], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      uint32_t w[16];
-      {
-        uint32_t us[32], up[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + half * 32), us);
-        ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + half * 32), up);
-        ptx::tmem_wait_ld();
-        const int key0 = j * 64 + half * 32;
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float ds2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float p = key0 + e + u <= qrow ? ex2(fmaf(__uint_as_float(us[e + u]), a.c, -lse2)) : 0.0f;
-            ds2[u] = p * (__uint_as_float(up[e + u]) - di);
-          }
-          w[e / 2] = pack2(ds2[0], ds2[1]);
+    int it = 0, gb = 0;
+    for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
+      const Item t = item_of(item);
+      const int qrow = t.qt * 128 + r;  // position in the sequence
+      const float lse2 = a.lse[static_cast<int64_t>(t.h) * M + t.row0 + r] * kLog2e;
+      const float di = a.Di[static_cast<int64_t>(t.h) * M + t.row0 + r];
+      for (int j = 0; j < t.n; ++j) {
+        const int cur = gb + j;
+        const int s = cur & 1;
+        if (!wait_all(&sp_full[s], (cur >> 1) & 1)) {
+          ok = false;
+          break;
         }
+        ptx::tc_fence_after();
+        uint32_t w[16];
+        {
+          uint32_t us[32], up[32];
+          ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(s * 64 + half * 32), us);
+          ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + half * 32), up);
+          ptx::tmem_wait_ld();
+          const int key0 = j * 64 + half * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float ds2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float p = key0 + e + u <= qrow ? ex2(fmaf(__uint_as_float(us[e + u]), a.c, -lse2)) : 0.0f;
+              ds2[u] = p * (__uint_as_float(up[e + u]) - di);
+            }
+            w[e / 2] = pack2(ds2[0], ds2[1]);
+          }
+        }
+        // dS buffer cur & 1 must have been consumed by the dQ MMA of block cur - 2
+        if (!wait_all(&ds_empty[s], ((cur >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t ds_buf = ptx::smem_addr(sDS) + s * kAtAtom128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          sts_swz(ds_buf, r, half * 4 + q4, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ds_full[s]);
       }
-      // dS buffer j & 1 must have been consumed by the MMA of iteration j - 2
-      if (!wait_all(&ds_empty[j & 1], ((j >> 1) & 1) ^ 1)) {
+      if (!ok || !wait_all(acc_full, it & 1)) {
         ok = false;
         break;
       }
-      const uint32_t ds_buf = ptx::smem_addr(sDS) + (j & 1) * kAtAtom128;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        sts_swz(ds_buf, r, half * 4 + q4, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ds_full[j & 1]);
-    }
-    if (ok && wait_all(acc_full, 0)) {
+      // dQ leaves TMEM before this warp's next dS arrival, after which the
+      // next item's first dQ MMA overwrites it
       ptx::tc_fence_after();
       uint32_t lo[32], hi[32];
       ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(half * 32), lo);
       ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(64 + half * 32), hi);
       ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
       store_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, qrow, half,
-                       a.out0 + static_cast<int64_t>(row0 + r) * a.ld0 + h * 128);
+                       a.out0 + static_cast<int64_t>(t.row0 + r) * a.ld0 + t.h * 128);
+      gb += t.n;
     }
   }
   ptx::tc_fence_before();
@@ -821,12 +887,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 }
 
 // ------------------------------------------------------------ dK, dV
-// One CTA per (128-key tile, group of heads_per_cta query heads, sequence):
-// dK and dV of the key tile accumulate in TMEM over those heads' query blocks
-// that see it.  heads_per_cta = H / Hkv (enough CTAs to fill the GPU): the CTA
-// covers its kv head's query heads in head order and writes bf16 dk (scaled,
-// rotated back) and dv itself; heads_per_cta = 1: fp32 per-head partials
-// [H][M][128] that attn_kv_reduce_kernel sums in head order.
+// One work item per (128-key tile, group of heads_per_cta query heads,
+// sequence): dK and dV of the key tile accumulate in TMEM over those heads'
+// query blocks that see it.  heads_per_cta = H / Hkv (enough items to fill the
+// GPU): the item covers its kv head's query heads in head order and writes
+// bf16 dk (scaled, rotated back) and dv itself; heads_per_cta = 1: fp32
+// per-head partials [H][M][128] that attn_kv_reduce_kernel sums in head order.
 struct DkvCfg {
   static constexpr int kOffK = 0;                    // [128][128]
   static constexpr int kOffV = kOffK + kAtTile;      // [128][128]
@@ -842,8 +908,13 @@ struct DkvCfg {
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
 static_assert(DkvCfg::kSmem <= 232448, "dK/dV shared memory exceeds the per-CTA limit");
-static_assert(1 + 2 * kKvStages + 8 <= DkvCfg::kNumBars, "dK/dV barrier count");
+static_assert(1 + 2 * kKvStages + 9 <= DkvCfg::kNumBars, "dK/dV barrier count");
 
+// Persistent: one CTA per SM walks the (key tile, head group, sequence)
+// items, numbered heaviest first (the first key tiles are seen by the most
+// query blocks), in the order nth_item gives.  The query/dO ring and the
+// S^T / dP^T / P^T / dS^T buffers run on across items; K and V of the next
+// item load once the current item's last S^T / dP^T MMAs have completed.
 __global__ void __launch_bounds__(kAtThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                      const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -857,14 +928,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sPT = smem + DkvCfg::kOffPT;
   uint8_t* sDST = smem + DkvCfg::kOffDST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DkvCfg::kOffBar);
-  uint64_t* kv_full = bars;        // K and V landed
+  uint64_t* kv_full = bars;                      // K and V of the item landed
   uint64_t* st_full = bars + 1;                  // [kKvStages]
   uint64_t* st_empty = bars + 1 + kKvStages;     // [kKvStages]
   uint64_t* sp_full = bars + 1 + 2 * kKvStages;  // [2] S^T and dP^T in TMEM buffer b
   uint64_t* ds_full = sp_full + 2;               // [2] P^T and dS^T buffer b written (8 warp arrivals)
   uint64_t* ds_empty = sp_full + 4;              // [2] their MMAs done
-  uint64_t* acc_full = sp_full + 6;              // dK, dV complete
+  uint64_t* acc_full = sp_full + 6;              // dK, dV of the item complete
   uint64_t* drain = sp_full + 7;                 // failure path: every issued MMA completed
+  uint64_t* kv_empty = sp_full + 8;              // the item's last S^T / dP^T MMAs done: K, V may be replaced
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DkvCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DkvCfg::kOffMisc + 4);
 
@@ -872,17 +944,28 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   const int hpc = a.heads_per_cta;
   const int ngrp = a.H / hpc;
   const int per = ngrp * a.nseq;
-  const int kt = static_cast<int>(blockIdx.x) / per;  // key tile; heaviest (kt = 0) first
-  const int hb = static_cast<int>(blockIdx.x) % per;
-  const int h0 = (hb % ngrp) * hpc, b = hb / ngrp;
-  const int g = h0 / (a.H / a.Hkv);
-  const int key0 = b * a.S + kt * 128;
-  const int nqb = a.S / 64 - 2 * kt;  // query blocks of 64 that see this key tile
-  const int n = hpc * nqb;            // iterations: (query head, query block)
+  const int ntk = a.S / 128;
+  const int nitems = ntk * per;
   const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
+  struct Item {
+    int kt, h0, g, b, key0, nqb, n;
+  };
+  auto item_of = [&](int item) {
+    Item t;
+    t.kt = item / per;  // key tile; heaviest (kt = 0) first
+    const int hb = item % per;
+    t.h0 = (hb % ngrp) * hpc;
+    t.b = hb / ngrp;
+    t.g = t.h0 / (a.H / a.Hkv);
+    t.key0 = t.b * a.S + t.kt * 128;
+    t.nqb = a.S / 64 - 2 * t.kt;  // query blocks of 64 that see this key tile
+    t.n = hpc * t.nqb;            // iterations: (query head, query block)
+    return t;
+  };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(kv_full, 1);
+    ptx::mbar_init(kv_empty, 1);
     for (int i = 0; i < kKvStages; ++i) {
       ptx::mbar_init(&st_full[i], 1);
       ptx::mbar_init(&st_empty[i], 1);
@@ -896,6 +979,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&map_q);
+    ptx::tma_prefetch_desc(&map_do);
+    ptx::tma_prefetch_desc(&map_k);
+    ptx::tma_prefetch_desc(&map_v);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, 512);
@@ -905,10 +992,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // No early pdl_trigger: these grids run in several waves and issue-bound;
-  // dependents that launched early would wait beside the last wave and take
-  // its issue slots (measured: 0.834 -> 0.900 ms per attention step).  They
-  // launch as this grid's CTAs exit.
+  // No early pdl_trigger: the grid keeps every SM busy until its end; the
+  // next kernel launches as its CTAs exit.
   pdl_wait();  // the previous kernel's writes are visible from here on
   // TMEM: S^T buffers at 0 / 64, dP^T at 128 / 192, dV at 256, dK at 384
   auto give_up = [&]() {
@@ -918,36 +1003,45 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
+      int issued = 0, issued_kv = 0, it = 0, gs = 0;
       bool ok = true;
-      ptx::mbar_arrive_expect_tx(kv_full, 2 * kAtTile);
-      ptx::tma_load_2d(sK, &map_k, kv_full, g * 128, key0);
-      ptx::tma_load_2d(sK + kAtAtom128, &map_k, kv_full, g * 128 + 64, key0);
-      ptx::tma_load_2d(sV, &map_v, kv_full, g * 128, key0);
-      ptx::tma_load_2d(sV + kAtAtom128, &map_v, kv_full, g * 128 + 64, key0);
-      for (int t = 0; t < n; ++t) {
-        const int s = t % kKvStages;
-        if (!ptx::mbar_wait(&st_empty[s], ((t / kKvStages) & 1) ^ 1, abort_flag)) {
-          give_up();
+      for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
+        const Item t = item_of(item);
+        if (!ptx::mbar_wait(kv_empty, (it & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        const int h = h0 + t / nqb, qrow = b * a.S + (2 * kt + t % nqb) * 64;
-        uint8_t* st = sStage + s * DkvCfg::kStage;
-        ptx::mbar_arrive_expect_tx(&st_full[s], DkvCfg::kStageBytes);
-        ptx::tma_load_2d(st, &map_q, &st_full[s], h * 128, qrow);
-        ptx::tma_load_2d(st + kAtAtom64, &map_q, &st_full[s], h * 128 + 64, qrow);
-        ptx::tma_load_2d(st + 2 * kAtAtom64, &map_do, &st_full[s], h * 128, qrow);
-        ptx::tma_load_2d(st + 3 * kAtAtom64, &map_do, &st_full[s], h * 128 + 64, qrow);
-        uint8_t* ld = smem + DkvCfg::kOffLD + s * 512;
-        ptx::tma_load_2d(ld, &map_lse, &st_full[s], qrow, h);
-        ptx::tma_load_2d(ld + 256, &map_di, &st_full[s], qrow, h);
-        ++issued;
+        ptx::mbar_arrive_expect_tx(kv_full, 2 * kAtTile);
+        ptx::tma_load_2d(sK, &map_k, kv_full, t.g * 128, t.key0);
+        ptx::tma_load_2d(sK + kAtAtom128, &map_k, kv_full, t.g * 128 + 64, t.key0);
+        ptx::tma_load_2d(sV, &map_v, kv_full, t.g * 128, t.key0);
+        ptx::tma_load_2d(sV + kAtAtom128, &map_v, kv_full, t.g * 128 + 64, t.key0);
+        ++issued_kv;
+        for (int u = 0; u < t.n; ++u, ++gs) {
+          const int s = gs % kKvStages;
+          if (!ptx::mbar_wait(&st_empty[s], ((gs / kKvStages) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int h = t.h0 + u / t.nqb, qrow = t.b * a.S + (2 * t.kt + u % t.nqb) * 64;
+          uint8_t* st = sStage + s * DkvCfg::kStage;
+          ptx::mbar_arrive_expect_tx(&st_full[s], DkvCfg::kStageBytes);
+          ptx::tma_load_2d(st, &map_q, &st_full[s], h * 128, qrow);
+          ptx::tma_load_2d(st + kAtAtom64, &map_q, &st_full[s], h * 128 + 64, qrow);
+          ptx::tma_load_2d(st + 2 * kAtAtom64, &map_do, &st_full[s], h * 128, qrow);
+          ptx::tma_load_2d(st + 3 * kAtAtom64, &map_do, &st_full[s], h * 128 + 64, qrow);
+          uint8_t* ld = smem + DkvCfg::kOffLD + s * 512;
+          ptx::tma_load_2d(ld, &map_lse, &st_full[s], qrow, h);
+          ptx::tma_load_2d(ld + 256, &map_di, &st_full[s], qrow, h);
+          ++issued;
+        }
       }
-      ptx::mbar_wait(kv_full, 0, nullptr);
-      if (!ok)
-        for (int t = (issued > kKvStages ? issued - kKvStages : 0); t < issued; ++t)
-          ptx::mbar_wait(&st_full[t % kKvStages], (t / kKvStages) & 1, nullptr);
+      if (!ok) {  // before the CTA exits every issued copy must have landed
+        give_up();
+        if (issued_kv > 0) ptx::mbar_wait(kv_full, (issued_kv - 1) & 1, nullptr);
+        for (int u = (issued > kKvStages ? issued - kKvStages : 0); u < issued; ++u)
+          ptx::mbar_wait(&st_full[u % kKvStages], (u / kKvStages) & 1, nullptr);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -956,10 +1050,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       const uint64_t dk0 = kdesc0(ptx::smem_addr(sK)), dv0 = kdesc0(ptx::smem_addr(sV)),
                      dst0 = kdesc0(ptx::smem_addr(sStage)), dstmn0 = mndesc0(ptx::smem_addr(sStage), kAtAtom64),
                      dpt0 = kdesc0(ptx::smem_addr(sPT)), ddst0 = kdesc0(ptx::smem_addr(sDST));
-      bool ok = ptx::mbar_wait(kv_full, 0, abort_flag);
-      auto issue_sp = [&](int t) {
-        const int s = t % kKvStages, b2 = t & 1;
-        if (!ptx::mbar_wait(&st_full[s], (t / kKvStages) & 1, abort_flag)) return false;
+      auto issue_sp = [&](int gs) {  // S^T and dP^T of the CTA's iteration gs into TMEM buffer gs & 1
+        const int s = gs % kKvStages, b2 = gs & 1;
+        if (!ptx::mbar_wait(&st_full[s], (gs / kKvStages) & 1, abort_flag)) return false;
         ptx::tc_fence_after();
         const uint64_t dq = dadd(dst0, s * DkvCfg::kStage), ddo = dadd(dq, 2 * kAtAtom64);
 #pragma unroll
@@ -973,31 +1066,44 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::mma_commit(&sp_full[b2]);
         return true;
       };
-      if (ok && n > 0) ok = issue_sp(0);
-      for (int t = 0; ok && t < n; ++t) {
-        if (t + 1 < n && !issue_sp(t + 1)) {
+      bool ok = true;
+      int it = 0, gs = 0;
+      for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
+        const int n = item_of(item).n;  // >= hpc * 2
+        if (!ptx::mbar_wait(kv_full, it & 1, abort_flag) || !issue_sp(gs)) {
           ok = false;
           break;
         }
-        if (!ptx::mbar_wait(&ds_full[t & 1], (t >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
+        for (int u = 0; u < n; ++u) {
+          const int cur = gs + u;
+          if (u + 1 < n) {
+            if (!issue_sp(cur + 1)) {
+              ok = false;
+              break;
+            }
+            if (u + 2 == n) ptx::mma_commit(kv_empty);  // the item's last S^T / dP^T have been issued
+          }
+          if (!ptx::mbar_wait(&ds_full[cur & 1], (cur >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t qmn = dadd(dstmn0, (cur % kKvStages) * DkvCfg::kStage), domn = dadd(qmn, 2 * kAtAtom64);
+          const uint64_t dpt = dadd(dpt0, (cur & 1) * kAtAtom128), ddst = dadd(ddst0, (cur & 1) * kAtAtom128);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_bf16(tmem + 256u, kstep(dpt, kk, kAtAtom128), mnstep(domn, kk), id_g, (u | kk) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_bf16(tmem + 384u, kstep(ddst, kk, kAtAtom128), mnstep(qmn, kk), id_g, (u | kk) ? 1u : 0u);
+          ptx::mma_commit(&ds_empty[cur & 1]);
+          ptx::mma_commit(&st_empty[cur % kKvStages]);
         }
-        ptx::tc_fence_after();
-        const uint64_t qmn = dadd(dstmn0, (t % kKvStages) * DkvCfg::kStage), domn = dadd(qmn, 2 * kAtAtom64);
-        const uint64_t dpt = dadd(dpt0, (t & 1) * kAtAtom128), ddst = dadd(ddst0, (t & 1) * kAtAtom128);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_bf16(tmem + 256u, kstep(dpt, kk, kAtAtom128), mnstep(domn, kk), id_g, (t | kk) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_bf16(tmem + 384u, kstep(ddst, kk, kAtAtom128), mnstep(qmn, kk), id_g, (t | kk) ? 1u : 0u);
-        ptx::mma_commit(&ds_empty[t & 1]);
-        ptx::mma_commit(&st_empty[t % kKvStages]);
-      }
-      if (ok) {
+        if (!ok) break;
         ptx::mma_commit(acc_full);
-      } else {
+        gs += n;
+      }
+      if (!ok) {
         give_up();
         ptx::mma_commit(drain);
         ptx::mbar_wait(drain, 0, nullptr);
@@ -1009,7 +1115,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // key row in the tile
-    const int kpos = kt * 128 + r;      // key position in the sequence
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     auto wait_all = [&](uint64_t* bar, uint32_t par) {
       bool w = ptx::mbar_wait(bar, par, abort_flag);
@@ -1018,102 +1123,114 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       return w;
     };
     bool ok = true;
-    for (int t = 0; t < n; ++t) {
-      const int b2 = t & 1;
-      if (!wait_all(&sp_full[b2], (t >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      // this half's 32 query rows: lse (scaled to log2) and Di, from the stage's shared copy
-      const uint32_t ls_addr = ptx::smem_addr(smem + DkvCfg::kOffLD) + (t % kKvStages) * 512 + half * 128;
-      float lse2[32], dis[32];
+    int it = 0, gs = 0;
+    for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
+      const Item t = item_of(item);
+      const int kpos = t.kt * 128 + r;  // key position in the sequence
+      for (int u = 0; u < t.n; ++u) {
+        const int cur = gs + u;
+        const int b2 = cur & 1;
+        if (!wait_all(&sp_full[b2], (cur >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        // this half's 32 query rows: lse (scaled to log2) and Di, from the stage's shared copy
+        const uint32_t ls_addr = ptx::smem_addr(smem + DkvCfg::kOffLD) + (cur % kKvStages) * 512 + half * 128;
+        float lse2[32], dis[32];
 #pragma unroll
-      for (int v4 = 0; v4 < 8; ++v4) {
-        const float4 lv = lds128(ls_addr + v4 * 16), dv4 = lds128(ls_addr + 256 + v4 * 16);
-        lse2[4 * v4] = lv.x * kLog2e;
-        lse2[4 * v4 + 1] = lv.y * kLog2e;
-        lse2[4 * v4 + 2] = lv.z * kLog2e;
-        lse2[4 * v4 + 3] = lv.w * kLog2e;
-        dis[4 * v4] = dv4.x;
-        dis[4 * v4 + 1] = dv4.y;
-        dis[4 * v4 + 2] = dv4.z;
-        dis[4 * v4 + 3] = dv4.w;
-      }
-      const int q0 = (2 * kt + t % nqb) * 64 + half * 32;
-      uint32_t wp[16], wd[16];
-      {
-        uint32_t us[32], up[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(b2 * 64 + half * 32), us);
-        ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(b2 * 64 + half * 32), up);
-        ptx::tmem_wait_ld();
+        for (int v4 = 0; v4 < 8; ++v4) {
+          const float4 lv = lds128(ls_addr + v4 * 16), dv4 = lds128(ls_addr + 256 + v4 * 16);
+          lse2[4 * v4] = lv.x * kLog2e;
+          lse2[4 * v4 + 1] = lv.y * kLog2e;
+          lse2[4 * v4 + 2] = lv.z * kLog2e;
+          lse2[4 * v4 + 3] = lv.w * kLog2e;
+          dis[4 * v4] = dv4.x;
+          dis[4 * v4 + 1] = dv4.y;
+          dis[4 * v4 + 2] = dv4.z;
+          dis[4 * v4 + 3] = dv4.w;
+        }
+        const int q0 = (2 * t.kt + u % t.nqb) * 64 + half * 32;
+        uint32_t wp[16], wd[16];
+        {
+          uint32_t us[32], up[32];
+          ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(b2 * 64 + half * 32), us);
+          ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(b2 * 64 + half * 32), up);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p2[2], d2[2];
+          for (int e = 0; e < 32; e += 2) {
+            float p2[2], d2[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qi = e + u;
-            const float p =
-                (q0 + qi >= kpos) ? ex2(fmaf(__uint_as_float(us[qi]), a.c, -lse2[qi])) : 0.0f;
-            p2[u] = p;
-            d2[u] = p * (__uint_as_float(up[qi]) - dis[qi]);
+            for (int v = 0; v < 2; ++v) {
+              const int qi = e + v;
+              const float p = (q0 + qi >= kpos) ? ex2(fmaf(__uint_as_float(us[qi]), a.c, -lse2[qi])) : 0.0f;
+              p2[v] = p;
+              d2[v] = p * (__uint_as_float(up[qi]) - dis[qi]);
+            }
+            wp[e / 2] = pack2(p2[0], p2[1]);
+            wd[e / 2] = pack2(d2[0], d2[1]);
           }
-          wp[e / 2] = pack2(p2[0], p2[1]);
-          wd[e / 2] = pack2(d2[0], d2[1]);
         }
+        // buffer cur & 1 must have been consumed by the MMAs of iteration cur - 2
+        if (!wait_all(&ds_empty[b2], ((cur >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t pt_buf = ptx::smem_addr(sPT) + b2 * kAtAtom128;
+        const uint32_t dst_buf = ptx::smem_addr(sDST) + b2 * kAtAtom128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          sts_swz(pt_buf, r, half * 4 + q4, wp[4 * q4], wp[4 * q4 + 1], wp[4 * q4 + 2], wp[4 * q4 + 3]);
+          sts_swz(dst_buf, r, half * 4 + q4, wd[4 * q4], wd[4 * q4 + 1], wd[4 * q4 + 2], wd[4 * q4 + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ds_full[b2]);
       }
-      // buffer t & 1 must have been consumed by the MMAs of iteration t - 2
-      if (!wait_all(&ds_empty[t & 1], ((t >> 1) & 1) ^ 1)) {
+      if (!ok || !wait_all(acc_full, it & 1)) {
         ok = false;
         break;
       }
-      const uint32_t pt_buf = ptx::smem_addr(sPT) + (t & 1) * kAtAtom128;
-      const uint32_t dst_buf = ptx::smem_addr(sDST) + (t & 1) * kAtAtom128;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        sts_swz(pt_buf, r, half * 4 + q4, wp[4 * q4], wp[4 * q4 + 1], wp[4 * q4 + 2], wp[4 * q4 + 3]);
-        sts_swz(dst_buf, r, half * 4 + q4, wd[4 * q4], wd[4 * q4 + 1], wd[4 * q4 + 2], wd[4 * q4 + 3]);
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ds_full[t & 1]);
-    }
-    const bool fin = ok && n > 0 && wait_all(acc_full, 0);
-    if (fin && hpc == a.H / a.Hkv) {
-      // every query head of the kv head is in: dV and dK of rotation pairs 32 half ..
+      // dV and dK leave TMEM before this warp's next arrival, after which the
+      // next item's first MMAs overwrite them
       ptx::tc_fence_after();
-      uint32_t lo[32], hi[32];
-      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(half * 32), lo);
-      ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(64 + half * 32), hi);
-      ptx::tmem_wait_ld();
-      store_grad_pairs(lo, hi, 1.0f, nullptr, 0, half, a.out1 + static_cast<int64_t>(key0 + r) * a.ld1 + g * 128);
-      ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(half * 32), lo);
-      ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(64 + half * 32), hi);
-      ptx::tmem_wait_ld();
-      store_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, kpos, half,
-                       a.out0 + static_cast<int64_t>(key0 + r) * a.ld0 + g * 128);
-    } else if (fin) {
-      // fp32 partials of this query head, row key0 + r, columns 64 half ..
-      ptx::tc_fence_after();
-      const int64_t row = static_cast<int64_t>(h0) * M + key0 + r;
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        float* dst = (part ? part_dk : part_dv) + row * 128 + half * 64;
-        uint32_t u0[32], u1[32];
-        const uint32_t base = lane_base + (part ? 384u : 256u) + static_cast<uint32_t>(half * 64);
-        ptx::tmem_ld_32x32b_x32(base, u0);
-        ptx::tmem_ld_32x32b_x32(base + 32, u1);
+      if (hpc == a.H / a.Hkv) {
+        // every query head of the kv head is in: dV and dK of rotation pairs 32 half ..
+        uint32_t lo[32], hi[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(half * 32), lo);
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(64 + half * 32), hi);
         ptx::tmem_wait_ld();
+        store_grad_pairs(lo, hi, 1.0f, nullptr, 0, half, a.out1 + static_cast<int64_t>(t.key0 + r) * a.ld1 + t.g * 128);
+        ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(half * 32), lo);
+        ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(64 + half * 32), hi);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        store_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, kpos, half,
+                         a.out0 + static_cast<int64_t>(t.key0 + r) * a.ld0 + t.g * 128);
+      } else {
+        // fp32 partials of this query head, row key0 + r, columns 64 half ..
+        const int64_t row = static_cast<int64_t>(t.h0) * M + t.key0 + r;
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          reinterpret_cast<float4*>(dst)[e / 4] = make_float4(__uint_as_float(u0[e]), __uint_as_float(u0[e + 1]),
-                                                              __uint_as_float(u0[e + 2]), __uint_as_float(u0[e + 3]));
-          reinterpret_cast<float4*>(dst + 32)[e / 4] =
-              make_float4(__uint_as_float(u1[e]), __uint_as_float(u1[e + 1]), __uint_as_float(u1[e + 2]),
-                          __uint_as_float(u1[e + 3]));
+        for (int part = 0; part < 2; ++part) {
+          float* dst = (part ? part_dk : part_dv) + row * 128 + half * 64;
+          uint32_t u0[32], u1[32];
+          const uint32_t base = lane_base + (part ? 384u : 256u) + static_cast<uint32_t>(half * 64);
+          ptx::tmem_ld_32x32b_x32(base, u0);
+          ptx::tmem_ld_32x32b_x32(base + 32, u1);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            reinterpret_cast<float4*>(dst)[e / 4] = make_float4(__uint_as_float(u0[e]), __uint_as_float(u0[e + 1]),
+                                                                __uint_as_float(u0[e + 2]), __uint_as_float(u0[e + 3]));
+            reinterpret_cast<float4*>(dst + 32)[e / 4] =
+                make_float4(__uint_as_float(u1[e]), __uint_as_float(u1[e + 1]), __uint_as_float(u1[e + 2]),
+                            __uint_as_float(u1[e + 3]));
+          }
         }
+        ptx::tc_fence_before();
       }
+      gs += t.n;
     }
   }
   ptx::tc_fence_before();
@@ -1344,7 +1461,8 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
     ad.out0 = dq;
     ad.ld0 = lddq;
     if ((st = set_smem(attn_dq_kernel, DqCfg::kSmem)) != SL_OK) return st;
-    const unsigned grid = static_cast<unsigned>((sh.S / 128) * sh.H * a.nseq);
+    const int64_t items = (sh.S / 128) * sh.H * a.nseq;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, num_sms()));
     if ((st = launch_pdl("attn_dq_kernel", attn_dq_kernel, dim3(grid), dim3(kAtThreads), DqCfg::kSmem, stream, mq, mdo,
                          mk, mv, ad)) != SL_OK)
       return st;
@@ -1367,8 +1485,8 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
     float* part_dk = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(Di) + di_bytes(sh.M, sh.H));
     float* part_dv = part_dk + static_cast<size_t>(sh.M) * sh.H * 128;
     if ((st = set_smem(attn_dkdv_kernel, DkvCfg::kSmem)) != SL_OK) return st;
-    // a CTA per kv head when that alone fills the GPU or a kv head has one query
-    // head (no partials), else per query head
+    // an item per kv head when that alone fills the GPU or a kv head has one
+    // query head (no partials), else per query head
     const bool direct = sh.H == sh.Hkv || (sh.S / 128) * sh.Hkv * a.nseq >= num_sms();
     AttnArgs ak = a;
     ak.heads_per_cta = direct ? sh.H / sh.Hkv : 1;
@@ -1376,7 +1494,8 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
     ak.ld0 = lddk;
     ak.out1 = dv;
     ak.ld1 = lddv;
-    const unsigned grid = static_cast<unsigned>((sh.S / 128) * (sh.H / ak.heads_per_cta) * a.nseq);
+    const int64_t items = (sh.S / 128) * (sh.H / ak.heads_per_cta) * a.nseq;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, num_sms()));
     if ((st = launch_pdl("attn_dkdv_kernel", attn_dkdv_kernel, dim3(grid), dim3(kAtThreads), DkvCfg::kSmem, stream, mq,
                          mdo, mk, mv, ml, md, ak, part_dk, part_dv)) != SL_OK)
       return st;
