@@ -63,13 +63,6 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Store 16 bytes at chunk c (0..7) of row `row` of a 128-byte-swizzled atom
-// at shared address `atom` (st.shared: the address space is explicit).
-__device__ __forceinline__ void sts_swz(uint32_t atom, int row, int c, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(atom + row * 128 + ((c ^ (row & 7)) << 4)), "r"(x),
-               "r"(y), "r"(z), "r"(w)
-               : "memory");
-}
 __device__ __forceinline__ float4 lds128(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -172,8 +165,7 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kAtTile;        // 2 stages
   static constexpr int kOffV = kOffK + 2 * kAtTile;    // 2 stages
-  static constexpr int kOffP = kOffV + 2 * kAtTile;
-  static constexpr int kOffRed = kOffP + kAtTile;       // row maxima [2][2][128], row sums [2][128], stop flags
+  static constexpr int kOffRed = kOffV + 2 * kAtTile;  // row maxima [2][2][128], row sums [2][128], stop flags
   static constexpr int kOffBar = kOffRed + 6 * 128 * 4 + 16;
   static constexpr int kNumBars = 20;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -194,7 +186,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sQ = smem + FwdCfg::kOffQ;
   uint8_t* sK = smem + FwdCfg::kOffK;
   uint8_t* sV = smem + FwdCfg::kOffV;
-  uint8_t* sP = smem + FwdCfg::kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FwdCfg::kOffBar);
   uint64_t* q_full = bars;        // Q of the item landed
   uint64_t* k_full = bars + 1;    // [2] K tile of the stage landed
@@ -245,8 +236,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     ptx::mbar_init(p_full, kAtWorkers);
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
-    reinterpret_cast<volatile int*>(sP + kAtTile + 6 * 128 * 4)[0] = 0;
-    reinterpret_cast<volatile int*>(sP + kAtTile + 6 * 128 * 4)[1] = 0;
+    reinterpret_cast<volatile int*>(smem + FwdCfg::kOffRed + 6 * 128 * 4)[0] = 0;
+    reinterpret_cast<volatile int*>(smem + FwdCfg::kOffRed + 6 * 128 * 4)[1] = 0;
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&map_q);
     ptx::tma_prefetch_desc(&map_k);
@@ -319,7 +310,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       constexpr uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t id_o = ptx::idesc_bf16(128, 128, 0, 1);
       const uint64_t dq0 = kdesc0(ptx::smem_addr(sQ)), dk0 = kdesc0(ptx::smem_addr(sK)),
-                     dp0 = kdesc0(ptx::smem_addr(sP)), dv0 = mndesc0(ptx::smem_addr(sV), kAtAtom128);
+                     dv0 = mndesc0(ptx::smem_addr(sV), kAtAtom128);
       auto issue_s = [&](int gt) {  // S of the CTA's tile gt into TMEM buffer gt & 1
         const int s = gt & 1;
         if (!ptx::mbar_wait(&k_full[s], (gt >> 1) & 1, abort_flag)) return false;
@@ -361,9 +352,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ptx::tc_fence_after();
           const uint32_t d = tmem + 256u + static_cast<uint32_t>(s * 128);
           const uint64_t dv = dadd(dv0, s * kAtTile);
+          // P of keys 16 kk ..: the column half kk / 4 wrote it over its first 32 S columns
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            ptx::mma_bf16(d, kstep(dp0, kk, kAtAtom128), mnstep(dv, kk), id_o, kk ? 1u : 0u);
+            ptx::mma_bf16_ts(d, tmem + static_cast<uint32_t>(s * 128 + (kk >> 2) * 64 + (kk & 3) * 8), mnstep(dv, kk),
+                             id_o, kk ? 1u : 0u);
           ptx::mma_commit(&o_full[s]);
           ptx::mma_commit(&v_empty[s]);
         }
@@ -387,9 +380,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // query row in the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 64);
-    float* red = reinterpret_cast<float*>(sP + kAtTile);  // maxima [2 parity][2 half][128], sums [2 half][128]
+    float* red = reinterpret_cast<float*>(smem + FwdCfg::kOffRed);  // maxima [2 parity][2 half][128], sums [2][128]
     volatile int* stop = reinterpret_cast<volatile int*>(red + 6 * 128);  // [2 parity]
-    const uint32_t atom = ptx::smem_addr(sP) + half * kAtAtom128;
     auto wait_all = [&](uint64_t* bar, uint32_t par) {
       bool w = ptx::mbar_wait(bar, par, abort_flag);
       w = __all_sync(0xffffffffu, w);
@@ -458,14 +450,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
         const float m_new = fmaxf(m, fmaxf(mt, red[(s * 2 + (half ^ 1)) * 128 + r]) * a.c);
         const float alpha = ex2(m - m_new);
-        // O_part of the previous tile joins O with the previous alpha; this also
-        // frees the P tile (its MMA has completed)
-        if (j > 0 && !accumulate(cur - 1)) {
-          bad = true;
-          continue;  // raise the stop flag at the next barrier
-        }
-        alpha_prev = alpha;
-        // P = exp2(S c - m_new) as bf16 into this half's atom of the P tile
+        // P = exp2(S c - m_new) as bf16 pairs over the first 32 of the 64 S
+        // columns this thread has read (every worker has read its S: the
+        // barrier above), the P V MMA's A operand
         float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -478,16 +465,21 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             ls[(e + 1) & 3] += p1;
             w[e / 2] = pack2(p0, p1);
           }
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            sts_swz(atom, r, c * 4 + q4, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+          ptx::tmem_st_32x32b_x16(lane_base + static_cast<uint32_t>(s * 128 + c * 16), w);
         }
-        l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-        m = m_new;
-        ptx::fence_proxy_async_smem();
+        ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(p_full);
+        l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        m = m_new;
+        // O_part of the previous tile joins O with the previous alpha, while
+        // the tensor pipe runs this tile's P V
+        if (j > 0 && !accumulate(cur - 1)) {
+          bad = true;
+          continue;  // raise the stop flag at the next barrier
+        }
+        alpha_prev = alpha;
       }
       if (stopped) break;
       // the last O_part, then the two halves' row sums (the barrier of the
@@ -595,6 +587,13 @@ __device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const
 }
 
 // ------------------------------------------------------------ dQ
+// TMEM column of k16 step kk (keys 16 kk ..) of a 64-key block's bf16 dS or
+// P^T / dS^T stored over fp32 buffer b (64 columns at 64 b): each half of the
+// block (32 keys) sits in the first 16 columns of its own 32.
+__device__ __forceinline__ uint32_t ds_col(int b, int kk) {
+  return static_cast<uint32_t>(b * 64 + (kk >> 1) * 32 + (kk & 1) * 8);
+}
+
 constexpr int kAtStages = 3;  // key/value ring of the dQ kernel
 constexpr int kKvStages = 3;  // query/dO ring of the dK dV kernel
 
@@ -603,8 +602,7 @@ struct DqCfg {
   static constexpr int kOffDO = kOffQ + kAtTile;       // [128][128]
   static constexpr int kOffK = kOffDO + kAtTile;       // kAtStages stages of [64][128]
   static constexpr int kOffV = kOffK + kAtStages * 2 * kAtAtom64;
-  static constexpr int kOffDS = kOffV + kAtStages * 2 * kAtAtom64;  // 2 buffers of [128][64]
-  static constexpr int kOffBar = kOffDS + 2 * kAtAtom128;
+  static constexpr int kOffBar = kOffV + kAtStages * 2 * kAtAtom64;
   static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
@@ -625,14 +623,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sDO = smem + DqCfg::kOffDO;
   uint8_t* sK = smem + DqCfg::kOffK;
   uint8_t* sV = smem + DqCfg::kOffV;
-  uint8_t* sDS = smem + DqCfg::kOffDS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DqCfg::kOffBar);
   uint64_t* q_full = bars;         // Q and dO of the item landed
   uint64_t* kv_full = bars + 1;    // [kAtStages]
   uint64_t* kv_empty = bars + 4;   // [kAtStages]
   uint64_t* sp_full = bars + 7;    // [2] S and dP in TMEM buffer b
-  uint64_t* ds_full = bars + 9;    // [2] dS buffer b written (8 warp arrivals); S/dP buffer b read
-  uint64_t* ds_empty = bars + 11;  // [2] the dQ MMA of dS buffer b done
+  uint64_t* ds_full = bars + 9;    // [2] dS written over S in buffer b (8 warp arrivals)
   uint64_t* acc_full = bars + 13;  // dQ of the item complete
   uint64_t* drain = bars + 14;     // failure path: every issued MMA completed
   uint64_t* q_empty = bars + 15;   // the item's last S / dP MMAs done: Q and dO may be replaced
@@ -667,10 +663,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       ptx::mbar_init(&kv_full[i], 1);
       ptx::mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) ptx::mbar_init(&sp_full[i], 1);
     for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&sp_full[i], 1);
       ptx::mbar_init(&ds_full[i], kAtWorkers);
-      ptx::mbar_init(&ds_empty[i], 1);
     }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain, 1);
@@ -692,7 +687,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   // No early pdl_trigger: the grid keeps every SM busy until its end; the
   // next kernel launches as its CTAs exit.
   pdl_wait();  // the previous kernel's writes are visible from here on
-  // TMEM: S buffers at 0 / 64, dP at 128 / 192, dQ at 256
+  // TMEM: S buffers at 0 / 64 (dS over them as bf16 pairs), dP at 128 / 192,
+  // dQ at 256.  A buffer is rewritten by the S MMA two blocks later, which the
+  // tensor pipe runs after the dQ MMA that reads its dS (issue order).
   auto give_up = [&]() {
     *abort_flag = 1;
     report_device_error(a.err, SL_ERR_TIMEOUT);
@@ -744,7 +741,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       constexpr uint32_t id_q = ptx::idesc_bf16(128, 128, 0, 1);
       const uint64_t dq0 = kdesc0(ptx::smem_addr(sQ)), ddo0 = kdesc0(ptx::smem_addr(sDO)),
                      dk0 = kdesc0(ptx::smem_addr(sK)), dv0 = kdesc0(ptx::smem_addr(sV)),
-                     dkmn0 = mndesc0(ptx::smem_addr(sK), kAtAtom64), dds0 = kdesc0(ptx::smem_addr(sDS));
+                     dkmn0 = mndesc0(ptx::smem_addr(sK), kAtAtom64);
       auto issue_sp = [&](int gb) {  // S and dP of the CTA's block gb into TMEM buffer gb & 1
         const int s = gb % kAtStages, b2 = gb & 1;
         if (!ptx::mbar_wait(&kv_full[s], (gb / kAtStages) & 1, abort_flag)) return false;
@@ -784,11 +781,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           }
           ptx::tc_fence_after();
           const uint64_t dkmn = dadd(dkmn0, (cur % kAtStages) * 2 * kAtAtom64);
-          const uint64_t dds = dadd(dds0, (cur & 1) * kAtAtom128);
+          // dS of keys 16 kk .. in the columns the two halves wrote (see the workers)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_bf16(tmem + 256u, kstep(dds, kk, kAtAtom128), mnstep(dkmn, kk), id_q, (j | kk) ? 1u : 0u);
-          ptx::mma_commit(&ds_empty[cur & 1]);
+            ptx::mma_bf16_ts(tmem + 256u, tmem + ds_col(cur & 1, kk), mnstep(dkmn, kk), id_q, (j | kk) ? 1u : 0u);
           ptx::mma_commit(&kv_empty[cur % kAtStages]);
         }
         if (!ok) break;
@@ -847,16 +843,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             w[e / 2] = pack2(ds2[0], ds2[1]);
           }
         }
-        // dS buffer cur & 1 must have been consumed by the dQ MMA of block cur - 2
-        if (!wait_all(&ds_empty[s], ((cur >> 1) & 1) ^ 1)) {
-          ok = false;
-          break;
-        }
-        const uint32_t ds_buf = ptx::smem_addr(sDS) + s * kAtAtom128;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          sts_swz(ds_buf, r, half * 4 + q4, w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-        ptx::fence_proxy_async_smem();
+        // dS of this half's 32 keys over the first 16 columns of the S columns
+        // this thread has just read (no other warp reads them)
+        ptx::tmem_st_32x32b_x16(lane_base + static_cast<uint32_t>(s * 64 + half * 32), w);
+        ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ds_full[s]);
@@ -899,9 +889,7 @@ struct DkvCfg {
   static constexpr int kStage = 4 * kAtAtom64;              // Q [64][128], dO [64][128] (1024-aligned tiles)
   static constexpr int kStageBytes = kStage + 512;           // + lse and Di of the 64 rows
   static constexpr int kOffStage = kOffV + kAtTile;          // kKvStages stages
-  static constexpr int kOffPT = kOffStage + kKvStages * kStage;  // 2 buffers of [128][64]
-  static constexpr int kOffDST = kOffPT + 2 * kAtAtom128;        // 2 buffers of [128][64]
-  static constexpr int kOffLD = kOffDST + 2 * kAtAtom128;        // kKvStages x (lse [64], Di [64]) fp32
+  static constexpr int kOffLD = kOffStage + kKvStages * kStage;  // kKvStages x (lse [64], Di [64]) fp32
   static constexpr int kOffBar = kOffLD + kKvStages * 512;
   static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -925,15 +913,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sK = smem + DkvCfg::kOffK;
   uint8_t* sV = smem + DkvCfg::kOffV;
   uint8_t* sStage = smem + DkvCfg::kOffStage;
-  uint8_t* sPT = smem + DkvCfg::kOffPT;
-  uint8_t* sDST = smem + DkvCfg::kOffDST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DkvCfg::kOffBar);
   uint64_t* kv_full = bars;                      // K and V of the item landed
   uint64_t* st_full = bars + 1;                  // [kKvStages]
   uint64_t* st_empty = bars + 1 + kKvStages;     // [kKvStages]
   uint64_t* sp_full = bars + 1 + 2 * kKvStages;  // [2] S^T and dP^T in TMEM buffer b
-  uint64_t* ds_full = sp_full + 2;               // [2] P^T and dS^T buffer b written (8 warp arrivals)
-  uint64_t* ds_empty = sp_full + 4;              // [2] their MMAs done
+  uint64_t* ds_full = sp_full + 2;               // [2] P^T, dS^T written over buffer b (8 warp arrivals)
   uint64_t* acc_full = sp_full + 6;              // dK, dV of the item complete
   uint64_t* drain = sp_full + 7;                 // failure path: every issued MMA completed
   uint64_t* kv_empty = sp_full + 8;              // the item's last S^T / dP^T MMAs done: K, V may be replaced
@@ -973,7 +958,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&sp_full[i], 1);
       ptx::mbar_init(&ds_full[i], kAtWorkers);
-      ptx::mbar_init(&ds_empty[i], 1);
     }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain, 1);
@@ -995,7 +979,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   // No early pdl_trigger: the grid keeps every SM busy until its end; the
   // next kernel launches as its CTAs exit.
   pdl_wait();  // the previous kernel's writes are visible from here on
-  // TMEM: S^T buffers at 0 / 64, dP^T at 128 / 192, dV at 256, dK at 384
+  // TMEM: S^T buffers at 0 / 64 (P^T over them as bf16 pairs), dP^T at
+  // 128 / 192 (dS^T over them), dV at 256, dK at 384.  A buffer is rewritten
+  // by the S^T / dP^T MMAs two iterations later, which the tensor pipe runs
+  // after the dV / dK MMAs that read it (issue order).
   auto give_up = [&]() {
     *abort_flag = 1;
     report_device_error(a.err, SL_ERR_TIMEOUT);
@@ -1048,8 +1035,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       constexpr uint32_t id_s = ptx::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_g = ptx::idesc_bf16(128, 128, 0, 1);
       const uint64_t dk0 = kdesc0(ptx::smem_addr(sK)), dv0 = kdesc0(ptx::smem_addr(sV)),
-                     dst0 = kdesc0(ptx::smem_addr(sStage)), dstmn0 = mndesc0(ptx::smem_addr(sStage), kAtAtom64),
-                     dpt0 = kdesc0(ptx::smem_addr(sPT)), ddst0 = kdesc0(ptx::smem_addr(sDST));
+                     dst0 = kdesc0(ptx::smem_addr(sStage)), dstmn0 = mndesc0(ptx::smem_addr(sStage), kAtAtom64);
       auto issue_sp = [&](int gs) {  // S^T and dP^T of the CTA's iteration gs into TMEM buffer gs & 1
         const int s = gs % kKvStages, b2 = gs & 1;
         if (!ptx::mbar_wait(&st_full[s], (gs / kKvStages) & 1, abort_flag)) return false;
@@ -1089,14 +1075,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           }
           ptx::tc_fence_after();
           const uint64_t qmn = dadd(dstmn0, (cur % kKvStages) * DkvCfg::kStage), domn = dadd(qmn, 2 * kAtAtom64);
-          const uint64_t dpt = dadd(dpt0, (cur & 1) * kAtAtom128), ddst = dadd(ddst0, (cur & 1) * kAtAtom128);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_bf16(tmem + 256u, kstep(dpt, kk, kAtAtom128), mnstep(domn, kk), id_g, (u | kk) ? 1u : 0u);
+            ptx::mma_bf16_ts(tmem + 256u, tmem + ds_col(cur & 1, kk), mnstep(domn, kk), id_g, (u | kk) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_bf16(tmem + 384u, kstep(ddst, kk, kAtAtom128), mnstep(qmn, kk), id_g, (u | kk) ? 1u : 0u);
-          ptx::mma_commit(&ds_empty[cur & 1]);
+            ptx::mma_bf16_ts(tmem + 384u, tmem + 128u + ds_col(cur & 1, kk), mnstep(qmn, kk), id_g,
+                             (u | kk) ? 1u : 0u);
           ptx::mma_commit(&st_empty[cur % kKvStages]);
         }
         if (!ok) break;
@@ -1171,19 +1156,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             wd[e / 2] = pack2(d2[0], d2[1]);
           }
         }
-        // buffer cur & 1 must have been consumed by the MMAs of iteration cur - 2
-        if (!wait_all(&ds_empty[b2], ((cur >> 1) & 1) ^ 1)) {
-          ok = false;
-          break;
-        }
-        const uint32_t pt_buf = ptx::smem_addr(sPT) + b2 * kAtAtom128;
-        const uint32_t dst_buf = ptx::smem_addr(sDST) + b2 * kAtAtom128;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          sts_swz(pt_buf, r, half * 4 + q4, wp[4 * q4], wp[4 * q4 + 1], wp[4 * q4 + 2], wp[4 * q4 + 3]);
-          sts_swz(dst_buf, r, half * 4 + q4, wd[4 * q4], wd[4 * q4 + 1], wd[4 * q4 + 2], wd[4 * q4 + 3]);
-        }
-        ptx::fence_proxy_async_smem();
+        // P^T and dS^T of this half's 32 queries over the first 16 columns of
+        // the S^T and dP^T columns this thread has just read
+        ptx::tmem_st_32x32b_x16(lane_base + static_cast<uint32_t>(b2 * 64 + half * 32), wp);
+        ptx::tmem_st_32x32b_x16(lane_base + 128u + static_cast<uint32_t>(b2 * 64 + half * 32), wd);
+        ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ds_full[b2]);
