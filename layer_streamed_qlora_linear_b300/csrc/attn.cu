@@ -11,23 +11,30 @@
 // (K released once S is computed, V once P V is).  The MMA warp computes
 // S = Q K^T into one of two TMEM buffers one tile ahead.  Eight row workers
 // (TMEM lane quarter x column half; 64 scores per thread) exchange their
-// row maxima through shared memory, write P = exp2(S c - m) as bf16 into a
-// 128-byte-swizzled tile, and the MMA warp computes O_part = P V (V as an
-// MN-major operand) into one of two more TMEM buffers.  The workers keep O
-// in registers: O = O alpha + O_part with alpha = exp2(m_old - m_new).
+// row maxima through shared memory and write P = exp2(S c - m) as bf16
+// pairs back into TMEM over the scores; the MMA warp computes O_part = P V
+// with P as a TMEM operand and V as an MN-major shared operand, into one of
+// two more TMEM buffers.  The workers keep O in registers:
+// O = O alpha + O_part with alpha = exp2(m_old - m_new), folding in the
+// previous tile's O_part while the tensor pipe runs the current P V.
 //
 // Backward (no atomics: every output element is summed in one CTA in a
 // fixed order, so results are bitwise reproducible):
-//   dq kernel  (items: 128-query tile and head): over the key blocks of 64,
-//              S = Q K^T and dP = dO V^T, dS = P (dP - Di) into a
-//              double-buffered shared tile, dQ += dS K;
+//   dq kernel  (items: 128-query tile and head): over the key blocks of 64
+//              (a three-stage ring), S = Q K^T and dP = dO V^T into TMEM,
+//              dS = P (dP - Di) written back over S, dQ += dS K with dS as
+//              a TMEM operand;
 //   dkdv kernel (items: 128-key tile and kv head, or query head when the
 //              kv heads alone leave SMs idle): over the query blocks of 64
 //              that see the key tile (a three-stage ring), S^T = K Q^T and
-//              dP^T = V dO^T, P^T and dS^T into double-buffered shared
-//              tiles, dV += P^T dO, dK += dS^T Q; per-query-head results
-//              leave as fp32 partials that attn_kv_reduce_kernel sums over
-//              the heads of each kv head in head order.
+//              dP^T = V dO^T into TMEM, P^T and dS^T written back over
+//              them, dV += P^T dO and dK += dS^T Q with TMEM operands;
+//              per-query-head results leave as fp32 partials that
+//              attn_kv_reduce_kernel sums over the heads of each kv head in
+//              head order.
+// A TMEM buffer is rewritten by the MMA two blocks later, which the tensor
+// pipe runs after the MMA that read it (tcgen05.mma ops of one thread run in
+// issue order).
 // Di = rowsum(dO * O) comes from a small pre-pass.  The epilogues scale dQ
 // and dK by 1/sqrt(128) and rotate them back by the inverse rotary angle.
 // Every wait is bounded; a timeout raises SL_ERR_TIMEOUT through the
@@ -625,13 +632,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sV = smem + DqCfg::kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DqCfg::kOffBar);
   uint64_t* q_full = bars;         // Q and dO of the item landed
-  uint64_t* kv_full = bars + 1;    // [kAtStages]
-  uint64_t* kv_empty = bars + 4;   // [kAtStages]
-  uint64_t* sp_full = bars + 7;    // [2] S and dP in TMEM buffer b
-  uint64_t* ds_full = bars + 9;    // [2] dS written over S in buffer b (8 warp arrivals)
-  uint64_t* acc_full = bars + 13;  // dQ of the item complete
-  uint64_t* drain = bars + 14;     // failure path: every issued MMA completed
-  uint64_t* q_empty = bars + 15;   // the item's last S / dP MMAs done: Q and dO may be replaced
+  uint64_t* kv_full = bars + 1;                  // [kAtStages]
+  uint64_t* kv_empty = bars + 1 + kAtStages;     // [kAtStages]
+  uint64_t* sp_full = bars + 1 + 2 * kAtStages;  // [2] S and dP in TMEM buffer b
+  uint64_t* ds_full = sp_full + 2;               // [2] dS written over S in buffer b (8 warp arrivals)
+  uint64_t* acc_full = sp_full + 4;              // dQ of the item complete
+  uint64_t* drain = sp_full + 5;                 // failure path: every issued MMA completed
+  uint64_t* q_empty = sp_full + 6;               // the item's last S / dP MMAs done: Q and dO may be replaced
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DqCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DqCfg::kOffMisc + 4);
 
@@ -896,6 +903,8 @@ struct DkvCfg {
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
 static_assert(DkvCfg::kSmem <= 232448, "dK/dV shared memory exceeds the per-CTA limit");
+static_assert(DqCfg::kSmem <= 232448, "dQ shared memory exceeds the per-CTA limit");
+static_assert(1 + 2 * kAtStages + 7 <= DqCfg::kNumBars, "dQ barrier count");
 static_assert(1 + 2 * kKvStages + 9 <= DkvCfg::kNumBars, "dK/dV barrier count");
 
 // Persistent: one CTA per SM walks the (key tile, head group, sequence)
