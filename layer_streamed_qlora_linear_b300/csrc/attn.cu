@@ -70,6 +70,13 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Store 16 bytes at chunk c (0..7) of row `row` of a 128-byte-swizzled atom
+// at shared address `atom` (st.shared: the address space is explicit).
+__device__ __forceinline__ void sts_swz(uint32_t atom, int row, int c, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(atom + row * 128 + ((c ^ (row & 7)) << 4)), "r"(x),
+               "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
 __device__ __forceinline__ float4 lds128(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -172,7 +179,8 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kAtTile;        // 2 stages
   static constexpr int kOffV = kOffK + 2 * kAtTile;    // 2 stages
-  static constexpr int kOffRed = kOffV + 2 * kAtTile;  // row maxima [2][2][128], row sums [2][128], stop flags
+  static constexpr int kOffO = kOffV + 2 * kAtTile;    // O staging for its TMA store: 2 atoms of [128][64]
+  static constexpr int kOffRed = kOffO + kAtTile;       // row maxima [2][2][128], row sums [2][128], stop flags
   static constexpr int kOffBar = kOffRed + 6 * 128 * 4 + 16;
   static constexpr int kNumBars = 20;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -187,7 +195,8 @@ struct FwdCfg {
 // completed, while the row workers finish the item.
 __global__ void __launch_bounds__(kAtThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                    const __grid_constant__ CUtensorMap map_v, const AttnArgs a) {
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                    const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = ptx::align1024(smem_raw);
   uint8_t* sQ = smem + FwdCfg::kOffQ;
@@ -249,6 +258,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     ptx::tma_prefetch_desc(&map_q);
     ptx::tma_prefetch_desc(&map_k);
     ptx::tma_prefetch_desc(&map_v);
+    ptx::tma_prefetch_desc(&map_o);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, 512);
@@ -388,6 +398,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int r = quarter * 32 + lane;  // query row in the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 64);
     float* red = reinterpret_cast<float*>(smem + FwdCfg::kOffRed);  // maxima [2 parity][2 half][128], sums [2][128]
+    const uint32_t o_atom = ptx::smem_addr(smem + FwdCfg::kOffO) + half * kAtAtom128;
     volatile int* stop = reinterpret_cast<volatile int*>(red + 6 * 128);  // [2 parity]
     auto wait_all = [&](uint64_t* bar, uint32_t par) {
       bool w = ptx::mbar_wait(bar, par, abort_flag);
@@ -503,18 +514,28 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       const Item t = item_of(item);
       const float lrow = red[(4 + 0) * 128 + r] + red[(4 + 1) * 128 + r];
       const float inv = 1.0f / lrow;
-      uint16_t* dst = a.out0 + static_cast<int64_t>(t.row0 + r) * a.ld0 + t.h * 128 + half * 64;
+      // O leaves through shared memory: this warp's 32 rows x 64 columns are
+      // one TMA box (its previous box has been read out before it is reused)
+      if (lane == 0) ptx::bulk_wait_read0();
+      __syncwarp();
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        reinterpret_cast<uint4*>(dst)[c] =
-            make_uint4(pack2(O[8 * c] * inv, O[8 * c + 1] * inv), pack2(O[8 * c + 2] * inv, O[8 * c + 3] * inv),
-                       pack2(O[8 * c + 4] * inv, O[8 * c + 5] * inv), pack2(O[8 * c + 6] * inv, O[8 * c + 7] * inv));
+        sts_swz(o_atom, r, c, pack2(O[8 * c] * inv, O[8 * c + 1] * inv), pack2(O[8 * c + 2] * inv, O[8 * c + 3] * inv),
+                pack2(O[8 * c + 4] * inv, O[8 * c + 5] * inv), pack2(O[8 * c + 6] * inv, O[8 * c + 7] * inv));
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(&map_o, smem + FwdCfg::kOffO + half * kAtAtom128 + quarter * 32 * 128, t.h * 128 + half * 64,
+                          t.row0 + quarter * 32);
+        ptx::bulk_commit();
+      }
       if (half == 0) {
         const int64_t M = static_cast<int64_t>(a.nseq) * a.S;
         a.lse[static_cast<int64_t>(t.h) * M + t.row0 + r] = (m + log2f(lrow)) * 0.69314718055994531f;
       }
       gt = nxt;
     }
+    if (lane == 0) ptx::bulk_wait0();  // this warp's O stores are complete
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -551,11 +572,11 @@ __global__ void attn_di_kernel(const uint16_t* __restrict__ o, int64_t ldo, cons
 
 // Rotation pairs 32 half .. 32 half + 31 of one 128-wide gradient row: lo
 // holds columns 32 half .., hi columns 64 + 32 half ..; scale by 1/sqrt(128),
-// rotate back by the inverse angle of position `pos` (table may be null),
-// round to bf16 and store both 64-byte pieces of the row.
-__device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
-                                                 const float* table, int pos, int half, uint16_t* row) {
-  uint32_t o1[16], o2[16];
+// rotate back by the inverse angle of position `pos` (table may be null) and
+// round to bf16 pairs: o1 the columns 32 half .., o2 64 + 32 half ...
+__device__ __forceinline__ void grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
+                                           const float* table, int pos, int half, uint32_t (&o1)[16],
+                                           uint32_t (&o2)[16]) {
   // the table row holds cos at 0..63 and sin at 64..127; 16-byte loads
   const float4* cs = table ? reinterpret_cast<const float4*>(table + static_cast<int64_t>(pos) * 128 + half * 32)
                            : nullptr;
@@ -584,6 +605,12 @@ __device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const
     o2[e4 / 2] = pack2(y2[0], y2[1]);
     o2[e4 / 2 + 1] = pack2(y2[2], y2[3]);
   }
+}
+// ... stored straight into the gradient row
+__device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
+                                                 const float* table, int pos, int half, uint16_t* row) {
+  uint32_t o1[16], o2[16];
+  grad_pairs(lo, hi, scale, table, pos, half, o1, o2);
   uint4* d1 = reinterpret_cast<uint4*>(row + half * 32);
   uint4* d2 = reinterpret_cast<uint4*>(row + 64 + half * 32);
 #pragma unroll
@@ -592,7 +619,18 @@ __device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const
     d2[c] = make_uint4(o2[4 * c], o2[4 * c + 1], o2[4 * c + 2], o2[4 * c + 3]);
   }
 }
-
+// ... or into row r of a [128][128] staging tile of two 128-byte-swizzled
+// atoms (columns 0..63 at atom0, 64..127 at atom1) for a TMA store
+__device__ __forceinline__ void stage_grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
+                                                 const float* table, int pos, int half, uint32_t atom0, int r) {
+  uint32_t o1[16], o2[16];
+  grad_pairs(lo, hi, scale, table, pos, half, o1, o2);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    sts_swz(atom0, r, half * 4 + c, o1[4 * c], o1[4 * c + 1], o1[4 * c + 2], o1[4 * c + 3]);
+    sts_swz(atom0 + kAtAtom128, r, half * 4 + c, o2[4 * c], o2[4 * c + 1], o2[4 * c + 2], o2[4 * c + 3]);
+  }
+}
 // ------------------------------------------------------------ dQ
 // TMEM column of k16 step kk (keys 16 kk ..) of a 64-key block's bf16 dS or
 // P^T / dS^T stored over fp32 buffer b (64 columns at 64 b): each half of the
@@ -609,8 +647,9 @@ struct DqCfg {
   static constexpr int kOffDO = kOffQ + kAtTile;       // [128][128]
   static constexpr int kOffK = kOffDO + kAtTile;       // kAtStages stages of [64][128]
   static constexpr int kOffV = kOffK + kAtStages * 2 * kAtAtom64;
-  static constexpr int kOffBar = kOffV + kAtStages * 2 * kAtAtom64;
-  static constexpr int kNumBars = 18;
+  static constexpr int kOffOut = kOffV + kAtStages * 2 * kAtAtom64;  // dQ staging: 2 atoms of [128][64]
+  static constexpr int kOffBar = kOffOut + kAtTile;
+  static constexpr int kNumBars = 24;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 16 + 1024;
 };
@@ -623,7 +662,7 @@ struct DqCfg {
 __global__ void __launch_bounds__(kAtThreads, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                   const AttnArgs a) {
+                   const __grid_constant__ CUtensorMap map_dq, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = ptx::align1024(smem_raw);
   uint8_t* sQ = smem + DqCfg::kOffQ;
@@ -639,6 +678,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint64_t* acc_full = sp_full + 4;              // dQ of the item complete
   uint64_t* drain = sp_full + 5;                 // failure path: every issued MMA completed
   uint64_t* q_empty = sp_full + 6;               // the item's last S / dP MMAs done: Q and dO may be replaced
+  uint64_t* stage_full = sp_full + 7;            // [4] quarter q's staging rows written (2 warp arrivals)
+  uint64_t* stage_free = sp_full + 11;           // [4] quarter q's previous TMA stores have read them
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DqCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DqCfg::kOffMisc + 4);
 
@@ -676,12 +717,17 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      ptx::mbar_init(&stage_full[i], 2);
+      ptx::mbar_init(&stage_free[i], 1);
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&map_q);
     ptx::tma_prefetch_desc(&map_do);
     ptx::tma_prefetch_desc(&map_k);
     ptx::tma_prefetch_desc(&map_v);
+    ptx::tma_prefetch_desc(&map_dq);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, 512);
@@ -870,10 +916,40 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(64 + half * 32), hi);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
-      store_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, qrow, half,
-                       a.out0 + static_cast<int64_t>(t.row0 + r) * a.ld0 + t.h * 128);
+      // dQ leaves through shared memory: the quarter's two warps fill its 32
+      // rows of both atoms, then the half-0 warp issues one TMA store per
+      // atom.  The rows are rewritten only after the previous item's stores
+      // have read them (stage_free, raised by the issuing lane).
+      if (half == 0 && it > 0) {
+        if (lane == 0) {
+          ptx::bulk_wait_read0();
+          ptx::mbar_arrive(&stage_free[quarter]);
+        }
+        __syncwarp();
+      }
+      if (!wait_all(&stage_free[quarter], (it & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      stage_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, qrow, half, ptx::smem_addr(smem + DqCfg::kOffOut), r);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&stage_full[quarter]);
+      if (half == 0) {
+        if (!wait_all(&stage_full[quarter], it & 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* box = smem + DqCfg::kOffOut + quarter * 32 * 128;
+          ptx::tma_store_2d(&map_dq, box, t.h * 128, t.row0 + quarter * 32);
+          ptx::tma_store_2d(&map_dq, box + kAtAtom128, t.h * 128 + 64, t.row0 + quarter * 32);
+          ptx::bulk_commit();
+        }
+      }
       gb += t.n;
     }
+    if (half == 0 && lane == 0) ptx::bulk_wait0();  // this quarter's dQ stores are complete
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -904,7 +980,8 @@ struct DkvCfg {
 };
 static_assert(DkvCfg::kSmem <= 232448, "dK/dV shared memory exceeds the per-CTA limit");
 static_assert(DqCfg::kSmem <= 232448, "dQ shared memory exceeds the per-CTA limit");
-static_assert(1 + 2 * kAtStages + 7 <= DqCfg::kNumBars, "dQ barrier count");
+static_assert(FwdCfg::kSmem <= 232448, "forward shared memory exceeds the per-CTA limit");
+static_assert(1 + 2 * kAtStages + 15 <= DqCfg::kNumBars, "dQ barrier count");
 static_assert(1 + 2 * kKvStages + 9 <= DkvCfg::kNumBars, "dK/dV barrier count");
 
 // Persistent: one CTA per SM walks the (key tile, head group, sequence)
@@ -1351,10 +1428,11 @@ sl_status attention_fwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, con
   if (st != SL_OK) return st;
   SL_REQUIRE(o && lse && ldo >= sh.H * 128 && ldo % 8 == 0 && (reinterpret_cast<uintptr_t>(o) & 15) == 0,
              "attention_fwd: bad output");
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if ((st = map_rows(&mq, q, sh.H * 128, sh.M, ldq, 128)) != SL_OK) return st;
   if ((st = map_rows(&mk, k, sh.Hkv * 128, sh.M, ldk, 128)) != SL_OK) return st;
   if ((st = map_rows(&mv, v, sh.Hkv * 128, sh.M, ldv, 128)) != SL_OK) return st;
+  if ((st = map_rows(&mo, o, sh.H * 128, sh.M, ldo, 32)) != SL_OK) return st;
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   AttnArgs a{};
@@ -1372,7 +1450,7 @@ sl_status attention_fwd(const AttnShape& sh, const uint16_t* q, int64_t ldq, con
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, num_sms()));
   const TimingToken tt = timing_begin(9, 2.0 * 2.0 * kAtD * causal_pairs(sh), stream);
   st = launch_pdl("attn_fwd_kernel", attn_fwd_kernel, dim3(grid), dim3(kAtThreads), FwdCfg::kSmem, stream, mq, mk, mv,
-                  a);
+                  mo, a);
   timing_end(tt, stream);
   return st;
 }
@@ -1438,9 +1516,10 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
   a.err = err;
   // dQ
   {
-    CUtensorMap mq, mdo, mk, mv;
+    CUtensorMap mq, mdo, mk, mv, mdq;
     if ((st = map_rows(&mq, q, sh.H * 128, sh.M, ldq, 128)) != SL_OK) return st;
     if ((st = map_rows(&mdo, dout, sh.H * 128, sh.M, lddo, 128)) != SL_OK) return st;
+    if ((st = map_rows(&mdq, dq, sh.H * 128, sh.M, lddq, 32)) != SL_OK) return st;
     if ((st = map_rows(&mk, k, sh.Hkv * 128, sh.M, ldk, 64)) != SL_OK) return st;
     if ((st = map_rows(&mv, v, sh.Hkv * 128, sh.M, ldv, 64)) != SL_OK) return st;
     AttnArgs ad = a;
@@ -1450,7 +1529,7 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
     const int64_t items = (sh.S / 128) * sh.H * a.nseq;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, num_sms()));
     if ((st = launch_pdl("attn_dq_kernel", attn_dq_kernel, dim3(grid), dim3(kAtThreads), DqCfg::kSmem, stream, mq, mdo,
-                         mk, mv, ad)) != SL_OK)
+                         mk, mv, mdq, ad)) != SL_OK)
       return st;
   }
   // dK, dV
