@@ -41,6 +41,7 @@
 // library's device error word.
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 #include <utility>
 
 #include "attn.cuh"
@@ -885,16 +886,23 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(s * 64 + half * 32), up);
           ptx::tmem_wait_ld();
           const int key0 = j * 64 + half * 32;
+          auto dS = [&](auto masked) {  // only the item's last two blocks reach the diagonal
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float ds2[2];
+            for (int e = 0; e < 32; e += 2) {
+              float ds2[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const float p = key0 + e + u <= qrow ? ex2(fmaf(__uint_as_float(us[e + u]), a.c, -lse2)) : 0.0f;
-              ds2[u] = p * (__uint_as_float(up[e + u]) - di);
+              for (int u = 0; u < 2; ++u) {
+                float p = ex2(fmaf(__uint_as_float(us[e + u]), a.c, -lse2));
+                if (decltype(masked)::value && key0 + e + u > qrow) p = 0.0f;
+                ds2[u] = p * (__uint_as_float(up[e + u]) - di);
+              }
+              w[e / 2] = pack2(ds2[0], ds2[1]);
             }
-            w[e / 2] = pack2(ds2[0], ds2[1]);
-          }
+          };
+          if (j + 2 >= t.n)
+            dS(std::true_type{});
+          else
+            dS(std::false_type{});
         }
         // dS of this half's 32 keys over the first 16 columns of the S columns
         // this thread has just read (no other warp reads them)
@@ -1228,19 +1236,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(b2 * 64 + half * 32), us);
           ptx::tmem_ld_32x32b_x32(lane_base + 128u + static_cast<uint32_t>(b2 * 64 + half * 32), up);
           ptx::tmem_wait_ld();
+          auto pds = [&](auto masked) {  // only the two query blocks of the key tile's own rows reach the diagonal
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float p2[2], d2[2];
+            for (int e = 0; e < 32; e += 2) {
+              float p2[2], d2[2];
 #pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              const int qi = e + v;
-              const float p = (q0 + qi >= kpos) ? ex2(fmaf(__uint_as_float(us[qi]), a.c, -lse2[qi])) : 0.0f;
-              p2[v] = p;
-              d2[v] = p * (__uint_as_float(up[qi]) - dis[qi]);
+              for (int v = 0; v < 2; ++v) {
+                const int qi = e + v;
+                float p = ex2(fmaf(__uint_as_float(us[qi]), a.c, -lse2[qi]));
+                if (decltype(masked)::value && q0 + qi < kpos) p = 0.0f;
+                p2[v] = p;
+                d2[v] = p * (__uint_as_float(up[qi]) - dis[qi]);
+              }
+              wp[e / 2] = pack2(p2[0], p2[1]);
+              wd[e / 2] = pack2(d2[0], d2[1]);
             }
-            wp[e / 2] = pack2(p2[0], p2[1]);
-            wd[e / 2] = pack2(d2[0], d2[1]);
-          }
+          };
+          if (u % t.nqb < 2)
+            pds(std::true_type{});
+          else
+            pds(std::false_type{});
         }
         // P^T and dS^T of this half's 32 queries over the first 16 columns of
         // the S^T and dP^T columns this thread has just read
