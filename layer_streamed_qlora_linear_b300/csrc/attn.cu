@@ -571,21 +571,32 @@ __global__ void attn_di_kernel(const uint16_t* __restrict__ o, int64_t ldo, cons
   if (valid && lane == 0) Di[static_cast<int64_t>(h) * M + row] = s;
 }
 
+// cos and sin of the rotation pairs 32 half .. 32 half + 31 at one position
+// (the table row holds cos at 0..63 and sin at 64..127), loaded ahead of use.
+struct RotRow {
+  float4 c[8], s[8];
+};
+__device__ __forceinline__ void load_rot(const float* table, int pos, int half, RotRow& t) {
+  const float4* cs = reinterpret_cast<const float4*>(table + static_cast<int64_t>(pos) * 128 + half * 32);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    t.c[i] = __ldg(cs + i);
+    t.s[i] = __ldg(cs + 16 + i);
+  }
+}
+
 // Rotation pairs 32 half .. 32 half + 31 of one 128-wide gradient row: lo
 // holds columns 32 half .., hi columns 64 + 32 half ..; scale by 1/sqrt(128),
-// rotate back by the inverse angle of position `pos` (table may be null) and
-// round to bf16 pairs: o1 the columns 32 half .., o2 64 + 32 half ...
+// rotate back by the inverse angle of the row's position (rot may be null:
+// no rotation) and round to bf16 pairs: o1 the columns 32 half .., o2
+// 64 + 32 half ...
 __device__ __forceinline__ void grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
-                                           const float* table, int pos, int half, uint32_t (&o1)[16],
-                                           uint32_t (&o2)[16]) {
-  // the table row holds cos at 0..63 and sin at 64..127; 16-byte loads
-  const float4* cs = table ? reinterpret_cast<const float4*>(table + static_cast<int64_t>(pos) * 128 + half * 32)
-                           : nullptr;
+                                           const RotRow* rot, uint32_t (&o1)[16], uint32_t (&o2)[16]) {
 #pragma unroll
   for (int e4 = 0; e4 < 32; e4 += 4) {
     float cv[4] = {1.0f, 1.0f, 1.0f, 1.0f}, sv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (cs) {
-      const float4 c = __ldg(cs + e4 / 4), sn = __ldg(cs + 16 + e4 / 4);
+    if (rot) {
+      const float4 c = rot->c[e4 / 4], sn = rot->s[e4 / 4];
       cv[0] = c.x, cv[1] = c.y, cv[2] = c.z, cv[3] = c.w;
       sv[0] = sn.x, sv[1] = sn.y, sv[2] = sn.z, sv[3] = sn.w;
     }
@@ -593,7 +604,7 @@ __device__ __forceinline__ void grad_pairs(const uint32_t (&lo)[32], const uint3
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const float x1 = __uint_as_float(lo[e4 + u]) * scale, x2 = __uint_as_float(hi[e4 + u]) * scale;
-      if (cs) {
+      if (rot) {
         y1[u] = x1 * cv[u] + x2 * sv[u];
         y2[u] = x2 * cv[u] - x1 * sv[u];
       } else {
@@ -609,9 +620,9 @@ __device__ __forceinline__ void grad_pairs(const uint32_t (&lo)[32], const uint3
 }
 // ... stored straight into the gradient row
 __device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
-                                                 const float* table, int pos, int half, uint16_t* row) {
+                                                 const RotRow* rot, int half, uint16_t* row) {
   uint32_t o1[16], o2[16];
-  grad_pairs(lo, hi, scale, table, pos, half, o1, o2);
+  grad_pairs(lo, hi, scale, rot, o1, o2);
   uint4* d1 = reinterpret_cast<uint4*>(row + half * 32);
   uint4* d2 = reinterpret_cast<uint4*>(row + 64 + half * 32);
 #pragma unroll
@@ -623,9 +634,9 @@ __device__ __forceinline__ void store_grad_pairs(const uint32_t (&lo)[32], const
 // ... or into row r of a [128][128] staging tile of two 128-byte-swizzled
 // atoms (columns 0..63 at atom0, 64..127 at atom1) for a TMA store
 __device__ __forceinline__ void stage_grad_pairs(const uint32_t (&lo)[32], const uint32_t (&hi)[32], float scale,
-                                                 const float* table, int pos, int half, uint32_t atom0, int r) {
+                                                 const RotRow* rot, int half, uint32_t atom0, int r) {
   uint32_t o1[16], o2[16];
-  grad_pairs(lo, hi, scale, table, pos, half, o1, o2);
+  grad_pairs(lo, hi, scale, rot, o1, o2);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     sts_swz(atom0, r, half * 4 + c, o1[4 * c], o1[4 * c + 1], o1[4 * c + 2], o1[4 * c + 3]);
@@ -912,6 +923,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ds_full[s]);
       }
+      RotRow rot;  // its loads overlap the wait for the last dQ MMA
+      const bool rotate = a.rope != nullptr;
+      if (rotate) load_rot(a.rope, qrow, half, rot);
       if (!ok || !wait_all(acc_full, it & 1)) {
         ok = false;
         break;
@@ -939,7 +953,10 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ok = false;
         break;
       }
-      stage_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, qrow, half, ptx::smem_addr(smem + DqCfg::kOffOut), r);
+      if (rotate)
+        stage_grad_pairs(lo, hi, 0.08838834764831845f, &rot, half, ptx::smem_addr(smem + DqCfg::kOffOut), r);
+      else
+        stage_grad_pairs(lo, hi, 0.08838834764831845f, nullptr, half, ptx::smem_addr(smem + DqCfg::kOffOut), r);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&stage_full[quarter]);
@@ -1279,13 +1296,23 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(half * 32), lo);
         ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(64 + half * 32), hi);
         ptx::tmem_wait_ld();
-        store_grad_pairs(lo, hi, 1.0f, nullptr, 0, half, a.out1 + static_cast<int64_t>(t.key0 + r) * a.ld1 + t.g * 128);
-        ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(half * 32), lo);
-        ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(64 + half * 32), hi);
-        ptx::tmem_wait_ld();
-        ptx::tc_fence_before();
-        store_grad_pairs(lo, hi, 0.08838834764831845f, a.rope, kpos, half,
-                         a.out0 + static_cast<int64_t>(t.key0 + r) * a.ld0 + t.g * 128);
+        store_grad_pairs(lo, hi, 1.0f, nullptr, half, a.out1 + static_cast<int64_t>(t.key0 + r) * a.ld1 + t.g * 128);
+        uint16_t* dk_row = a.out0 + static_cast<int64_t>(t.key0 + r) * a.ld0 + t.g * 128;
+        if (a.rope) {
+          RotRow rot;  // its loads overlap the TMEM read of dK
+          load_rot(a.rope, kpos, half, rot);
+          ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(half * 32), lo);
+          ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(64 + half * 32), hi);
+          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          store_grad_pairs(lo, hi, 0.08838834764831845f, &rot, half, dk_row);
+        } else {
+          ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(half * 32), lo);
+          ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(64 + half * 32), hi);
+          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          store_grad_pairs(lo, hi, 0.08838834764831845f, nullptr, half, dk_row);
+        }
       } else {
         // fp32 partials of this query head, row key0 + r, columns 64 half ..
         const int64_t row = static_cast<int64_t>(t.h0) * M + t.key0 + r;
