@@ -35,7 +35,8 @@
 // A TMEM buffer is rewritten by the MMA two blocks later, which the tensor
 // pipe runs after the MMA that read it (tcgen05.mma ops of one thread run in
 // issue order).
-// Di = rowsum(dO * O) comes from a small pre-pass.  The epilogues scale dQ
+// Di = rowsum(dO * O) is computed by the dq kernel's row workers from the
+// O and dO tiles it loads, and stored for the dkdv kernel.  The epilogues scale dQ
 // and dK by 1/sqrt(128) and rotate them back by the inverse rotary angle.
 // Every wait is bounded; a timeout raises SL_ERR_TIMEOUT through the
 // library's device error word.
@@ -161,7 +162,7 @@ struct AttnArgs {
   uint16_t* out1; // dkdv kernel: dv (in-CTA head sum only)
   int64_t ld1;
   float* lse;     // fwd output [H][M] (natural log); bwd input
-  const float* Di;  // bwd: [H][M]
+  float* Di;       // bwd: [H][M], written by the dq kernel, read by the dkdv kernel
   const float* rope;  // bwd: table [S][128] or nullptr
   int heads_per_cta;  // dK dV kernel: query heads summed inside one CTA (1, or H / Hkv: direct bf16 output)
   int* err;
@@ -546,30 +547,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   }
 }
 
-// ------------------------------------------------------------ Di pre-pass
-// Di[h][row] = sum_d dO[row, h*128 + d] * O[row, h*128 + d]: half a warp per
-// (row, head), 16-byte loads (8 elements per lane), a 16-lane shuffle sum.
-__global__ void attn_di_kernel(const uint16_t* __restrict__ o, int64_t ldo, const uint16_t* __restrict__ dout,
-                               int64_t lddo, int64_t M, int H, float* __restrict__ Di) {
-  pdl_trigger();
-  pdl_wait();
-  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
-  const int lane = threadIdx.x & 15;
-  const bool valid = w < M * H;
-  const int64_t row = valid ? w / H : 0;
-  const int h = valid ? static_cast<int>(w % H) : 0;
-  float s = 0.0f;
-  if (valid) {
-    const uint4 ov = *reinterpret_cast<const uint4*>(o + row * ldo + h * 128 + lane * 8);
-    const uint4 dv = *reinterpret_cast<const uint4*>(dout + row * lddo + h * 128 + lane * 8);
-    const uint32_t a[4] = {ov.x, ov.y, ov.z, ov.w}, b[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s += bf_lo(a[e]) * bf_lo(b[e]) + bf_hi(a[e]) * bf_hi(b[e]);
-  }
-#pragma unroll
-  for (int off = 8; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (valid && lane == 0) Di[static_cast<int64_t>(h) * M + row] = s;
-}
 
 // cos and sin of the rotation pairs 32 half .. 32 half + 31 at one position
 // (the table row holds cos at 0..63 and sin at 64..127), loaded ahead of use.
@@ -657,7 +634,8 @@ constexpr int kKvStages = 3;  // query/dO ring of the dK dV kernel
 struct DqCfg {
   static constexpr int kOffQ = 0;                      // [128][128]
   static constexpr int kOffDO = kOffQ + kAtTile;       // [128][128]
-  static constexpr int kOffK = kOffDO + kAtTile;       // kAtStages stages of [64][128]
+  static constexpr int kOffO = kOffDO + kAtTile;       // [128][128]: O, for Di = rowsum(dO * O)
+  static constexpr int kOffK = kOffO + kAtTile;        // kAtStages stages of [64][128]
   static constexpr int kOffV = kOffK + kAtStages * 2 * kAtAtom64;
   static constexpr int kOffOut = kOffV + kAtStages * 2 * kAtAtom64;  // dQ staging: 2 atoms of [128][64]
   static constexpr int kOffBar = kOffOut + kAtTile;
@@ -673,8 +651,9 @@ struct DqCfg {
 // as soon as the current item's last S / dP MMAs have completed.
 __global__ void __launch_bounds__(kAtThreads, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
-                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                   const __grid_constant__ CUtensorMap map_dq, const AttnArgs a) {
+                   const __grid_constant__ CUtensorMap map_o, const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_dq,
+                   const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = ptx::align1024(smem_raw);
   uint8_t* sQ = smem + DqCfg::kOffQ;
@@ -682,14 +661,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint8_t* sK = smem + DqCfg::kOffK;
   uint8_t* sV = smem + DqCfg::kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DqCfg::kOffBar);
-  uint64_t* q_full = bars;         // Q and dO of the item landed
+  uint64_t* q_full = bars;         // Q, dO and O of the item landed
   uint64_t* kv_full = bars + 1;                  // [kAtStages]
   uint64_t* kv_empty = bars + 1 + kAtStages;     // [kAtStages]
   uint64_t* sp_full = bars + 1 + 2 * kAtStages;  // [2] S and dP in TMEM buffer b
   uint64_t* ds_full = sp_full + 2;               // [2] dS written over S in buffer b (8 warp arrivals)
   uint64_t* acc_full = sp_full + 4;              // dQ of the item complete
   uint64_t* drain = sp_full + 5;                 // failure path: every issued MMA completed
-  uint64_t* q_empty = sp_full + 6;               // the item's last S / dP MMAs done: Q and dO may be replaced
+  uint64_t* q_empty = sp_full + 6;               // the item's last S / dP MMAs done and Di read out of dO, O
+                                                 // (1 commit + 8 warp arrivals): they may be replaced
   uint64_t* stage_full = sp_full + 7;            // [4] quarter q's staging rows written (2 warp arrivals)
   uint64_t* stage_free = sp_full + 11;           // [4] quarter q's previous TMA stores have read them
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DqCfg::kOffMisc);
@@ -718,7 +698,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    ptx::mbar_init(q_empty, 1);
+    ptx::mbar_init(q_empty, 1 + kAtWorkers);
     for (int i = 0; i < kAtStages; ++i) {
       ptx::mbar_init(&kv_full[i], 1);
       ptx::mbar_init(&kv_empty[i], 1);
@@ -740,6 +720,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     ptx::tma_prefetch_desc(&map_k);
     ptx::tma_prefetch_desc(&map_v);
     ptx::tma_prefetch_desc(&map_dq);
+    ptx::tma_prefetch_desc(&map_o);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, 512);
@@ -770,11 +751,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ok = false;
           break;
         }
-        ptx::mbar_arrive_expect_tx(q_full, 2 * kAtTile);
+        ptx::mbar_arrive_expect_tx(q_full, 3 * kAtTile);
         ptx::tma_load_2d(sQ, &map_q, q_full, t.h * 128, t.row0);
         ptx::tma_load_2d(sQ + kAtAtom128, &map_q, q_full, t.h * 128 + 64, t.row0);
         ptx::tma_load_2d(sDO, &map_do, q_full, t.h * 128, t.row0);
         ptx::tma_load_2d(sDO + kAtAtom128, &map_do, q_full, t.h * 128 + 64, t.row0);
+        ptx::tma_load_2d(smem + DqCfg::kOffO, &map_o, q_full, t.h * 128, t.row0);
+        ptx::tma_load_2d(smem + DqCfg::kOffO + kAtAtom128, &map_o, q_full, t.h * 128 + 64, t.row0);
         ++issued_q;
         for (int j = 0; j < t.n; ++j, ++gb) {
           const int s = gb % kAtStages;
@@ -881,7 +864,31 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       const Item t = item_of(item);
       const int qrow = t.qt * 128 + r;  // position in the sequence
       const float lse2 = a.lse[static_cast<int64_t>(t.h) * M + t.row0 + r] * kLog2e;
-      const float di = a.Di[static_cast<int64_t>(t.h) * M + t.row0 + r];
+      // Di = rowsum(dO * O) of row r over all 128 columns (both warps of the
+      // row compute it), from the item's shared tiles; half 0 stores it for
+      // the dK dV kernel
+      if (!wait_all(q_full, it & 1)) {
+        ok = false;
+        break;
+      }
+      float di;
+      {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint32_t sdo = ptx::smem_addr(sDO), so = ptx::smem_addr(smem + DqCfg::kOffO);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t off = (c >> 3) * kAtAtom128 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          const float4 x = lds128(sdo + off), y = lds128(so + off);
+          const uint32_t xa[4] = {__float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w)};
+          const uint32_t ya[4] = {__float_as_uint(y.x), __float_as_uint(y.y), __float_as_uint(y.z), __float_as_uint(y.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[e] += bf_lo(xa[e]) * bf_lo(ya[e]) + bf_hi(xa[e]) * bf_hi(ya[e]);
+        }
+        di = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(q_empty);
+      if (half == 0) a.Di[static_cast<int64_t>(t.h) * M + t.row0 + r] = di;
       for (int j = 0; j < t.n; ++j) {
         const int cur = gb + j;
         const int s = cur & 1;
@@ -1540,12 +1547,6 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
                                       int64_t lddq, uint16_t* dk, int64_t lddk, uint16_t* dv, int64_t lddv,
                                       const float* rope, float* Di, int* err, cudaStream_t stream) {
   sl_status st;
-  {
-    const int64_t threads = sh.M * sh.H * 16;
-    if ((st = launch_pdl("attn_di_kernel", attn_di_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
-                         0, stream, o, ldo, dout, lddo, sh.M, sh.H, Di)) != SL_OK)
-      return st;
-  }
   AttnArgs a{};
   a.S = static_cast<int>(sh.S);
   a.H = sh.H;
@@ -1558,9 +1559,10 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
   a.err = err;
   // dQ
   {
-    CUtensorMap mq, mdo, mk, mv, mdq;
+    CUtensorMap mq, mdo, mo, mk, mv, mdq;
     if ((st = map_rows(&mq, q, sh.H * 128, sh.M, ldq, 128)) != SL_OK) return st;
     if ((st = map_rows(&mdo, dout, sh.H * 128, sh.M, lddo, 128)) != SL_OK) return st;
+    if ((st = map_rows(&mo, o, sh.H * 128, sh.M, ldo, 128)) != SL_OK) return st;
     if ((st = map_rows(&mdq, dq, sh.H * 128, sh.M, lddq, 32)) != SL_OK) return st;
     if ((st = map_rows(&mk, k, sh.Hkv * 128, sh.M, ldk, 64)) != SL_OK) return st;
     if ((st = map_rows(&mv, v, sh.Hkv * 128, sh.M, ldv, 64)) != SL_OK) return st;
@@ -1571,7 +1573,7 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
     const int64_t items = (sh.S / 128) * sh.H * a.nseq;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, num_sms()));
     if ((st = launch_pdl("attn_dq_kernel", attn_dq_kernel, dim3(grid), dim3(kAtThreads), DqCfg::kSmem, stream, mq, mdo,
-                         mk, mv, mdq, ad)) != SL_OK)
+                         mo, mk, mv, mdq, ad)) != SL_OK)
       return st;
   }
   // dK, dV
