@@ -12,11 +12,12 @@
 // S = Q K^T into one of two TMEM buffers one tile ahead.  Eight row workers
 // (TMEM lane quarter x column half; 64 scores per thread) exchange their
 // row maxima through shared memory and write P = exp2(S c - m) as bf16
-// pairs back into TMEM over the scores; the MMA warp computes O_part = P V
-// with P as a TMEM operand and V as an MN-major shared operand, into one of
-// two more TMEM buffers.  The workers keep O in registers:
-// O = O alpha + O_part with alpha = exp2(m_old - m_new), folding in the
-// previous tile's O_part while the tensor pipe runs the current P V.
+// pairs back into TMEM over the scores; the MMA warp accumulates O += P V
+// in TMEM with P as a TMEM operand and V as an MN-major shared operand.  A
+// row's reference maximum moves only when a tile's maximum exceeds it by
+// more than 8 (log2 units); only then is the row's O rescaled in TMEM (after
+// the previous P V has completed), so most tiles hand P over without
+// waiting for the tensor pipe.
 //
 // Backward (no atomics: every output element is summed in one CTA in a
 // fixed order, so results are bitwise reproducible):
@@ -212,8 +213,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint64_t* v_empty = bars + 7;   // [2] its PV MMA done
   uint64_t* s_full = bars + 9;    // [2] S tile in TMEM buffer b
   uint64_t* p_full = bars + 11;   // P written (8 warp arrivals); S buffer read
-  uint64_t* o_full = bars + 12;   // [2] O_part in TMEM buffer b
-  uint64_t* o_empty = bars + 14;  // [2] O_part read (8 warp arrivals)
+  uint64_t* o_full = bars + 12;   // [2] the P V of a tile of parity b completed
   uint64_t* drain = bars + 16;    // failure path: every issued MMA completed
   uint64_t* q_empty = bars + 17;  // the item's last S MMA done: Q may be replaced
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + FwdCfg::kOffMisc);
@@ -249,7 +249,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       ptx::mbar_init(&v_empty[i], 1);
       ptx::mbar_init(&s_full[i], 1);
       ptx::mbar_init(&o_full[i], 1);
-      ptx::mbar_init(&o_empty[i], kAtWorkers);
     }
     ptx::mbar_init(p_full, kAtWorkers);
     ptx::mbar_init(drain, 1);
@@ -362,20 +361,19 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             if (j + 2 == n) ptx::mma_commit(q_empty);  // the item's last S has been issued
           }
           const int s = cur & 1;
+          // P written (and O rescaled where a row's maximum moved)
           if (!ptx::mbar_wait(p_full, cur & 1, abort_flag) ||
-              !ptx::mbar_wait(&v_full[s], (cur >> 1) & 1, abort_flag) ||
-              !ptx::mbar_wait(&o_empty[s], ((cur >> 1) & 1) ^ 1, abort_flag)) {
+              !ptx::mbar_wait(&v_full[s], (cur >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t d = tmem + 256u + static_cast<uint32_t>(s * 128);
           const uint64_t dv = dadd(dv0, s * kAtTile);
-          // P of keys 16 kk ..: the column half kk / 4 wrote it over its first 32 S columns
+          // O += P V; P of keys 16 kk ..: the column half kk / 4 wrote it over its first 32 S columns
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            ptx::mma_bf16_ts(d, tmem + static_cast<uint32_t>(s * 128 + (kk >> 2) * 64 + (kk & 3) * 8), mnstep(dv, kk),
-                             id_o, kk ? 1u : 0u);
+            ptx::mma_bf16_ts(tmem + 256u, tmem + static_cast<uint32_t>(s * 128 + (kk >> 2) * 64 + (kk & 3) * 8),
+                             mnstep(dv, kk), id_o, (j | kk) ? 1u : 0u);
           ptx::mma_commit(&o_full[s]);
           ptx::mma_commit(&v_empty[s]);
         }
@@ -408,32 +406,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       if (!w && lane == 0 && !*abort_flag) give_up();
       return w;
     };
+    // O accumulates in TMEM (P V MMAs with accumulate); a row's reference
+    // maximum m only moves when the tile maximum exceeds it by more than
+    // kRescale (log2 units), and only then is the row's O rescaled in TMEM.
+    // P = exp2(S c - m) stays below 2^kRescale.
+    constexpr float kRescale = 8.0f;
     bool bad = false, stopped = false;
     int gt = 0;
     for (int k = 0, item = nth_item(0); !stopped && item < nitems; item = nth_item(++k)) {
       const int n = ntq - item / per;  // key tiles of the item (its query tile + 1)
-      float O[64];
-#pragma unroll
-      for (int e = 0; e < 64; ++e) O[e] = 0.0f;
-      float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
-      auto accumulate = [&](int cur) {  // O = O alpha + O_part of the CTA's tile cur
-        const int s = cur & 1;
-        if (!wait_all(&o_full[s], (cur >> 1) & 1)) return false;
-        ptx::tc_fence_after();
-        uint32_t u0[32], u1[32];
-        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128), u0);
-        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(s * 128 + 32), u1);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          O[e] = fmaf(O[e], alpha_prev, __uint_as_float(u0[e]));
-          O[32 + e] = fmaf(O[32 + e], alpha_prev, __uint_as_float(u1[e]));
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&o_empty[s]);
-        return true;
-      };
+      float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < n; ++j) {
         const int cur = gt + j;
         const int s = cur & 1;
@@ -468,9 +450,29 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           stopped = true;
           break;
         }
-        const float m_new = fmaxf(m, fmaxf(mt, red[(s * 2 + (half ^ 1)) * 128 + r]) * a.c);
-        const float alpha = ex2(m - m_new);
-        // P = exp2(S c - m_new) as bf16 pairs over the first 32 of the 64 S
+        const float m_tile = fmaxf(mt, red[(s * 2 + (half ^ 1)) * 128 + r]) * a.c;
+        const bool move = m_tile > m + kRescale;  // always on the item's first tile
+        const float alpha = move ? ex2(m - m_tile) : 1.0f;
+        if (move) m = m_tile;
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          // O through the previous tile: wait for its P V (this tile's S has
+          // completed, so every earlier P V but that one has), then O *= alpha
+          if (!wait_all(&o_full[(cur - 1) & 1], ((cur - 1) >> 1) & 1)) {
+            bad = true;
+            continue;  // raise the stop flag at the next barrier
+          }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t ov[32];
+            ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(c * 32), ov);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            ptx::tmem_st_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(c * 32), ov);
+          }
+        }
+        // P = exp2(S c - m) as bf16 pairs over the first 32 of the 64 S
         // columns this thread has read (every worker has read its S: the
         // barrier above), the P V MMA's A operand
         float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -479,8 +481,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(u[c][e]), a.c, -m_new));
-            const float p1 = ex2(fmaf(__uint_as_float(u[c][e + 1]), a.c, -m_new));
+            const float p0 = ex2(fmaf(__uint_as_float(u[c][e]), a.c, -m));
+            const float p1 = ex2(fmaf(__uint_as_float(u[c][e + 1]), a.c, -m));
             ls[e & 3] += p0;
             ls[(e + 1) & 3] += p1;
             w[e / 2] = pack2(p0, p1);
@@ -492,20 +494,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(p_full);
         l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-        m = m_new;
-        // O_part of the previous tile joins O with the previous alpha, while
-        // the tensor pipe runs this tile's P V
-        if (j > 0 && !accumulate(cur - 1)) {
-          bad = true;
-          continue;  // raise the stop flag at the next barrier
-        }
-        alpha_prev = alpha;
       }
       if (stopped) break;
-      // the last O_part, then the two halves' row sums (the barrier of the
-      // CTA's next tile parity)
+      // the final O once the last P V has completed, then the two halves'
+      // row sums (the barrier of the CTA's next tile parity)
       const int nxt = gt + n;
-      if (!bad) bad = !accumulate(nxt - 1);
+      if (!bad) bad = !wait_all(&o_full[(nxt - 1) & 1], ((nxt - 1) >> 1) & 1);
       red[(2 * 2 + half) * 128 + r] = l;
       if (bad && lane == 0) stop[nxt & 1] = 1;
       workers_sync();
@@ -520,10 +514,22 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       // one TMA box (its previous box has been read out before it is reused)
       if (lane == 0) ptx::bulk_wait_read0();
       __syncwarp();
+      ptx::tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        sts_swz(o_atom, r, c, pack2(O[8 * c] * inv, O[8 * c + 1] * inv), pack2(O[8 * c + 2] * inv, O[8 * c + 3] * inv),
-                pack2(O[8 * c + 4] * inv, O[8 * c + 5] * inv), pack2(O[8 * c + 6] * inv, O[8 * c + 7] * inv));
+      for (int c = 0; c < 2; ++c) {
+        uint32_t ov[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + 256u + static_cast<uint32_t>(c * 32), ov);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float* f = reinterpret_cast<const float*>(ov + 8 * q4);
+          sts_swz(o_atom, r, c * 4 + q4, pack2(f[0] * inv, f[1] * inv), pack2(f[2] * inv, f[3] * inv),
+                  pack2(f[4] * inv, f[5] * inv), pack2(f[6] * inv, f[7] * inv));
+        }
+      }
+      // O has left TMEM before this warp's next P arrival, after which the
+      // next item's first P V overwrites it
+      ptx::tc_fence_before();
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
