@@ -134,3 +134,44 @@ def test_attention_rejects_bad_shapes(gpu_lib):
     k2 = torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(gpu_lib.SLError):                  # 3 query heads over 2 kv heads
         gpu_lib.sl_attention_fwd(q3, k2, k2, 128, torch.empty_like(q3), torch.empty(3, 256, device="cuda"))
+
+
+def test_attention_rescales_when_the_row_maximum_grows(gpu_lib):
+    """Key norms that grow along the sequence make a row's maximum score rise by
+    more than 2^8 between 128-key tiles, so the forward has to rescale O
+    (checked on the inputs below); o, lse and the gradients still match."""
+    M, S, H, Hkv = 1024, 1024, 4, 2
+    D, Dkv = H * 128, Hkv * 128
+    g = np.random.default_rng(21)
+    grow = (1.0 + np.arange(S) / 64.0)[:, None]
+    q = round_bf16(g.standard_normal((M, D)) * 2.0).astype(np.float32)
+    k = round_bf16(g.standard_normal((M, Dkv)) * grow).astype(np.float32)
+    v = round_bf16(g.standard_normal((M, Dkv))).astype(np.float32)
+    dO = round_bf16(g.standard_normal((M, D))).astype(np.float32)
+    # the inputs exercise the rescale: per row, the running maximum (log2 units)
+    # grows by more than 8 at a later tile for most rows of the later query tiles
+    moved = 0
+    for h in range(H):
+        s2 = (q[:, h * 128:(h + 1) * 128].astype(np.float64) @ k[:, (h // 2) * 128:(h // 2 + 1) * 128].T.astype(np.float64))
+        s2 *= np.log2(np.e) / np.sqrt(128.0)
+        s2[np.triu_indices(S, 1)] = -np.inf
+        tile_max = s2.reshape(S, S // 128, 128).max(axis=2)
+        run = np.maximum.accumulate(tile_max, axis=1)
+        moved += int(np.sum(np.any(tile_max[:, 1:] > run[:, :-1] + 8.0, axis=1)))
+    assert moved > H * S // 2
+    qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    o = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(H, M, dtype=torch.float32, device="cuda")
+    gpu_lib.sl_attention_fwd(qd, kd, vd, S, o, lse)
+    dq = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
+    dk = torch.empty(M, Dkv, dtype=torch.bfloat16, device="cuda")
+    dv = torch.empty(M, Dkv, dtype=torch.bfloat16, device="cuda")
+    gpu_lib.sl_attention_bwd(qd, kd, vd, o, dev_bf16(dO), lse, S, dq, dk, dv)
+    gpu_lib.sl_check_device_errors()
+    o_ref, lse_ref = at.attention_fwd(q, k, v, S)
+    assert rel_fro(host(o), o_ref) <= BF16_TOL
+    np.testing.assert_allclose(host(lse).T, lse_ref, rtol=2e-5, atol=2e-5)
+    dq_ref, dk_ref, dv_ref = at.attention_bwd(q, k, v, o_ref, dO, S)
+    assert rel_fro(host(dq), dq_ref) <= BF16_TOL
+    assert rel_fro(host(dk), dk_ref) <= BF16_TOL
+    assert rel_fro(host(dv), dv_ref) <= BF16_TOL
