@@ -175,3 +175,25 @@ def test_attention_rescales_when_the_row_maximum_grows(gpu_lib):
     assert rel_fro(host(dq), dq_ref) <= BF16_TOL
     assert rel_fro(host(dk), dk_ref) <= BF16_TOL
     assert rel_fro(host(dv), dv_ref) <= BF16_TOL
+
+
+def test_attention_full_bench_shape_sampled_sequences(gpu_lib):
+    """The launch the attention bench times (8 sequences of 1024 tokens, 32 query
+    heads over 8 kv heads, rotary table on), sampled: in two sequences, every
+    row of o, lse and dq of one kv head's four query heads, and every row of
+    that kv head's dk and dv, against the oracle run on just those heads."""
+    M, S, H, Hkv, theta = 8192, 1024, 32, 8, 500000.0
+    (q, k, v, dO), (o, lse, dq, dk, dv) = run_attention(gpu_lib, M, S, H, Hkv, seed=77, rope=table(gpu_lib, S, theta))
+    o, lse, dq, dk, dv = host(o), host(lse).T, host(dq), host(dk), host(dv)
+    grp = H // Hkv
+    for b, g in ((0, 0), (5, 6)):
+        rows = slice(b * S, (b + 1) * S)
+        qc = slice(g * grp * 128, (g + 1) * grp * 128)   # the query heads of kv head g
+        kc = slice(g * 128, (g + 1) * 128)
+        o_ref, lse_ref = at.attention_fwd(q[rows, qc], k[rows, kc], v[rows, kc], S)
+        assert rel_fro(o[rows, qc], o_ref) <= BF16_TOL
+        np.testing.assert_allclose(lse[rows, g * grp:(g + 1) * grp], lse_ref, rtol=2e-5, atol=2e-5)
+        dq_ref, dk_ref, dv_ref = at.attention_bwd(q[rows, qc], k[rows, kc], v[rows, kc], o_ref, dO[rows, qc], S)
+        assert rel_fro(dq[rows, qc], at.rope(dq_ref, S, theta, inverse=True)) <= BF16_TOL
+        assert rel_fro(dk[rows, kc], at.rope(dk_ref, S, theta, inverse=True)) <= BF16_TOL
+        assert rel_fro(dv[rows, kc], dv_ref) <= BF16_TOL
