@@ -168,8 +168,21 @@ static sl_status run(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
     SL_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem));
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
+  // The output moves by TMA when a tensor map can describe it (16-byte
+  // aligned base and row stride); otherwise the epilogue stores directly.
+  GemmArgs ao = a;
+  CUtensorMap mo = ma;
+  {
+    const bool f32 = EPI == kEpiAddF32;
+    const int esz = f32 ? 4 : 2;
+    ao.tma_out = a.M >= 32 && a.N >= 128 && (reinterpret_cast<uintptr_t>(a.out) % 16 == 0) &&
+                 (a.ld_out * esz) % 16 == 0 &&
+                 make_map(&mo, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, a.N,
+                          a.M, static_cast<uint64_t>(a.ld_out) * esz, f32 ? 32 : 64, 32,
+                          CU_TENSOR_MAP_SWIZZLE_128B) == SL_OK;
+  }
   dim3 grid(static_cast<unsigned>(ceil_div(a.N, kBN)), static_cast<unsigned>(ceil_div(a.M, kBM)));
-  return launch_pdl("gemm_tc_kernel", kern, grid, dim3(kGemmThreads), Cfg::kSmem, stream, ma, mb, ms, a);
+  return launch_pdl("gemm_tc_kernel", kern, grid, dim3(kGemmThreads), Cfg::kSmem, stream, ma, mb, ms, mo, ao);
 }
 
 sl_status dispatch(const GemmLaunch& g, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms,

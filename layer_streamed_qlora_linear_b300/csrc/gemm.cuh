@@ -64,7 +64,7 @@ struct GemmCfg {
   static constexpr int kOffRaw = kOffB + S * kBTileBytes;
   static constexpr int kOffTab = kOffRaw + S * kRawBytes;
   static constexpr int kOffBar = kOffTab + 128;
-  static constexpr int kNumBars = 3 * S + 3;
+  static constexpr int kNumBars = 3 * S + 3 + 8;  // + one epilogue barrier per epilogue warp
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
@@ -93,6 +93,7 @@ struct GemmArgs {
   int part_ld;                 // half tiles of a chunk
   const float* row_alpha;      // [M] kEpiAddF32: factor on the accumulated output, or nullptr
   int accumulate;              // kEpiAddF32: add into out (1) or overwrite (0)
+  int tma_out;                 // gemm_tc_kernel: the output moves by TMA through map_o (else direct stores)
   int* err;                    // device error word
 };
 
@@ -155,7 +156,8 @@ __device__ __forceinline__ void nf4_row_bf16(const uint8_t* codes, float amax, u
 template <int BSRC, int BMN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   const __grid_constant__ CUtensorMap map_s, const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_o,
+                   const GemmArgs args) {
   using Cfg = GemmCfg<BSRC>;
   constexpr int S = Cfg::S;
   extern __shared__ uint8_t smem_raw[];
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* lora_full = bars + 3 * S;
   uint64_t* acc_full = bars + 3 * S + 1;
   uint64_t* main_done = bars + 3 * S + 2;
+  uint64_t* epi_bar = bars + 3 * S + 3;  // [8] kEpiAddF32 with TMA: the epilogue warp's old output landed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
 
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::mbar_init(lora_full, kNumDq);
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(main_done, 1);
+    for (int i = 0; i < 8; ++i) ptx::mbar_init(&epi_bar[i], 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&map_a);
@@ -458,7 +462,92 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row = q * 32 + lane;
       const int gm = m0 + row;
       const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      if (EPI == kEpiStoreBF16) {
+      // TMA-store path: the main loop is over and every stage consumed, so the
+      // stage buffers serve as staging.  This warp's 32 rows x 128 columns
+      // leave as 64-column bf16 boxes (2 x 4 KB) or 32-column fp32 boxes
+      // (4 x 4 KB) in the 128-byte-swizzled layout; rows and columns past the
+      // output are clipped by the tensor map.
+      uint8_t* stg = smem + (warp - 2) * (EPI == kEpiAddF32 ? 16384 : 8192);
+      const uint32_t stg_a = ptx::smem_addr(stg);
+      auto stg_chunk = [&](int lc, int j) {  // 16-byte chunk j of local column block lc / (box width)
+        constexpr int kBoxCols = EPI == kEpiAddF32 ? 32 : 64;
+        return stg_a + (lc / kBoxCols) * 4096 + lane * 128 + ((j ^ (lane & 7)) << 4);
+      };
+      auto tma_store_boxes = [&]() {
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          constexpr int kBoxes = EPI == kEpiAddF32 ? 4 : 2, kBoxCols = 128 / kBoxes;
+          for (int b = 0; b < kBoxes; ++b)
+            ptx::tma_store_2d(&map_o, stg + b * 4096, n0 + cbeg + b * kBoxCols, m0 + q * 32);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read0();  // the staging is read before the CTA's shared memory goes
+        }
+        __syncwarp();
+      };
+      if (args.tma_out && EPI == kEpiStoreBF16) {
+#pragma unroll 1
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c0, v);
+          ptx::tmem_wait_ld();
+          const int lc = c0 - cbeg;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg_chunk(lc, (lc % 64) / 8 + g)),
+                         "r"(pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]))),
+                         "r"(pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]))),
+                         "r"(pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]))),
+                         "r"(pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7])))
+                         : "memory");
+        }
+        tma_store_boxes();
+      } else if (args.tma_out && EPI == kEpiAddF32) {
+        const float alpha = (args.row_alpha && gm < args.M) ? args.row_alpha[gm] : 1.0f;
+        bool got = true;
+        if (args.accumulate) {  // the old output of these rows and columns, by TMA
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&epi_bar[warp - 2], 4 * 4096);
+            for (int b = 0; b < 4; ++b)
+              ptx::tma_load_2d(stg + b * 4096, &map_o, &epi_bar[warp - 2], n0 + cbeg + b * 32, m0 + q * 32);
+          }
+          got = ptx::mbar_wait(&epi_bar[warp - 2], 0, abort_flag);
+          got = __all_sync(0xffffffffu, got);
+          if (!got && lane == 0) {
+            give_up();
+            ptx::mbar_wait(&epi_bar[warp - 2], 0, nullptr);  // the copy lands before the smem goes
+          }
+        }
+        if (got) {
+#pragma unroll 1
+          for (int c0 = cbeg; c0 < cend; c0 += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(t_row + c0, v);
+            ptx::tmem_wait_ld();
+            const int lc = c0 - cbeg;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const uint32_t at = stg_chunk(lc, g);
+              float4 o = make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                     __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+              if (args.accumulate) {
+                float4 p;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(p.x), "=f"(p.y), "=f"(p.z), "=f"(p.w)
+                             : "r"(at));
+                o.x = fmaf(p.x, alpha, o.x);
+                o.y = fmaf(p.y, alpha, o.y);
+                o.z = fmaf(p.z, alpha, o.z);
+                o.w = fmaf(p.w, alpha, o.w);
+              }
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(at), "f"(o.x), "f"(o.y), "f"(o.z),
+                           "f"(o.w)
+                           : "memory");
+            }
+          }
+          tma_store_boxes();
+        }
+      } else if (EPI == kEpiStoreBF16) {
         uint16_t* out = reinterpret_cast<uint16_t*>(args.out);
 #pragma unroll 1
         for (int c0 = cbeg; c0 < cend; c0 += 32) {
@@ -478,7 +567,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
-      } else if (EPI == kEpiAddF32) {
+      } else if (EPI == kEpiAddF32) {  // direct stores
         float* out = reinterpret_cast<float*>(args.out);
         const float alpha = (args.row_alpha && gm < args.M) ? args.row_alpha[gm] : 1.0f;
 #pragma unroll 1
@@ -533,7 +622,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               f[e] = __expf(__uint_as_float(v[e]) - mx);
               sm += f[e];
             }
-            if (gm < args.M) {
+            if (args.tma_out) {
+              const int lc = c0 - cbeg;
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg_chunk(lc, (lc % 64) / 8 + g)),
+                             "r"(pack_bf16x2(f[8 * g + 0], f[8 * g + 1])), "r"(pack_bf16x2(f[8 * g + 2], f[8 * g + 3])),
+                             "r"(pack_bf16x2(f[8 * g + 4], f[8 * g + 5])), "r"(pack_bf16x2(f[8 * g + 6], f[8 * g + 7]))
+                             : "memory");
+            } else if (gm < args.M) {
               uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(gm) * args.ld_out + n0 + c0);
 #pragma unroll
               for (int g = 0; g < 4; ++g) {
@@ -553,6 +650,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
+        if (args.tma_out) tma_store_boxes();
         if (gm < args.M) {
           const int64_t p = static_cast<int64_t>(gm) * args.part_ld + 2 * blockIdx.x + ch;
           args.part_max[p] = mx;
