@@ -152,8 +152,15 @@ static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, co
   }
   const int ntiles = ceil_div(a.M, 256) * ceil_div(a.N, kBN);
   const int nclusters = std::min(ntiles, pair_clusters_resident<BMN, SMALL>());
+  // bf16 output by TMA boxes of 64 columns x 32 rows when a tensor map can
+  // describe it (16-byte aligned base and row stride); else direct stores
+  GemmArgs ao = a;
+  CUtensorMap mo = ma;
+  ao.tma_out = (reinterpret_cast<uintptr_t>(a.out) % 16 == 0) && (a.ld_out * 2) % 16 == 0 &&
+               make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, a.N, a.M, static_cast<uint64_t>(a.ld_out) * 2, 64,
+                        32, CU_TENSOR_MAP_SWIZZLE_128B) == SL_OK;
   return launch_pdl("gemm_nf4_pair_persistent_kernel", kern, dim3(static_cast<unsigned>(2 * nclusters)),
-                    dim3(kGemm3Threads), Gemm3Cfg<SMALL>::kSmem, stream, ma, mc, ms, ms2, a);
+                    dim3(kGemm3Threads), Gemm3Cfg<SMALL>::kSmem, stream, ma, mc, ms, ms2, mo, ao);
 }
 
 template <int BSRC, int BMN, int EPI>

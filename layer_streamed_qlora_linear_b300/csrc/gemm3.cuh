@@ -51,6 +51,10 @@ struct Gemm3Cfg {
   static constexpr int kSmem = kBytes + 1024;
 };
 static_assert(Gemm3Cfg<0>::kSmem <= 232448 && Gemm3Cfg<1>::kSmem <= 232448, "persistent GEMM shared memory");
+// the epilogue's TMA staging (4 warps x 8 KB) lives in the LoRA region
+static_assert(Gemm3Cfg<1>::kOffLA % 1024 == 0 && Gemm3Cfg<1>::kLA * kLoraAtom + Gemm3Cfg<1>::kLBBytes >= 4 * 8192 &&
+                  Gemm3Cfg<0>::kOffLA % 1024 == 0 && Gemm3Cfg<0>::kLA * kLoraAtom + Gemm3Cfg<0>::kLBBytes >= 4 * 8192,
+              "persistent GEMM epilogue staging");
 
 // Barrier of the four epilogue warps only (named barrier 1).
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kNumEpi3) : "memory"); }
@@ -59,6 +63,7 @@ template <int BMN, int SMALL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     gemm_nf4_pair_persistent_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
                                     const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_s2,
+                                    const __grid_constant__ CUtensorMap map_o,
                                     const GemmArgs args) {
   using Cfg = Gemm3Cfg<SMALL>;
   constexpr int S = Cfg::S;
@@ -444,15 +449,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       const int gm = tile_m0(t) + row;
       const int n0 = tile_n0(t);
       const uint32_t t_row = tmem + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(q * 32) << 16);
+      if (args.tma_out) {
+        // The LoRA region is free from the fold's completion (acc_full) until
+        // the next stage_lora, which follows the epilogue warps' barrier:
+        // this warp stages its 32 rows there as 64-column bf16 boxes (two
+        // 4 KB buffers in turn) and stores them by TMA.
+        uint8_t* stg = sLA + (warp - 10) * 8192;
+        const uint32_t stg_a = ptx::smem_addr(stg);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        uint32_t u[32];
-        ptx::tmem_ld_32x32b_x32(t_row + c0, u);
-        ptx::tmem_wait_ld();
-        float v[32];
+        for (int p = 0; p < kBN / 64; ++p) {
+          const int b = p & 1;
+          if (p >= 2) {  // buffer b's previous box has been read out
+            if (lane == 0) ptx::bulk_wait_read1();
+            __syncwarp();
+          }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
-        store32(gm, n0, c0, v);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t u[32];
+            ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(p * 64 + h * 32), u);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               stg_a + b * 4096 + lane * 128 + (((h * 4 + g4) ^ (lane & 7)) << 4)),
+                           "r"(pack_bf16x2(__uint_as_float(u[8 * g4 + 0]), __uint_as_float(u[8 * g4 + 1]))),
+                           "r"(pack_bf16x2(__uint_as_float(u[8 * g4 + 2]), __uint_as_float(u[8 * g4 + 3]))),
+                           "r"(pack_bf16x2(__uint_as_float(u[8 * g4 + 4]), __uint_as_float(u[8 * g4 + 5]))),
+                           "r"(pack_bf16x2(__uint_as_float(u[8 * g4 + 6]), __uint_as_float(u[8 * g4 + 7])))
+                           : "memory");
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&map_o, stg + b * 4096, n0 + p * 64, tile_m0(t) + q * 32);
+            ptx::bulk_commit();
+          }
+        }
+        if (lane == 0) ptx::bulk_wait_read0();  // the region is free again before any warp passes the next barrier
+        __syncwarp();
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          uint32_t u[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c0, u);
+          ptx::tmem_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+          store32(gm, n0, c0, v);
+        }
       }
       // accumulator drained: let the leader reuse it
       ptx::tc_fence_before();
