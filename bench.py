@@ -611,7 +611,7 @@ def run_ours(args):
     # step of a 4-layer stack: the per-layer launch mix of the 32-layer workload); null elsewhere
     traffic, traffic_note = None, None
     if w["kind"] == "stack" and w["base"] == "nf4" and w["D"] == 4096 and w["M"] == 1024:
-        traffic = 51.7e6
+        traffic = 52.3e6
         traffic_note = {"unit": "bytes per launch", "algorithmic_read_bytes_per_launch": 48.5e6,
                         "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the 32 NF4 GEMM launches "
                                   "of one step of the 4-layer stack (profiles/ncu_nf4_gemm_dram_traffic_stack4_m1024.md)"}
