@@ -105,8 +105,16 @@ static sl_status run_pair(const CUtensorMap& ma, const CUtensorMap& mc, const CU
     SL_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gemm2Cfg::kSmem));
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
+  // bf16 output by TMA boxes of 64 columns x 32 rows when a tensor map can
+  // describe it (16-byte aligned base and row stride); else direct stores
+  GemmArgs ao = a;
+  CUtensorMap mo = ma;
+  ao.tma_out = (reinterpret_cast<uintptr_t>(a.out) % 16 == 0) && (a.ld_out * 2) % 16 == 0 &&
+               make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, a.N, a.M, static_cast<uint64_t>(a.ld_out) * 2, 64,
+                        32, CU_TENSOR_MAP_SWIZZLE_128B) == SL_OK;
   dim3 grid(static_cast<unsigned>(2 * ceil_div(a.M, 256)), static_cast<unsigned>(ceil_div(a.N, kBN)));
-  return launch_pdl("gemm_nf4_pair_kernel", kern, grid, dim3(kGemm2Threads), Gemm2Cfg::kSmem, stream, ma, mc, ms, a);
+  return launch_pdl("gemm_nf4_pair_kernel", kern, grid, dim3(kGemm2Threads), Gemm2Cfg::kSmem, stream, ma, mc, ms, mo,
+                    ao);
 }
 
 // CTA pairs of the persistent kernel that the device holds at once (driver

@@ -80,7 +80,8 @@ __device__ __forceinline__ void nf4_words_bf16(const uint32_t (&words)[NW], floa
 template <int BMN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
     gemm_nf4_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
-                         const __grid_constant__ CUtensorMap map_s, const GemmArgs args) {
+                         const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_o,
+                         const GemmArgs args) {
   using Cfg = Gemm2Cfg;
   constexpr int S = Cfg::S;
   extern __shared__ uint8_t smem_raw[];
@@ -402,6 +403,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
       const int gm = m0 + row;
       const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
       uint16_t* out = reinterpret_cast<uint16_t*>(args.out);
+      if (args.tma_out) {
+        // Every MMA of the pair has completed, so the stage buffers are free:
+        // this warp's 32 rows x 128 columns leave as two 64-column bf16 TMA
+        // boxes (128-byte swizzle); the tensor map clips rows and columns past
+        // the output.
+        uint8_t* stg = smem + (warp - 2) * 8192;
+        const uint32_t stg_a = ptx::smem_addr(stg);
+#pragma unroll 1
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c0, v);
+          ptx::tmem_wait_ld();
+          const int lc = c0 - cbeg;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             stg_a + (lc / 64) * 4096 + lane * 128 + ((((lc % 64) / 8 + g) ^ (lane & 7)) << 4)),
+                         "r"(pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]))),
+                         "r"(pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]))),
+                         "r"(pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]))),
+                         "r"(pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7])))
+                         : "memory");
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&map_o, stg, n0 + cbeg, m0 + q * 32);
+          ptx::tma_store_2d(&map_o, stg + 4096, n0 + cbeg + 64, m0 + q * 32);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read0();  // the staging is read before the CTA's shared memory goes
+        }
+        __syncwarp();
+      } else {
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cend; c0 += 32) {
         uint32_t v[32];
@@ -419,6 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
             dst[g] = o;
           }
         }
+      }
       }
     } else if (!*abort_flag) {
       give_up();
