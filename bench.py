@@ -31,6 +31,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -113,7 +114,8 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples (set SL_BENCH_OUT to keep them somewhere else); the JSON line carries the summary
+        self.path = os.path.join(os.environ.get("SL_BENCH_OUT", tempfile.gettempdir()), f"sl_clocks_{os.getpid()}.csv")
 
     def start(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
