@@ -219,3 +219,60 @@ def test_sft_step_matches_torch_autograd():
     np.testing.assert_allclose(dh0, dh0_ref, rtol=1e-10, atol=1e-13)
     for n in ("q", "o", "down"):
         np.testing.assert_allclose(grads[0][n][0], grads_ref[0][n][0], rtol=1e-10, atol=1e-14)
+
+
+def _moving_reference_softmax(q, k, v, S, tile, tau):
+    """Causal attention of one head group, accumulated tile by tile over the keys
+    with a per-row reference maximum m (log2 units) that moves only when a
+    tile's maximum exceeds it by more than tau; O and l are rescaled only then.
+    Returns (o, lse, the largest P formed)."""
+    M, D = q.shape
+    group = D // k.shape[1]
+    c = math.log2(math.e) / math.sqrt(128)
+    o = np.zeros((M, D))
+    lse = np.zeros((M, D // 128))
+    pmax = 0.0
+    for h in range(D // 128):
+        g = h // group
+        for row in range(M):
+            b, pos = divmod(row, S)
+            qh = q[row, h * 128:(h + 1) * 128]
+            m, l, acc = -math.inf, 0.0, np.zeros(128)
+            for t0 in range(0, pos + 1, tile):
+                keys = range(b * S + t0, b * S + min(t0 + tile, pos + 1))
+                s2 = np.array([qh @ k[j, g * 128:(g + 1) * 128] for j in keys]) * c
+                mt = s2.max()
+                if mt > m + tau:                       # the reference moves; rescale what was summed
+                    alpha = 2.0 ** (m - mt) if m > -math.inf else 0.0
+                    acc *= alpha
+                    l *= alpha
+                    m = mt
+                p = 2.0 ** (s2 - m)
+                pmax = max(pmax, p.max())
+                l += p.sum()
+                acc += p @ v[list(keys), g * 128:(g + 1) * 128]
+            o[row, h * 128:(h + 1) * 128] = acc / l
+            lse[row, h] = (m + math.log2(l)) * math.log(2.0)
+    return o, lse, pmax
+
+
+def test_moving_reference_maximum_reproduces_the_softmax():
+    """The forward's reading: P = 2^(s c - m) against a reference m that moves only
+    when a key tile's maximum exceeds it by more than 8 gives the softmax's O and
+    lse exactly (up to float64 rounding), with every P at most 2^8; with key norms
+    growing along the sequence the reference does move."""
+    S, M, tile = 64, 128, 16
+    g = np.random.default_rng(5)
+    grow = (1.0 + np.arange(S) / 4.0)[:, None]
+    q = g.standard_normal((M, 256)) * 2.0
+    k = g.standard_normal((M, 128)) * np.tile(grow, (M // S, 1))
+    v = g.standard_normal((M, 128))
+    o_ref, lse_ref = at.attention_fwd(q, k, v, S)
+    for tau in (0.0, 8.0):
+        o, lse, pmax = _moving_reference_softmax(q, k, v, S, tile, tau)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-10)
+        assert pmax <= 2.0 ** tau * (1 + 1e-12)
+    # inputs where the lazy reference does lag the true running maximum by up to 8
+    _, _, pmax8 = _moving_reference_softmax(q, k, v, S, tile, 8.0)
+    assert pmax8 > 2.0
