@@ -437,23 +437,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
         __syncwarp();
       } else {
 #pragma unroll 1
-      for (int c0 = cbeg; c0 < cend; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(t_row + c0, v);
-        ptx::tmem_wait_ld();
-        if (gm < args.M && n0 + c0 < args.N) {
-          uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(gm) * args.ld_out + n0 + c0);
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c0, v);
+          ptx::tmem_wait_ld();
+          if (gm < args.M && n0 + c0 < args.N) {
+            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(gm) * args.ld_out + n0 + c0);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
-            o.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
-            o.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
-            o.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
-            dst[g] = o;
+            for (int g = 0; g < 4; ++g) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
+              o.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+              o.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
+              o.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+              dst[g] = o;
+            }
           }
         }
-      }
       }
     } else if (!*abort_flag) {
       give_up();
