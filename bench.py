@@ -75,6 +75,60 @@ def load_peaks():
         return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+def pick_peak(peaks, clk):
+    """The dense bf16 denominator for the clock the timed region actually ran at.
+
+    The burst figure was measured with the SM clock at its maximum; the
+    sustained one under the power cap at a lower clock.  A kernel timed while
+    the clock stayed at its maximum with no power-cap sample is held to the
+    burst figure; otherwise to the sustained one."""
+    burst = peaks["bf16_tflops"]
+    sus = peaks.get("bf16_tflops_sustained", burst)
+    at_max = bool(clk) and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"] and "sw_power_cap" not in clk["reasons"]
+    if at_max:
+        return burst, "bf16_tflops (burst): SM clock at its maximum and no sw_power_cap sample in the timed region"
+    return sus, "bf16_tflops_sustained: SM clock below its maximum or sw_power_cap seen in the timed region"
+
+
+def _sources_digest(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# The kernel sources whose DRAM traffic a committed ncu summary records.
+GEMM_SOURCES = ["layer_streamed_qlora_linear_b300/csrc/" + f
+                for f in ("gemm.cu", "gemm.cuh", "gemm2.cuh", "gemm3.cuh", "ptx.cuh", "common.cuh")]
+
+
+def profiled_traffic(summary, sources):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel sources as they are now; (None, why) otherwise.
+
+    The summary carries two lines: `traffic_bytes_per_launch: <float>` and
+    `sources_sha256: <hex digest of the sources, concatenated in order>`."""
+    path = os.path.join(ROOT, summary)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, f"no summary at {summary}"
+    val = dig = None
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if line.startswith("traffic_bytes_per_launch:"):
+            val = float(line.split(":", 1)[1])
+        elif line.startswith("sources_sha256:"):
+            dig = line.split(":", 1)[1].strip()
+    if val is None or dig is None:
+        return None, f"{summary} records no traffic for a known source digest"
+    if dig != _sources_digest(sources):
+        return None, f"the kernel sources changed since {summary} was captured"
+    return val, f"ncu dram__bytes_read.sum + dram__bytes_write.sum per launch ({summary})"
+
+
 def rank_barrier(world):
     """All replicas meet (no-op for one process)."""
     if world > 1:
@@ -609,18 +663,19 @@ def run_ours(args):
     ms_d = sum(timing[k][1] for k in dominant)
     fl_d = sum(timing[k][2] for k in dominant)
     achieved = fl_d / (ms_d * 1e-3) / 1e12 if ms_d > 0 else 0.0
-    # DRAM bytes per launch of the dominant kernel from an ncu capture of the same kernels (one full
-    # step of a 4-layer stack: the per-layer launch mix of the 32-layer workload); null elsewhere
+    # DRAM bytes per launch of the dominant kernel: from the committed ncu summary of the same
+    # kernels (one layer's NF4 GEMM launches of the 8B stack at M = 1024), only while the kernel
+    # sources are the ones it was captured on; null elsewhere
     traffic, traffic_note = None, None
     if w["kind"] == "stack" and w["base"] == "nf4" and w["D"] == 4096 and w["M"] == 1024:
-        traffic = 52.3e6
-        traffic_note = {"unit": "bytes per launch", "algorithmic_read_bytes_per_launch": 48.5e6,
-                        "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the 32 NF4 GEMM launches "
-                                  "of one step of the 4-layer stack (profiles/ncu_nf4_gemm_dram_traffic_stack4_m1024.md)"}
-    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        traffic, why = profiled_traffic("profiles/ncu_nf4_gemm_dram_traffic_stack4_m1024.md", GEMM_SOURCES)
+        traffic_note = {"unit": "bytes per launch", "source": why}
+    peak, peak_why = pick_peak(peaks, clk)
+    burst = peaks["bf16_tflops"]
+    sus = peaks.get("bf16_tflops_sustained", burst)
     roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                "frac": achieved / peak, "peak_source": f"{peak_src} {peak_why}",
+                "frac_burst": achieved / burst, "frac_sustained": achieved / sus,
                 "traffic": traffic, "traffic_note": traffic_note, "launches": n_d,
                 "avg_launch_ms": ms_d / max(1, n_d),
                 "share_of_step": ms_d / ms_instr,
@@ -658,6 +713,24 @@ def run_ours(args):
             barrier()
             line["resident"] = {"tokens_per_s": M * nres / (e0.elapsed_time(e1) * 1e-3),
                                 "ms_per_step": e0.elapsed_time(e1) / nres}
+            # the pages' exactness check at this configuration: one more streamed step on the same
+            # inputs into separate outputs (adapters laid out the same way), compared bit for bit
+            # with the resident step's hL, dh0 and every dA, dB
+            hL_s, dh0_s = torch.empty_like(hL), torch.empty_like(dh0)
+            dA_s, dB_s = [], []
+            for _ in range(L):
+                dA_s += sl.packed_views(sa, torch.float32, dev)
+                dB_s += sl.packed_views(sb, torch.float32, dev)
+            stk.step(sl.SL_MODE_STREAMED, h0, dh, A, B, r, alpha, hL_s, dh0_s, dA_s, dB_s, ws)
+            torch.cuda.synchronize()
+            same = lambda x, y: torch.equal(x.view(torch.int32), y.view(torch.int32))
+            bad = [n for n, x, y in [("hL", hL_s, hL), ("dh0", dh0_s, dh0)] if not same(x, y)]
+            bad += [f"dA[{i}]" for i, (x, y) in enumerate(zip(dA_s, dA)) if not same(x, y)]
+            bad += [f"dB[{i}]" for i, (x, y) in enumerate(zip(dB_s, dB)) if not same(x, y)]
+            line["streamed_equals_resident"] = not bad
+            line["streamed_vs_resident"] = {"compared": f"hL, dh0 and {len(dA) + len(dB)} adapter gradients",
+                                            "mismatched": bad[:8]}
+            sl.sl_check_device_errors()
             stk_r.close()
             del dev_blobs
     else:
@@ -665,7 +738,10 @@ def run_ours(args):
         t_roof = max(fl / (peaks["bf16_tflops"] * 1e12), nb / (peaks["hbm_gbs"] * 1e9))
         sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         t_roof_s = max(fl / (sus * 1e12), nb / (peaks["hbm_gbs"] * 1e9))
-        line["step_roofline"] = {"algorithmic_flops": fl, "algorithmic_bytes": nb,
+        pk, pk_why = pick_peak(peaks, clk)
+        t_roof_c = max(fl / (pk * 1e12), nb / (peaks["hbm_gbs"] * 1e9))
+        line["step_roofline"] = {"frac_at_clock": t_roof_c / (ms_step * 1e-3), "peak_at_clock": f"{peak_src} {pk_why}",
+                                 "algorithmic_flops": fl, "algorithmic_bytes": nb,
                                  "roofline_ms": t_roof * 1e3, "frac": t_roof / (ms_step * 1e-3),
                                  "peaks": f"{peak_src} bf16_tflops (burst) and hbm_gbs",
                                  "roofline_ms_sustained": t_roof_s * 1e3,

@@ -24,7 +24,9 @@
  * Conventions for every call:
  *  - Device pointers unless stated; the CALLER owns every tensor passed in.
  *    libsl owns only what sl_stack_create allocates (two device layer buffers,
- *    a copy stream, events) and one int per device for error reporting.
+ *    a copy stream, events) and two file-scope device arrays that every
+ *    device loading the library holds until exit: the error word (two ints)
+ *    and the 4 MiB scratch of sl_lora_linear_fwd_noalloc.
  *  - Work is enqueued on the caller's stream and the call returns without
  *    waiting, except where a call says it synchronises.
  *  - bf16 tensors are passed as void* (IEEE bfloat16 bit patterns, row-major,
@@ -219,9 +221,10 @@ sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const void* dY, 
  * sums of X A^T, lives in one fixed 4 MiB device array inside libsl that
  * every device loading the library holds until exit; a call needing more
  * than 4 MiB (ceil(K/512) * M * r * 4 bytes) returns SL_ERR_INVALID and
- * enqueues nothing.  The first call on a device looks up that array's
- * device address (cudaGetSymbolAddress) and should come before any stream
- * capture.  All calls share the array and it keeps the last call's
+ * enqueues nothing, as does a base pointer (X, A, B, Y, T_save) that is not
+ * 16-byte aligned.  The first call on a device looks up the device
+ * addresses of that array and of the error word (cudaGetSymbolAddress) and
+ * should come before any stream capture.  All calls share the array and it keeps the last call's
  * contents (nothing in it needs to start at zero); calls that overlap on
  * the GPU, e.g. on two streams, race on it and must be serialised. */
 sl_status sl_lora_linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t M,

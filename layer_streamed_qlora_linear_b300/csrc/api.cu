@@ -34,10 +34,14 @@ sl_status check_launch(const char* what) {
 
 uint64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
+// words[0]: error word; words[1]: a flag that nothing ever sets (timeout probe).
+// A file-scope device array, zero when the module loads, so that no call of
+// libsl allocates (or synchronises) to get it; its device address is looked
+// up once per device with that device current.
+static __device__ int g_device_words[2];
 static std::mutex g_word_mu;
 static int* g_words[64] = {nullptr};
 
-// words[0]: error word; words[1]: a flag that nothing ever sets (timeout probe).
 static int* device_words() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -46,17 +50,13 @@ static int* device_words() {
   }
   std::lock_guard<std::mutex> lk(g_word_mu);
   if (!g_words[dev]) {
-    int* p = nullptr;
-    if (cudaMalloc(&p, 2 * sizeof(int)) != cudaSuccess) {
-      set_error(SL_ERR_OOM, "device_error_word: cudaMalloc failed");
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_device_words);
+    if (e != cudaSuccess || !p) {
+      cuda_error(e, "device_error_word: cudaGetSymbolAddress");
       return nullptr;
     }
-    if (cudaMemset(p, 0, 2 * sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-      cudaFree(p);
-      set_error(SL_ERR_CUDA, "device_error_word: cudaMemset failed");
-      return nullptr;
-    }
-    g_words[dev] = p;
+    g_words[dev] = static_cast<int*>(p);
   }
   return g_words[dev];
 }

@@ -61,10 +61,11 @@ sl_status launch_pdl(const char* what, void (*kern)(KArgs...), dim3 grid, dim3 b
 }
 
 // ------------------------------------------------------ device error word
-// One int per device, allocated on first use, read and cleared by
-// sl_check_device_errors().  Kernels whose bounded waits give up write a
-// nonzero sl_status code here instead of trapping.
-int* device_error_word();   // nullptr (and sl_last_error set) if it cannot be allocated
+// One int per device in a file-scope device array (zero at module load; no
+// allocation), read and cleared by sl_check_device_errors().  Kernels whose
+// bounded waits give up write a nonzero sl_status code here instead of
+// trapping.
+int* device_error_word();   // nullptr (and sl_last_error set) if its address cannot be found
 
 // Bounded-wait limit used by every spin in libsl kernels (nanoseconds of
 // %globaltimer).  A healthy wait in these kernels lasts microseconds; two

@@ -143,10 +143,10 @@ int down_splits(int64_t K) { return static_cast<int>(ceil_div(K, kDnCols)); }
 static size_t down_smem(int R) {
   return (static_cast<size_t>(kDnRows) * (kDnCols + kDnPad) + static_cast<size_t>(R) * (kDnCols + kDnPad)) * 2;
 }
+// Set on every call (a cheap host-side call), so the attribute holds on
+// whichever device is current.
 template <typename Kern>
 static sl_status set_smem(Kern k, size_t bytes) {
-  static bool done[64] = {false};
-  (void)done;
   SL_CHECK_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)));
   return SL_OK;
 }
@@ -162,12 +162,8 @@ sl_status lora_down(const uint16_t* X, int64_t M, int K, const uint16_t* W, int 
   const size_t sm = down_smem(R);
 #define SL_DOWN(RR, WT)                                                                           \
   do {                                                                                            \
-    static bool attr = false;                                                                     \
-    if (!attr) {                                                                                  \
-      sl_status st_ = set_smem(lora_down_kernel<RR, WT>, sm);                                     \
-      if (st_ != SL_OK) return st_;                                                               \
-      attr = true;                                                                                \
-    }                                                                                             \
+    sl_status st_ = set_smem(lora_down_kernel<RR, WT>, sm);                                       \
+    if (st_ != SL_OK) return st_;                                                                 \
     lora_down_kernel<RR, WT><<<grid, 128, sm, stream>>>(X, M, K, W, r, dst);                      \
   } while (0)
   if (R == 8) { if (wt) SL_DOWN(8, 1); else SL_DOWN(8, 0); }
@@ -515,6 +511,14 @@ sl_status linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t M, const
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_fwd_noalloc: M too large");
   st = check_rows(w, M, "sl_lora_linear_fwd_noalloc");
   if (st != SL_OK) return st;
+  // The rank-r pass reads X and A with 16-byte cp.async loads and the GEMM
+  // moves X, B, T_save and Y by TMA: check every base up front, so that a
+  // misaligned pointer is an error status before anything is launched.
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  SL_REQUIRE(al16(X) && al16(Y) && (w->K * 2) % 16 == 0 && (w->N * 2) % 16 == 0,
+             "sl_lora_linear_fwd_noalloc: X and Y must be 16-byte aligned");
+  SL_REQUIRE(!lora || (al16(A) && al16(B) && al16(T_save)),
+             "sl_lora_linear_fwd_noalloc: A, B and T_save must be 16-byte aligned");
   const size_t need = lora ? noalloc_need(M, w->K, r) : 0;
   if (need > kNoAllocScratchBytes)
     return set_error(SL_ERR_INVALID, "sl_lora_linear_fwd_noalloc: needs " + std::to_string(need) +
