@@ -79,15 +79,18 @@ def pick_peak(peaks, clk):
     """The dense bf16 denominator for the clock the timed region actually ran at.
 
     The burst figure was measured with the SM clock at its maximum; the
-    sustained one under the power cap at a lower clock.  A kernel timed while
-    the clock stayed at its maximum with no power-cap sample is held to the
-    burst figure; otherwise to the sustained one."""
+    sustained one under the power cap, at a much lower clock.  A kernel timed
+    while the median SM clock stayed within 3% of its maximum (power-cap
+    samples or not) is held to the burst figure; otherwise to the sustained
+    one."""
     burst = peaks["bf16_tflops"]
     sus = peaks.get("bf16_tflops_sustained", burst)
-    at_max = bool(clk) and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"] and "sw_power_cap" not in clk["reasons"]
-    if at_max:
-        return burst, "bf16_tflops (burst): SM clock at its maximum and no sw_power_cap sample in the timed region"
-    return sus, "bf16_tflops_sustained: SM clock below its maximum or sw_power_cap seen in the timed region"
+    if not clk:
+        return sus, "bf16_tflops_sustained: no clock samples from the timed region"
+    cap = " (sw_power_cap seen)" if "sw_power_cap" in clk["reasons"] else ""
+    if clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"]:
+        return burst, f"bf16_tflops (burst): median SM clock {clk['sm_mhz']:.0f} of {clk['sm_max_mhz']:.0f} MHz{cap}"
+    return sus, f"bf16_tflops_sustained: median SM clock {clk['sm_mhz']:.0f} of {clk['sm_max_mhz']:.0f} MHz{cap}"
 
 
 def _sources_digest(paths):
