@@ -10,9 +10,10 @@
 //     memory at the same offsets and writes each CTA's 128 accumulator rows
 //     into that CTA's TMEM;
 //   * A tiles of both CTAs complete on the leader's `full` barrier (TMA
-//     .cta_group::2); each CTA's dequant warps arrive on its local
-//     `b_local`, and one thread of the peer forwards that to the leader's
-//     `b_peer` as a 16-byte async-proxy copy (complete_tx); MMA
+//     .cta_group::2); the leader's dequant warps arrive on `full` too, the
+//     peer's on their local `b_local`, and one thread of the peer forwards
+//     that to the leader's `full` as a 16-byte async-proxy copy
+//     (complete_tx): the MMA issuer waits once per k-block; MMA
 //     completion is multicast to both CTAs' `empty` / `main_done` /
 //     `acc_full` barriers.
 // Per SM this halves the dequant work of every k-block while keeping one
@@ -36,7 +37,7 @@ struct Gemm2Cfg {
   static constexpr int kOffB = kOffA + S * kATileBytes;
   static constexpr int kOffRaw = kOffB + S * kHalfBTileBytes;
   static constexpr int kOffBar = kOffRaw + S * kRawBytes;
-  static constexpr int kNumBars = 5 * S + 3;
+  static constexpr int kNumBars = 4 * S + 3;
   static constexpr int kOffSink = (kOffBar + kNumBars * 8 + 15) / 16 * 16;  // 16-byte signal landing pad
   static constexpr int kOffMisc = kOffSink + 16;
   static constexpr int kBytes = kOffMisc + 16;
@@ -90,14 +91,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
   uint8_t* sB = smem + Cfg::kOffB;
   uint8_t* sRaw = smem + Cfg::kOffRaw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
-  uint64_t* full = bars;               // leader: A tiles of both CTAs landed
+  uint64_t* full = bars;               // leader: stage ready (A of both CTAs, both B halves)
   uint64_t* raw_full = bars + S;       // each CTA: its codes + absmax landed
-  uint64_t* b_local = bars + 2 * S;    // each CTA: its own B half dequantised (its 8 warps)
+  uint64_t* b_local = bars + 2 * S;    // peer: its own B half dequantised (4 warps of one group)
   uint64_t* empty = bars + 3 * S;      // each CTA: stage consumed by the MMAs
-  uint64_t* b_peer = bars + 4 * S;     // leader: the peer's B half dequantised (one forwarded arrive)
-  uint64_t* lora_full = bars + 5 * S;  // leader: both CTAs staged the LoRA operands
-  uint64_t* acc_full = bars + 5 * S + 1;
-  uint64_t* main_done = bars + 5 * S + 2;
+  uint64_t* lora_full = bars + 4 * S;  // leader: both CTAs staged the LoRA operands
+  uint64_t* acc_full = bars + 4 * S + 1;
+  uint64_t* main_done = bars + 4 * S + 2;
   uint8_t* sink = smem + Cfg::kOffSink;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
@@ -115,11 +115,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
-      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&full[i], 1 + kNumDq2 / 64);  // producer + the 4 warps of the owning dequant group
       ptx::mbar_init(&raw_full[i], 1);
       ptx::mbar_init(&b_local[i], kNumDq2 / 64);  // the 4 warps of the group that owns this k-block
       ptx::mbar_init(&empty[i], 1);
-      ptx::mbar_init(&b_peer[i], 1);
     }
     ptx::mbar_init(lora_full, 2 * (kNumDq2 / 32));
     ptx::mbar_init(acc_full, 1);
@@ -158,7 +157,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
           give_up();
           break;
         }
-        if (leader) ptx::mbar_arrive_expect_tx(&full[s], 2 * kATileBytes);
+        if (leader) ptx::mbar_arrive_expect_tx(&full[s], 2 * kATileBytes + 16);  // + the peer's signal
         ptx::tma_load_2d_pair(sA + s * kATileBytes, &map_a, ptx::map_to_rank(&full[s], 0), kb * kBK, m0);
         uint8_t* raw = sRaw + s * Cfg::kRawBytes;
         ptx::mbar_arrive_expect_tx(&raw_full[s], rawtx);
@@ -182,30 +181,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
       constexpr uint32_t idesc = ptx::idesc_bf16(256, kBN, 0, BMN);
       const uint32_t a_base = ptx::smem_addr(sA);
       const uint32_t b_base = ptx::smem_addr(sB);
+      // descriptors of stage 0, k-step 0; offsets / 16 add to the start address
+      const uint64_t a_desc0 = ptx::smem_desc(a_base, 16, 1024, 2);
+      const uint64_t b_desc0 = BMN ? ptx::smem_desc(b_base, 64 * 128, 1024, 2) : ptx::smem_desc(b_base, 16, 1024, 2);
+      constexpr uint32_t kBStep = BMN ? 2048 : 32;
       bool ok = true;
       for (int kb = 0; kb < KB && ok; ++kb) {
         const int s = kb % S;
         const uint32_t ph = (kb / S) & 1;
-        if (!ptx::mbar_wait_cluster(&full[s], ph, abort_flag) || !ptx::mbar_wait(&b_local[s], ph, abort_flag)) {
-          give_up();
-          ok = false;
-          break;
-        }
-        // The peer's half arrives as a 16-byte async copy (complete_tx) on b_peer.
-        ptx::mbar_arrive_expect_tx(&b_peer[s], 16);
-        if (!ptx::mbar_wait_cluster(&b_peer[s], ph, abort_flag)) {
+        if (!ptx::mbar_wait_cluster(&full[s], ph, abort_flag)) {
           give_up();
           ok = false;
           break;
         }
         ptx::tc_fence_after();
+        const uint64_t ad_s = a_desc0 + static_cast<uint64_t>((s * kATileBytes) >> 4);
+        const uint64_t bd_s = b_desc0 + static_cast<uint64_t>((s * kHalfBTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t ad = ptx::smem_desc(a_base + s * kATileBytes + kk * 32, 16, 1024, 2);
-          const uint64_t bd = BMN ? ptx::smem_desc(b_base + s * kHalfBTileBytes + kk * 2048, 64 * 128, 1024, 2)
-                                  : ptx::smem_desc(b_base + s * kHalfBTileBytes + kk * 32, 16, 1024, 2);
-          ptx::mma_bf16_pair(tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          ptx::mma_bf16_pair(tmem, ad_s + static_cast<uint64_t>((kk * 32) >> 4),
+                             bd_s + static_cast<uint64_t>((kk * kBStep) >> 4), idesc, (kb | kk) ? 1u : 0u);
         ptx::mma_commit_pair(&empty[s], 0x3);
       }
       if (ok && has_lora) {
@@ -231,8 +226,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
       // Peer CTA: tell the leader "my B half of stage s is ready" once the
       // local dequant warps have arrived (their smem writes were fenced for
       // the async proxy), with a 16-byte async-proxy copy that completes on
-      // the leader's b_peer -- no memory fence on this path.
-      const uint32_t leader_b_peer = ptx::map_to_rank(&b_peer[0], 0);
+      // the leader's full[s] -- no memory fence on this path.
+      const uint32_t leader_full = ptx::map_to_rank(&full[0], 0);
       const uint32_t leader_sink = ptx::map_to_rank(sink, 0);
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % S;
@@ -240,7 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
           give_up();
           break;
         }
-        ptx::bulk_signal_16(leader_sink, sink, leader_b_peer + s * 8);
+        ptx::bulk_signal_16(leader_sink, sink, leader_full + s * 8);
       }
     }
   } else {
@@ -359,7 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
       }
       ptx::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&b_local[s]);
+      if (lane == 0) ptx::mbar_arrive(leader ? &full[s] : &b_local[s]);
     }
     if (ok && has_lora) {
       const int s = KB % S;

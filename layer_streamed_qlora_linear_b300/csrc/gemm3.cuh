@@ -14,6 +14,9 @@
 //     in the forward each tile folds the side product of the projection it
 //     lies in (T_cat columns g r .., row stride G r); the grouped dX is the
 //     plain fold at rank G r (s U_cat A_cat), up to 64;
+// The MMA issuer waits once per k-block: the leader's full[s] counts the A
+// tiles of both CTAs, the leader's own dequant warps and the peer's
+// forwarded "B half ready" signal.
 // Warps: 0 A/code TMA producer, 1 MMA issuer (leader) or peer forwarder,
 // 2..9 NF4 dequant (two groups on alternate k-blocks), 10..13 LoRA staging +
 // epilogue.  Every wait is bounded.
@@ -44,7 +47,7 @@ struct Gemm3Cfg {
   static constexpr int kOffLB = kOffLA + kLA * kLoraAtom;        // LoRA Be: K-major [128 x 2r] / MN-major 2 atoms of [2R x 64]
   static constexpr int kOffRaw = kOffLB + kLBBytes;
   static constexpr int kOffBar = kOffRaw + S * kRawBytes;
-  static constexpr int kNumBars = 5 * S + 7;
+  static constexpr int kNumBars = 4 * S + 7;
   static constexpr int kOffSink = (kOffBar + kNumBars * 8 + 15) / 16 * 16;
   static constexpr int kOffMisc = kOffSink + 16;
   static constexpr int kBytes = kOffMisc + 16;
@@ -75,12 +78,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
   uint8_t* sLB = smem + Cfg::kOffLB;
   uint8_t* sRaw = smem + Cfg::kOffRaw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
-  uint64_t* full = bars;                 // [S] leader: A tiles of both CTAs landed
+  // full[s] (leader) completes when stage s is ready for the MMAs: the A
+  // tiles of both CTAs landed (TMA bytes), the leader's B half is
+  // dequantised (4 warp arrivals) and the peer's is (a 16-byte async-proxy
+  // signal from the peer, counted as bytes) -- one wait per k-block.
+  uint64_t* full = bars;                 // [S] leader: stage s ready for the MMAs
   uint64_t* raw_full = bars + S;         // [S] each CTA: codes + absmax landed
-  uint64_t* b_local = bars + 2 * S;      // [S] each CTA: its B half dequantised (4 warps of one group)
+  uint64_t* b_local = bars + 2 * S;      // [S] peer: its B half dequantised (4 warps of one group)
   uint64_t* empty = bars + 3 * S;        // [S] each CTA: stage consumed by the MMAs
-  uint64_t* b_peer = bars + 4 * S;       // [S] leader: the peer's B half dequantised
-  uint64_t* lora_full = bars + 5 * S;    // leader: both CTAs staged this tile's LoRA operands
+  uint64_t* lora_full = bars + 4 * S;    // leader: both CTAs staged this tile's LoRA operands
   uint64_t* lora_empty = lora_full + 1;  // each CTA: the fold MMAs of the previous tile are done with them
   uint64_t* acc_full = lora_full + 2;    // [2] each CTA: accumulator a holds a finished segment
   uint64_t* acc_empty = lora_full + 4;   // [2] leader: both CTAs' epilogues drained accumulator a
@@ -108,11 +114,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
-      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&full[i], 1 + kNumDq2 / 64);  // producer + the 4 warps of the owning dequant group
       ptx::mbar_init(&raw_full[i], 1);
       ptx::mbar_init(&b_local[i], kNumDq2 / 64);
       ptx::mbar_init(&empty[i], 1);
-      ptx::mbar_init(&b_peer[i], 1);
     }
     ptx::mbar_init(lora_full, 2 * (kNumEpi3 / 32));
     ptx::mbar_init(lora_empty, 1);
@@ -164,7 +169,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
             ok = false;
             break;
           }
-          if (leader) ptx::mbar_arrive_expect_tx(&full[s], 2 * kATileBytes);
+          // A tiles of both CTAs and the peer's 16-byte "B half ready" signal
+          if (leader) ptx::mbar_arrive_expect_tx(&full[s], 2 * kATileBytes + 16);
           ptx::tma_load_2d_pair(sA + s * kATileBytes, &map_a, ptx::map_to_rank(&full[s], 0), kb * kBK, m0);
           uint8_t* raw = sRaw + s * Cfg::kRawBytes;
           ptx::mbar_arrive_expect_tx(&raw_full[s], rawtx);
@@ -203,6 +209,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       const uint32_t b_base = ptx::smem_addr(sB);
       const uint32_t la = ptx::smem_addr(sLA);
       const uint32_t lb = ptx::smem_addr(sLB);
+      // descriptors of stage 0, k-step 0; a stage / k-step adds its byte
+      // offset / 16 to the start-address field (bits 0..13)
+      const uint64_t a_desc0 = ptx::smem_desc(a_base, 16, 1024, 2);
+      const uint64_t b_desc0 = BMN ? ptx::smem_desc(b_base, 64 * 128, 1024, 2) : ptx::smem_desc(b_base, 16, 1024, 2);
+      constexpr uint32_t kBStep = BMN ? 2048 : 32;  // bytes between k16 steps of the B half
       const int ksteps = has_lora ? (2 * args.r + 15) / 16 : 0;
       int g = 0, it = 0;
       bool ok = true;
@@ -219,24 +230,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
         for (int kb = 0; kb < KB; ++kb, ++g) {
           const int s = g % S;
           const uint32_t ph = (g / S) & 1;
-          if (!ptx::mbar_wait_cluster(&full[s], ph, abort_flag) || !ptx::mbar_wait(&b_local[s], ph, abort_flag)) {
-            give_up();
-            ok = false;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(&b_peer[s], 16);
-          if (!ptx::mbar_wait_cluster(&b_peer[s], ph, abort_flag)) {
+          if (!ptx::mbar_wait_cluster(&full[s], ph, abort_flag)) {
             give_up();
             ok = false;
             break;
           }
           ptx::tc_fence_after();
+          const uint64_t ad_s = a_desc0 + static_cast<uint64_t>((s * kATileBytes) >> 4);
+          const uint64_t bd_s = b_desc0 + static_cast<uint64_t>((s * kHalfBTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = ptx::smem_desc(a_base + s * kATileBytes + kk * 32, 16, 1024, 2);
-            const uint64_t bd = BMN ? ptx::smem_desc(b_base + s * kHalfBTileBytes + kk * 2048, 64 * 128, 1024, 2)
-                                    : ptx::smem_desc(b_base + s * kHalfBTileBytes + kk * 32, 16, 1024, 2);
-            ptx::mma_bf16_pair(d, ad, bd, idesc, accum);
+            ptx::mma_bf16_pair(d, ad_s + static_cast<uint64_t>((kk * 32) >> 4),
+                               bd_s + static_cast<uint64_t>((kk * kBStep) >> 4), idesc, accum);
             accum = 1;
           }
           ptx::mma_commit_pair(&empty[s], 0x3);
@@ -265,7 +270,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       }
     } else if (lane == 0) {
       // -------------------------------------------------- peer: B-ready forwarder
-      const uint32_t leader_b_peer = ptx::map_to_rank(&b_peer[0], 0);
+      // (a 16-byte async-proxy copy whose bytes complete on the leader's full[s])
+      const uint32_t leader_full = ptx::map_to_rank(&full[0], 0);
       const uint32_t leader_sink = ptx::map_to_rank(sink, 0);
       int g = 0;
       bool ok = true;
@@ -277,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
             ok = false;
             break;
           }
-          ptx::bulk_signal_16(leader_sink, sink, leader_b_peer + s * 8);
+          ptx::bulk_signal_16(leader_sink, sink, leader_full + s * 8);
         }
       }
     }
@@ -323,7 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&b_local[s]);
+        if (lane == 0) ptx::mbar_arrive(leader ? &full[s] : &b_local[s]);
       }
     }
   } else {
