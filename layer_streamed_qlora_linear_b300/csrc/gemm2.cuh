@@ -181,27 +181,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
       constexpr uint32_t idesc = ptx::idesc_bf16(256, kBN, 0, BMN);
       const uint32_t a_base = ptx::smem_addr(sA);
       const uint32_t b_base = ptx::smem_addr(sB);
-      // descriptors of stage 0, k-step 0; offsets / 16 add to the start address
+      // descriptors of stage 0, k-step 0; the start-address field sits in the
+      // low word below 2^14, so a stage / k-step offset is a 32-bit add
       const uint64_t a_desc0 = ptx::smem_desc(a_base, 16, 1024, 2);
       const uint64_t b_desc0 = BMN ? ptx::smem_desc(b_base, 64 * 128, 1024, 2) : ptx::smem_desc(b_base, 16, 1024, 2);
+      const uint32_t a_lo0 = static_cast<uint32_t>(a_desc0), a_hi = static_cast<uint32_t>(a_desc0 >> 32);
+      const uint32_t b_lo0 = static_cast<uint32_t>(b_desc0), b_hi = static_cast<uint32_t>(b_desc0 >> 32);
       constexpr uint32_t kBStep = BMN ? 2048 : 32;
       bool ok = true;
+      int s = 0;
+      uint32_t ph = 0;
       for (int kb = 0; kb < KB && ok; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (kb / S) & 1;
         if (!ptx::mbar_wait_cluster(&full[s], ph, abort_flag)) {
           give_up();
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint64_t ad_s = a_desc0 + static_cast<uint64_t>((s * kATileBytes) >> 4);
-        const uint64_t bd_s = b_desc0 + static_cast<uint64_t>((s * kHalfBTileBytes) >> 4);
+        const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(s) * (kATileBytes >> 4);
+        const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(s) * (kHalfBTileBytes >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-          ptx::mma_bf16_pair(tmem, ad_s + static_cast<uint64_t>((kk * 32) >> 4),
-                             bd_s + static_cast<uint64_t>((kk * kBStep) >> 4), idesc, (kb | kk) ? 1u : 0u);
+          ptx::mma_bf16_pair_lohi(tmem, a_lo + kk * (32 >> 4), a_hi, b_lo + kk * (kBStep >> 4), b_hi, idesc,
+                                  (kb | kk) ? 1u : 0u);
         ptx::mma_commit_pair(&empty[s], 0x3);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (ok && has_lora) {
         ptx::mma_commit_pair(main_done, 0x3);

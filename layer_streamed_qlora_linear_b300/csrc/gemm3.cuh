@@ -213,6 +213,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       // offset / 16 to the start-address field (bits 0..13)
       const uint64_t a_desc0 = ptx::smem_desc(a_base, 16, 1024, 2);
       const uint64_t b_desc0 = BMN ? ptx::smem_desc(b_base, 64 * 128, 1024, 2) : ptx::smem_desc(b_base, 16, 1024, 2);
+      // the start-address field is in the low word and stays below 2^14
+      // (shared memory < 256 KB): stepping it is a 32-bit add
+      const uint32_t a_lo0 = static_cast<uint32_t>(a_desc0), a_hi = static_cast<uint32_t>(a_desc0 >> 32);
+      const uint32_t b_lo0 = static_cast<uint32_t>(b_desc0), b_hi = static_cast<uint32_t>(b_desc0 >> 32);
       constexpr uint32_t kBStep = BMN ? 2048 : 32;  // bytes between k16 steps of the B half
       const int ksteps = has_lora ? (2 * args.r + 15) / 16 : 0;
       int g = 0, it = 0;
@@ -226,25 +230,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           break;
         }
         ptx::tc_fence_after();
-        uint32_t accum = 0;
+        int s = g % S;                       // stage and phase, stepped without division
+        uint32_t ph = (g / S) & 1;
         for (int kb = 0; kb < KB; ++kb, ++g) {
-          const int s = g % S;
-          const uint32_t ph = (g / S) & 1;
           if (!ptx::mbar_wait_cluster(&full[s], ph, abort_flag)) {
             give_up();
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint64_t ad_s = a_desc0 + static_cast<uint64_t>((s * kATileBytes) >> 4);
-          const uint64_t bd_s = b_desc0 + static_cast<uint64_t>((s * kHalfBTileBytes) >> 4);
+          const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(s) * (kATileBytes >> 4);
+          const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(s) * (kHalfBTileBytes >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            ptx::mma_bf16_pair(d, ad_s + static_cast<uint64_t>((kk * 32) >> 4),
-                               bd_s + static_cast<uint64_t>((kk * kBStep) >> 4), idesc, accum);
-            accum = 1;
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            ptx::mma_bf16_pair_lohi(d, a_lo + kk * (32 >> 4), a_hi, b_lo + kk * (kBStep >> 4), b_hi, idesc,
+                                    (kb | kk) ? 1u : 0u);
           ptx::mma_commit_pair(&empty[s], 0x3);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
         if (has_lora) {  // fold the LoRA side product into this accumulator
