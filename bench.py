@@ -716,6 +716,25 @@ def run_ours(args):
             barrier()
             line["resident"] = {"tokens_per_s": M * nres / (e0.elapsed_time(e1) * 1e-3),
                                 "ms_per_step": e0.elapsed_time(e1) / nres}
+            # the same resident steps with a CUDA event pair around every tensor-core launch
+            sl.sl_kernel_timing(True)
+            barrier()
+            e0.record(stream)
+            for _ in range(nres):
+                stk_r.step(sl.SL_MODE_RESIDENT, h0, dh, A, B, r, alpha, hL, dh0, dA, dB, ws)
+            e1.record(stream)
+            barrier()
+            sl.sl_kernel_timing(False)
+            rk = {}
+            for i, name in enumerate(sl.TIMED_VARIANTS):
+                n_, ms_, wk = sl.sl_kernel_timing_read(i)
+                if n_:
+                    rate = wk / (ms_ * 1e-3) if ms_ else 0.0
+                    rk[name] = ({"launches": n_, "ms_per_step": ms_ / nres, "gbs": rate / 1e9}
+                                if name in sl.RANK_R_VARIANTS else
+                                {"launches": n_, "ms_per_step": ms_ / nres, "tflops": rate / 1e12})
+            line["resident"]["kernels"] = rk
+            line["resident"]["ms_per_step_timed"] = e0.elapsed_time(e1) / nres
             # the pages' exactness check at this configuration: one more streamed step on the same
             # inputs into separate outputs (adapters laid out the same way), compared bit for bit
             # with the resident step's hL, dh0 and every dA, dB

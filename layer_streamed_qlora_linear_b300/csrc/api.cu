@@ -63,6 +63,34 @@ static int* device_words() {
 
 int* device_error_word() { return device_words(); }
 
+cudaStream_t hi_stream() {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!streams[dev]) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, greatest) != cudaSuccess) {
+      cudaGetLastError();
+      streams[dev] = nullptr;
+    }
+  }
+  return streams[dev];
+}
+
+cudaEvent_t fork_event(int i) {
+  thread_local cudaEvent_t events[64][4] = {};
+  int dev = 0;
+  if (i < 0 || i >= 4 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!events[dev][i] && cudaEventCreateWithFlags(&events[dev][i], cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    events[dev][i] = nullptr;
+  }
+  return events[dev][i];
+}
+
 int num_sms() {
   static int sms[64] = {0};
   int dev = 0;

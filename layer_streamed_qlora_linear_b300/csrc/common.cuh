@@ -102,4 +102,14 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int num_sms();
 
+// A library-owned stream per device at the highest stream priority, created
+// on first use (nullptr if that fails).  The LoRA backward runs its U pass
+// and dX GEMM there while the adapter-gradient passes run on the caller's
+// stream; blocks of the high-priority stream are dispatched first, so the
+// gradient passes fill the SMs the GEMM leaves idle.
+cudaStream_t hi_stream();
+// Thread-local events for fork/join between a caller's stream and
+// hi_stream() (per device; `i` < 4).
+cudaEvent_t fork_event(int i);
+
 }  // namespace sl

@@ -282,9 +282,9 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
   return launch_gemm(g, stream);
 }
 
-sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A, const void* B,
-                     int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
-                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+sl_status linear_bwd_split(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A, const void* B,
+                           int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
+                           void* ws, size_t ws_bytes, cudaStream_t stream, const GradSide* side) {
   sl_status st = check_weight(w);
   if (st != SL_OK) return st;
   SL_REQUIRE(dY && M > 0, "sl_lora_linear_bwd: null dY or M <= 0");
@@ -309,6 +309,10 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
     st = skinny_down(static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), static_cast<const uint16_t*>(B), 1,
                      r, 1, nullptr, U, stream);
     if (st != SL_OK) return st;
+    if (side) {  // dA and dB go to the side stream once U is written
+      SL_CHECK_CUDA(cudaEventRecord(side->fork, stream));
+      SL_CHECK_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
+    }
   }
   if (dX) {
     GemmLaunch g{};
@@ -333,15 +337,48 @@ sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t 
   }
   if (lora) {
     const float s = alpha / static_cast<float>(r);
+    cudaStream_t gs = side ? side->stream : stream;
     // dA [r, K] = s U^T X;  dB [N, r] = s dY^T T
     st = skinny_grad(U, static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), r, 1, nullptr, 0, s, dA, 1,
-                     accumulate, stream);
+                     accumulate, gs);
     if (st != SL_OK) return st;
     st = skinny_grad(static_cast<const float*>(T_save), static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), r,
-                     1, nullptr, 1, s, dB, 0, accumulate, stream);
+                     1, nullptr, 1, s, dB, 0, accumulate, gs);
     if (st != SL_OK) return st;
+    if (side && side->done) SL_CHECK_CUDA(cudaEventRecord(side->done, gs));
   }
   return SL_OK;
+}
+
+// The caller's stream waits for `main` after running `body` there with the
+// adapter-gradient passes on the caller's stream itself: U and the dX GEMM
+// run on the high-priority library stream, whose blocks the GPU dispatches
+// first, and dA / dB take the SMs the GEMM leaves idle.  Without that
+// stream everything runs in order on the caller's stream.
+template <typename Body>
+static sl_status run_bwd_split(cudaStream_t stream, bool lora, Body body) {
+  cudaStream_t hi = lora ? hi_stream() : nullptr;
+  cudaEvent_t e_in = hi ? fork_event(0) : nullptr, e_fork = hi ? fork_event(1) : nullptr,
+              e_out = hi ? fork_event(2) : nullptr;
+  if (!hi || !e_in || !e_fork || !e_out) return body(stream, nullptr);
+  SL_CHECK_CUDA(cudaEventRecord(e_in, stream));
+  SL_CHECK_CUDA(cudaStreamWaitEvent(hi, e_in, 0));
+  const GradSide side{stream, e_fork, nullptr};
+  const sl_status st = body(hi, &side);
+  // join even after a failure, so that the caller's stream stays ordered after all of it
+  const cudaError_t e1 = cudaEventRecord(e_out, hi);
+  const cudaError_t e2 = e1 == cudaSuccess ? cudaStreamWaitEvent(stream, e_out, 0) : e1;
+  if (st != SL_OK) return st;
+  if (e2 != cudaSuccess) return cuda_error(e2, "backward: joining the library stream");
+  return SL_OK;
+}
+
+sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A, const void* B,
+                     int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
+                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return run_bwd_split(stream, r > 0 && A && B, [&](cudaStream_t main, const GradSide* side) {
+    return linear_bwd_split(w, X, dY, M, A, B, r, alpha, T_save, dX, dA, dB, accumulate, ws, ws_bytes, main, side);
+  });
 }
 
 // ---------------------------------------------------------- projection groups
@@ -411,9 +448,10 @@ sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
   return launch_gemm(g, stream);
 }
 
-sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
-                    const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX, float* dA_cat,
-                    float* dB_cat, int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream) {
+sl_status group_bwd_split(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
+                          const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX,
+                          float* dA_cat, float* dB_cat, int accumulate, void* ws, size_t ws_bytes,
+                          cudaStream_t stream, const GradSide* side) {
   int bounds[5];
   sl_status st = check_group(w, G, N_g, M, r, bounds);
   if (st != SL_OK) return st;
@@ -432,6 +470,10 @@ sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
     st = skinny_down(static_cast<const uint16_t*>(dY_cat), M, NN, static_cast<const uint16_t*>(B_cat), 1, r, G, bounds,
                      U, stream);
     if (st != SL_OK) return st;
+    if (side) {  // dA and dB go to the side stream once U is written
+      SL_CHECK_CUDA(cudaEventRecord(side->fork, stream));
+      SL_CHECK_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
+    }
   }
   if (dX) {
     // dX = dY_cat W_cat + s U_cat A_cat: the plain dX GEMM at rank G r
@@ -456,11 +498,24 @@ sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
     if (st != SL_OK) return st;
   }
   if (!lora) return SL_OK;
+  cudaStream_t gs = side ? side->stream : stream;
   // dA_cat [G r, K] = s U_cat^T X;  dB_cat [sum N_g, r]: rows of projection g = s dY_g^T T_g
-  st = skinny_grad(U, static_cast<const uint16_t*>(X), M, K, r, G, nullptr, 0, s, dA_cat, 1, accumulate, stream);
+  st = skinny_grad(U, static_cast<const uint16_t*>(X), M, K, r, G, nullptr, 0, s, dA_cat, 1, accumulate, gs);
   if (st != SL_OK) return st;
-  return skinny_grad(static_cast<const float*>(T_cat), static_cast<const uint16_t*>(dY_cat), M, NN, r, G, bounds, 1, s,
-                     dB_cat, 0, accumulate, stream);
+  st = skinny_grad(static_cast<const float*>(T_cat), static_cast<const uint16_t*>(dY_cat), M, NN, r, G, bounds, 1, s,
+                   dB_cat, 0, accumulate, gs);
+  if (st != SL_OK) return st;
+  if (side && side->done) SL_CHECK_CUDA(cudaEventRecord(side->done, gs));
+  return SL_OK;
+}
+
+sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
+                    const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX, float* dA_cat,
+                    float* dB_cat, int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return run_bwd_split(stream, r > 0, [&](cudaStream_t main, const GradSide* side) {
+    return group_bwd_split(w, G, N_g, X, dY_cat, M, A_cat, B_cat, r, alpha, T_cat, dX, dA_cat, dB_cat, accumulate, ws,
+                           ws_bytes, main, side);
+  });
 }
 
 // ------------------------------------------------ allocation-free forward

@@ -50,6 +50,15 @@ struct sl_stack {
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ready[2] = {nullptr, nullptr};
   cudaEvent_t freed[2] = {nullptr, nullptr};
+  // The step runs on main_stream (highest priority); each projection unit's
+  // adapter-gradient passes (dA, dB) run on the caller's stream once its U
+  // is written (fork[u]) and mark done[u]; main_stream waits on done[u]
+  // only before it overwrites what those passes read.  step_in / step_out
+  // join the caller's stream at the start and end of a step.
+  cudaStream_t main_stream = nullptr;
+  cudaEvent_t step_in = nullptr, step_out = nullptr;
+  cudaEvent_t fork[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t done[4] = {nullptr, nullptr, nullptr, nullptr};
   int device = 0;
   uint64_t last_h2d = 0;
   uint64_t last_kernels = 0;
@@ -146,6 +155,10 @@ struct Plan {
   std::vector<size_t> Tqkv, To, Tgu, Td, lse;
   // shared
   size_t o, d, dhA, dhB, dd, dm, dgu, dx2a, dx2b, dh1, do_, da, dqkv, dx1q, dx1k, dx1v, lin_ws;
+  // U of each projection unit's backward (down, gate/up, o, q/k/v), kept
+  // until that unit's dA pass has read it: [M, G r] fp32 each
+  size_t U[4] = {0, 0, 0, 0};
+  size_t U_bytes[4] = {0, 0, 0, 0};
   size_t att_ws = 0, rope = 0;  // attention: Di [H, M] and the rotary table [S, 128]
   size_t lin_ws_bytes = 0;
 };
@@ -203,6 +216,11 @@ Plan make_plan(const sl_stack* s, int64_t M, int r) {
   if (rr) lw = std::max(lw, group_ws_bytes(M, 3, rr));
   P.lin_ws_bytes = lw;
   P.lin_ws = take(lw ? lw : 256);
+  const int unit_G[4] = {1, 2, 1, 3};  // down, gate/up, o, q/k/v
+  for (int u = 0; u < 4; ++u) {  // G regions of [M, r] (a group's [M, G r] fits in them)
+    P.U_bytes[u] = unit_G[u] * align_up(static_cast<size_t>(M) * (rr ? rr : 1) * 4, 256);
+    P.U[u] = take(P.U_bytes[u]);
+  }
   if (s->mixer == SL_MIX_ATTENTION) {
     P.att_ws = take(attention_ws_bytes(M, static_cast<int>(s->D / 128)));
     P.rope = take(static_cast<size_t>(s->seq_len) * 128 * 4);
@@ -222,7 +240,8 @@ struct StepCtx {
   const void* const* B;
   float* const* dA;
   float* const* dB;
-  cudaStream_t stream;
+  cudaStream_t stream;   // the step's main stream (the handle's high-priority stream)
+  cudaStream_t side;     // the caller's stream: adapter-gradient passes
   int accumulate = 0;
   bool group_qkv = false;  // q, k, v as one projection group
   bool group_gu = false;   // gate, up as one projection group
@@ -379,8 +398,6 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   auto B = [&](int p) { return r > 0 ? c.B[7 * l + p] : nullptr; };
   auto dA = [&](int p) { return r > 0 ? c.dA[7 * l + p] : nullptr; };
   auto dB = [&](int p) { return r > 0 ? c.dB[7 * l + p] : nullptr; };
-  void* lws = c.at<uint8_t>(P.lin_ws);
-  const size_t lwb = P.lin_ws_bytes;
   uint16_t* dm = c.at<uint16_t>(P.dm);
   uint16_t* dgu = c.at<uint16_t>(P.dgu);
   uint16_t* dx2a = c.at<uint16_t>(P.dx2a);
@@ -398,28 +415,54 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   const uint16_t* gu = c.at<uint16_t>(P.gu[l]);
   const float* Tqkv = c.at<float>(P.Tqkv[l]);
   const float* Tgu = c.at<float>(P.Tgu[l]);
-  SL_TRY(linear_bwd(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, c.at<float>(P.Td[l]), dm, dA(6),
-                    dB(6), c.accumulate, lws, lwb, c.stream));
+  // Unit u's dA / dB run on the side stream (the caller's); before this
+  // layer overwrites what the previous layer's passes of unit u read (its U
+  // region, its dY region), the main stream waits for them (done[u]).
+  enum { kDown = 0, kGU = 1, kO = 2, kQKV = 3 };
+  auto side = [&](int u) {
+    return GradSide{c.side, s->fork[u], s->done[u]};
+  };
+  auto wait_unit = [&](int u) -> sl_status {
+    SL_CHECK_CUDA(cudaStreamWaitEvent(c.stream, s->done[u], 0));
+    return SL_OK;
+  };
+  const size_t U1 = align_up(static_cast<size_t>(M) * rr * 4, 256);
+  auto U_of = [&](int u, int i) { return c.ws + P.U[u] + static_cast<size_t>(i) * U1; };
+  {
+    SL_TRY(wait_unit(kDown));
+    const GradSide sd = side(kDown);
+    SL_TRY(linear_bwd_split(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, c.at<float>(P.Td[l]), dm,
+                            dA(6), dB(6), c.accumulate, U_of(kDown, 0), P.U_bytes[kDown], c.stream, &sd));
+  }
   // gate, up
+  SL_TRY(wait_unit(kGU));
   if (c.group_gu) {
     SL_TRY(glue_swiglu_bwd(dm, gu, gu + F, dgu, dgu + F, M, F, 2 * F, c.stream));
     const sl_weight wg = group_weight(w, 4, 2);
     const int64_t Ng[2] = {F, F};
-    SL_TRY(group_bwd(&wg, 2, Ng, x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate, lws, lwb,
-                     c.stream));
+    const GradSide sd = side(kGU);
+    SL_TRY(group_bwd_split(&wg, 2, Ng, x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate,
+                           U_of(kGU, 0), P.U_bytes[kGU], c.stream, &sd));
+    SL_TRY(wait_unit(kO));
     SL_TRY(glue_rms_bwd(dh2, dx2a, nullptr, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]),
                         norms[1], dh1, do_, M, D, c.stream));
   } else {
     SL_TRY(glue_swiglu_bwd(dm, gu, gu + M * F, dgu, dgu + M * F, M, F, F, c.stream));
-    SL_TRY(linear_bwd(&w[4], x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate, lws, lwb,
-                      c.stream));
-    SL_TRY(linear_bwd(&w[5], x2, dgu + M * F, M, A(5), B(5), r, c.alpha, Tgu + M * rr, dx2b, dA(5), dB(5),
-                      c.accumulate, lws, lwb, c.stream));
+    const GradSide s0{c.side, s->fork[kGU], nullptr};
+    const GradSide s1 = side(kGU);
+    SL_TRY(linear_bwd_split(&w[4], x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate,
+                            U_of(kGU, 0), U1, c.stream, &s0));
+    SL_TRY(linear_bwd_split(&w[5], x2, dgu + M * F, M, A(5), B(5), r, c.alpha, Tgu + M * rr, dx2b, dA(5), dB(5),
+                            c.accumulate, U_of(kGU, 1), U1, c.stream, &s1));
+    SL_TRY(wait_unit(kO));
     SL_TRY(glue_rms_bwd(dh2, dx2a, dx2b, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]),
                         norms[1], dh1, do_, M, D, c.stream));
   }
-  SL_TRY(linear_bwd(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, c.at<float>(P.To[l]), da, dA(3),
-                    dB(3), c.accumulate, lws, lwb, c.stream));
+  {
+    const GradSide sd = side(kO);
+    SL_TRY(linear_bwd_split(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, c.at<float>(P.To[l]), da,
+                            dA(3), dB(3), c.accumulate, U_of(kO, 0), P.U_bytes[kO], c.stream, &sd));
+  }
   // q, k, v: the mixing step's backward into the dq/dk/dv region
   auto mix_bwd = [&](const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t ldq, int64_t ldkv,
                      uint16_t* dq, uint16_t* dk, uint16_t* dv) -> sl_status {
@@ -428,13 +471,16 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
     return attention_bwd(sh, q, ldq, k, ldkv, v, ldkv, c.at<uint16_t>(P.a[l]), D, da, D, c.at<float>(P.lse[l]), dq,
                          ldq, dk, ldkv, dv, ldkv, c.at<float>(P.rope), c.at<uint8_t>(P.att_ws), c.stream);
   };
+  SL_TRY(wait_unit(kQKV));
   if (c.group_qkv) {
     const int64_t ld = D + 2 * Dkv;
     SL_TRY(mix_bwd(qkv, qkv + D, qkv + D + Dkv, ld, ld, dqkv, dqkv + D, dqkv + D + Dkv));
     const sl_weight wg = group_weight(w, 0, 3);
     const int64_t Ng[3] = {D, Dkv, Dkv};
-    SL_TRY(group_bwd(&wg, 3, Ng, x1, dqkv, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate, lws, lwb,
-                     c.stream));
+    const GradSide sd = side(kQKV);
+    SL_TRY(group_bwd_split(&wg, 3, Ng, x1, dqkv, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate,
+                           U_of(kQKV, 0), P.U_bytes[kQKV], c.stream, &sd));
+    SL_TRY(wait_unit(kDown));  // dd (this layer's down dY) is overwritten next
     SL_TRY(glue_rms_bwd(dh1, dx1q, nullptr, nullptr, nullptr, h_in, c.at<float>(P.rstd1[l]), norms[0], dh, dh_bf16, M,
                         D, c.stream));
   } else {
@@ -442,12 +488,15 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
     uint16_t* dk = dqkv + M * D;
     uint16_t* dv = dk + M * Dkv;
     SL_TRY(mix_bwd(qkv, qkv + M * D, qkv + M * D + M * Dkv, D, Dkv, dq, dk, dv));
-    SL_TRY(linear_bwd(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate, lws, lwb,
-                      c.stream));
-    SL_TRY(linear_bwd(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, Tqkv + M * rr, dx1k, dA(1), dB(1), c.accumulate, lws,
-                      lwb, c.stream));
-    SL_TRY(linear_bwd(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, Tqkv + 2 * M * rr, dx1v, dA(2), dB(2), c.accumulate,
-                      lws, lwb, c.stream));
+    const GradSide s0{c.side, s->fork[kQKV], nullptr};
+    const GradSide s2 = side(kQKV);
+    SL_TRY(linear_bwd_split(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate,
+                            U_of(kQKV, 0), U1, c.stream, &s0));
+    SL_TRY(linear_bwd_split(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, Tqkv + M * rr, dx1k, dA(1), dB(1),
+                            c.accumulate, U_of(kQKV, 1), U1, c.stream, &s0));
+    SL_TRY(linear_bwd_split(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, Tqkv + 2 * M * rr, dx1v, dA(2), dB(2),
+                            c.accumulate, U_of(kQKV, 2), U1, c.stream, &s2));
+    SL_TRY(wait_unit(kDown));  // dd (this layer's down dY) is overwritten next
     SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, nullptr, h_in, c.at<float>(P.rstd1[l]), norms[0], dh, dh_bf16, M, D,
                         c.stream));
   }
@@ -596,6 +645,16 @@ extern "C" sl_status sl_stack_create(const sl_stack_desc* desc, sl_stack** out, 
   }
   if ((e = cudaStreamCreateWithFlags(&s->copy_stream, cudaStreamNonBlocking)) != cudaSuccess)
     return fail(e, "sl_stack_create: copy stream");
+  int least = 0, greatest = 0;
+  if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess)
+    return fail(e, "sl_stack_create: stream priorities");
+  if ((e = cudaStreamCreateWithPriority(&s->main_stream, cudaStreamNonBlocking, greatest)) != cudaSuccess)
+    return fail(e, "sl_stack_create: main stream");
+  cudaEvent_t* evs[10] = {&s->step_in, &s->step_out, &s->fork[0], &s->fork[1], &s->fork[2], &s->fork[3],
+                          &s->done[0], &s->done[1], &s->done[2], &s->done[3]};
+  for (cudaEvent_t* ev : evs)
+    if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
+      return fail(e, "sl_stack_create: event");
   if (host_bytes) *host_bytes = bytes * static_cast<size_t>(desc->L);
   if (buffer_bytes) *buffer_bytes = 2 * bytes;
   *out = s;
@@ -612,6 +671,14 @@ extern "C" sl_status sl_stack_destroy(sl_stack* s) {
     if (s->freed[b]) cudaEventDestroy(s->freed[b]);
   }
   if (s->copy_stream) cudaStreamDestroy(s->copy_stream);
+  if (s->main_stream) {
+    cudaStreamSynchronize(s->main_stream);
+    cudaStreamDestroy(s->main_stream);
+  }
+  cudaEvent_t evs[10] = {s->step_in, s->step_out, s->fork[0], s->fork[1], s->fork[2], s->fork[3],
+                         s->done[0], s->done[1], s->done[2], s->done[3]};
+  for (cudaEvent_t ev : evs)
+    if (ev) cudaEventDestroy(ev);
   delete s;
   return SL_OK;
 }
@@ -732,6 +799,41 @@ SftPlan make_sft_plan(const Plan& P, int64_t M, int64_t D, int64_t V, int64_t ch
   return S;
 }
 
+// The step's main stream starts after the caller's stream has reached the
+// call, and the caller's stream continues after the main stream's last
+// kernel (its own queue already holds every adapter-gradient pass).
+sl_status join_in(sl_stack* s, cudaStream_t caller) {
+  SL_CHECK_CUDA(cudaEventRecord(s->step_in, caller));
+  SL_CHECK_CUDA(cudaStreamWaitEvent(s->main_stream, s->step_in, 0));
+  return SL_OK;
+}
+sl_status join_out(sl_stack* s, cudaStream_t caller) {
+  SL_CHECK_CUDA(cudaEventRecord(s->step_out, s->main_stream));
+  SL_CHECK_CUDA(cudaStreamWaitEvent(caller, s->step_out, 0));
+  return SL_OK;
+}
+
+sl_status sft_body(StepCtx& c, Runner& run, const SftPlan& S, const int32_t* tokens, const int32_t* labels,
+                          int64_t M, const void* embed, int64_t V, const float* norm_final, const void* W_head,
+                          int64_t chunk_V, float* loss, int* err) {
+  const sl_stack* s = c.s;
+  const int D = static_cast<int>(s->D);
+  cudaStream_t stream = c.stream;
+  float* h0 = c.at<float>(S.h0);
+  float* hL = c.at<float>(S.hL);
+  uint16_t* xf = c.at<uint16_t>(S.xf);
+  float* rstd = c.at<float>(S.rstd);
+  float* dX = c.at<float>(S.dX);
+  float* dh_top = c.at<float>(S.dh_top);
+  SL_TRY(glue_embed(tokens, static_cast<const uint16_t*>(embed), V, h0, M, D, err, stream));
+  SL_TRY(run.forward(h0, hL));
+  SL_TRY(glue_rms_fwd(hL, nullptr, nullptr, xf, rstd, norm_final, M, D, stream));
+  SL_TRY(sl_ce_fwd_bwd(xf, M, D, W_head, V, labels, -100, chunk_V, loss, dX, c.at<uint8_t>(S.ce_ws), S.ce_bytes,
+                       stream));
+  SL_TRY(glue_rms_bwd(nullptr, nullptr, nullptr, nullptr, dX, hL, rstd, norm_final, dh_top, nullptr, M, D, stream));
+  return run.backward(h0, dh_top, c.at<float>(S.dh0));
+}
+
 }  // namespace
 
 extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64_t M,
@@ -745,14 +847,17 @@ extern "C" sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float
   const Plan P = make_plan(s, M, r);
   SL_REQUIRE(ws_bytes >= P.total, "sl_stream_stack_step: workspace too small (need " + std::to_string(P.total) +
                                       " bytes)");
-  StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, stream};
+  StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, s->main_stream, stream};
   c.accumulate = accumulate ? 1 : 0;
   c.group_qkv = can_group(s, M, r, 0, 3, A, B, dA, dB);
   c.group_gu = can_group(s, M, r, 4, 2, A, B, dA, dB);
   const uint64_t launches0 = launch_count();
   Runner run{s, c, P, mode == SL_MODE_STREAMED};
-  SL_TRY(run.forward(h0, hL));
-  SL_TRY(run.backward(h0, dh_top, dh0));
+  SL_TRY(join_in(s, stream));
+  const sl_status st1 = run.forward(h0, hL);
+  const sl_status st2 = st1 == SL_OK ? run.backward(h0, dh_top, dh0) : st1;
+  SL_TRY(join_out(s, stream));
+  SL_TRY(st2);
   s->last_h2d = run.h2d;
   s->last_kernels = launch_count() - launches0;
   return SL_OK;
@@ -776,26 +881,16 @@ extern "C" sl_status sl_sft_step(sl_stack* s, int32_t mode, const int32_t* token
   SL_REQUIRE(ws_bytes >= S.total, "sl_sft_step: workspace too small (need " + std::to_string(S.total) + " bytes)");
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
-  StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, stream};
+  StepCtx c{s, &P, static_cast<uint8_t*>(ws), M, r, alpha, A, B, dA, dB, s->main_stream, stream};
   c.accumulate = accumulate ? 1 : 0;
   c.group_qkv = can_group(s, M, r, 0, 3, A, B, dA, dB);
   c.group_gu = can_group(s, M, r, 4, 2, A, B, dA, dB);
   const uint64_t launches0 = launch_count();
   Runner run{s, c, P, mode == SL_MODE_STREAMED};
-  const int D = static_cast<int>(s->D);
-  float* h0 = c.at<float>(S.h0);
-  float* hL = c.at<float>(S.hL);
-  uint16_t* xf = c.at<uint16_t>(S.xf);
-  float* rstd = c.at<float>(S.rstd);
-  float* dX = c.at<float>(S.dX);
-  float* dh_top = c.at<float>(S.dh_top);
-  SL_TRY(glue_embed(tokens, static_cast<const uint16_t*>(embed), V, h0, M, D, err, stream));
-  SL_TRY(run.forward(h0, hL));
-  SL_TRY(glue_rms_fwd(hL, nullptr, nullptr, xf, rstd, norm_final, M, D, stream));
-  SL_TRY(sl_ce_fwd_bwd(xf, M, D, W_head, V, labels, -100, chunk_V, loss, dX, c.at<uint8_t>(S.ce_ws), S.ce_bytes,
-                       stream));
-  SL_TRY(glue_rms_bwd(nullptr, nullptr, nullptr, nullptr, dX, hL, rstd, norm_final, dh_top, nullptr, M, D, stream));
-  SL_TRY(run.backward(h0, dh_top, c.at<float>(S.dh0)));
+  SL_TRY(join_in(s, stream));
+  const sl_status st1 = sft_body(c, run, S, tokens, labels, M, embed, V, norm_final, W_head, chunk_V, loss, err);
+  SL_TRY(join_out(s, stream));
+  SL_TRY(st1);
   s->last_h2d = run.h2d;
   s->last_kernels = launch_count() - launches0;
   return SL_OK;
