@@ -24,9 +24,11 @@
  * Conventions for every call:
  *  - Device pointers unless stated; the CALLER owns every tensor passed in.
  *    libsl owns only what sl_stack_create allocates (two device layer buffers,
- *    a copy stream, events) and two file-scope device arrays that every
- *    device loading the library holds until exit: the error word (two ints)
- *    and the 4 MiB scratch of sl_lora_linear_fwd_noalloc.
+ *    a copy stream, a high-priority main stream, events), one high-priority
+ *    stream per device (created on the first LoRA backward there) with a few
+ *    events per thread, and two file-scope device arrays that every device
+ *    loading the library holds until exit: the error word (two ints) and the
+ *    4 MiB scratch of sl_lora_linear_fwd_noalloc.
  *  - Work is enqueued on the caller's stream and the call returns without
  *    waiting, except where a call says it synchronises.
  *  - bf16 tensors are passed as void* (IEEE bfloat16 bit patterns, row-major,
@@ -188,9 +190,12 @@ sl_status sl_weight_dequantize(const sl_weight* w, int32_t out_dtype, void* out,
  * the backward; the side product s T B^T is folded into the same
  * accumulator with fp32 accuracy); may be NULL only when r == 0; 16-byte
  * aligned (it is read by TMA).  r == 0 (or A == B == NULL) computes the base
- * alone -- the adapters-off pass.  r <= 32, r % 8 == 0.  The forward needs
- * no scratch: `ws` may be NULL (the argument stays so that one buffer of
- * sl_lora_linear_workspace_size bytes serves both directions). */
+ * alone -- the adapters-off pass.  r <= 32, r % 8 == 0.  `ws` may be NULL;
+ * given a buffer of sl_lora_linear_workspace_size bytes (256-byte aligned),
+ * the forward uses the part after U to split the GEMM's last partial wave
+ * of tiles along K (pieces' fp32 partial sums added in a fixed order: the
+ * result is bitwise reproducible, and equal to the unsplit one up to fp32
+ * summation order). */
 sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M,
                              const void* A, const void* B, int32_t r, float alpha,
                              void* Y, void* T_save, void* ws, size_t ws_bytes,
@@ -202,8 +207,11 @@ sl_status sl_lora_linear_fwd(const sl_weight* w, const void* X, int64_t M,
  * dX [M, K] bf16 (may be NULL to skip); dA [r, K] and dB [N, r] fp32,
  * overwritten when accumulate == 0, added to otherwise.  Every reduction
  * runs in a fixed order: results are bitwise reproducible.  `ws` must hold
- * sl_lora_linear_workspace_size(M, N, K, r) bytes (256-byte aligned): it
- * carries U between the rank-r passes. */
+ * U [M, r] fp32 (256-byte aligned): it carries U between the rank-r passes;
+ * with sl_lora_linear_workspace_size(M, N, K, r) bytes the rest serves the
+ * dX GEMM's split-K scratch as in the forward.  U and the dX GEMM run on a
+ * high-priority library stream and dA, dB on `stream` beside them; the call
+ * leaves `stream` ordered after all of it. */
 sl_status sl_lora_linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M,
                              const void* A, const void* B, int32_t r, float alpha,
                              const void* T_save, void* dX, float* dA, float* dB,
@@ -231,8 +239,10 @@ sl_status sl_lora_linear_fwd_noalloc(const sl_weight* w, const void* X, int64_t 
                                      const void* A, const void* B, int32_t r, float alpha,
                                      void* Y, void* T_save, cudaStream_t stream);
 
-/* Scratch bytes of one linear call: the backward's U [M, r] fp32, rounded up
- * to 256 (the forward needs none); 0 when r == 0. */
+/* Workspace bytes of one linear call: the backward's U [M, r] fp32, rounded
+ * up to 256, then, when M > 128, the CTA-pair GEMM's split-K scratch (a
+ * fixed ~19 MB on a 148-SM B300: a flag and a 256 KB fp32 partial tile per
+ * SM pair); 0 when r == 0. */
 size_t sl_lora_linear_workspace_size(int64_t M, int64_t N, int64_t K, int32_t r);
 
 /* ------------------------------------------------------ projection groups */
@@ -260,9 +270,11 @@ sl_status sl_lora_group_fwd(const sl_weight* w_cat, int32_t G, const int64_t* N_
  * (one fused GEMM), dA_cat [G r, K] (rows of adapter g = s U_g^T X) and
  * dB_cat [sum N_g, r] (rows of projection g = s dY_g^T T_g), fp32,
  * overwritten when accumulate == 0, added to otherwise.  dX [M, K] bf16 may
- * be NULL.  `ws` must hold sl_lora_group_workspace_size(M, G, r) bytes
- * (256-byte aligned): U_cat [M, G r] fp32.  r == 0: dX of the bases only.
- * Reductions run in a fixed order: results are bitwise reproducible. */
+ * be NULL.  `ws` must hold U_cat [M, G r] fp32 (256-byte aligned); with
+ * sl_lora_group_workspace_size(M, G, r) bytes the rest serves the dX GEMM's
+ * split-K scratch (as in sl_lora_linear_fwd).  r == 0: dX of the bases
+ * only.  Reductions run in a fixed order: results are bitwise
+ * reproducible.  Streams as in sl_lora_linear_bwd. */
 sl_status sl_lora_group_bwd(const sl_weight* w_cat, int32_t G, const int64_t* N_g,
                             const void* X, const void* dY_cat, int64_t M,
                             const void* A_cat, const void* B_cat, int32_t r, float alpha,
@@ -322,8 +334,8 @@ typedef struct sl_stack sl_stack;
 
 /* Creates a stack handle: checks that every host blob is page-locked
  * (cudaPointerGetAttributes; pageable memory -> SL_ERR_INVALID), allocates
- * the two device layer buffers, a copy stream and the buffer events on the
- * current device.  The pre-flight report ("Soup: Fine-Tuning ...", "Layer
+ * the two device layer buffers, a copy stream, a main stream at the highest
+ * priority and the events on the current device.  The pre-flight report ("Soup: Fine-Tuning ...", "Layer
  * Streaming: The Mechanism ...") comes back in *host_bytes (L * blob bytes)
  * and *buffer_bytes (the two buffers together).  The descriptor's pointer
  * arrays are copied; the blobs themselves stay owned by the caller and must
@@ -358,8 +370,11 @@ size_t sl_stack_workspace_size(const sl_stack* s, int64_t M, int32_t r);
  * after the last kernel that read the buffer and each layer's kernels after
  * its copy.  The backward reuses the two layers already resident at the
  * turn.  SL_MODE_RESIDENT: the same kernels, in the same order, read the
- * descriptor's device_blobs; results are bitwise identical.  `ws` must hold
- * sl_stack_workspace_size(s, M, r) bytes, 256-byte aligned. */
+ * descriptor's device_blobs; results are bitwise identical.  The step runs
+ * on the handle's main stream once `stream` reaches the call; every
+ * projection's dA and dB passes run on `stream` beside the next kernels,
+ * and `stream` is ordered after the whole step when the call returns.
+ * `ws` must hold sl_stack_workspace_size(s, M, r) bytes, 256-byte aligned. */
 sl_status sl_stream_stack_step(sl_stack* s, int32_t mode, const float* h0, int64_t M,
                                const float* dh_top, const void* const* A,
                                const void* const* B, int32_t r, float alpha,

@@ -2,6 +2,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -147,9 +148,44 @@ static int pair_clusters_resident() {
 
 // Persistent NF4 GEMM on CTA pairs: one cluster per SM pair walks its share
 // of the pair tiles.
+// Most pieces a split tail tile is cut into: the owning piece reads every
+// other piece's 128 KB partial per CTA, so pieces pay only while a piece's
+// k-loop outlasts those reads (about KB / 4 pieces squared).
+static int split_pieces(int KB) {
+  int p = 1;
+  while ((p + 1) * (p + 1) * 4 <= KB) ++p;
+  return p;
+}
+
+static int max_split_slots() { return num_sms() / 2; }
+static size_t split_flag_bytes() { return align_up(static_cast<size_t>(max_split_slots()) * 2 * 8, 256); }
+size_t split_scratch_bytes() {
+  return split_flag_bytes() + static_cast<size_t>(max_split_slots()) * 2 * kBN * 128 * 4;
+}
+
+// Splits the last partial wave along K when the tail tiles are few enough
+// for two or more pieces each and scratch is given.
+static void set_split(GemmArgs& a, int ntiles, int nclusters, void* ws, size_t bytes) {
+  static std::atomic<unsigned long long> tag{0x5EEDull << 48};
+  a.split_P = 0;
+  const int R = ntiles % nclusters;
+  if (!ws || bytes < split_scratch_bytes() || R == 0 || ntiles < nclusters) return;
+  const int KB = static_cast<int>(ceil_div(a.K, kBK));
+  const int P = std::min(nclusters / R, split_pieces(KB));
+  if (P < 2 || R * (P - 1) > max_split_slots()) return;
+  a.split_P = P;
+  a.split_R = R;
+  a.split_rounds = ntiles / nclusters;
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  a.split_flag = reinterpret_cast<unsigned long long*>(p);
+  a.split_part = reinterpret_cast<float*>(p + split_flag_bytes());
+  a.split_tag = tag.fetch_add(1) + 1;
+}
+
 template <int BMN, int SMALL>
 static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, const CUtensorMap& ms,
-                                const CUtensorMap& ms2, const GemmArgs& a, cudaStream_t stream) {
+                                const CUtensorMap& ms2, const GemmArgs& a, void* split_ws, size_t split_bytes,
+                                cudaStream_t stream) {
   auto kern = gemm_nf4_pair_persistent_kernel<BMN, SMALL>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -160,9 +196,10 @@ static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, co
   }
   const int ntiles = ceil_div(a.M, 256) * ceil_div(a.N, kBN);
   const int nclusters = std::min(ntiles, pair_clusters_resident<BMN, SMALL>());
+  GemmArgs ao = a;
+  set_split(ao, ntiles, nclusters, split_ws, split_bytes);
   // bf16 output by TMA boxes of 64 columns x 32 rows when a tensor map can
   // describe it (16-byte aligned base and row stride); else direct stores
-  GemmArgs ao = a;
   CUtensorMap mo = ma;
   ao.tma_out = (reinterpret_cast<uintptr_t>(a.out) % 16 == 0) && (a.ld_out * 2) % 16 == 0 &&
                make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, a.N, a.M, static_cast<uint64_t>(a.ld_out) * 2, 64,
@@ -288,9 +325,11 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
                                                     (g.bmn ? pair_clusters_resident<1, 1>() : pair_clusters_resident<0, 1>()));
   // folded rank <= 32: the five-stage variant; above (a group's dX): four stages
   if (persistent && a.r <= 32)
-    st = g.bmn ? run_persistent<1, 1>(ma, mb, ms, ms2, a, stream) : run_persistent<0, 1>(ma, mb, ms, ms2, a, stream);
+    st = g.bmn ? run_persistent<1, 1>(ma, mb, ms, ms2, a, g.split_ws, g.split_ws_bytes, stream)
+               : run_persistent<0, 1>(ma, mb, ms, ms2, a, g.split_ws, g.split_ws_bytes, stream);
   else if (persistent)
-    st = g.bmn ? run_persistent<1, 0>(ma, mb, ms, ms2, a, stream) : run_persistent<0, 0>(ma, mb, ms, ms2, a, stream);
+    st = g.bmn ? run_persistent<1, 0>(ma, mb, ms, ms2, a, g.split_ws, g.split_ws_bytes, stream)
+               : run_persistent<0, 0>(ma, mb, ms, ms2, a, g.split_ws, g.split_ws_bytes, stream);
   else
     st = pair ? (g.bmn ? run_pair<1>(ma, mb, ms, a, stream) : run_pair<0>(ma, mb, ms, a, stream))
               : dispatch(g, ma, mb, ms, stream);

@@ -95,6 +95,17 @@ struct GemmArgs {
   int accumulate;              // kEpiAddF32: add into out (1) or overwrite (0)
   int tma_out;                 // gemm_tc_kernel: the output moves by TMA through map_o (else direct stores)
   int* err;                    // device error word
+  // persistent pair GEMM, last partial wave split along K: every cluster
+  // takes split_rounds full tiles, then the split_R tail tiles go in
+  // split_P pieces of contiguous k-blocks to clusters 0 .. split_R*split_P-1;
+  // piece p > 0 leaves its fp32 accumulator in split_part (slot
+  // j*(split_P-1)+p-1 of tail tile j: [2 CTAs][256 columns][128 rows]) and
+  // raises split_flag[slot * 2 + CTA] to split_tag; piece 0 adds them in
+  // piece order.  split_P < 2: no split.
+  int split_P, split_R, split_rounds;
+  float* split_part;
+  unsigned long long* split_flag;
+  unsigned long long split_tag;
 };
 
 // One row segment of 64 NF4 elements (32 packed code bytes, one absmax) ->
@@ -689,8 +700,16 @@ struct GemmLaunch {
   int64_t q_ld;
   const float* absmax2;
   int64_t a2_ld;
+  // scratch for splitting the persistent kernel's last partial wave along K
+  // (split_scratch_bytes(); 256-byte aligned); nullptr: no split
+  void* split_ws;
+  size_t split_ws_bytes;
 };
 
 sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream);
+// Scratch that lets a persistent pair GEMM split its last partial wave
+// along K: a flag and a [2][256][128] fp32 partial tile per piece, for up to
+// one piece per resident cluster.
+size_t split_scratch_bytes();
 
 }  // namespace sl

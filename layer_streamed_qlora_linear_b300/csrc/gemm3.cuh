@@ -111,6 +111,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
   // pair tile t -> (m pair, n tile); concurrent clusters share the n tile (weight reuse in L2)
   auto tile_m0 = [&](int t) { return (t % mpairs) * 256 + static_cast<int>(rank) * 128; };
   auto tile_n0 = [&](int t) { return (t / mpairs) * kBN; };
+  // This cluster's work items, the same list for every role: its full tiles
+  // (cluster, cluster + nclusters, ...) and, when the last partial wave is
+  // split along K, one piece of a tail tile (piece 0 folds the side product
+  // and adds the other pieces' partial sums in piece order).
+  const int split_P = args.split_P;
+  const bool split = split_P >= 2;
+  const int rounds = split ? args.split_rounds : (ntiles - cluster + nclusters - 1) / nclusters;
+  const int n_items = rounds + ((split && cluster < args.split_R * split_P) ? 1 : 0);
+  struct Item {
+    int t, kb0, kb1, piece, slot0;  // piece -1: a full tile
+  };
+  auto item = [&](int i) {
+    Item x;
+    if (i < rounds) {
+      x.t = cluster + i * nclusters;
+      x.kb0 = 0;
+      x.kb1 = KB;
+      x.piece = -1;
+      x.slot0 = 0;
+    } else {
+      const int j = cluster / split_P, p = cluster % split_P;
+      x.t = rounds * nclusters + j;
+      x.kb0 = p * KB / split_P;
+      x.kb1 = (p + 1) * KB / split_P;
+      x.piece = p;
+      x.slot0 = j * (split_P - 1);
+    }
+    return x;
+  };
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
@@ -160,9 +189,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           kHalfCodesBytes + (args.dq ? (128 + (BMN ? 32 : 16)) : (BMN ? kBK * 16 : 128 * 16));
       int g = 0;  // k-blocks issued by this cluster
       bool ok = true;
-      for (int t = cluster; ok && t < ntiles; t += nclusters) {
+      for (int i = 0; ok && i < n_items; ++i) {
+        const Item x = item(i);
+        const int t = x.t;
         const int m0 = tile_m0(t), n0 = tile_n0(t), nh = n0 + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
+        for (int kb = x.kb0; kb < x.kb1; ++kb, ++g) {
           const int s = g % S;
           if (!ptx::mbar_wait_cluster(&empty[s], ((g / S) & 1) ^ 1, abort_flag)) {
             give_up();
@@ -219,9 +250,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       const uint32_t b_lo0 = static_cast<uint32_t>(b_desc0), b_hi = static_cast<uint32_t>(b_desc0 >> 32);
       constexpr uint32_t kBStep = BMN ? 2048 : 32;  // bytes between k16 steps of the B half
       const int ksteps = has_lora ? (2 * args.r + 15) / 16 : 0;
-      int g = 0, it = 0;
+      int g = 0, it = 0, lit = 0;  // k-blocks, items and folded items of this cluster
       bool ok = true;
-      for (int t = cluster; ok && t < ntiles; t += nclusters, ++it) {
+      for (; ok && it < n_items; ++it) {
+        const Item x = item(it);
+        const bool fold = has_lora && x.piece <= 0;
         const int acc = it & 1;
         const uint32_t d = tmem + static_cast<uint32_t>(acc * kBN);
         if (!ptx::mbar_wait_cluster(&acc_empty[acc], ((it >> 1) & 1) ^ 1, abort_flag)) {
@@ -232,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
         ptx::tc_fence_after();
         int s = g % S;                       // stage and phase, stepped without division
         uint32_t ph = (g / S) & 1;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
+        for (int kb = x.kb0; kb < x.kb1; ++kb, ++g) {
           if (!ptx::mbar_wait_cluster(&full[s], ph, abort_flag)) {
             give_up();
             ok = false;
@@ -241,10 +274,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           ptx::tc_fence_after();
           const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(s) * (kATileBytes >> 4);
           const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(s) * (kHalfBTileBytes >> 4);
+          const uint32_t first = kb == x.kb0 ? 0u : 1u;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             ptx::mma_bf16_pair_lohi(d, a_lo + kk * (32 >> 4), a_hi, b_lo + kk * (kBStep >> 4), b_hi, idesc,
-                                    (kb | kk) ? 1u : 0u);
+                                    (first | kk) ? 1u : 0u);
           ptx::mma_commit_pair(&empty[s], 0x3);
           if (++s == S) {
             s = 0;
@@ -252,8 +286,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           }
         }
         if (!ok) break;
-        if (has_lora) {  // fold the LoRA side product into this accumulator
-          if (!ptx::mbar_wait_cluster(lora_full, it & 1, abort_flag)) {
+        if (fold) {  // fold the LoRA side product into this accumulator
+          if (!ptx::mbar_wait_cluster(lora_full, lit & 1, abort_flag)) {
             give_up();
             ok = false;
             break;
@@ -266,6 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
             ptx::mma_bf16_pair(d, ad, bd, idesc, 1u);
           }
           ptx::mma_commit_pair(lora_empty, 0x3);
+          ++lit;
         }
         ptx::mma_commit_pair(&acc_full[acc], 0x3);
       }
@@ -280,8 +315,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       const uint32_t leader_sink = ptx::map_to_rank(sink, 0);
       int g = 0;
       bool ok = true;
-      for (int t = cluster; ok && t < ntiles; t += nclusters) {
-        for (int kb = 0; kb < KB; ++kb, ++g) {
+      for (int i = 0; ok && i < n_items; ++i) {
+        const Item x = item(i);
+        for (int kb = x.kb0; kb < x.kb1; ++kb, ++g) {
           const int s = g % S;
           if (!ptx::mbar_wait(&b_local[s], (g / S) & 1, abort_flag)) {
             give_up();
@@ -299,9 +335,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     const int tr = dq & 127;
     int g = 0;
     bool ok = true;
-    for (int t = cluster; ok && t < ntiles; t += nclusters) {
+    for (int i = 0; ok && i < n_items; ++i) {
+      const Item x = item(i);
+      const int t = x.t;
       // two groups of four warps take alternate k-blocks (cluster counter g)
-      for (int kb = 0; kb < KB; ++kb, ++g) {
+      for (int kb = x.kb0; kb < x.kb1; ++kb, ++g) {
         if ((g & 1) != grp) continue;
         const int s = g % S;
         if (!ptx::mbar_wait_cluster(&raw_full[s], (g / S) & 1, abort_flag)) {
@@ -438,12 +476,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       epi_bar_sync();
       return go;
     };
-    int it = 0;
-    for (int t = cluster; t < ntiles; t += nclusters, ++it) {
+    // Split tail tiles: this CTA's slot of a piece's partial sums, column-major
+    // over its 128 rows ([256 columns][128 rows] fp32), and its flag.
+    auto part_of = [&](int slot) {
+      return args.split_part + (static_cast<size_t>(slot) * 2 + rank) * (static_cast<size_t>(kBN) * 128);
+    };
+    auto flag_of = [&](int slot) { return args.split_flag + static_cast<size_t>(slot) * 2 + rank; };
+    int it = 0, lit = 0;  // items and folded items of this cluster
+    for (; it < n_items; ++it) {
+      const Item x = item(it);
+      const int t = x.t;
       const int acc = it & 1;
-      if (has_lora) {
+      if (has_lora && x.piece <= 0) {
         // the region is free once the previous tile's fold MMAs completed
-        bool free_ = ptx::mbar_wait_cluster_backoff(lora_empty, (it & 1) ^ 1, abort_flag) && !*abort_flag;
+        bool free_ = ptx::mbar_wait_cluster_backoff(lora_empty, (lit & 1) ^ 1, abort_flag) && !*abort_flag;
         free_ = __all_sync(0xffffffffu, free_);
         if (!free_ && !*abort_flag) give_up();
         if (!agree(free_)) break;
@@ -451,6 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(lora_full_leader);
+        ++lit;
       }
       bool ready = ptx::mbar_wait_cluster_backoff(&acc_full[acc], (it >> 1) & 1, abort_flag) && !*abort_flag;
       ready = __all_sync(0xffffffffu, ready);
@@ -460,54 +507,97 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
       const int gm = tile_m0(t) + row;
       const int n0 = tile_n0(t);
       const uint32_t t_row = tmem + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(q * 32) << 16);
-      if (args.tma_out) {
-        // The LoRA region is free from the fold's completion (acc_full) until
-        // the next stage_lora, which follows the epilogue warps' barrier:
-        // this warp stages its 32 rows there as 64-column bf16 boxes (two
-        // 4 KB buffers in turn) and stores them by TMA.
-        uint8_t* stg = sLA + (warp - 10) * 8192;
-        const uint32_t stg_a = ptx::smem_addr(stg);
-#pragma unroll 1
-        for (int p = 0; p < kBN / 64; ++p) {
-          const int b = p & 1;
-          if (p >= 2) {  // buffer b's previous box has been read out
-            if (lane == 0) ptx::bulk_wait_read1();
-            __syncwarp();
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t u[32];
-            ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(p * 64 + h * 32), u);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4)
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                               stg_a + b * 4096 + lane * 128 + (((h * 4 + g4) ^ (lane & 7)) << 4)),
-                           "r"(pack_bf16x2(__uint_as_float(u[8 * g4 + 0]), __uint_as_float(u[8 * g4 + 1]))),
-                           "r"(pack_bf16x2(__uint_as_float(u[8 * g4 + 2]), __uint_as_float(u[8 * g4 + 3]))),
-                           "r"(pack_bf16x2(__uint_as_float(u[8 * g4 + 4]), __uint_as_float(u[8 * g4 + 5]))),
-                           "r"(pack_bf16x2(__uint_as_float(u[8 * g4 + 6]), __uint_as_float(u[8 * g4 + 7])))
-                           : "memory");
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(&map_o, stg + b * 4096, n0 + p * 64, tile_m0(t) + q * 32);
-            ptx::bulk_commit();
-          }
-        }
-        if (lane == 0) ptx::bulk_wait_read0();  // the region is free again before any warp passes the next barrier
-        __syncwarp();
-      } else {
+      if (x.piece > 0) {
+        // a later piece of a split tile: its partial sums go to its slot, then the flag
+        float* part = part_of(x.slot0 + x.piece - 1);
 #pragma unroll 1
         for (int c0 = 0; c0 < kBN; c0 += 32) {
           uint32_t u[32];
           ptx::tmem_ld_32x32b_x32(t_row + c0, u);
           ptx::tmem_wait_ld();
-          float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
-          store32(gm, n0, c0, v);
+          for (int j = 0; j < 32; ++j) part[(c0 + j) * 128 + row] = __uint_as_float(u[j]);
+        }
+        epi_bar_sync();  // every row of this CTA is stored
+        if (e == 0) {
+          __threadfence();
+          ptx::st_release_gpu_u64(flag_of(x.slot0 + x.piece - 1), args.split_tag);
+        }
+      } else {
+        // piece 0 of a split tile adds the later pieces' partial sums, in piece order
+        int nparts = x.piece == 0 ? split_P - 1 : 0;
+        if (nparts > 0) {
+          bool got = true;
+          if (lane == 0)
+            for (int p = 0; p < nparts && got; ++p) got = ptx::wait_flag_u64(flag_of(x.slot0 + p), args.split_tag, abort_flag);
+          got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+          if (!got) {  // a piece never arrived: the error is recorded and the tile left incomplete
+            if (!*abort_flag) give_up();
+            nparts = 0;
+          }
+          for (int p = 0; p < nparts; ++p) ptx::wait_flag_u64(flag_of(x.slot0 + p), args.split_tag, nullptr);
+        }
+        auto add_parts = [&](float (&v)[32], int c0) {
+          for (int p = 0; p < nparts; ++p) {
+            const float* part = part_of(x.slot0 + p);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += __ldcg(part + (c0 + j) * 128 + row);
+          }
+        };
+        if (args.tma_out) {
+          // The LoRA region is free from the fold's completion (acc_full) until
+          // the next stage_lora, which follows the epilogue warps' barrier:
+          // this warp stages its 32 rows there as 64-column bf16 boxes (two
+          // 4 KB buffers in turn) and stores them by TMA.
+          uint8_t* stg = sLA + (warp - 10) * 8192;
+          const uint32_t stg_a = ptx::smem_addr(stg);
+#pragma unroll 1
+          for (int p = 0; p < kBN / 64; ++p) {
+            const int b = p & 1;
+            if (p >= 2) {  // buffer b's previous box has been read out
+              if (lane == 0) ptx::bulk_wait_read1();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t u[32];
+              ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(p * 64 + h * 32), u);
+              ptx::tmem_wait_ld();
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+              add_parts(v, p * 64 + h * 32);
+#pragma unroll
+              for (int g4 = 0; g4 < 4; ++g4)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 stg_a + b * 4096 + lane * 128 + (((h * 4 + g4) ^ (lane & 7)) << 4)),
+                             "r"(pack_bf16x2(v[8 * g4 + 0], v[8 * g4 + 1])),
+                             "r"(pack_bf16x2(v[8 * g4 + 2], v[8 * g4 + 3])),
+                             "r"(pack_bf16x2(v[8 * g4 + 4], v[8 * g4 + 5])),
+                             "r"(pack_bf16x2(v[8 * g4 + 6], v[8 * g4 + 7]))
+                             : "memory");
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(&map_o, stg + b * 4096, n0 + p * 64, tile_m0(t) + q * 32);
+              ptx::bulk_commit();
+            }
+          }
+          if (lane == 0) ptx::bulk_wait_read0();  // the region is free again before any warp passes the next barrier
+          __syncwarp();
+        } else {
+#pragma unroll 1
+          for (int c0 = 0; c0 < kBN; c0 += 32) {
+            uint32_t u[32];
+            ptx::tmem_ld_32x32b_x32(t_row + c0, u);
+            ptx::tmem_wait_ld();
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+            add_parts(v, c0);
+            store32(gm, n0, c0, v);
+          }
         }
       }
       // accumulator drained: let the leader reuse it

@@ -179,9 +179,11 @@ sl_status lora_down(const uint16_t* X, int64_t M, int K, const uint16_t* W, int 
   return check_launch("sum_splits_kernel");
 }
 
-// Workspace of one linear: U [M, r] fp32 (backward only; the forward needs none).
+// Workspace of one linear: U [M, r] fp32 (backward only), then, when the
+// CTA-pair GEMM runs (M > 128), the scratch that lets its last partial wave
+// split along K (either direction).
 struct LinWs {
-  size_t U, total;
+  size_t U, U_bytes, split, total;
 };
 
 static LinWs lin_ws(int64_t M, int64_t N, int64_t K, int r) {
@@ -190,8 +192,16 @@ static LinWs lin_ws(int64_t M, int64_t N, int64_t K, int r) {
   LinWs w{};
   if (r <= 0) return w;
   w.U = 0;
-  w.total = align_up(static_cast<size_t>(M) * r * 4, 256);
+  w.U_bytes = align_up(static_cast<size_t>(M) * r * 4, 256);
+  w.split = w.U_bytes;
+  w.total = w.U_bytes + (M > 128 ? split_scratch_bytes() : 0);
   return w;
+}
+
+// The split scratch inside a caller's workspace laid out as [U | split], if it is there.
+static void* split_in(void* ws, size_t ws_bytes, size_t U_bytes) {
+  if (!ws || ws_bytes < U_bytes + split_scratch_bytes() || (reinterpret_cast<uintptr_t>(ws) & 255)) return nullptr;
+  return static_cast<uint8_t*>(ws) + U_bytes;
 }
 
 size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return lin_ws(M, N, K, r).total; }
@@ -246,6 +256,13 @@ static sl_status check_rows(const sl_weight* w, int64_t M, const char* who) {
 
 sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
                      float alpha, void* Y, void* T_save, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const size_t U_bytes = r > 0 ? lin_ws(M, 0, 0, r).U_bytes : 0;
+  void* split = split_in(ws, ws_bytes, U_bytes);
+  return linear_fwd_x(w, X, M, A, B, r, alpha, Y, T_save, split, split ? split_scratch_bytes() : 0, stream);
+}
+
+sl_status linear_fwd_x(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
+                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream) {
   sl_status st = check_weight(w);
   if (st != SL_OK) return st;
   SL_REQUIRE(X && Y && M > 0, "sl_lora_linear_fwd: null X/Y or M <= 0");
@@ -254,8 +271,6 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
   SL_REQUIRE(M < (1LL << 31), "sl_lora_linear_fwd: M too large");
   st = check_rows(w, M, "sl_lora_linear_fwd");
   if (st != SL_OK) return st;
-  (void)ws;
-  (void)ws_bytes;
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
   if (lora) {
@@ -264,6 +279,8 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
+  g.split_ws = split_ws;
+  g.split_ws_bytes = split_bytes;
   bind_weight(g, w);
   g.bmn = 0;
   g.epi = kEpiStoreBF16;
@@ -284,7 +301,8 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
 
 sl_status linear_bwd_split(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A, const void* B,
                            int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
-                           void* ws, size_t ws_bytes, cudaStream_t stream, const GradSide* side) {
+                           void* ws, size_t ws_bytes, cudaStream_t stream, const GradSide* side, void* split_ws,
+                           size_t split_bytes) {
   sl_status st = check_weight(w);
   if (st != SL_OK) return st;
   SL_REQUIRE(dY && M > 0, "sl_lora_linear_bwd: null dY or M <= 0");
@@ -297,7 +315,7 @@ sl_status linear_bwd_split(const sl_weight* w, const void* X, const void* dY, in
     if (st != SL_OK) return st;
   }
   const LinWs L = lin_ws(M, w->N, w->K, lora ? r : 0);
-  SL_REQUIRE(ws_bytes >= L.total && (L.total == 0 || ws), "sl_lora_linear_bwd: workspace too small");
+  SL_REQUIRE(ws_bytes >= L.U_bytes && (L.U_bytes == 0 || ws), "sl_lora_linear_bwd: workspace too small");
   SL_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "sl_lora_linear_bwd: workspace must be 256-byte aligned");
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
@@ -316,6 +334,8 @@ sl_status linear_bwd_split(const sl_weight* w, const void* X, const void* dY, in
   }
   if (dX) {
     GemmLaunch g{};
+    g.split_ws = split_ws;
+    g.split_ws_bytes = split_bytes;
     bind_weight(g, w);
     g.bmn = 1;
     g.epi = kEpiStoreBF16;
@@ -376,8 +396,11 @@ static sl_status run_bwd_split(cudaStream_t stream, bool lora, Body body) {
 sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A, const void* B,
                      int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const size_t U_bytes = r > 0 ? lin_ws(M, 0, 0, r).U_bytes : 0;
+  void* split = split_in(ws, ws_bytes, U_bytes);
   return run_bwd_split(stream, r > 0 && A && B, [&](cudaStream_t main, const GradSide* side) {
-    return linear_bwd_split(w, X, dY, M, A, B, r, alpha, T_save, dX, dA, dB, accumulate, ws, ws_bytes, main, side);
+    return linear_bwd_split(w, X, dY, M, A, B, r, alpha, T_save, dX, dA, dB, accumulate, ws, ws_bytes, main, side,
+                            split, split ? split_scratch_bytes() : 0);
   });
 }
 
@@ -406,12 +429,22 @@ static sl_status check_group(const sl_weight* w, int G, const int64_t* N_g, int6
   return SL_OK;
 }
 
-size_t group_ws_bytes(int64_t M, int G, int r) {
+// U_cat [M, G r] fp32, then the split-K scratch of the CTA-pair GEMM (M > 128).
+static size_t group_U_bytes(int64_t M, int G, int r) {
   return r > 0 ? align_up(static_cast<size_t>(M) * G * r * 4, 256) : 0;
+}
+size_t group_ws_bytes(int64_t M, int G, int r) {
+  return r > 0 ? group_U_bytes(M, G, r) + (M > 128 ? split_scratch_bytes() : 0) : 0;
 }
 
 sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, int64_t M, const void* A_cat,
                     const void* B_cat, int r, float alpha, void* Y_cat, void* T_cat, cudaStream_t stream) {
+  return group_fwd_x(w, G, N_g, X, M, A_cat, B_cat, r, alpha, Y_cat, T_cat, nullptr, 0, stream);
+}
+
+sl_status group_fwd_x(const sl_weight* w, int G, const int64_t* N_g, const void* X, int64_t M, const void* A_cat,
+                      const void* B_cat, int r, float alpha, void* Y_cat, void* T_cat, void* split_ws,
+                      size_t split_bytes, cudaStream_t stream) {
   int bounds[5];
   sl_status st = check_group(w, G, N_g, M, r, bounds);
   if (st != SL_OK) return st;
@@ -426,6 +459,8 @@ sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
     if (st != SL_OK) return st;
   }
   GemmLaunch g{};
+  g.split_ws = split_ws;
+  g.split_ws_bytes = split_bytes;
   bind_weight(g, w);
   g.bmn = 0;
   g.epi = kEpiStoreBF16;
@@ -451,14 +486,14 @@ sl_status group_fwd(const sl_weight* w, int G, const int64_t* N_g, const void* X
 sl_status group_bwd_split(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
                           const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX,
                           float* dA_cat, float* dB_cat, int accumulate, void* ws, size_t ws_bytes,
-                          cudaStream_t stream, const GradSide* side) {
+                          cudaStream_t stream, const GradSide* side, void* split_ws, size_t split_bytes) {
   int bounds[5];
   sl_status st = check_group(w, G, N_g, M, r, bounds);
   if (st != SL_OK) return st;
   const bool lora = r > 0;
   SL_REQUIRE(dY_cat && (!lora || (X && A_cat && B_cat && T_cat && dA_cat && dB_cat)),
              "sl_lora_group_bwd: null argument");
-  SL_REQUIRE(!lora || (ws && ws_bytes >= group_ws_bytes(M, G, r) && (reinterpret_cast<uintptr_t>(ws) & 255) == 0),
+  SL_REQUIRE(!lora || (ws && ws_bytes >= group_U_bytes(M, G, r) && (reinterpret_cast<uintptr_t>(ws) & 255) == 0),
              "sl_lora_group_bwd: workspace too small or not 256-byte aligned");
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
@@ -478,6 +513,8 @@ sl_status group_bwd_split(const sl_weight* w, int G, const int64_t* N_g, const v
   if (dX) {
     // dX = dY_cat W_cat + s U_cat A_cat: the plain dX GEMM at rank G r
     GemmLaunch g{};
+    g.split_ws = split_ws;
+    g.split_ws_bytes = split_bytes;
     bind_weight(g, w);
     g.bmn = 1;
     g.epi = kEpiStoreBF16;
@@ -512,9 +549,10 @@ sl_status group_bwd_split(const sl_weight* w, int G, const int64_t* N_g, const v
 sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
                     const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX, float* dA_cat,
                     float* dB_cat, int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  void* split = split_in(ws, ws_bytes, group_U_bytes(M, G, r));
   return run_bwd_split(stream, r > 0, [&](cudaStream_t main, const GradSide* side) {
     return group_bwd_split(w, G, N_g, X, dY_cat, M, A_cat, B_cat, r, alpha, T_cat, dX, dA_cat, dB_cat, accumulate, ws,
-                           ws_bytes, main, side);
+                           ws_bytes, main, side, split, split ? split_scratch_bytes() : 0);
   });
 }
 

@@ -313,6 +313,28 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
       : "memory");
 }
 
+// Release store / acquire load of a 64-bit flag in global memory (GPU scope).
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits until *p == v (acquire), giving up after kWaitLimitNs or when
+// *abort (shared) is set; returns false when it gave up.
+__device__ __forceinline__ bool wait_flag_u64(const unsigned long long* p, unsigned long long v, volatile int* abort) {
+  if (ld_acquire_gpu_u64(p) == v) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu_u64(p) == v) return true;
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading-
 // and stride-dimension byte offsets, version 1, swizzle mode in bits 61-63
 // (2 = 128-byte swizzle).

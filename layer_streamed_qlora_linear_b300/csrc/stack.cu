@@ -26,6 +26,7 @@
 #include "attn.cuh"
 #include "common.cuh"
 #include "glue.cuh"
+#include "gemm.cuh"
 #include "linear.cuh"
 
 using namespace sl;
@@ -159,6 +160,9 @@ struct Plan {
   // until that unit's dA pass has read it: [M, G r] fp32 each
   size_t U[4] = {0, 0, 0, 0};
   size_t U_bytes[4] = {0, 0, 0, 0};
+  // scratch that lets the persistent GEMMs split their last partial wave
+  // along K (the GEMMs run one after another on the main stream)
+  size_t split = 0, split_bytes = 0;
   size_t att_ws = 0, rope = 0;  // attention: Di [H, M] and the rotary table [S, 128]
   size_t lin_ws_bytes = 0;
 };
@@ -220,6 +224,10 @@ Plan make_plan(const sl_stack* s, int64_t M, int r) {
   for (int u = 0; u < 4; ++u) {  // G regions of [M, r] (a group's [M, G r] fits in them)
     P.U_bytes[u] = unit_G[u] * align_up(static_cast<size_t>(M) * (rr ? rr : 1) * 4, 256);
     P.U[u] = take(P.U_bytes[u]);
+  }
+  if (M > 128 && s->kind != SL_WEIGHT_BF16) {
+    P.split_bytes = split_scratch_bytes();
+    P.split = take(P.split_bytes);
   }
   if (s->mixer == SL_MIX_ATTENTION) {
     P.att_ws = take(attention_ws_bytes(M, static_cast<int>(s->D / 128)));
@@ -314,8 +322,8 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   const int64_t rr = r > 0 ? r : 1;
   auto A = [&](int p) { return r > 0 ? c.A[7 * l + p] : nullptr; };
   auto B = [&](int p) { return r > 0 ? c.B[7 * l + p] : nullptr; };
-  void* lws = c.at<uint8_t>(P.lin_ws);
-  const size_t lwb = P.lin_ws_bytes;
+  void* spl = P.split_bytes ? c.at<uint8_t>(P.split) : nullptr;
+  const size_t spb = P.split_bytes;
   uint16_t* x1 = c.at<uint16_t>(P.x1[l]);
   uint16_t* qkv = c.at<uint16_t>(P.qkv[l]);
   uint16_t* a = c.at<uint16_t>(P.a[l]);
@@ -334,7 +342,7 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   if (c.group_qkv) {
     const sl_weight wg = group_weight(w, 0, 3);
     const int64_t Ng[3] = {D, Dkv, Dkv};
-    SL_TRY(group_fwd(&wg, 3, Ng, x1, M, A(0), B(0), r, c.alpha, qkv, Tqkv, c.stream));
+    SL_TRY(group_fwd_x(&wg, 3, Ng, x1, M, A(0), B(0), r, c.alpha, qkv, Tqkv, spl, spb, c.stream));
     q = qkv;
     k = qkv + D;
     v = qkv + D + Dkv;
@@ -343,9 +351,9 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
     uint16_t* yq = qkv;
     uint16_t* yk = qkv + M * D;
     uint16_t* yv = yk + M * Dkv;
-    SL_TRY(linear_fwd(&w[0], x1, M, A(0), B(0), r, c.alpha, yq, Tqkv, lws, lwb, c.stream));
-    SL_TRY(linear_fwd(&w[1], x1, M, A(1), B(1), r, c.alpha, yk, Tqkv + M * rr, lws, lwb, c.stream));
-    SL_TRY(linear_fwd(&w[2], x1, M, A(2), B(2), r, c.alpha, yv, Tqkv + 2 * M * rr, lws, lwb, c.stream));
+    SL_TRY(linear_fwd_x(&w[0], x1, M, A(0), B(0), r, c.alpha, yq, Tqkv, spl, spb, c.stream));
+    SL_TRY(linear_fwd_x(&w[1], x1, M, A(1), B(1), r, c.alpha, yk, Tqkv + M * rr, spl, spb, c.stream));
+    SL_TRY(linear_fwd_x(&w[2], x1, M, A(2), B(2), r, c.alpha, yv, Tqkv + 2 * M * rr, spl, spb, c.stream));
     q = yq;
     k = yk;
     v = yv;
@@ -366,20 +374,20 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   } else {
     SL_TRY(glue_mix_fwd(q, k, v, a, M, D, Dkv, ldq, ldkv, c.stream));
   }
-  SL_TRY(linear_fwd(&w[3], a, M, A(3), B(3), r, c.alpha, o, c.at<float>(P.To[l]), lws, lwb, c.stream));
+  SL_TRY(linear_fwd_x(&w[3], a, M, A(3), B(3), r, c.alpha, o, c.at<float>(P.To[l]), spl, spb, c.stream));
   SL_TRY(glue_rms_fwd(h_in, o, h1, x2, c.at<float>(P.rstd2[l]), norms[1], M, D, c.stream));
   // gate, up
   if (c.group_gu) {
     const sl_weight wg = group_weight(w, 4, 2);
     const int64_t Ng[2] = {F, F};
-    SL_TRY(group_fwd(&wg, 2, Ng, x2, M, A(4), B(4), r, c.alpha, gu, Tgu, c.stream));
+    SL_TRY(group_fwd_x(&wg, 2, Ng, x2, M, A(4), B(4), r, c.alpha, gu, Tgu, spl, spb, c.stream));
     SL_TRY(glue_swiglu_fwd(gu, gu + F, m, M, F, 2 * F, c.stream));
   } else {
-    SL_TRY(linear_fwd(&w[4], x2, M, A(4), B(4), r, c.alpha, gu, Tgu, lws, lwb, c.stream));
-    SL_TRY(linear_fwd(&w[5], x2, M, A(5), B(5), r, c.alpha, gu + M * F, Tgu + M * rr, lws, lwb, c.stream));
+    SL_TRY(linear_fwd_x(&w[4], x2, M, A(4), B(4), r, c.alpha, gu, Tgu, spl, spb, c.stream));
+    SL_TRY(linear_fwd_x(&w[5], x2, M, A(5), B(5), r, c.alpha, gu + M * F, Tgu + M * rr, spl, spb, c.stream));
     SL_TRY(glue_swiglu_fwd(gu, gu + M * F, m, M, F, F, c.stream));
   }
-  SL_TRY(linear_fwd(&w[6], m, M, A(6), B(6), r, c.alpha, d, c.at<float>(P.Td[l]), lws, lwb, c.stream));
+  SL_TRY(linear_fwd_x(&w[6], m, M, A(6), B(6), r, c.alpha, d, c.at<float>(P.Td[l]), spl, spb, c.stream));
   SL_TRY(glue_resid_add(h1, d, h_out, M * s->D, c.stream));
   return SL_OK;
 }
@@ -398,6 +406,8 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   auto B = [&](int p) { return r > 0 ? c.B[7 * l + p] : nullptr; };
   auto dA = [&](int p) { return r > 0 ? c.dA[7 * l + p] : nullptr; };
   auto dB = [&](int p) { return r > 0 ? c.dB[7 * l + p] : nullptr; };
+  void* spl = P.split_bytes ? c.at<uint8_t>(P.split) : nullptr;
+  const size_t spb = P.split_bytes;
   uint16_t* dm = c.at<uint16_t>(P.dm);
   uint16_t* dgu = c.at<uint16_t>(P.dgu);
   uint16_t* dx2a = c.at<uint16_t>(P.dx2a);
@@ -432,7 +442,7 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
     SL_TRY(wait_unit(kDown));
     const GradSide sd = side(kDown);
     SL_TRY(linear_bwd_split(&w[6], c.at<uint16_t>(P.m[l]), dd, M, A(6), B(6), r, c.alpha, c.at<float>(P.Td[l]), dm,
-                            dA(6), dB(6), c.accumulate, U_of(kDown, 0), P.U_bytes[kDown], c.stream, &sd));
+                            dA(6), dB(6), c.accumulate, U_of(kDown, 0), P.U_bytes[kDown], c.stream, &sd, spl, spb));
   }
   // gate, up
   SL_TRY(wait_unit(kGU));
@@ -442,7 +452,7 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
     const int64_t Ng[2] = {F, F};
     const GradSide sd = side(kGU);
     SL_TRY(group_bwd_split(&wg, 2, Ng, x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate,
-                           U_of(kGU, 0), P.U_bytes[kGU], c.stream, &sd));
+                           U_of(kGU, 0), P.U_bytes[kGU], c.stream, &sd, spl, spb));
     SL_TRY(wait_unit(kO));
     SL_TRY(glue_rms_bwd(dh2, dx2a, nullptr, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]),
                         norms[1], dh1, do_, M, D, c.stream));
@@ -451,9 +461,9 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
     const GradSide s0{c.side, s->fork[kGU], nullptr};
     const GradSide s1 = side(kGU);
     SL_TRY(linear_bwd_split(&w[4], x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate,
-                            U_of(kGU, 0), U1, c.stream, &s0));
+                            U_of(kGU, 0), U1, c.stream, &s0, spl, spb));
     SL_TRY(linear_bwd_split(&w[5], x2, dgu + M * F, M, A(5), B(5), r, c.alpha, Tgu + M * rr, dx2b, dA(5), dB(5),
-                            c.accumulate, U_of(kGU, 1), U1, c.stream, &s1));
+                            c.accumulate, U_of(kGU, 1), U1, c.stream, &s1, spl, spb));
     SL_TRY(wait_unit(kO));
     SL_TRY(glue_rms_bwd(dh2, dx2a, dx2b, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]),
                         norms[1], dh1, do_, M, D, c.stream));
@@ -461,7 +471,7 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   {
     const GradSide sd = side(kO);
     SL_TRY(linear_bwd_split(&w[3], c.at<uint16_t>(P.a[l]), do_, M, A(3), B(3), r, c.alpha, c.at<float>(P.To[l]), da,
-                            dA(3), dB(3), c.accumulate, U_of(kO, 0), P.U_bytes[kO], c.stream, &sd));
+                            dA(3), dB(3), c.accumulate, U_of(kO, 0), P.U_bytes[kO], c.stream, &sd, spl, spb));
   }
   // q, k, v: the mixing step's backward into the dq/dk/dv region
   auto mix_bwd = [&](const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t ldq, int64_t ldkv,
@@ -479,7 +489,7 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
     const int64_t Ng[3] = {D, Dkv, Dkv};
     const GradSide sd = side(kQKV);
     SL_TRY(group_bwd_split(&wg, 3, Ng, x1, dqkv, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate,
-                           U_of(kQKV, 0), P.U_bytes[kQKV], c.stream, &sd));
+                           U_of(kQKV, 0), P.U_bytes[kQKV], c.stream, &sd, spl, spb));
     SL_TRY(wait_unit(kDown));  // dd (this layer's down dY) is overwritten next
     SL_TRY(glue_rms_bwd(dh1, dx1q, nullptr, nullptr, nullptr, h_in, c.at<float>(P.rstd1[l]), norms[0], dh, dh_bf16, M,
                         D, c.stream));
@@ -491,11 +501,11 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
     const GradSide s0{c.side, s->fork[kQKV], nullptr};
     const GradSide s2 = side(kQKV);
     SL_TRY(linear_bwd_split(&w[0], x1, dq, M, A(0), B(0), r, c.alpha, Tqkv, dx1q, dA(0), dB(0), c.accumulate,
-                            U_of(kQKV, 0), U1, c.stream, &s0));
+                            U_of(kQKV, 0), U1, c.stream, &s0, spl, spb));
     SL_TRY(linear_bwd_split(&w[1], x1, dk, M, A(1), B(1), r, c.alpha, Tqkv + M * rr, dx1k, dA(1), dB(1),
-                            c.accumulate, U_of(kQKV, 1), U1, c.stream, &s0));
+                            c.accumulate, U_of(kQKV, 1), U1, c.stream, &s0, spl, spb));
     SL_TRY(linear_bwd_split(&w[2], x1, dv, M, A(2), B(2), r, c.alpha, Tqkv + 2 * M * rr, dx1v, dA(2), dB(2),
-                            c.accumulate, U_of(kQKV, 2), U1, c.stream, &s2));
+                            c.accumulate, U_of(kQKV, 2), U1, c.stream, &s2, spl, spb));
     SL_TRY(wait_unit(kDown));  // dd (this layer's down dY) is overwritten next
     SL_TRY(glue_rms_bwd(dh1, dx1q, dx1k, dx1v, nullptr, h_in, c.at<float>(P.rstd1[l]), norms[0], dh, dh_bf16, M, D,
                         c.stream));

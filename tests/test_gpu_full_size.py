@@ -133,3 +133,39 @@ def test_qwen3b_bf16_stack_m2048_streamed_equals_resident_bitwise(gpu_lib):
     for g in a[2] + a[3]:
         assert torch.isfinite(g).all() and g.abs().sum() > 0
     S.stack.close()
+
+
+def test_llama8b_layer_split_tail_m1024_matches_oracle(gpu_lib):
+    """One Llama-8B-shaped NF4 layer through the stack at M = 1024 with the
+    q/k/v and gate/up groups: the persistent GEMMs' last partial waves split
+    along K (q/k/v forward: 96 tiles on 74 SM pairs, the 22 tail tiles in 3
+    pieces; gate/up forward: 448 tiles, 4 in 4 pieces; down dX: 224 tiles, 2
+    in 7 pieces), checked against the oracle's layer."""
+    sl = gpu_lib
+    S = Setup(sl, sl.SL_WEIGHT_NF4, L=1, M=1024, D=LLAMA["D"], Dkv=LLAMA["Dkv"], F=LLAMA["F"], r=16, alpha=32.0,
+              seed=71, packed=True)
+    hL, dh0, dA, dB = S.run(sl.SL_MODE_STREAMED)
+    ohL, odh0, ograds = stack.stack_step(S.h0_np, S.dh_np, S.ref_layers, 32.0, rnd=True)
+    errs = {"hL": rel_fro(host(hL), ohL), "dh0": rel_fro(host(dh0), odh0)}
+    for p, n in enumerate(si.PROJ_NAMES):
+        errs[f"dA_{n}"] = rel_fro(host(dA[p]), ograds[0][n][0])
+        errs[f"dB_{n}"] = rel_fro(host(dB[p]), ograds[0][n][1])
+    print({k: round(float(v), 5) for k, v in errs.items()})
+    assert max(errs.values()) <= BF16_TOL, errs
+    S.stack.close()
+
+
+def test_llama8b_stack_split_tail_m1024_streamed_equals_resident_bitwise(gpu_lib):
+    """Three 8B-shaped NF4 layers at the headline M = 1024 (every split tail
+    of the step) streamed and resident: bitwise equal, and repeatable."""
+    sl = gpu_lib
+    S = Setup(sl, sl.SL_WEIGHT_NF4, L=3, M=1024, D=LLAMA["D"], Dkv=LLAMA["Dkv"], F=LLAMA["F"], r=16, alpha=32.0,
+              seed=73, with_oracle=False, torch_weights=True, packed=True)
+    a = S.run(sl.SL_MODE_STREAMED)
+    b = S.run(sl.SL_MODE_RESIDENT)
+    c = S.run(sl.SL_MODE_STREAMED)
+    for x, y, z in zip((a[0], a[1], *a[2], *a[3]), (b[0], b[1], *b[2], *b[3]), (c[0], c[1], *c[2], *c[3])):
+        assert same_bits(x, y) and same_bits(x, z)
+    for g in a[2] + a[3]:
+        assert torch.isfinite(g).all() and g.abs().sum() > 0
+    S.stack.close()

@@ -98,12 +98,16 @@ def test_bounded_wait_times_out_without_fault(gpu_lib):
     assert float(x.sum()) == 4.0
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 2560, 2560), (300, 1248, 2048)])
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 2560), (300, 1248, 2048), (1024, 4864, 4096), (1024, 4096, 4864)])
 def test_pair_gemm_tile_walk_matches_oracle(gpu_lib, M, N, K):
     """The CTA-pair NF4 GEMM at sizes where tiles outnumber the SM pairs
     (80 pair tiles on 74: some clusters run two tiles, alternating their
     TMEM accumulators and LoRA staging) and with a ragged M pair and a
-    partial N tile; bitwise repeatable, and the forward ignores `ws`."""
+    partial N tile. With a workspace the persistent kernel splits its last
+    partial wave along K (80 tiles: the 6 tail tiles in 3 pieces; 76 tiles
+    in the forward of N = 4864 or the dX of K = 4864: 2 tail tiles in 4
+    pieces, the partial sums added in piece order): bitwise repeatable, and
+    within rounding of the forward without a workspace (no split)."""
     r, alpha = 16, 32.0
     c, W_ref, w, t = make(gpu_lib, 11, M, N, K, r, "nf4")
     a = run(gpu_lib, w, t, M, N, K, r, alpha)
@@ -114,7 +118,7 @@ def test_pair_gemm_tile_walk_matches_oracle(gpu_lib, M, N, K):
     T = torch.empty(M, r, dtype=torch.float32, device="cuda")
     gpu_lib.sl_lora_linear_fwd(w, t["X"], t["A"], t["B"], r, alpha, Y, T, None)
     gpu_lib.sl_check_device_errors()
-    assert torch.equal(Y, a[0]) and torch.equal(T, a[1])
+    assert torch.equal(T, a[1]) and rel_fro(host(Y), host(a[0])) <= 2e-3
     Yo = lora.lora_linear_fwd(c["X"], W_ref, c["A"], c["B"], alpha)
     dXo, dAo, dBo = lora.lora_linear_bwd(c["X"], c["dY"], W_ref, c["A"], c["B"], alpha)
     assert rel_fro(host(a[0]), Yo) <= BF16_TOL
