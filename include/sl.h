@@ -145,6 +145,16 @@ sl_status sl_kernel_timing(int32_t enable);
  * pair: 2 products forward; 5 backward, S recomputed once). */
 sl_status sl_kernel_timing_read(int32_t variant, uint64_t* launches, double* ms, double* work);
 
+/* The GEMM variants (0-5) timed on the device clock: every timed GEMM launch
+ * records its own span, from the first CTA past its dependency wait to the
+ * last CTA whose output stores have completed (%globaltimer), into a slot
+ * buffer libsl allocates on the first sl_kernel_timing(1) (which therefore
+ * synchronises the device).  Returns the launches that recorded a span and
+ * their summed span in ms.  Unlike an event pair around a launch, the span
+ * is not lengthened by delayed event timestamps (a host-to-device copy in
+ * flight delays them by ~16 us per pair on B300). */
+sl_status sl_kernel_timing_read_clock(int32_t variant, uint64_t* launches, double* ms);
+
 /* ------------------------------------------------------------- NF4 (K0/K1) */
 
 /* NF4-quantise W [N, K] (dtype SL_DTYPE_BF16 or SL_DTYPE_F32) into codes

@@ -57,6 +57,7 @@ _SIGS = {
     "sl_debug_timeout_probe": (_I32, [_I64, _I32, _P]),
     "sl_kernel_timing": (_I32, [_I32]),
     "sl_kernel_timing_read": (_I32, [_I32, _P, _P, _P]),
+    "sl_kernel_timing_read_clock": (_I32, [_I32, _P, _P]),
     "sl_nf4_quantize": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P]),
     "sl_nf4_dequantize": (_I32, [_P, _P, _I64, _I64, _I32, _P, _P]),
     "sl_nf4_double_quantize": (_I32, [_P, _I64, _I64, _P, _I64, _P, _I64, _P]),
@@ -163,6 +164,13 @@ TIMED_VARIANTS = GEMM_VARIANTS + RANK_R_VARIANTS + ATTN_VARIANTS
 
 def sl_kernel_timing(enable: bool):
     _check(lib().sl_kernel_timing(int(bool(enable))))
+
+
+def sl_kernel_timing_read_clock(variant: int):
+    """(launches, ms) of one GEMM variant (0-5) on the device clock since timing was enabled."""
+    n, ms = ctypes.c_uint64(0), ctypes.c_double(0)
+    _check(lib().sl_kernel_timing_read_clock(int(variant), ctypes.byref(n), ctypes.byref(ms)))
+    return n.value, ms.value
 
 
 def sl_kernel_timing_read(variant: int):

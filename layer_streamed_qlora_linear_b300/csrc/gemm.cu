@@ -56,6 +56,20 @@ std::mutex g_time_mu;
 bool g_time_on = false;
 std::vector<TimedLaunch> g_timed;
 std::vector<cudaEvent_t> g_event_pool;
+// Device-clock slots of the timed GEMM launches ({first start, last end}
+// per launch, %globaltimer ns), allocated on the first timing enable.
+constexpr int kClkSlots = 16384;
+unsigned long long* g_clk = nullptr;
+int g_clk_dev = -1;
+int g_clk_used = 0;
+std::vector<int> g_clk_slot;  // slot of g_timed[i], or -1
+
+__global__ void clk_init_kernel(unsigned long long* c, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    c[2 * i] = ~0ull;
+    c[2 * i + 1] = 0ull;
+  }
+}
 
 cudaEvent_t pool_event() {
   if (!g_event_pool.empty()) {
@@ -83,6 +97,9 @@ TimingToken timing_begin(int variant, double work, cudaStream_t stream) {
   t.stop = pool_event();
   t.variant = variant;
   t.work = work;
+  int dev = -1;
+  if (variant <= 5 && g_clk && cudaGetDevice(&dev) == cudaSuccess && dev == g_clk_dev && g_clk_used < kClkSlots)
+    t.clk = g_clk + 2 * g_clk_used++;
   if (t.start) cudaEventRecord(t.start, stream);
   return t;
 }
@@ -92,6 +109,7 @@ void timing_end(const TimingToken& t, cudaStream_t stream) {
   cudaEventRecord(t.stop, stream);
   std::lock_guard<std::mutex> lk(g_time_mu);
   g_timed.push_back(TimedLaunch{t.start, t.stop, t.variant, t.work});
+  g_clk_slot.push_back(t.clk ? static_cast<int>((t.clk - g_clk) / 2) : -1);
 }
 
 // NF4 GEMM on CTA pairs (M = 256 per pair); used when M > 128.
@@ -239,6 +257,9 @@ static sl_status run(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
 
 sl_status dispatch(const GemmLaunch& g, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms,
                    cudaStream_t stream);
+static sl_status launch_timed(const GemmLaunch& g, bool pair, const CUtensorMap& ma, const CUtensorMap& mb,
+                              const CUtensorMap& ms, const CUtensorMap& ms2, const TimingToken& tl,
+                              cudaStream_t stream);
 
 sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
   const GemmArgs& a = g.args;
@@ -315,9 +336,18 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
     }
     if (st != SL_OK) return st;
   }
-  TimingToken tl = timing_begin(variant_of(g),
-                                2.0 * a.M * static_cast<double>(a.N) * a.K + 2.0 * a.M * static_cast<double>(a.N) * a.r,
-                                stream);
+  const TimingToken tl = timing_begin(
+      variant_of(g), 2.0 * a.M * static_cast<double>(a.N) * a.K + 2.0 * a.M * static_cast<double>(a.N) * a.r, stream);
+  GemmLaunch gc = g;  // with the launch's device-clock slot, if timed
+  gc.args.clk = tl.clk;
+  return launch_timed(gc, pair, ma, mb, ms, ms2, tl, stream);
+}
+
+static sl_status launch_timed(const GemmLaunch& g, bool pair, const CUtensorMap& ma, const CUtensorMap& mb,
+                              const CUtensorMap& ms, const CUtensorMap& ms2, const TimingToken& tl,
+                              cudaStream_t stream) {
+  const GemmArgs& a = g.args;
+  sl_status st = SL_OK;
   // More pair tiles than resident clusters: the persistent kernel (its
   // epilogue overlaps the next tile); one wave or less: one cluster per tile
   // with the epilogue spread over all eight dequant warps.
@@ -363,8 +393,49 @@ extern "C" sl_status sl_kernel_timing(int32_t enable) {
     g_event_pool.push_back(t.start);
     g_event_pool.push_back(t.stop);
   }
-  if (enable) g_timed.clear();
+  if (enable) {
+    g_timed.clear();
+    g_clk_slot.clear();
+    // device-clock slots on the current device (outside any timed region: this synchronises)
+    int dev = -1;
+    SL_CHECK_CUDA(cudaGetDevice(&dev));
+    if (g_clk && g_clk_dev != dev) {
+      cudaFree(g_clk);
+      g_clk = nullptr;
+    }
+    if (!g_clk) {
+      SL_CHECK_CUDA(cudaMalloc(&g_clk, sizeof(unsigned long long) * 2 * kClkSlots));
+      g_clk_dev = dev;
+    }
+    clk_init_kernel<<<64, 256>>>(g_clk, kClkSlots);
+    SL_CHECK_CUDA(cudaGetLastError());
+    SL_CHECK_CUDA(cudaDeviceSynchronize());
+    g_clk_used = 0;
+  }
   g_time_on = enable != 0;
+  return SL_OK;
+}
+
+extern "C" sl_status sl_kernel_timing_read_clock(int32_t variant, uint64_t* launches, double* ms) {
+  SL_REQUIRE(variant >= 0 && variant <= 5, "sl_kernel_timing_read_clock: variant must be a GEMM variant 0..5");
+  std::lock_guard<std::mutex> lk(g_time_mu);
+  uint64_t n = 0;
+  double t = 0.0;
+  if (g_clk && g_clk_used > 0) {
+    for (auto& tl : g_timed) SL_CHECK_CUDA(cudaEventSynchronize(tl.stop));
+    std::vector<unsigned long long> h(2 * static_cast<size_t>(g_clk_used));
+    SL_CHECK_CUDA(cudaMemcpy(h.data(), g_clk, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+    for (size_t i = 0; i < g_timed.size(); ++i) {
+      const int sl_ = g_clk_slot[i];
+      if (g_timed[i].variant != variant || sl_ < 0) continue;
+      const unsigned long long a = h[2 * sl_], b = h[2 * sl_ + 1];
+      if (a == ~0ull || b < a) continue;  // a launch that never stamped
+      ++n;
+      t += static_cast<double>(b - a) * 1e-6;
+    }
+  }
+  if (launches) *launches = n;
+  if (ms) *ms = t;
   return SL_OK;
 }
 

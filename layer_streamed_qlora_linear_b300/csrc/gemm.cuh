@@ -106,7 +106,17 @@ struct GemmArgs {
   float* split_part;
   unsigned long long* split_flag;
   unsigned long long split_tag;
+  // launch timing on the device clock (nullptr: off): clk[0] = min over CTAs
+  // of %globaltimer once past the dependency wait, clk[1] = max once done
+  unsigned long long* clk;
 };
+
+__device__ __forceinline__ void clk_start(const GemmArgs& a) {
+  if (a.clk && threadIdx.x == 0) atomicMin(a.clk, globaltimer_ns());
+}
+__device__ __forceinline__ void clk_end(const GemmArgs& a) {
+  if (a.clk && threadIdx.x == 0) atomicMax(a.clk + 1, globaltimer_ns());
+}
 
 // One row segment of 64 NF4 elements (32 packed code bytes, one absmax) ->
 // 64 bf16 = bf16(T[code] * absmax), written as eight 16-byte chunks of a
@@ -223,6 +233,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // dependents launch as its CTAs exit (an early trigger let small follow-up
   // kernels wait beside the last wave and slowed it).
   pdl_wait();  // the previous kernel's writes are visible from here on
+  clk_start(args);
 
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -673,9 +684,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   __syncwarp();
+  if (args.clk) ptx::bulk_wait0();  // this thread's output stores complete before the end stamp
 
   ptx::tc_fence_before();
   __syncthreads();
+  clk_end(args);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 256);

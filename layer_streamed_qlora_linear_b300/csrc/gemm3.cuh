@@ -174,6 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
   const uint32_t tmem = *tmem_holder;
   pdl_trigger();  // the next kernel may start its prologue
   pdl_wait();     // the previous kernel's writes are visible from here on
+  clk_start(args);
 
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -607,8 +608,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     }
   }
   __syncwarp();
+  if (args.clk) ptx::bulk_wait0();  // this thread's output stores complete before the end stamp
   ptx::tc_fence_before();
   __syncthreads();
+  clk_end(args);
   ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();

@@ -13,6 +13,9 @@ struct TimingToken {
   cudaEvent_t start = nullptr, stop = nullptr;
   int variant = 0;
   double work = 0.0;  // algorithmic FLOPs (GEMMs) or bytes (rank-r passes)
+  // GEMMs: the launch's device-clock slot {first start, last end} in %globaltimer
+  // ns, which the kernel fills itself (nullptr when not timing)
+  unsigned long long* clk = nullptr;
 };
 
 // No-ops (null events) unless timing is enabled.

@@ -125,3 +125,23 @@ def test_pair_gemm_tile_walk_matches_oracle(gpu_lib, M, N, K):
     assert rel_fro(host(a[2]), dXo) <= BF16_TOL
     assert rel_fro(host(a[3]), dAo) <= BF16_TOL
     assert rel_fro(host(a[4]), dBo) <= BF16_TOL
+
+
+def test_kernel_timing_on_the_device_clock(gpu_lib):
+    """A timed GEMM launch records its own span on the device clock; with no
+    copy in flight it is within the CUDA-event pair around the launch."""
+    sl = gpu_lib
+    M, N, K, r = 300, 768, 1024, 16
+    c, W_ref, w, t = make(sl, 13, M, N, K, r, "nf4")
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    T = torch.empty(M, r, dtype=torch.float32, device="cuda")
+    sl.sl_lora_linear_fwd(w, t["X"], t["A"], t["B"], r, 32.0, Y, T, None)
+    sl.sl_kernel_timing(True)
+    for _ in range(3):
+        sl.sl_lora_linear_fwd(w, t["X"], t["A"], t["B"], r, 32.0, Y, T, None)
+    sl.sl_kernel_timing(False)
+    n_ev, ms_ev, flops = sl.sl_kernel_timing_read(0)
+    n_ck, ms_ck = sl.sl_kernel_timing_read_clock(0)
+    assert n_ev == 3 and n_ck == 3 and flops > 0
+    assert 0 < ms_ck <= ms_ev * 1.05, (ms_ck, ms_ev)
+    sl.sl_check_device_errors()
