@@ -680,8 +680,8 @@ def run_ours(args):
     # the same launches timed by the kernels themselves on the device clock: an event pair
     # around a launch also counts the delay of its timestamps, which a host-to-device copy
     # in flight (the streamed step) stretches by ~16 us
-    n_c = sum(clock[k][0] for k in dominant)
-    ms_c = sum(clock[k][1] for k in dominant)
+    n_c = sum(clock.get(k, (0, 0.0))[0] for k in dominant)
+    ms_c = sum(clock.get(k, (0, 0.0))[1] for k in dominant)
     achieved_c = fl_d / (ms_c * 1e-3) / 1e12 if ms_c > 0 and n_c == n_d else None
     roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": f"{peak_src} {peak_why}",
