@@ -388,12 +388,14 @@ using namespace sl;
 
 extern "C" sl_status sl_kernel_timing(int32_t enable) {
   std::lock_guard<std::mutex> lk(g_time_mu);
-  for (auto& t : g_timed) {
-    cudaEventSynchronize(t.stop);
-    g_event_pool.push_back(t.start);
-    g_event_pool.push_back(t.stop);
-  }
   if (enable) {
+    // the previous region's records stay readable until timing is enabled
+    // again; only then do their events go back to the pool (once each)
+    for (auto& t : g_timed) {
+      cudaEventSynchronize(t.stop);
+      g_event_pool.push_back(t.start);
+      g_event_pool.push_back(t.stop);
+    }
     g_timed.clear();
     g_clk_slot.clear();
     // device-clock slots on the current device (outside any timed region: this synchronises)

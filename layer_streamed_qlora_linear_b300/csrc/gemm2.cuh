@@ -353,7 +353,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm2Threads, 1)
         const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         nf4_words_bf16<8>(w, amax[t * 4 + (kb & 3)], bt + t * 128, 0, t & 7);
       } else {     // reduction row n, 64-column atom a (of 2)
-        const int n = t >> 1, a = t & 1;
+        // eight consecutive lanes (one 128-byte store phase) take eight rows
+        // n with distinct n % 8, so their swizzled chunks fall in different banks
+        const int n = ((t >> 5) << 4) | (t & 7) | ((t >> 1) & 8);
+        const int a = ((t >> 1) ^ (t >> 3)) & 1;
         const uint4 q0 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32);
         const uint4 q1 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32 + 16);
         const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};

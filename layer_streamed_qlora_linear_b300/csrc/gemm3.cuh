@@ -362,7 +362,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
               args.dq ? fmaf(cs[2 * p + 1], static_cast<float>(qam[tr]), cs[2 * p]) : amax[tr * 4 + (kb & 3)];
           nf4_words_bf16<8>(w, am, bt + tr * 128, 0, tr & 7);
         } else {
-          const int n = tr >> 1, a = tr & 1;
+          // eight consecutive lanes (one 128-byte store phase) take eight rows
+          // n with distinct n % 8, so their swizzled chunks fall in different banks
+          const int n = ((tr >> 5) << 4) | (tr & 7) | ((tr >> 1) & 8);
+          const int a = ((tr >> 1) ^ (tr >> 3)) & 1;
           const uint4 q0 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32);
           const uint4 q1 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32 + 16);
           const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
