@@ -262,7 +262,8 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
 }
 
 sl_status linear_fwd_x(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
-                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream) {
+                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream,
+                       bool t_ready) {
   sl_status st = check_weight(w);
   if (st != SL_OK) return st;
   SL_REQUIRE(X && Y && M > 0, "sl_lora_linear_fwd: null X/Y or M <= 0");
@@ -273,7 +274,7 @@ sl_status linear_fwd_x(const sl_weight* w, const void* X, int64_t M, const void*
   if (st != SL_OK) return st;
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
-  if (lora) {
+  if (lora && !t_ready) {
     st = skinny_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A), 0, r,
                      1, nullptr, static_cast<float*>(T_save), stream);
     if (st != SL_OK) return st;
@@ -486,7 +487,8 @@ sl_status group_fwd_x(const sl_weight* w, int G, const int64_t* N_g, const void*
 sl_status group_bwd_split(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
                           const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX,
                           float* dA_cat, float* dB_cat, int accumulate, void* ws, size_t ws_bytes,
-                          cudaStream_t stream, const GradSide* side, void* split_ws, size_t split_bytes) {
+                          cudaStream_t stream, const GradSide* side, void* split_ws, size_t split_bytes,
+                          bool u_ready) {
   int bounds[5];
   sl_status st = check_group(w, G, N_g, M, r, bounds);
   if (st != SL_OK) return st;
@@ -502,9 +504,11 @@ sl_status group_bwd_split(const sl_weight* w, int G, const int64_t* N_g, const v
   float* U = lora ? static_cast<float*>(ws) : nullptr;
   if (lora) {
     // U_cat [M, G r] = dY_cat blockdiag(B_g)
-    st = skinny_down(static_cast<const uint16_t*>(dY_cat), M, NN, static_cast<const uint16_t*>(B_cat), 1, r, G, bounds,
-                     U, stream);
-    if (st != SL_OK) return st;
+    if (!u_ready) {
+      st = skinny_down(static_cast<const uint16_t*>(dY_cat), M, NN, static_cast<const uint16_t*>(B_cat), 1, r, G,
+                       bounds, U, stream);
+      if (st != SL_OK) return st;
+    }
     if (side) {  // dA and dB go to the side stream once U is written
       SL_CHECK_CUDA(cudaEventRecord(side->fork, stream));
       SL_CHECK_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));

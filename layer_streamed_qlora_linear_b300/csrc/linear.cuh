@@ -8,9 +8,12 @@ namespace sl {
 
 sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
                      float alpha, void* Y, void* T_save, void* ws, size_t ws_bytes, cudaStream_t stream);
-// The forward with the GEMM's split-K scratch given directly (nullptr: none).
+// The forward with the GEMM's split-K scratch given directly (nullptr: none);
+// t_ready: T_save already holds X A^T (written by a fused producer), so the
+// T pass is skipped.
 sl_status linear_fwd_x(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
-                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream);
+                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream,
+                       bool t_ready = false);
 sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A, const void* B,
                      int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
                      void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -38,10 +41,12 @@ sl_status group_fwd_x(const sl_weight* w, int G, const int64_t* N_g, const void*
 sl_status group_bwd(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
                     const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX, float* dA_cat,
                     float* dB_cat, int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
+// u_ready: the workspace's U_cat region already holds dY_cat blockdiag(B_g)
+// (written by a fused producer), so the U pass is skipped.
 sl_status group_bwd_split(const sl_weight* w, int G, const int64_t* N_g, const void* X, const void* dY_cat, int64_t M,
                           const void* A_cat, const void* B_cat, int r, float alpha, const void* T_cat, void* dX,
                           float* dA_cat, float* dB_cat, int accumulate, void* ws, size_t ws_bytes, cudaStream_t main,
-                          const GradSide* side, void* split_ws, size_t split_bytes);
+                          const GradSide* side, void* split_ws, size_t split_bytes, bool u_ready = false);
 size_t group_ws_bytes(int64_t M, int G, int r);
 
 }  // namespace sl

@@ -24,6 +24,18 @@
 //     two-term bf16 split of the fp32 operand (U or T) written by the
 //     converter warps (hi in D columns 0.., lo from the next multiple of 32), so
 //     D = Q^T P to fp32 accuracy.
+// Two variants fuse the SwiGLU step of the layer into the pass that reads
+// its output, so that output is written once and never read back:
+//   GLUE = 1 (mode K, A_cat): m = SiLU(g) u from g, u tiles; T = m A^T;
+//   GLUE = 2 (mode K, blockdiag(B)^T): dg = dm u s (1 + g (1 - s)) and
+//            du = dm g s (s = sigmoid(g)) from dm, g, u tiles; each step is
+//            64 columns of dg followed by the same 64 columns of du, and
+//            U = [dg | du] blockdiag(B_g, B_u).
+// The converter warps compute the glue from the TMA-staged inputs in the
+// same 128-byte-swizzled positions, write the result over an input tile
+// (which becomes the MMA operand) and store it to global memory; the glue
+// arithmetic is the elementwise kernels' (glue.cu), expression for
+// expression, so the stored tensors are bitwise the same.
 // The long reduction is split over the CTAs of a thread-block cluster (up to
 // 16, sized so that the grid is one wave); their fp32 partials are summed
 // through distributed shared memory in rank order, so one launch writes the
@@ -42,7 +54,10 @@ namespace sl {
 
 enum SkMode { kSkKA = 0, kSkKB = 1, kSkM = 2 };
 
-constexpr int kSkThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 converters + epilogue
+// warp 0 TMA, warp 1 MMA, warps 2..5 converters + epilogue; the fused
+// SwiGLU variants add twelve converter warps for the glue arithmetic
+constexpr int kSkThreads = 192;
+__host__ __device__ constexpr int sk_threads(int glue) { return glue ? 64 + 512 : kSkThreads; }
 constexpr int kSkMaxStages = 8;
 constexpr int kSkTmemCols = 128;
 constexpr int kSkBarBytes = 1024; // barriers + misc, ahead of the 1024-aligned data
@@ -66,6 +81,10 @@ struct SkArgs {
   int accumulate;  // mode M: out += result
   float* out;
   int* err;
+  uint16_t* glue0;  // GLUE 1: m [M, C]; GLUE 2: dg
+  uint16_t* glue1;  // GLUE 2: du
+  int64_t glue_ld;  // row stride of glue0 / glue1 (elements)
+  int F;            // GLUE 2: columns of dg (= of du); C = 2 F
 };
 
 // Mode M: first D column of the lo half (32-aligned, so TMEM loads of
@@ -79,11 +98,13 @@ __host__ __device__ inline int sk_q_bytes(int step) { return 128 * step * 2; }
 __host__ __device__ inline int sk_op_bytes(int mode, int R, int rout, int step) {
   return sk_n_mma(mode, R, rout) * step * 2;
 }
-__host__ __device__ inline int sk_raw_bytes(int mode, int r, int rout, int step) {
+__host__ __device__ inline int sk_raw_bytes(int mode, int r, int rout, int step, int glue = 0) {
+  if (glue == 1) return sk_q_bytes(step);                  // the u tile
+  if (glue == 2) return sk_q_bytes(64) + step * r * 2;     // the dm tile + B_g, B_u rows of the step
   return mode == kSkKA ? 0 : (mode == kSkKB ? step * r * 2 : step * rout * 4);
 }
-__host__ __device__ inline int sk_stage_bytes(int mode, int r, int R, int rout, int step) {
-  return sk_q_bytes(step) + sk_op_bytes(mode, R, rout, step) + sk_raw_bytes(mode, r, rout, step);
+__host__ __device__ inline int sk_stage_bytes(int mode, int r, int R, int rout, int step, int glue = 0) {
+  return sk_q_bytes(step) + sk_op_bytes(mode, R, rout, step) + sk_raw_bytes(mode, r, rout, step, glue);
 }
 
 __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr) {
@@ -107,10 +128,32 @@ __device__ __forceinline__ int group_of(const SkArgs& a, int col) {
   return g;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kSkThreads, 1)
+// The logistic function as glue.cu computes it (fast exponential and
+// division: the IEEE division dominated the fused kernels' time).
+__device__ __forceinline__ float sk_sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[2 * e] = bf16_lo(w[e]);
+    f[2 * e + 1] = bf16_hi(w[e]);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// GLUE: 0 plain pass over a TMA-loaded Q; 1 / 2 the fused SwiGLU forward /
+// backward (map_x1, map_x2: u, or g and u; map_q: g, or dm).
+template <int MODE, int GLUE>
+__global__ void __launch_bounds__(sk_threads(GLUE), 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w,
+                  const __grid_constant__ CUtensorMap map_x1, const __grid_constant__ CUtensorMap map_x2,
                   const SkArgs a) {
+  static_assert(GLUE == 0 || (GLUE == 1 && MODE == kSkKA) || (GLUE == 2 && MODE == kSkKB), "skinny_kernel glue");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = ptx::align1024(smem_raw);
   const int r = a.r;
@@ -121,7 +164,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int op_half = n_mma * 128;  // one 64-wide K chunk of the skinny operand
   const int q_bytes = sk_q_bytes(step);
   const int op_bytes = sk_op_bytes(MODE, a.R, a.rout, step);
-  const int raw_bytes = sk_raw_bytes(MODE, r, a.rout, step);
+  const int raw_bytes = sk_raw_bytes(MODE, r, a.rout, step, GLUE);
   const int ncols = MODE == kSkM ? a.rout : a.R;  // result columns per row of the accumulator
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint64_t* full = bars;                      // TMA bytes of the stage landed
@@ -150,7 +193,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       ptx::mbar_init(&full[i], 1);
-      ptx::mbar_init(&conv[i], 4);
+      ptx::mbar_init(&conv[i], (sk_threads(GLUE) - 64) / 32);
       ptx::mbar_init(&empty[i], 1);
     }
     ptx::mbar_init(acc_full, 1);
@@ -158,6 +201,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&map_q);
     ptx::tma_prefetch_desc(&map_w);
+    if (GLUE >= 1) ptx::tma_prefetch_desc(&map_x1);
+    if (GLUE == 2) ptx::tma_prefetch_desc(&map_x2);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, kSkTmemCols);
@@ -178,7 +223,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint32_t tx = q_bytes + (MODE == kSkKA ? nh * op_half : raw_bytes);
+      const uint32_t tx = q_bytes + (MODE == kSkKA ? nh * op_half : 0) + raw_bytes;
       int j = 0;
       for (; j < nloc; ++j) {
         const int st = j % S;
@@ -189,7 +234,21 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const int k0 = (s0 + j) * step;
         uint8_t* q = sQ + st * q_bytes;
         ptx::mbar_arrive_expect_tx(&full[st], tx);
-        if (MODE != kSkM) {  // Q [128 rows x step], 64-wide halves 16 KB apart
+        if (GLUE == 1) {  // g into the Q stage (m is written over it), u into the raw region, A_cat rows
+          for (int h = 0; h < nh; ++h) {
+            ptx::tma_load_2d(q + h * 16384, &map_q, &full[st], k0 + 64 * h, base);
+            ptx::tma_load_2d(sRaw + st * raw_bytes + h * 16384, &map_x1, &full[st], k0 + 64 * h, base);
+            ptx::tma_load_2d(sOp + st * op_bytes + h * op_half, &map_w, &full[st], k0 + 64 * h, 0);
+          }
+        } else if (GLUE == 2) {  // step j: columns c .. c+63 of dg then du; u / g tiles become dg / du
+          const int c = (s0 + j) * 64;
+          uint8_t* raw = sRaw + st * raw_bytes;
+          ptx::tma_load_2d(q, &map_x2, &full[st], c, base);
+          ptx::tma_load_2d(q + 16384, &map_x1, &full[st], c, base);
+          ptx::tma_load_2d(raw, &map_q, &full[st], c, base);
+          ptx::tma_load_2d(raw + 16384, &map_w, &full[st], 0, c);
+          ptx::tma_load_2d(raw + 16384 + 64 * r * 2, &map_w, &full[st], 0, a.F + c);
+        } else if (MODE != kSkM) {  // Q [128 rows x step], 64-wide halves 16 KB apart
           for (int h = 0; h < nh; ++h) ptx::tma_load_2d(q + h * 16384, &map_q, &full[st], k0 + 64 * h, base);
           if (MODE == kSkKA)
             for (int h = 0; h < nh; ++h)
@@ -215,7 +274,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const int st = j % S;
         const uint32_t ph = (j / S) & 1;
         if (!ptx::mbar_wait(&full[st], ph, abort_flag) ||
-            (MODE != kSkKA && !ptx::mbar_wait(&conv[st], ph, abort_flag))) {
+            ((MODE != kSkKA || GLUE != 0) && !ptx::mbar_wait(&conv[st], ph, abort_flag))) {
           give_up();
           break;
         }
@@ -237,8 +296,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     }
   } else {
     // ------------------------------------ converters (modes KB, M), then epilogue
-    const int e = tid - 64;  // 0..127
-    if (MODE != kSkKA) {
+    const int e = tid - 64;  // 0 .. NT-1
+    constexpr int NT = sk_threads(GLUE) - 64;
+    if (MODE != kSkKA || GLUE != 0) {
       for (int j = 0; j < nloc; ++j) {
         const int st = j % S;
         if (!ptx::mbar_wait(&full[st], (j / S) & 1, abort_flag)) {
@@ -246,9 +306,69 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           break;
         }
         uint8_t* op = sOp + st * op_bytes;
-        const uint8_t* raw = sRaw + st * raw_bytes;
+        uint8_t* raw = sRaw + st * raw_bytes;
+        uint8_t* q = sQ + st * q_bytes;
         const int nch = step / 8;  // 8-element chunks of the step
-        if (MODE == kSkKB) {
+        if (GLUE == 1) {
+          // m = bf16(SiLU(g) u) over the g tile; eight consecutive threads
+          // take one row's eight chunks of a 64-column half (one 128-byte
+          // global segment, eight different banks)
+          const int k0 = (s0 + j) * step;
+          for (int task = e; task < 128 * nch; task += NT) {
+            const int h = task / (128 * 8), row = (task >> 3) & 127, c8 = task & 7;
+            const int off = h * 16384 + row * 128 + ((c8 ^ (row & 7)) << 4);
+            float fg[8], fu[8], fm[8];
+            unpack8(*reinterpret_cast<const uint4*>(q + off), fg);
+            unpack8(*reinterpret_cast<const uint4*>(raw + off), fu);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) fm[i] = fg[i] * sk_sigmoid(fg[i]) * fu[i];
+            const uint4 v = pack8(fm);
+            *reinterpret_cast<uint4*>(q + off) = v;
+            const int64_t gm = base + row;
+            const int col = k0 + h * 64 + c8 * 8;
+            if (gm < a.M && col < a.C) *reinterpret_cast<uint4*>(a.glue0 + gm * a.glue_ld + col) = v;
+          }
+        } else if (GLUE == 2) {
+          // dg over the u tile (K half 0), du over the g tile (K half 1)
+          const int c = (s0 + j) * 64;
+          for (int task = e; task < 128 * 8; task += NT) {
+            const int row = task >> 3, c8 = task & 7;
+            const int off = row * 128 + ((c8 ^ (row & 7)) << 4);
+            float fdm[8], fg[8], fu[8], odg[8], odu[8];
+            unpack8(*reinterpret_cast<const uint4*>(raw + off), fdm);
+            unpack8(*reinterpret_cast<const uint4*>(q + 16384 + off), fg);
+            unpack8(*reinterpret_cast<const uint4*>(q + off), fu);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float sg = sk_sigmoid(fg[i]);
+              odg[i] = fdm[i] * fu[i] * sg * (1.0f + fg[i] * (1.0f - sg));
+              odu[i] = fdm[i] * fg[i] * sg;
+            }
+            const uint4 vg = pack8(odg), vu = pack8(odu);
+            *reinterpret_cast<uint4*>(q + off) = vg;
+            *reinterpret_cast<uint4*>(q + 16384 + off) = vu;
+            const int64_t gm = base + row;
+            const int col = c + c8 * 8;
+            if (gm < a.M && col < a.F) {
+              *reinterpret_cast<uint4*>(a.glue0 + gm * a.glue_ld + col) = vg;
+              *reinterpret_cast<uint4*>(a.glue1 + gm * a.glue_ld + col) = vu;
+            }
+          }
+          // operand rows i (K half 0) = B_g[c + k][i], rows r + i (K half 1) = B_u[c + k][i]; zero elsewhere
+          const uint16_t* rb = reinterpret_cast<const uint16_t*>(raw + 16384);
+          for (int task = e; task < n_mma * 16; task += NT) {
+            const int row = task % n_mma, ch = task / n_mma, h = ch >> 3;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            const int i = row - h * r;
+            if (i >= 0 && i < r) {
+              const uint16_t* pb = rb + h * 64 * r + ((ch & 7) * 8) * r + i;
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq)
+                w[qq] = static_cast<uint32_t>(pb[(2 * qq) * r]) | (static_cast<uint32_t>(pb[(2 * qq + 1) * r]) << 16);
+            }
+            *sw128_chunk(op + h * op_half, row, ch & 7) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else if (MODE == kSkKB) {
           // raw: B_cat rows k0 .. k0+step-1 (r bf16 each), all of group g;
           // operand rows g r + i = B[k][i], every other row zero
           const int g0 = group_of(a, (s0 + j) * step) * r;
@@ -290,9 +410,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&conv[st]);
       }
     }
-    // epilogue: TMEM lane `row` holds this CTA's partial for row `row` of
-    // the 128 block; result columns are read 32 at a time (mode M adds the
-    // lo half from column lo_col + c)
+    // epilogue (warps 2..5): TMEM lane `row` holds this CTA's partial for
+    // row `row` of the 128 block; result columns are read 32 at a time
+    // (mode M adds the lo half from column lo_col + c)
+    if (warp < 6) {
     bool ready = ptx::mbar_wait(acc_full, 0, abort_flag) && !*abort_flag;
     ready = __all_sync(0xffffffffu, ready);
     if (!ready && !*abort_flag) give_up();
@@ -348,6 +469,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             *reinterpret_cast<float4*>(dst + i4 * 4) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
       }
     }
+    }
   }
 
   ptx::tc_fence_before();
@@ -360,7 +482,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int r0 = rank * 128 / cs, nrows = (rank + 1) * 128 / cs - r0;
     const int nq = ncols / 4;
     const bool by_col = MODE == kSkM && a.transpose;  // dA: rows vary fastest for coalesced stores
-    for (int task = tid; task < nrows * nq; task += kSkThreads) {
+    for (int task = tid; task < nrows * nq; task += sk_threads(GLUE)) {
       const int rl = by_col ? task % nrows : task / nq;
       const int i4 = by_col ? task / nrows : task % nq;
       const int row = r0 + rl;
@@ -417,11 +539,15 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 // ------------------------------------------------------------------ host side
 namespace {
 
-// Step width and pipeline depth: the pair with the most Q bytes in flight.
-void choose_pipeline(int mode, int r, int R, int rout, SkArgs& a) {
+// Step width and pipeline depth: the pair with the most Q bytes in flight
+// (the fused SwiGLU backward's paired steps are 128 wide; the forward takes
+// 64-wide steps, the deeper ring).
+void choose_pipeline(int mode, int r, int R, int rout, SkArgs& a, int glue = 0) {
   int best = -1;
   for (int step : {128, 64}) {
-    const int s = std::min(kSkMaxStages, kSkSmemBudget / sk_stage_bytes(mode, r, R, rout, step));
+    if (glue == 2 && step != 128) continue;
+    if (glue == 1 && step != 64) continue;  // six stages of g, u tiles rather than three
+    const int s = std::min(kSkMaxStages, kSkSmemBudget / sk_stage_bytes(mode, r, R, rout, step, glue));
     if (s >= 2 && s * sk_q_bytes(step) > best) {
       best = s * sk_q_bytes(step);
       a.step = step;
@@ -430,26 +556,26 @@ void choose_pipeline(int mode, int r, int R, int rout, SkArgs& a) {
   }
 }
 
-template <int MODE>
+template <int MODE, int GLUE>
 sl_status set_attributes() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(skinny_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    err = cudaFuncSetAttribute(skinny_kernel<MODE, GLUE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(skinny_kernel<MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      err = cudaFuncSetAttribute(skinny_kernel<MODE, GLUE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   return err == cudaSuccess ? SL_OK : cuda_error(err, "skinny_kernel attributes");
 }
 
-template <int MODE>
+template <int MODE, int GLUE>
 cudaLaunchConfig_t make_config(int64_t blocks, int cs, const SkArgs& a, cudaStream_t stream,
                                cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(cs), 1);
-  cfg.blockDim = dim3(kSkThreads, 1, 1);
+  cfg.blockDim = dim3(sk_threads(GLUE), 1, 1);
   cfg.dynamicSmemBytes =
-      static_cast<size_t>(1024 + kSkBarBytes + a.stages * sk_stage_bytes(MODE, a.r, a.R, a.rout, a.step));
+      static_cast<size_t>(1024 + kSkBarBytes + a.stages * sk_stage_bytes(MODE, a.r, a.R, a.rout, a.step, GLUE));
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -462,20 +588,20 @@ cudaLaunchConfig_t make_config(int64_t blocks, int cs, const SkArgs& a, cudaStre
 
 // Clusters of `cs` CTAs that the device can hold at once for this shared-
 // memory size (driver query, cached per device, size and cluster size).
-template <int MODE>
+template <int MODE, int GLUE>
 int max_active_clusters(int cs, const SkArgs& a) {
   static std::mutex mu;
   static int cache[64][64][17];  // [device][smem / 4 KB][cs], 0 = not yet asked
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_config<MODE>(1, cs, a, nullptr, attr);
+  cudaLaunchConfig_t cfg = make_config<MODE, GLUE>(1, cs, a, nullptr, attr);
   const int key = static_cast<int>(cfg.dynamicSmemBytes / 4096) & 63;
   std::lock_guard<std::mutex> lk(mu);
   int& slot = cache[dev][key][cs];
   if (slot == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, skinny_kernel<MODE>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, skinny_kernel<MODE, GLUE>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -487,11 +613,11 @@ int max_active_clusters(int cs, const SkArgs& a) {
 // Cluster size: the largest split of the reduction (at least two steps per
 // CTA) whose clusters all fit on the device at once, so that the launch is
 // one wave of at most one CTA per SM.
-template <int MODE>
+template <int MODE, int GLUE>
 int choose_split(int64_t blocks, const SkArgs& a) {
   for (int cs = 16; cs > 1; --cs) {
     if (blocks * cs > num_sms() || a.nsteps < 2 * cs) continue;
-    if (max_active_clusters<MODE>(cs, a) >= blocks) return cs;
+    if (max_active_clusters<MODE, GLUE>(cs, a) >= blocks) return cs;
   }
   return 1;
 }
@@ -504,19 +630,21 @@ double pass_bytes(int mode, const SkArgs& a) {
   return q + 4.0 * a.M * a.rout + 4.0 * a.C * a.rout * (a.accumulate ? 2 : 1);
 }
 
-template <int MODE>
+template <int MODE, int GLUE = 0>
 sl_status launch(const CUtensorMap& mq, const CUtensorMap& mw, const SkArgs& a, int64_t blocks,
-                 cudaStream_t stream) {
-  sl_status st = set_attributes<MODE>();
+                 cudaStream_t stream, const CUtensorMap* mx1 = nullptr, const CUtensorMap* mx2 = nullptr,
+                 double bytes = 0.0) {
+  sl_status st = set_attributes<MODE, GLUE>();
   if (st != SL_OK) return st;
-  const int cs = choose_split<MODE>(blocks, a);
+  const int cs = choose_split<MODE, GLUE>(blocks, a);
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_config<MODE>(blocks, cs, a, stream, attr);
+  cudaLaunchConfig_t cfg = make_config<MODE, GLUE>(blocks, cs, a, stream, attr);
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_trigger / pdl_wait
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
-  const TimingToken tt = timing_begin(MODE == kSkKA ? 6 : (MODE == kSkKB ? 7 : 8), pass_bytes(MODE, a), stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_kernel<MODE>, mq, mw, a);
+  const TimingToken tt =
+      timing_begin(MODE == kSkKA ? 6 : (MODE == kSkKB ? 7 : 8), GLUE ? bytes : pass_bytes(MODE, a), stream);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_kernel<MODE, GLUE>, mq, mw, mx1 ? *mx1 : mq, mx2 ? *mx2 : mq, a);
   timing_end(tt, stream);
   if (e != cudaSuccess) return cuda_error(e, "skinny_kernel launch");
   return check_launch("skinny_kernel");
@@ -608,6 +736,87 @@ sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r
   if (st != SL_OK) return st;
   const int64_t blocks = ceil_div(C, 128);
   return launch<kSkM>(mq, mw, a, blocks, stream);
+}
+
+sl_status skinny_swiglu_t(const uint16_t* g, const uint16_t* u, int64_t ld_in, uint16_t* m, int64_t M, int F,
+                          const uint16_t* A, int r, float* T, cudaStream_t stream) {
+  SL_REQUIRE(g && u && m && A && T && M > 0 && M < (1LL << 31), "fused SwiGLU forward: null pointer or bad M");
+  SL_REQUIRE(F % 64 == 0 && ld_in % 8 == 0 && ld_in >= F, "fused SwiGLU forward: need F % 64 == 0, ld % 8 == 0");
+  SL_REQUIRE((reinterpret_cast<uintptr_t>(m) & 15) == 0, "fused SwiGLU forward: m must be 16-byte aligned");
+  SkArgs a{};
+  sl_status st = check_groups(1, nullptr, F, r, a);
+  if (st != SL_OK) return st;
+  int* err = device_error_word();
+  if (!err) return SL_ERR_CUDA;
+  a.M = static_cast<int>(M);
+  a.C = F;
+  a.rout = a.R;
+  choose_pipeline(kSkKA, r, a.R, a.rout, a, 1);
+  a.nsteps = static_cast<int>(ceil_div(F, a.step));
+  a.s = 1.0f;
+  a.out = T;
+  a.err = err;
+  a.glue0 = m;
+  a.glue_ld = F;
+  CUtensorMap mg, mu, mw;
+  st = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g, F, M, static_cast<uint64_t>(ld_in) * 2, 64, 128,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  st = make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, F, M, static_cast<uint64_t>(ld_in) * 2, 64, 128,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, F, a.R, static_cast<uint64_t>(F) * 2, 64,
+                sk_n_mma(kSkKA, a.R, a.rout), CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  // g and u read, m written, A read, T written
+  const double bytes = 6.0 * static_cast<double>(M) * F + 2.0 * r * F + 4.0 * static_cast<double>(M) * r;
+  return launch<kSkKA, 1>(mg, mw, a, ceil_div(M, 128), stream, &mu, nullptr, bytes);
+}
+
+sl_status skinny_swiglu_u(const uint16_t* dm, const uint16_t* g, const uint16_t* u, int64_t ld_in, uint16_t* dg,
+                          uint16_t* du, int64_t ld_out, int64_t M, int F, const uint16_t* B_cat, int r, float* U,
+                          cudaStream_t stream) {
+  SL_REQUIRE(dm && g && u && dg && du && B_cat && U && M > 0 && M < (1LL << 31),
+             "fused SwiGLU backward: null pointer or bad M");
+  SL_REQUIRE(F % 128 == 0 && ld_in % 8 == 0 && ld_out % 8 == 0 && ld_in >= F && ld_out >= F,
+             "fused SwiGLU backward: need F % 128 == 0 and row strides % 8 == 0");
+  SL_REQUIRE(((reinterpret_cast<uintptr_t>(dg) | reinterpret_cast<uintptr_t>(du)) & 15) == 0,
+             "fused SwiGLU backward: dg and du must be 16-byte aligned");
+  SkArgs a{};
+  const int bounds[3] = {0, F, 2 * F};
+  sl_status st = check_groups(2, bounds, 2 * F, r, a);
+  if (st != SL_OK) return st;
+  int* err = device_error_word();
+  if (!err) return SL_ERR_CUDA;
+  a.M = static_cast<int>(M);
+  a.C = 2 * F;
+  a.F = F;
+  a.rout = a.R;
+  choose_pipeline(kSkKB, r, a.R, a.rout, a, 2);
+  a.nsteps = F / 64;
+  a.s = 1.0f;
+  a.out = U;
+  a.err = err;
+  a.glue0 = dg;
+  a.glue1 = du;
+  a.glue_ld = ld_out;
+  CUtensorMap mdm, mg, mu, mw;
+  st = make_map(&mdm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dm, F, M, static_cast<uint64_t>(F) * 2, 64, 128,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  st = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g, F, M, static_cast<uint64_t>(ld_in) * 2, 64, 128,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  st = make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, F, M, static_cast<uint64_t>(ld_in) * 2, 64, 128,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SL_OK) return st;
+  // B_cat [2F, r]: raw 64 x r tiles of B_g (rows c ..) and B_u (rows F + c ..)
+  st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B_cat, r, 2 * F, static_cast<uint64_t>(r) * 2, r, 64,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != SL_OK) return st;
+  // dm, g, u read, dg and du written, B read, U written
+  const double bytes = 10.0 * static_cast<double>(M) * F + 4.0 * r * F + 8.0 * static_cast<double>(M) * r;
+  return launch<kSkKB, 2>(mdm, mw, a, ceil_div(M, 128), stream, &mg, &mu, bytes);
 }
 
 }  // namespace sl

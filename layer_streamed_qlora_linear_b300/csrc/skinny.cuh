@@ -21,5 +21,15 @@ sl_status skinny_down(const uint16_t* Q, int64_t M, int C, const uint16_t* W, in
 //               out [C, r] (transpose = 0, dB_cat).
 sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, int G, const int* bounds, int select,
                       float s, float* out, int transpose, int accumulate, cudaStream_t stream);
+// The SwiGLU step fused with the rank-r pass over its output (bitwise the
+// output of glue_swiglu_fwd / glue_swiglu_bwd):
+//   m [M, F] = bf16(SiLU(g) u) and T [M, r] = m A^T   (g, u at row stride ld_in);
+sl_status skinny_swiglu_t(const uint16_t* g, const uint16_t* u, int64_t ld_in, uint16_t* m, int64_t M, int F,
+                          const uint16_t* A, int r, float* T, cudaStream_t stream);
+//   dg, du [M, F] (row stride ld_out) from dm [M, F] (dense), g, u, and
+//   U [M, 2 r] = [dg | du] blockdiag(B_g, B_u) with B_cat = [B_g; B_u] [2F, r].
+sl_status skinny_swiglu_u(const uint16_t* dm, const uint16_t* g, const uint16_t* u, int64_t ld_in, uint16_t* dg,
+                          uint16_t* du, int64_t ld_out, int64_t M, int F, const uint16_t* B_cat, int r, float* U,
+                          cudaStream_t stream);
 
 }  // namespace sl

@@ -28,6 +28,7 @@
 #include "glue.cuh"
 #include "gemm.cuh"
 #include "linear.cuh"
+#include "skinny.cuh"
 
 using namespace sl;
 
@@ -376,18 +377,24 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   }
   SL_TRY(linear_fwd_x(&w[3], a, M, A(3), B(3), r, c.alpha, o, c.at<float>(P.To[l]), spl, spb, c.stream));
   SL_TRY(glue_rms_fwd(h_in, o, h1, x2, c.at<float>(P.rstd2[l]), norms[1], M, D, c.stream));
-  // gate, up
+  // gate, up; m = SiLU(g) u, fused with the down adapter's T = m A^T when it has one
+  const bool fuse_t = A(6) && B(6) && F % 64 == 0;
+  auto swiglu = [&](const uint16_t* g, const uint16_t* u, int64_t ld) {
+    return fuse_t ? skinny_swiglu_t(g, u, ld, m, M, F, static_cast<const uint16_t*>(A(6)), r,
+                                    c.at<float>(P.Td[l]), c.stream)
+                  : glue_swiglu_fwd(g, u, m, M, F, ld, c.stream);
+  };
   if (c.group_gu) {
     const sl_weight wg = group_weight(w, 4, 2);
     const int64_t Ng[2] = {F, F};
     SL_TRY(group_fwd_x(&wg, 2, Ng, x2, M, A(4), B(4), r, c.alpha, gu, Tgu, spl, spb, c.stream));
-    SL_TRY(glue_swiglu_fwd(gu, gu + F, m, M, F, 2 * F, c.stream));
+    SL_TRY(swiglu(gu, gu + F, 2 * F));
   } else {
     SL_TRY(linear_fwd_x(&w[4], x2, M, A(4), B(4), r, c.alpha, gu, Tgu, spl, spb, c.stream));
     SL_TRY(linear_fwd_x(&w[5], x2, M, A(5), B(5), r, c.alpha, gu + M * F, Tgu + M * rr, spl, spb, c.stream));
-    SL_TRY(glue_swiglu_fwd(gu, gu + M * F, m, M, F, F, c.stream));
+    SL_TRY(swiglu(gu, gu + M * F, F));
   }
-  SL_TRY(linear_fwd_x(&w[6], m, M, A(6), B(6), r, c.alpha, d, c.at<float>(P.Td[l]), spl, spb, c.stream));
+  SL_TRY(linear_fwd_x(&w[6], m, M, A(6), B(6), r, c.alpha, d, c.at<float>(P.Td[l]), spl, spb, c.stream, fuse_t));
   SL_TRY(glue_resid_add(h1, d, h_out, M * s->D, c.stream));
   return SL_OK;
 }
@@ -447,12 +454,18 @@ sl_status layer_bwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   // gate, up
   SL_TRY(wait_unit(kGU));
   if (c.group_gu) {
-    SL_TRY(glue_swiglu_bwd(dm, gu, gu + F, dgu, dgu + F, M, F, 2 * F, c.stream));
+    // dg, du fused with the group's U_cat = [dg | du] blockdiag(B_g, B_u) when it has adapters
+    const bool fuse_u = A(4) && B(4) && F % 128 == 0;
+    if (fuse_u)
+      SL_TRY(skinny_swiglu_u(dm, gu, gu + F, 2 * F, dgu, dgu + F, 2 * F, M, F, static_cast<const uint16_t*>(B(4)), r,
+                             reinterpret_cast<float*>(U_of(kGU, 0)), c.stream));
+    else
+      SL_TRY(glue_swiglu_bwd(dm, gu, gu + F, dgu, dgu + F, M, F, 2 * F, c.stream));
     const sl_weight wg = group_weight(w, 4, 2);
     const int64_t Ng[2] = {F, F};
     const GradSide sd = side(kGU);
     SL_TRY(group_bwd_split(&wg, 2, Ng, x2, dgu, M, A(4), B(4), r, c.alpha, Tgu, dx2a, dA(4), dB(4), c.accumulate,
-                           U_of(kGU, 0), P.U_bytes[kGU], c.stream, &sd, spl, spb));
+                           U_of(kGU, 0), P.U_bytes[kGU], c.stream, &sd, spl, spb, fuse_u));
     SL_TRY(wait_unit(kO));
     SL_TRY(glue_rms_bwd(dh2, dx2a, nullptr, nullptr, nullptr, c.at<float>(P.h1[l]), c.at<float>(P.rstd2[l]),
                         norms[1], dh1, do_, M, D, c.stream));
