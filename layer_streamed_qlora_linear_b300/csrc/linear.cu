@@ -262,8 +262,7 @@ sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A
 }
 
 sl_status linear_fwd_x(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
-                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream,
-                       bool t_ready) {
+                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream) {
   sl_status st = check_weight(w);
   if (st != SL_OK) return st;
   SL_REQUIRE(X && Y && M > 0, "sl_lora_linear_fwd: null X/Y or M <= 0");
@@ -274,7 +273,7 @@ sl_status linear_fwd_x(const sl_weight* w, const void* X, int64_t M, const void*
   if (st != SL_OK) return st;
   int* err = device_error_word();
   if (!err) return SL_ERR_CUDA;
-  if (lora && !t_ready) {
+  if (lora) {
     st = skinny_down(static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), static_cast<const uint16_t*>(A), 0, r,
                      1, nullptr, static_cast<float*>(T_save), stream);
     if (st != SL_OK) return st;
@@ -359,12 +358,11 @@ sl_status linear_bwd_split(const sl_weight* w, const void* X, const void* dY, in
   if (lora) {
     const float s = alpha / static_cast<float>(r);
     cudaStream_t gs = side ? side->stream : stream;
-    // dA [r, K] = s U^T X;  dB [N, r] = s dY^T T
-    st = skinny_grad(U, static_cast<const uint16_t*>(X), M, static_cast<int>(w->K), r, 1, nullptr, 0, s, dA, 1,
-                     accumulate, gs);
-    if (st != SL_OK) return st;
-    st = skinny_grad(static_cast<const float*>(T_save), static_cast<const uint16_t*>(dY), M, static_cast<int>(w->N), r,
-                     1, nullptr, 1, s, dB, 0, accumulate, gs);
+    // dA [r, K] = s U^T X;  dB [N, r] = s dY^T T  (one launch)
+    const GradPass pa{U, static_cast<const uint16_t*>(X), static_cast<int>(w->K), nullptr, 0, dA, 1};
+    const GradPass pb{static_cast<const float*>(T_save), static_cast<const uint16_t*>(dY), static_cast<int>(w->N),
+                      nullptr, 1, dB, 0};
+    st = skinny_grad_pair(pa, pb, M, r, 1, s, accumulate, gs);
     if (st != SL_OK) return st;
     if (side && side->done) SL_CHECK_CUDA(cudaEventRecord(side->done, gs));
   }
@@ -540,11 +538,10 @@ sl_status group_bwd_split(const sl_weight* w, int G, const int64_t* N_g, const v
   }
   if (!lora) return SL_OK;
   cudaStream_t gs = side ? side->stream : stream;
-  // dA_cat [G r, K] = s U_cat^T X;  dB_cat [sum N_g, r]: rows of projection g = s dY_g^T T_g
-  st = skinny_grad(U, static_cast<const uint16_t*>(X), M, K, r, G, nullptr, 0, s, dA_cat, 1, accumulate, gs);
-  if (st != SL_OK) return st;
-  st = skinny_grad(static_cast<const float*>(T_cat), static_cast<const uint16_t*>(dY_cat), M, NN, r, G, bounds, 1, s,
-                   dB_cat, 0, accumulate, gs);
+  // dA_cat [G r, K] = s U_cat^T X;  dB_cat [sum N_g, r]: rows of projection g = s dY_g^T T_g  (one launch)
+  const GradPass pa{U, static_cast<const uint16_t*>(X), K, nullptr, 0, dA_cat, 1};
+  const GradPass pb{static_cast<const float*>(T_cat), static_cast<const uint16_t*>(dY_cat), NN, bounds, 1, dB_cat, 0};
+  st = skinny_grad_pair(pa, pb, M, r, G, s, accumulate, gs);
   if (st != SL_OK) return st;
   if (side && side->done) SL_CHECK_CUDA(cudaEventRecord(side->done, gs));
   return SL_OK;

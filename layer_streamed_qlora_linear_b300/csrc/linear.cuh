@@ -8,12 +8,9 @@ namespace sl {
 
 sl_status linear_fwd(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
                      float alpha, void* Y, void* T_save, void* ws, size_t ws_bytes, cudaStream_t stream);
-// The forward with the GEMM's split-K scratch given directly (nullptr: none);
-// t_ready: T_save already holds X A^T (written by a fused producer), so the
-// T pass is skipped.
+// The forward with the GEMM's split-K scratch given directly (nullptr: none).
 sl_status linear_fwd_x(const sl_weight* w, const void* X, int64_t M, const void* A, const void* B, int r,
-                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream,
-                       bool t_ready = false);
+                       float alpha, void* Y, void* T_save, void* split_ws, size_t split_bytes, cudaStream_t stream);
 sl_status linear_bwd(const sl_weight* w, const void* X, const void* dY, int64_t M, const void* A, const void* B,
                      int r, float alpha, const void* T_save, void* dX, float* dA, float* dB, int accumulate,
                      void* ws, size_t ws_bytes, cudaStream_t stream);

@@ -24,18 +24,19 @@
 //     two-term bf16 split of the fp32 operand (U or T) written by the
 //     converter warps (hi in D columns 0.., lo from the next multiple of 32), so
 //     D = Q^T P to fp32 accuracy.
-// Two variants fuse the SwiGLU step of the layer into the pass that reads
-// its output, so that output is written once and never read back:
-//   GLUE = 1 (mode K, A_cat): m = SiLU(g) u from g, u tiles; T = m A^T;
-//   GLUE = 2 (mode K, blockdiag(B)^T): dg = dm u s (1 + g (1 - s)) and
-//            du = dm g s (s = sigmoid(g)) from dm, g, u tiles; each step is
-//            64 columns of dg followed by the same 64 columns of du, and
-//            U = [dg | du] blockdiag(B_g, B_u).
-// The converter warps compute the glue from the TMA-staged inputs in the
-// same 128-byte-swizzled positions, write the result over an input tile
-// (which becomes the MMA operand) and store it to global memory; the glue
-// arithmetic is the elementwise kernels' (glue.cu), expression for
-// expression, so the stored tensors are bitwise the same.
+// One variant fuses the SwiGLU backward into the U pass that reads its
+// output, so dY of the gate/up group is written once and never read back
+// (GLUE = 2, mode K with blockdiag(B)^T): dg = dm u s (1 + g (1 - s)) and
+// du = dm g s (s = sigmoid(g)) from dm, g, u tiles, each step 64 columns of
+// dg followed by the same 64 columns of du, and U = [dg | du]
+// blockdiag(B_g, B_u).  Sixteen converter warps compute the glue from the
+// TMA-staged inputs in the same 128-byte-swizzled positions, write it over
+// the u and g tiles (which become the MMA operand) and store it to global
+// memory; the arithmetic is glue.cu's, expression for expression, so dg and
+// du are bitwise the elementwise kernel's.  (The same fusion of the forward,
+// m = SiLU(g) u with the down adapter's T = m A^T, measured slower than the
+// two separate kernels: 28.9 against 12.1 + 11.4 us at M = 1024, F = 14336,
+// and is not built.)
 // The long reduction is split over the CTAs of a thread-block cluster (up to
 // 16, sized so that the grid is one wave); their fp32 partials are summed
 // through distributed shared memory in rank order, so one launch writes the
@@ -55,9 +56,9 @@ namespace sl {
 enum SkMode { kSkKA = 0, kSkKB = 1, kSkM = 2 };
 
 // warp 0 TMA, warp 1 MMA, warps 2..5 converters + epilogue; the fused
-// SwiGLU variants add twelve converter warps for the glue arithmetic
+// SwiGLU backward adds twelve converter warps for the glue arithmetic
 constexpr int kSkThreads = 192;
-__host__ __device__ constexpr int sk_threads(int glue) { return glue ? 64 + 512 : kSkThreads; }
+__host__ __device__ constexpr int sk_threads(int glue) { return glue == 2 ? 64 + 512 : kSkThreads; }
 constexpr int kSkMaxStages = 8;
 constexpr int kSkTmemCols = 128;
 constexpr int kSkBarBytes = 1024; // barriers + misc, ahead of the 1024-aligned data
@@ -81,10 +82,11 @@ struct SkArgs {
   int accumulate;  // mode M: out += result
   float* out;
   int* err;
-  uint16_t* glue0;  // GLUE 1: m [M, C]; GLUE 2: dg
+  uint16_t* glue0;  // GLUE 2: dg
   uint16_t* glue1;  // GLUE 2: du
   int64_t glue_ld;  // row stride of glue0 / glue1 (elements)
   int F;            // GLUE 2: columns of dg (= of du); C = 2 F
+  int nb0;          // GLUE 3: blocks of the first pass (the rest run the second)
 };
 
 // Mode M: first D column of the lo half (32-aligned, so TMEM loads of
@@ -99,7 +101,6 @@ __host__ __device__ inline int sk_op_bytes(int mode, int R, int rout, int step) 
   return sk_n_mma(mode, R, rout) * step * 2;
 }
 __host__ __device__ inline int sk_raw_bytes(int mode, int r, int rout, int step, int glue = 0) {
-  if (glue == 1) return sk_q_bytes(step);                  // the u tile
   if (glue == 2) return sk_q_bytes(64) + step * r * 2;     // the dm tile + B_g, B_u rows of the step
   return mode == kSkKA ? 0 : (mode == kSkKB ? step * r * 2 : step * rout * 4);
 }
@@ -146,14 +147,21 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16x2(f[6], f[7]));
 }
 
-// GLUE: 0 plain pass over a TMA-loaded Q; 1 / 2 the fused SwiGLU forward /
-// backward (map_x1, map_x2: u, or g and u; map_q: g, or dm).
+// GLUE: 0 plain pass over a TMA-loaded Q; 2 the fused SwiGLU backward
+// (map_q: dm, map_x1: g, map_x2: u); 3 two mode-M passes in one launch (dA
+// and dB of one backward): the blocks from a0.nb0 on run the second with
+// map_x1, map_x2 and a1.
 template <int MODE, int GLUE>
 __global__ void __launch_bounds__(sk_threads(GLUE), 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w,
                   const __grid_constant__ CUtensorMap map_x1, const __grid_constant__ CUtensorMap map_x2,
-                  const SkArgs a) {
-  static_assert(GLUE == 0 || (GLUE == 1 && MODE == kSkKA) || (GLUE == 2 && MODE == kSkKB), "skinny_kernel glue");
+                  const SkArgs a0, const SkArgs a1) {
+  static_assert(GLUE == 0 || (GLUE == 2 && MODE == kSkKB) || (GLUE == 3 && MODE == kSkM),
+                "skinny_kernel glue");
+  const bool second = GLUE == 3 && static_cast<int>(blockIdx.x) >= a0.nb0;
+  const SkArgs& a = second ? a1 : a0;
+  const CUtensorMap* mq = second ? &map_x1 : &map_q;
+  const CUtensorMap* mw = second ? &map_x2 : &map_w;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = ptx::align1024(smem_raw);
   const int r = a.r;
@@ -186,7 +194,8 @@ __global__ void __launch_bounds__(sk_threads(GLUE), 1)
   const int s0 = static_cast<int>(static_cast<int64_t>(a.nsteps) * rank / cs);
   const int s1 = static_cast<int>(static_cast<int64_t>(a.nsteps) * (rank + 1) / cs);
   const int nloc = s1 - s0;
-  const int base = static_cast<int>(blockIdx.x) * 128;  // rows of Q (mode K) or columns of Q (mode M)
+  // rows of Q (mode K) or columns of Q (mode M)
+  const int base = (static_cast<int>(blockIdx.x) - (second ? a0.nb0 : 0)) * 128;
   // mode M with select: this column block's adapter g reads P columns g r ..
   const int p_col0 = (MODE == kSkM && a.select) ? group_of(a, base) * r : 0;
 
@@ -199,10 +208,12 @@ __global__ void __launch_bounds__(sk_threads(GLUE), 1)
     ptx::mbar_init(acc_full, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
-    ptx::tma_prefetch_desc(&map_q);
-    ptx::tma_prefetch_desc(&map_w);
-    if (GLUE >= 1) ptx::tma_prefetch_desc(&map_x1);
-    if (GLUE == 2) ptx::tma_prefetch_desc(&map_x2);
+    ptx::tma_prefetch_desc(mq);
+    ptx::tma_prefetch_desc(mw);
+    if (GLUE == 2) {
+      ptx::tma_prefetch_desc(&map_x1);
+      ptx::tma_prefetch_desc(&map_x2);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, kSkTmemCols);
@@ -234,13 +245,7 @@ __global__ void __launch_bounds__(sk_threads(GLUE), 1)
         const int k0 = (s0 + j) * step;
         uint8_t* q = sQ + st * q_bytes;
         ptx::mbar_arrive_expect_tx(&full[st], tx);
-        if (GLUE == 1) {  // g into the Q stage (m is written over it), u into the raw region, A_cat rows
-          for (int h = 0; h < nh; ++h) {
-            ptx::tma_load_2d(q + h * 16384, &map_q, &full[st], k0 + 64 * h, base);
-            ptx::tma_load_2d(sRaw + st * raw_bytes + h * 16384, &map_x1, &full[st], k0 + 64 * h, base);
-            ptx::tma_load_2d(sOp + st * op_bytes + h * op_half, &map_w, &full[st], k0 + 64 * h, 0);
-          }
-        } else if (GLUE == 2) {  // step j: columns c .. c+63 of dg then du; u / g tiles become dg / du
+        if (GLUE == 2) {  // step j: columns c .. c+63 of dg then du; u / g tiles become dg / du
           const int c = (s0 + j) * 64;
           uint8_t* raw = sRaw + st * raw_bytes;
           ptx::tma_load_2d(q, &map_x2, &full[st], c, base);
@@ -249,16 +254,16 @@ __global__ void __launch_bounds__(sk_threads(GLUE), 1)
           ptx::tma_load_2d(raw + 16384, &map_w, &full[st], 0, c);
           ptx::tma_load_2d(raw + 16384 + 64 * r * 2, &map_w, &full[st], 0, a.F + c);
         } else if (MODE != kSkM) {  // Q [128 rows x step], 64-wide halves 16 KB apart
-          for (int h = 0; h < nh; ++h) ptx::tma_load_2d(q + h * 16384, &map_q, &full[st], k0 + 64 * h, base);
+          for (int h = 0; h < nh; ++h) ptx::tma_load_2d(q + h * 16384, mq, &full[st], k0 + 64 * h, base);
           if (MODE == kSkKA)
             for (int h = 0; h < nh; ++h)
-              ptx::tma_load_2d(sOp + st * op_bytes + h * op_half, &map_w, &full[st], k0 + 64 * h, 0);
+              ptx::tma_load_2d(sOp + st * op_bytes + h * op_half, mw, &full[st], k0 + 64 * h, 0);
           else
-            ptx::tma_load_2d(sRaw + st * raw_bytes, &map_w, &full[st], 0, k0);
+            ptx::tma_load_2d(sRaw + st * raw_bytes, mw, &full[st], 0, k0);
         } else {  // Q rows k0 .. k0+step-1, columns base .. base+127 (two 64-column atoms); raw P rows
-          ptx::tma_load_2d(q, &map_q, &full[st], base, k0);
-          ptx::tma_load_2d(q + step * 128, &map_q, &full[st], base + 64, k0);
-          ptx::tma_load_2d(sRaw + st * raw_bytes, &map_w, &full[st], p_col0, k0);
+          ptx::tma_load_2d(q, mq, &full[st], base, k0);
+          ptx::tma_load_2d(q + step * 128, mq, &full[st], base + 64, k0);
+          ptx::tma_load_2d(sRaw + st * raw_bytes, mw, &full[st], p_col0, k0);
         }
       }
       if (*abort_flag)
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(sk_threads(GLUE), 1)
         const int st = j % S;
         const uint32_t ph = (j / S) & 1;
         if (!ptx::mbar_wait(&full[st], ph, abort_flag) ||
-            ((MODE != kSkKA || GLUE != 0) && !ptx::mbar_wait(&conv[st], ph, abort_flag))) {
+            (MODE != kSkKA && !ptx::mbar_wait(&conv[st], ph, abort_flag))) {
           give_up();
           break;
         }
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(sk_threads(GLUE), 1)
     // ------------------------------------ converters (modes KB, M), then epilogue
     const int e = tid - 64;  // 0 .. NT-1
     constexpr int NT = sk_threads(GLUE) - 64;
-    if (MODE != kSkKA || GLUE != 0) {
+    if (MODE != kSkKA) {
       for (int j = 0; j < nloc; ++j) {
         const int st = j % S;
         if (!ptx::mbar_wait(&full[st], (j / S) & 1, abort_flag)) {
@@ -309,26 +314,7 @@ __global__ void __launch_bounds__(sk_threads(GLUE), 1)
         uint8_t* raw = sRaw + st * raw_bytes;
         uint8_t* q = sQ + st * q_bytes;
         const int nch = step / 8;  // 8-element chunks of the step
-        if (GLUE == 1) {
-          // m = bf16(SiLU(g) u) over the g tile; eight consecutive threads
-          // take one row's eight chunks of a 64-column half (one 128-byte
-          // global segment, eight different banks)
-          const int k0 = (s0 + j) * step;
-          for (int task = e; task < 128 * nch; task += NT) {
-            const int h = task / (128 * 8), row = (task >> 3) & 127, c8 = task & 7;
-            const int off = h * 16384 + row * 128 + ((c8 ^ (row & 7)) << 4);
-            float fg[8], fu[8], fm[8];
-            unpack8(*reinterpret_cast<const uint4*>(q + off), fg);
-            unpack8(*reinterpret_cast<const uint4*>(raw + off), fu);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) fm[i] = fg[i] * sk_sigmoid(fg[i]) * fu[i];
-            const uint4 v = pack8(fm);
-            *reinterpret_cast<uint4*>(q + off) = v;
-            const int64_t gm = base + row;
-            const int col = k0 + h * 64 + c8 * 8;
-            if (gm < a.M && col < a.C) *reinterpret_cast<uint4*>(a.glue0 + gm * a.glue_ld + col) = v;
-          }
-        } else if (GLUE == 2) {
+        if (GLUE == 2) {
           // dg over the u tile (K half 0), du over the g tile (K half 1)
           const int c = (s0 + j) * 64;
           for (int task = e; task < 128 * 8; task += NT) {
@@ -540,13 +526,11 @@ __global__ void __launch_bounds__(sk_threads(GLUE), 1)
 namespace {
 
 // Step width and pipeline depth: the pair with the most Q bytes in flight
-// (the fused SwiGLU backward's paired steps are 128 wide; the forward takes
-// 64-wide steps, the deeper ring).
+// (the fused SwiGLU backward's paired steps are 128 wide).
 void choose_pipeline(int mode, int r, int R, int rout, SkArgs& a, int glue = 0) {
   int best = -1;
   for (int step : {128, 64}) {
     if (glue == 2 && step != 128) continue;
-    if (glue == 1 && step != 64) continue;  // six stages of g, u tiles rather than three
     const int s = std::min(kSkMaxStages, kSkSmemBudget / sk_stage_bytes(mode, r, R, rout, step, glue));
     if (s >= 2 && s * sk_q_bytes(step) > best) {
       best = s * sk_q_bytes(step);
@@ -633,7 +617,7 @@ double pass_bytes(int mode, const SkArgs& a) {
 template <int MODE, int GLUE = 0>
 sl_status launch(const CUtensorMap& mq, const CUtensorMap& mw, const SkArgs& a, int64_t blocks,
                  cudaStream_t stream, const CUtensorMap* mx1 = nullptr, const CUtensorMap* mx2 = nullptr,
-                 double bytes = 0.0) {
+                 double bytes = 0.0, const SkArgs* a2 = nullptr) {
   sl_status st = set_attributes<MODE, GLUE>();
   if (st != SL_OK) return st;
   const int cs = choose_split<MODE, GLUE>(blocks, a);
@@ -644,7 +628,28 @@ sl_status launch(const CUtensorMap& mq, const CUtensorMap& mw, const SkArgs& a, 
   cfg.numAttrs = 2;
   const TimingToken tt =
       timing_begin(MODE == kSkKA ? 6 : (MODE == kSkKB ? 7 : 8), GLUE ? bytes : pass_bytes(MODE, a), stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_kernel<MODE, GLUE>, mq, mw, mx1 ? *mx1 : mq, mx2 ? *mx2 : mq, a);
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, skinny_kernel<MODE, GLUE>, mq, mw, mx1 ? *mx1 : mq, mx2 ? *mx2 : mq, a, a2 ? *a2 : a);
+  timing_end(tt, stream);
+  if (e != cudaSuccess) return cuda_error(e, "skinny_kernel launch");
+  return check_launch("skinny_kernel");
+}
+
+// Two mode-M passes in one launch: `q` sizes the launch (shared memory,
+// cluster split); each block runs its own pass's arguments.
+sl_status launch_pair(const CUtensorMap& mq0, const CUtensorMap& mw0, const CUtensorMap& mq1, const CUtensorMap& mw1,
+                      const SkArgs& a0, const SkArgs& a1, const SkArgs& q, int64_t blocks, double bytes,
+                      cudaStream_t stream) {
+  sl_status st = set_attributes<kSkM, 3>();
+  if (st != SL_OK) return st;
+  const int cs = choose_split<kSkM, 3>(blocks, q);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = make_config<kSkM, 3>(blocks, cs, q, stream, attr);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_trigger / pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
+  const TimingToken tt = timing_begin(8, bytes, stream);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_kernel<kSkM, 3>, mq0, mw0, mq1, mw1, a0, a1);
   timing_end(tt, stream);
   if (e != cudaSuccess) return cuda_error(e, "skinny_kernel launch");
   return check_launch("skinny_kernel");
@@ -707,10 +712,13 @@ sl_status skinny_down(const uint16_t* Q, int64_t M, int C, const uint16_t* W, in
   return wt == 0 ? launch<kSkKA>(mq, mw, a, blocks, stream) : launch<kSkKB>(mq, mw, a, blocks, stream);
 }
 
-sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, int G, const int* bounds, int select,
-                      float s, float* out, int transpose, int accumulate, cudaStream_t stream) {
+namespace {
+
+// Arguments and tensor maps of one mode-M pass (dA or dB).
+sl_status prep_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, int G, const int* bounds, int select,
+                    float s, float* out, int transpose, int accumulate, SkArgs& a, CUtensorMap& mq, CUtensorMap& mw) {
   SL_REQUIRE(C % 8 == 0 && M > 0 && M < (1LL << 31), "rank-r product: need C % 8 == 0 and 0 < M < 2^31");
-  SkArgs a{};
+  a = SkArgs{};
   sl_status st = check_groups(G, bounds, C, r, a);
   if (st != SL_OK) return st;
   int* err = device_error_word();
@@ -727,50 +735,45 @@ sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r
   a.accumulate = accumulate;
   a.out = out;
   a.err = err;
-  CUtensorMap mq, mw;
   st = make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, C, M, static_cast<uint64_t>(C) * 2, 64, a.step,
                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != SL_OK) return st;
-  st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, P, a.R, M, static_cast<uint64_t>(a.R) * 4, a.rout, a.step,
-                CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st != SL_OK) return st;
-  const int64_t blocks = ceil_div(C, 128);
-  return launch<kSkM>(mq, mw, a, blocks, stream);
+  return make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, P, a.R, M, static_cast<uint64_t>(a.R) * 4, a.rout, a.step,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-sl_status skinny_swiglu_t(const uint16_t* g, const uint16_t* u, int64_t ld_in, uint16_t* m, int64_t M, int F,
-                          const uint16_t* A, int r, float* T, cudaStream_t stream) {
-  SL_REQUIRE(g && u && m && A && T && M > 0 && M < (1LL << 31), "fused SwiGLU forward: null pointer or bad M");
-  SL_REQUIRE(F % 64 == 0 && ld_in % 8 == 0 && ld_in >= F, "fused SwiGLU forward: need F % 64 == 0, ld % 8 == 0");
-  SL_REQUIRE((reinterpret_cast<uintptr_t>(m) & 15) == 0, "fused SwiGLU forward: m must be 16-byte aligned");
-  SkArgs a{};
-  sl_status st = check_groups(1, nullptr, F, r, a);
+}  // namespace
+
+sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, int G, const int* bounds, int select,
+                      float s, float* out, int transpose, int accumulate, cudaStream_t stream) {
+  SkArgs a;
+  CUtensorMap mq, mw;
+  const sl_status st = prep_grad(P, Q, M, C, r, G, bounds, select, s, out, transpose, accumulate, a, mq, mw);
   if (st != SL_OK) return st;
-  int* err = device_error_word();
-  if (!err) return SL_ERR_CUDA;
-  a.M = static_cast<int>(M);
-  a.C = F;
-  a.rout = a.R;
-  choose_pipeline(kSkKA, r, a.R, a.rout, a, 1);
-  a.nsteps = static_cast<int>(ceil_div(F, a.step));
-  a.s = 1.0f;
-  a.out = T;
-  a.err = err;
-  a.glue0 = m;
-  a.glue_ld = F;
-  CUtensorMap mg, mu, mw;
-  st = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g, F, M, static_cast<uint64_t>(ld_in) * 2, 64, 128,
-                CU_TENSOR_MAP_SWIZZLE_128B);
+  return launch<kSkM>(mq, mw, a, ceil_div(C, 128), stream);
+}
+
+sl_status skinny_grad_pair(const GradPass& p0, const GradPass& p1, int64_t M, int r, int G, float s, int accumulate,
+                           cudaStream_t stream) {
+  SkArgs a0, a1;
+  CUtensorMap mq0, mw0, mq1, mw1;
+  sl_status st = prep_grad(p0.P, p0.Q, M, p0.C, r, G, p0.bounds, p0.select, s, p0.out, p0.transpose, accumulate, a0,
+                           mq0, mw0);
   if (st != SL_OK) return st;
-  st = make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, F, M, static_cast<uint64_t>(ld_in) * 2, 64, 128,
-                CU_TENSOR_MAP_SWIZZLE_128B);
+  st = prep_grad(p1.P, p1.Q, M, p1.C, r, G, p1.bounds, p1.select, s, p1.out, p1.transpose, accumulate, a1, mq1, mw1);
   if (st != SL_OK) return st;
-  st = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, F, a.R, static_cast<uint64_t>(F) * 2, 64,
-                sk_n_mma(kSkKA, a.R, a.rout), CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != SL_OK) return st;
-  // g and u read, m written, A read, T written
-  const double bytes = 6.0 * static_cast<double>(M) * F + 2.0 * r * F + 4.0 * static_cast<double>(M) * r;
-  return launch<kSkKA, 1>(mg, mw, a, ceil_div(M, 128), stream, &mu, nullptr, bytes);
+  const int64_t b0 = ceil_div(p0.C, 128), b1 = ceil_div(p1.C, 128);
+  a0.nb0 = static_cast<int>(b0);
+  // one launch, one cluster size and the larger of the two shared-memory footprints: the cluster
+  // split and the occupancy query read the pass with the larger stages and the fewer steps
+  SkArgs q = a0;
+  if (sk_stage_bytes(kSkM, a1.r, a1.R, a1.rout, a1.step) * a1.stages >
+      sk_stage_bytes(kSkM, a0.r, a0.R, a0.rout, a0.step) * a0.stages) {
+    q = a1;
+    q.nb0 = a0.nb0;
+  }
+  q.nsteps = std::min(a0.nsteps, a1.nsteps);
+  return launch_pair(mq0, mw0, mq1, mw1, a0, a1, q, b0 + b1, pass_bytes(kSkM, a0) + pass_bytes(kSkM, a1), stream);
 }
 
 sl_status skinny_swiglu_u(const uint16_t* dm, const uint16_t* g, const uint16_t* u, int64_t ld_in, uint16_t* dg,

@@ -21,13 +21,23 @@ sl_status skinny_down(const uint16_t* Q, int64_t M, int C, const uint16_t* W, in
 //               out [C, r] (transpose = 0, dB_cat).
 sl_status skinny_grad(const float* P, const uint16_t* Q, int64_t M, int C, int r, int G, const int* bounds, int select,
                       float s, float* out, int transpose, int accumulate, cudaStream_t stream);
-// The SwiGLU step fused with the rank-r pass over its output (bitwise the
-// output of glue_swiglu_fwd / glue_swiglu_bwd):
-//   m [M, F] = bf16(SiLU(g) u) and T [M, r] = m A^T   (g, u at row stride ld_in);
-sl_status skinny_swiglu_t(const uint16_t* g, const uint16_t* u, int64_t ld_in, uint16_t* m, int64_t M, int F,
-                          const uint16_t* A, int r, float* T, cudaStream_t stream);
-//   dg, du [M, F] (row stride ld_out) from dm [M, F] (dense), g, u, and
-//   U [M, 2 r] = [dg | du] blockdiag(B_g, B_u) with B_cat = [B_g; B_u] [2F, r].
+// dA and dB of one backward (two skinny_grad passes sharing M, r, G, s and
+// accumulate) as one launch.
+struct GradPass {
+  const float* P;
+  const uint16_t* Q;
+  int C;
+  const int* bounds;
+  int select;
+  float* out;
+  int transpose;
+};
+sl_status skinny_grad_pair(const GradPass& p0, const GradPass& p1, int64_t M, int r, int G, float s, int accumulate,
+                           cudaStream_t stream);
+// The SwiGLU backward fused with the gate/up group's U pass (dg, du bitwise
+// glue_swiglu_bwd's): dg, du [M, F] (row stride ld_out) from dm [M, F]
+// (dense) and g, u (row stride ld_in), and U [M, 2 r] = [dg | du]
+// blockdiag(B_g, B_u) with B_cat = [B_g; B_u] [2F, r].
 sl_status skinny_swiglu_u(const uint16_t* dm, const uint16_t* g, const uint16_t* u, int64_t ld_in, uint16_t* dg,
                           uint16_t* du, int64_t ld_out, int64_t M, int F, const uint16_t* B_cat, int r, float* U,
                           cudaStream_t stream);

@@ -377,24 +377,18 @@ sl_status layer_fwd(StepCtx& c, int l, const sl_weight w[7], const float* const 
   }
   SL_TRY(linear_fwd_x(&w[3], a, M, A(3), B(3), r, c.alpha, o, c.at<float>(P.To[l]), spl, spb, c.stream));
   SL_TRY(glue_rms_fwd(h_in, o, h1, x2, c.at<float>(P.rstd2[l]), norms[1], M, D, c.stream));
-  // gate, up; m = SiLU(g) u, fused with the down adapter's T = m A^T when it has one
-  const bool fuse_t = A(6) && B(6) && F % 64 == 0;
-  auto swiglu = [&](const uint16_t* g, const uint16_t* u, int64_t ld) {
-    return fuse_t ? skinny_swiglu_t(g, u, ld, m, M, F, static_cast<const uint16_t*>(A(6)), r,
-                                    c.at<float>(P.Td[l]), c.stream)
-                  : glue_swiglu_fwd(g, u, m, M, F, ld, c.stream);
-  };
+  // gate, up
   if (c.group_gu) {
     const sl_weight wg = group_weight(w, 4, 2);
     const int64_t Ng[2] = {F, F};
     SL_TRY(group_fwd_x(&wg, 2, Ng, x2, M, A(4), B(4), r, c.alpha, gu, Tgu, spl, spb, c.stream));
-    SL_TRY(swiglu(gu, gu + F, 2 * F));
+    SL_TRY(glue_swiglu_fwd(gu, gu + F, m, M, F, 2 * F, c.stream));
   } else {
     SL_TRY(linear_fwd_x(&w[4], x2, M, A(4), B(4), r, c.alpha, gu, Tgu, spl, spb, c.stream));
     SL_TRY(linear_fwd_x(&w[5], x2, M, A(5), B(5), r, c.alpha, gu + M * F, Tgu + M * rr, spl, spb, c.stream));
-    SL_TRY(swiglu(gu, gu + M * F, F));
+    SL_TRY(glue_swiglu_fwd(gu, gu + M * F, m, M, F, F, c.stream));
   }
-  SL_TRY(linear_fwd_x(&w[6], m, M, A(6), B(6), r, c.alpha, d, c.at<float>(P.Td[l]), spl, spb, c.stream, fuse_t));
+  SL_TRY(linear_fwd_x(&w[6], m, M, A(6), B(6), r, c.alpha, d, c.at<float>(P.Td[l]), spl, spb, c.stream));
   SL_TRY(glue_resid_add(h1, d, h_out, M * s->D, c.stream));
   return SL_OK;
 }
