@@ -740,8 +740,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   // next kernel launches as its CTAs exit.
   pdl_wait();  // the previous kernel's writes are visible from here on
   // TMEM: S buffers at 0 / 64 (dS over them as bf16 pairs), dP at 128 / 192,
-  // dQ at 256.  A buffer is rewritten by the S MMA two blocks later, which the
-  // tensor pipe runs after the dQ MMA that reads its dS (issue order).
+  // dQ at 256, each worker's rotary row at 384 + 64 half.  A buffer is
+  // rewritten by the S MMA two blocks later, which the tensor pipe runs after
+  // the dQ MMA that reads its dS (issue order).
   auto give_up = [&]() {
     *abort_flag = 1;
     report_device_error(a.err, SL_ERR_TIMEOUT);
@@ -864,12 +865,24 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       if (!w && lane == 0 && !*abort_flag) give_up();
       return w;
     };
+    // The epilogue rotates dQ back with the row's 32 cos and 32 sin of this
+    // warp's half.  Read from global in one burst at the item's end, those
+    // loads held up the issue of the item's last dQ MMAs by ~3 us per item
+    // (the row's 16-byte pieces sit 512 bytes apart from the next row's);
+    // the first four 64-key blocks now bring four pieces each into TMEM
+    // columns 384 + 64 half .. (cos at +0, sin at +32), read back in the
+    // epilogue (an item of two blocks loads its last eight pieces there).
+    const bool rotate = a.rope != nullptr;
+    const uint32_t rope_col = lane_base + 384u + static_cast<uint32_t>(half * 64);
     bool ok = true;
     int it = 0, gb = 0;
     for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
       const Item t = item_of(item);
       const int qrow = t.qt * 128 + r;  // position in the sequence
       const float lse2 = a.lse[static_cast<int64_t>(t.h) * M + t.row0 + r] * kLog2e;
+      // 16-byte piece p of the row: cos p (p < 8) or sin p - 8, TMEM column rope_col + 4 p
+      const float4* rope_row =
+          rotate ? reinterpret_cast<const float4*>(a.rope + static_cast<int64_t>(qrow) * 128 + half * 32) : nullptr;
       // Di = rowsum(dO * O) of row r over all 128 columns (both warps of the
       // row compute it), from the item's shared tiles; half 0 stores it for
       // the dK dV kernel
@@ -903,6 +916,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           break;
         }
         ptx::tc_fence_after();
+        // pieces 4 j .. 4 j + 3 of the rotary row in the first four blocks
+        const bool rope_here = rotate && j < 4;
+        float4 rv[4];
+        if (rope_here) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rv[i] = __ldg(rope_row + (j < 2 ? 4 * j + i : 8 + 4 * j + i));
+        }
         uint32_t w[16];
         {
           uint32_t us[32], up[32];
@@ -935,10 +955,35 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ds_full[s]);
+        if (rope_here) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            ptx::tmem_st_32x32b_x4(rope_col + 4u * static_cast<uint32_t>(4 * j + i), __float_as_uint(rv[i].x),
+                                   __float_as_uint(rv[i].y), __float_as_uint(rv[i].z), __float_as_uint(rv[i].w));
+        }
       }
-      RotRow rot;  // its loads overlap the wait for the last dQ MMA
-      const bool rotate = a.rope != nullptr;
-      if (rotate) load_rot(a.rope, qrow, half, rot);
+      RotRow rot;
+      if (ok && rotate) {
+        ptx::tmem_wait_st();  // this thread's rotary pieces have landed
+        uint32_t u[32];
+        ptx::tmem_ld_32x32b_x32(rope_col, u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          rot.c[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]), __uint_as_float(u[4 * i + 2]),
+                                 __uint_as_float(u[4 * i + 3]));
+        if (t.n >= 4) {
+          ptx::tmem_ld_32x32b_x32(rope_col + 32u, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            rot.s[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                   __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rot.s[i] = __ldg(rope_row + 16 + i);
+        }
+      }
       if (!ok || !wait_all(acc_full, it & 1)) {
         ok = false;
         break;
