@@ -1055,7 +1055,11 @@ struct DkvCfg {
   static constexpr int kStage = 4 * kAtAtom64;              // Q [64][128], dO [64][128] (1024-aligned tiles)
   static constexpr int kStageBytes = kStage + 512;           // + lse and Di of the 64 rows
   static constexpr int kOffStage = kOffV + kAtTile;          // kKvStages stages
-  static constexpr int kOffLD = kOffStage + kKvStages * kStage;  // kKvStages x (lse [64], Di [64]) fp32
+  // the item's 128 rotary rows (direct dK only): four 128-byte-swizzled
+  // boxes [128 rows][32 fp32]: cos of pairs 0.., 32.., sin of pairs 0.., 32..
+  static constexpr int kOffRope = kOffStage + kKvStages * kStage;
+  static constexpr int kRopeBytes = 4 * 128 * 128;
+  static constexpr int kOffLD = kOffRope + kRopeBytes;       // kKvStages x (lse [64], Di [64]) fp32
   static constexpr int kOffBar = kOffLD + kKvStages * 512;
   static constexpr int kNumBars = 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -1065,7 +1069,8 @@ static_assert(DkvCfg::kSmem <= 232448, "dK/dV shared memory exceeds the per-CTA 
 static_assert(DqCfg::kSmem <= 232448, "dQ shared memory exceeds the per-CTA limit");
 static_assert(FwdCfg::kSmem <= 232448, "forward shared memory exceeds the per-CTA limit");
 static_assert(1 + 2 * kAtStages + 15 <= DqCfg::kNumBars, "dQ barrier count");
-static_assert(1 + 2 * kKvStages + 9 <= DkvCfg::kNumBars, "dK/dV barrier count");
+static_assert(1 + 2 * kKvStages + 11 <= DkvCfg::kNumBars, "dK/dV barrier count");
+static_assert(DkvCfg::kOffRope % 1024 == 0, "dK/dV rotary boxes must be 1024-byte aligned");
 
 // Persistent: one CTA per SM walks the (key tile, head group, sequence)
 // items, numbered heaviest first (the first key tiles are seen by the most
@@ -1076,7 +1081,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                      const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                      const __grid_constant__ CUtensorMap map_lse, const __grid_constant__ CUtensorMap map_di,
-                     const AttnArgs a, float* __restrict__ part_dk, float* __restrict__ part_dv) {
+                     const __grid_constant__ CUtensorMap map_rope, const AttnArgs a, float* __restrict__ part_dk,
+                     float* __restrict__ part_dv) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = ptx::align1024(smem_raw);
   uint8_t* sK = smem + DkvCfg::kOffK;
@@ -1091,11 +1097,19 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint64_t* acc_full = sp_full + 6;              // dK, dV of the item complete
   uint64_t* drain = sp_full + 7;                 // failure path: every issued MMA completed
   uint64_t* kv_empty = sp_full + 8;              // the item's last S^T / dP^T MMAs done: K, V may be replaced
+  uint64_t* rope_full = sp_full + 9;             // the item's rotary rows landed (direct dK with rotation)
+  uint64_t* rope_empty = sp_full + 10;           // the epilogue has read them (8 warp arrivals)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DkvCfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DkvCfg::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hpc = a.heads_per_cta;
+  // The direct epilogue rotates dK back with each key row's 64 cos and sin.
+  // Read from global at the item's end (each thread its own row, 512 bytes
+  // from the next), those loads held up the MMA issue and the workers; the
+  // producer now brings the item's rows into shared memory by TMA while the
+  // item's last query blocks stream in.
+  const bool rope_smem = a.rope != nullptr && hpc == a.H / a.Hkv;
   const int ngrp = a.H / hpc;
   const int per = ngrp * a.nseq;
   const int ntk = a.S / 128;
@@ -1130,12 +1144,15 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(rope_full, 1);
+    ptx::mbar_init(rope_empty, kAtWorkers);
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&map_q);
     ptx::tma_prefetch_desc(&map_do);
     ptx::tma_prefetch_desc(&map_k);
     ptx::tma_prefetch_desc(&map_v);
+    if (rope_smem) ptx::tma_prefetch_desc(&map_rope);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, 512);
@@ -1159,7 +1176,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0, issued_kv = 0, it = 0, gs = 0;
+      int issued = 0, issued_kv = 0, issued_rope = 0, it = 0, gs = 0;
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < nitems; item = nth_item(++k), ++it) {
         const Item t = item_of(item);
@@ -1190,11 +1207,25 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           ptx::tma_load_2d(ld, &map_lse, &st_full[s], qrow, h);
           ptx::tma_load_2d(ld + 256, &map_di, &st_full[s], qrow, h);
           ++issued;
+          if (rope_smem && u + 1 == t.n) {
+            // the item's rotary rows (positions kt 128 ..), once the previous
+            // item's epilogue has read its own
+            if (!ptx::mbar_wait(rope_empty, (it & 1) ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            uint8_t* rb = smem + DkvCfg::kOffRope;
+            ptx::mbar_arrive_expect_tx(rope_full, DkvCfg::kRopeBytes);
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx) ptx::tma_load_2d(rb + bx * 16384, &map_rope, rope_full, bx * 32, t.kt * 128);
+            ++issued_rope;
+          }
         }
       }
       if (!ok) {  // before the CTA exits every issued copy must have landed
         give_up();
         if (issued_kv > 0) ptx::mbar_wait(kv_full, (issued_kv - 1) & 1, nullptr);
+        if (issued_rope > 0) ptx::mbar_wait(rope_full, (issued_rope - 1) & 1, nullptr);
         for (int u = (issued > kKvStages ? issued - kKvStages : 0); u < issued; ++u)
           ptx::mbar_wait(&st_full[u % kKvStages], (u / kKvStages) & 1, nullptr);
       }
@@ -1357,8 +1388,23 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         store_grad_pairs(lo, hi, 1.0f, nullptr, half, a.out1 + static_cast<int64_t>(t.key0 + r) * a.ld1 + t.g * 128);
         uint16_t* dk_row = a.out0 + static_cast<int64_t>(t.key0 + r) * a.ld0 + t.g * 128;
         if (a.rope) {
-          RotRow rot;  // its loads overlap the TMEM read of dK
-          load_rot(a.rope, kpos, half, rot);
+          RotRow rot;
+          if (!wait_all(rope_full, it & 1)) {
+            ok = false;
+            break;
+          }
+          {
+            // row r of the cos box of this half and of the sin box, 16 bytes at a time
+            const uint32_t rb = ptx::smem_addr(smem + DkvCfg::kOffRope);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t off = static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+              rot.c[c] = lds128(rb + static_cast<uint32_t>(half * 16384) + off);
+              rot.s[c] = lds128(rb + static_cast<uint32_t>((2 + half) * 16384) + off);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(rope_empty);
           ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(half * 32), lo);
           ptx::tmem_ld_32x32b_x32(lane_base + 384u + static_cast<uint32_t>(64 + half * 32), hi);
           ptx::tmem_wait_ld();
@@ -1656,8 +1702,14 @@ static sl_status attention_bwd_launch(const AttnShape& sh, const uint16_t* q, in
     ak.ld1 = lddv;
     const int64_t items = (sh.S / 128) * (sh.H / ak.heads_per_cta) * a.nseq;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, num_sms()));
+    // the rotary table [S, 128] fp32 as 128-row boxes of 32 columns (the direct epilogue's rows)
+    CUtensorMap mr = ml;
+    if (rope && direct &&
+        (st = make_map(&mr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rope, 128, static_cast<uint64_t>(sh.S), 128 * 4, 32, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != SL_OK)
+      return st;
     if ((st = launch_pdl("attn_dkdv_kernel", attn_dkdv_kernel, dim3(grid), dim3(kAtThreads), DkvCfg::kSmem, stream, mq,
-                         mdo, mk, mv, ml, md, ak, part_dk, part_dv)) != SL_OK)
+                         mdo, mk, mv, ml, md, mr, ak, part_dk, part_dv)) != SL_OK)
       return st;
     if (direct) return SL_OK;
     const int64_t nt = sh.M * sh.Hkv * 8;
