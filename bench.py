@@ -406,7 +406,7 @@ def run_ours(args):
         kind = {"nf4": sl.SL_WEIGHT_NF4, "nf4dq": sl.SL_WEIGHT_NF4_DQ, "bf16": sl.SL_WEIGHT_BF16}[w["base"]]
         if kind == sl.SL_WEIGHT_BF16:
             dominant = ("bf16_fwd", "bf16_dx")
-            kname = "gemm_tc_kernel<BF16> (bf16 base + LoRA fold; fwd and dX)"
+            kname = "gemm_bf16_pair_persistent_kernel (bf16 base by TMA on CTA pairs + LoRA fold; fwd and dX)"
         D, Dkv, F, L, r, alpha = w["D"], w["Dkv"], w["F"], w["L"], w["r"], w["alpha"]
         shapes = sl.proj_shapes(D, Dkv, F)
         sa, sb = sl.adapter_shapes(D, Dkv, F, r)

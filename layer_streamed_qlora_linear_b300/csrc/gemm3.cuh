@@ -20,6 +20,9 @@
 // Warps: 0 A/code TMA producer, 1 MMA issuer (leader) or peer forwarder,
 // 2..9 NF4 dequant (two groups on alternate k-blocks), 10..13 LoRA staging +
 // epilogue.  Every wait is bounded.
+// gemm_bf16_pair_persistent_kernel is the same kernel for a bf16 (unquantised)
+// weight: each CTA's producer loads its B half by TMA next to its A tile, both
+// counted on the leader's full[s], and warps 2..9 have no work.
 #pragma once
 #include "gemm2.cuh"
 
@@ -62,12 +65,15 @@ static_assert(Gemm3Cfg<1>::kOffLA % 1024 == 0 && Gemm3Cfg<1>::kLA * kLoraAtom + 
 // Barrier of the four epilogue warps only (named barrier 1).
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kNumEpi3) : "memory"); }
 
-template <int BMN, int SMALL>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
-    gemm_nf4_pair_persistent_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
-                                    const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_s2,
-                                    const __grid_constant__ CUtensorMap map_o,
-                                    const GemmArgs args) {
+// The kernel body, over the weight source: BF16 = 0 NF4 (codes + absmax by
+// TMA, dequantised by warps 2..9 into the B halves), BF16 = 1 bf16 weights
+// (each CTA's B half by TMA straight into the operand layout, counted on the
+// leader's full[s] like the A tiles; warps 2..9 and the peer forwarder idle).
+// map_c: NF4 codes / the bf16 weight; map_s, map_s2: absmax (NF4 only).
+template <int BF16, int BMN, int SMALL>
+__device__ __forceinline__ void pair_persistent_body(const CUtensorMap& map_a, const CUtensorMap& map_c,
+                                                     const CUtensorMap& map_s, const CUtensorMap& map_s2,
+                                                     const CUtensorMap& map_o, const GemmArgs& args) {
   using Cfg = Gemm3Cfg<SMALL>;
   constexpr int S = Cfg::S;
   extern __shared__ uint8_t smem_raw[];
@@ -143,7 +149,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
-      ptx::mbar_init(&full[i], 1 + kNumDq2 / 64);  // producer + the 4 warps of the owning dequant group
+      ptx::mbar_init(&full[i], BF16 ? 1 : 1 + kNumDq2 / 64);  // producer (+ the 4 warps of the owning dequant group)
       ptx::mbar_init(&raw_full[i], 1);
       ptx::mbar_init(&b_local[i], kNumDq2 / 64);
       ptx::mbar_init(&empty[i], 1);
@@ -160,8 +166,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&map_a);
     ptx::tma_prefetch_desc(&map_c);
-    ptx::tma_prefetch_desc(&map_s);
-    if (args.dq) ptx::tma_prefetch_desc(&map_s2);
+    if (!BF16) ptx::tma_prefetch_desc(&map_s);
+    if (!BF16 && args.dq) ptx::tma_prefetch_desc(&map_s2);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(tmem_holder, 512);
@@ -202,8 +208,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
             break;
           }
           // A tiles of both CTAs and the peer's 16-byte "B half ready" signal
-          if (leader) ptx::mbar_arrive_expect_tx(&full[s], 2 * kATileBytes + 16);
+          // (bf16 weights: the B halves of both CTAs instead)
+          if (leader) ptx::mbar_arrive_expect_tx(&full[s], BF16 ? 2 * (kATileBytes + kHalfBTileBytes) : 2 * kATileBytes + 16);
           ptx::tma_load_2d_pair(sA + s * kATileBytes, &map_a, ptx::map_to_rank(&full[s], 0), kb * kBK, m0);
+          if (BF16) {  // this CTA's 128 weight rows (K-major) / columns (MN-major, two 64-column atoms)
+            uint8_t* bt = sB + s * kHalfBTileBytes;
+            if (!BMN) {
+              ptx::tma_load_2d_pair(bt, &map_c, ptx::map_to_rank(&full[s], 0), kb * kBK, nh);
+            } else {
+              ptx::tma_load_2d_pair(bt, &map_c, ptx::map_to_rank(&full[s], 0), nh, kb * kBK);
+              ptx::tma_load_2d_pair(bt + 64 * 128, &map_c, ptx::map_to_rank(&full[s], 0), nh + 64, kb * kBK);
+            }
+            continue;
+          }
           uint8_t* raw = sRaw + s * Cfg::kRawBytes;
           ptx::mbar_arrive_expect_tx(&raw_full[s], rawtx);
           if (!BMN) {
@@ -229,7 +246,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && !BF16) {
         for (int k = (g > S ? g - S : 0); k < g; ++k) ptx::mbar_wait_cluster(&raw_full[k % S], (k / S) & 1, nullptr);
       }
     }
@@ -309,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
         ptx::mma_commit_pair(drain, 0x1);
         ptx::mbar_wait(drain, 0, nullptr);
       }
-    } else if (lane == 0) {
+    } else if (lane == 0 && !BF16) {
       // -------------------------------------------------- peer: B-ready forwarder
       // (a 16-byte async-proxy copy whose bytes complete on the leader's full[s])
       const uint32_t leader_full = ptx::map_to_rank(&full[0], 0);
@@ -331,52 +348,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     }
   } else if (warp < 10) {
     // ------------------------------------------- NF4 dequant (each CTA, 256 threads)
-    const int dq = tid - 64;
-    const int grp = (warp - 2) >> 2;
-    const int tr = dq & 127;
-    int g = 0;
-    bool ok = true;
-    for (int i = 0; ok && i < n_items; ++i) {
-      const Item x = item(i);
-      const int t = x.t;
-      // two groups of four warps take alternate k-blocks (cluster counter g)
-      for (int kb = x.kb0; kb < x.kb1; ++kb, ++g) {
-        if ((g & 1) != grp) continue;
-        const int s = g % S;
-        if (!ptx::mbar_wait_cluster(&raw_full[s], (g / S) & 1, abort_flag)) {
-          give_up();
-          ok = false;
-          break;
+    if (!BF16) {
+      const int dq = tid - 64;
+      const int grp = (warp - 2) >> 2;
+      const int tr = dq & 127;
+      int g = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < n_items; ++i) {
+        const Item x = item(i);
+        const int t = x.t;
+        // two groups of four warps take alternate k-blocks (cluster counter g)
+        for (int kb = x.kb0; kb < x.kb1; ++kb, ++g) {
+          if ((g & 1) != grp) continue;
+          const int s = g % S;
+          if (!ptx::mbar_wait_cluster(&raw_full[s], (g / S) & 1, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          const uint8_t* codes = sRaw + s * Cfg::kRawBytes;
+          const float* amax = reinterpret_cast<const float*>(codes + kHalfCodesBytes);
+          const int8_t* qam = reinterpret_cast<const int8_t*>(codes + kHalfCodesBytes);
+          const float* cs = reinterpret_cast<const float*>(codes + kHalfCodesBytes + 128);
+          uint8_t* bt = sB + s * kHalfBTileBytes;
+          if (!BMN) {
+            const uint4 q0 = *reinterpret_cast<const uint4*>(codes + tr * 32);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(codes + tr * 32 + 16);
+            const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            const int p = ((args.dq_col0 + tile_n0(t) + static_cast<int>(rank) * 128) >> 8) & 1;
+            const float am =
+                args.dq ? fmaf(cs[2 * p + 1], static_cast<float>(qam[tr]), cs[2 * p]) : amax[tr * 4 + (kb & 3)];
+            nf4_words_bf16<8>(w, am, bt + tr * 128, 0, tr & 7);
+          } else {
+            // eight consecutive lanes (one 128-byte store phase) take eight rows
+            // n with distinct n % 8, so their swizzled chunks fall in different banks
+            const int n = ((tr >> 5) << 4) | (tr & 7) | ((tr >> 1) & 8);
+            const int a = ((tr >> 1) ^ (tr >> 3)) & 1;
+            const uint4 q0 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32 + 16);
+            const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            const int p = ((args.dq_col0 + kb * kBK) >> 8) & 1;
+            const float am = args.dq ? fmaf(cs[a * 4 + 2 * p + 1], static_cast<float>(qam[a * 64 + n]), cs[a * 4 + 2 * p])
+                                     : amax[n * 4 + 2 * static_cast<int>(rank) + a];
+            nf4_words_bf16<8>(w, am, bt + a * (64 * 128) + n * 128, 0, n & 7);
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(leader ? &full[s] : &b_local[s]);
         }
-        const uint8_t* codes = sRaw + s * Cfg::kRawBytes;
-        const float* amax = reinterpret_cast<const float*>(codes + kHalfCodesBytes);
-        const int8_t* qam = reinterpret_cast<const int8_t*>(codes + kHalfCodesBytes);
-        const float* cs = reinterpret_cast<const float*>(codes + kHalfCodesBytes + 128);
-        uint8_t* bt = sB + s * kHalfBTileBytes;
-        if (!BMN) {
-          const uint4 q0 = *reinterpret_cast<const uint4*>(codes + tr * 32);
-          const uint4 q1 = *reinterpret_cast<const uint4*>(codes + tr * 32 + 16);
-          const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          const int p = ((args.dq_col0 + tile_n0(t) + static_cast<int>(rank) * 128) >> 8) & 1;
-          const float am =
-              args.dq ? fmaf(cs[2 * p + 1], static_cast<float>(qam[tr]), cs[2 * p]) : amax[tr * 4 + (kb & 3)];
-          nf4_words_bf16<8>(w, am, bt + tr * 128, 0, tr & 7);
-        } else {
-          // eight consecutive lanes (one 128-byte store phase) take eight rows
-          // n with distinct n % 8, so their swizzled chunks fall in different banks
-          const int n = ((tr >> 5) << 4) | (tr & 7) | ((tr >> 1) & 8);
-          const int a = ((tr >> 1) ^ (tr >> 3)) & 1;
-          const uint4 q0 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32);
-          const uint4 q1 = *reinterpret_cast<const uint4*>(codes + n * 64 + a * 32 + 16);
-          const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          const int p = ((args.dq_col0 + kb * kBK) >> 8) & 1;
-          const float am = args.dq ? fmaf(cs[a * 4 + 2 * p + 1], static_cast<float>(qam[a * 64 + n]), cs[a * 4 + 2 * p])
-                                   : amax[n * 4 + 2 * static_cast<int>(rank) + a];
-          nf4_words_bf16<8>(w, am, bt + a * (64 * 128) + n * 128, 0, n & 7);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(leader ? &full[s] : &b_local[s]);
       }
     }
   } else {
@@ -620,6 +639,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc_pair(tmem, 512);
   }
+}
+
+template <int BMN, int SMALL>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
+    gemm_nf4_pair_persistent_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
+                                    const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_s2,
+                                    const __grid_constant__ CUtensorMap map_o,
+                                    const GemmArgs args) {
+  pair_persistent_body<0, BMN, SMALL>(map_a, map_c, map_s, map_s2, map_o, args);
+}
+
+// bf16 weights (unquantised base, K-major W [N, K] or MN-major W [K, N] by
+// TMA boxes of 64 x 128 / 64 x 64); map_s, map_s2 are not read.
+template <int BMN, int SMALL>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
+    gemm_bf16_pair_persistent_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
+                                     const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_s2,
+                                     const __grid_constant__ CUtensorMap map_o,
+                                     const GemmArgs args) {
+  pair_persistent_body<1, BMN, SMALL>(map_a, map_w, map_s, map_s2, map_o, args);
 }
 
 }  // namespace sl

@@ -98,9 +98,12 @@ def test_bounded_wait_times_out_without_fault(gpu_lib):
     assert float(x.sum()) == 4.0
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 2560, 2560), (300, 1248, 2048), (1024, 4864, 4096), (1024, 4096, 4864)])
-def test_pair_gemm_tile_walk_matches_oracle(gpu_lib, M, N, K):
-    """The CTA-pair NF4 GEMM at sizes where tiles outnumber the SM pairs
+@pytest.mark.parametrize("M,N,K,kind", [(2048, 2560, 2560, "nf4"), (300, 1248, 2048, "nf4"), (1024, 4864, 4096, "nf4"),
+                                        (1024, 4096, 4864, "nf4"), (2048, 2560, 2560, "bf16"), (300, 1248, 2048, "bf16"),
+                                        (1024, 4096, 4864, "bf16")])
+def test_pair_gemm_tile_walk_matches_oracle(gpu_lib, M, N, K, kind):
+    """The CTA-pair GEMM (NF4 weights dequantised in the kernel, or bf16
+    weights loaded by TMA) at sizes where tiles outnumber the SM pairs
     (80 pair tiles on 74: some clusters run two tiles, alternating their
     TMEM accumulators and LoRA staging) and with a ragged M pair and a
     partial N tile. With a workspace the persistent kernel splits its last
@@ -109,7 +112,7 @@ def test_pair_gemm_tile_walk_matches_oracle(gpu_lib, M, N, K):
     pieces, the partial sums added in piece order): bitwise repeatable, and
     within rounding of the forward without a workspace (no split)."""
     r, alpha = 16, 32.0
-    c, W_ref, w, t = make(gpu_lib, 11, M, N, K, r, "nf4")
+    c, W_ref, w, t = make(gpu_lib, 11, M, N, K, r, kind)
     a = run(gpu_lib, w, t, M, N, K, r, alpha)
     b = run(gpu_lib, w, t, M, N, K, r, alpha)
     for x, y in zip(a, b):
