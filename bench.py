@@ -580,7 +580,8 @@ def run_ours(args):
     else:  # cross-entropy
         D, V, chunk = w["D"], w["V"], w["chunk"]
         dominant = ("ce_logits", "ce_dh")
-        kname = "gemm_tc_kernel<BF16> CE epilogues (logits chunk with exp, rescaled dH accumulation)"
+        kname = ("gemm_bf16_pair_persistent_kernel CE epilogues (logits chunk with exp, rescaled dH accumulation; "
+                 "CTA pairs)")
         H = rnd((M, D), 1.0)
         Wh = rnd((V, D), 0.02)
         lab = torch.randint(0, V, (M,), generator=gen, device=dev, dtype=torch.int32)

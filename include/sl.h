@@ -469,7 +469,9 @@ sl_status sl_attention_bwd(const void* q, int64_t ldq, const void* k, int64_t ld
  * stream's gradient dtype; it can feed sl_stream_stack_step's dh_top).  The
  * vocab is processed in chunks of chunk_V (multiple of 256) rows of W_head;
  * no [M, V] logits tensor ever exists, only an [M, chunk_V] bf16 softmax
- * chunk and O(M * V / 256) per-tile partials in `ws`.  N_valid == 0 gives
+ * chunk and O(M * V / 256) per-tile partials in `ws` (plus, for M > 128, a
+ * fixed ~19 MB scratch in which the CTA-pair GEMMs split their last partial
+ * wave along K).  N_valid == 0 gives
  * loss 0 and dH 0.  D % 256 == 0, V % 32 == 0.  A label outside [0, V) that
  * is not ignore_index is treated as ignored and recorded as SL_ERR_INVALID
  * in the device error word.  `ws` must hold sl_ce_workspace_size(M, D, V,

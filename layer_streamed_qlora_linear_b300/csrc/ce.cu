@@ -25,7 +25,7 @@ namespace sl {
 namespace {
 
 struct CEPlan {
-  size_t part_max, part_sum, label_logit, run_max, run_sum, alpha, lse, term, scale, P, total;
+  size_t part_max, part_sum, label_logit, run_max, run_sum, alpha, lse, term, scale, P, split, split_bytes, total;
   int halves;  // 128-column half tiles of a chunk
 };
 
@@ -50,6 +50,9 @@ CEPlan ce_plan(int64_t M, int64_t D, int64_t V, int64_t chunk_V) {
   p.term = take(M * 4);
   p.scale = take(M * 4);
   p.P = take(static_cast<size_t>(M) * chunk_V * 2);
+  // the pair GEMMs (M > 128) split a last partial wave along K in this scratch
+  p.split_bytes = M > 128 ? split_scratch_bytes() : 0;
+  p.split = take(p.split_bytes);
   p.total = off;
   return p;
 }
@@ -246,6 +249,8 @@ sl_status ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W, int64_t
     g.args.label_logit = zlab;
     g.args.part_ld = P.halves;
     g.args.err = err;
+    g.split_ws = P.split_bytes ? base + P.split : nullptr;
+    g.split_ws_bytes = P.split_bytes;
     st = launch_gemm(g, stream);
     if (st != SL_OK) return st;
     // running (max, sum); P rescaled to the running max; alpha for dH
@@ -271,6 +276,8 @@ sl_status ce_fwd_bwd(const void* H, int64_t M, int64_t D, const void* W, int64_t
     h.args.accumulate = v0 > 0 ? 1 : 0;
     h.args.row_alpha = alpha;
     h.args.err = err;
+    h.split_ws = P.split_bytes ? base + P.split : nullptr;
+    h.split_ws_bytes = P.split_bytes;
     st = launch_gemm(h, stream);
     if (st != SL_OK) return st;
   }

@@ -136,17 +136,19 @@ static sl_status run_pair(const CUtensorMap& ma, const CUtensorMap& mc, const CU
                     ao);
 }
 
-// The persistent pair kernel for a weight source (BF16 = 1: bf16 weights by TMA).
-template <int BF16, int BMN, int SMALL>
+// The persistent pair kernel for a weight source (BF16 = 1: bf16 weights by
+// TMA) and epilogue (NF4: the bf16 store only).
+template <int BF16, int BMN, int SMALL, int EPI>
 static auto pair_persistent_kernel() {
-  if constexpr (BF16) return gemm_bf16_pair_persistent_kernel<BMN, SMALL>;
+  static_assert(BF16 || EPI == kEpiStoreBF16, "NF4 pair GEMM: bf16 store epilogue only");
+  if constexpr (BF16) return gemm_bf16_pair_persistent_kernel<BMN, SMALL, EPI>;
   else return gemm_nf4_pair_persistent_kernel<BMN, SMALL>;
 }
 
 // CTA pairs of the persistent kernel that the device holds at once (driver
 // query, once per device); the grid never exceeds it, so all clusters run
 // together and none waits for a second wave.
-template <int BF16, int BMN, int SMALL>
+template <int BF16, int BMN, int SMALL, int EPI = kEpiStoreBF16>
 static int pair_clusters_resident() {
   static std::mutex mu;
   static int cached[64] = {0};
@@ -154,14 +156,14 @@ static int pair_clusters_resident() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms() / 2;
   std::lock_guard<std::mutex> lk(mu);
   if (cached[dev] == 0) {
-    cudaFuncSetAttribute(pair_persistent_kernel<BF16, BMN, SMALL>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(pair_persistent_kernel<BF16, BMN, SMALL, EPI>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Gemm3Cfg<SMALL>::kSmem);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kGemm3Threads, 1, 1);
     cfg.dynamicSmemBytes = Gemm3Cfg<SMALL>::kSmem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_persistent_kernel<BF16, BMN, SMALL>(), &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, pair_persistent_kernel<BF16, BMN, SMALL, EPI>(), &cfg) != cudaSuccess ||
         n <= 0) {
       cudaGetLastError();
       n = num_sms() / 2;
@@ -207,11 +209,11 @@ static void set_split(GemmArgs& a, int ntiles, int nclusters, void* ws, size_t b
   a.split_tag = tag.fetch_add(1) + 1;
 }
 
-template <int BF16, int BMN, int SMALL>
+template <int BF16, int BMN, int SMALL, int EPI = kEpiStoreBF16>
 static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, const CUtensorMap& ms,
                                 const CUtensorMap& ms2, const GemmArgs& a, void* split_ws, size_t split_bytes,
                                 cudaStream_t stream) {
-  auto kern = pair_persistent_kernel<BF16, BMN, SMALL>();
+  auto kern = pair_persistent_kernel<BF16, BMN, SMALL, EPI>();
   static bool attr_set[64] = {false};
   int dev = 0;
   SL_CHECK_CUDA(cudaGetDevice(&dev));
@@ -220,13 +222,14 @@ static sl_status run_persistent(const CUtensorMap& ma, const CUtensorMap& mc, co
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int ntiles = ceil_div(a.M, 256) * ceil_div(a.N, kBN);
-  const int nclusters = std::min(ntiles, pair_clusters_resident<BF16, BMN, SMALL>());
+  const int nclusters = std::min(ntiles, pair_clusters_resident<BF16, BMN, SMALL, EPI>());
   GemmArgs ao = a;
   set_split(ao, ntiles, nclusters, split_ws, split_bytes);
   // bf16 output by TMA boxes of 64 columns x 32 rows when a tensor map can
   // describe it (16-byte aligned base and row stride); else direct stores
+  // (always for the fp32 accumulation)
   CUtensorMap mo = ma;
-  ao.tma_out = (reinterpret_cast<uintptr_t>(a.out) % 16 == 0) && (a.ld_out * 2) % 16 == 0 &&
+  ao.tma_out = EPI != kEpiAddF32 && (reinterpret_cast<uintptr_t>(a.out) % 16 == 0) && (a.ld_out * 2) % 16 == 0 &&
                make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, a.N, a.M, static_cast<uint64_t>(a.ld_out) * 2, 64,
                         32, CU_TENSOR_MAP_SWIZZLE_128B) == SL_OK;
   return launch_pdl(BF16 ? "gemm_bf16_pair_persistent_kernel" : "gemm_nf4_pair_persistent_kernel", kern,
@@ -285,9 +288,10 @@ sl_status launch_gemm(const GemmLaunch& g, cudaStream_t stream) {
                           CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != SL_OK) return st;
   if (g.bsrc == kBSrcBF16) {
-    // CTA pairs (the persistent kernel) for the plain store epilogue at M > 128:
-    // each CTA loads its own 128 weight rows (K-major) or two 64-column boxes (MN-major)
-    pair = g.epi == kEpiStoreBF16 && a.M > kBM;
+    // CTA pairs (the persistent kernel) at M > 128 for the bf16 store and the
+    // CE epilogues: each CTA loads its own 128 weight rows (K-major) or two
+    // 64-column boxes (MN-major)
+    pair = a.M > kBM && (g.epi == kEpiStoreBF16 || (g.epi == kEpiCEExp && !g.bmn) || (g.epi == kEpiAddF32 && g.bmn));
     if (!g.bmn)
       st = make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.w, a.K, a.N, g.ldw * 2, kBK, pair ? 128 : kBN,
                     CU_TENSOR_MAP_SWIZZLE_128B);
@@ -371,7 +375,11 @@ static sl_status launch_timed(const GemmLaunch& g, bool pair, const CUtensorMap&
                ceil_div(a.M, 256) * ceil_div(a.N, kBN) >
                    (g.bmn ? pair_clusters_resident<0, 1, 1>() : pair_clusters_resident<0, 0, 1>()));
   // folded rank <= 32: the five-stage variant; above (a group's dX): four stages
-  if (bf16_pair)
+  if (bf16_pair && g.epi == kEpiCEExp)
+    st = run_persistent<1, 0, 1, kEpiCEExp>(ma, mb, ms, ms2, a, g.split_ws, g.split_ws_bytes, stream);
+  else if (bf16_pair && g.epi == kEpiAddF32)
+    st = run_persistent<1, 1, 1, kEpiAddF32>(ma, mb, ms, ms2, a, g.split_ws, g.split_ws_bytes, stream);
+  else if (bf16_pair)
     st = g.bmn ? run_persistent<1, 1, 1>(ma, mb, ms, ms2, a, g.split_ws, g.split_ws_bytes, stream)
                : run_persistent<1, 0, 1>(ma, mb, ms, ms2, a, g.split_ws, g.split_ws_bytes, stream);
   else if (persistent && a.r <= 32)

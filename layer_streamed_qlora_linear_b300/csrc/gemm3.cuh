@@ -70,7 +70,7 @@ __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" 
 // (each CTA's B half by TMA straight into the operand layout, counted on the
 // leader's full[s] like the A tiles; warps 2..9 and the peer forwarder idle).
 // map_c: NF4 codes / the bf16 weight; map_s, map_s2: absmax (NF4 only).
-template <int BF16, int BMN, int SMALL>
+template <int BF16, int BMN, int SMALL, int EPI>
 __device__ __forceinline__ void pair_persistent_body(const CUtensorMap& map_a, const CUtensorMap& map_c,
                                                      const CUtensorMap& map_s, const CUtensorMap& map_s2,
                                                      const CUtensorMap& map_o, const GemmArgs& args) {
@@ -567,7 +567,132 @@ __device__ __forceinline__ void pair_persistent_body(const CUtensorMap& map_a, c
             for (int j = 0; j < 32; ++j) v[j] += __ldcg(part + (c0 + j) * 128 + row);
           }
         };
-        if (args.tma_out) {
+        if (EPI == kEpiCEExp) {
+          // This thread's row over each 128-column half of the tile: the max
+          // (one read of the accumulator), then bf16(exp(z - max)) to the
+          // chunk scratch and the fp32 sum of exp(z - max) (a second read),
+          // both left to right, and the label's logit; half h's partials go
+          // to column 2 (n0 / 256) + h.  The exp values leave as 64-column
+          // TMA boxes staged like the bf16 store below.
+          const int lab = gm < args.M ? args.labels[gm] : args.ignore_index;
+          uint8_t* stg = sLA + (warp - 10) * 8192;
+          const uint32_t stg_a = ptx::smem_addr(stg);
+#pragma unroll 1
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int c0 = h2 * 128; c0 < h2 * 128 + 128; c0 += 32) {
+              uint32_t u[32];
+              ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c0), u);
+              ptx::tmem_wait_ld();
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+              add_parts(v, c0);
+              if (n0 + c0 < args.N)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) mx = fmaxf(mx, v[j]);
+            }
+            float sm = 0.0f;
+#pragma unroll 1
+            for (int pp = 0; pp < 2; ++pp) {
+              const int p = h2 * 2 + pp, b = p & 1;
+              if (args.tma_out && p >= 2) {  // buffer b's previous box has been read out
+                if (lane == 0) ptx::bulk_wait_read1();
+                __syncwarp();
+              }
+#pragma unroll 1
+              for (int hh = 0; hh < 2; ++hh) {
+                const int c0 = p * 64 + hh * 32;
+                uint32_t u[32];
+                ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c0), u);
+                ptx::tmem_wait_ld();
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+                add_parts(v, c0);
+                const bool in = n0 + c0 < args.N;
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  f[j] = in ? __expf(v[j] - mx) : 0.0f;
+                  sm += f[j];
+                }
+                if (args.tma_out) {
+#pragma unroll
+                  for (int g4 = 0; g4 < 4; ++g4)
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     stg_a + b * 4096 + lane * 128 + (((hh * 4 + g4) ^ (lane & 7)) << 4)),
+                                 "r"(pack_bf16x2(f[8 * g4 + 0], f[8 * g4 + 1])),
+                                 "r"(pack_bf16x2(f[8 * g4 + 2], f[8 * g4 + 3])),
+                                 "r"(pack_bf16x2(f[8 * g4 + 4], f[8 * g4 + 5])),
+                                 "r"(pack_bf16x2(f[8 * g4 + 6], f[8 * g4 + 7]))
+                                 : "memory");
+                } else {
+                  store32(gm, n0, c0, f);
+                }
+                const int vid = args.vocab_base + n0 + c0;
+                if (in && gm < args.M && lab >= vid && lab < vid + 32) {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    if (lab == vid + j) args.label_logit[gm] = v[j];
+                }
+              }
+              if (args.tma_out) {
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  ptx::tma_store_2d(&map_o, stg + b * 4096, n0 + p * 64, tile_m0(t) + q * 32);
+                  ptx::bulk_commit();
+                }
+              }
+            }
+            if (gm < args.M) {
+              const int64_t pi = static_cast<int64_t>(gm) * args.part_ld + 2 * (n0 / kBN) + h2;
+              args.part_max[pi] = mx;
+              args.part_sum[pi] = sm;
+            }
+          }
+          if (args.tma_out) {
+            if (lane == 0) ptx::bulk_wait_read0();  // the region is free again before the next barrier
+            __syncwarp();
+          }
+        } else if (EPI == kEpiAddF32) {
+          // fp32 out[m, j] = (accumulate ? out[m, j] * alpha[m] : 0) + acc,
+          // each thread its row's 32 columns at a time (128 contiguous bytes)
+          float* outf = reinterpret_cast<float*>(args.out);
+          const float ra = (args.row_alpha && gm < args.M) ? args.row_alpha[gm] : 1.0f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kBN; c0 += 32) {
+            uint32_t u[32];
+            ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c0), u);
+            const bool in = gm < args.M && n0 + c0 < args.N;
+            float4* dst = reinterpret_cast<float4*>(outf + static_cast<int64_t>(in ? gm : 0) * args.ld_out + (in ? n0 + c0 : 0));
+            float4 old[8];
+            if (in && args.accumulate) {  // loads in flight beside the accumulator read
+#pragma unroll
+              for (int g8 = 0; g8 < 8; ++g8) old[g8] = dst[g8];
+            }
+            ptx::tmem_wait_ld();
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+            add_parts(v, c0);
+            if (in) {
+#pragma unroll
+              for (int g8 = 0; g8 < 8; ++g8) {
+                float4 o = make_float4(v[4 * g8], v[4 * g8 + 1], v[4 * g8 + 2], v[4 * g8 + 3]);
+                if (args.accumulate) {
+                  o.x = fmaf(old[g8].x, ra, o.x);
+                  o.y = fmaf(old[g8].y, ra, o.y);
+                  o.z = fmaf(old[g8].z, ra, o.z);
+                  o.w = fmaf(old[g8].w, ra, o.w);
+                }
+                dst[g8] = o;
+              }
+            }
+          }
+        } else if (args.tma_out) {
           // The LoRA region is free from the fold's completion (acc_full) until
           // the next stage_lora, which follows the epilogue warps' barrier:
           // this warp stages its 32 rows there as 64-column bf16 boxes (two
@@ -647,18 +772,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
                                     const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_s2,
                                     const __grid_constant__ CUtensorMap map_o,
                                     const GemmArgs args) {
-  pair_persistent_body<0, BMN, SMALL>(map_a, map_c, map_s, map_s2, map_o, args);
+  pair_persistent_body<0, BMN, SMALL, kEpiStoreBF16>(map_a, map_c, map_s, map_s2, map_o, args);
 }
 
 // bf16 weights (unquantised base, K-major W [N, K] or MN-major W [K, N] by
-// TMA boxes of 64 x 128 / 64 x 64); map_s, map_s2 are not read.
-template <int BMN, int SMALL>
+// TMA boxes of 64 x 128 / 64 x 64); map_s, map_s2 are not read.  EPI: the
+// bf16 store (with the LoRA fold), or the cross-entropy epilogues of
+// gemm.cuh (the logits chunk's exp values and half-tile partials; the fp32
+// dH accumulation), which fold no side product.
+template <int BMN, int SMALL, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemm3Threads, 1)
     gemm_bf16_pair_persistent_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
                                      const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_s2,
                                      const __grid_constant__ CUtensorMap map_o,
                                      const GemmArgs args) {
-  pair_persistent_body<1, BMN, SMALL>(map_a, map_w, map_s, map_s2, map_o, args);
+  pair_persistent_body<1, BMN, SMALL, EPI>(map_a, map_w, map_s, map_s2, map_o, args);
 }
 
 }  // namespace sl
