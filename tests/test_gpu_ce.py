@@ -27,6 +27,7 @@ def run(sl, H, W, lab, chunk):
     (64, 256, 256, 8192, 0.05),      # one chunk larger than the vocabulary
     (192, 256, 2048, 256, 0.5),      # logits spread ~ +-25: the running max moves across 8 chunks
     (1280, 1024, 8192, 8192, 0.05),  # CTA pairs: 160 logits tiles on 74 clusters, the 12 tail tiles split along K
+    (129, 256, 768, 512, 0.05),      # CTA pairs with one row in the second CTA; last chunk 256 wide
 ])
 def test_ce_matches_oracle(gpu_lib, M, D, V, chunk, w_std):
     c = si.ce_case(3 + M, M, D, V, h_std=1.0, w_std=w_std)

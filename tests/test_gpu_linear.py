@@ -45,6 +45,12 @@ CASES = [
     (130, 1024, 512, 32, 16.0, "nf4"),     # rank 32: two extra K-steps
     (70, 352, 128, 8, 16.0, "bf16"),       # fewer K-blocks than stages, partial N tile
     (150, 96, 256, 16, 32.0, "nf4"),       # N < one tile; dX reduction ends mid-block
+    # CTA-pair edges: M = 129 (the pair's second CTA holds one row), M = 257 (a second
+    # pair of one row), N = 32, one k-block of a bf16 weight, ranks 24 and 32
+    (129, 32, 256, 8, 16.0, "nf4"),
+    (129, 288, 64, 32, 8.0, "bf16"),
+    (257, 256, 512, 16, 32.0, "bf16"),
+    (256, 256, 256, 24, 48.0, "nf4"),
 ]
 
 
