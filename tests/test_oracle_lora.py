@@ -52,3 +52,23 @@ def test_matches_torch_autograd():
     np.testing.assert_allclose(dX, tX.grad.numpy(), rtol=1e-12)
     np.testing.assert_allclose(dA, tA.grad.numpy(), rtol=1e-12)
     np.testing.assert_allclose(dB, tB.grad.numpy(), rtol=1e-12)
+
+
+def test_scale_is_alpha_over_rank():
+    """The adapter scale is s = alpha / r (the PEFT convention the pages' tool follows): padding A and B
+    with zero ranks while scaling alpha alike changes nothing, which fails for s = alpha or
+    s = alpha / sqrt(r); and one hand-sized case gives the value computed by hand."""
+    X, W, A, B, dY = _case(3, r=3)
+    A2, B2 = np.vstack([A, np.zeros_like(A)]), np.hstack([B, np.zeros_like(B)])
+    np.testing.assert_allclose(lora.lora_linear_fwd(X, W, A2, B2, 12.0), lora.lora_linear_fwd(X, W, A, B, 6.0),
+                               rtol=1e-13)
+    dX, dA, dB = lora.lora_linear_bwd(X, dY, W, A, B, 6.0)
+    dX2, dA2, dB2 = lora.lora_linear_bwd(X, dY, W, A2, B2, 12.0)
+    np.testing.assert_allclose(dX2, dX, rtol=1e-13)
+    np.testing.assert_allclose(dA2[:3], dA, rtol=1e-13)
+    np.testing.assert_allclose(dB2[:, :3], dB, rtol=1e-13)
+    assert np.all(dA2[3:] == 0) and np.all(dB2[:, 3:] == 0)
+    # X A^T = [1, 2], (X A^T) B^T = 3, s = 4 / 2 = 2: Y = 6 on a zero base
+    X1, W1 = np.array([[1.0, 2.0]]), np.zeros((1, 2))
+    A1, B1 = np.eye(2), np.array([[1.0, 1.0]])
+    assert lora.lora_linear_fwd(X1, W1, A1, B1, 4.0)[0, 0] == 6.0
